@@ -1,0 +1,508 @@
+"""Benchmark of the GB300 SGEMM library.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--mode auto|fp32|3xtf32|tf32]
+                    [--impl ours|reference] [--no-extra]
+
+One step = one SGEMM C = alpha*A@B + beta*C at M = N = K = 4092 (fp32,
+row-major, A and B ~ N(0,1) from seed 2, alpha = 1, beta = 0: the benchmark
+shape of "From 1% to 94% of cuBLAS, one kernel at a time") through the C ABI,
+inputs resident in HBM.  L2 is flushed (a 2 x L2-sized write) between timed
+steps, outside the timed events.  Each rank runs its own replica (weak
+scaling; no data-path collective); `value` is the FLOPs of all ranks divided
+by the slowest rank's time.
+
+Rank 0 prints one JSON line with the metric, the roofline of the dominant
+kernel, the oracle timed on the host cores (cpu_baseline), an end-to-end
+figure with host buffers (e2e), the clocks seen during the timed region, and
+per-path and batched-GEMM figures.
+
+--impl reference times the CPU oracle (the only reference this library has)
+on a bounded row sample of the same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SGEMM TFLOP/s at M=N=K=4092 fp32 (and % of roofline); BMM TFLOP/s"
+UNIT = "TFLOP/s"
+WORKLOAD = "sgemm_4092"
+# Fallbacks when the driver-written measured peaks are absent.
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0}
+# Dense tensor-core throughput ratio tf32 : bf16 (1.1 : 2.25 PFLOP/s nominal).
+TF32_PER_BF16 = 1.1 / 2.25
+FP32_LANES_PER_SM = 128
+
+
+def gemm_flops(M, N, K, Q=1):
+    """2*M*N*K*Q: one multiply and one add per term of every dot product
+    (the pages' 137 GFLOP for 4092^3)."""
+    return 2.0 * M * N * K * Q
+
+
+def naive_read_bytes(M, N, K):
+    """Bytes a kernel with no data reuse reads: two fp32 loads per
+    multiply-add (the pages' 548 GB for 4092^3)."""
+    return 2.0 * 4 * M * N * K
+
+
+def compulsory_bytes(M, N, K, Q=1, beta_nonzero=False):
+    """Minimum HBM traffic: read A and B once, write C (and read it if beta != 0)."""
+    return 4.0 * Q * (M * K + K * N + M * N * (2 if beta_nonzero else 1))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def roofline_peak(mode, num_sms, peaks, source):
+    """(bound, peak TFLOP/s, note) of a contraction path."""
+    if mode == "fp32":
+        mhz = float(peaks.get("sm_max_mhz", FALLBACK_PEAKS["sm_max_mhz"]))
+        peak = num_sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+        return "alu", peak, (f"FP32 FFMA peak: {num_sms} SMs x {FP32_LANES_PER_SM} lanes x 2 "
+                             f"x {mhz:.0f} MHz max SM clock")
+    tf32 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * TF32_PER_BF16
+    if mode == "3xtf32":
+        return "tensor", tf32 / 3.0, (f"tf32 tensor peak ({source} bf16 burst x 1.1/2.25) "
+                                      f"/ 3 passes; credited 2MNK")
+    return "tensor", tf32, f"tf32 tensor peak ({source} bf16 burst x 1.1/2.25)"
+
+
+def kernel_source_hash():
+    import glob
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "dense_fp32_matrix_03_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel_key):
+    """Per-launch DRAM bytes from the committed ncu summary, or None when the
+    kernel sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(kernel_key)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while active."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"), r[4:8]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        loaded = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max((num(r[2]) or 0.0) for r in rows)}
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_max(value, world, device=None):
+    """Max of a float over ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value, world, device=None):
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ oracle
+
+def cpu_baseline(w, target_s=10.0):
+    """The oracle, as it stands, on a bounded row sample of workload w on the
+    host cores.  Returns the cpu_baseline object (value in TFLOP/s)."""
+    import numpy as np
+    import oracle
+    M, N, K = w["M"], w["N"], w["K"]
+    A, B, C0 = w["A"], w["B"], w["C0"]
+    beta = w["betas"][0]
+
+    def run(nrows):
+        rows = [(0, int(i)) for i in np.linspace(0, M - 1, nrows).astype(int)]
+        t0 = time.perf_counter()
+        oracle.sgemm_ref(M, N, K, w["alpha"], A, K, B, N, beta, C0, N, rows=rows)
+        return time.perf_counter() - t0
+
+    t = run(8)
+    rate = 8 / max(t, 1e-6)
+    nrows = int(min(M, max(8, rate * target_s)))
+    t = run(nrows)
+    flops = gemm_flops(nrows, N, K)
+    return {"value": flops / t / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(t, 3),
+            "sample": f"{nrows} of {M} output rows of the {M}x{N}x{K} problem "
+                      f"(fp64 accumulation, {2 * N * K / 1e6:.1f} MFLOP per row)"}
+
+
+def reference_arm(args, rank, world):
+    """--impl reference: the oracle timed per step on the host cores."""
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    import workloads
+    oracle.build()
+    w = workloads.make(WORKLOAD)
+    M, N, K = w["M"], w["N"], w["K"]
+    steps, warmup = args.steps, args.warmup
+    budget = 150.0  # seconds for the whole run
+    per_step = budget / max(1, steps + warmup)
+    # calibrate rows per step
+    rows8 = [(0, int(i)) for i in range(8)]
+    t0 = time.perf_counter()
+    oracle.sgemm_ref(M, N, K, w["alpha"], w["A"], K, w["B"], N, 0.0, None, N, rows=rows8)
+    rate = 8 / max(time.perf_counter() - t0, 1e-6)
+    nrows = int(min(M, max(1, rate * per_step)))
+    rng = np.random.default_rng(0)
+    times = []
+    for s in range(warmup + steps):
+        rows = [(0, int(i)) for i in rng.choice(M, nrows, replace=False)]
+        t0 = time.perf_counter()
+        oracle.sgemm_ref(M, N, K, w["alpha"], w["A"], K, w["B"], N, 0.0, None, N, rows=rows)
+        dt = time.perf_counter() - t0
+        if s >= warmup:
+            times.append(dt)
+    ms = 1e3 * statistics.mean(times)
+    value = gemm_flops(nrows, N, K) / (ms / 1e3) / 1e12
+    sample = (f"{nrows} random output rows of the {M}x{N}x{K} problem per step "
+              f"(fp64 accumulation)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "alpha": 1.0, "beta": 0.0,
+                   "inputs": "normal(0,1) seed 2", "device": "host cores"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------- GPU arm
+
+def time_calls(call, steps, warmup, stream, flush):
+    """Per-step CUDA-event times (ms) on `stream`, L2 flushed before each."""
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def resolve_mode(lib, requested):
+    if requested != "auto":
+        return requested
+    import torch
+    a = torch.ones(16, 16, device="cuda")
+    c = torch.zeros(16, 16, device="cuda")
+    st = lib.sgemm_batched_ex("3xtf32", 16, 16, 16, 1.0, a, 16, a, 16, 0.0, c, 16, 0, 0, 0, 0,
+                              0, 1)
+    torch.cuda.synchronize()
+    return "3xtf32" if st == lib.SGEMM_OK else "fp32"
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--mode", default="auto", choices=["auto", "fp32", "3xtf32", "tf32"])
+    ap.add_argument("--no-extra", action="store_true", help="skip per-path and BMM figures")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = dist_env()
+
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    import torch
+    import dense_fp32_matrix_03_gb300 as lib
+    import workloads
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    lib.load()
+    props = torch.cuda.get_device_properties(dev)
+    num_sms = props.multi_processor_count
+    peaks, peak_src = load_peaks()
+    mode = resolve_mode(lib, args.mode)
+
+    w = workloads.make(WORKLOAD)
+    M, N, K = w["M"], w["N"], w["K"]
+    alpha, beta = w["alpha"], w["betas"][0]
+    A = torch.from_numpy(w["A"]).to(dev)
+    B = torch.from_numpy(w["B"]).to(dev)
+    C = torch.from_numpy(w["C0"]).to(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_call = 1
+
+    def call():
+        lib.check(lib.sgemm_batched_ex(mode, M, N, K, alpha, A, K, B, N, beta, C, N, 0, 0, 0, 0,
+                                       0, 1, stream))
+
+    gpu_id = None
+    uuid = getattr(props, "uuid", None)
+    if uuid is not None:
+        gpu_id = "GPU-" + str(uuid) if not str(uuid).startswith("GPU-") else str(uuid)
+
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id) as clk:
+        t_wall0 = time.perf_counter()
+        times = time_calls(call, args.steps, args.warmup, stream, flush)
+        t_wall = time.perf_counter() - t_wall0
+    torch.cuda.synchronize()
+    barrier(world)
+    lib.check(lib.sgemm_poll_error(stream))
+    clocks = clk.summary()
+
+    ms_local = statistics.mean(times)
+    ms = reduce_max(ms_local, world, dev)
+    flops_step = gemm_flops(M, N, K)
+    total_flops = reduce_sum(flops_step, world, dev)
+    value = total_flops / (ms / 1e3) / 1e12
+
+    bound, peak, peak_note = roofline_peak(mode, num_sms, peaks, peak_src)
+    achieved = flops_step / (ms_local / 1e3) / 1e12
+    kernel_key = f"{mode}:{WORKLOAD}"
+    traffic = committed_traffic(kernel_key)
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": UNIT,
+                "frac": achieved / peak, "traffic": traffic,
+                "kernel": f"sgemm {mode} path ({kernel_key})",
+                "peak_source": f"{peak_note}; {peak_src} MEASURED_PEAKS.json" if bound != "alu"
+                else peak_note,
+                "algorithmic_flops_per_launch": flops_step}
+    if clocks and clocks.get("sm_mhz") and bound == "alu":
+        roofline["frac_at_sampled_clock"] = achieved / (
+            num_sms * FP32_LANES_PER_SM * 2 * clocks["sm_mhz"] * 1e6 / 1e12)
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if rank == 0 or world > 1:
+        hA = torch.from_numpy(w["A"]).pin_memory()
+        hB = torch.from_numpy(w["B"]).pin_memory()
+        hC = torch.empty(M, N, dtype=torch.float32).pin_memory()
+        dA = torch.empty_like(A)
+        dB = torch.empty_like(B)
+        dC = torch.empty_like(C)
+
+        def e2e_call():
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            lib.check(lib.sgemm_batched_ex(mode, M, N, K, alpha, dA, K, dB, N, beta, dC, N, 0, 0,
+                                           0, 0, 0, 1, stream))
+            hC.copy_(dC, non_blocking=True)
+        e_steps = max(3, min(args.steps, 10))
+        et = time_calls(e2e_call, e_steps, 3, stream, flush)
+        e_ms = statistics.mean(et)
+        e2e = {"value": flops_step / (e_ms / 1e3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": 4 * (M * K + K * N), "d2h_bytes_per_step": 4 * M * N,
+               "ms_per_step": e_ms}
+
+    extra = {}
+    if not args.no_extra and rank == 0:
+        extra = extra_figures(lib, mode, dev, stream, flush, num_sms, peaks, peak_src)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "alpha": alpha,
+                       "beta": beta, "mode": mode, "inputs": "normal(0,1) seed 2",
+                       "l2": f"flushed before every timed step ({2 * l2 >> 20} MB write)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_call * args.steps,
+            "clocks": clocks,
+            "wall_s_timed_loop": t_wall,
+        }
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def extra_figures(lib, default_mode, dev, stream, flush, num_sms, peaks, peak_src):
+    """Per-path figures at 4092^3 and batched-GEMM figures (fewer steps)."""
+    import torch
+    import workloads
+    out = {"paths": {}, "bmm": {}}
+    w = workloads.make(WORKLOAD)
+    M, N, K = w["M"], w["N"], w["K"]
+    A = torch.from_numpy(w["A"]).to(dev)
+    B = torch.from_numpy(w["B"]).to(dev)
+    C = torch.zeros(M, N, device=dev)
+    for mode in ("fp32", "3xtf32", "tf32"):
+        st = lib.sgemm_batched_ex(mode, 16, 16, 16, 1.0, A, K, B, N, 0.0, C, N, 0, 0, 0, 0, 0, 1,
+                                  stream)
+        if st != lib.SGEMM_OK:
+            out["paths"][mode] = {"status": lib.sgemm_status_string(st)}
+            continue
+
+        def call(mode=mode):
+            lib.check(lib.sgemm_batched_ex(mode, M, N, K, 1.0, A, K, B, N, 0.0, C, N, 0, 0, 0, 0,
+                                           0, 1, stream))
+        t = statistics.median(time_calls(call, 10, 3, stream, flush))
+        tf = gemm_flops(M, N, K) / (t / 1e3) / 1e12
+        bound, peak, note = roofline_peak(mode, num_sms, peaks, peak_src)
+        out["paths"][mode] = {"tflops": tf, "ms": t, "bound": bound, "peak": peak,
+                              "frac": tf / peak}
+    del A, B, C
+    wb = workloads.make("bmm_q32_1024x1024x512")
+    Q, M, N, K = wb["Q"], wb["M"], wb["N"], wb["K"]
+    A = torch.from_numpy(wb["A"]).to(dev)
+    Bn = torch.from_numpy(wb["B"]).to(dev)                             # Q x K x N
+    Bt = torch.from_numpy(wb["B"].transpose(0, 2, 1).copy()).to(dev)   # Q x N x K
+    C = torch.from_numpy(wb["C0"]).to(dev)
+    for tB, Bd, ldb in ((1, Bt, K), (0, Bn, N)):
+        def call(tB=tB, Bd=Bd, ldb=ldb):
+            lib.check(lib.sgemm_batched_ex(default_mode, M, N, K, wb["alpha"], A, K, Bd, ldb,
+                                           wb["betas"][0], C, N, 0, tB, M * K, K * N, M * N, Q,
+                                           stream))
+        t = statistics.median(time_calls(call, 10, 3, stream, flush))
+        out["bmm"][f"transB={tB}"] = {"tflops": gemm_flops(M, N, K, Q) / (t / 1e3) / 1e12,
+                                      "ms": t, "mode": default_mode}
+    return out
+
+
+if __name__ == "__main__":
+    sys.exit(main())

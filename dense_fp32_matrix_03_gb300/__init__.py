@@ -1,0 +1,165 @@
+"""Python binding of libsgemm_gb300.so: single-precision GEMM on one GB300.
+
+A thin ctypes layer over the C ABI in include/sgemm.h, with the same names:
+it only marshals arguments (a torch tensor is passed by its data_ptr(), a
+torch stream by its cuda_stream handle) and returns the C status code.  Every
+step of the computation runs in the library's CUDA kernels; there is no
+fallback: the first call fails loudly (ImportError) if the library has not
+been built.
+
+    C = alpha * op(A) @ op(B) + beta * C        (row-major, fp32)
+
+Build the library with `python -m dense_fp32_matrix_03_gb300.build`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libsgemm_gb300.so")
+
+SGEMM_OK = 0
+SGEMM_ERR_INVALID_ARG = 1
+SGEMM_ERR_UNSUPPORTED = 2
+SGEMM_ERR_LAUNCH = 3
+SGEMM_ERR_TIMEOUT = 4
+
+SGEMM_MODE_DEFAULT = -1
+SGEMM_MODE_FP32 = 0
+SGEMM_MODE_3XTF32 = 1
+SGEMM_MODE_TF32 = 2
+MODES = {"fp32": SGEMM_MODE_FP32, "3xtf32": SGEMM_MODE_3XTF32, "tf32": SGEMM_MODE_TF32}
+
+# Exported symbols declared in include/sgemm.h: name -> (restype, argtypes)
+_i, _f, _p, _ll = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_longlong
+SIGNATURES = {
+    "sgemm": (_i, [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]),
+    "sgemm_batched": (_i, [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _i, _i, _ll, _ll, _ll,
+                           _i, _p]),
+    "sgemm_batched_ex": (_i, [_i, _i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _i, _i, _ll, _ll,
+                              _ll, _i, _p]),
+    "sgemm_set_default_mode": (_i, [_i]),
+    "sgemm_get_default_mode": (_i, []),
+    "sgemm_status_string": (ctypes.c_char_p, [_i]),
+    "sgemm_poll_error": (_i, [_p]),
+    "sgemm_selftest_wait_timeout": (_i, [_ll, _p]),
+    "sgemm_version": (_i, []),
+}
+
+
+class SgemmError(RuntimeError):
+    def __init__(self, status: int):
+        super().__init__(f"sgemm status {status}: {sgemm_status_string(status)}")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -m dense_fp32_matrix_03_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+class _Lazy:
+    """Opens the library on first use, so that the build module of this
+    package can be imported before the library exists."""
+
+    def __init__(self):
+        self._h = None
+
+    def __getattr__(self, name):
+        if self._h is None:
+            self._h = _load()
+        return getattr(self._h, name)
+
+
+_lib = _Lazy()
+
+
+def load():
+    """Open the library now (raises ImportError if it was not built)."""
+    return _lib.sgemm_version
+
+
+def _ptr(x):
+    """Device address of a tensor (data_ptr) or a raw integer address."""
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(s):
+    """cudaStream_t of a torch stream, a raw handle, or torch's current stream
+    when None (0, the legacy default stream, without torch)."""
+    if s is None:
+        try:
+            import torch
+            if torch.cuda.is_available() and torch.cuda.is_initialized():
+                return torch.cuda.current_stream().cuda_stream
+        except ImportError:
+            pass
+        return None
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream
+    return int(s) or None
+
+
+def sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
+    return _lib.sgemm(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C), ldc,
+                      _stream(stream))
+
+
+def sgemm_batched(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, transA, transB, strideA,
+                  strideB, strideC, Q, stream=None) -> int:
+    return _lib.sgemm_batched(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C), ldc,
+                              int(transA), int(transB), strideA, strideB, strideC, Q,
+                              _stream(stream))
+
+
+def sgemm_batched_ex(mode, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, transA, transB,
+                     strideA, strideB, strideC, Q, stream=None) -> int:
+    if isinstance(mode, str):
+        mode = MODES[mode]
+    return _lib.sgemm_batched_ex(mode, M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta,
+                                 _ptr(C), ldc, int(transA), int(transB), strideA, strideB,
+                                 strideC, Q, _stream(stream))
+
+
+def sgemm_set_default_mode(mode) -> int:
+    if isinstance(mode, str):
+        mode = MODES[mode]
+    return _lib.sgemm_set_default_mode(mode)
+
+
+def sgemm_get_default_mode() -> int:
+    return _lib.sgemm_get_default_mode()
+
+
+def sgemm_status_string(status: int) -> str:
+    return _lib.sgemm_status_string(status).decode()
+
+
+def sgemm_poll_error(stream=None) -> int:
+    return _lib.sgemm_poll_error(_stream(stream))
+
+
+def sgemm_selftest_wait_timeout(wait_cycles: int, stream=None) -> int:
+    return _lib.sgemm_selftest_wait_timeout(wait_cycles, _stream(stream))
+
+
+def sgemm_version() -> int:
+    return _lib.sgemm_version()
+
+
+def check(status: int) -> None:
+    """Raise SgemmError for a non-zero status."""
+    if status != SGEMM_OK:
+        raise SgemmError(status)

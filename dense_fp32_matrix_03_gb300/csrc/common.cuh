@@ -1,0 +1,168 @@
+// common.cuh -- device-side building blocks shared by the SGEMM kernels:
+// mbarrier waits with an iteration bound, TMA tile loads, cp.async copies,
+// the 128-byte shared-memory swizzle and the persistent grouped tile order.
+//
+// Everything here is inline PTX or plain CUDA written for sm_103a.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "params.h"
+
+namespace sg {
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Per-CTA abort state kept in shared memory.  A wait that runs out of
+// iterations records why in the device status word, raises the CTA's abort
+// flag so that every other role stops waiting too, and reports failure.
+struct Abort {
+    volatile int *flag;     // shared memory, 0 = running
+    unsigned int *status;   // global device status word
+    long long limit;        // clock64 cycles a wait may spin
+};
+
+// Waits until the phase with the given parity of `bar` has completed.
+// Returns false (and aborts the CTA) if the wait exceeds ab.limit cycles or
+// another role of the CTA has aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const Abort &ab,
+                                          unsigned int code)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*ab.flag) return false;
+        if (clock64() - t0 > ab.limit) {
+            atomicOr(ab.status, code);
+            *ab.flag = 1;
+            return false;
+        }
+    }
+}
+
+// --------------------------------------------------------------------- TMA
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+// 3-D tiled load of one box into shared memory; completion is signalled on
+// `bar` as transaction bytes.
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *m, uint64_t *bar,
+                                            int c0, int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// ---------------------------------------------------------------- cp.async
+
+// Copies `src_bytes` (0..16) bytes and zero-fills the rest of 16 bytes.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+// Copies `src_bytes` (0 or 4) bytes and zero-fills the rest of 4 bytes.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+// The mbarrier counts one (pre-declared) arrival when all of this thread's
+// earlier cp.async copies have landed.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// ------------------------------------------------------------------ layout
+
+// Byte offset of element (row, k) in a tile of 32-float (128-byte) rows laid
+// out with the 128-byte swizzle that TMA's SWIZZLE_128B mode writes: the
+// 16-byte chunk index inside a row is XORed with the row index modulo 8.
+// The tile base must be 1024-byte aligned.
+__device__ __forceinline__ uint32_t sw128_offset(int row, int k)
+{
+    return static_cast<uint32_t>(row * 128 + ((((k >> 2) ^ row) & 7) << 4) + ((k & 3) << 2));
+}
+
+// --------------------------------------------------------------- scheduler
+
+// Persistent grouped tile order.  Linear tile id t -> (q, tm, tn): batch
+// outermost; inside a batch, GROUP_M rows of tiles are walked column by column
+// so that CTAs running at the same time share A rows and B columns in L2.
+struct TileCoord {
+    int q, tm, tn;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(long long t, const GemmParams &p)
+{
+    const long long per_q = static_cast<long long>(p.tiles_m) * p.tiles_n;
+    TileCoord c;
+    c.q = static_cast<int>(t / per_q);
+    int r = static_cast<int>(t - c.q * per_q);
+    const int in_group = p.group_m * p.tiles_n;
+    const int g = r / in_group;
+    const int first_m = g * p.group_m;
+    const int gsize = min(p.tiles_m - first_m, p.group_m);
+    const int rr = r - g * in_group;
+    c.tm = first_m + rr % gsize;
+    c.tn = rr / gsize;
+    return c;
+}
+
+}  // namespace sg

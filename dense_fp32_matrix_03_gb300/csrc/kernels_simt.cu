@@ -1,0 +1,71 @@
+// kernels_simt.cu -- instantiations and the host launcher of the FP32
+// CUDA-core SGEMM kernel (simt_fp32.cuh).
+#include <cstring>
+
+#include "../../include/sgemm.h"
+#include "internal.h"
+#include "simt_fp32.cuh"
+
+namespace sg {
+
+namespace {
+
+// Tile configuration of the FP32 path: a 128 x 128 CTA tile, eight consumer
+// warps of 64 x 32 (8 x 8 outputs per lane), four 32 KB stages.
+using SimtMain = SimtCfg<128, 128, 64, 32, 4>;
+constexpr int kGroupM = 8;
+
+template <class Cfg, bool A_KIN, bool B_KIN, bool USE_TMA, bool EVEN_K>
+int launch_one(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
+{
+    auto kern = simt_sgemm_kernel<Cfg, A_KIN, B_KIN, USE_TMA, EVEN_K>;
+    // The attribute is per device; setting it on every call costs about a
+    // microsecond and keeps the launcher free of per-device caches.
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::SMEM_BYTES) != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
+    long long grid = plan.p.num_tiles;
+    if (grid > plan.num_sms) grid = plan.num_sms;
+    kern<<<static_cast<unsigned>(grid), Cfg::THREADS, Cfg::SMEM_BYTES, plan.stream>>>(tmA, tmB,
+                                                                                     plan.p);
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
+template <class Cfg, bool USE_TMA, bool EVEN_K>
+int dispatch_layout(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
+{
+    const bool a_kin = !plan.transA, b_kin = plan.transB;
+    if (a_kin && !b_kin) return launch_one<Cfg, true, false, USE_TMA, EVEN_K>(plan, tmA, tmB);
+    if (a_kin && b_kin) return launch_one<Cfg, true, true, USE_TMA, EVEN_K>(plan, tmA, tmB);
+    if (!a_kin && !b_kin) return launch_one<Cfg, false, false, USE_TMA, EVEN_K>(plan, tmA, tmB);
+    return launch_one<Cfg, false, true, USE_TMA, EVEN_K>(plan, tmA, tmB);
+}
+
+}  // namespace
+
+int launch_simt(Plan &plan)
+{
+    using Cfg = SimtMain;
+    GemmParams &p = plan.p;
+    p.tiles_m = (p.M + Cfg::BM - 1) / Cfg::BM;
+    p.tiles_n = (p.N + Cfg::BN - 1) / Cfg::BN;
+    p.k_blocks = (p.K + kBK - 1) / kBK;
+    p.group_m = kGroupM;
+    p.num_tiles = static_cast<long long>(p.Q) * p.tiles_m * p.tiles_n;
+    plan.even_k = (p.K % kBK) == 0;
+
+    alignas(64) CUtensorMap tmA;
+    alignas(64) CUtensorMap tmB;
+    std::memset(&tmA, 0, sizeof(tmA));
+    std::memset(&tmB, 0, sizeof(tmB));
+    bool use_tma = plan.a_tma && plan.b_tma;
+    if (use_tma) {
+        use_tma = encode_operand(&tmA, p.A, !plan.transA, p.M, p.K, p.lda, p.Q, p.sA, Cfg::BM) &&
+                  encode_operand(&tmB, p.B, plan.transB, p.N, p.K, p.ldb, p.Q, p.sB, Cfg::BN);
+    }
+    if (use_tma) return dispatch_layout<Cfg, true, false>(plan, tmA, tmB);
+    if (plan.even_k) return dispatch_layout<Cfg, false, true>(plan, tmA, tmB);
+    return dispatch_layout<Cfg, false, false>(plan, tmA, tmB);
+}
+
+}  // namespace sg

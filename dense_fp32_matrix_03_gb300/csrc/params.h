@@ -1,0 +1,39 @@
+// params.h -- the launch parameters every SGEMM kernel receives, and the
+// per-call plan the host builds.  Internal to the library (not part of the
+// C ABI in include/sgemm.h).
+#pragma once
+
+#include <cstdint>
+
+namespace sg {
+
+// Device status word bits (read back by sgemm_poll_error()).
+enum : unsigned int {
+    kStatusWaitFull = 1u << 0,   // a consumer waited too long for a loaded stage
+    kStatusWaitEmpty = 1u << 1,  // the producer waited too long for a free stage
+    kStatusWaitMma = 1u << 2,    // a tensor-core completion never arrived
+    kStatusWaitAcc = 1u << 3,    // the epilogue waited too long for an accumulator
+    kStatusWaitTest = 1u << 4,   // the bounded-wait self test ran out (expected)
+    kStatusWaitConv = 1u << 5,   // the MMA issuer waited too long for split operands
+};
+
+struct GemmParams {
+    int M, N, K, Q;
+    float alpha, beta;
+    const float *A;
+    const float *B;
+    float *C;
+    long long lda, ldb, ldc;
+    long long sA, sB, sC;      // batch strides in elements (0 = broadcast)
+    int tiles_m, tiles_n;      // output tiles per batch entry
+    int k_blocks;              // ceil(K / BK)
+    int group_m;               // rows of tiles per scheduler group
+    long long num_tiles;       // Q * tiles_m * tiles_n
+    int a_q_step, b_q_step;    // TMA batch coordinate multiplier (0 = broadcast)
+    int a_vec4, b_vec4;        // fallback producer may copy 16 bytes at a time
+    int c_vec4;                // epilogue may use 16-byte C accesses
+    unsigned int *status;      // device status word
+    long long wait_limit;      // clock64 cycles a bounded wait may spin
+};
+
+}  // namespace sg

@@ -1,0 +1,116 @@
+/*
+ * sgemm.h -- C ABI of the GB300 single-precision GEMM library
+ * (libsgemm_gb300.so).
+ *
+ * Operation (the SGEMM of "From 1% to 94% of cuBLAS, one kernel at a time",
+ * arpit2412.github.io/blog/cuda-sgemm.html, section "Napkin math for
+ * 4092 x 4092", and its first kernel's per-element rule):
+ *
+ *     C = alpha * op(A) @ op(B) + beta * C
+ *
+ * with op(A) M x K, op(B) K x N, C M x N, fp32, every matrix row-major:
+ * element (r, c) of a matrix with leading dimension ld is at r * ld + c
+ * (the same page's storage paragraph).  Transposed operands and a strided
+ * batch follow "Triton Optimization Reference (cuTile -> Triton)",
+ * sections 2 (transpose by strides) and 3 (batch index with a per-batch
+ * stride):
+ *   transA == 0: A is stored M x K, lda >= K;  op(A)[i,k] = A[i*lda + k]
+ *   transA != 0: A is stored K x M, lda >= M;  op(A)[i,k] = A[k*lda + i]
+ *   transB == 0: B is stored K x N, ldb >= N;  op(B)[k,j] = B[k*ldb + j]
+ *   transB != 0: B is stored N x K, ldb >= K;  op(B)[k,j] = B[j*ldb + k]
+ *   C is stored M x N, ldc >= N.
+ *   Batch q (0 <= q < Q) uses A + q*strideA, B + q*strideB, C + q*strideC;
+ *   strides count elements; strideA or strideB may be 0 (broadcast).
+ *
+ * BLAS conventions where the pages are silent:
+ *   - beta == 0: C is not read (NaN/Inf already in C do not propagate).
+ *   - alpha == 0 or K == 0: C = beta * C; A and B are not read.
+ *   - M == 0, N == 0 or Q == 0: nothing is done.
+ *
+ * Pointers A, B, C are DEVICE pointers owned by the caller.  The library
+ * allocates no memory, never synchronises, and returns as soon as the work
+ * is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ * The output is valid once the stream reaches that point.
+ *
+ * Errors: arguments are checked on the host before anything is launched; an
+ * invalid call returns SGEMM_ERR_INVALID_ARG and launches nothing.  A kernel
+ * whose internal wait runs out of its bound (about a second) stops, leaves C
+ * unspecified, and sets a device status word that sgemm_poll_error() reports
+ * as SGEMM_ERR_TIMEOUT.  Calls are thread-safe; one call's kernels may run
+ * concurrently with another call's only on different streams.
+ */
+#ifndef SGEMM_GB300_H
+#define SGEMM_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+#define SGEMM_OK 0
+#define SGEMM_ERR_INVALID_ARG 1 /* a dimension, leading dimension, stride, pointer or mode */
+#define SGEMM_ERR_UNSUPPORTED 2 /* valid call this build cannot run (e.g. no sm_103 GPU)   */
+#define SGEMM_ERR_LAUNCH 3      /* the CUDA runtime refused a launch or attribute call    */
+#define SGEMM_ERR_TIMEOUT 4     /* a kernel's bounded internal wait ran out (device word) */
+
+/* Contraction paths.
+ *   FP32  : FP32 CUDA-core (FFMA) path; every product and sum in fp32.
+ *   3XTF32: tensor-core path; each operand x is split into hi = tf32(x) and
+ *           lo = tf32(x - hi) and the product is accumulated in fp32 as
+ *           lo*hi + hi*lo + hi*hi, which meets the FP32 accuracy bound.
+ *   TF32  : one tensor-core pass on tf32-rounded operands (looser accuracy,
+ *           max |C - C_ref| / (|alpha| |A||B| + |beta C|) <= 2e-3).
+ *   DEFAULT: the process default (sgemm_set_default_mode), initially FP32. */
+#define SGEMM_MODE_DEFAULT (-1)
+#define SGEMM_MODE_FP32 0
+#define SGEMM_MODE_3XTF32 1
+#define SGEMM_MODE_TF32 2
+
+/* C = alpha*A@B + beta*C, no transposes, Q = 1, default mode. */
+int sgemm(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
+          float beta, float *C, int ldc, void *stream);
+
+/* Strided-batched, transposed-operand form (conventions above), default mode.
+ * Requires strideC >= (M-1)*ldc + N when Q > 1 (batch outputs may not
+ * overlap); strides must be >= 0. */
+int sgemm_batched(int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+                  int ldb, float beta, float *C, int ldc, int transA, int transB,
+                  long long strideA, long long strideB, long long strideC, int Q, void *stream);
+
+/* As sgemm_batched, with the contraction path chosen explicitly
+ * (SGEMM_MODE_*; DEFAULT means the process default). */
+int sgemm_batched_ex(int mode, int M, int N, int K, float alpha, const float *A, int lda,
+                     const float *B, int ldb, float beta, float *C, int ldc, int transA,
+                     int transB, long long strideA, long long strideB, long long strideC, int Q,
+                     void *stream);
+
+/* Process-wide default path used by sgemm() and sgemm_batched().  Returns
+ * SGEMM_ERR_INVALID_ARG for an unknown mode (DEFAULT is not a valid value
+ * here). */
+int sgemm_set_default_mode(int mode);
+int sgemm_get_default_mode(void);
+
+/* Static, never-NULL description of a status code. */
+const char *sgemm_status_string(int status);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word.  Returns SGEMM_OK, SGEMM_ERR_TIMEOUT if a kernel's bounded wait ran
+ * out since the last poll, or SGEMM_ERR_LAUNCH if the stream reports a CUDA
+ * error. */
+int sgemm_poll_error(void *stream);
+
+/* Self test of the bounded-wait machinery: launches one small kernel whose
+ * mbarrier wait is never satisfied and whose bound is `wait_cycles` clock
+ * cycles (1 .. 2^31), so that it gives up, records the timeout in the status
+ * word and exits normally.  A following sgemm_poll_error() returns
+ * SGEMM_ERR_TIMEOUT.  Nothing faults and the context stays usable. */
+int sgemm_selftest_wait_timeout(long long wait_cycles, void *stream);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int sgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_GB300_H */

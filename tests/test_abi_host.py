@@ -1,0 +1,108 @@
+"""CPU-only checks of the C ABI: the library loads, exports every entry point
+that include/sgemm.h declares, and rejects invalid arguments on the host
+before touching a GPU."""
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dense_fp32_matrix_03_gb300 import build
+    build.build()
+    import dense_fp32_matrix_03_gb300 as m
+    m.load()
+    return m
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "sgemm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(sgemm\w*)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("sgemm", "sgemm_batched", "sgemm_batched_ex", "sgemm_poll_error",
+                 "sgemm_status_string", "sgemm_set_default_mode"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s+(\w+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert name in lib.SIGNATURES, f"binding lacks {name}"
+    assert set(lib.SIGNATURES) == set(declared_functions())
+
+
+def test_version_and_status_strings(lib):
+    assert lib.sgemm_version() >= 100
+    for code in range(0, 5):
+        assert lib.sgemm_status_string(code)
+    assert lib.sgemm_status_string(99) == "unknown status"
+
+
+def test_default_mode_roundtrip(lib):
+    old = lib.sgemm_get_default_mode()
+    try:
+        for mode in (lib.SGEMM_MODE_3XTF32, lib.SGEMM_MODE_TF32, lib.SGEMM_MODE_FP32):
+            assert lib.sgemm_set_default_mode(mode) == lib.SGEMM_OK
+            assert lib.sgemm_get_default_mode() == mode
+        assert lib.sgemm_set_default_mode(7) == lib.SGEMM_ERR_INVALID_ARG
+        assert lib.sgemm_set_default_mode(lib.SGEMM_MODE_DEFAULT) == lib.SGEMM_ERR_INVALID_ARG
+    finally:
+        lib.sgemm_set_default_mode(old)
+
+
+FAKE = 1 << 40  # a never-dereferenced, 16-byte aligned address
+
+
+def ex(lib, **kw):
+    a = dict(mode=0, M=8, N=8, K=8, alpha=1.0, A=FAKE, lda=8, B=FAKE, ldb=8, beta=0.0, C=FAKE,
+             ldc=8, transA=0, transB=0, strideA=0, strideB=0, strideC=0, Q=1)
+    a.update(kw)
+    return lib.sgemm_batched_ex(a["mode"], a["M"], a["N"], a["K"], a["alpha"], a["A"], a["lda"],
+                                a["B"], a["ldb"], a["beta"], a["C"], a["ldc"], a["transA"],
+                                a["transB"], a["strideA"], a["strideB"], a["strideC"], a["Q"])
+
+
+@pytest.mark.parametrize("bad", [
+    dict(M=-1), dict(N=-1), dict(K=-1), dict(Q=-1),
+    dict(lda=7), dict(ldb=7), dict(ldc=7),
+    dict(transA=1, M=9, lda=8), dict(transB=1, K=9, ldb=8, lda=9),
+    dict(C=0), dict(A=0), dict(B=0),
+    dict(Q=2, strideC=7 * 8 + 7),          # batch outputs would overlap
+    dict(Q=2, strideA=-1, strideC=64), dict(Q=2, strideB=-8, strideC=64),
+    dict(mode=3), dict(mode=-2),
+])
+def test_invalid_arguments_are_rejected_before_any_launch(lib, bad):
+    assert ex(lib, **bad) == lib.SGEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("empty", [dict(M=0), dict(N=0), dict(Q=0),
+                                   dict(M=0, C=0, A=0, B=0)])
+def test_empty_problems_are_a_no_op(lib, empty):
+    assert ex(lib, **empty) == lib.SGEMM_OK
+
+
+def test_null_operands_allowed_when_not_read(lib):
+    # alpha == 0 or K == 0: A and B are not read, so NULL passes validation.
+    # Validation passes; without a GPU the call then reports UNSUPPORTED.
+    rc = ex(lib, A=0, B=0, alpha=0.0)
+    assert rc in (lib.SGEMM_OK, lib.SGEMM_ERR_UNSUPPORTED)
+    rc = ex(lib, A=0, B=0, K=0, lda=1)
+    assert rc in (lib.SGEMM_OK, lib.SGEMM_ERR_UNSUPPORTED)
+
+
+def test_plain_sgemm_validates_too(lib):
+    assert lib.sgemm(4, 4, 4, 1.0, FAKE, 3, FAKE, 4, 0.0, FAKE, 4) == lib.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_batched(4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4, 0, 0, 0, 0, 10, 2) \
+        == lib.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_selftest_wait_timeout(0) == lib.SGEMM_ERR_INVALID_ARG
