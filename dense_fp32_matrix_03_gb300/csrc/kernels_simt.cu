@@ -10,9 +10,16 @@ namespace sg {
 
 namespace {
 
-// Tile configuration of the FP32 path: a 128 x 128 CTA tile, eight consumer
-// warps of 64 x 32 (8 x 8 outputs per lane), four 32 KB stages.
-using SimtMain = SimtCfg<128, 128, 64, 32, 4>;
+// Tile configuration of the FP32 path (overridable at build time for
+// tuning sweeps): CTA tile BM x BN, warp tile WM x WN, pipeline stages.
+#ifndef SG_SIMT_BM
+#define SG_SIMT_BM 128
+#define SG_SIMT_BN 128
+#define SG_SIMT_WM 64
+#define SG_SIMT_WN 32
+#define SG_SIMT_STAGES 4
+#endif
+using SimtMain = SimtCfg<SG_SIMT_BM, SG_SIMT_BN, SG_SIMT_WM, SG_SIMT_WN, SG_SIMT_STAGES>;
 constexpr int kGroupM = 8;
 
 template <class Cfg, bool A_KIN, bool B_KIN, bool USE_TMA, bool EVEN_K>
@@ -25,9 +32,10 @@ int launch_one(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
                              Cfg::SMEM_BYTES) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
     long long grid = plan.p.num_tiles;
-    if (grid > plan.num_sms) grid = plan.num_sms;
-    kern<<<static_cast<unsigned>(grid), Cfg::THREADS, Cfg::SMEM_BYTES, plan.stream>>>(tmA, tmB,
-                                                                                     plan.p);
+    if (grid > static_cast<long long>(plan.num_sms) * kMinBlocks)
+        grid = static_cast<long long>(plan.num_sms) * kMinBlocks;
+    kern<<<static_cast<unsigned>(grid), Cfg::THREADS, Cfg::SMEM_BYTES, plan.stream>>>(
+        tmA, tmB, plan.p);
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
 

@@ -29,18 +29,23 @@
 //  * the epilogue fuses alpha and beta: C is read only when beta != 0.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace sg {
 
 constexpr int kBK = 32;  // K per pipeline stage (one 128-byte swizzle row of fp32)
 
+
 template <int BM_, int BN_, int WM_, int WN_, int STAGES_>
 struct SimtCfg {
     static constexpr int BM = BM_, BN = BN_, WM = WM_, WN = WN_, STAGES = STAGES_;
     static constexpr int WARPS_M = BM / WM, WARPS_N = BN / WN;
     static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
-    static constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;
+    // The consumer warps issue the copies themselves (no producer warp), so
+    // that each warp may use up to 255 registers.
+    static constexpr int THREADS = CONSUMER_WARPS * 32;
     static constexpr int WMITER = WM / 32, WNITER = WN / 16;
     static constexpr int TM = 4 * WMITER, TN = 4 * WNITER;
     static constexpr int A_BYTES = BM * kBK * 4, B_BYTES = BN * kBK * 4;
@@ -78,59 +83,144 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
 
 // ------------------------------------------------------------ producers
 
+// Who fills the stages.  The CTA's k-blocks are numbered j = 0, 1, ... over
+// all of its tiles in order; k-block j lives in stage j % STAGES.  All stages
+// are filled up front; after the warps have consumed k-block `it`, the stage
+// of k-block it-kLag (which every warp has normally released by then) is
+// refilled, so the copies run STAGES-1-kLag k-blocks ahead of the consumers.
+// The wait for that release is bounded like every other wait.  Positions are
+// advanced incrementally: no division on the per-k-block path.
+#ifndef SG_SIMT_LAG
+#define SG_SIMT_LAG 1
+#endif
+constexpr int kLag = SG_SIMT_LAG;
+// Consumer loop form: software-pipelined over k-groups (1) or a plain loop
+// unrolled kGroupUnroll times (0); CTAs per SM the kernel is compiled for.
+#ifndef SG_SIMT_PIPE
+#define SG_SIMT_PIPE 0
+#endif
+#ifndef SG_SIMT_UNROLL
+#define SG_SIMT_UNROLL 4
+#endif
+#ifndef SG_SIMT_MINB
+#define SG_SIMT_MINB 1
+#endif
+constexpr bool kPipelined = SG_SIMT_PIPE != 0;
+constexpr int kGroupUnroll = SG_SIMT_UNROLL;
+constexpr int kMinBlocks = SG_SIMT_MINB;
+
+// Walks the (tile, k-block) sequence of one CTA.
+struct KPos {
+    long long tile;   // global tile index
+    int kb;           // k-block inside the tile
+    int stage;        // stage of this k-block
+    uint32_t phase;   // round parity of this k-block's stage
+    TileCoord tc;
+
+    __device__ __forceinline__ void start(const GemmParams &p)
+    {
+        tile = blockIdx.x;
+        kb = 0;
+        stage = 0;
+        phase = 0;
+        if (tile < p.num_tiles) tc = tile_coord(tile, p);
+    }
+    template <int STAGES>
+    __device__ __forceinline__ void next(const GemmParams &p)
+    {
+        if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+        }
+        if (++kb == p.k_blocks) {
+            kb = 0;
+            tile += gridDim.x;
+            if (tile < p.num_tiles) tc = tile_coord(tile, p);
+        }
+    }
+};
+
+// TMA: lane 0 of warp 0 issues two tensor loads per stage.
 template <class Cfg, bool A_KIN, bool B_KIN>
-__device__ __forceinline__ void simt_tma_producer(const CUtensorMap *tmA, const CUtensorMap *tmB,
-                                                  const GemmParams &p, uint8_t *smem,
-                                                  uint64_t *full, uint64_t *empty,
-                                                  const Abort &ab)
-{
-    tma_prefetch_desc(tmA);
-    tma_prefetch_desc(tmB);
-    long long it = 0;
-    bool ok = true;
-    for (long long t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-        const TileCoord tc = tile_coord(t, p);
-        const int m0 = tc.tm * Cfg::BM, n0 = tc.tn * Cfg::BN;
-        const int qa = tc.q * p.a_q_step, qb = tc.q * p.b_q_step;
-        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
-            const int s = static_cast<int>(it % Cfg::STAGES);
-            const uint32_t ph = static_cast<uint32_t>((it / Cfg::STAGES) & 1);
-            if (!mbar_wait(&empty[s], ph ^ 1u, ab, kStatusWaitEmpty)) {
-                ok = false;
-                break;
-            }
+struct TmaIssuer {
+    static constexpr unsigned kFullCount = 1;
+    const CUtensorMap *tmA, *tmB;
+    const GemmParams *p;
+    uint8_t *smem;
+    uint64_t *full, *empty;
+    long long total;   // k-blocks this CTA will consume
+    long long issued;  // k-blocks issued so far (lane 0 of warp 0)
+    KPos pos;          // next k-block to issue
+
+    // Issues k-blocks until `target` (exclusive) have been issued.
+    __device__ __forceinline__ bool issue_to(long long target, const Abort &ab)
+    {
+        if (target > total) target = total;
+        while (issued < target) {
+            const int s = pos.stage;
+            // a fresh barrier passes parity 1 at once, so the first round
+            // needs no special case
+            if (!mbar_wait(&empty[s], pos.phase ^ 1u, ab, kStatusWaitEmpty)) return false;
             uint8_t *sa = smem + s * Cfg::STAGE_BYTES;
             uint8_t *sb = sa + Cfg::A_BYTES;
+            const int m0 = pos.tc.tm * Cfg::BM, n0 = pos.tc.tn * Cfg::BN, k0 = pos.kb * kBK;
+            const int qa = pos.tc.q * p->a_q_step, qb = pos.tc.q * p->b_q_step;
             mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
-            const int k0 = kb * kBK;
             if (A_KIN) tma_load_3d(sa, tmA, &full[s], k0, m0, qa);
             else       tma_load_3d(sa, tmA, &full[s], m0, k0, qa);
             if (B_KIN) tma_load_3d(sb, tmB, &full[s], k0, n0, qb);
             else       tma_load_3d(sb, tmB, &full[s], n0, k0, qb);
+            ++issued;
+            pos.template next<Cfg::STAGES>(*p);
         }
+        return true;
     }
-    if (!ok) {  // let the copies already issued land before leaving
-        for (long long j = it - 1; j >= 0 && j >= it - Cfg::STAGES; --j)
-            mbar_drain(&full[j % Cfg::STAGES], static_cast<uint32_t>((j / Cfg::STAGES) & 1),
-                       ab.limit);
-    }
-}
 
-// One operand tile by cp.async.  KIN: tile rows are `rows` (M or N) of 32
-// k-values, swizzled; otherwise the tile is [32 k][ROWS] unswizzled.
-// Global element (r, k) of a K-inner operand is at base[r*ld + k]; of an
-// M/N-inner operand at base[k*ld + r].
+    __device__ __forceinline__ void prologue(int warp, int lane, const Abort &ab)
+    {
+        if (warp != 0 || lane != 0) return;
+        tma_prefetch_desc(tmA);
+        tma_prefetch_desc(tmB);
+        issued = 0;
+        pos.start(*p);
+        issue_to(Cfg::STAGES, ab);
+    }
+
+    // Called by every lane of every consumer warp after k-block `it` was
+    // consumed and released.  Returns false (warp-uniformly) on abort.
+    __device__ __forceinline__ bool refill(long long it, const Abort &ab, int warp, int lane)
+    {
+        if (warp != 0) return true;
+        int ok = 1;
+        if (lane == 0) ok = issue_to(it + 1 - kLag + Cfg::STAGES, ab) ? 1 : 0;
+        return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    }
+
+    // After an abort: let every issued copy land before the CTA exits.
+    __device__ __forceinline__ void drain(long long limit, int warp, int lane)
+    {
+        if (warp != 0 || lane != 0) return;
+        for (long long j = issued - 1; j >= 0 && j >= issued - Cfg::STAGES; --j)
+            mbar_drain(&full[j % Cfg::STAGES], static_cast<uint32_t>((j / Cfg::STAGES) & 1),
+                       limit);
+    }
+};
+
+// One operand tile by cp.async, spread over `nthr` threads.  KIN: tile rows
+// are ROWS (M or N) rows of 32 k-values, swizzled; otherwise the tile is
+// [32 k][ROWS] unswizzled.  Global element (r, k) of a K-inner operand is at
+// base[r*ld + k]; of an M/N-inner operand at base[k*ld + r].  Out-of-range
+// elements are zero-filled (source size 0), never read.
 template <int ROWS, bool KIN, bool EVEN_K>
 __device__ __forceinline__ void cp_async_tile(uint8_t *dst, const float *base, long long ld,
-                                              int r0, int rlim, int k0, int K, bool vec4,
-                                              int lane)
+                                              int r0, int rlim, int k0, int K, bool vec4, int tid,
+                                              int nthr)
 {
     const uint32_t d0 = smem_u32(dst);
     if (vec4) {
         if (KIN) {
             constexpr int UNITS = ROWS * (kBK / 4);
-#pragma unroll 4
-            for (int u = lane; u < UNITS; u += 32) {
+            for (int u = tid; u < UNITS; u += nthr) {
                 const int r = u >> 3, c = u & 7;
                 const int gr = r0 + r, gk = k0 + 4 * c;
                 int nval = (gr < rlim) ? (EVEN_K ? 4 : min(4, K - gk)) : 0;
@@ -140,8 +230,7 @@ __device__ __forceinline__ void cp_async_tile(uint8_t *dst, const float *base, l
             }
         } else {
             constexpr int UNITS = kBK * (ROWS / 4);
-#pragma unroll 4
-            for (int u = lane; u < UNITS; u += 32) {
+            for (int u = tid; u < UNITS; u += nthr) {
                 const int k = u / (ROWS / 4), c = u % (ROWS / 4);
                 const int gk = k0 + k, gr = r0 + 4 * c;
                 int nval = (EVEN_K || gk < K) ? min(4, rlim - gr) : 0;
@@ -153,8 +242,7 @@ __device__ __forceinline__ void cp_async_tile(uint8_t *dst, const float *base, l
     } else {
         if (KIN) {
             constexpr int UNITS = ROWS * kBK;
-#pragma unroll 4
-            for (int u = lane; u < UNITS; u += 32) {
+            for (int u = tid; u < UNITS; u += nthr) {
                 const int r = u >> 5, k = u & 31;
                 const int gr = r0 + r, gk = k0 + k;
                 const bool v = gr < rlim && (EVEN_K || gk < K);
@@ -162,8 +250,7 @@ __device__ __forceinline__ void cp_async_tile(uint8_t *dst, const float *base, l
             }
         } else {
             constexpr int UNITS = kBK * ROWS;
-#pragma unroll 4
-            for (int u = lane; u < UNITS; u += 32) {
+            for (int u = tid; u < UNITS; u += nthr) {
                 const int k = u / ROWS, r = u % ROWS;
                 const int gk = k0 + k, gr = r0 + r;
                 const bool v = gr < rlim && (EVEN_K || gk < K);
@@ -173,45 +260,174 @@ __device__ __forceinline__ void cp_async_tile(uint8_t *dst, const float *base, l
     }
 }
 
+// cp.async: every thread copies its share of the stage (operands TMA cannot
+// describe: unaligned bases, row pitches or batch strides that are not
+// multiples of 16 bytes) and the stage's full barrier counts one arrival per
+// thread when that thread's copies have landed.
 template <class Cfg, bool A_KIN, bool B_KIN, bool EVEN_K>
-__device__ __forceinline__ void simt_cpasync_producer(const GemmParams &p, uint8_t *smem,
-                                                      uint64_t *full, uint64_t *empty,
-                                                      const Abort &ab, int lane)
-{
-    long long it = 0;
-    bool ok = true;
-    for (long long t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-        const TileCoord tc = tile_coord(t, p);
-        const int m0 = tc.tm * Cfg::BM, n0 = tc.tn * Cfg::BN;
-        const float *Aq = p.A + tc.q * p.sA;
-        const float *Bq = p.B + tc.q * p.sB;
-        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
-            const int s = static_cast<int>(it % Cfg::STAGES);
-            const uint32_t ph = static_cast<uint32_t>((it / Cfg::STAGES) & 1);
-            if (!warp_wait(&empty[s], ph ^ 1u, ab, kStatusWaitEmpty, lane)) {
-                ok = false;
-                break;
-            }
+struct CpAsyncIssuer {
+    static constexpr unsigned kFullCount = Cfg::THREADS;
+    const GemmParams *p;
+    uint8_t *smem;
+    uint64_t *full, *empty;
+    long long total;
+    long long issued;
+    KPos pos;
+
+    __device__ __forceinline__ bool issue_to(long long target, const Abort &ab, int warp,
+                                             int lane)
+    {
+        if (target > total) target = total;
+        const int tid = warp * 32 + lane;
+        while (issued < target) {
+            const int s = pos.stage;
+            if (!warp_wait(&empty[s], pos.phase ^ 1u, ab, kStatusWaitEmpty, lane)) return false;
             uint8_t *sa = smem + s * Cfg::STAGE_BYTES;
             uint8_t *sb = sa + Cfg::A_BYTES;
-            const int k0 = kb * kBK;
-            cp_async_tile<Cfg::BM, A_KIN, EVEN_K>(sa, Aq, p.lda, m0, p.M, k0, p.K,
-                                                  p.a_vec4 != 0, lane);
-            cp_async_tile<Cfg::BN, B_KIN, EVEN_K>(sb, Bq, p.ldb, n0, p.N, k0, p.K,
-                                                  p.b_vec4 != 0, lane);
+            const int k0 = pos.kb * kBK;
+            const TileCoord &tc = pos.tc;
+            cp_async_tile<Cfg::BM, A_KIN, EVEN_K>(sa, p->A + tc.q * p->sA, p->lda,
+                                                  tc.tm * Cfg::BM, p->M, k0, p->K,
+                                                  p->a_vec4 != 0, tid, Cfg::THREADS);
+            cp_async_tile<Cfg::BN, B_KIN, EVEN_K>(sb, p->B + tc.q * p->sB, p->ldb,
+                                                  tc.tn * Cfg::BN, p->N, k0, p->K,
+                                                  p->b_vec4 != 0, tid, Cfg::THREADS);
             cp_async_arrive_noinc(&full[s]);
+            ++issued;
+            pos.template next<Cfg::STAGES>(*p);
         }
+        return true;
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
+
+    __device__ __forceinline__ void prologue(int warp, int lane, const Abort &ab)
+    {
+        issued = 0;
+        pos.start(*p);
+        issue_to(Cfg::STAGES, ab, warp, lane);
+    }
+
+    __device__ __forceinline__ bool refill(long long it, const Abort &ab, int warp, int lane)
+    {
+        return issue_to(it + 1 - kLag + Cfg::STAGES, ab, warp, lane);
+    }
+
+    __device__ __forceinline__ void drain(long long, int, int)
+    {
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    }
+};
 
 // ------------------------------------------------------------- consumer
 
+__device__ __forceinline__ float4 lds128(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// Operand fragments of one k-group (4 consecutive k) for one lane:
+// a[kk][i] = op(A)[row i of the lane, k = 4g + kk], b[kk][j] likewise.
+template <class Cfg>
+struct Frag {
+    float a[4][Cfg::TM];
+    float b[4][Cfg::TN];
+};
+
+// Loads the fragments of k-group g from a stage.  a_base / b_base are this
+// lane's base addresses inside the stage (see simt_consumer).
 template <class Cfg, bool A_KIN, bool B_KIN>
+__device__ __forceinline__ void load_frag(Frag<Cfg> &f, uint32_t a_base, uint32_t b_base,
+                                          uint32_t a_key, uint32_t b_key, int g)
+{
+    constexpr int WMITER = Cfg::WMITER, WNITER = Cfg::WNITER;
+    if (A_KIN) {
+        const uint32_t ag = a_base + ((static_cast<uint32_t>(g) << 4) ^ a_key);
+#pragma unroll
+        for (int wm = 0; wm < WMITER; ++wm)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 v = lds128(ag + (wm * 32 + i * 8) * 128);
+                f.a[0][wm * 4 + i] = v.x;
+                f.a[1][wm * 4 + i] = v.y;
+                f.a[2][wm * 4 + i] = v.z;
+                f.a[3][wm * 4 + i] = v.w;
+            }
+    } else {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+            for (int wm = 0; wm < WMITER; ++wm) {
+                const float4 v = lds128(a_base + ((4 * g + kk) * Cfg::BM + wm * 32) * 4);
+                f.a[kk][wm * 4 + 0] = v.x;
+                f.a[kk][wm * 4 + 1] = v.y;
+                f.a[kk][wm * 4 + 2] = v.z;
+                f.a[kk][wm * 4 + 3] = v.w;
+            }
+    }
+    if (B_KIN) {
+        const uint32_t bg0 = b_base + ((static_cast<uint32_t>(g) << 4) ^ b_key);
+        const uint32_t bg1 = b_base + ((static_cast<uint32_t>(g ^ 4) << 4) ^ b_key);
+#pragma unroll
+        for (int wn = 0; wn < WNITER; ++wn)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 v = lds128(((j & 1) ? bg1 : bg0) + (wn * 16 + j * 4) * 128);
+                f.b[0][wn * 4 + j] = v.x;
+                f.b[1][wn * 4 + j] = v.y;
+                f.b[2][wn * 4 + j] = v.z;
+                f.b[3][wn * 4 + j] = v.w;
+            }
+    } else {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+            for (int wn = 0; wn < WNITER; ++wn) {
+                const float4 v = lds128(b_base + ((4 * g + kk) * Cfg::BN + wn * 16) * 4);
+                f.b[kk][wn * 4 + 0] = v.x;
+                f.b[kk][wn * 4 + 1] = v.y;
+                f.b[kk][wn * 4 + 2] = v.z;
+                f.b[kk][wn * 4 + 3] = v.w;
+            }
+    }
+}
+
+template <class Cfg>
+__device__ __forceinline__ void fma_frag(float (&acc)[Cfg::TM][Cfg::TN], const Frag<Cfg> &f)
+{
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+        for (int i = 0; i < Cfg::TM; ++i)
+#pragma unroll
+            for (int j = 0; j < Cfg::TN; ++j) acc[i][j] = fmaf(f.a[kk][i], f.b[kk][j], acc[i][j]);
+}
+
+// One consumer warp: WM x WN outputs of the CTA tile; each lane holds
+// TM x TN accumulators as (WM/32) x (WN/16) sub-blocks of 4 x 4.
+//
+// Addressing is resolved once into per-lane base addresses so that every
+// shared load is "base + immediate".  For a K-inner (swizzled) operand the
+// lane's rows are `base + 8*i` (A) or `base + 4*j` (B) with base = lane row
+// (A) or lane column (B), so the row modulo 8 -- the swizzle key -- is lr for
+// A and lc + 4*(j odd) for B, and the 16-byte chunk of k-group g sits at
+// (g ^ key) * 16: one XOR per k-group.
+//
+// The k loop is software-pipelined over k-groups: the fragments of the next
+// k-group (or of the next stage's first k-group) are loaded into the second
+// register set while the current one feeds the FFMAs.  A stage is released
+// after the FFMAs of its last k-group, i.e. once every value read from it has
+// been consumed.
+template <class Cfg, bool A_KIN, bool B_KIN, class Issuer>
 __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem, uint64_t *full,
-                                              uint64_t *empty, const Abort &ab, int cw, int lane)
+                                              uint64_t *empty, const Abort &ab, int cw, int lane,
+                                              Issuer &iss)
 {
     constexpr int WMITER = Cfg::WMITER, WNITER = Cfg::WNITER, TM = Cfg::TM, TN = Cfg::TN;
+    constexpr int BM = Cfg::BM, BN = Cfg::BN;
+    constexpr int GROUPS = kBK / 4;
     const int wm0 = (cw / Cfg::WARPS_N) * Cfg::WM;
     const int wn0 = (cw % Cfg::WARPS_N) * Cfg::WN;
     const int lr = lane >> 2, lc = lane & 3;
@@ -227,7 +443,20 @@ __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem
         return wn0 + wn * 16 + (B_KIN ? j * 4 + lc : lc * 4 + j);
     };
 
-    long long it = 0;
+    const uint32_t smem0 = smem_u32(smem);
+    // Lane-relative byte offsets inside a stage (runtime part only).
+    const uint32_t a_lane = A_KIN ? (wm0 + lr) * 128 : (wm0 + lr * 4) * 4;
+    const uint32_t b_lane = Cfg::A_BYTES + (B_KIN ? (wn0 + lc) * 128 : (wn0 + lc * 4) * 4);
+    const uint32_t a_key = static_cast<uint32_t>(lr) << 4;
+    const uint32_t b_key = static_cast<uint32_t>(lc) << 4;
+    auto stage_addr = [&](int s) { return smem0 + static_cast<uint32_t>(s) * Cfg::STAGE_BYTES; };
+    auto wait_full = [&](int s, uint32_t ph) {
+        return warp_wait(&full[s], ph, ab, kStatusWaitFull, lane);
+    };
+    int cs = 0;         // stage of the current k-block
+    uint32_t cph = 0;   // its round parity
+
+    long long it = 0;  // k-blocks consumed so far by this CTA
     for (long long t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
         const TileCoord tc = tile_coord(t, p);
         float acc[TM][TN];
@@ -236,79 +465,67 @@ __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem
 #pragma unroll
             for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
-        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
-            const int s = static_cast<int>(it % Cfg::STAGES);
-            const uint32_t ph = static_cast<uint32_t>((it / Cfg::STAGES) & 1);
-            if (!warp_wait(&full[s], ph, ab, kStatusWaitFull, lane)) return;
-            const uint8_t *sa = smem + s * Cfg::STAGE_BYTES;
-            const uint8_t *sb = sa + Cfg::A_BYTES;
-#pragma unroll 2
-            for (int g = 0; g < kBK / 4; ++g) {
-                float a[4][TM], b[4][TN];
-                if (A_KIN) {
-#pragma unroll
-                    for (int wm = 0; wm < WMITER; ++wm)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float4 v = *reinterpret_cast<const float4 *>(
-                                sa + sw128_offset(row_of(wm, i), 4 * g));
-                            a[0][wm * 4 + i] = v.x;
-                            a[1][wm * 4 + i] = v.y;
-                            a[2][wm * 4 + i] = v.z;
-                            a[3][wm * 4 + i] = v.w;
+        if (kPipelined) {
+            Frag<Cfg> f[2];
+            if (!wait_full(cs, cph)) return;
+            uint32_t stage = stage_addr(cs);
+            load_frag<Cfg, A_KIN, B_KIN>(f[0], stage + a_lane, stage + b_lane, a_key, b_key, 0);
+
+            for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+    #pragma unroll 1
+                for (int gp = 0; gp < GROUPS / 2; ++gp) {
+                    // even k-group 2*gp: compute f[0], prefetch 2*gp+1 into f[1]
+                    load_frag<Cfg, A_KIN, B_KIN>(f[1], stage + a_lane, stage + b_lane, a_key, b_key,
+                                                 2 * gp + 1);
+                    fma_frag<Cfg>(acc, f[0]);
+                    // odd k-group 2*gp+1: compute f[1], prefetch the next group into f[0]
+                    if (gp + 1 < GROUPS / 2) {
+                        load_frag<Cfg, A_KIN, B_KIN>(f[0], stage + a_lane, stage + b_lane, a_key,
+                                                     b_key, 2 * gp + 2);
+                        fma_frag<Cfg>(acc, f[1]);
+                    } else {
+                        const bool more = kb + 1 < p.k_blocks;
+                        const int ns = (cs + 1 == Cfg::STAGES) ? 0 : cs + 1;
+                        const uint32_t nph = (cs + 1 == Cfg::STAGES) ? (cph ^ 1u) : cph;
+                        if (more) {
+                            if (!wait_full(ns, nph)) return;
+                            const uint32_t nstage = stage_addr(ns);
+                            load_frag<Cfg, A_KIN, B_KIN>(f[0], nstage + a_lane, nstage + b_lane,
+                                                         a_key, b_key, 0);
                         }
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                        for (int wm = 0; wm < WMITER; ++wm) {
-                            const float4 v = *reinterpret_cast<const float4 *>(
-                                sa + ((4 * g + kk) * Cfg::BM + row_of(wm, 0)) * 4);
-                            a[kk][wm * 4 + 0] = v.x;
-                            a[kk][wm * 4 + 1] = v.y;
-                            a[kk][wm * 4 + 2] = v.z;
-                            a[kk][wm * 4 + 3] = v.w;
-                        }
+                        fma_frag<Cfg>(acc, f[1]);
+                        // every value read from this stage has been consumed
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&empty[cs]);
+                        if (!iss.refill(it, ab, cw, lane)) return;
+                        cs = ns;
+                        cph = nph;
+                        stage = stage_addr(cs);
+                    }
                 }
-                if (B_KIN) {
-#pragma unroll
-                    for (int wn = 0; wn < WNITER; ++wn)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float4 v = *reinterpret_cast<const float4 *>(
-                                sb + sw128_offset(col_of(wn, j), 4 * g));
-                            b[0][wn * 4 + j] = v.x;
-                            b[1][wn * 4 + j] = v.y;
-                            b[2][wn * 4 + j] = v.z;
-                            b[3][wn * 4 + j] = v.w;
-                        }
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                        for (int wn = 0; wn < WNITER; ++wn) {
-                            const float4 v = *reinterpret_cast<const float4 *>(
-                                sb + ((4 * g + kk) * Cfg::BN + col_of(wn, 0)) * 4);
-                            b[kk][wn * 4 + 0] = v.x;
-                            b[kk][wn * 4 + 1] = v.y;
-                            b[kk][wn * 4 + 2] = v.z;
-                            b[kk][wn * 4 + 3] = v.w;
-                        }
-                }
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                    for (int i = 0; i < TM; ++i)
-#pragma unroll
-                        for (int j = 0; j < TN; ++j)
-                            acc[i][j] = fmaf(a[kk][i], b[kk][j], acc[i][j]);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
+        } else {
+            for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+                if (!wait_full(cs, cph)) return;
+                const uint32_t stage = stage_addr(cs);
+#pragma unroll kGroupUnroll
+                for (int g = 0; g < GROUPS; ++g) {
+                    Frag<Cfg> f;
+                    load_frag<Cfg, A_KIN, B_KIN>(f, stage + a_lane, stage + b_lane, a_key, b_key, g);
+                    fma_frag<Cfg>(acc, f);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[cs]);
+                if (!iss.refill(it, ab, cw, lane)) return;
+                if (++cs == Cfg::STAGES) {
+                    cs = 0;
+                    cph ^= 1u;
+                }
+            }
         }
 
         // ---- epilogue: C = alpha * acc + beta * C, masked at the M/N edges
-        const int mt = tc.tm * Cfg::BM, nt = tc.tn * Cfg::BN;
+        const int mt = tc.tm * BM, nt = tc.tn * BN;
         float *Cq = p.C + tc.q * p.sC;
         const bool use_beta = p.beta != 0.f;
 #pragma unroll
@@ -368,7 +585,7 @@ __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem
 // ---------------------------------------------------------------- kernel
 
 template <class Cfg, bool A_KIN, bool B_KIN, bool USE_TMA, bool EVEN_K>
-__global__ void __launch_bounds__(Cfg::THREADS, 1)
+__global__ void __launch_bounds__(Cfg::THREADS, kMinBlocks)
     simt_sgemm_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const GemmParams p)
 {
@@ -378,11 +595,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
     uint64_t *empty = full + Cfg::STAGES;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + Cfg::STAGES);
+    using Issuer = typename std::conditional<USE_TMA, TmaIssuer<Cfg, A_KIN, B_KIN>,
+                                             CpAsyncIssuer<Cfg, A_KIN, B_KIN, EVEN_K>>::type;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
-            mbar_init(&full[s], USE_TMA ? 1u : 32u);
+            mbar_init(&full[s], Issuer::kFullCount);
             mbar_init(&empty[s], Cfg::CONSUMER_WARPS);
         }
         *abort_flag = 0;
@@ -391,16 +610,24 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     __syncthreads();
     const Abort ab{abort_flag, p.status, p.wait_limit};
 
-    if (warp == Cfg::CONSUMER_WARPS) {
-        if (USE_TMA) {
-            if (lane == 0) simt_tma_producer<Cfg, A_KIN, B_KIN>(&tmA, &tmB, p, smem, full, empty, ab);
-        } else {
-            simt_cpasync_producer<Cfg, A_KIN, B_KIN, EVEN_K>(p, smem, full, empty, ab, lane);
-        }
-    } else {
-        simt_consumer<Cfg, A_KIN, B_KIN>(p, smem, full, empty, ab, warp, lane);
+    // k-blocks this CTA consumes: its tiles are blockIdx.x + i*gridDim.x
+    const long long my_tiles =
+        (p.num_tiles - blockIdx.x + gridDim.x - 1) / static_cast<long long>(gridDim.x);
+    Issuer iss;
+    if constexpr (USE_TMA) {
+        iss.tmA = &tmA;
+        iss.tmB = &tmB;
     }
+    iss.p = &p;
+    iss.smem = smem;
+    iss.full = full;
+    iss.empty = empty;
+    iss.total = my_tiles * p.k_blocks;
+    iss.prologue(warp, lane, ab);
     __syncwarp();
+    simt_consumer<Cfg, A_KIN, B_KIN>(p, smem, full, empty, ab, warp, lane, iss);
+    __syncwarp();
+    if (*abort_flag) iss.drain(ab.limit, warp, lane);
     __syncthreads();
 }
 
