@@ -57,32 +57,6 @@ struct SimtCfg {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
-// Bounded wait that ignores the abort flag: used to let copies already in
-// flight land before the CTA exits after an abort.
-__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, long long limit)
-{
-    long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > limit) return;
-    }
-}
-
-// Warp-wide bounded wait: lane 0 spins (bounded), the verdict is broadcast,
-// then every lane observes the completed phase itself (which returns at once)
-// so that each lane acquires the stage's contents.  Keeps the warp converged
-// whatever the outcome.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const Abort &ab,
-                                          unsigned int code, int lane)
-{
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait(bar, parity, ab, code) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) mbar_drain(bar, parity, ab.limit);
-    return ok != 0;
-}
-
-// ------------------------------------------------------------ producers
-
 // Who fills the stages.  The CTA's k-blocks are numbered j = 0, 1, ... over
 // all of its tiles in order; k-block j lives in stage j % STAGES.  All stages
 // are filled up front; after the warps have consumed k-block `it`, the stage
@@ -205,60 +179,6 @@ struct TmaIssuer {
                        limit);
     }
 };
-
-// One operand tile by cp.async, spread over `nthr` threads.  KIN: tile rows
-// are ROWS (M or N) rows of 32 k-values, swizzled; otherwise the tile is
-// [32 k][ROWS] unswizzled.  Global element (r, k) of a K-inner operand is at
-// base[r*ld + k]; of an M/N-inner operand at base[k*ld + r].  Out-of-range
-// elements are zero-filled (source size 0), never read.
-template <int ROWS, bool KIN, bool EVEN_K>
-__device__ __forceinline__ void cp_async_tile(uint8_t *dst, const float *base, long long ld,
-                                              int r0, int rlim, int k0, int K, bool vec4, int tid,
-                                              int nthr)
-{
-    const uint32_t d0 = smem_u32(dst);
-    if (vec4) {
-        if (KIN) {
-            constexpr int UNITS = ROWS * (kBK / 4);
-            for (int u = tid; u < UNITS; u += nthr) {
-                const int r = u >> 3, c = u & 7;
-                const int gr = r0 + r, gk = k0 + 4 * c;
-                int nval = (gr < rlim) ? (EVEN_K ? 4 : min(4, K - gk)) : 0;
-                nval = max(nval, 0);
-                const float *src = nval ? base + gr * ld + gk : base;
-                cp_async_16(d0 + sw128_offset(r, 4 * c), src, nval * 4);
-            }
-        } else {
-            constexpr int UNITS = kBK * (ROWS / 4);
-            for (int u = tid; u < UNITS; u += nthr) {
-                const int k = u / (ROWS / 4), c = u % (ROWS / 4);
-                const int gk = k0 + k, gr = r0 + 4 * c;
-                int nval = (EVEN_K || gk < K) ? min(4, rlim - gr) : 0;
-                nval = max(nval, 0);
-                const float *src = nval ? base + gk * ld + gr : base;
-                cp_async_16(d0 + (k * ROWS + 4 * c) * 4, src, nval * 4);
-            }
-        }
-    } else {
-        if (KIN) {
-            constexpr int UNITS = ROWS * kBK;
-            for (int u = tid; u < UNITS; u += nthr) {
-                const int r = u >> 5, k = u & 31;
-                const int gr = r0 + r, gk = k0 + k;
-                const bool v = gr < rlim && (EVEN_K || gk < K);
-                cp_async_4(d0 + sw128_offset(r, k), v ? base + gr * ld + gk : base, v ? 4 : 0);
-            }
-        } else {
-            constexpr int UNITS = kBK * ROWS;
-            for (int u = tid; u < UNITS; u += nthr) {
-                const int k = u / ROWS, r = u % ROWS;
-                const int gk = k0 + k, gr = r0 + r;
-                const bool v = gr < rlim && (EVEN_K || gk < K);
-                cp_async_4(d0 + (k * ROWS + r) * 4, v ? base + gk * ld + gr : base, v ? 4 : 0);
-            }
-        }
-    }
-}
 
 // cp.async: every thread copies its share of the stage (operands TMA cannot
 // describe: unaligned bases, row pitches or batch strides that are not

@@ -1,0 +1,547 @@
+// tc_tf32.cuh -- the tcgen05 tensor-core SGEMM kernel (3xTF32 and TF32).
+//
+// C = alpha * op(A) @ op(B) + beta * C with fp32 inputs and output, the
+// contraction on the 5th-generation tensor cores ("Tensor cores" in the
+// future-work list of "From 1% to 94% of cuBLAS, one kernel at a time": TF32
+// inputs raise peak throughput and turn the problem back into a
+// data-movement one).  Accumulators live in tensor memory (TMEM), as the
+// "TMEM-friendly block sizes" item of "Triton Optimization Reference (cuTile
+// -> Triton)", section 9.4, describes for Blackwell.
+//
+// FP32 accuracy from TF32 units (3xTF32): every operand value x is split
+// into hi = tf32(x) (round to nearest, ties away) and lo = tf32(x - hi); the
+// product a*b is accumulated in fp32 as lo_a*hi_b + hi_a*lo_b + hi_a*hi_b,
+// small terms first.  The dropped lo_a*lo_b and the rounding of lo are each
+// below 2^-22 |a||b|.  Plain TF32 issues hi_a*hi_b only.
+//
+// Structure (one CTA per SM, persistent over 128 x BN output tiles):
+//   warp 0      TMA producer: raw fp32 tiles of A and B into a RAW_STAGES
+//               ring (or masked cp.async for operands TMA cannot describe)
+//   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=BN, K=8)
+//               from the split ring into a double-buffered TMEM accumulator
+//   warps 2-5   converters: raw tile -> hi (and lo) planes, K-major with the
+//               128-byte swizzle; M/N-inner tiles are transposed on the way
+//   warps 6-9   epilogue: tcgen05.ld of one accumulator buffer (the TMEM
+//               lane quarter of warp w is w % 4) while the MMA fills the
+//               other; C = alpha*acc + beta*C, masked at the edges
+// Every mbarrier wait is bounded; on a timeout the CTA stops, lets copies and
+// MMAs already issued finish, frees TMEM and exits.
+#pragma once
+
+#include <type_traits>
+
+#include "common.cuh"
+
+namespace sg {
+namespace tc {
+
+constexpr int BM = 128;   // UMMA M (one CTA)
+constexpr int BK = 32;    // k per stage: one 128-byte swizzle row of fp32
+constexpr int UK = 8;     // k per tcgen05.mma of kind::tf32
+constexpr int kThreads = 320;
+constexpr int kConvThreads = 128;
+constexpr int kConvWarp0 = 2, kEpiWarp0 = 6;
+
+template <int BN_, bool SPLIT3_, bool A_KIN_, bool B_KIN_, bool USE_TMA_>
+struct Cfg {
+    static constexpr int BN = BN_;
+    static constexpr bool SPLIT3 = SPLIT3_, A_KIN = A_KIN_, B_KIN = B_KIN_, USE_TMA = USE_TMA_;
+    static constexpr int A_BYTES = BM * BK * 4;          // one 128 x 32 fp32 tile
+    static constexpr int B_BYTES = BN * BK * 4;
+    static constexpr int RAW_BYTES = A_BYTES + B_BYTES;
+    static constexpr int PLANES = SPLIT3 ? 2 : 1;        // hi (+ lo)
+    static constexpr int SPLIT_BYTES = PLANES * RAW_BYTES;
+    static constexpr int RAW_STAGES = 2;
+    static constexpr int SPLIT_STAGES = SPLIT3 ? 2 : 3;
+    static constexpr int TMEM_COLS = 2 * BN;             // two accumulator buffers
+    static constexpr int NBAR = 2 * RAW_STAGES + 2 * SPLIT_STAGES + 4 + 1;
+    static constexpr int SMEM_BYTES =
+        RAW_STAGES * RAW_BYTES + SPLIT_STAGES * SPLIT_BYTES + NBAR * 8 + 16 + 1024;
+    static_assert(BN == 128 || BN == 256, "UMMA N");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+    // split stage layout: A_hi | B_hi | A_lo | B_lo
+    static constexpr int OFF_AHI = 0, OFF_BHI = A_BYTES;
+    static constexpr int OFF_ALO = RAW_BYTES, OFF_BLO = RAW_BYTES + A_BYTES;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory writes by threads become visible to the tensor core (async
+// proxy) only after this fence.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::tf32, one CTA.
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The mbarrier receives one arrival when every tcgen05 operation this
+// thread issued before the commit has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one per lane).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+        "[%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Round to the nearest TF32 value (10 explicit mantissa bits), ties away.
+__device__ __forceinline__ float to_tf32(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile stored as
+// 128-byte rows (32 fp32 of K) with the 128-byte swizzle: 8-row atoms of
+// 1024 bytes stacked along M/N (stride byte offset 1024).  The leading byte
+// offset is unused for this layout (K of one MMA stays inside one row).
+__device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t smem_addr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);  // start address
+    d |= static_cast<uint64_t>(1) << 16;                        // leading byte offset (16 B)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;                // stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;                        // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                        // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: kind::tf32, fp32 accumulate, both operands K-major,
+// M = 128, N = BN.
+template <int BN>
+__host__ __device__ constexpr uint32_t idesc_tf32()
+{
+    return (1u << 4)                  // D format: f32
+           | (2u << 7)                // A format: tf32
+           | (2u << 10)               // B format: tf32
+           | (static_cast<uint32_t>(BN >> 3) << 17)   // N / 8
+           | (static_cast<uint32_t>(BM >> 4) << 24);  // M / 16
+}
+
+// ------------------------------------------------------------ the kernel
+
+template <class C>
+struct Smem {
+    uint8_t *raw;      // RAW_STAGES x (A tile | B tile)
+    uint8_t *split;    // SPLIT_STAGES x (A_hi | B_hi | A_lo | B_lo)
+    uint64_t *raw_full, *raw_empty, *split_full, *split_empty, *acc_full, *acc_empty, *mma_done;
+    uint32_t *tmem_base;
+    volatile int *abort_flag;
+};
+
+// Ring position walker: stage index and round parity, advanced per use.
+template <int N>
+struct Ring {
+    int s = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void next()
+    {
+        if (++s == N) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
+// Converts one raw tile (R rows of the operand, BK k) into K-major swizzled
+// hi (and lo) planes.  K-inner raw tiles already have that layout (TMA wrote
+// them with the same swizzle): the split is element-wise.  M/N-inner raw
+// tiles ([BK][R], unswizzled) are transposed in 4 x 4 blocks; the block
+// assignment (k-block rotated by lane/2) keeps each quarter-warp's 16-byte
+// stores on eight distinct bank groups.
+template <int R, bool KIN, bool SPLIT3>
+__device__ __forceinline__ void convert_tile(const uint8_t *raw, uint8_t *hi, uint8_t *lo, int ct)
+{
+    const uint32_t raw_a = smem_u32(raw), hi_a = smem_u32(hi), lo_a = smem_u32(lo);
+    if (KIN) {
+        constexpr int CHUNKS = R * BK / 4;  // 16-byte chunks
+#pragma unroll 4
+        for (int c = ct; c < CHUNKS; c += kConvThreads) {
+            float4 x;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                         : "r"(raw_a + c * 16));
+            float4 h, l;
+            h.x = to_tf32(x.x); h.y = to_tf32(x.y); h.z = to_tf32(x.z); h.w = to_tf32(x.w);
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(hi_a + c * 16),
+                         "f"(h.x), "f"(h.y), "f"(h.z), "f"(h.w)
+                         : "memory");
+            if (SPLIT3) {
+                l.x = to_tf32(x.x - h.x); l.y = to_tf32(x.y - h.y);
+                l.z = to_tf32(x.z - h.z); l.w = to_tf32(x.w - h.w);
+                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(lo_a + c * 16),
+                             "f"(l.x), "f"(l.y), "f"(l.z), "f"(l.w)
+                             : "memory");
+            }
+        }
+    } else {
+        // raw: element (k, r) at (k*R + r)*4.  out: element (r, k) at sw128_offset(r, k).
+        const int warp = ct >> 5, lane = ct & 31;
+        constexpr int RB4 = R / 4;                // 4-row blocks along R
+        constexpr int PASSES = RB4 / 32;          // lanes cover 32 row blocks per pass
+#pragma unroll
+        for (int pass = 0; pass < PASSES; ++pass) {
+            const int rb4 = pass * 32 + lane;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                // the 4 warps x 2 halves cover the 8 k-blocks of 4 for every rb4
+                const int kb4 = (warp * 2 + half + (lane >> 1)) & 7;
+                float v[4][4];  // v[kk][i] = raw(k = 4kb4+kk, r = 4rb4+i)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t a = raw_a + ((4 * kb4 + kk) * R + 4 * rb4) * 4;
+                    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                 : "=f"(v[kk][0]), "=f"(v[kk][1]), "=f"(v[kk][2]), "=f"(v[kk][3])
+                                 : "r"(a));
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = 4 * rb4 + i;
+                    const uint32_t off = sw128_offset(r, 4 * kb4);
+                    float h[4], l[4];
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        h[kk] = to_tf32(v[kk][i]);
+                        l[kk] = to_tf32(v[kk][i] - h[kk]);
+                    }
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(hi_a + off),
+                                 "f"(h[0]), "f"(h[1]), "f"(h[2]), "f"(h[3])
+                                 : "memory");
+                    if (SPLIT3)
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(lo_a + off),
+                                     "f"(l[0]), "f"(l[1]), "f"(l[2]), "f"(l[3])
+                                     : "memory");
+                }
+            }
+        }
+    }
+}
+
+template <class C>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_sgemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const GemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Smem<C> sm;
+    sm.raw = base;
+    sm.split = base + C::RAW_STAGES * C::RAW_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm.split + C::SPLIT_STAGES * C::SPLIT_BYTES);
+    sm.raw_full = bars;
+    sm.raw_empty = sm.raw_full + C::RAW_STAGES;
+    sm.split_full = sm.raw_empty + C::RAW_STAGES;
+    sm.split_empty = sm.split_full + C::SPLIT_STAGES;
+    sm.acc_full = sm.split_empty + C::SPLIT_STAGES;
+    sm.acc_empty = sm.acc_full + 2;
+    sm.mma_done = sm.acc_empty + 2;
+    sm.tmem_base = reinterpret_cast<uint32_t *>(sm.mma_done + 1);
+    sm.abort_flag = reinterpret_cast<volatile int *>(sm.tmem_base + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::RAW_STAGES; ++s) {
+            mbar_init(&sm.raw_full[s], C::USE_TMA ? 1u : 32u);
+            mbar_init(&sm.raw_empty[s], kConvThreads / 32);
+        }
+        for (int s = 0; s < C::SPLIT_STAGES; ++s) {
+            mbar_init(&sm.split_full[s], kConvThreads / 32);
+            mbar_init(&sm.split_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.acc_full[b], 1);
+            mbar_init(&sm.acc_empty[b], 4);
+        }
+        mbar_init(sm.mma_done, 1);
+        *sm.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(sm.tmem_base, C::TMEM_COLS);
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *sm.tmem_base;
+    const Abort ab{sm.abort_flag, p.status, p.wait_limit};
+    const int k_blocks = p.k_blocks;
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer
+        Ring<C::RAW_STAGES> rr;
+        long long issued = 0;
+        bool ok = true;
+        if (C::USE_TMA && lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+        }
+        for (long long t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            const TileCoord tc = tile_coord(t, p);
+            const int m0 = tc.tm * BM, n0 = tc.tn * C::BN;
+            for (int kb = 0; kb < k_blocks; ++kb) {
+                uint8_t *sa = sm.raw + rr.s * C::RAW_BYTES;
+                uint8_t *sb = sa + C::A_BYTES;
+                const int k0 = kb * BK;
+                if (C::USE_TMA) {
+                    if (lane == 0) {
+                        if (!mbar_wait(&sm.raw_empty[rr.s], rr.ph ^ 1u, ab, kStatusWaitEmpty)) {
+                            ok = false;
+                        } else {
+                            const int qa = tc.q * p.a_q_step, qb = tc.q * p.b_q_step;
+                            mbar_arrive_expect_tx(&sm.raw_full[rr.s], C::RAW_BYTES);
+                            if (C::A_KIN) tma_load_3d(sa, &tmA, &sm.raw_full[rr.s], k0, m0, qa);
+                            else          tma_load_3d(sa, &tmA, &sm.raw_full[rr.s], m0, k0, qa);
+                            if (C::B_KIN) tma_load_3d(sb, &tmB, &sm.raw_full[rr.s], k0, n0, qb);
+                            else          tma_load_3d(sb, &tmB, &sm.raw_full[rr.s], n0, k0, qb);
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                } else {
+                    int w = 1;
+                    if (lane == 0)
+                        w = mbar_wait(&sm.raw_empty[rr.s], rr.ph ^ 1u, ab, kStatusWaitEmpty) ? 1 : 0;
+                    ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+                    if (ok) {
+                        cp_async_tile<BM, C::A_KIN, false>(sa, p.A + tc.q * p.sA, p.lda, m0, p.M,
+                                                           k0, p.K, p.a_vec4 != 0, lane, 32);
+                        cp_async_tile<C::BN, C::B_KIN, false>(sb, p.B + tc.q * p.sB, p.ldb, n0,
+                                                              p.N, k0, p.K, p.b_vec4 != 0, lane, 32);
+                        cp_async_arrive_noinc(&sm.raw_full[rr.s]);
+                    }
+                }
+                if (!ok) break;
+                ++issued;
+                rr.next();
+            }
+        }
+        if (!ok) {
+            if (C::USE_TMA) {
+                if (lane == 0) {
+                    // the stages issued last may still be landing
+                    Ring<C::RAW_STAGES> d;
+                    for (long long j = 0; j < issued; ++j) {
+                        if (j + C::RAW_STAGES >= issued)
+                            mbar_drain(&sm.raw_full[d.s], d.ph, ab.limit);
+                        d.next();
+                    }
+                }
+            } else {
+                asm volatile("cp.async.wait_all;" ::: "memory");
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            Ring<C::SPLIT_STAGES> sr;
+            Ring<2> acc;
+            constexpr uint32_t idesc = idesc_tf32<C::BN>();
+            bool ok = true;
+            bool any = false;
+            for (long long t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                if (!mbar_wait(&sm.acc_empty[acc.s], acc.ph ^ 1u, ab, kStatusWaitAcc)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc.s * C::BN);
+                for (int kb = 0; kb < k_blocks; ++kb) {
+                    if (!mbar_wait(&sm.split_full[sr.s], sr.ph, ab, kStatusWaitConv)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = smem_u32(sm.split + sr.s * C::SPLIT_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / UK; ++kk) {
+                        const uint32_t koff = kk * UK * 4;  // bytes along the 128-byte row
+                        const uint64_t a_hi = kmajor_sw128_desc(st + C::OFF_AHI + koff);
+                        const uint64_t b_hi = kmajor_sw128_desc(st + C::OFF_BHI + koff);
+                        const uint32_t acc_in = (kb > 0 || kk > 0) ? 1u : 0u;
+                        if (C::SPLIT3) {
+                            const uint64_t a_lo = kmajor_sw128_desc(st + C::OFF_ALO + koff);
+                            const uint64_t b_lo = kmajor_sw128_desc(st + C::OFF_BLO + koff);
+                            umma_tf32(d_tmem, a_lo, b_hi, idesc, acc_in);
+                            umma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
+                            umma_tf32(d_tmem, a_hi, b_hi, idesc, 1u);
+                        } else {
+                            umma_tf32(d_tmem, a_hi, b_hi, idesc, acc_in);
+                        }
+                    }
+                    any = true;
+                    umma_commit(&sm.split_empty[sr.s]);  // frees the split stage
+                    sr.next();
+                }
+                if (!ok) break;
+                umma_commit(&sm.acc_full[acc.s]);  // accumulator ready for the epilogue
+                acc.next();
+            }
+            // wait until every MMA issued has completed (TMEM is freed next)
+            if (any) {
+                umma_commit(sm.mma_done);
+                mbar_drain(sm.mma_done, 0, ab.limit);
+            }
+        }
+        __syncwarp();
+    } else if (warp < kEpiWarp0) {
+        // ------------------------------------------------ converters
+        const int ct = threadIdx.x - kConvWarp0 * 32;
+        Ring<C::RAW_STAGES> rr;
+        Ring<C::SPLIT_STAGES> sr;
+        bool ok = true;
+        for (long long t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (int kb = 0; kb < k_blocks; ++kb) {
+                int w = 1;
+                if (lane == 0) {
+                    w = mbar_wait(&sm.raw_full[rr.s], rr.ph, ab, kStatusWaitFull) &&
+                        mbar_wait(&sm.split_empty[sr.s], sr.ph ^ 1u, ab, kStatusWaitMma);
+                }
+                if (!__shfl_sync(0xffffffffu, w, 0)) {
+                    ok = false;
+                    break;
+                }
+                // every lane acquires both phases (they completed: returns at once)
+                mbar_drain(&sm.raw_full[rr.s], rr.ph, ab.limit);
+                mbar_drain(&sm.split_empty[sr.s], sr.ph ^ 1u, ab.limit);
+                const uint8_t *sa = sm.raw + rr.s * C::RAW_BYTES;
+                const uint8_t *sb = sa + C::A_BYTES;
+                uint8_t *st = sm.split + sr.s * C::SPLIT_BYTES;
+                convert_tile<BM, C::A_KIN, C::SPLIT3>(sa, st + C::OFF_AHI, st + C::OFF_ALO, ct);
+                convert_tile<C::BN, C::B_KIN, C::SPLIT3>(sb, st + C::OFF_BHI, st + C::OFF_BLO, ct);
+                fence_proxy_async_smem();  // our stores -> visible to the tensor core
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&sm.raw_empty[rr.s]);
+                    mbar_arrive(&sm.split_full[sr.s]);
+                }
+                rr.next();
+                sr.next();
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;            // TMEM lane quarter this warp may access
+        const int row_in_tile = q * 32 + lane;
+        Ring<2> acc;
+        const bool use_beta = p.beta != 0.f;
+        for (long long t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+            int w = 1;
+            if (lane == 0) w = mbar_wait(&sm.acc_full[acc.s], acc.ph, ab, kStatusWaitAcc);
+            if (!__shfl_sync(0xffffffffu, w, 0)) break;
+            mbar_drain(&sm.acc_full[acc.s], acc.ph, ab.limit);
+            tc_fence_after();
+            const TileCoord tc = tile_coord(t, p);
+            const int r = tc.tm * BM + row_in_tile;
+            const int n_tile = tc.tn * C::BN;
+            float *crow = p.C + tc.q * p.sC + static_cast<long long>(r) * p.ldc;
+            const uint32_t tbase =
+                tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc.s * C::BN);
+#pragma unroll 1
+            for (int c0 = 0; c0 < C::BN; c0 += 32) {
+                float v[32];
+                tmem_ld32(tbase + c0, v);  // all lanes take part, rows in range or not
+                if (r < p.M) {
+                    const int n0 = n_tile + c0;
+                    if (p.c_vec4 && n0 + 32 <= p.N) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            float4 o = make_float4(p.alpha * v[j], p.alpha * v[j + 1],
+                                                   p.alpha * v[j + 2], p.alpha * v[j + 3]);
+                            float4 *dst = reinterpret_cast<float4 *>(crow + n0 + j);
+                            if (use_beta) {
+                                const float4 old = *dst;
+                                o.x = fmaf(p.beta, old.x, o.x);
+                                o.y = fmaf(p.beta, old.y, o.y);
+                                o.z = fmaf(p.beta, old.z, o.z);
+                                o.w = fmaf(p.beta, old.w, o.w);
+                            }
+                            *dst = o;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int n = n0 + j;
+                            if (n < p.N) {
+                                float o = p.alpha * v[j];
+                                if (use_beta) o = fmaf(p.beta, crow[n], o);
+                                crow[n] = o;
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.acc_empty[acc.s]);
+            acc.next();
+        }
+    }
+
+    // ---- teardown: every role is done; free TMEM
+    tc_fence_before();
+    __syncwarp();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace tc
+}  // namespace sg
