@@ -113,7 +113,7 @@ def committed_traffic(kernel_key):
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while active."""
+    """nvidia-smi clock/throttle samples every 100 ms while active."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -128,7 +128,7 @@ class ClockSampler:
         fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
         os.close(fd)
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-               "-lms", "200"]
+               "-lms", "100"]
         if self.gpu_id:
             cmd += ["-i", self.gpu_id]
         try:
@@ -325,7 +325,7 @@ def resolve_mode(lib, requested):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--mode", default="auto", choices=["auto", "fp32", "3xtf32", "tf32"])

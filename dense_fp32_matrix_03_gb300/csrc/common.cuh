@@ -56,6 +56,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete yet is
+// suspended until it completes or about `hint_ns` nanoseconds pass, instead
+// of returning at once: a waiting warp then takes no issue slots and no
+// shared-memory bandwidth from the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                    uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Suspend hint of the bounded waits (the wait still ends as soon as the
+// phase completes).
+constexpr uint32_t kWaitSleepNs = 200000;
+
 // Per-CTA abort state kept in shared memory.  A wait that runs out of
 // iterations records why in the device status word, raises the CTA's abort
 // flag so that every other role stops waiting too, and reports failure.
@@ -67,14 +89,17 @@ struct Abort {
 
 // Waits until the phase with the given parity of `bar` has completed.
 // Returns false (and aborts the CTA) if the wait exceeds ab.limit cycles or
-// another role of the CTA has aborted.
+// another role of the CTA has aborted.  Critical-path waits poll; `sleep`
+// waits, for roles that wait long off the critical path, suspend between
+// polls so that they take no issue slots from the warps doing the work.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const Abort &ab,
-                                          unsigned int code)
+                                          unsigned int code, bool sleep = false)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    long long t0 = clock64();
+    const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (sleep ? mbar_try_wait_sleep(bar, parity, kWaitSleepNs) : mbar_try_wait(bar, parity))
+            return true;
         if (*ab.flag) return false;
         if (clock64() - t0 > ab.limit) {
             atomicOr(ab.status, code);
@@ -94,18 +119,15 @@ __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, long 
     }
 }
 
-// Warp-wide bounded wait: lane 0 spins (bounded), the verdict is broadcast,
-// then every lane observes the completed phase itself (which returns at once)
-// so that each lane acquires the stage's contents.  Keeps the warp converged
-// whatever the outcome.
+// Warp-wide bounded wait: every lane polls the barrier (and so acquires the
+// stage's contents itself); the lanes then agree on the outcome, keeping the
+// warp converged whatever happens.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const Abort &ab,
                                           unsigned int code, int lane)
 {
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait(bar, parity, ab, code) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) mbar_drain(bar, parity, ab.limit);
-    return ok != 0;
+    (void)lane;
+    const bool ok = mbar_wait(bar, parity, ab, code);
+    return __all_sync(0xffffffffu, ok) != 0;
 }
 
 // ------------------------------------------------------------ producers

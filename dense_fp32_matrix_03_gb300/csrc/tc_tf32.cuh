@@ -9,19 +9,22 @@
 // -> Triton)", section 9.4, describes for Blackwell.
 //
 // FP32 accuracy from TF32 units (3xTF32): every operand value x is split
-// into hi = tf32(x) (round to nearest, ties away) and lo = tf32(x - hi); the
-// product a*b is accumulated in fp32 as lo_a*hi_b + hi_a*lo_b + hi_a*hi_b,
-// small terms first.  The dropped lo_a*lo_b and the rounding of lo are each
-// below 2^-22 |a||b|.  Plain TF32 issues hi_a*hi_b only.
+// into hi = x with the 13 low mantissa bits cleared (a TF32 value) and
+// lo = (x - hi) likewise truncated (x - hi is exact in fp32); the product a*b
+// is accumulated in fp32 as lo_a*hi_b + hi_a*lo_b + hi_a*hi_b, small terms
+// first.  |lo| < 2^-10 |x|, so the dropped lo_a*lo_b and the truncation of
+// the two lo terms are each below 2^-20 |a||b|.  Plain TF32 issues
+// hi_a*hi_b only, with hi rounded to nearest (ties away) for accuracy
+// margin.
 //
 // Structure (one CTA per SM, persistent over 128 x BN output tiles):
 //   warp 0      TMA producer: raw fp32 tiles of A and B into a RAW_STAGES
 //               ring (or masked cp.async for operands TMA cannot describe)
 //   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=BN, K=8)
 //               from the split ring into a double-buffered TMEM accumulator
-//   warps 2-5   converters: raw tile -> hi (and lo) planes, K-major with the
+//   warps 2-9   converters: raw tile -> hi (and lo) planes, K-major with the
 //               128-byte swizzle; M/N-inner tiles are transposed on the way
-//   warps 6-9   epilogue: tcgen05.ld of one accumulator buffer (the TMEM
+//   warps 10-13 epilogue: tcgen05.ld of one accumulator buffer (the TMEM
 //               lane quarter of warp w is w % 4) while the MMA fills the
 //               other; C = alpha*acc + beta*C, masked at the edges
 // Every mbarrier wait is bounded; on a timeout the CTA stops, lets copies and
@@ -32,15 +35,25 @@
 
 #include "common.cuh"
 
+// Ring depths (raw fp32 tiles / split tf32 planes) per mode; overridable at
+// build time for tuning sweeps.
+#ifndef SG_TC_RAW3
+#define SG_TC_RAW3 3
+#define SG_TC_SPLIT3 2
+#define SG_TC_RAW1 4
+#define SG_TC_SPLIT1 3
+#endif
+
 namespace sg {
 namespace tc {
 
 constexpr int BM = 128;   // UMMA M (one CTA)
 constexpr int BK = 32;    // k per stage: one 128-byte swizzle row of fp32
 constexpr int UK = 8;     // k per tcgen05.mma of kind::tf32
-constexpr int kThreads = 320;
-constexpr int kConvThreads = 128;
-constexpr int kConvWarp0 = 2, kEpiWarp0 = 6;
+constexpr int kConvWarps = 8;
+constexpr int kConvThreads = kConvWarps * 32;
+constexpr int kConvWarp0 = 2, kEpiWarp0 = kConvWarp0 + kConvWarps;
+constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 
 template <int BN_, bool SPLIT3_, bool A_KIN_, bool B_KIN_, bool USE_TMA_>
 struct Cfg {
@@ -51,8 +64,8 @@ struct Cfg {
     static constexpr int RAW_BYTES = A_BYTES + B_BYTES;
     static constexpr int PLANES = SPLIT3 ? 2 : 1;        // hi (+ lo)
     static constexpr int SPLIT_BYTES = PLANES * RAW_BYTES;
-    static constexpr int RAW_STAGES = 2;
-    static constexpr int SPLIT_STAGES = SPLIT3 ? 2 : 3;
+    static constexpr int RAW_STAGES = SPLIT3 ? SG_TC_RAW3 : SG_TC_RAW1;
+    static constexpr int SPLIT_STAGES = SPLIT3 ? SG_TC_SPLIT3 : SG_TC_SPLIT1;
     static constexpr int TMEM_COLS = 2 * BN;             // two accumulator buffers
     static constexpr int NBAR = 2 * RAW_STAGES + 2 * SPLIT_STAGES + 4 + 1;
     static constexpr int SMEM_BYTES =
@@ -147,6 +160,26 @@ __device__ __forceinline__ float to_tf32(float x)
     return __uint_as_float(r);
 }
 
+// x with its 13 low mantissa bits cleared: a TF32 value.
+__device__ __forceinline__ float trunc_tf32(float x)
+{
+    return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+
+// The operand planes of one value: 3xTF32 -> (hi, lo) truncated split,
+// TF32 -> hi rounded to nearest.
+template <bool SPLIT3>
+__device__ __forceinline__ void split_value(float x, float &hi, float &lo)
+{
+    if (SPLIT3) {
+        hi = trunc_tf32(x);
+        lo = trunc_tf32(x - hi);  // x - hi is exact
+    } else {
+        hi = to_tf32(x);
+        lo = 0.f;
+    }
+}
+
 // Shared-memory matrix descriptor of a K-major operand tile stored as
 // 128-byte rows (32 fp32 of K) with the 128-byte swizzle: 8-row atoms of
 // 1024 bytes stacked along M/N (stride byte offset 1024).  The leading byte
@@ -218,13 +251,14 @@ __device__ __forceinline__ void convert_tile(const uint8_t *raw, uint8_t *hi, ui
                          : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
                          : "r"(raw_a + c * 16));
             float4 h, l;
-            h.x = to_tf32(x.x); h.y = to_tf32(x.y); h.z = to_tf32(x.z); h.w = to_tf32(x.w);
+            split_value<SPLIT3>(x.x, h.x, l.x);
+            split_value<SPLIT3>(x.y, h.y, l.y);
+            split_value<SPLIT3>(x.z, h.z, l.z);
+            split_value<SPLIT3>(x.w, h.w, l.w);
             asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(hi_a + c * 16),
                          "f"(h.x), "f"(h.y), "f"(h.z), "f"(h.w)
                          : "memory");
             if (SPLIT3) {
-                l.x = to_tf32(x.x - h.x); l.y = to_tf32(x.y - h.y);
-                l.z = to_tf32(x.z - h.z); l.w = to_tf32(x.w - h.w);
                 asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(lo_a + c * 16),
                              "f"(l.x), "f"(l.y), "f"(l.z), "f"(l.w)
                              : "memory");
@@ -235,13 +269,15 @@ __device__ __forceinline__ void convert_tile(const uint8_t *raw, uint8_t *hi, ui
         const int warp = ct >> 5, lane = ct & 31;
         constexpr int RB4 = R / 4;                // 4-row blocks along R
         constexpr int PASSES = RB4 / 32;          // lanes cover 32 row blocks per pass
+        constexpr int SHARE = 8 / kConvWarps;     // k-blocks of 4 per warp and row block
+        static_assert(8 % kConvWarps == 0, "converter warps must divide the 8 k-blocks");
 #pragma unroll
         for (int pass = 0; pass < PASSES; ++pass) {
             const int rb4 = pass * 32 + lane;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                // the 4 warps x 2 halves cover the 8 k-blocks of 4 for every rb4
-                const int kb4 = (warp * 2 + half + (lane >> 1)) & 7;
+            for (int half = 0; half < SHARE; ++half) {
+                // the warps x SHARE cover the 8 k-blocks of 4 for every rb4
+                const int kb4 = (warp * SHARE + half + (lane >> 1)) & 7;
                 float v[4][4];  // v[kk][i] = raw(k = 4kb4+kk, r = 4rb4+i)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
@@ -256,10 +292,7 @@ __device__ __forceinline__ void convert_tile(const uint8_t *raw, uint8_t *hi, ui
                     const uint32_t off = sw128_offset(r, 4 * kb4);
                     float h[4], l[4];
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        h[kk] = to_tf32(v[kk][i]);
-                        l[kk] = to_tf32(v[kk][i] - h[kk]);
-                    }
+                    for (int kk = 0; kk < 4; ++kk) split_value<SPLIT3>(v[kk][i], h[kk], l[kk]);
                     asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(hi_a + off),
                                  "f"(h[0]), "f"(h[1]), "f"(h[2]), "f"(h[3])
                                  : "memory");
@@ -299,10 +332,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::RAW_STAGES; ++s) {
             mbar_init(&sm.raw_full[s], C::USE_TMA ? 1u : 32u);
-            mbar_init(&sm.raw_empty[s], kConvThreads / 32);
+            mbar_init(&sm.raw_empty[s], kConvWarps);
         }
         for (int s = 0; s < C::SPLIT_STAGES; ++s) {
-            mbar_init(&sm.split_full[s], kConvThreads / 32);
+            mbar_init(&sm.split_full[s], kConvWarps);
             mbar_init(&sm.split_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -447,18 +480,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (long long t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
             for (int kb = 0; kb < k_blocks; ++kb) {
-                int w = 1;
-                if (lane == 0) {
-                    w = mbar_wait(&sm.raw_full[rr.s], rr.ph, ab, kStatusWaitFull) &&
-                        mbar_wait(&sm.split_empty[sr.s], sr.ph ^ 1u, ab, kStatusWaitMma);
-                }
-                if (!__shfl_sync(0xffffffffu, w, 0)) {
+                if (!warp_wait(&sm.raw_full[rr.s], rr.ph, ab, kStatusWaitFull, lane) ||
+                    !warp_wait(&sm.split_empty[sr.s], sr.ph ^ 1u, ab, kStatusWaitMma, lane)) {
                     ok = false;
                     break;
                 }
-                // every lane acquires both phases (they completed: returns at once)
-                mbar_drain(&sm.raw_full[rr.s], rr.ph, ab.limit);
-                mbar_drain(&sm.split_empty[sr.s], sr.ph ^ 1u, ab.limit);
                 const uint8_t *sa = sm.raw + rr.s * C::RAW_BYTES;
                 const uint8_t *sb = sa + C::A_BYTES;
                 uint8_t *st = sm.split + sr.s * C::SPLIT_BYTES;
@@ -482,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool use_beta = p.beta != 0.f;
         for (long long t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
             int w = 1;
-            if (lane == 0) w = mbar_wait(&sm.acc_full[acc.s], acc.ph, ab, kStatusWaitAcc);
+            if (lane == 0) w = mbar_wait(&sm.acc_full[acc.s], acc.ph, ab, kStatusWaitAcc, true);
             if (!__shfl_sync(0xffffffffu, w, 0)) break;
             mbar_drain(&sm.acc_full[acc.s], acc.ph, ab.limit);
             tc_fence_after();
