@@ -331,6 +331,9 @@ def main():
     ap.add_argument("--mode", default="auto", choices=["auto", "fp32", "3xtf32", "tf32"])
     ap.add_argument("--no-extra", action="store_true", help="skip per-path and BMM figures")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="instead of the benchmark line, print one JSON line per workload "
+                         "configuration and path (256^3, ragged, size sweep, batched)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -338,6 +341,8 @@ def main():
 
     if args.impl == "reference":
         return reference_arm(args, rank, world)
+    if args.all_configs:
+        return all_configs(args)
 
     import torch
     import dense_fp32_matrix_03_gb300 as lib
@@ -502,6 +507,55 @@ def extra_figures(lib, default_mode, dev, stream, flush, num_sms, peaks, peak_sr
         out["bmm"][f"transB={tB}"] = {"tflops": gemm_flops(M, N, K, Q) / (t / 1e3) / 1e12,
                                       "ms": t, "mode": default_mode}
     return out
+
+
+def all_configs(args):
+    """One JSON line per (workload, path): TFLOP/s and the roofline it is
+    bound by, min(peak, AI * HBM bandwidth) with AI over compulsory bytes."""
+    import numpy as np
+    import torch
+    import dense_fp32_matrix_03_gb300 as lib
+    import workloads
+    dev = torch.device("cuda", 0)
+    props = torch.cuda.get_device_properties(dev)
+    peaks, src = load_peaks()
+    bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])) / 1e3  # TB/s
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    cases = [("sgemm_256", 0), ("sgemm_ragged_1000x1500x777", 0),
+             ("sgemm_ragged_1000x1500x777", 1)]
+    cases += [(f"sweep_{n}", 0) for n in workloads.SWEEP_SIZES]
+    cases += [("bmm_q32_1024x1024x512", 0)]
+    for name, beta_idx in cases:
+        w = workloads.make(name)
+        M, N, K, Q = w["M"], w["N"], w["K"], w["Q"]
+        beta = w["betas"][beta_idx]
+        A = torch.from_numpy(w["A"]).to(dev)
+        Bn = torch.from_numpy(w["B"]).to(dev)
+        C = torch.from_numpy(w["C0"]).to(dev)
+        variants = [(0, Bn, N)]
+        if Q > 1:
+            Bt = torch.from_numpy(np.ascontiguousarray(np.swapaxes(w["B"], 1, 2))).to(dev)
+            variants = [(1, Bt, K), (0, Bn, N)]
+        flops = gemm_flops(M, N, K, Q)
+        ai = flops / compulsory_bytes(M, N, K, Q, beta != 0)
+        for tB, Bd, ldb in variants:
+            for mode in ("fp32", "3xtf32", "tf32"):
+                def call(mode=mode, Bd=Bd, ldb=ldb, tB=tB):
+                    lib.check(lib.sgemm_batched_ex(mode, M, N, K, w["alpha"], A, K, Bd, ldb, beta,
+                                                   C, N, 0, tB, M * K, K * N, M * N, Q, stream))
+                ms = statistics.median(time_calls(call, args.steps, args.warmup, stream, flush))
+                tf = flops / (ms / 1e3) / 1e12
+                bound, peak, _ = roofline_peak(mode, props.multi_processor_count, peaks, src)
+                roof = min(peak, ai * bw)
+                print(json.dumps({"workload": name, "beta": beta, "transB": tB, "mode": mode,
+                                  "ms": round(ms, 4), "tflops": round(tf, 2),
+                                  "roof_tflops": round(roof, 1),
+                                  "roof_bound": bound if roof == peak else "hbm",
+                                  "frac": round(tf / roof, 3)}), flush=True)
+    lib.check(lib.sgemm_poll_error(stream))
+    return 0
 
 
 if __name__ == "__main__":

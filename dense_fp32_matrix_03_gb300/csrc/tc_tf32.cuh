@@ -17,31 +17,40 @@
 // hi_a*hi_b only, with hi rounded to nearest (ties away) for accuracy
 // margin.
 //
-// Structure (one CTA per SM, persistent over 128 x BN output tiles):
-//   warp 0      TMA producer: raw fp32 tiles of A and B into a RAW_STAGES
-//               ring (or masked cp.async for operands TMA cannot describe)
-//   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=BN, K=8)
-//               from the split ring into a double-buffered TMEM accumulator
-//   warps 2-9   converters: raw tile -> hi (and lo) planes, K-major with the
-//               128-byte swizzle; M/N-inner tiles are transposed on the way
-//   warps 10-13 epilogue: tcgen05.ld of one accumulator buffer (the TMEM
-//               lane quarter of warp w is w % 4) while the MMA fills the
-//               other; C = alpha*acc + beta*C, masked at the edges
-// Every mbarrier wait is bounded; on a timeout the CTA stops, lets copies and
-// MMAs already issued finish, frees TMEM and exits.
+// Data flow per 128 x BN output tile and 32-wide k-block:
+//   TMA (or cp.async)  raw fp32 A and B tiles -> shared-memory raw ring
+//   A converters       raw A rows -> hi/lo planes in TMEM (tcgen05.st); the
+//                      MMA reads A from TMEM, so A's split planes never
+//                      touch shared memory
+//   B converters       raw B tile -> hi/lo planes in shared memory, K-major
+//                      with the 128-byte swizzle (N-inner tiles transposed)
+//   MMA (one thread)   tcgen05.mma kind::tf32, M=128, N=BN, K=8, A from
+//                      TMEM, B by shared-memory descriptor, into one of two
+//                      TMEM accumulator buffers
+//   epilogue           tcgen05.ld of the other buffer; C = alpha*acc + beta*C
+// Shared-memory traffic per k-block (3xTF32, BN=128) is thus 32 KB of TMA
+// writes, 32 KB of converter reads, 32 KB of B-plane writes and 48 KB of MMA
+// B reads, instead of 224 KB with both operands' planes in shared memory.
+//
+// Warps: 0 producer, 1 TMEM allocator + MMA issuer, 2-5 A converters (warp
+// w owns TMEM lanes 32*(w%4) .. +31, i.e. those rows of A), 6-9 B
+// converters, 10-13 epilogue (lane quarter w%4).  One CTA per SM, persistent
+// over tiles in grouped order.  Every mbarrier wait is bounded; on a timeout
+// the CTA stops, lets copies and MMAs already issued finish, frees TMEM and
+// exits.
 #pragma once
 
 #include <type_traits>
 
 #include "common.cuh"
 
-// Ring depths (raw fp32 tiles / split tf32 planes) per mode; overridable at
-// build time for tuning sweeps.
+// Ring depths (raw fp32 tiles / split stages) per mode; overridable at build
+// time for tuning sweeps.
 #ifndef SG_TC_RAW3
 #define SG_TC_RAW3 3
-#define SG_TC_SPLIT3 2
+#define SG_TC_SPLIT3 3
 #define SG_TC_RAW1 4
-#define SG_TC_SPLIT1 3
+#define SG_TC_SPLIT1 4
 #endif
 
 namespace sg {
@@ -50,10 +59,13 @@ namespace tc {
 constexpr int BM = 128;   // UMMA M (one CTA)
 constexpr int BK = 32;    // k per stage: one 128-byte swizzle row of fp32
 constexpr int UK = 8;     // k per tcgen05.mma of kind::tf32
-constexpr int kConvWarps = 8;
-constexpr int kConvThreads = kConvWarps * 32;
-constexpr int kConvWarp0 = 2, kEpiWarp0 = kConvWarp0 + kConvWarps;
+constexpr int kAConvWarp0 = 2;                   // warps 2-5: A -> TMEM
+constexpr int kBConvWarp0 = 6, kBConvWarps = 4;  // warps 6-9: B -> shared memory
+constexpr int kBConvThreads = kBConvWarps * 32;
+constexpr int kEpiWarp0 = kBConvWarp0 + kBConvWarps;  // warps 10-13: epilogue
 constexpr int kThreads = (kEpiWarp0 + 4) * 32;
+constexpr int kConvWarps = 4 + kBConvWarps;      // arrivals that complete a stage
+constexpr uint32_t kTmemCols = 512;
 
 template <int BN_, bool SPLIT3_, bool A_KIN_, bool B_KIN_, bool USE_TMA_>
 struct Cfg {
@@ -63,18 +75,21 @@ struct Cfg {
     static constexpr int B_BYTES = BN * BK * 4;
     static constexpr int RAW_BYTES = A_BYTES + B_BYTES;
     static constexpr int PLANES = SPLIT3 ? 2 : 1;        // hi (+ lo)
-    static constexpr int SPLIT_BYTES = PLANES * RAW_BYTES;
+    static constexpr int SPLIT_BYTES = PLANES * B_BYTES; // B planes in shared memory
     static constexpr int RAW_STAGES = SPLIT3 ? SG_TC_RAW3 : SG_TC_RAW1;
     static constexpr int SPLIT_STAGES = SPLIT3 ? SG_TC_SPLIT3 : SG_TC_SPLIT1;
-    static constexpr int TMEM_COLS = 2 * BN;             // two accumulator buffers
+    // TMEM columns: two accumulator buffers of BN fp32 columns, then the A
+    // planes of every split stage (BK columns per plane, one row per lane).
+    static constexpr int ACC_COLS = 2 * BN;
+    static constexpr int A_COLS = PLANES * BK;
     static constexpr int NBAR = 2 * RAW_STAGES + 2 * SPLIT_STAGES + 4 + 1;
     static constexpr int SMEM_BYTES =
         RAW_STAGES * RAW_BYTES + SPLIT_STAGES * SPLIT_BYTES + NBAR * 8 + 16 + 1024;
-    static_assert(BN == 128 || BN == 256, "UMMA N");
+    static_assert(BN == 128, "one UMMA N per tile (BN = 128 keeps two accumulators in TMEM)");
+    static_assert(ACC_COLS + SPLIT_STAGES * A_COLS <= static_cast<int>(kTmemCols), "TMEM columns");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
-    // split stage layout: A_hi | B_hi | A_lo | B_lo
-    static constexpr int OFF_AHI = 0, OFF_BHI = A_BYTES;
-    static constexpr int OFF_ALO = RAW_BYTES, OFF_BLO = RAW_BYTES + A_BYTES;
+    // split stage layout (shared memory): B_hi | B_lo
+    static constexpr int OFF_BHI = 0, OFF_BLO = B_BYTES;
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -108,15 +123,16 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::tf32, one CTA.
-__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate)
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::tf32, one CTA.  A is M rows (TMEM
+// lanes) by K fp32 columns starting at a_tmem.
+__device__ __forceinline__ void umma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -150,6 +166,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Stores 16 consecutive fp32 columns into this warp's 32 TMEM lanes (one row
+// per lane).  Completion is awaited with tmem_wait_st().
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Round to the nearest TF32 value (10 explicit mantissa bits), ties away.
@@ -207,16 +244,7 @@ __host__ __device__ constexpr uint32_t idesc_tf32()
            | (static_cast<uint32_t>(BM >> 4) << 24);  // M / 16
 }
 
-// ------------------------------------------------------------ the kernel
-
-template <class C>
-struct Smem {
-    uint8_t *raw;      // RAW_STAGES x (A tile | B tile)
-    uint8_t *split;    // SPLIT_STAGES x (A_hi | B_hi | A_lo | B_lo)
-    uint64_t *raw_full, *raw_empty, *split_full, *split_empty, *acc_full, *acc_empty, *mma_done;
-    uint32_t *tmem_base;
-    volatile int *abort_flag;
-};
+// ------------------------------------------------------------ converters
 
 // Ring position walker: stage index and round parity, advanced per use.
 template <int N>
@@ -232,20 +260,58 @@ struct Ring {
     }
 };
 
-// Converts one raw tile (R rows of the operand, BK k) into K-major swizzled
-// hi (and lo) planes.  K-inner raw tiles already have that layout (TMA wrote
-// them with the same swizzle): the split is element-wise.  M/N-inner raw
-// tiles ([BK][R], unswizzled) are transposed in 4 x 4 blocks; the block
-// assignment (k-block rotated by lane/2) keeps each quarter-warp's 16-byte
-// stores on eight distinct bank groups.
+// A converter: this thread's row of the raw A tile (row = TMEM lane) ->
+// hi (and lo) planes in TMEM columns [t_hi, t_hi+32) and [t_lo, t_lo+32).
+// K-inner raw A is swizzled 128-byte rows (TMA's SWIZZLE_128B layout):
+// chunk c of row r sits at chunk c ^ (r mod 8).  M-inner raw A is [32 k][128 m].
+template <bool KIN, bool SPLIT3>
+__device__ __forceinline__ void convert_a_row(const uint8_t *raw_a, int row, uint32_t t_hi,
+                                              uint32_t t_lo)
+{
+    const uint32_t base = smem_u32(raw_a);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {  // 16 k per half
+        float x[16];
+        if (KIN) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int chunk = half * 4 + c;
+                const uint32_t a = base + row * 128 + (((chunk ^ row) & 7) << 4);
+                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(x[4 * c]), "=f"(x[4 * c + 1]), "=f"(x[4 * c + 2]),
+                               "=f"(x[4 * c + 3])
+                             : "r"(a));
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const uint32_t a = base + ((half * 16 + k) * BM + row) * 4;
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(x[k]) : "r"(a));
+            }
+        }
+        float h[16], l[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) split_value<SPLIT3>(x[k], h[k], l[k]);
+        tmem_st16(t_hi + half * 16, h);
+        if (SPLIT3) tmem_st16(t_lo + half * 16, l);
+    }
+}
+
+// B converter: one raw B tile (R = BN rows of B^T, BK k) -> K-major swizzled
+// hi (and lo) planes in shared memory.  K-inner raw tiles already have that
+// layout (TMA wrote them with the same swizzle): the split is element-wise.
+// N-inner raw tiles ([BK][R], unswizzled) are transposed in 4 x 4 blocks;
+// the block assignment (k-block rotated by lane/2) keeps each quarter-warp's
+// 16-byte loads and stores on eight distinct bank groups.
 template <int R, bool KIN, bool SPLIT3>
-__device__ __forceinline__ void convert_tile(const uint8_t *raw, uint8_t *hi, uint8_t *lo, int ct)
+__device__ __forceinline__ void convert_b_tile(const uint8_t *raw, uint8_t *hi, uint8_t *lo,
+                                               int ct)
 {
     const uint32_t raw_a = smem_u32(raw), hi_a = smem_u32(hi), lo_a = smem_u32(lo);
     if (KIN) {
         constexpr int CHUNKS = R * BK / 4;  // 16-byte chunks
 #pragma unroll 4
-        for (int c = ct; c < CHUNKS; c += kConvThreads) {
+        for (int c = ct; c < CHUNKS; c += kBConvThreads) {
             float4 x;
             asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                          : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
@@ -269,15 +335,15 @@ __device__ __forceinline__ void convert_tile(const uint8_t *raw, uint8_t *hi, ui
         const int warp = ct >> 5, lane = ct & 31;
         constexpr int RB4 = R / 4;                // 4-row blocks along R
         constexpr int PASSES = RB4 / 32;          // lanes cover 32 row blocks per pass
-        constexpr int SHARE = 8 / kConvWarps;     // k-blocks of 4 per warp and row block
-        static_assert(8 % kConvWarps == 0, "converter warps must divide the 8 k-blocks");
+        constexpr int SHARE = 8 / kBConvWarps;    // k-blocks of 4 per warp and row block
+        static_assert(8 % kBConvWarps == 0, "converter warps must divide the 8 k-blocks");
 #pragma unroll
         for (int pass = 0; pass < PASSES; ++pass) {
             const int rb4 = pass * 32 + lane;
 #pragma unroll
-            for (int half = 0; half < SHARE; ++half) {
+            for (int sh = 0; sh < SHARE; ++sh) {
                 // the warps x SHARE cover the 8 k-blocks of 4 for every rb4
-                const int kb4 = (warp * SHARE + half + (lane >> 1)) & 7;
+                const int kb4 = (warp * SHARE + sh + (lane >> 1)) & 7;
                 float v[4][4];  // v[kk][i] = raw(k = 4kb4+kk, r = 4rb4+i)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
@@ -305,6 +371,17 @@ __device__ __forceinline__ void convert_tile(const uint8_t *raw, uint8_t *hi, ui
         }
     }
 }
+
+// ------------------------------------------------------------ the kernel
+
+template <class C>
+struct Smem {
+    uint8_t *raw;      // RAW_STAGES x (A tile | B tile)
+    uint8_t *split;    // SPLIT_STAGES x (B_hi | B_lo)
+    uint64_t *raw_full, *raw_empty, *split_full, *split_empty, *acc_full, *acc_empty, *mma_done;
+    uint32_t *tmem_base;
+    volatile int *abort_flag;
+};
 
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -347,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(sm.tmem_base, C::TMEM_COLS);
+        tmem_alloc(sm.tmem_base, kTmemCols);
         tc_fence_before();
     }
     __syncthreads();
@@ -387,10 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 } else {
-                    int w = 1;
-                    if (lane == 0)
-                        w = mbar_wait(&sm.raw_empty[rr.s], rr.ph ^ 1u, ab, kStatusWaitEmpty) ? 1 : 0;
-                    ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+                    ok = warp_wait(&sm.raw_empty[rr.s], rr.ph ^ 1u, ab, kStatusWaitEmpty, lane);
                     if (ok) {
                         cp_async_tile<BM, C::A_KIN, false>(sa, p.A + tc.q * p.sA, p.lda, m0, p.M,
                                                            k0, p.K, p.a_vec4 != 0, lane, 32);
@@ -441,20 +515,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t st = smem_u32(sm.split + sr.s * C::SPLIT_BYTES);
+                    const uint32_t a_hi = tmem + C::ACC_COLS + sr.s * C::A_COLS;
+                    const uint32_t a_lo = a_hi + BK;
 #pragma unroll
                     for (int kk = 0; kk < BK / UK; ++kk) {
                         const uint32_t koff = kk * UK * 4;  // bytes along the 128-byte row
-                        const uint64_t a_hi = kmajor_sw128_desc(st + C::OFF_AHI + koff);
                         const uint64_t b_hi = kmajor_sw128_desc(st + C::OFF_BHI + koff);
                         const uint32_t acc_in = (kb > 0 || kk > 0) ? 1u : 0u;
                         if (C::SPLIT3) {
-                            const uint64_t a_lo = kmajor_sw128_desc(st + C::OFF_ALO + koff);
                             const uint64_t b_lo = kmajor_sw128_desc(st + C::OFF_BLO + koff);
-                            umma_tf32(d_tmem, a_lo, b_hi, idesc, acc_in);
-                            umma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
-                            umma_tf32(d_tmem, a_hi, b_hi, idesc, 1u);
+                            umma_tf32_ts(d_tmem, a_lo + kk * UK, b_hi, idesc, acc_in);
+                            umma_tf32_ts(d_tmem, a_hi + kk * UK, b_lo, idesc, 1u);
+                            umma_tf32_ts(d_tmem, a_hi + kk * UK, b_hi, idesc, 1u);
                         } else {
-                            umma_tf32(d_tmem, a_hi, b_hi, idesc, acc_in);
+                            umma_tf32_ts(d_tmem, a_hi + kk * UK, b_hi, idesc, acc_in);
                         }
                     }
                     any = true;
@@ -474,7 +548,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp < kEpiWarp0) {
         // ------------------------------------------------ converters
-        const int ct = threadIdx.x - kConvWarp0 * 32;
+        const bool is_a = warp < kBConvWarp0;
+        const int quarter = warp & 3;  // TMEM lanes this warp may access (A converters)
+        const int row = quarter * 32 + lane;
+        const int ct = threadIdx.x - kBConvWarp0 * 32;
         Ring<C::RAW_STAGES> rr;
         Ring<C::SPLIT_STAGES> sr;
         bool ok = true;
@@ -487,10 +564,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint8_t *sa = sm.raw + rr.s * C::RAW_BYTES;
                 const uint8_t *sb = sa + C::A_BYTES;
-                uint8_t *st = sm.split + sr.s * C::SPLIT_BYTES;
-                convert_tile<BM, C::A_KIN, C::SPLIT3>(sa, st + C::OFF_AHI, st + C::OFF_ALO, ct);
-                convert_tile<C::BN, C::B_KIN, C::SPLIT3>(sb, st + C::OFF_BHI, st + C::OFF_BLO, ct);
-                fence_proxy_async_smem();  // our stores -> visible to the tensor core
+                if (is_a) {
+                    tc_fence_after();  // the MMA that read this TMEM stage has completed
+                    const uint32_t t_hi = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                          C::ACC_COLS + sr.s * C::A_COLS;
+                    convert_a_row<C::A_KIN, C::SPLIT3>(sa, row, t_hi, t_hi + BK);
+                    tmem_wait_st();
+                    tc_fence_before();  // our TMEM stores -> visible to the MMA
+                } else {
+                    uint8_t *st = sm.split + sr.s * C::SPLIT_BYTES;
+                    convert_b_tile<C::BN, C::B_KIN, C::SPLIT3>(sb, st + C::OFF_BHI,
+                                                               st + C::OFF_BLO, ct);
+                    fence_proxy_async_smem();  // our stores -> visible to the tensor core
+                }
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&sm.raw_empty[rr.s]);
@@ -565,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, C::TMEM_COLS);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
