@@ -248,15 +248,41 @@ __device__ __forceinline__ float4 lds128(uint32_t addr)
     return v;
 }
 
-// Operand fragments of one k-group (4 consecutive k) for one lane:
-// a[kk][i] = op(A)[row i of the lane, k = 4g + kk], b[kk][j] likewise.
+// k values per fragment step: 4 (128-bit loads of K-inner rows) or 2 (64-bit
+// loads; an 8 x 8 lane tile then fits 128 registers, so two CTAs -- four
+// warps per scheduler -- fit on an SM).  Measured on GB300 at 4092^3 the two
+// are within 2%; 4 is the default.
+#ifndef SG_SIMT_KSTEP
+#define SG_SIMT_KSTEP 4
+#endif
+constexpr int kKStep = SG_SIMT_KSTEP;
+static_assert(kKStep == 2 || kKStep == 4, "fragment step");
+
+// Operand fragments of one k-step for one lane:
+// a[kk][i] = op(A)[row i of the lane, k = kKStep*g + kk], b[kk][j] likewise.
 template <class Cfg>
 struct Frag {
-    float a[4][Cfg::TM];
-    float b[4][Cfg::TN];
+    float a[kKStep][Cfg::TM];
+    float b[kKStep][Cfg::TN];
 };
 
-// Loads the fragments of k-group g from a stage.  a_base / b_base are this
+__device__ __forceinline__ float2 lds64(uint32_t addr)
+{
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+    return v;
+}
+
+// Byte offset, inside a lane's swizzled 128-byte row, of k-step g: the
+// 16-byte chunk (k / 4) moves by the XOR key, the 8-byte half (2-k steps)
+// stays in place.
+__device__ __forceinline__ uint32_t kstep_offset(int g, uint32_t key)
+{
+    if (kKStep == 4) return (static_cast<uint32_t>(g) << 4) ^ key;
+    return ((static_cast<uint32_t>(g >> 1) << 4) ^ key) + (static_cast<uint32_t>(g & 1) << 3);
+}
+
+// Loads the fragments of k-step g from a stage.  a_base / b_base are this
 // lane's base addresses inside the stage (see simt_consumer).
 template <class Cfg, bool A_KIN, bool B_KIN>
 __device__ __forceinline__ void load_frag(Frag<Cfg> &f, uint32_t a_base, uint32_t b_base,
@@ -264,23 +290,30 @@ __device__ __forceinline__ void load_frag(Frag<Cfg> &f, uint32_t a_base, uint32_
 {
     constexpr int WMITER = Cfg::WMITER, WNITER = Cfg::WNITER;
     if (A_KIN) {
-        const uint32_t ag = a_base + ((static_cast<uint32_t>(g) << 4) ^ a_key);
+        const uint32_t ag = a_base + kstep_offset(g, a_key);
 #pragma unroll
         for (int wm = 0; wm < WMITER; ++wm)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float4 v = lds128(ag + (wm * 32 + i * 8) * 128);
-                f.a[0][wm * 4 + i] = v.x;
-                f.a[1][wm * 4 + i] = v.y;
-                f.a[2][wm * 4 + i] = v.z;
-                f.a[3][wm * 4 + i] = v.w;
+                const uint32_t addr = ag + (wm * 32 + i * 8) * 128;
+                if (kKStep == 4) {
+                    const float4 v = lds128(addr);
+                    f.a[0][wm * 4 + i] = v.x;
+                    f.a[1 % kKStep][wm * 4 + i] = v.y;
+                    f.a[2 % kKStep][wm * 4 + i] = v.z;
+                    f.a[3 % kKStep][wm * 4 + i] = v.w;
+                } else {
+                    const float2 v = lds64(addr);
+                    f.a[0][wm * 4 + i] = v.x;
+                    f.a[1][wm * 4 + i] = v.y;
+                }
             }
     } else {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
+        for (int kk = 0; kk < kKStep; ++kk)
 #pragma unroll
             for (int wm = 0; wm < WMITER; ++wm) {
-                const float4 v = lds128(a_base + ((4 * g + kk) * Cfg::BM + wm * 32) * 4);
+                const float4 v = lds128(a_base + ((kKStep * g + kk) * Cfg::BM + wm * 32) * 4);
                 f.a[kk][wm * 4 + 0] = v.x;
                 f.a[kk][wm * 4 + 1] = v.y;
                 f.a[kk][wm * 4 + 2] = v.z;
@@ -288,24 +321,32 @@ __device__ __forceinline__ void load_frag(Frag<Cfg> &f, uint32_t a_base, uint32_
             }
     }
     if (B_KIN) {
-        const uint32_t bg0 = b_base + ((static_cast<uint32_t>(g) << 4) ^ b_key);
-        const uint32_t bg1 = b_base + ((static_cast<uint32_t>(g ^ 4) << 4) ^ b_key);
+        // rows j = 1, 3 of a 4-row group have the swizzle key lc + 4
+        const uint32_t bg0 = b_base + kstep_offset(g, b_key);
+        const uint32_t bg1 = b_base + kstep_offset(g, b_key ^ (4u << 4));
 #pragma unroll
         for (int wn = 0; wn < WNITER; ++wn)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float4 v = lds128(((j & 1) ? bg1 : bg0) + (wn * 16 + j * 4) * 128);
-                f.b[0][wn * 4 + j] = v.x;
-                f.b[1][wn * 4 + j] = v.y;
-                f.b[2][wn * 4 + j] = v.z;
-                f.b[3][wn * 4 + j] = v.w;
+                const uint32_t addr = ((j & 1) ? bg1 : bg0) + (wn * 16 + j * 4) * 128;
+                if (kKStep == 4) {
+                    const float4 v = lds128(addr);
+                    f.b[0][wn * 4 + j] = v.x;
+                    f.b[1 % kKStep][wn * 4 + j] = v.y;
+                    f.b[2 % kKStep][wn * 4 + j] = v.z;
+                    f.b[3 % kKStep][wn * 4 + j] = v.w;
+                } else {
+                    const float2 v = lds64(addr);
+                    f.b[0][wn * 4 + j] = v.x;
+                    f.b[1][wn * 4 + j] = v.y;
+                }
             }
     } else {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
+        for (int kk = 0; kk < kKStep; ++kk)
 #pragma unroll
             for (int wn = 0; wn < WNITER; ++wn) {
-                const float4 v = lds128(b_base + ((4 * g + kk) * Cfg::BN + wn * 16) * 4);
+                const float4 v = lds128(b_base + ((kKStep * g + kk) * Cfg::BN + wn * 16) * 4);
                 f.b[kk][wn * 4 + 0] = v.x;
                 f.b[kk][wn * 4 + 1] = v.y;
                 f.b[kk][wn * 4 + 2] = v.z;
@@ -318,7 +359,7 @@ template <class Cfg>
 __device__ __forceinline__ void fma_frag(float (&acc)[Cfg::TM][Cfg::TN], const Frag<Cfg> &f)
 {
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
+    for (int kk = 0; kk < kKStep; ++kk)
 #pragma unroll
         for (int i = 0; i < Cfg::TM; ++i)
 #pragma unroll
@@ -347,7 +388,7 @@ __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem
 {
     constexpr int WMITER = Cfg::WMITER, WNITER = Cfg::WNITER, TM = Cfg::TM, TN = Cfg::TN;
     constexpr int BM = Cfg::BM, BN = Cfg::BN;
-    constexpr int GROUPS = kBK / 4;
+    constexpr int GROUPS = kBK / kKStep;
     const int wm0 = (cw / Cfg::WARPS_N) * Cfg::WM;
     const int wn0 = (cw % Cfg::WARPS_N) * Cfg::WN;
     const int lr = lane >> 2, lc = lane & 3;
