@@ -542,18 +542,29 @@ def all_configs(args):
         ai = flops / compulsory_bytes(M, N, K, Q, beta != 0)
         for tB, Bd, ldb in variants:
             for mode in ("fp32", "3xtf32", "tf32"):
-                def call(mode=mode, Bd=Bd, ldb=ldb, tB=tB):
-                    lib.check(lib.sgemm_batched_ex(mode, M, N, K, w["alpha"], A, K, Bd, ldb, beta,
-                                                   C, N, 0, tB, M * K, K * N, M * N, Q, stream))
-                ms = statistics.median(time_calls(call, args.steps, args.warmup, stream, flush))
-                tf = flops / (ms / 1e3) / 1e12
-                bound, peak, _ = roofline_peak(mode, props.multi_processor_count, peaks, src)
-                roof = min(peak, ai * bw)
-                print(json.dumps({"workload": name, "beta": beta, "transB": tB, "mode": mode,
-                                  "ms": round(ms, 4), "tflops": round(tf, 2),
-                                  "roof_tflops": round(roof, 1),
-                                  "roof_bound": bound if roof == peak else "hbm",
-                                  "frac": round(tf / roof, 3)}), flush=True)
+                ws_bytes = lib.sgemm_workspace_size(mode, M, N, K, Q)
+                ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+                for entry in (("plain", "split_k") if ws_bytes else ("plain",)):
+                    def call(mode=mode, Bd=Bd, ldb=ldb, tB=tB, entry=entry):
+                        if entry == "plain":
+                            st = lib.sgemm_batched_ex(mode, M, N, K, w["alpha"], A, K, Bd, ldb,
+                                                      beta, C, N, 0, tB, M * K, K * N, M * N, Q,
+                                                      stream)
+                        else:
+                            st = lib.sgemm_batched_ex_ws(mode, M, N, K, w["alpha"], A, K, Bd, ldb,
+                                                         beta, C, N, 0, tB, M * K, K * N, M * N,
+                                                         Q, ws, ws_bytes, stream)
+                        lib.check(st)
+                    ms = statistics.median(time_calls(call, args.steps, args.warmup, stream,
+                                                      flush))
+                    tf = flops / (ms / 1e3) / 1e12
+                    bound, peak, _ = roofline_peak(mode, props.multi_processor_count, peaks, src)
+                    roof = min(peak, ai * bw)
+                    print(json.dumps({"workload": name, "beta": beta, "transB": tB, "mode": mode,
+                                      "entry": entry, "ms": round(ms, 4), "tflops": round(tf, 2),
+                                      "roof_tflops": round(roof, 1),
+                                      "roof_bound": bound if roof == peak else "hbm",
+                                      "frac": round(tf / roof, 3)}), flush=True)
     lib.check(lib.sgemm_poll_error(stream))
     return 0
 

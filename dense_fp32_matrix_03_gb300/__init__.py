@@ -39,6 +39,9 @@ SIGNATURES = {
                            _i, _p]),
     "sgemm_batched_ex": (_i, [_i, _i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _i, _i, _ll, _ll,
                               _ll, _i, _p]),
+    "sgemm_workspace_size": (ctypes.c_size_t, [_i, _i, _i, _i, _i]),
+    "sgemm_batched_ex_ws": (_i, [_i, _i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _i, _i, _ll, _ll,
+                                 _ll, _i, _p, ctypes.c_size_t, _p]),
     "sgemm_set_default_mode": (_i, [_i]),
     "sgemm_get_default_mode": (_i, []),
     "sgemm_status_string": (ctypes.c_char_p, [_i]),
@@ -131,6 +134,23 @@ def sgemm_batched_ex(mode, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, transA,
     return _lib.sgemm_batched_ex(mode, M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta,
                                  _ptr(C), ldc, int(transA), int(transB), strideA, strideB,
                                  strideC, Q, _stream(stream))
+
+
+def sgemm_workspace_size(mode, M, N, K, Q=1) -> int:
+    if isinstance(mode, str):
+        mode = MODES[mode]
+    return int(_lib.sgemm_workspace_size(mode, M, N, K, Q))
+
+
+def sgemm_batched_ex_ws(mode, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, transA, transB,
+                        strideA, strideB, strideC, Q, workspace, workspace_bytes,
+                        stream=None) -> int:
+    if isinstance(mode, str):
+        mode = MODES[mode]
+    return _lib.sgemm_batched_ex_ws(mode, M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta,
+                                    _ptr(C), ldc, int(transA), int(transB), strideA, strideB,
+                                    strideC, Q, _ptr(workspace), int(workspace_bytes),
+                                    _stream(stream))
 
 
 def sgemm_set_default_mode(mode) -> int:

@@ -159,6 +159,49 @@ bool encode_operand(CUtensorMap *map, const float *base, bool kin, long long row
     return r == CUDA_SUCCESS;
 }
 
+int min_slice_kblocks(int mode) { return mode == SGEMM_MODE_FP32 ? 2 : 8; }
+
+int choose_splits(long long num_tiles, int k_blocks, int num_sms, int mode)
+{
+    // as many slices as keep every unit in one wave (units <= multiprocessors)
+    if (num_tiles <= 0 || 2 * num_tiles > num_sms) return 1;
+    long long s = num_sms / num_tiles;
+    const long long by_k = k_blocks / min_slice_kblocks(mode);
+    if (s > by_k) s = by_k;
+    if (s > kMaxSplits) s = kMaxSplits;
+    return s < 2 ? 1 : static_cast<int>(s);
+}
+
+size_t splitk_workspace_bytes(long long num_tiles, int splits)
+{
+    if (splits <= 1) return 0;
+    const size_t ctr = (static_cast<size_t>(num_tiles) * kSplitRegions * sizeof(unsigned int) + 255) &
+                       ~static_cast<size_t>(255);
+    return ctr + static_cast<size_t>(num_tiles) * splits * kSplitTile * kSplitTile * sizeof(float);
+}
+
+int plan_splits(Plan &plan)
+{
+    GemmParams &p = plan.p;
+    p.splits = 1;
+    p.ws_part = nullptr;
+    p.ws_ctr = nullptr;
+    const int s = plan.ws ? choose_splits(p.num_tiles, p.k_blocks, plan.num_sms, plan.mode) : 1;
+    const size_t need = splitk_workspace_bytes(p.num_tiles, s);
+    if (s > 1 && need <= plan.ws_bytes) {
+        const size_t ctr = (static_cast<size_t>(p.num_tiles) * kSplitRegions * sizeof(unsigned int) +
+                            255) & ~static_cast<size_t>(255);
+        p.splits = s;
+        p.ws_ctr = static_cast<unsigned int *>(plan.ws);
+        p.ws_part = reinterpret_cast<float *>(static_cast<char *>(plan.ws) + ctr);
+        // counters start at zero (the last slice of every region re-arms its
+        // counter, but a call that stopped early may have left one raised)
+        if (cudaMemsetAsync(plan.ws, 0, ctr, plan.stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    }
+    p.num_units = p.num_tiles * p.splits;
+    return SGEMM_OK;
+}
+
 }  // namespace sg
 
 using namespace sg;
@@ -176,7 +219,8 @@ bool tma_eligible(const float *p, long long ld, int Q, long long stride)
 
 int run(int mode, int M, int N, int K, float alpha, const float *A, int lda, const float *B,
         int ldb, float beta, float *C, int ldc, int transA, int transB, long long sA,
-        long long sB, long long sC, int Q, void *stream)
+        long long sB, long long sC, int Q, void *stream, void *ws = nullptr,
+        size_t ws_bytes = 0)
 {
     if (mode == SGEMM_MODE_DEFAULT) mode = g_default_mode.load();
     int rc = check_args(mode, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, transA, transB, sA,
@@ -229,6 +273,8 @@ int run(int mode, int M, int N, int K, float alpha, const float *A, int lda, con
     plan.num_sms = di->num_sms;
     plan.device = dev;
     plan.stream = st;
+    plan.ws = ws;
+    plan.ws_bytes = ws_bytes;
 
     if (mode == SGEMM_MODE_FP32) return launch_simt(plan);
     return launch_tc(plan);
@@ -260,6 +306,33 @@ int sgemm_batched_ex(int mode, int M, int N, int K, float alpha, const float *A,
 {
     return run(mode, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, transA, transB, strideA,
                strideB, strideC, Q, stream);
+}
+
+int sgemm_batched_ex_ws(int mode, int M, int N, int K, float alpha, const float *A, int lda,
+                        const float *B, int ldb, float beta, float *C, int ldc, int transA,
+                        int transB, long long strideA, long long strideB, long long strideC,
+                        int Q, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (workspace_bytes > 0 &&
+        (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return SGEMM_ERR_INVALID_ARG;
+    return run(mode, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, transA, transB, strideA,
+               strideB, strideC, Q, stream, workspace_bytes ? workspace : nullptr,
+               workspace_bytes);
+}
+
+size_t sgemm_workspace_size(int mode, int M, int N, int K, int Q)
+{
+    if (mode == SGEMM_MODE_DEFAULT) mode = g_default_mode.load();
+    if (mode != SGEMM_MODE_FP32 && mode != SGEMM_MODE_3XTF32 && mode != SGEMM_MODE_TF32) return 0;
+    if (M <= 0 || N <= 0 || K <= 0 || Q <= 0) return 0;
+    int dev = 0;
+    const DeviceInfo *di = device_info(&dev);
+    if (di == nullptr) return 0;
+    const long long tiles = static_cast<long long>(Q) * ((M + kSplitTile - 1) / kSplitTile) *
+                            ((N + kSplitTile - 1) / kSplitTile);
+    const int k_blocks = (K + kTileK - 1) / kTileK;
+    return splitk_workspace_bytes(tiles, choose_splits(tiles, k_blocks, di->num_sms, mode));
 }
 
 int sgemm_set_default_mode(int mode)

@@ -270,4 +270,53 @@ __device__ __forceinline__ TileCoord tile_coord(long long t, const GemmParams &p
     return c;
 }
 
+// One work unit of the persistent scheduler: a tile and its k-block slice.
+struct WorkUnit {
+    TileCoord tc;
+    long long tile;   // linear tile index
+    int slice;        // 0 .. splits-1
+    int kb_lo, kb_hi; // k-blocks [kb_lo, kb_hi) of this slice (never empty)
+};
+
+__device__ __forceinline__ WorkUnit work_unit(long long u, const GemmParams &p)
+{
+    WorkUnit w;
+    if (p.splits <= 1) {
+        w.tile = u;
+        w.slice = 0;
+        w.kb_lo = 0;
+        w.kb_hi = p.k_blocks;
+    } else {
+        w.tile = u / p.splits;
+        w.slice = static_cast<int>(u - w.tile * p.splits);
+        w.kb_lo = static_cast<int>((static_cast<long long>(w.slice) * p.k_blocks) / p.splits);
+        w.kb_hi = static_cast<int>((static_cast<long long>(w.slice + 1) * p.k_blocks) / p.splits);
+    }
+    w.tc = tile_coord(w.tile, p);
+    return w;
+}
+
+// Split-K hand-off for one region of a tile (a warp's share of the output
+// tile), called by all 32 lanes after they stored their partial values with
+// plain global stores.  Returns true (warp-uniformly) in the warp of the last
+// slice to finish the region, which may then read every slice's partial:
+// the fences order each writer's stores before its counter increment and the
+// last reader's loads after its own.  The last one also re-arms the counter.
+__device__ __forceinline__ bool splitk_arrive(unsigned int *ctr, int splits, int lane)
+{
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+        last = (atomicAdd(ctr, 1u) == static_cast<unsigned int>(splits - 1)) ? 1 : 0;
+        if (last) *ctr = 0u;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) __threadfence();
+    return last != 0;
+}
+
+// Loads that bypass L1 (partials written by other SMs must come from L2).
+__device__ __forceinline__ float4 ldcg4(const float *p) { return __ldcg(reinterpret_cast<const float4 *>(p)); }
+
 }  // namespace sg

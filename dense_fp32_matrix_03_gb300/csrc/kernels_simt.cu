@@ -25,13 +25,14 @@ constexpr int kGroupM = 8;
 template <class Cfg, bool A_KIN, bool B_KIN, bool USE_TMA, bool EVEN_K>
 int launch_one(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
 {
-    auto kern = simt_sgemm_kernel<Cfg, A_KIN, B_KIN, USE_TMA, EVEN_K>;
+    auto kern = plan.p.splits > 1 ? simt_sgemm_kernel<Cfg, A_KIN, B_KIN, USE_TMA, EVEN_K, true>
+                                  : simt_sgemm_kernel<Cfg, A_KIN, B_KIN, USE_TMA, EVEN_K, false>;
     // The attribute is per device; setting it on every call costs about a
     // microsecond and keeps the launcher free of per-device caches.
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg::SMEM_BYTES) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
-    long long grid = plan.p.num_tiles;
+    long long grid = plan.p.num_units;
     if (grid > static_cast<long long>(plan.num_sms) * kMinBlocks)
         grid = static_cast<long long>(plan.num_sms) * kMinBlocks;
     kern<<<static_cast<unsigned>(grid), Cfg::THREADS, Cfg::SMEM_BYTES, plan.stream>>>(
@@ -61,6 +62,10 @@ int launch_simt(Plan &plan)
     p.group_m = kGroupM;
     p.num_tiles = static_cast<long long>(p.Q) * p.tiles_m * p.tiles_n;
     plan.even_k = (p.K % kBK) == 0;
+    static_assert(Cfg::BM == kSplitTile && Cfg::BN == kSplitTile, "split-K workspace tile");
+    static_assert(Cfg::CONSUMER_WARPS <= kSplitRegions, "split-K counters per tile");
+    const int rc = plan_splits(plan);
+    if (rc != SGEMM_OK) return rc;
 
     alignas(64) CUtensorMap tmA;
     alignas(64) CUtensorMap tmB;

@@ -16,12 +16,14 @@ constexpr int kGroupM = 8;
 template <bool SPLIT3, bool A_KIN, bool B_KIN, bool USE_TMA>
 int launch_one(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
 {
-    using C = tc::Cfg<kBN, SPLIT3, A_KIN, B_KIN, USE_TMA>;
-    auto kern = tc::tc_sgemm_kernel<C>;
+    using C = tc::Cfg<kBN, SPLIT3, A_KIN, B_KIN, USE_TMA, false>;
+    using CS = tc::Cfg<kBN, SPLIT3, A_KIN, B_KIN, USE_TMA, true>;
+    static_assert(C::SMEM_BYTES == CS::SMEM_BYTES, "same layout with and without split-K");
+    auto kern = plan.p.splits > 1 ? tc::tc_sgemm_kernel<CS> : tc::tc_sgemm_kernel<C>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
-    long long grid = plan.p.num_tiles;
+    long long grid = plan.p.num_units;
     if (grid > plan.num_sms) grid = plan.num_sms;
     kern<<<static_cast<unsigned>(grid), tc::kThreads, C::SMEM_BYTES, plan.stream>>>(tmA, tmB,
                                                                                   plan.p);
@@ -49,6 +51,9 @@ int launch_tc(Plan &plan)
     p.group_m = kGroupM;
     p.num_tiles = static_cast<long long>(p.Q) * p.tiles_m * p.tiles_n;
     plan.even_k = (p.K % tc::BK) == 0;
+    static_assert(tc::BM == kSplitTile && kBN == kSplitTile, "split-K workspace tile");
+    const int rc = plan_splits(plan);
+    if (rc != SGEMM_OK) return rc;
 
     alignas(64) CUtensorMap tmA;
     alignas(64) CUtensorMap tmB;

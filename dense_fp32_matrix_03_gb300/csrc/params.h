@@ -34,6 +34,14 @@ struct GemmParams {
     int c_vec4;                // epilogue may use 16-byte C accesses
     unsigned int *status;      // device status word
     long long wait_limit;      // clock64 cycles a bounded wait may spin
+    // split-K: every tile's k-blocks are cut into `splits` contiguous slices;
+    // work unit u = tile * splits + slice.  With splits > 1 each slice writes
+    // its fp32 partial tile to ws_part and the last slice to finish a region
+    // (per-region counters in ws_ctr) sums all partials and writes C.
+    int splits;                // 1 = no split
+    long long num_units;       // num_tiles * splits
+    float *ws_part;            // num_tiles * splits partial tiles (BM x BN fp32 each)
+    unsigned int *ws_ctr;      // num_tiles * regions arrival counters (zero on entry)
 };
 
 }  // namespace sg

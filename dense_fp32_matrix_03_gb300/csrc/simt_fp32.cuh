@@ -68,36 +68,39 @@ struct SimtCfg {
 #define SG_SIMT_LAG 1
 #endif
 constexpr int kLag = SG_SIMT_LAG;
-// Consumer loop form: software-pipelined over k-groups (1) or a plain loop
-// unrolled kGroupUnroll times (0); CTAs per SM the kernel is compiled for.
-#ifndef SG_SIMT_PIPE
-#define SG_SIMT_PIPE 0
-#endif
+// Unroll of the consumer's k-step loop; CTAs per SM the kernel is compiled for.
 #ifndef SG_SIMT_UNROLL
 #define SG_SIMT_UNROLL 4
 #endif
 #ifndef SG_SIMT_MINB
 #define SG_SIMT_MINB 1
 #endif
-constexpr bool kPipelined = SG_SIMT_PIPE != 0;
 constexpr int kGroupUnroll = SG_SIMT_UNROLL;
 constexpr int kMinBlocks = SG_SIMT_MINB;
 
-// Walks the (tile, k-block) sequence of one CTA.
+// Walks the (work unit, k-block) sequence of one CTA.
 struct KPos {
-    long long tile;   // global tile index
-    int kb;           // k-block inside the tile
+    long long unit;   // global work-unit index
+    int kb, kb_end;   // current k-block and end of the unit's slice
     int stage;        // stage of this k-block
     uint32_t phase;   // round parity of this k-block's stage
     TileCoord tc;
 
+    __device__ __forceinline__ void load_unit(const GemmParams &p)
+    {
+        if (unit < p.num_units) {
+            const WorkUnit w = work_unit(unit, p);
+            tc = w.tc;
+            kb = w.kb_lo;
+            kb_end = w.kb_hi;
+        }
+    }
     __device__ __forceinline__ void start(const GemmParams &p)
     {
-        tile = blockIdx.x;
-        kb = 0;
+        unit = blockIdx.x;
         stage = 0;
         phase = 0;
-        if (tile < p.num_tiles) tc = tile_coord(tile, p);
+        load_unit(p);
     }
     template <int STAGES>
     __device__ __forceinline__ void next(const GemmParams &p)
@@ -106,10 +109,9 @@ struct KPos {
             stage = 0;
             phase ^= 1u;
         }
-        if (++kb == p.k_blocks) {
-            kb = 0;
-            tile += gridDim.x;
-            if (tile < p.num_tiles) tc = tile_coord(tile, p);
+        if (++kb == kb_end) {
+            unit += gridDim.x;
+            load_unit(p);
         }
     }
 };
@@ -366,6 +368,49 @@ __device__ __forceinline__ void fma_frag(float (&acc)[Cfg::TM][Cfg::TN], const F
             for (int j = 0; j < Cfg::TN; ++j) acc[i][j] = fmaf(f.a[kk][i], f.b[kk][j], acc[i][j]);
 }
 
+// Split-K hand-off of one warp's accumulators (its region of the tile).
+// Partials are stored lane-interleaved (float4 v of lane l at v*32 + l within
+// the region) so that every store and load of a warp is one contiguous 512
+// bytes.  Returns false when another slice will finish the region; in the
+// warp of the last slice, replaces acc by the sum over all slices, taken in
+// slice order 0, 1, ..., so the result does not depend on arrival order.
+template <class Cfg>
+__device__ __forceinline__ bool splitk_exchange(const GemmParams &p, const WorkUnit &wu, int cw,
+                                                int lane, float (&acc)[Cfg::TM][Cfg::TN])
+{
+    constexpr int TM = Cfg::TM, TN = Cfg::TN, V = TM * TN / 4;
+    constexpr long long REGION = static_cast<long long>(V) * 32;  // float4 per region
+    float4 *ws = reinterpret_cast<float4 *>(p.ws_part);
+    const long long slot0 = wu.tile * p.splits;
+    float4 *mine = ws + ((slot0 + wu.slice) * Cfg::CONSUMER_WARPS + cw) * REGION + lane;
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int jg = 0; jg < TN / 4; ++jg)
+            mine[(i * (TN / 4) + jg) * 32] =
+                make_float4(acc[i][4 * jg], acc[i][4 * jg + 1], acc[i][4 * jg + 2], acc[i][4 * jg + 3]);
+    if (!splitk_arrive(p.ws_ctr + wu.tile * Cfg::CONSUMER_WARPS + cw, p.splits, lane)) return false;
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+    for (int sl = 0; sl < p.splits; ++sl) {
+        const float *src = reinterpret_cast<const float *>(
+            ws + ((slot0 + sl) * Cfg::CONSUMER_WARPS + cw) * REGION + lane);
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int jg = 0; jg < TN / 4; ++jg) {
+                const float4 x = ldcg4(src + (i * (TN / 4) + jg) * 32 * 4);
+                acc[i][4 * jg] += x.x;
+                acc[i][4 * jg + 1] += x.y;
+                acc[i][4 * jg + 2] += x.z;
+                acc[i][4 * jg + 3] += x.w;
+            }
+    }
+    return true;
+}
+
 // One consumer warp: WM x WN outputs of the CTA tile; each lane holds
 // TM x TN accumulators as (WM/32) x (WN/16) sub-blocks of 4 x 4.
 //
@@ -381,7 +426,7 @@ __device__ __forceinline__ void fma_frag(float (&acc)[Cfg::TM][Cfg::TN], const F
 // register set while the current one feeds the FFMAs.  A stage is released
 // after the FFMAs of its last k-group, i.e. once every value read from it has
 // been consumed.
-template <class Cfg, bool A_KIN, bool B_KIN, class Issuer>
+template <class Cfg, bool A_KIN, bool B_KIN, bool SPLITK, class Issuer>
 __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem, uint64_t *full,
                                               uint64_t *empty, const Abort &ab, int cw, int lane,
                                               Issuer &iss)
@@ -418,72 +463,34 @@ __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem
     uint32_t cph = 0;   // its round parity
 
     long long it = 0;  // k-blocks consumed so far by this CTA
-    for (long long t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-        const TileCoord tc = tile_coord(t, p);
+    for (long long u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+        const WorkUnit wu = work_unit(u, p);
+        const TileCoord &tc = wu.tc;
         float acc[TM][TN];
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
             for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
-        if (kPipelined) {
-            Frag<Cfg> f[2];
+        for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb, ++it) {
             if (!wait_full(cs, cph)) return;
-            uint32_t stage = stage_addr(cs);
-            load_frag<Cfg, A_KIN, B_KIN>(f[0], stage + a_lane, stage + b_lane, a_key, b_key, 0);
-
-            for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
-    #pragma unroll 1
-                for (int gp = 0; gp < GROUPS / 2; ++gp) {
-                    // even k-group 2*gp: compute f[0], prefetch 2*gp+1 into f[1]
-                    load_frag<Cfg, A_KIN, B_KIN>(f[1], stage + a_lane, stage + b_lane, a_key, b_key,
-                                                 2 * gp + 1);
-                    fma_frag<Cfg>(acc, f[0]);
-                    // odd k-group 2*gp+1: compute f[1], prefetch the next group into f[0]
-                    if (gp + 1 < GROUPS / 2) {
-                        load_frag<Cfg, A_KIN, B_KIN>(f[0], stage + a_lane, stage + b_lane, a_key,
-                                                     b_key, 2 * gp + 2);
-                        fma_frag<Cfg>(acc, f[1]);
-                    } else {
-                        const bool more = kb + 1 < p.k_blocks;
-                        const int ns = (cs + 1 == Cfg::STAGES) ? 0 : cs + 1;
-                        const uint32_t nph = (cs + 1 == Cfg::STAGES) ? (cph ^ 1u) : cph;
-                        if (more) {
-                            if (!wait_full(ns, nph)) return;
-                            const uint32_t nstage = stage_addr(ns);
-                            load_frag<Cfg, A_KIN, B_KIN>(f[0], nstage + a_lane, nstage + b_lane,
-                                                         a_key, b_key, 0);
-                        }
-                        fma_frag<Cfg>(acc, f[1]);
-                        // every value read from this stage has been consumed
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&empty[cs]);
-                        if (!iss.refill(it, ab, cw, lane)) return;
-                        cs = ns;
-                        cph = nph;
-                        stage = stage_addr(cs);
-                    }
-                }
-            }
-        } else {
-            for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
-                if (!wait_full(cs, cph)) return;
-                const uint32_t stage = stage_addr(cs);
+            const uint32_t stage = stage_addr(cs);
 #pragma unroll kGroupUnroll
-                for (int g = 0; g < GROUPS; ++g) {
-                    Frag<Cfg> f;
-                    load_frag<Cfg, A_KIN, B_KIN>(f, stage + a_lane, stage + b_lane, a_key, b_key, g);
-                    fma_frag<Cfg>(acc, f);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[cs]);
-                if (!iss.refill(it, ab, cw, lane)) return;
-                if (++cs == Cfg::STAGES) {
-                    cs = 0;
-                    cph ^= 1u;
-                }
+            for (int g = 0; g < GROUPS; ++g) {
+                Frag<Cfg> f;
+                load_frag<Cfg, A_KIN, B_KIN>(f, stage + a_lane, stage + b_lane, a_key, b_key, g);
+                fma_frag<Cfg>(acc, f);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[cs]);
+            if (!iss.refill(it, ab, cw, lane)) return;
+            if (++cs == Cfg::STAGES) {
+                cs = 0;
+                cph ^= 1u;
             }
         }
+
+        if (SPLITK && !splitk_exchange<Cfg>(p, wu, cw, lane, acc)) continue;
 
         // ---- epilogue: C = alpha * acc + beta * C, masked at the M/N edges
         const int mt = tc.tm * BM, nt = tc.tn * BN;
@@ -545,7 +552,7 @@ __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem
 
 // ---------------------------------------------------------------- kernel
 
-template <class Cfg, bool A_KIN, bool B_KIN, bool USE_TMA, bool EVEN_K>
+template <class Cfg, bool A_KIN, bool B_KIN, bool USE_TMA, bool EVEN_K, bool SPLITK>
 __global__ void __launch_bounds__(Cfg::THREADS, kMinBlocks)
     simt_sgemm_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const GemmParams p)
@@ -571,9 +578,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, kMinBlocks)
     __syncthreads();
     const Abort ab{abort_flag, p.status, p.wait_limit};
 
-    // k-blocks this CTA consumes: its tiles are blockIdx.x + i*gridDim.x
-    const long long my_tiles =
-        (p.num_tiles - blockIdx.x + gridDim.x - 1) / static_cast<long long>(gridDim.x);
+    // k-blocks this CTA consumes: its units are blockIdx.x + i*gridDim.x
+    long long my_kblocks;
+    if (!SPLITK) {
+        my_kblocks = (p.num_units - blockIdx.x + gridDim.x - 1) / static_cast<long long>(gridDim.x) *
+                     p.k_blocks;
+    } else {
+        my_kblocks = 0;
+        for (long long u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+            const WorkUnit w = work_unit(u, p);
+            my_kblocks += w.kb_hi - w.kb_lo;
+        }
+    }
     Issuer iss;
     if constexpr (USE_TMA) {
         iss.tmA = &tmA;
@@ -583,10 +599,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, kMinBlocks)
     iss.smem = smem;
     iss.full = full;
     iss.empty = empty;
-    iss.total = my_tiles * p.k_blocks;
+    iss.total = my_kblocks;
     iss.prologue(warp, lane, ab);
     __syncwarp();
-    simt_consumer<Cfg, A_KIN, B_KIN>(p, smem, full, empty, ab, warp, lane, iss);
+    simt_consumer<Cfg, A_KIN, B_KIN, SPLITK>(p, smem, full, empty, ab, warp, lane, iss);
     __syncwarp();
     if (*abort_flag) iss.drain(ab.limit, warp, lane);
     __syncthreads();

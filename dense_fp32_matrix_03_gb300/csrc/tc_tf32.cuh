@@ -67,10 +67,11 @@ constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 constexpr int kConvWarps = 4 + kBConvWarps;      // arrivals that complete a stage
 constexpr uint32_t kTmemCols = 512;
 
-template <int BN_, bool SPLIT3_, bool A_KIN_, bool B_KIN_, bool USE_TMA_>
+template <int BN_, bool SPLIT3_, bool A_KIN_, bool B_KIN_, bool USE_TMA_, bool SPLITK_>
 struct Cfg {
     static constexpr int BN = BN_;
     static constexpr bool SPLIT3 = SPLIT3_, A_KIN = A_KIN_, B_KIN = B_KIN_, USE_TMA = USE_TMA_;
+    static constexpr bool SPLITK = SPLITK_;   // K cut into slices (split-K epilogue)
     static constexpr int A_BYTES = BM * BK * 4;          // one 128 x 32 fp32 tile
     static constexpr int B_BYTES = BN * BK * 4;
     static constexpr int RAW_BYTES = A_BYTES + B_BYTES;
@@ -372,6 +373,42 @@ __device__ __forceinline__ void convert_b_tile(const uint8_t *raw, uint8_t *hi, 
     }
 }
 
+// Epilogue of 32 consecutive columns of one output row:
+// C[r][n0 .. n0+31] = alpha * v + beta * C, masked at the M/N edges; C is
+// read only when beta != 0.
+__device__ __forceinline__ void store_c_chunk(const GemmParams &p, float *crow, int r, int n0,
+                                              const float (&v)[32])
+{
+    if (r >= p.M) return;
+    const bool use_beta = p.beta != 0.f;
+    if (p.c_vec4 && n0 + 32 <= p.N) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            float4 o = make_float4(p.alpha * v[j], p.alpha * v[j + 1], p.alpha * v[j + 2],
+                                   p.alpha * v[j + 3]);
+            float4 *dst = reinterpret_cast<float4 *>(crow + n0 + j);
+            if (use_beta) {
+                const float4 old = *dst;
+                o.x = fmaf(p.beta, old.x, o.x);
+                o.y = fmaf(p.beta, old.y, o.y);
+                o.z = fmaf(p.beta, old.z, o.z);
+                o.w = fmaf(p.beta, old.w, o.w);
+            }
+            *dst = o;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int n = n0 + j;
+            if (n < p.N) {
+                float o = p.alpha * v[j];
+                if (use_beta) o = fmaf(p.beta, crow[n], o);
+                crow[n] = o;
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------ the kernel
 
 template <class C>
@@ -431,7 +468,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *sm.tmem_base;
     const Abort ab{sm.abort_flag, p.status, p.wait_limit};
-    const int k_blocks = p.k_blocks;
 
     if (warp == 0) {
         // ------------------------------------------------ producer
@@ -442,10 +478,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
         }
-        for (long long t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-            const TileCoord tc = tile_coord(t, p);
+        for (long long u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            const WorkUnit wu = work_unit(u, p);
+            const TileCoord &tc = wu.tc;
             const int m0 = tc.tm * BM, n0 = tc.tn * C::BN;
-            for (int kb = 0; kb < k_blocks; ++kb) {
+            for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
                 uint8_t *sa = sm.raw + rr.s * C::RAW_BYTES;
                 uint8_t *sb = sa + C::A_BYTES;
                 const int k0 = kb * BK;
@@ -501,14 +538,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc = idesc_tf32<C::BN>();
             bool ok = true;
             bool any = false;
-            for (long long t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (long long u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                const WorkUnit wu = work_unit(u, p);
                 if (!mbar_wait(&sm.acc_empty[acc.s], acc.ph ^ 1u, ab, kStatusWaitAcc)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc.s * C::BN);
-                for (int kb = 0; kb < k_blocks; ++kb) {
+                for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
                     if (!mbar_wait(&sm.split_full[sr.s], sr.ph, ab, kStatusWaitConv)) {
                         ok = false;
                         break;
@@ -521,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < BK / UK; ++kk) {
                         const uint32_t koff = kk * UK * 4;  // bytes along the 128-byte row
                         const uint64_t b_hi = kmajor_sw128_desc(st + C::OFF_BHI + koff);
-                        const uint32_t acc_in = (kb > 0 || kk > 0) ? 1u : 0u;
+                        const uint32_t acc_in = (kb > wu.kb_lo || kk > 0) ? 1u : 0u;
                         if (C::SPLIT3) {
                             const uint64_t b_lo = kmajor_sw128_desc(st + C::OFF_BLO + koff);
                             umma_tf32_ts(d_tmem, a_lo + kk * UK, b_hi, idesc, acc_in);
@@ -555,8 +593,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         Ring<C::RAW_STAGES> rr;
         Ring<C::SPLIT_STAGES> sr;
         bool ok = true;
-        for (long long t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-            for (int kb = 0; kb < k_blocks; ++kb) {
+        for (long long u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            const WorkUnit wu = work_unit(u, p);
+            for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
                 if (!warp_wait(&sm.raw_full[rr.s], rr.ph, ab, kStatusWaitFull, lane) ||
                     !warp_wait(&sm.split_empty[sr.s], sr.ph ^ 1u, ab, kStatusWaitMma, lane)) {
                     ok = false;
@@ -591,56 +630,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;            // TMEM lane quarter this warp may access
         const int row_in_tile = q * 32 + lane;
         Ring<2> acc;
-        const bool use_beta = p.beta != 0.f;
-        for (long long t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+        for (long long u = blockIdx.x; u < p.num_units; u += gridDim.x) {
             int w = 1;
             if (lane == 0) w = mbar_wait(&sm.acc_full[acc.s], acc.ph, ab, kStatusWaitAcc, true);
             if (!__shfl_sync(0xffffffffu, w, 0)) break;
             mbar_drain(&sm.acc_full[acc.s], acc.ph, ab.limit);
             tc_fence_after();
-            const TileCoord tc = tile_coord(t, p);
-            const int r = tc.tm * BM + row_in_tile;
-            const int n_tile = tc.tn * C::BN;
-            float *crow = p.C + tc.q * p.sC + static_cast<long long>(r) * p.ldc;
+            const WorkUnit wu = work_unit(u, p);
+            const int r = wu.tc.tm * BM + row_in_tile;
+            const int n_tile = wu.tc.tn * C::BN;
+            float *crow = p.C + wu.tc.q * p.sC + static_cast<long long>(r) * p.ldc;
             const uint32_t tbase =
                 tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc.s * C::BN);
+            if (!C::SPLITK) {
 #pragma unroll 1
-            for (int c0 = 0; c0 < C::BN; c0 += 32) {
-                float v[32];
-                tmem_ld32(tbase + c0, v);  // all lanes take part, rows in range or not
-                if (r < p.M) {
-                    const int n0 = n_tile + c0;
-                    if (p.c_vec4 && n0 + 32 <= p.N) {
+                for (int c0 = 0; c0 < C::BN; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(tbase + c0, v);  // all lanes take part, rows in range or not
+                    store_c_chunk(p, crow, r, n_tile + c0, v);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.acc_empty[acc.s]);
+            } else {
+                // split-K: this slice's partial goes to the workspace, lane-interleaved
+                // (float4 v of lane l at v*32 + l of the warp's region)
+                constexpr long long REGION = (C::BN / 4) * 32;  // float4 per region
+                float4 *ws = reinterpret_cast<float4 *>(p.ws_part);
+                const long long slot0 = wu.tile * p.splits;
+                float4 *mine = ws + ((slot0 + wu.slice) * 4 + q) * REGION + lane;
+#pragma unroll 1
+                for (int c0 = 0; c0 < C::BN; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(tbase + c0, v);
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            float4 o = make_float4(p.alpha * v[j], p.alpha * v[j + 1],
-                                                   p.alpha * v[j + 2], p.alpha * v[j + 3]);
-                            float4 *dst = reinterpret_cast<float4 *>(crow + n0 + j);
-                            if (use_beta) {
-                                const float4 old = *dst;
-                                o.x = fmaf(p.beta, old.x, o.x);
-                                o.y = fmaf(p.beta, old.y, o.y);
-                                o.z = fmaf(p.beta, old.z, o.z);
-                                o.w = fmaf(p.beta, old.w, o.w);
-                            }
-                            *dst = o;
-                        }
-                    } else {
+                    for (int j = 0; j < 32; j += 4)
+                        mine[((c0 + j) / 4) * 32] = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                }
+                // the accumulator is no longer needed
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.acc_empty[acc.s]);
+                if (splitk_arrive(p.ws_ctr + wu.tile * 4 + q, p.splits, lane)) {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < C::BN; c0 += 32) {
+                        float v[32];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int n = n0 + j;
-                            if (n < p.N) {
-                                float o = p.alpha * v[j];
-                                if (use_beta) o = fmaf(p.beta, crow[n], o);
-                                crow[n] = o;
+                        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+                        for (int sl = 0; sl < p.splits; ++sl) {  // slice order: deterministic
+                            const float *src = reinterpret_cast<const float *>(
+                                ws + ((slot0 + sl) * 4 + q) * REGION + lane);
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4) {
+                                const float4 x = ldcg4(src + ((c0 + j) / 4) * 32 * 4);
+                                v[j] += x.x;
+                                v[j + 1] += x.y;
+                                v[j + 2] += x.z;
+                                v[j + 3] += x.w;
                             }
                         }
+                        store_c_chunk(p, crow, r, n_tile + c0, v);
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.acc_empty[acc.s]);
             acc.next();
         }
     }

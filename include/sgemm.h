@@ -42,6 +42,8 @@
 #ifndef SGEMM_GB300_H
 #define SGEMM_GB300_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -55,8 +57,9 @@ extern "C" {
 
 /* Contraction paths.
  *   FP32  : FP32 CUDA-core (FFMA) path; every product and sum in fp32.
- *   3XTF32: tensor-core path; each operand x is split into hi = tf32(x) and
- *           lo = tf32(x - hi) and the product is accumulated in fp32 as
+ *   3XTF32: tensor-core path; each operand x is split into hi = x with its 13
+ *           low mantissa bits cleared (a TF32 value) and lo = (x - hi)
+ *           likewise, and the product is accumulated in fp32 as
  *           lo*hi + hi*lo + hi*hi, which meets the FP32 accuracy bound.
  *   TF32  : one tensor-core pass on tf32-rounded operands (looser accuracy,
  *           max |C - C_ref| / (|alpha| |A||B| + |beta C|) <= 2e-3).
@@ -83,6 +86,32 @@ int sgemm_batched_ex(int mode, int M, int N, int K, float alpha, const float *A,
                      const float *B, int ldb, float beta, float *C, int ldc, int transA,
                      int transB, long long strideA, long long strideB, long long strideC, int Q,
                      void *stream);
+
+/* Split-K workspace.  When the output has fewer 128 x 128 tiles than the GPU
+ * has multiprocessors (small or skinny products, e.g. 1024^3 or the ragged
+ * 1000 x 1500 x 777 case), the library can cut K into slices computed in
+ * parallel and combine them -- the split-K scheme the SGEMM worklog sees
+ * cuBLAS use at 256^3 ("From 1% to 94% of cuBLAS", comparison across sizes).
+ * The partial sums need scratch memory, which the caller provides:
+ *
+ * sgemm_workspace_size returns the bytes of workspace the split path wants
+ * for this shape on the current device (0: the shape is not split, or the
+ * arguments are invalid, or there is no usable device).
+ *
+ * sgemm_batched_ex_ws is sgemm_batched_ex plus a DEVICE workspace owned by
+ * the caller: `workspace` must be 256-byte aligned when workspace_bytes > 0
+ * (else SGEMM_ERR_INVALID_ARG).  With workspace_bytes at least
+ * sgemm_workspace_size(...) the call may split K; with less (or NULL / 0)
+ * it runs unsplit, with the same results up to rounding.  Every slice's
+ * partial tile is stored in fp32 and the slices are summed in a fixed order,
+ * so repeated calls give identical bits.  The call zeroes the workspace's
+ * counter area on `stream` itself (no memset needed by the caller); the
+ * workspace must not be used by another call running at the same time. */
+size_t sgemm_workspace_size(int mode, int M, int N, int K, int Q);
+int sgemm_batched_ex_ws(int mode, int M, int N, int K, float alpha, const float *A, int lda,
+                        const float *B, int ldb, float beta, float *C, int ldc, int transA,
+                        int transB, long long strideA, long long strideB, long long strideC,
+                        int Q, void *workspace, size_t workspace_bytes, void *stream);
 
 /* Process-wide default path used by sgemm() and sgemm_batched().  Returns
  * SGEMM_ERR_INVALID_ARG for an unknown mode (DEFAULT is not a valid value

@@ -43,8 +43,10 @@ class Problem:
         self.sB = sB if strideB is None else strideB
         self.sC = sC
 
-    def run_gpu(self, mode: str, api: str = "ex", stream=None):
-        """Runs the library on the device and returns C as (Q, M, N) float32."""
+    def run_gpu(self, mode: str, api: str = "ex", stream=None, ws_bytes=None):
+        """Runs the library on the device and returns C as (Q, M, N) float32.
+        api="ws" passes a split-K workspace of ws_bytes (default: the size the
+        library asks for)."""
         import torch
         import dense_fp32_matrix_03_gb300 as lib
         dev = torch.device("cuda", 0)
@@ -54,7 +56,16 @@ class Problem:
         pa = A.data_ptr() + 4 * self.offA
         pb = B.data_ptr() + 4 * self.offB
         pc = C.data_ptr() + 4 * self.offC
-        if api == "sgemm":
+        if api == "ws":
+            if ws_bytes is None:
+                ws_bytes = lib.sgemm_workspace_size(mode, self.M, self.N, self.K, self.Q)
+            ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+            self.last_ws_bytes = ws_bytes
+            st = lib.sgemm_batched_ex_ws(mode, self.M, self.N, self.K, self.alpha, pa, self.lda,
+                                         pb, self.ldb, self.beta, pc, self.ldc, self.transA,
+                                         self.transB, self.sA, self.sB, self.sC, self.Q, ws,
+                                         ws_bytes, stream)
+        elif api == "sgemm":
             assert self.Q == 1 and not self.transA and not self.transB
             assert lib.sgemm_get_default_mode() == lib.MODES[mode]
             st = lib.sgemm(self.M, self.N, self.K, self.alpha, pa, self.lda, pb, self.ldb,

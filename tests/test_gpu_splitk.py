@@ -1,0 +1,99 @@
+"""GPU parity of the split-K path (sgemm_batched_ex_ws): shapes with fewer
+output tiles than multiprocessors are cut along K, each slice's partial tile
+goes through the caller's workspace, and the last slice of every region sums
+them in slice order.  Checked against the fp64 oracle like every other path."""
+import numpy as np
+import pytest
+
+import workloads
+from _helpers import TOL, Problem
+
+pytestmark = pytest.mark.gpu
+
+MODES = ["fp32", "3xtf32", "tf32"]
+SPLIT_SHAPES = [  # (M, N, K, Q, transA, transB, alpha, beta): all split on every path
+    (1024, 1024, 1024, 1, 0, 0, 1.0, 0.0),
+    (600, 700, 777, 1, 0, 0, 1.0, -2.0),     # ragged, lda not TMA-describable
+    (256, 256, 600, 1, 0, 0, 1.5, 0.5),
+    (128, 128, 1024, 1, 0, 0, 1.0, 0.0),
+    (512, 512, 512, 1, 1, 1, 0.5, 1.0),
+    (300, 200, 2000, 1, 0, 1, 1.0, 0.25),    # skinny output, long K
+    (200, 150, 600, 3, 1, 0, -1.0, 0.5),     # batched
+    (1, 7, 4000, 1, 0, 0, 1.0, 0.0),         # a single row
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu_ready():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import dense_fp32_matrix_03_gb300 as lib
+    lib.load()
+
+
+def make_problem(shape, seed):
+    M, N, K, Q, tA, tB, alpha, beta = shape
+    A, B, C0 = workloads.random_inputs(M, N, K, Q=Q, seed=seed)
+    return Problem(A, B, C0, alpha, beta, transA=tA, transB=tB)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("shape", SPLIT_SHAPES)
+def test_split_k_parity(oracle_mod, mode, shape):
+    import dense_fp32_matrix_03_gb300 as lib
+    M, N, K, Q = shape[:4]
+    assert lib.sgemm_workspace_size(mode, M, N, K, Q) > 0, "shape expected to split"
+    prob = make_problem(shape, seed=M + N + K)
+    C = prob.run_gpu(mode, api="ws")
+    Cref, D = prob.oracle(oracle_mod)
+    err = oracle_mod.max_rel_err(C, Cref, D)
+    assert err <= TOL[mode], f"{mode} {shape}: max rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_split_k_integer_bit_exact(oracle_mod, mode):
+    A, B, C0 = workloads.integer_inputs(700, 900, 1500, seed=5)
+    prob = Problem(A, B, C0, 2.0, -1.0)
+    C = prob.run_gpu(mode, api="ws")
+    Cref, _ = prob.oracle(oracle_mod)
+    assert np.array_equal(C.astype(np.float64), Cref)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_split_k_is_deterministic(mode):
+    prob = make_problem((600, 700, 777, 1, 0, 0, 1.0, 0.5), seed=9)
+    C1 = prob.run_gpu(mode, api="ws")
+    C2 = prob.run_gpu(mode, api="ws")
+    assert np.array_equal(C1, C2)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_small_or_missing_workspace_runs_unsplit(oracle_mod, mode):
+    prob = make_problem((1024, 1024, 1024, 1, 0, 1, 1.0, 0.0), seed=3)
+    Cref, D = prob.oracle(oracle_mod)
+    for nbytes in (0, 1024):
+        C = prob.run_gpu(mode, api="ws", ws_bytes=nbytes)
+        assert oracle_mod.max_rel_err(C, Cref, D) <= TOL[mode]
+
+
+def test_workspace_size_query():
+    import dense_fp32_matrix_03_gb300 as lib
+    assert lib.sgemm_workspace_size("fp32", 4092, 4092, 4092, 1) == 0    # fills the GPU already
+    assert lib.sgemm_workspace_size("fp32", 1024, 1024, 128, 1) > 0     # 4 k-blocks: 2 slices
+    assert lib.sgemm_workspace_size("3xtf32", 1024, 1024, 128, 1) == 0  # tensor path: >= 8 per slice
+    assert lib.sgemm_workspace_size("fp32", 1000, 1500, 777, 1) == 0    # 96 tiles: no room to split
+    assert lib.sgemm_workspace_size("fp32", 1024, 1024, 32, 1) == 0      # one k-block: no split
+    assert lib.sgemm_workspace_size("fp32", 0, 10, 10, 1) == 0
+    assert lib.sgemm_workspace_size(7, 100, 100, 100, 1) == 0
+
+
+def test_misaligned_workspace_is_rejected():
+    import torch
+    import dense_fp32_matrix_03_gb300 as lib
+    a = torch.ones(64, 64, device="cuda")
+    c = torch.zeros(64, 64, device="cuda")
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    st = lib.sgemm_batched_ex_ws("fp32", 64, 64, 64, 1.0, a, 64, a, 64, 0.0, c, 64, 0, 0, 0, 0, 0,
+                                 1, ws.data_ptr() + 16, 4096)
+    assert st == lib.SGEMM_ERR_INVALID_ARG
