@@ -24,6 +24,7 @@ SGEMM_ERR_INVALID_ARG = 1
 SGEMM_ERR_UNSUPPORTED = 2
 SGEMM_ERR_LAUNCH = 3
 SGEMM_ERR_TIMEOUT = 4
+SGEMM_ERR_SCRATCH_LIMIT = 5
 
 SGEMM_MODE_DEFAULT = -1
 SGEMM_MODE_FP32 = 0
@@ -42,6 +43,8 @@ SIGNATURES = {
     "sgemm_workspace_size": (ctypes.c_size_t, [_i, _i, _i, _i, _i]),
     "sgemm_batched_ex_ws": (_i, [_i, _i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _i, _i, _ll, _ll,
                                  _ll, _i, _p, ctypes.c_size_t, _p]),
+    "sgemm_batched_ex_noalloc": (_i, [_i, _i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _i, _i, _ll,
+                                      _ll, _ll, _i, _p]),
     "sgemm_set_default_mode": (_i, [_i]),
     "sgemm_get_default_mode": (_i, []),
     "sgemm_status_string": (ctypes.c_char_p, [_i]),
@@ -151,6 +154,17 @@ def sgemm_batched_ex_ws(mode, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, tran
                                     _ptr(C), ldc, int(transA), int(transB), strideA, strideB,
                                     strideC, Q, _ptr(workspace), int(workspace_bytes),
                                     _stream(stream))
+
+
+def sgemm_batched_ex_noalloc(mode, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, transA, transB,
+                             strideA, strideB, strideC, Q, stream=None) -> int:
+    """Split-K GEMM whose scratch is a fixed array inside the library: for
+    callers that may not allocate device memory (see include/sgemm.h)."""
+    if isinstance(mode, str):
+        mode = MODES[mode]
+    return _lib.sgemm_batched_ex_noalloc(mode, M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta,
+                                         _ptr(C), ldc, int(transA), int(transB), strideA, strideB,
+                                         strideC, Q, _stream(stream))
 
 
 def sgemm_set_default_mode(mode) -> int:

@@ -353,6 +353,8 @@ const char *sgemm_status_string(int status)
     case SGEMM_ERR_UNSUPPORTED: return "unsupported: needs a compute capability 10.3 GPU";
     case SGEMM_ERR_LAUNCH: return "CUDA launch or runtime error";
     case SGEMM_ERR_TIMEOUT: return "a kernel's bounded wait ran out (device status word)";
+    case SGEMM_ERR_SCRATCH_LIMIT:
+        return "the shape needs more split-K scratch than the built-in array holds";
     default: return "unknown status";
     }
 }

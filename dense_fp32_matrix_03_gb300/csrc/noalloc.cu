@@ -1,0 +1,76 @@
+// noalloc.cu -- the split-K GEMM for callers that cannot allocate device
+// memory.
+//
+// sgemm_batched_ex_ws needs a device workspace for its partial tiles.  Some
+// callers cannot provide one: code that runs where cudaMalloc is not allowed
+// or not wanted (inside a host callback or another library's critical
+// section, under a memory pool that may not grow, in a plugin handed only
+// the input and output pointers).  sgemm_batched_ex_noalloc gives them the
+// same computation with the scratch taken from a fixed array that is part of
+// the library image: every GPU that loads the library holds kScratchBytes
+// of it until the process exits, and no call allocates or frees anything.
+#include <cstddef>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/sgemm.h"
+
+namespace {
+
+// Enough for the split-K workspace of any shape on a GPU with up to ~190
+// multiprocessors (at most one 128 x 128 fp32 partial tile per
+// multiprocessor, plus the arrival counters).
+constexpr size_t kScratchBytes = static_cast<size_t>(12) << 20;
+
+// The scratch: shared by every call on a device, keeps the last call's
+// contents between calls.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void *g_scratch_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+bool g_scratch_ready[kMaxDevices];
+
+// Device address of the scratch array on the current device.  The host-side
+// name g_noalloc_scratch is only a stand-in; the address a kernel may use is
+// obtained once per device, with that device current.
+int scratch_address(void **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return SGEMM_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_scratch_ready[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return SGEMM_ERR_LAUNCH;
+        g_scratch_addr[dev] = p;
+        g_scratch_ready[dev] = true;
+    }
+    *out = g_scratch_addr[dev];
+    return SGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" int sgemm_batched_ex_noalloc(int mode, int M, int N, int K, float alpha,
+                                        const float *A, int lda, const float *B, int ldb,
+                                        float beta, float *C, int ldc, int transA, int transB,
+                                        long long strideA, long long strideB, long long strideC,
+                                        int Q, void *stream)
+{
+    // what the split path would use for this shape (0 when it does not split)
+    const size_t need = sgemm_workspace_size(mode, M, N, K, Q);
+    if (need > kScratchBytes) return SGEMM_ERR_SCRATCH_LIMIT;
+    void *ws = nullptr;
+    if (need > 0) {
+        const int rc = scratch_address(&ws);
+        if (rc != SGEMM_OK) return rc;
+    }
+    // The workspace path clears the counter area of the scratch on `stream`
+    // before its kernel, so what an earlier call left there does not matter.
+    return sgemm_batched_ex_ws(mode, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, transA, transB,
+                               strideA, strideB, strideC, Q, ws, ws ? kScratchBytes : 0, stream);
+}

@@ -54,6 +54,7 @@ extern "C" {
 #define SGEMM_ERR_UNSUPPORTED 2 /* valid call this build cannot run (e.g. no sm_103 GPU)   */
 #define SGEMM_ERR_LAUNCH 3      /* the CUDA runtime refused a launch or attribute call    */
 #define SGEMM_ERR_TIMEOUT 4     /* a kernel's bounded internal wait ran out (device word) */
+#define SGEMM_ERR_SCRATCH_LIMIT 5 /* sgemm_batched_ex_noalloc: shape needs more than its scratch */
 
 /* Contraction paths.
  *   FP32  : FP32 CUDA-core (FFMA) path; every product and sum in fp32.
@@ -112,6 +113,32 @@ int sgemm_batched_ex_ws(int mode, int M, int N, int K, float alpha, const float 
                         const float *B, int ldb, float beta, float *C, int ldc, int transA,
                         int transB, long long strideA, long long strideB, long long strideC,
                         int Q, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Split-K for callers that cannot allocate device memory.  (No counterpart on
+ * the pages: an addition of this library.)
+ *
+ * Same arguments and results as sgemm_batched_ex_ws, without the workspace:
+ * the partial tiles live in a fixed 12 MB scratch array inside the library
+ * image.  For code that may not call cudaMalloc or may not grow a memory pool
+ * at the point where it multiplies (a host callback, another library's
+ * critical section, a plugin that is handed only its input and output
+ * buffers).  The function allocates and frees nothing.
+ *  - Every GPU that loads the library holds the 12 MB until the process exits.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the array and it keeps the last call's
+ *    contents; the call clears what must start at zero itself.  Calls whose
+ *    kernels overlap on the GPU (different streams, or another thread) race
+ *    on the array: serialise them.
+ *  - A shape whose split workspace (sgemm_workspace_size) exceeds 12 MB
+ *    returns SGEMM_ERR_SCRATCH_LIMIT and launches nothing; that cannot
+ *    happen on a GPU with at most ~190 multiprocessors.  Shapes that do not
+ *    split run exactly as sgemm_batched_ex. */
+int sgemm_batched_ex_noalloc(int mode, int M, int N, int K, float alpha, const float *A, int lda,
+                             const float *B, int ldb, float beta, float *C, int ldc, int transA,
+                             int transB, long long strideA, long long strideB, long long strideC,
+                             int Q, void *stream);
 
 /* Process-wide default path used by sgemm() and sgemm_batched().  Returns
  * SGEMM_ERR_INVALID_ARG for an unknown mode (DEFAULT is not a valid value

@@ -65,6 +65,11 @@ class Problem:
                                          pb, self.ldb, self.beta, pc, self.ldc, self.transA,
                                          self.transB, self.sA, self.sB, self.sC, self.Q, ws,
                                          ws_bytes, stream)
+        elif api == "noalloc":
+            st = lib.sgemm_batched_ex_noalloc(mode, self.M, self.N, self.K, self.alpha, pa,
+                                              self.lda, pb, self.ldb, self.beta, pc, self.ldc,
+                                              self.transA, self.transB, self.sA, self.sB,
+                                              self.sC, self.Q, stream)
         elif api == "sgemm":
             assert self.Q == 1 and not self.transA and not self.transB
             assert lib.sgemm_get_default_mode() == lib.MODES[mode]
