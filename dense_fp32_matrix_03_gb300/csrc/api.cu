@@ -159,14 +159,14 @@ bool encode_operand(CUtensorMap *map, const float *base, bool kin, long long row
     return r == CUDA_SUCCESS;
 }
 
-int min_slice_kblocks(int mode) { return mode == SGEMM_MODE_FP32 ? 2 : 8; }
+int min_slice_k(int mode) { return mode == SGEMM_MODE_FP32 ? 64 : 256; }
 
-int choose_splits(long long num_tiles, int k_blocks, int num_sms, int mode)
+int choose_splits(long long num_tiles, int K, int num_sms, int mode)
 {
     // as many slices as keep every unit in one wave (units <= multiprocessors)
     if (num_tiles <= 0 || 2 * num_tiles > num_sms) return 1;
     long long s = num_sms / num_tiles;
-    const long long by_k = k_blocks / min_slice_kblocks(mode);
+    const long long by_k = K / min_slice_k(mode);
     if (s > by_k) s = by_k;
     if (s > kMaxSplits) s = kMaxSplits;
     return s < 2 ? 1 : static_cast<int>(s);
@@ -186,7 +186,7 @@ int plan_splits(Plan &plan)
     p.splits = 1;
     p.ws_part = nullptr;
     p.ws_ctr = nullptr;
-    const int s = plan.ws ? choose_splits(p.num_tiles, p.k_blocks, plan.num_sms, plan.mode) : 1;
+    const int s = plan.ws ? choose_splits(p.num_tiles, p.K, plan.num_sms, plan.mode) : 1;
     const size_t need = splitk_workspace_bytes(p.num_tiles, s);
     if (s > 1 && need <= plan.ws_bytes) {
         const size_t ctr = (static_cast<size_t>(p.num_tiles) * kSplitRegions * sizeof(unsigned int) +
@@ -331,8 +331,7 @@ size_t sgemm_workspace_size(int mode, int M, int N, int K, int Q)
     if (di == nullptr) return 0;
     const long long tiles = static_cast<long long>(Q) * ((M + kSplitTile - 1) / kSplitTile) *
                             ((N + kSplitTile - 1) / kSplitTile);
-    const int k_blocks = (K + kTileK - 1) / kTileK;
-    return splitk_workspace_bytes(tiles, choose_splits(tiles, k_blocks, di->num_sms, mode));
+    return splitk_workspace_bytes(tiles, choose_splits(tiles, K, di->num_sms, mode));
 }
 
 int sgemm_set_default_mode(int mode)

@@ -23,19 +23,21 @@ struct Plan {
     size_t ws_bytes;
 };
 
-// Split-K plan shared by both kernels (128 x 128 output tiles, 32-wide
-// k-blocks).  A grid with at most half as many tiles as multiprocessors is
-// cut along K into `splits` slices, as many as keep all work units in one
-// wave, each at least min_slice_kblocks(mode) long: 2 for the FP32 path, 8
-// for the tensor-core paths, whose per-unit pipeline start-up (copy, split,
-// MMA, TMEM read-back) is longer (measured on GB300: shorter slices made
-// 128^3..512^3 slower).  The workspace holds one arrival counter per tile
-// region and one fp32 partial tile per (tile, slice).
+// Split-K plan shared by both kernels (128 x 128 output tiles).  A grid with
+// at most half as many tiles as multiprocessors is cut along K into `splits`
+// slices, as many as keep all work units in one wave, each at least
+// min_slice_k(mode) long: 64 for the FP32 path, 256 for the tensor-core
+// paths, whose per-unit pipeline start-up (copy, split, MMA, TMEM read-back)
+// is longer (measured on GB300: shorter slices made 128^3..512^3 slower).
+// The slices are whole k-blocks of the kernel that runs (each kernel's
+// k-block is at most the minimum slice, so no slice is empty).  The
+// workspace holds one arrival counter per tile region and one fp32 partial
+// tile per (tile, slice).
 constexpr int kSplitTile = 128;            // output tile edge of both paths
 constexpr int kSplitRegions = 8;           // counters per tile (>= warps writing a tile)
 constexpr int kMaxSplits = 16;
-int min_slice_kblocks(int mode);
-int choose_splits(long long num_tiles, int k_blocks, int num_sms, int mode);
+int min_slice_k(int mode);
+int choose_splits(long long num_tiles, int K, int num_sms, int mode);
 size_t splitk_workspace_bytes(long long num_tiles, int splits);
 // Fills p.splits / num_units / ws_* for the launch: splits if the plan's
 // workspace is large enough (and clears its counters on the stream), else

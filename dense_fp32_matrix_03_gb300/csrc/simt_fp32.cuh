@@ -8,8 +8,9 @@
 // swizzled conflict-free layouts, hardware copy engines, warp
 // specialisation), built for sm_103a:
 //
-//  * one producer warp fills a STAGES-deep ring of shared-memory stages.
-//    With TMA it issues two tiled tensor loads per stage (out-of-bounds rows,
+//  * lane 0 of warp 0 fills a STAGES-deep ring of shared-memory stages,
+//    each SUBS x 32 deep in K.  With TMA it issues two tiled tensor loads per
+//    sub-block (out-of-bounds rows,
 //    columns and the K tail are zero-filled by the copy engine, so no mask is
 //    evaluated in the main loop); for operands TMA cannot describe (a row
 //    pitch that is not a multiple of 16 bytes, an unaligned base) it copies
@@ -25,6 +26,8 @@
 //    grid and each lane accumulates (WM/32) x (WN/16) sub-blocks of 4 x 4
 //    outputs in registers (the page's kernel 10 warptiling).  K is walked in
 //    groups of 4 so that one 128-bit load of a K-inner row yields four k.
+//    The FMAs are issued two per instruction (fma.rn.f32x2) where one operand
+//    arrives in adjacent registers (see Acc below).
 //  * tiles are visited in a persistent, grouped order (one CTA per SM).
 //  * the epilogue fuses alpha and beta: C is read only when beta != 0.
 #pragma once
@@ -35,12 +38,18 @@
 
 namespace sg {
 
-constexpr int kBK = 32;  // K per pipeline stage (one 128-byte swizzle row of fp32)
+// K per sub-block: one 128-byte swizzle row of fp32, the widest box a
+// 128-byte-swizzled TMA copy takes along its contiguous dimension.
+constexpr int kSubK = 32;
 
 
-template <int BM_, int BN_, int WM_, int WN_, int STAGES_>
+// A stage holds SUBS sub-blocks of K (BK = 32 * SUBS): all of A's
+// sub-blocks (each BM x 32), then all of B's.  More sub-blocks per stage
+// means fewer barrier round trips per FFMA.
+template <int BM_, int BN_, int WM_, int WN_, int STAGES_, int SUBS_ = 1>
 struct SimtCfg {
     static constexpr int BM = BM_, BN = BN_, WM = WM_, WN = WN_, STAGES = STAGES_;
+    static constexpr int SUBS = SUBS_, BK = kSubK * SUBS_;
     static constexpr int WARPS_M = BM / WM, WARPS_N = BN / WN;
     static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
     // The consumer warps issue the copies themselves (no producer warp), so
@@ -48,7 +57,8 @@ struct SimtCfg {
     static constexpr int THREADS = CONSUMER_WARPS * 32;
     static constexpr int WMITER = WM / 32, WNITER = WN / 16;
     static constexpr int TM = 4 * WMITER, TN = 4 * WNITER;
-    static constexpr int A_BYTES = BM * kBK * 4, B_BYTES = BN * kBK * 4;
+    static constexpr int A_SUB = BM * kSubK * 4, B_SUB = BN * kSubK * 4;
+    static constexpr int A_BYTES = SUBS * A_SUB, B_BYTES = SUBS * B_SUB;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int BAR_BYTES = 2 * STAGES * 8 + 16;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
@@ -139,13 +149,17 @@ struct TmaIssuer {
             if (!mbar_wait(&empty[s], pos.phase ^ 1u, ab, kStatusWaitEmpty)) return false;
             uint8_t *sa = smem + s * Cfg::STAGE_BYTES;
             uint8_t *sb = sa + Cfg::A_BYTES;
-            const int m0 = pos.tc.tm * Cfg::BM, n0 = pos.tc.tn * Cfg::BN, k0 = pos.kb * kBK;
+            const int m0 = pos.tc.tm * Cfg::BM, n0 = pos.tc.tn * Cfg::BN;
             const int qa = pos.tc.q * p->a_q_step, qb = pos.tc.q * p->b_q_step;
             mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
-            if (A_KIN) tma_load_3d(sa, tmA, &full[s], k0, m0, qa);
-            else       tma_load_3d(sa, tmA, &full[s], m0, k0, qa);
-            if (B_KIN) tma_load_3d(sb, tmB, &full[s], k0, n0, qb);
-            else       tma_load_3d(sb, tmB, &full[s], n0, k0, qb);
+#pragma unroll
+            for (int sub = 0; sub < Cfg::SUBS; ++sub) {
+                const int k0 = pos.kb * Cfg::BK + sub * kSubK;
+                if (A_KIN) tma_load_3d(sa + sub * Cfg::A_SUB, tmA, &full[s], k0, m0, qa);
+                else       tma_load_3d(sa + sub * Cfg::A_SUB, tmA, &full[s], m0, k0, qa);
+                if (B_KIN) tma_load_3d(sb + sub * Cfg::B_SUB, tmB, &full[s], k0, n0, qb);
+                else       tma_load_3d(sb + sub * Cfg::B_SUB, tmB, &full[s], n0, k0, qb);
+            }
             ++issued;
             pos.template next<Cfg::STAGES>(*p);
         }
@@ -206,14 +220,17 @@ struct CpAsyncIssuer {
             if (!warp_wait(&empty[s], pos.phase ^ 1u, ab, kStatusWaitEmpty, lane)) return false;
             uint8_t *sa = smem + s * Cfg::STAGE_BYTES;
             uint8_t *sb = sa + Cfg::A_BYTES;
-            const int k0 = pos.kb * kBK;
             const TileCoord &tc = pos.tc;
-            cp_async_tile<Cfg::BM, A_KIN, EVEN_K>(sa, p->A + tc.q * p->sA, p->lda,
-                                                  tc.tm * Cfg::BM, p->M, k0, p->K,
-                                                  p->a_vec4 != 0, tid, Cfg::THREADS);
-            cp_async_tile<Cfg::BN, B_KIN, EVEN_K>(sb, p->B + tc.q * p->sB, p->ldb,
-                                                  tc.tn * Cfg::BN, p->N, k0, p->K,
-                                                  p->b_vec4 != 0, tid, Cfg::THREADS);
+#pragma unroll
+            for (int sub = 0; sub < Cfg::SUBS; ++sub) {
+                const int k0 = pos.kb * Cfg::BK + sub * kSubK;
+                cp_async_tile<Cfg::BM, A_KIN, EVEN_K>(sa + sub * Cfg::A_SUB, p->A + tc.q * p->sA,
+                                                      p->lda, tc.tm * Cfg::BM, p->M, k0, p->K,
+                                                      p->a_vec4 != 0, tid, Cfg::THREADS);
+                cp_async_tile<Cfg::BN, B_KIN, EVEN_K>(sb + sub * Cfg::B_SUB, p->B + tc.q * p->sB,
+                                                      p->ldb, tc.tn * Cfg::BN, p->N, k0, p->K,
+                                                      p->b_vec4 != 0, tid, Cfg::THREADS);
+            }
             cp_async_arrive_noinc(&full[s]);
             ++issued;
             pos.template next<Cfg::STAGES>(*p);
@@ -357,16 +374,114 @@ __device__ __forceinline__ void load_frag(Frag<Cfg> &f, uint32_t a_base, uint32_
     }
 }
 
-template <class Cfg>
-__device__ __forceinline__ void fma_frag(float (&acc)[Cfg::TM][Cfg::TN], const Frag<Cfg> &f)
+// ------------------------------------------------------- accumulators
+//
+// sm_100-class SMs execute two fp32 FMAs per lane in one instruction
+// (fma.rn.f32x2 on 64-bit register pairs).  Each of the two products is
+// rounded exactly as a scalar fmaf would round it, so results are the same
+// as with scalar FFMA; what changes is that one issue slot now carries two
+// FMAs, leaving room for the shared loads.  Pairs are taken along the
+// dimension whose fragment values arrive adjacent in registers (one 128-bit
+// shared load gives four consecutive columns of an N-inner B, or four
+// consecutive rows of an M-inner A); the other operand is broadcast into
+// both halves.  When both operands are K-inner, no dimension pairs for free.
+enum PairDim { kPairNone = 0, kPairJ = 1, kPairI = 2 };
+#ifndef SG_SIMT_FFMA2
+#define SG_SIMT_FFMA2 1
+#endif
+#ifndef SG_SIMT_NT_PAIR
+#define SG_SIMT_NT_PAIR 0
+#endif
+template <bool A_KIN, bool B_KIN>
+constexpr int pair_dim()
 {
-#pragma unroll
-    for (int kk = 0; kk < kKStep; ++kk)
-#pragma unroll
-        for (int i = 0; i < Cfg::TM; ++i)
-#pragma unroll
-            for (int j = 0; j < Cfg::TN; ++j) acc[i][j] = fmaf(f.a[kk][i], f.b[kk][j], acc[i][j]);
+    return !SG_SIMT_FFMA2 ? kPairNone : !B_KIN ? kPairJ : !A_KIN ? kPairI : SG_SIMT_NT_PAIR;
 }
+
+__device__ __forceinline__ uint64_t pack2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// d.lo = fma(a.lo, b.lo, d.lo), d.hi = fma(a.hi, b.hi, d.hi), each rounded once.
+__device__ __forceinline__ void ffma2(uint64_t &d, uint64_t a, uint64_t b)
+{
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
+// TM x TN fp32 accumulators of one lane, stored as PD says.
+template <class Cfg, int PD>
+struct Acc {
+    static constexpr int TM = Cfg::TM, TN = Cfg::TN;
+    static constexpr int R = PD == kPairI ? TM / 2 : TM;
+    static constexpr int C = PD == kPairJ ? TN / 2 : TN;
+    using T = typename std::conditional<PD == kPairNone, float, uint64_t>::type;
+    T v[R][C];
+
+    __device__ __forceinline__ void zero()
+    {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int c = 0; c < C; ++c) v[r][c] = T(0);
+    }
+
+    __device__ __forceinline__ void fma(const Frag<Cfg> &f)
+    {
+#pragma unroll
+        for (int kk = 0; kk < kKStep; ++kk) {
+            if constexpr (PD == kPairNone) {
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+#pragma unroll
+                    for (int j = 0; j < TN; ++j) v[i][j] = fmaf(f.a[kk][i], f.b[kk][j], v[i][j]);
+            } else if constexpr (PD == kPairJ) {
+                uint64_t bp[C];
+#pragma unroll
+                for (int c = 0; c < C; ++c) bp[c] = pack2(f.b[kk][2 * c], f.b[kk][2 * c + 1]);
+#pragma unroll
+                for (int i = 0; i < TM; ++i) {
+                    const uint64_t ab = pack2(f.a[kk][i], f.a[kk][i]);
+#pragma unroll
+                    for (int c = 0; c < C; ++c) ffma2(v[i][c], ab, bp[c]);
+                }
+            } else {
+                uint64_t ap[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) ap[r] = pack2(f.a[kk][2 * r], f.a[kk][2 * r + 1]);
+#pragma unroll
+                for (int j = 0; j < TN; ++j) {
+                    const uint64_t bb = pack2(f.b[kk][j], f.b[kk][j]);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) ffma2(v[r][j], ap[r], bb);
+                }
+            }
+        }
+    }
+
+    __device__ __forceinline__ void to_float(float (&out)[TM][TN]) const
+    {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int c = 0; c < C; ++c) {
+                if constexpr (PD == kPairNone) {
+                    out[r][c] = v[r][c];
+                } else if constexpr (PD == kPairJ) {
+                    unpack2(v[r][c], out[r][2 * c], out[r][2 * c + 1]);
+                } else {
+                    unpack2(v[r][c], out[2 * r][c], out[2 * r + 1][c]);
+                }
+            }
+    }
+};
 
 // Split-K hand-off of one warp's accumulators (its region of the tile).
 // Partials are stored lane-interleaved (float4 v of lane l at v*32 + l within
@@ -433,7 +548,7 @@ __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem
 {
     constexpr int WMITER = Cfg::WMITER, WNITER = Cfg::WNITER, TM = Cfg::TM, TN = Cfg::TN;
     constexpr int BM = Cfg::BM, BN = Cfg::BN;
-    constexpr int GROUPS = kBK / kKStep;
+    constexpr int GROUPS = kSubK / kKStep;  // k-steps per sub-block
     const int wm0 = (cw / Cfg::WARPS_N) * Cfg::WM;
     const int wn0 = (cw % Cfg::WARPS_N) * Cfg::WN;
     const int lr = lane >> 2, lc = lane & 3;
@@ -466,20 +581,20 @@ __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem
     for (long long u = blockIdx.x; u < p.num_units; u += gridDim.x) {
         const WorkUnit wu = work_unit(u, p);
         const TileCoord &tc = wu.tc;
-        float acc[TM][TN];
-#pragma unroll
-        for (int i = 0; i < TM; ++i)
-#pragma unroll
-            for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+        Acc<Cfg, pair_dim<A_KIN, B_KIN>()> accp;
+        accp.zero();
 
         for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb, ++it) {
             if (!wait_full(cs, cph)) return;
             const uint32_t stage = stage_addr(cs);
 #pragma unroll kGroupUnroll
-            for (int g = 0; g < GROUPS; ++g) {
+            for (int g = 0; g < Cfg::SUBS * GROUPS; ++g) {
+                const int sub = g / GROUPS;
                 Frag<Cfg> f;
-                load_frag<Cfg, A_KIN, B_KIN>(f, stage + a_lane, stage + b_lane, a_key, b_key, g);
-                fma_frag<Cfg>(acc, f);
+                load_frag<Cfg, A_KIN, B_KIN>(f, stage + sub * Cfg::A_SUB + a_lane,
+                                             stage + sub * Cfg::B_SUB + b_lane, a_key, b_key,
+                                             g % GROUPS);
+                accp.fma(f);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[cs]);
@@ -490,6 +605,8 @@ __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem
             }
         }
 
+        float acc[TM][TN];
+        accp.to_float(acc);
         if (SPLITK && !splitk_exchange<Cfg>(p, wu, cw, lane, acc)) continue;
 
         // ---- epilogue: C = alpha * acc + beta * C, masked at the M/N edges
