@@ -368,11 +368,14 @@ def main():
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
     flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_call = 1
+    # split-K workspace (the last, partial wave of tiles is cut along K),
+    # allocated once, outside the timed region, like a library handle's
+    ws_bytes, ws = workspace(lib, mode, M, N, K, 1, dev)
+    launches_per_call = 2 if ws_bytes else 1   # the GEMM kernel (+ the split-K fix-up)
 
     def call():
-        lib.check(lib.sgemm_batched_ex(mode, M, N, K, alpha, A, K, B, N, beta, C, N, 0, 0, 0, 0,
-                                       0, 1, stream))
+        lib.check(lib.sgemm_batched_ex_ws(mode, M, N, K, alpha, A, K, B, N, beta, C, N, 0, 0, 0,
+                                          0, 0, 1, ws, ws_bytes, stream))
 
     gpu_id = None
     uuid = getattr(props, "uuid", None)
@@ -423,8 +426,8 @@ def main():
         def e2e_call():
             dA.copy_(hA, non_blocking=True)
             dB.copy_(hB, non_blocking=True)
-            lib.check(lib.sgemm_batched_ex(mode, M, N, K, alpha, dA, K, dB, N, beta, dC, N, 0, 0,
-                                           0, 0, 0, 1, stream))
+            lib.check(lib.sgemm_batched_ex_ws(mode, M, N, K, alpha, dA, K, dB, N, beta, dC, N, 0,
+                                              0, 0, 0, 0, 1, ws, ws_bytes, stream))
             hC.copy_(dC, non_blocking=True)
         e_steps = max(3, min(args.steps, 10))
         et = time_calls(e2e_call, e_steps, 3, stream, flush)
@@ -449,6 +452,7 @@ def main():
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "alpha": alpha,
                        "beta": beta, "mode": mode, "inputs": "normal(0,1) seed 2",
+                       "entry": "sgemm_batched_ex_ws", "workspace_bytes": ws_bytes,
                        "l2": f"flushed before every timed step ({2 * l2 >> 20} MB write)",
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline,
@@ -464,6 +468,13 @@ def main():
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def workspace(lib, mode, M, N, K, Q, dev):
+    """The split-K workspace the library asks for this call: (bytes, tensor)."""
+    import torch
+    ws_bytes = lib.sgemm_workspace_size(mode, M, N, K, Q)
+    return ws_bytes, torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
 
 
 def extra_figures(lib, default_mode, dev, stream, flush, num_sms, peaks, peak_src):
@@ -483,9 +494,11 @@ def extra_figures(lib, default_mode, dev, stream, flush, num_sms, peaks, peak_sr
             out["paths"][mode] = {"status": lib.sgemm_status_string(st)}
             continue
 
-        def call(mode=mode):
-            lib.check(lib.sgemm_batched_ex(mode, M, N, K, 1.0, A, K, B, N, 0.0, C, N, 0, 0, 0, 0,
-                                           0, 1, stream))
+        ws_bytes, ws = workspace(lib, mode, M, N, K, 1, dev)
+
+        def call(mode=mode, ws=ws, ws_bytes=ws_bytes):
+            lib.check(lib.sgemm_batched_ex_ws(mode, M, N, K, 1.0, A, K, B, N, 0.0, C, N, 0, 0, 0,
+                                              0, 0, 1, ws, ws_bytes, stream))
         t = statistics.median(time_calls(call, 10, 3, stream, flush))
         tf = gemm_flops(M, N, K) / (t / 1e3) / 1e12
         bound, peak, note = roofline_peak(mode, num_sms, peaks, peak_src)
@@ -498,11 +511,12 @@ def extra_figures(lib, default_mode, dev, stream, flush, num_sms, peaks, peak_sr
     Bn = torch.from_numpy(wb["B"]).to(dev)                             # Q x K x N
     Bt = torch.from_numpy(wb["B"].transpose(0, 2, 1).copy()).to(dev)   # Q x N x K
     C = torch.from_numpy(wb["C0"]).to(dev)
+    ws_bytes, ws = workspace(lib, default_mode, M, N, K, Q, dev)
     for tB, Bd, ldb in ((1, Bt, K), (0, Bn, N)):
         def call(tB=tB, Bd=Bd, ldb=ldb):
-            lib.check(lib.sgemm_batched_ex(default_mode, M, N, K, wb["alpha"], A, K, Bd, ldb,
-                                           wb["betas"][0], C, N, 0, tB, M * K, K * N, M * N, Q,
-                                           stream))
+            lib.check(lib.sgemm_batched_ex_ws(default_mode, M, N, K, wb["alpha"], A, K, Bd, ldb,
+                                              wb["betas"][0], C, N, 0, tB, M * K, K * N, M * N, Q,
+                                              ws, ws_bytes, stream))
         t = statistics.median(time_calls(call, 10, 3, stream, flush))
         out["bmm"][f"transB={tB}"] = {"tflops": gemm_flops(M, N, K, Q) / (t / 1e3) / 1e12,
                                       "ms": t, "mode": default_mode}

@@ -92,6 +92,61 @@ __global__ void scale_c_kernel(float *C, int M, int N, long long ldc, long long 
     }
 }
 
+// Split-K fix-up: for every split tile, sums its slices' partial tiles in
+// slice order 0, 1, ..., splits-1 and writes C = alpha * sum + beta * C
+// (C not read when beta == 0), masked at the M/N edges: the same result for
+// the same inputs whatever order the slices ran in.  One thread per four
+// consecutive columns of a tile row, grid-stride.  It runs after the GEMM
+// kernel on the same stream; when launched as a programmatic dependent it
+// first waits for that kernel's completion and memory.
+__global__ void __launch_bounds__(256) splitk_fixup_kernel(const GemmParams p, int bm, int bn)
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int row_v4 = bn / 4;                        // float4 per tile row
+    const long long tile_v4 = static_cast<long long>(bm) * row_v4;
+    const long long total = (p.num_tiles - p.dp_tiles) * tile_v4;
+    const bool use_beta = p.beta != 0.f;
+    for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
+         e += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long sidx = e / tile_v4;
+        const int within = static_cast<int>(e - sidx * tile_v4);
+        const int r = within / row_v4, c = (within - r * row_v4) * 4;
+        const TileCoord tc = tile_coord(p.dp_tiles + sidx, p);
+        const int m = tc.tm * bm + r, n0 = tc.tn * bn + c;
+        if (m >= p.M || n0 >= p.N) continue;
+        const float4 *slot =
+            reinterpret_cast<const float4 *>(p.ws_part) + sidx * p.splits * tile_v4 + within;
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sl = 0; sl < p.splits; ++sl) {
+            const float4 x = slot[sl * tile_v4];
+            sum.x += x.x;
+            sum.y += x.y;
+            sum.z += x.z;
+            sum.w += x.w;
+        }
+        float *crow = p.C + tc.q * p.sC + static_cast<long long>(m) * p.ldc;
+        const float v[4] = {sum.x, sum.y, sum.z, sum.w};
+        if (p.c_vec4 && n0 + 3 < p.N) {
+            float4 o = make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2], p.alpha * v[3]);
+            float4 *dst = reinterpret_cast<float4 *>(crow + n0);
+            if (use_beta) {
+                const float4 old = *dst;
+                o.x = fmaf(p.beta, old.x, o.x);
+                o.y = fmaf(p.beta, old.y, o.y);
+                o.z = fmaf(p.beta, old.z, o.z);
+                o.w = fmaf(p.beta, old.w, o.w);
+            }
+            *dst = o;
+        } else {
+            for (int j = 0; j < 4 && n0 + j < p.N; ++j) {
+                float o = p.alpha * v[j];
+                if (use_beta) o = fmaf(p.beta, crow[n0 + j], o);
+                crow[n0 + j] = o;
+            }
+        }
+    }
+}
+
 // Bounded-wait self test: one thread waits on an mbarrier that nobody arrives
 // on, gives up after `limit` cycles, then completes the phase itself so the
 // barrier is left in a clean state.
@@ -161,46 +216,114 @@ bool encode_operand(CUtensorMap *map, const float *base, bool kin, long long row
 
 int min_slice_k(int mode) { return mode == SGEMM_MODE_FP32 ? 64 : 256; }
 
-int choose_splits(long long num_tiles, int K, int num_sms, int mode)
+size_t splitk_workspace_bytes(long long split_tiles, int splits)
 {
-    // as many slices as keep every unit in one wave (units <= multiprocessors)
-    if (num_tiles <= 0 || 2 * num_tiles > num_sms) return 1;
-    long long s = num_sms / num_tiles;
-    const long long by_k = K / min_slice_k(mode);
-    if (s > by_k) s = by_k;
-    if (s > kMaxSplits) s = kMaxSplits;
-    return s < 2 ? 1 : static_cast<int>(s);
+    if (splits <= 1 || split_tiles <= 0) return 0;
+    return static_cast<size_t>(split_tiles) * splits * kSplitTile * kSplitTile * sizeof(float);
 }
 
-size_t splitk_workspace_bytes(long long num_tiles, int splits)
+SplitPlan choose_plan(long long num_tiles, int K, int num_sms, int mode, size_t budget)
 {
-    if (splits <= 1) return 0;
-    const size_t ctr = (static_cast<size_t>(num_tiles) * kSplitRegions * sizeof(unsigned int) + 255) &
-                       ~static_cast<size_t>(255);
-    return ctr + static_cast<size_t>(num_tiles) * splits * kSplitTile * kSplitTile * sizeof(float);
+    SplitPlan best{1, num_tiles, 0};
+    if (num_tiles <= 0 || num_sms <= 0) return best;
+    const long long full = num_tiles / num_sms, rem = num_tiles % num_sms;
+    if (rem == 0) return best;
+    long long smax = K / min_slice_k(mode);
+    if (smax > kMaxSplits) smax = kMaxSplits;
+    double best_t = static_cast<double>(full) + 1.0 + kSliceCost;
+    for (int s = 2; s <= smax; ++s) {
+        const long long waves = (rem * s + num_sms - 1) / num_sms;
+        const double t = static_cast<double>(full) + static_cast<double>(waves) / s + kSliceCost * s;
+        const size_t ws = splitk_workspace_bytes(rem, s);
+        if (t < best_t - 1e-9 && ws <= budget) {
+            best_t = t;
+            best = SplitPlan{s, full * num_sms, ws};
+        }
+    }
+    return best;
 }
 
 int plan_splits(Plan &plan)
 {
     GemmParams &p = plan.p;
     p.splits = 1;
+    p.dp_tiles = p.num_tiles;
     p.ws_part = nullptr;
-    p.ws_ctr = nullptr;
-    const int s = plan.ws ? choose_splits(p.num_tiles, p.K, plan.num_sms, plan.mode) : 1;
-    const size_t need = splitk_workspace_bytes(p.num_tiles, s);
-    if (s > 1 && need <= plan.ws_bytes) {
-        const size_t ctr = (static_cast<size_t>(p.num_tiles) * kSplitRegions * sizeof(unsigned int) +
-                            255) & ~static_cast<size_t>(255);
-        p.splits = s;
-        p.ws_ctr = static_cast<unsigned int *>(plan.ws);
-        p.ws_part = reinterpret_cast<float *>(static_cast<char *>(plan.ws) + ctr);
-        // counters start at zero (the last slice of every region re-arms its
-        // counter, but a call that stopped early may have left one raised)
-        if (cudaMemsetAsync(plan.ws, 0, ctr, plan.stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    if (plan.ws != nullptr) {
+        const SplitPlan sp = choose_plan(p.num_tiles, p.K, plan.num_sms, plan.mode, plan.ws_bytes);
+        if (sp.splits > 1) {
+            p.splits = sp.splits;
+            p.dp_tiles = sp.dp_tiles;
+            p.ws_part = static_cast<float *>(plan.ws);
+        }
     }
-    p.num_units = p.num_tiles * p.splits;
+    p.num_units = p.dp_tiles + (p.num_tiles - p.dp_tiles) * p.splits;
     return SGEMM_OK;
 }
+
+namespace {
+
+// Tiles of a call and the multiprocessors of the current device, or false.
+bool tiles_and_sms(int &mode, int M, int N, int K, int Q, long long &tiles, int &sms)
+{
+    if (mode == SGEMM_MODE_DEFAULT) mode = g_default_mode.load();
+    if (mode != SGEMM_MODE_FP32 && mode != SGEMM_MODE_3XTF32 && mode != SGEMM_MODE_TF32) return false;
+    if (M <= 0 || N <= 0 || K <= 0 || Q <= 0) return false;
+    int dev = 0;
+    const DeviceInfo *di = device_info(&dev);
+    if (di == nullptr) return false;
+    tiles = static_cast<long long>(Q) * ((M + kSplitTile - 1) / kSplitTile) *
+            ((N + kSplitTile - 1) / kSplitTile);
+    sms = di->num_sms;
+    return true;
+}
+
+}  // namespace
+
+int launch_fixup(Plan &plan, int bm, int bn)
+{
+    const GemmParams &p = plan.p;
+    const long long total = (p.num_tiles - p.dp_tiles) * (static_cast<long long>(bm) * bn / 4);
+    long long blocks = (total + 255) / 256;
+    if (blocks > 8LL * plan.num_sms) blocks = 8LL * plan.num_sms;
+    if (blocks < 1) return SGEMM_OK;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = plan.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, splitk_fixup_kernel, p, bm, bn) == cudaSuccess
+               ? SGEMM_OK
+               : SGEMM_ERR_LAUNCH;
+}
+
+SplitPlan preferred_plan(int mode, int M, int N, int K, int Q)
+{
+    long long tiles = 0;
+    int sms = 0;
+    if (!tiles_and_sms(mode, M, N, K, Q, tiles, sms)) return SplitPlan{1, 0, 0};
+    return choose_plan(tiles, K, sms, mode, ~static_cast<size_t>(0));
+}
+
+SplitPlan one_wave_plan(int mode, int M, int N, int K, int Q)
+{
+    long long tiles = 0;
+    int sms = 0;
+    if (!tiles_and_sms(mode, M, N, K, Q, tiles, sms)) return SplitPlan{1, 0, 0};
+    if (2 * tiles > sms) return SplitPlan{1, tiles, 0};
+    long long s = sms / tiles;
+    const long long by_k = K / min_slice_k(mode);
+    if (s > by_k) s = by_k;
+    if (s > kMaxSplits) s = kMaxSplits;
+    if (s < 2) return SplitPlan{1, tiles, 0};
+    return SplitPlan{static_cast<int>(s), 0, splitk_workspace_bytes(tiles, static_cast<int>(s))};
+}
+
 
 }  // namespace sg
 
@@ -323,15 +446,7 @@ int sgemm_batched_ex_ws(int mode, int M, int N, int K, float alpha, const float 
 
 size_t sgemm_workspace_size(int mode, int M, int N, int K, int Q)
 {
-    if (mode == SGEMM_MODE_DEFAULT) mode = g_default_mode.load();
-    if (mode != SGEMM_MODE_FP32 && mode != SGEMM_MODE_3XTF32 && mode != SGEMM_MODE_TF32) return 0;
-    if (M <= 0 || N <= 0 || K <= 0 || Q <= 0) return 0;
-    int dev = 0;
-    const DeviceInfo *di = device_info(&dev);
-    if (di == nullptr) return 0;
-    const long long tiles = static_cast<long long>(Q) * ((M + kSplitTile - 1) / kSplitTile) *
-                            ((N + kSplitTile - 1) / kSplitTile);
-    return splitk_workspace_bytes(tiles, choose_splits(tiles, K, di->num_sms, mode));
+    return preferred_plan(mode, M, N, K, Q).ws_bytes;
 }
 
 int sgemm_set_default_mode(int mode)

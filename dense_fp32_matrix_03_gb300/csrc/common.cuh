@@ -274,49 +274,68 @@ __device__ __forceinline__ TileCoord tile_coord(long long t, const GemmParams &p
 struct WorkUnit {
     TileCoord tc;
     long long tile;   // linear tile index
-    int slice;        // 0 .. splits-1
-    int kb_lo, kb_hi; // k-blocks [kb_lo, kb_hi) of this slice (never empty)
+    long long sidx;   // index among the split tiles (tile - dp_tiles); -1 if whole
+    int slice;        // 0 .. splits-1 (0 if whole)
+    int kb_lo, kb_hi; // k-blocks [kb_lo, kb_hi) of this unit (never empty)
+    bool split;       // part of a split tile: hand the partial over
 };
 
 __device__ __forceinline__ WorkUnit work_unit(long long u, const GemmParams &p)
 {
     WorkUnit w;
-    if (p.splits <= 1) {
+    if (p.splits <= 1 || u < p.dp_tiles) {
         w.tile = u;
+        w.sidx = -1;
         w.slice = 0;
         w.kb_lo = 0;
         w.kb_hi = p.k_blocks;
+        w.split = false;
     } else {
-        w.tile = u / p.splits;
-        w.slice = static_cast<int>(u - w.tile * p.splits);
+        const long long v = u - p.dp_tiles;
+        w.sidx = v / p.splits;
+        w.tile = p.dp_tiles + w.sidx;
+        w.slice = static_cast<int>(v - w.sidx * p.splits);
         w.kb_lo = static_cast<int>((static_cast<long long>(w.slice) * p.k_blocks) / p.splits);
         w.kb_hi = static_cast<int>((static_cast<long long>(w.slice + 1) * p.k_blocks) / p.splits);
+        w.split = true;
     }
     w.tc = tile_coord(w.tile, p);
     return w;
 }
 
-// Split-K hand-off for one region of a tile (a warp's share of the output
-// tile), called by all 32 lanes after they stored their partial values with
-// plain global stores.  Returns true (warp-uniformly) in the warp of the last
-// slice to finish the region, which may then read every slice's partial:
-// the fences order each writer's stores before its counter increment and the
-// last reader's loads after its own.  The last one also re-arms the counter.
-__device__ __forceinline__ bool splitk_arrive(unsigned int *ctr, int splits, int lane)
-{
-    __threadfence();
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-        last = (atomicAdd(ctr, 1u) == static_cast<unsigned int>(splits - 1)) ? 1 : 0;
-        if (last) *ctr = 0u;
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) __threadfence();
-    return last != 0;
-}
+// Where a work unit's BM x BN result goes.  A whole tile goes to C with the
+// caller's alpha and beta; one slice of a split tile goes, unscaled, to its
+// own row-major BM x BN slot of the split-K workspace (slot
+// sidx * splits + slice), from where the fix-up kernel sums the slices.
+struct OutTile {
+    float *base;        // element (0, 0) of the tile
+    long long ld;       // row pitch in elements
+    float alpha, beta;  // beta == 0: the destination is not read
+    int rows, cols;     // valid extent: min(BM, M - m0), min(BN, N - n0)
+    bool vec4;          // 16-byte accesses allowed (base and ld allow them)
+};
 
-// Loads that bypass L1 (partials written by other SMs must come from L2).
-__device__ __forceinline__ float4 ldcg4(const float *p) { return __ldcg(reinterpret_cast<const float4 *>(p)); }
+template <int BM, int BN>
+__device__ __forceinline__ OutTile out_tile(const GemmParams &p, const WorkUnit &wu)
+{
+    OutTile o;
+    const int m0 = wu.tc.tm * BM, n0 = wu.tc.tn * BN;
+    o.rows = min(BM, p.M - m0);
+    o.cols = min(BN, p.N - n0);
+    if (!wu.split) {
+        o.base = p.C + wu.tc.q * p.sC + static_cast<long long>(m0) * p.ldc + n0;
+        o.ld = p.ldc;
+        o.alpha = p.alpha;
+        o.beta = p.beta;
+        o.vec4 = p.c_vec4 != 0;
+    } else {
+        o.base = p.ws_part + (wu.sidx * p.splits + wu.slice) * static_cast<long long>(BM * BN);
+        o.ld = BN;
+        o.alpha = 1.f;
+        o.beta = 0.f;
+        o.vec4 = true;
+    }
+    return o;
+}
 
 }  // namespace sg

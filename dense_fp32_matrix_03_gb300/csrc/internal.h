@@ -23,26 +23,47 @@ struct Plan {
     size_t ws_bytes;
 };
 
-// Split-K plan shared by both kernels (128 x 128 output tiles).  A grid with
-// at most half as many tiles as multiprocessors is cut along K into `splits`
-// slices, as many as keep all work units in one wave, each at least
-// min_slice_k(mode) long: 64 for the FP32 path, 256 for the tensor-core
-// paths, whose per-unit pipeline start-up (copy, split, MMA, TMEM read-back)
-// is longer (measured on GB300: shorter slices made 128^3..512^3 slower).
-// The slices are whole k-blocks of the kernel that runs (each kernel's
-// k-block is at most the minimum slice, so no slice is empty).  The
-// workspace holds one arrival counter per tile region and one fp32 partial
-// tile per (tile, slice).
+// Split-K plan shared by both kernels (128 x 128 output tiles, one
+// persistent CTA per multiprocessor).  With T tiles on G multiprocessors the
+// grid runs floor(T/G) whole waves and a last wave of T mod G tiles that
+// leaves the rest of the GPU idle.  The planner may cut the tiles of that
+// last wave (all tiles when T < G) along K into `splits` slices, so that the
+// slices spread over the whole GPU: modelled finishing time, in tile times,
+//     floor(T/G) + ceil((T mod G) * s / G) / s + kSliceCost * s,
+// minimised over s = 1 .. min(16, K / min_slice_k(mode)).  Each slice is at
+// least min_slice_k(mode) deep: 64 for the FP32 path, 256 for the
+// tensor-core paths, whose per-unit pipeline start-up (copy, split, MMA,
+// TMEM read-back) is longer (measured on GB300: shorter slices made
+// 128^3..512^3 slower).  The slices are whole k-blocks of the kernel that
+// runs (each kernel's k-block is at most the minimum slice, so no slice is
+// empty).  Each slice writes its partial tile, unscaled, to its own slot of
+// the workspace; a fix-up kernel launched right after on the same stream
+// sums every split tile's slots in slice order and applies alpha and beta.
+// The workspace is one 128 x 128 fp32 slot per (split tile, slice); a plan
+// whose workspace exceeds the caller's budget is not considered.
 constexpr int kSplitTile = 128;            // output tile edge of both paths
-constexpr int kSplitRegions = 8;           // counters per tile (>= warps writing a tile)
 constexpr int kMaxSplits = 16;
+constexpr double kSliceCost = 0.01;        // per-slice overhead, in tile times
+struct SplitPlan {
+    int splits;          // 1 = no split
+    long long dp_tiles;  // tiles computed whole (they come first in unit order)
+    size_t ws_bytes;     // workspace the plan needs
+};
 int min_slice_k(int mode);
-int choose_splits(long long num_tiles, int K, int num_sms, int mode);
-size_t splitk_workspace_bytes(long long num_tiles, int splits);
-// Fills p.splits / num_units / ws_* for the launch: splits if the plan's
-// workspace is large enough (and clears its counters on the stream), else
-// runs unsplit.  Returns an sgemm status.
+size_t splitk_workspace_bytes(long long split_tiles, int splits);
+SplitPlan choose_plan(long long num_tiles, int K, int num_sms, int mode, size_t budget);
+// Fills p.splits / dp_tiles / num_units / ws_part for the launch from the
+// best plan that fits the caller's workspace.  Returns an sgemm status.
 int plan_splits(Plan &plan);
+// Enqueues the split-K fix-up for a launch whose plan split (bm x bn tiles).
+int launch_fixup(Plan &plan, int bm, int bn);
+// The plan sgemm_workspace_size reports for a call (no budget), or splits = 1.
+SplitPlan preferred_plan(int mode, int M, int N, int K, int Q);
+// The plan of the allocation-free entry point: a grid of at most half as many
+// tiles as multiprocessors is cut into as many slices as keep every unit in
+// one wave (at most 16, each at least min_slice_k deep); other grids run
+// unsplit.  Its workspace is at most one partial tile per multiprocessor.
+SplitPlan one_wave_plan(int mode, int M, int N, int K, int Q);
 
 // Describes one operand for a TMA tensor map.
 //  kin  : contiguous dimension is K (rows are `rows` long runs of K values)

@@ -30,8 +30,7 @@ constexpr int kGroupM = 8;
 template <class Cfg, bool A_KIN, bool B_KIN, bool USE_TMA, bool EVEN_K>
 int launch_one(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
 {
-    auto kern = plan.p.splits > 1 ? simt_sgemm_kernel<Cfg, A_KIN, B_KIN, USE_TMA, EVEN_K, true>
-                                  : simt_sgemm_kernel<Cfg, A_KIN, B_KIN, USE_TMA, EVEN_K, false>;
+    auto kern = simt_sgemm_kernel<Cfg, A_KIN, B_KIN, USE_TMA, EVEN_K>;
     // The attribute is per device; setting it on every call costs about a
     // microsecond and keeps the launcher free of per-device caches.
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -42,7 +41,8 @@ int launch_one(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
         grid = static_cast<long long>(plan.num_sms) * kMinBlocks;
     kern<<<static_cast<unsigned>(grid), Cfg::THREADS, Cfg::SMEM_BYTES, plan.stream>>>(
         tmA, tmB, plan.p);
-    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    return plan.p.splits > 1 ? launch_fixup(plan, Cfg::BM, Cfg::BN) : SGEMM_OK;
 }
 
 template <class Cfg, bool USE_TMA, bool EVEN_K>
@@ -68,7 +68,7 @@ int launch_simt(Plan &plan)
     p.num_tiles = static_cast<long long>(p.Q) * p.tiles_m * p.tiles_n;
     plan.even_k = (p.K % Cfg::BK) == 0;
     static_assert(Cfg::BM == kSplitTile && Cfg::BN == kSplitTile, "split-K workspace tile");
-    static_assert(Cfg::CONSUMER_WARPS <= kSplitRegions, "split-K counters per tile");
+    static_assert(kMinBlocks == 1, "the split planner assumes one CTA per multiprocessor");
     const int rc = plan_splits(plan);
     if (rc != SGEMM_OK) return rc;
 

@@ -16,10 +16,8 @@ constexpr int kGroupM = 8;
 template <bool SPLIT3, bool A_KIN, bool B_KIN, bool USE_TMA>
 int launch_one(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
 {
-    using C = tc::Cfg<kBN, SPLIT3, A_KIN, B_KIN, USE_TMA, false>;
-    using CS = tc::Cfg<kBN, SPLIT3, A_KIN, B_KIN, USE_TMA, true>;
-    static_assert(C::SMEM_BYTES == CS::SMEM_BYTES, "same layout with and without split-K");
-    auto kern = plan.p.splits > 1 ? tc::tc_sgemm_kernel<CS> : tc::tc_sgemm_kernel<C>;
+    using C = tc::Cfg<kBN, SPLIT3, A_KIN, B_KIN, USE_TMA>;
+    auto kern = tc::tc_sgemm_kernel<C>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
@@ -27,7 +25,8 @@ int launch_one(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
     if (grid > plan.num_sms) grid = plan.num_sms;
     kern<<<static_cast<unsigned>(grid), tc::kThreads, C::SMEM_BYTES, plan.stream>>>(tmA, tmB,
                                                                                   plan.p);
-    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    return plan.p.splits > 1 ? launch_fixup(plan, tc::BM, kBN) : SGEMM_OK;
 }
 
 template <bool SPLIT3, bool USE_TMA>

@@ -16,16 +16,16 @@
 #include <cuda_runtime.h>
 
 #include "../../include/sgemm.h"
+#include "internal.h"
 
 namespace {
 
-// Enough for the split-K workspace of any shape on a GPU with up to ~190
-// multiprocessors (at most one 128 x 128 fp32 partial tile per
-// multiprocessor, plus the arrival counters).
+// Enough for the split-K workspace of this entry point's plan on a GPU with
+// up to ~190 multiprocessors (at most one 128 x 128 fp32 partial tile per
+// multiprocessor).
 constexpr size_t kScratchBytes = static_cast<size_t>(12) << 20;
 
-// The scratch: shared by every call on a device, keeps the last call's
-// contents between calls.
+// The scratch: shared by every call on a device; needs no initialisation.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -61,16 +61,19 @@ extern "C" int sgemm_batched_ex_noalloc(int mode, int M, int N, int K, float alp
                                         long long strideA, long long strideB, long long strideC,
                                         int Q, void *stream)
 {
-    // what the split path would use for this shape (0 when it does not split)
-    const size_t need = sgemm_workspace_size(mode, M, N, K, Q);
-    if (need > kScratchBytes) return SGEMM_ERR_SCRATCH_LIMIT;
+    // This entry point splits only grids of at most half as many tiles as
+    // multiprocessors, into one wave of slices; its workspace must fit.
+    const sg::SplitPlan sp = sg::one_wave_plan(mode, M, N, K, Q);
+    if (sp.ws_bytes > kScratchBytes) return SGEMM_ERR_SCRATCH_LIMIT;
     void *ws = nullptr;
-    if (need > 0) {
+    if (sp.splits > 1) {
         const int rc = scratch_address(&ws);
         if (rc != SGEMM_OK) return rc;
     }
-    // The workspace path clears the counter area of the scratch on `stream`
-    // before its kernel, so what an earlier call left there does not matter.
+    // The workspace path runs the best plan that fits the bytes it is given
+    // (this one, or one at least as good by its model); every slot it reads
+    // back was written by the same call, so what an earlier call left in the
+    // scratch does not matter.
     return sgemm_batched_ex_ws(mode, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, transA, transB,
-                               strideA, strideB, strideC, Q, ws, ws ? kScratchBytes : 0, stream);
+                               strideA, strideB, strideC, Q, ws, ws ? sp.ws_bytes : 0, stream);
 }

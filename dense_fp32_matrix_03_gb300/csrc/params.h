@@ -34,14 +34,17 @@ struct GemmParams {
     int c_vec4;                // epilogue may use 16-byte C accesses
     unsigned int *status;      // device status word
     long long wait_limit;      // clock64 cycles a bounded wait may spin
-    // split-K: every tile's k-blocks are cut into `splits` contiguous slices;
-    // work unit u = tile * splits + slice.  With splits > 1 each slice writes
-    // its fp32 partial tile to ws_part and the last slice to finish a region
-    // (per-region counters in ws_ctr) sums all partials and writes C.
+    // split-K: tiles [0, dp_tiles) are whole work units (u = tile); every
+    // later tile's k-blocks are cut into `splits` contiguous slices, unit
+    // u = dp_tiles + (tile - dp_tiles) * splits + slice.  Each slice writes its
+    // unscaled fp32 partial tile to its slot of ws_part; the fix-up kernel
+    // then sums the slices, in slice order, and applies alpha and beta.
+    // dp_tiles = 0 splits every tile (a grid smaller than the GPU); dp_tiles =
+    // whole waves of tiles splits only the last, partial wave.
     int splits;                // 1 = no split
-    long long num_units;       // num_tiles * splits
-    float *ws_part;            // num_tiles * splits partial tiles (BM x BN fp32 each)
-    unsigned int *ws_ctr;      // num_tiles * regions arrival counters (zero on entry)
+    long long dp_tiles;        // tiles computed whole (num_tiles when splits == 1)
+    long long num_units;       // dp_tiles + (num_tiles - dp_tiles) * splits
+    float *ws_part;            // one row-major BM x BN fp32 slot per split unit
 };
 
 }  // namespace sg

@@ -483,49 +483,6 @@ struct Acc {
     }
 };
 
-// Split-K hand-off of one warp's accumulators (its region of the tile).
-// Partials are stored lane-interleaved (float4 v of lane l at v*32 + l within
-// the region) so that every store and load of a warp is one contiguous 512
-// bytes.  Returns false when another slice will finish the region; in the
-// warp of the last slice, replaces acc by the sum over all slices, taken in
-// slice order 0, 1, ..., so the result does not depend on arrival order.
-template <class Cfg>
-__device__ __forceinline__ bool splitk_exchange(const GemmParams &p, const WorkUnit &wu, int cw,
-                                                int lane, float (&acc)[Cfg::TM][Cfg::TN])
-{
-    constexpr int TM = Cfg::TM, TN = Cfg::TN, V = TM * TN / 4;
-    constexpr long long REGION = static_cast<long long>(V) * 32;  // float4 per region
-    float4 *ws = reinterpret_cast<float4 *>(p.ws_part);
-    const long long slot0 = wu.tile * p.splits;
-    float4 *mine = ws + ((slot0 + wu.slice) * Cfg::CONSUMER_WARPS + cw) * REGION + lane;
-#pragma unroll
-    for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int jg = 0; jg < TN / 4; ++jg)
-            mine[(i * (TN / 4) + jg) * 32] =
-                make_float4(acc[i][4 * jg], acc[i][4 * jg + 1], acc[i][4 * jg + 2], acc[i][4 * jg + 3]);
-    if (!splitk_arrive(p.ws_ctr + wu.tile * Cfg::CONSUMER_WARPS + cw, p.splits, lane)) return false;
-#pragma unroll
-    for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
-    for (int sl = 0; sl < p.splits; ++sl) {
-        const float *src = reinterpret_cast<const float *>(
-            ws + ((slot0 + sl) * Cfg::CONSUMER_WARPS + cw) * REGION + lane);
-#pragma unroll
-        for (int i = 0; i < TM; ++i)
-#pragma unroll
-            for (int jg = 0; jg < TN / 4; ++jg) {
-                const float4 x = ldcg4(src + (i * (TN / 4) + jg) * 32 * 4);
-                acc[i][4 * jg] += x.x;
-                acc[i][4 * jg + 1] += x.y;
-                acc[i][4 * jg + 2] += x.z;
-                acc[i][4 * jg + 3] += x.w;
-            }
-    }
-    return true;
-}
-
 // One consumer warp: WM x WN outputs of the CTA tile; each lane holds
 // TM x TN accumulators as (WM/32) x (WN/16) sub-blocks of 4 x 4.
 //
@@ -541,7 +498,7 @@ __device__ __forceinline__ bool splitk_exchange(const GemmParams &p, const WorkU
 // register set while the current one feeds the FFMAs.  A stage is released
 // after the FFMAs of its last k-group, i.e. once every value read from it has
 // been consumed.
-template <class Cfg, bool A_KIN, bool B_KIN, bool SPLITK, class Issuer>
+template <class Cfg, bool A_KIN, bool B_KIN, class Issuer>
 __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem, uint64_t *full,
                                               uint64_t *empty, const Abort &ab, int cw, int lane,
                                               Issuer &iss)
@@ -580,7 +537,6 @@ __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem
     long long it = 0;  // k-blocks consumed so far by this CTA
     for (long long u = blockIdx.x; u < p.num_units; u += gridDim.x) {
         const WorkUnit wu = work_unit(u, p);
-        const TileCoord &tc = wu.tc;
         Acc<Cfg, pair_dim<A_KIN, B_KIN>()> accp;
         accp.zero();
 
@@ -607,58 +563,57 @@ __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem
 
         float acc[TM][TN];
         accp.to_float(acc);
-        if (SPLITK && !splitk_exchange<Cfg>(p, wu, cw, lane, acc)) continue;
 
-        // ---- epilogue: C = alpha * acc + beta * C, masked at the M/N edges
-        const int mt = tc.tm * BM, nt = tc.tn * BN;
-        float *Cq = p.C + tc.q * p.sC;
-        const bool use_beta = p.beta != 0.f;
+        // ---- epilogue: out = alpha * acc + beta * out, masked at the M/N
+        // edges (out = C, or this slice's workspace slot with alpha 1, beta 0)
+        const OutTile o = out_tile<BM, BN>(p, wu);
+        const bool use_beta = o.beta != 0.f;
 #pragma unroll
         for (int wm = 0; wm < WMITER; ++wm)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int r = mt + row_of(wm, i);
-                if (r >= p.M) continue;
-                float *crow = Cq + r * p.ldc;
+                const int r = row_of(wm, i);
+                if (r >= o.rows) continue;
+                float *orow = o.base + r * o.ld;
 #pragma unroll
                 for (int wn = 0; wn < WNITER; ++wn) {
                     const float *av = &acc[wm * 4 + i][wn * 4];
                     if (!B_KIN) {
-                        const int c0 = nt + col_of(wn, 0);
-                        if (p.c_vec4 && c0 + 3 < p.N) {
-                            float4 o;
-                            o.x = p.alpha * av[0];
-                            o.y = p.alpha * av[1];
-                            o.z = p.alpha * av[2];
-                            o.w = p.alpha * av[3];
-                            float4 *dst = reinterpret_cast<float4 *>(crow + c0);
+                        const int c0 = col_of(wn, 0);
+                        if (o.vec4 && c0 + 3 < o.cols) {
+                            float4 v;
+                            v.x = o.alpha * av[0];
+                            v.y = o.alpha * av[1];
+                            v.z = o.alpha * av[2];
+                            v.w = o.alpha * av[3];
+                            float4 *dst = reinterpret_cast<float4 *>(orow + c0);
                             if (use_beta) {
                                 const float4 old = *dst;
-                                o.x = fmaf(p.beta, old.x, o.x);
-                                o.y = fmaf(p.beta, old.y, o.y);
-                                o.z = fmaf(p.beta, old.z, o.z);
-                                o.w = fmaf(p.beta, old.w, o.w);
+                                v.x = fmaf(o.beta, old.x, v.x);
+                                v.y = fmaf(o.beta, old.y, v.y);
+                                v.z = fmaf(o.beta, old.z, v.z);
+                                v.w = fmaf(o.beta, old.w, v.w);
                             }
-                            *dst = o;
+                            *dst = v;
                         } else {
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 const int c = c0 + j;
-                                if (c < p.N) {
-                                    float o = p.alpha * av[j];
-                                    if (use_beta) o = fmaf(p.beta, crow[c], o);
-                                    crow[c] = o;
+                                if (c < o.cols) {
+                                    float v = o.alpha * av[j];
+                                    if (use_beta) v = fmaf(o.beta, orow[c], v);
+                                    orow[c] = v;
                                 }
                             }
                         }
                     } else {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const int c = nt + col_of(wn, j);
-                            if (c < p.N) {
-                                float o = p.alpha * av[j];
-                                if (use_beta) o = fmaf(p.beta, crow[c], o);
-                                crow[c] = o;
+                            const int c = col_of(wn, j);
+                            if (c < o.cols) {
+                                float v = o.alpha * av[j];
+                                if (use_beta) v = fmaf(o.beta, orow[c], v);
+                                orow[c] = v;
                             }
                         }
                     }
@@ -669,7 +624,7 @@ __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem
 
 // ---------------------------------------------------------------- kernel
 
-template <class Cfg, bool A_KIN, bool B_KIN, bool USE_TMA, bool EVEN_K, bool SPLITK>
+template <class Cfg, bool A_KIN, bool B_KIN, bool USE_TMA, bool EVEN_K>
 __global__ void __launch_bounds__(Cfg::THREADS, kMinBlocks)
     simt_sgemm_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const GemmParams p)
@@ -697,7 +652,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, kMinBlocks)
 
     // k-blocks this CTA consumes: its units are blockIdx.x + i*gridDim.x
     long long my_kblocks;
-    if (!SPLITK) {
+    if (p.splits <= 1) {
         my_kblocks = (p.num_units - blockIdx.x + gridDim.x - 1) / static_cast<long long>(gridDim.x) *
                      p.k_blocks;
     } else {
@@ -719,7 +674,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, kMinBlocks)
     iss.total = my_kblocks;
     iss.prologue(warp, lane, ab);
     __syncwarp();
-    simt_consumer<Cfg, A_KIN, B_KIN, SPLITK>(p, smem, full, empty, ab, warp, lane, iss);
+    simt_consumer<Cfg, A_KIN, B_KIN>(p, smem, full, empty, ab, warp, lane, iss);
     __syncwarp();
     if (*abort_flag) iss.drain(ab.limit, warp, lane);
     __syncthreads();

@@ -67,11 +67,10 @@ constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 constexpr int kConvWarps = 4 + kBConvWarps;      // arrivals that complete a stage
 constexpr uint32_t kTmemCols = 512;
 
-template <int BN_, bool SPLIT3_, bool A_KIN_, bool B_KIN_, bool USE_TMA_, bool SPLITK_>
+template <int BN_, bool SPLIT3_, bool A_KIN_, bool B_KIN_, bool USE_TMA_>
 struct Cfg {
     static constexpr int BN = BN_;
     static constexpr bool SPLIT3 = SPLIT3_, A_KIN = A_KIN_, B_KIN = B_KIN_, USE_TMA = USE_TMA_;
-    static constexpr bool SPLITK = SPLITK_;   // K cut into slices (split-K epilogue)
     static constexpr int A_BYTES = BM * BK * 4;          // one 128 x 32 fp32 tile
     static constexpr int B_BYTES = BN * BK * 4;
     static constexpr int RAW_BYTES = A_BYTES + B_BYTES;
@@ -373,37 +372,36 @@ __device__ __forceinline__ void convert_b_tile(const uint8_t *raw, uint8_t *hi, 
     }
 }
 
-// Epilogue of 32 consecutive columns of one output row:
-// C[r][n0 .. n0+31] = alpha * v + beta * C, masked at the M/N edges; C is
-// read only when beta != 0.
-__device__ __forceinline__ void store_c_chunk(const GemmParams &p, float *crow, int r, int n0,
-                                              const float (&v)[32])
+// Stores 32 consecutive columns [c0, c0 + 32) of tile row r: out = alpha * v
+// + beta * out (out not read when beta == 0), masked at the M/N edges.
+__device__ __forceinline__ void store_chunk(const OutTile &o, int r, int c0, const float (&v)[32])
 {
-    if (r >= p.M) return;
-    const bool use_beta = p.beta != 0.f;
-    if (p.c_vec4 && n0 + 32 <= p.N) {
+    if (r >= o.rows) return;
+    float *orow = o.base + static_cast<long long>(r) * o.ld;
+    const bool use_beta = o.beta != 0.f;
+    if (o.vec4 && c0 + 32 <= o.cols) {
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
-            float4 o = make_float4(p.alpha * v[j], p.alpha * v[j + 1], p.alpha * v[j + 2],
-                                   p.alpha * v[j + 3]);
-            float4 *dst = reinterpret_cast<float4 *>(crow + n0 + j);
+            float4 x = make_float4(o.alpha * v[j], o.alpha * v[j + 1], o.alpha * v[j + 2],
+                                   o.alpha * v[j + 3]);
+            float4 *dst = reinterpret_cast<float4 *>(orow + c0 + j);
             if (use_beta) {
                 const float4 old = *dst;
-                o.x = fmaf(p.beta, old.x, o.x);
-                o.y = fmaf(p.beta, old.y, o.y);
-                o.z = fmaf(p.beta, old.z, o.z);
-                o.w = fmaf(p.beta, old.w, o.w);
+                x.x = fmaf(o.beta, old.x, x.x);
+                x.y = fmaf(o.beta, old.y, x.y);
+                x.z = fmaf(o.beta, old.z, x.z);
+                x.w = fmaf(o.beta, old.w, x.w);
             }
-            *dst = o;
+            *dst = x;
         }
     } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-            const int n = n0 + j;
-            if (n < p.N) {
-                float o = p.alpha * v[j];
-                if (use_beta) o = fmaf(p.beta, crow[n], o);
-                crow[n] = o;
+            const int c = c0 + j;
+            if (c < o.cols) {
+                float x = o.alpha * v[j];
+                if (use_beta) x = fmaf(o.beta, orow[c], x);
+                orow[c] = x;
             }
         }
     }
@@ -637,62 +635,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_drain(&sm.acc_full[acc.s], acc.ph, ab.limit);
             tc_fence_after();
             const WorkUnit wu = work_unit(u, p);
-            const int r = wu.tc.tm * BM + row_in_tile;
-            const int n_tile = wu.tc.tn * C::BN;
-            float *crow = p.C + wu.tc.q * p.sC + static_cast<long long>(r) * p.ldc;
+            // C, or this slice's workspace slot (unscaled) when the tile is split
+            const OutTile o = out_tile<BM, C::BN>(p, wu);
             const uint32_t tbase =
                 tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc.s * C::BN);
-            if (!C::SPLITK) {
 #pragma unroll 1
-                for (int c0 = 0; c0 < C::BN; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(tbase + c0, v);  // all lanes take part, rows in range or not
-                    store_c_chunk(p, crow, r, n_tile + c0, v);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.acc_empty[acc.s]);
-            } else {
-                // split-K: this slice's partial goes to the workspace, lane-interleaved
-                // (float4 v of lane l at v*32 + l of the warp's region)
-                constexpr long long REGION = (C::BN / 4) * 32;  // float4 per region
-                float4 *ws = reinterpret_cast<float4 *>(p.ws_part);
-                const long long slot0 = wu.tile * p.splits;
-                float4 *mine = ws + ((slot0 + wu.slice) * 4 + q) * REGION + lane;
-#pragma unroll 1
-                for (int c0 = 0; c0 < C::BN; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(tbase + c0, v);
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        mine[((c0 + j) / 4) * 32] = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-                }
-                // the accumulator is no longer needed
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.acc_empty[acc.s]);
-                if (splitk_arrive(p.ws_ctr + wu.tile * 4 + q, p.splits, lane)) {
-#pragma unroll 1
-                    for (int c0 = 0; c0 < C::BN; c0 += 32) {
-                        float v[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = 0.f;
-                        for (int sl = 0; sl < p.splits; ++sl) {  // slice order: deterministic
-                            const float *src = reinterpret_cast<const float *>(
-                                ws + ((slot0 + sl) * 4 + q) * REGION + lane);
-#pragma unroll
-                            for (int j = 0; j < 32; j += 4) {
-                                const float4 x = ldcg4(src + ((c0 + j) / 4) * 32 * 4);
-                                v[j] += x.x;
-                                v[j + 1] += x.y;
-                                v[j + 2] += x.z;
-                                v[j + 3] += x.w;
-                            }
-                        }
-                        store_c_chunk(p, crow, r, n_tile + c0, v);
-                    }
-                }
+            for (int c0 = 0; c0 < C::BN; c0 += 32) {
+                float v[32];
+                tmem_ld32(tbase + c0, v);  // all lanes take part, rows in range or not
+                store_chunk(o, row_in_tile, c0, v);
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.acc_empty[acc.s]);
             acc.next();
         }
     }

@@ -88,26 +88,29 @@ int sgemm_batched_ex(int mode, int M, int N, int K, float alpha, const float *A,
                      int transB, long long strideA, long long strideB, long long strideC, int Q,
                      void *stream);
 
-/* Split-K workspace.  When the output has fewer 128 x 128 tiles than the GPU
- * has multiprocessors (small or skinny products, e.g. 1024^3 or the ragged
- * 1000 x 1500 x 777 case), the library can cut K into slices computed in
- * parallel and combine them -- the split-K scheme the SGEMM worklog sees
+/* Split-K workspace.  The output is cut into 128 x 128 tiles, one persistent
+ * CTA per multiprocessor.  When the tiles do not fill a whole number of waves
+ * (4092^3: 1024 tiles = 6.7 waves on 152 multiprocessors), or fill less than
+ * one (small or skinny products such as the ragged 1000 x 1500 x 777 case),
+ * the library can cut the tiles of the last, partial wave along K into
+ * slices computed in parallel -- the split-K scheme the SGEMM worklog sees
  * cuBLAS use at 256^3 ("From 1% to 94% of cuBLAS", comparison across sizes).
- * The partial sums need scratch memory, which the caller provides:
+ * Each slice's partial tile needs scratch memory, which the caller provides:
  *
- * sgemm_workspace_size returns the bytes of workspace the split path wants
- * for this shape on the current device (0: the shape is not split, or the
- * arguments are invalid, or there is no usable device).
+ * sgemm_workspace_size returns the bytes of workspace the preferred split
+ * plan wants for this shape on the current device (0: the shape is not
+ * split, or the arguments are invalid, or there is no usable device).
  *
  * sgemm_batched_ex_ws is sgemm_batched_ex plus a DEVICE workspace owned by
  * the caller: `workspace` must be 256-byte aligned when workspace_bytes > 0
- * (else SGEMM_ERR_INVALID_ARG).  With workspace_bytes at least
- * sgemm_workspace_size(...) the call may split K; with less (or NULL / 0)
- * it runs unsplit, with the same results up to rounding.  Every slice's
- * partial tile is stored in fp32 and the slices are summed in a fixed order,
- * so repeated calls give identical bits.  The call zeroes the workspace's
- * counter area on `stream` itself (no memset needed by the caller); the
- * workspace must not be used by another call running at the same time. */
+ * (else SGEMM_ERR_INVALID_ARG).  The call runs the best split plan whose
+ * workspace fits in workspace_bytes (with sgemm_workspace_size(...) bytes,
+ * the preferred one; with NULL / 0, none), with the same results up to
+ * rounding.  Every slice stores its partial tile in fp32; a second kernel,
+ * enqueued on `stream` right after the first, sums each tile's slices in a
+ * fixed order and applies alpha and beta, so repeated calls give identical
+ * bits.  The workspace needs no initialisation; it must not be used by
+ * another call running at the same time. */
 size_t sgemm_workspace_size(int mode, int M, int N, int K, int Q);
 int sgemm_batched_ex_ws(int mode, int M, int N, int K, float alpha, const float *A, int lda,
                         const float *B, int ldb, float beta, float *C, int ldc, int transA,
@@ -123,18 +126,20 @@ int sgemm_batched_ex_ws(int mode, int M, int N, int K, float alpha, const float 
  * at the point where it multiplies (a host callback, another library's
  * critical section, a plugin that is handed only its input and output
  * buffers).  The function allocates and frees nothing.
+ *  - It splits only grids of at most half as many tiles as the GPU has
+ *    multiprocessors, into as many slices as keep every slice in one wave
+ *    (at most one partial tile per multiprocessor); larger grids run
+ *    unsplit, exactly as sgemm_batched_ex.
  *  - Every GPU that loads the library holds the 12 MB until the process exits.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call
  *    before any stream capture.
- *  - All calls on a device share the array and it keeps the last call's
- *    contents; the call clears what must start at zero itself.  Calls whose
- *    kernels overlap on the GPU (different streams, or another thread) race
- *    on the array: serialise them.
- *  - A shape whose split workspace (sgemm_workspace_size) exceeds 12 MB
- *    returns SGEMM_ERR_SCRATCH_LIMIT and launches nothing; that cannot
- *    happen on a GPU with at most ~190 multiprocessors.  Shapes that do not
- *    split run exactly as sgemm_batched_ex. */
+ *  - All calls on a device share the array; it needs no initialisation.
+ *    Calls whose kernels overlap on the GPU (different streams, or another
+ *    thread) race on the array: serialise them.
+ *  - A shape whose split workspace exceeds 12 MB returns
+ *    SGEMM_ERR_SCRATCH_LIMIT and launches nothing; that cannot happen on a
+ *    GPU with at most ~190 multiprocessors. */
 int sgemm_batched_ex_noalloc(int mode, int M, int N, int K, float alpha, const float *A, int lda,
                              const float *B, int ldb, float beta, float *C, int ldc, int transA,
                              int transB, long long strideA, long long strideB, long long strideC,

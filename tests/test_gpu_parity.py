@@ -39,8 +39,8 @@ def supported(mode):
     assert st == lib.SGEMM_OK
 
 
-def check_full(prob, mode, oracle_mod, exact=False):
-    C = prob.run_gpu(mode)
+def check_full(prob, mode, oracle_mod, exact=False, api="ex"):
+    C = prob.run_gpu(mode, api=api)
     Cref, D = prob.oracle(oracle_mod)
     if exact:
         assert np.array_equal(C.astype(np.float64), Cref), "integer case not bit-exact"
@@ -49,8 +49,8 @@ def check_full(prob, mode, oracle_mod, exact=False):
     return err
 
 
-def check_rows(prob, mode, oracle_mod, rows, exact=False):
-    C = prob.run_gpu(mode)
+def check_rows(prob, mode, oracle_mod, rows, exact=False, api="ex"):
+    C = prob.run_gpu(mode, api=api)
     Cref, D = prob.oracle(oracle_mod, rows=rows)
     got = np.stack([C[q, i] for (q, i) in rows])
     if exact:
@@ -77,12 +77,13 @@ def test_sgemm_ragged_beta_zero_then_minus_two(oracle_mod, mode):
         check_full(Problem(w["A"], w["B"], w["C0"], w["alpha"], beta), mode, oracle_mod)
 
 
+@pytest.mark.parametrize("api", ["ex", "ws"])
 @pytest.mark.parametrize("mode", MODES)
-def test_sgemm_4092_sampled_rows(oracle_mod, mode):
+def test_sgemm_4092_sampled_rows(oracle_mod, mode, api):
     supported(mode)
     w = workloads.make("sgemm_4092")
     prob = Problem(w["A"], w["B"], w["C0"], w["alpha"], w["betas"][0])
-    C = check_rows(prob, mode, oracle_mod, sample_rows(1, 4092, 40, seed=2))
+    C = check_rows(prob, mode, oracle_mod, sample_rows(1, 4092, 40, seed=2), api=api)
     assert np.all(np.isfinite(C))
 
 
@@ -98,13 +99,14 @@ def test_size_sweep(oracle_mod, mode, n):
         check_rows(prob, mode, oracle_mod, sample_rows(1, n, 24, seed=n))
 
 
+@pytest.mark.parametrize("api", ["ex", "ws"])
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("transB", [1, 0])
-def test_batched_q32(oracle_mod, mode, transB):
+def test_batched_q32(oracle_mod, mode, transB, api):
     supported(mode)
     w = workloads.make("bmm_q32_1024x1024x512")
     prob = Problem(w["A"], w["B"], w["C0"], w["alpha"], w["betas"][0], transB=transB)
-    check_rows(prob, mode, oracle_mod, sample_rows(32, 1024, 64, seed=4))
+    check_rows(prob, mode, oracle_mod, sample_rows(32, 1024, 64, seed=4), api=api)
 
 
 # -------------------------------------------------------- exactness (integers)
@@ -124,12 +126,13 @@ def test_integer_inputs_bit_exact(oracle_mod, mode, shape, alpha, beta, tA, tB):
     check_full(Problem(A, B, C0, alpha, beta, transA=tA, transB=tB), mode, oracle_mod, exact=True)
 
 
+@pytest.mark.parametrize("api", ["ex", "ws"])
 @pytest.mark.parametrize("mode", MODES)
-def test_integer_4092_bit_exact_sampled(oracle_mod, mode):
+def test_integer_4092_bit_exact_sampled(oracle_mod, mode, api):
     supported(mode)
     A, B, C0 = workloads.integer_inputs(4092, 4092, 4092, seed=42)
     prob = Problem(A, B, C0, 1.0, 0.0)
-    check_rows(prob, mode, oracle_mod, sample_rows(1, 4092, 16, seed=3), exact=True)
+    check_rows(prob, mode, oracle_mod, sample_rows(1, 4092, 16, seed=3), exact=True, api=api)
 
 
 @pytest.mark.parametrize("mode", MODES)

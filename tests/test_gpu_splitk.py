@@ -1,7 +1,10 @@
-"""GPU parity of the split-K path (sgemm_batched_ex_ws): shapes with fewer
-output tiles than multiprocessors are cut along K, each slice's partial tile
-goes through the caller's workspace, and the last slice of every region sums
-them in slice order.  Checked against the fp64 oracle like every other path."""
+"""GPU parity of the split-K path (sgemm_batched_ex_ws): the tiles of a
+grid's last, partial wave (every tile of a grid smaller than the GPU) are cut
+along K, each slice's partial tile goes through the caller's workspace, and
+the last slice of every region sums them in slice order.  Checked against the
+fp64 oracle like every other path."""
+import math
+
 import numpy as np
 import pytest
 
@@ -20,6 +23,8 @@ SPLIT_SHAPES = [  # (M, N, K, Q, transA, transB, alpha, beta): all split on ever
     (300, 200, 2000, 1, 0, 1, 1.0, 0.25),    # skinny output, long K
     (200, 150, 600, 3, 1, 0, -1.0, 0.5),     # batched
     (1, 7, 4000, 1, 0, 0, 1.0, 0.0),         # a single row
+    (1664, 1664, 2048, 1, 0, 0, 1.0, 0.5),   # 169 tiles: one whole wave, the rest split
+    (1000, 1500, 777, 1, 0, 0, 1.0, -2.0),   # 96 tiles, under one wave: all split
 ]
 
 
@@ -77,13 +82,48 @@ def test_small_or_missing_workspace_runs_unsplit(oracle_mod, mode):
         assert oracle_mod.max_rel_err(C, Cref, D) <= TOL[mode]
 
 
+def planned_workspace(mode, M, N, K, Q, sms):
+    """The split plan as the library's header and planner describe it: whole
+    waves of 128 x 128 tiles, then the last wave's tiles cut into s slices
+    (s <= 16, each >= 64 deep for FP32 and >= 256 for the tensor paths),
+    s minimising floor(T/G) + ceil(r*s/G)/s + 0.01*s; returns its workspace
+    bytes (one 64 KB partial tile per split unit), 0 when it does not split."""
+    T = Q * math.ceil(M / 128) * math.ceil(N / 128)
+    full, rem = divmod(T, sms)
+    if rem == 0:
+        return 0
+    smax = min(16, K // (64 if mode == "fp32" else 256))
+    best_t, best = full + 1 + 0.01, 1
+    for s in range(2, smax + 1):
+        t = full + math.ceil(rem * s / sms) / s + 0.01 * s
+        if t < best_t - 1e-9:
+            best_t, best = t, s
+    if best == 1:
+        return 0
+    return rem * best * 128 * 128 * 4
+
+
+SIZE_CASES = [("fp32", 4092, 4092, 4092, 1), ("3xtf32", 4092, 4092, 4092, 1),
+              ("fp32", 1024, 1024, 128, 1), ("3xtf32", 1024, 1024, 128, 1),
+              ("fp32", 1000, 1500, 777, 1), ("tf32", 1000, 1500, 777, 1),
+              ("fp32", 1024, 1024, 32, 1), ("3xtf32", 1024, 1024, 512, 32),
+              ("fp32", 8192, 8192, 8192, 1), ("tf32", 2048, 2048, 2048, 1),
+              ("fp32", 1, 7, 4000, 1), ("3xtf32", 1664, 1664, 2048, 1)]
+
+
+@pytest.mark.parametrize("case", SIZE_CASES)
+def test_workspace_size_follows_the_plan(case):
+    import torch
+    import dense_fp32_matrix_03_gb300 as lib
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert lib.sgemm_workspace_size(*case) == planned_workspace(*case, sms)
+
+
 def test_workspace_size_query():
     import dense_fp32_matrix_03_gb300 as lib
-    assert lib.sgemm_workspace_size("fp32", 4092, 4092, 4092, 1) == 0    # fills the GPU already
-    assert lib.sgemm_workspace_size("fp32", 1024, 1024, 128, 1) > 0     # 4 k-blocks: 2 slices
-    assert lib.sgemm_workspace_size("3xtf32", 1024, 1024, 128, 1) == 0  # tensor path: >= 8 per slice
-    assert lib.sgemm_workspace_size("fp32", 1000, 1500, 777, 1) == 0    # 96 tiles: no room to split
     assert lib.sgemm_workspace_size("fp32", 1024, 1024, 32, 1) == 0      # one k-block: no split
+    assert lib.sgemm_workspace_size("3xtf32", 1024, 1024, 128, 1) == 0  # tensor path: >= 256 per slice
+    assert lib.sgemm_workspace_size("fp32", 1024, 1024, 128, 1) > 0     # 2 slices of 64
     assert lib.sgemm_workspace_size("fp32", 0, 10, 10, 1) == 0
     assert lib.sgemm_workspace_size(7, 100, 100, 100, 1) == 0
 
