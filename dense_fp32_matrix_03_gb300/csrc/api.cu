@@ -216,13 +216,24 @@ bool encode_operand(CUtensorMap *map, const float *base, bool kin, long long row
 
 int min_slice_k(int mode) { return mode == SGEMM_MODE_FP32 ? 64 : 256; }
 
-size_t splitk_workspace_bytes(long long split_tiles, int splits)
+// FLOP/s per multiprocessor each path sustains on GB300 (measured at 4092^3
+// with TMA-fed operands, and on the ragged 1000 x 1500 x 777 case, whose A
+// goes through the cp.async fallback).
+double path_rate_per_sm(int mode, bool tma)
 {
-    if (splits <= 1 || split_tiles <= 0) return 0;
-    return static_cast<size_t>(split_tiles) * splits * kSplitTile * kSplitTile * sizeof(float);
+    if (mode == SGEMM_MODE_FP32) return tma ? 0.40e12 : 0.24e12;
+    if (mode == SGEMM_MODE_3XTF32) return tma ? 1.54e12 : 0.16e12;
+    return tma ? 2.16e12 : 0.16e12;
 }
 
-SplitPlan choose_plan(long long num_tiles, int K, int num_sms, int mode, size_t budget)
+size_t splitk_workspace_bytes(long long split_tiles, int splits, int bm, int bn)
+{
+    if (splits <= 1 || split_tiles <= 0) return 0;
+    return static_cast<size_t>(split_tiles) * splits * static_cast<size_t>(bm) * bn * sizeof(float);
+}
+
+SplitPlan choose_plan(long long num_tiles, int K, int num_sms, int mode, int bm, int bn, bool tma,
+                      size_t budget)
 {
     SplitPlan best{1, num_tiles, 0};
     if (num_tiles <= 0 || num_sms <= 0) return best;
@@ -230,27 +241,34 @@ SplitPlan choose_plan(long long num_tiles, int K, int num_sms, int mode, size_t 
     if (rem == 0) return best;
     long long smax = K / min_slice_k(mode);
     if (smax > kMaxSplits) smax = kMaxSplits;
-    double best_t = static_cast<double>(full) + 1.0 + kSliceCost;
+    const double t_tile = 2.0 * bm * bn * static_cast<double>(K) / path_rate_per_sm(mode, tma);
+    const double t_whole = t_tile * static_cast<double>(full + 1);
+    double best_t = t_whole;
     for (int s = 2; s <= smax; ++s) {
+        const size_t ws = splitk_workspace_bytes(rem, s, bm, bn);
+        if (ws > budget) continue;
         const long long waves = (rem * s + num_sms - 1) / num_sms;
-        const double t = static_cast<double>(full) + static_cast<double>(waves) / s + kSliceCost * s;
-        const size_t ws = splitk_workspace_bytes(rem, s);
-        if (t < best_t - 1e-9 && ws <= budget) {
+        const double bw = ws <= (static_cast<size_t>(64) << 20) ? 8e12 : 3e12;
+        const double t = t_tile * (static_cast<double>(full) + static_cast<double>(waves) / s) +
+                         3e-6 + 2.0 * static_cast<double>(ws) / bw;
+        if (t < best_t) {
             best_t = t;
             best = SplitPlan{s, full * num_sms, ws};
         }
     }
+    if (best.splits > 1 && best_t > 0.99 * t_whole) best = SplitPlan{1, num_tiles, 0};
     return best;
 }
 
-int plan_splits(Plan &plan)
+int plan_splits(Plan &plan, int bm, int bn, bool tma)
 {
     GemmParams &p = plan.p;
     p.splits = 1;
     p.dp_tiles = p.num_tiles;
     p.ws_part = nullptr;
     if (plan.ws != nullptr) {
-        const SplitPlan sp = choose_plan(p.num_tiles, p.K, plan.num_sms, plan.mode, plan.ws_bytes);
+        const SplitPlan sp =
+            choose_plan(p.num_tiles, p.K, plan.num_sms, plan.mode, bm, bn, tma, plan.ws_bytes);
         if (sp.splits > 1) {
             p.splits = sp.splits;
             p.dp_tiles = sp.dp_tiles;
@@ -260,25 +278,6 @@ int plan_splits(Plan &plan)
     p.num_units = p.dp_tiles + (p.num_tiles - p.dp_tiles) * p.splits;
     return SGEMM_OK;
 }
-
-namespace {
-
-// Tiles of a call and the multiprocessors of the current device, or false.
-bool tiles_and_sms(int &mode, int M, int N, int K, int Q, long long &tiles, int &sms)
-{
-    if (mode == SGEMM_MODE_DEFAULT) mode = g_default_mode.load();
-    if (mode != SGEMM_MODE_FP32 && mode != SGEMM_MODE_3XTF32 && mode != SGEMM_MODE_TF32) return false;
-    if (M <= 0 || N <= 0 || K <= 0 || Q <= 0) return false;
-    int dev = 0;
-    const DeviceInfo *di = device_info(&dev);
-    if (di == nullptr) return false;
-    tiles = static_cast<long long>(Q) * ((M + kSplitTile - 1) / kSplitTile) *
-            ((N + kSplitTile - 1) / kSplitTile);
-    sms = di->num_sms;
-    return true;
-}
-
-}  // namespace
 
 int launch_fixup(Plan &plan, int bm, int bn)
 {
@@ -302,28 +301,66 @@ int launch_fixup(Plan &plan, int bm, int bn)
                : SGEMM_ERR_LAUNCH;
 }
 
+namespace {
+
+// The plans of a call for every tile shape its mode may use (the FP32 path's
+// depends on the operand layout, which the size queries do not take); the
+// one needing the most workspace is reported, so that a workspace of that
+// size serves the call whatever its layout.  one_wave: the allocation-free
+// entry point's rule (see one_wave_plan).
+SplitPlan plan_query(int mode, int M, int N, int K, int Q, bool one_wave)
+{
+    const SplitPlan none{1, 0, 0};
+    if (mode == SGEMM_MODE_DEFAULT) mode = g_default_mode.load();
+    if (mode != SGEMM_MODE_FP32 && mode != SGEMM_MODE_3XTF32 && mode != SGEMM_MODE_TF32) return none;
+    if (M <= 0 || N <= 0 || K <= 0 || Q <= 0) return none;
+    int dev = 0;
+    const DeviceInfo *di = device_info(&dev);
+    if (di == nullptr) return none;
+    const int sms = di->num_sms;
+    SplitPlan out = none;
+    for (int shape = 0; shape < (mode == SGEMM_MODE_FP32 ? 2 : 1); ++shape) {
+        int bm = 0, bn = 0;
+        if (mode == SGEMM_MODE_FP32)
+            simt_tile_dims(shape == 1, bm, bn);
+        else
+            tc_tile_dims(bm, bn);
+        const long long tiles =
+            static_cast<long long>(Q) * ((M + bm - 1) / bm) * ((N + bn - 1) / bn);
+        SplitPlan sp{1, tiles, 0};
+        if (!one_wave) {
+            // whether the operands go through TMA depends on pointers and
+            // leading dimensions the query does not take: plan for both
+            for (int tma = 0; tma < 2; ++tma) {
+                const SplitPlan t =
+                    choose_plan(tiles, K, sms, mode, bm, bn, tma != 0, ~static_cast<size_t>(0));
+                if (t.ws_bytes > sp.ws_bytes) sp = t;
+            }
+        } else if (2 * tiles <= sms) {
+            long long s = sms / tiles;
+            const long long by_k = K / min_slice_k(mode);
+            if (s > by_k) s = by_k;
+            if (s > kMaxSplits) s = kMaxSplits;
+            if (s >= 2)
+                sp = SplitPlan{static_cast<int>(s), 0,
+                               splitk_workspace_bytes(tiles, static_cast<int>(s), bm, bn)};
+        }
+        if (sp.ws_bytes > out.ws_bytes) out = sp;
+    }
+    return out;
+}
+
+}  // namespace
+
 SplitPlan preferred_plan(int mode, int M, int N, int K, int Q)
 {
-    long long tiles = 0;
-    int sms = 0;
-    if (!tiles_and_sms(mode, M, N, K, Q, tiles, sms)) return SplitPlan{1, 0, 0};
-    return choose_plan(tiles, K, sms, mode, ~static_cast<size_t>(0));
+    return plan_query(mode, M, N, K, Q, false);
 }
 
 SplitPlan one_wave_plan(int mode, int M, int N, int K, int Q)
 {
-    long long tiles = 0;
-    int sms = 0;
-    if (!tiles_and_sms(mode, M, N, K, Q, tiles, sms)) return SplitPlan{1, 0, 0};
-    if (2 * tiles > sms) return SplitPlan{1, tiles, 0};
-    long long s = sms / tiles;
-    const long long by_k = K / min_slice_k(mode);
-    if (s > by_k) s = by_k;
-    if (s > kMaxSplits) s = kMaxSplits;
-    if (s < 2) return SplitPlan{1, tiles, 0};
-    return SplitPlan{static_cast<int>(s), 0, splitk_workspace_bytes(tiles, static_cast<int>(s))};
+    return plan_query(mode, M, N, K, Q, true);
 }
-
 
 }  // namespace sg
 

@@ -23,38 +23,47 @@ struct Plan {
     size_t ws_bytes;
 };
 
-// Split-K plan shared by both kernels (128 x 128 output tiles, one
-// persistent CTA per multiprocessor).  With T tiles on G multiprocessors the
-// grid runs floor(T/G) whole waves and a last wave of T mod G tiles that
-// leaves the rest of the GPU idle.  The planner may cut the tiles of that
-// last wave (all tiles when T < G) along K into `splits` slices, so that the
-// slices spread over the whole GPU: modelled finishing time, in tile times,
-//     floor(T/G) + ceil((T mod G) * s / G) / s + kSliceCost * s,
-// minimised over s = 1 .. min(16, K / min_slice_k(mode)).  Each slice is at
-// least min_slice_k(mode) deep: 64 for the FP32 path, 256 for the
-// tensor-core paths, whose per-unit pipeline start-up (copy, split, MMA,
-// TMEM read-back) is longer (measured on GB300: shorter slices made
-// 128^3..512^3 slower).  The slices are whole k-blocks of the kernel that
-// runs (each kernel's k-block is at most the minimum slice, so no slice is
-// empty).  Each slice writes its partial tile, unscaled, to its own slot of
-// the workspace; a fix-up kernel launched right after on the same stream
-// sums every split tile's slots in slice order and applies alpha and beta.
-// The workspace is one 128 x 128 fp32 slot per (split tile, slice); a plan
-// whose workspace exceeds the caller's budget is not considered.
-constexpr int kSplitTile = 128;            // output tile edge of both paths
+// Split-K plan shared by both kernels (BM x BN output tiles, one persistent
+// CTA per multiprocessor).  With T tiles on G multiprocessors the grid runs
+// floor(T/G) whole waves and a last wave of r = T mod G tiles that leaves
+// the rest of the GPU idle.  The planner may cut the tiles of that last wave
+// (all tiles when T < G) along K into `splits` slices, so that the slices
+// spread over the whole GPU.  Each slice writes its partial tile, unscaled,
+// to its own BM x BN fp32 slot of the workspace, and a fix-up kernel
+// launched right after on the same stream sums every split tile's slots in
+// slice order and applies alpha and beta.  Modelled time of s slices:
+//     t_tile * (floor(T/G) + ceil(r * s / G) / s)
+//       + (s > 1: 3 us + 2 * workspace bytes / (8 TB/s if they stay in L2,
+//                                                 i.e. <= 64 MB, else 3 TB/s))
+// with t_tile = 2 * BM * BN * K / (per-multiprocessor rate of the path, as
+// measured on GB300: 0.40 TFLOP/s FP32, 1.54 3xTF32, 2.16 TF32 with TMA-fed
+// operands; 0.24, 0.16, 0.16 through the cp.async fallback).  s runs over
+// 1 .. min(16, K / min_slice_k(mode)); the best s is used only when it
+// saves at least 1%.  Each slice is at least
+// min_slice_k(mode) deep: 64 for the FP32 path, 256 for the tensor-core
+// paths, whose per-unit pipeline start-up (copy, split, MMA, TMEM
+// read-back) is longer (measured on GB300: shorter slices made 128^3..512^3
+// slower).  The slices are whole k-blocks of the kernel that runs (each
+// kernel's k-block is at most the minimum slice, so no slice is empty).  A
+// plan whose workspace exceeds the caller's budget is not considered.
 constexpr int kMaxSplits = 16;
-constexpr double kSliceCost = 0.01;        // per-slice overhead, in tile times
 struct SplitPlan {
     int splits;          // 1 = no split
     long long dp_tiles;  // tiles computed whole (they come first in unit order)
     size_t ws_bytes;     // workspace the plan needs
 };
 int min_slice_k(int mode);
-size_t splitk_workspace_bytes(long long split_tiles, int splits);
-SplitPlan choose_plan(long long num_tiles, int K, int num_sms, int mode, size_t budget);
-// Fills p.splits / dp_tiles / num_units / ws_part for the launch from the
-// best plan that fits the caller's workspace.  Returns an sgemm status.
-int plan_splits(Plan &plan);
+size_t splitk_workspace_bytes(long long split_tiles, int splits, int bm, int bn);
+SplitPlan choose_plan(long long num_tiles, int K, int num_sms, int mode, int bm, int bn, bool tma,
+                      size_t budget);
+// Fills p.splits / dp_tiles / num_units / ws_part for the launch (bm x bn
+// tiles, operands through TMA or not) from the best plan that fits the
+// caller's workspace.  Returns an sgemm status.
+int plan_splits(Plan &plan, int bm, int bn, bool tma);
+// Output tile of each kernel (defined beside its launcher); the FP32 path's
+// depends on whether both operands are K-inner.
+void simt_tile_dims(bool both_k_inner, int &bm, int &bn);
+void tc_tile_dims(int &bm, int &bn);
 // Enqueues the split-K fix-up for a launch whose plan split (bm x bn tiles).
 int launch_fixup(Plan &plan, int bm, int bn);
 // The plan sgemm_workspace_size reports for a call (no budget), or splits = 1.

@@ -10,21 +10,17 @@ namespace sg {
 
 namespace {
 
-// Tile configuration of the FP32 path (overridable at build time for
-// tuning sweeps): CTA tile BM x BN, warp tile WM x WN, pipeline stages of
-// SUBS x 32 k.  Measured on GB300 at 4092^3 (nn): 4 stages of 32 k, 50.1
-// TFLOP/s; 3 stages of 64 k, 52.8 (half the barrier round trips per FFMA).
-#ifndef SG_SIMT_BM
-#define SG_SIMT_BM 128
-#define SG_SIMT_BN 128
-#define SG_SIMT_WM 64
-#define SG_SIMT_WN 32
-#define SG_SIMT_STAGES 3
-#endif
-#ifndef SG_SIMT_SUBS
-#define SG_SIMT_SUBS 2
-#endif
-using SimtMain = SimtCfg<SG_SIMT_BM, SG_SIMT_BN, SG_SIMT_WM, SG_SIMT_WN, SG_SIMT_STAGES, SG_SIMT_SUBS>;
+// Tile configurations of the FP32 path.  Where one operand's fragment comes
+// in adjacent registers (every layout but A and B both K-inner), the FMAs are
+// packed two per instruction, and a wide lane tile (8 x 16 outputs, 64 x 64
+// per warp, 256 x 128 per CTA, two stages of 64 k) pays for the broadcast
+// of the other operand over twice as many FMAs.  With both operands K-inner
+// the FMAs stay scalar and the 8 x 8 lane tile (128 x 128 per CTA, three
+// stages of 64 k) is faster.  Measured on GB300 at 4092^3 with the last wave
+// split: nn 59.1 -> 63.2 TFLOP/s with the wide tile; nt 54.3 narrow, 51.6
+// wide.
+using SimtWide = SimtCfg<256, 128, 64, 64, 2, 2, 0>;
+using SimtNarrow = SimtCfg<128, 128, 64, 32, 3, 2, 1>;
 constexpr int kGroupM = 8;
 
 template <class Cfg, bool A_KIN, bool B_KIN, bool USE_TMA, bool EVEN_K>
@@ -45,21 +41,10 @@ int launch_one(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
     return plan.p.splits > 1 ? launch_fixup(plan, Cfg::BM, Cfg::BN) : SGEMM_OK;
 }
 
-template <class Cfg, bool USE_TMA, bool EVEN_K>
-int dispatch_layout(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
+// Plans and launches one layout with its tile configuration.
+template <class Cfg, bool A_KIN, bool B_KIN>
+int launch_cfg(Plan &plan)
 {
-    const bool a_kin = !plan.transA, b_kin = plan.transB;
-    if (a_kin && !b_kin) return launch_one<Cfg, true, false, USE_TMA, EVEN_K>(plan, tmA, tmB);
-    if (a_kin && b_kin) return launch_one<Cfg, true, true, USE_TMA, EVEN_K>(plan, tmA, tmB);
-    if (!a_kin && !b_kin) return launch_one<Cfg, false, false, USE_TMA, EVEN_K>(plan, tmA, tmB);
-    return launch_one<Cfg, false, true, USE_TMA, EVEN_K>(plan, tmA, tmB);
-}
-
-}  // namespace
-
-int launch_simt(Plan &plan)
-{
-    using Cfg = SimtMain;
     GemmParams &p = plan.p;
     p.tiles_m = (p.M + Cfg::BM - 1) / Cfg::BM;
     p.tiles_n = (p.N + Cfg::BN - 1) / Cfg::BN;
@@ -67,10 +52,6 @@ int launch_simt(Plan &plan)
     p.group_m = kGroupM;
     p.num_tiles = static_cast<long long>(p.Q) * p.tiles_m * p.tiles_n;
     plan.even_k = (p.K % Cfg::BK) == 0;
-    static_assert(Cfg::BM == kSplitTile && Cfg::BN == kSplitTile, "split-K workspace tile");
-    static_assert(kMinBlocks == 1, "the split planner assumes one CTA per multiprocessor");
-    const int rc = plan_splits(plan);
-    if (rc != SGEMM_OK) return rc;
 
     alignas(64) CUtensorMap tmA;
     alignas(64) CUtensorMap tmB;
@@ -78,12 +59,32 @@ int launch_simt(Plan &plan)
     std::memset(&tmB, 0, sizeof(tmB));
     bool use_tma = plan.a_tma && plan.b_tma;
     if (use_tma) {
-        use_tma = encode_operand(&tmA, p.A, !plan.transA, p.M, p.K, p.lda, p.Q, p.sA, Cfg::BM) &&
-                  encode_operand(&tmB, p.B, plan.transB, p.N, p.K, p.ldb, p.Q, p.sB, Cfg::BN);
+        use_tma = encode_operand(&tmA, p.A, A_KIN, p.M, p.K, p.lda, p.Q, p.sA, Cfg::BM) &&
+                  encode_operand(&tmB, p.B, B_KIN, p.N, p.K, p.ldb, p.Q, p.sB, Cfg::BN);
     }
-    if (use_tma) return dispatch_layout<Cfg, true, false>(plan, tmA, tmB);
-    if (plan.even_k) return dispatch_layout<Cfg, false, true>(plan, tmA, tmB);
-    return dispatch_layout<Cfg, false, false>(plan, tmA, tmB);
+    const int rc = plan_splits(plan, Cfg::BM, Cfg::BN, use_tma);
+    if (rc != SGEMM_OK) return rc;
+    if (use_tma) return launch_one<Cfg, A_KIN, B_KIN, true, false>(plan, tmA, tmB);
+    if (plan.even_k) return launch_one<Cfg, A_KIN, B_KIN, false, true>(plan, tmA, tmB);
+    return launch_one<Cfg, A_KIN, B_KIN, false, false>(plan, tmA, tmB);
+}
+
+}  // namespace
+
+void simt_tile_dims(bool both_k_inner, int &bm, int &bn)
+{
+    bm = both_k_inner ? SimtNarrow::BM : SimtWide::BM;
+    bn = both_k_inner ? SimtNarrow::BN : SimtWide::BN;
+}
+
+int launch_simt(Plan &plan)
+{
+    static_assert(kMinBlocks == 1, "the split planner assumes one CTA per multiprocessor");
+    const bool a_kin = !plan.transA, b_kin = plan.transB;
+    if (a_kin && b_kin) return launch_cfg<SimtNarrow, true, true>(plan);
+    if (a_kin) return launch_cfg<SimtWide, true, false>(plan);
+    if (b_kin) return launch_cfg<SimtWide, false, true>(plan);
+    return launch_cfg<SimtWide, false, false>(plan);
 }
 
 }  // namespace sg

@@ -41,6 +41,12 @@ int dispatch_layout(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
 
 }  // namespace
 
+void tc_tile_dims(int &bm, int &bn)
+{
+    bm = tc::BM;
+    bn = kBN;
+}
+
 int launch_tc(Plan &plan)
 {
     GemmParams &p = plan.p;
@@ -50,9 +56,6 @@ int launch_tc(Plan &plan)
     p.group_m = kGroupM;
     p.num_tiles = static_cast<long long>(p.Q) * p.tiles_m * p.tiles_n;
     plan.even_k = (p.K % tc::BK) == 0;
-    static_assert(tc::BM == kSplitTile && kBN == kSplitTile, "split-K workspace tile");
-    const int rc = plan_splits(plan);
-    if (rc != SGEMM_OK) return rc;
 
     alignas(64) CUtensorMap tmA;
     alignas(64) CUtensorMap tmB;
@@ -63,6 +66,8 @@ int launch_tc(Plan &plan)
         use_tma = encode_operand(&tmA, p.A, !plan.transA, p.M, p.K, p.lda, p.Q, p.sA, tc::BM) &&
                   encode_operand(&tmB, p.B, plan.transB, p.N, p.K, p.ldb, p.Q, p.sB, kBN);
     }
+    const int rc = plan_splits(plan, tc::BM, kBN, use_tma);
+    if (rc != SGEMM_OK) return rc;
     const bool split3 = plan.mode == SGEMM_MODE_3XTF32;
     if (split3) {
         return use_tma ? dispatch_layout<true, true>(plan, tmA, tmB)

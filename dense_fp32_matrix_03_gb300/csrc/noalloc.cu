@@ -21,9 +21,9 @@
 namespace {
 
 // Enough for the split-K workspace of this entry point's plan on a GPU with
-// up to ~190 multiprocessors (at most one 128 x 128 fp32 partial tile per
-// multiprocessor).
-constexpr size_t kScratchBytes = static_cast<size_t>(12) << 20;
+// up to ~190 multiprocessors (at most one partial tile per multiprocessor,
+// 256 x 128 fp32 at the largest).
+constexpr size_t kScratchBytes = static_cast<size_t>(24) << 20;
 
 // The scratch: shared by every call on a device; needs no initialisation.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];

@@ -46,10 +46,11 @@ constexpr int kSubK = 32;
 // A stage holds SUBS sub-blocks of K (BK = 32 * SUBS): all of A's
 // sub-blocks (each BM x 32), then all of B's.  More sub-blocks per stage
 // means fewer barrier round trips per FFMA.
-template <int BM_, int BN_, int WM_, int WN_, int STAGES_, int SUBS_ = 1>
+template <int BM_, int BN_, int WM_, int WN_, int STAGES_, int SUBS_ = 1, int LAG_ = 1>
 struct SimtCfg {
     static constexpr int BM = BM_, BN = BN_, WM = WM_, WN = WN_, STAGES = STAGES_;
     static constexpr int SUBS = SUBS_, BK = kSubK * SUBS_;
+    static constexpr int LAG = LAG_;  // see "Who fills the stages" below
     static constexpr int WARPS_M = BM / WM, WARPS_N = BN / WN;
     static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
     // The consumer warps issue the copies themselves (no producer warp), so
@@ -65,19 +66,16 @@ struct SimtCfg {
     static_assert(BM % WM == 0 && BN % WN == 0 && WM % 32 == 0 && WN % 16 == 0, "tile shape");
     static_assert(BM <= 256 && BN <= 256, "a TMA box spans at most 256 rows");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+    static_assert(LAG >= 0 && LAG < STAGES, "copies must run ahead of the consumers");
 };
 
 // Who fills the stages.  The CTA's k-blocks are numbered j = 0, 1, ... over
 // all of its tiles in order; k-block j lives in stage j % STAGES.  All stages
 // are filled up front; after the warps have consumed k-block `it`, the stage
-// of k-block it-kLag (which every warp has normally released by then) is
-// refilled, so the copies run STAGES-1-kLag k-blocks ahead of the consumers.
+// of k-block it-LAG (which every warp has normally released by then) is
+// refilled, so the copies run STAGES-1-LAG k-blocks ahead of the consumers.
 // The wait for that release is bounded like every other wait.  Positions are
 // advanced incrementally: no division on the per-k-block path.
-#ifndef SG_SIMT_LAG
-#define SG_SIMT_LAG 1
-#endif
-constexpr int kLag = SG_SIMT_LAG;
 // Unroll of the consumer's k-step loop; CTAs per SM the kernel is compiled for.
 #ifndef SG_SIMT_UNROLL
 #define SG_SIMT_UNROLL 4
@@ -182,7 +180,7 @@ struct TmaIssuer {
     {
         if (warp != 0) return true;
         int ok = 1;
-        if (lane == 0) ok = issue_to(it + 1 - kLag + Cfg::STAGES, ab) ? 1 : 0;
+        if (lane == 0) ok = issue_to(it + 1 - Cfg::LAG + Cfg::STAGES, ab) ? 1 : 0;
         return __shfl_sync(0xffffffffu, ok, 0) != 0;
     }
 
@@ -247,7 +245,7 @@ struct CpAsyncIssuer {
 
     __device__ __forceinline__ bool refill(long long it, const Abort &ab, int warp, int lane)
     {
-        return issue_to(it + 1 - kLag + Cfg::STAGES, ab, warp, lane);
+        return issue_to(it + 1 - Cfg::LAG + Cfg::STAGES, ab, warp, lane);
     }
 
     __device__ __forceinline__ void drain(long long, int, int)

@@ -121,7 +121,7 @@ int sgemm_batched_ex_ws(int mode, int M, int N, int K, float alpha, const float 
  * the pages: an addition of this library.)
  *
  * Same arguments and results as sgemm_batched_ex_ws, without the workspace:
- * the partial tiles live in a fixed 12 MB scratch array inside the library
+ * the partial tiles live in a fixed 24 MB scratch array inside the library
  * image.  For code that may not call cudaMalloc or may not grow a memory pool
  * at the point where it multiplies (a host callback, another library's
  * critical section, a plugin that is handed only its input and output
@@ -130,14 +130,14 @@ int sgemm_batched_ex_ws(int mode, int M, int N, int K, float alpha, const float 
  *    multiprocessors, into as many slices as keep every slice in one wave
  *    (at most one partial tile per multiprocessor); larger grids run
  *    unsplit, exactly as sgemm_batched_ex.
- *  - Every GPU that loads the library holds the 12 MB until the process exits.
+ *  - Every GPU that loads the library holds the 24 MB until the process exits.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call
  *    before any stream capture.
  *  - All calls on a device share the array; it needs no initialisation.
  *    Calls whose kernels overlap on the GPU (different streams, or another
  *    thread) race on the array: serialise them.
- *  - A shape whose split workspace exceeds 12 MB returns
+ *  - A shape whose split workspace exceeds 24 MB returns
  *    SGEMM_ERR_SCRATCH_LIMIT and launches nothing; that cannot happen on a
  *    GPU with at most ~190 multiprocessors. */
 int sgemm_batched_ex_noalloc(int mode, int M, int N, int K, float alpha, const float *A, int lda,

@@ -83,24 +83,40 @@ def test_small_or_missing_workspace_runs_unsplit(oracle_mod, mode):
 
 
 def planned_workspace(mode, M, N, K, Q, sms):
-    """The split plan as the library's header and planner describe it: whole
-    waves of 128 x 128 tiles, then the last wave's tiles cut into s slices
-    (s <= 16, each >= 64 deep for FP32 and >= 256 for the tensor paths),
-    s minimising floor(T/G) + ceil(r*s/G)/s + 0.01*s; returns its workspace
-    bytes (one 64 KB partial tile per split unit), 0 when it does not split."""
-    T = Q * math.ceil(M / 128) * math.ceil(N / 128)
-    full, rem = divmod(T, sms)
-    if rem == 0:
-        return 0
-    smax = min(16, K // (64 if mode == "fp32" else 256))
-    best_t, best = full + 1 + 0.01, 1
-    for s in range(2, smax + 1):
-        t = full + math.ceil(rem * s / sms) / s + 0.01 * s
-        if t < best_t - 1e-9:
-            best_t, best = t, s
-    if best == 1:
-        return 0
-    return rem * best * 128 * 128 * 4
+    """The split plan as the library's header and planner describe it, for
+    every output tile shape the mode may use (FP32: 256 x 128 where the FMAs
+    pair, 128 x 128 with both operands K-inner; tensor cores: 128 x 128):
+    whole waves of tiles, then the last wave's r tiles cut into s slices
+    (s <= 16, each >= 64 deep for FP32 and >= 256 for the tensor paths), s
+    minimising t_tile * (floor(T/G) + ceil(r*s/G)/s) + 3 us + 2 * ws / bw
+    (bw 8 TB/s up to 64 MB of workspace, else 3 TB/s; t_tile from the path's
+    per-multiprocessor rate with TMA-fed or cp.async-fed operands), used only
+    if it saves 1%; returns the largest workspace over the shapes and feeds
+    (one BM x BN fp32 slot per split unit), 0 when none splits."""
+    shapes = [(256, 128), (128, 128)] if mode == "fp32" else [(128, 128)]
+    need = 0
+    for (bm, bn), tma in [(sh, t) for sh in shapes for t in (False, True)]:
+        rate = {("fp32", True): 0.40e12, ("3xtf32", True): 1.54e12, ("tf32", True): 2.16e12,
+                ("fp32", False): 0.24e12, ("3xtf32", False): 0.16e12,
+                ("tf32", False): 0.16e12}[(mode, tma)]
+        T = Q * math.ceil(M / bm) * math.ceil(N / bn)
+        full, rem = divmod(T, sms)
+        if rem == 0:
+            continue
+        smax = min(16, K // (64 if mode == "fp32" else 256))
+        t_tile = 2.0 * bm * bn * float(K) / rate
+        t_whole = t_tile * float(full + 1)
+        best_t, best, best_ws = t_whole, 1, 0
+        for s in range(2, smax + 1):
+            ws = rem * s * bm * bn * 4
+            waves = (rem * s + sms - 1) // sms
+            bw = 8e12 if ws <= (64 << 20) else 3e12
+            t = t_tile * (float(full) + float(waves) / s) + 3e-6 + 2.0 * float(ws) / bw
+            if t < best_t:
+                best_t, best, best_ws = t, s, ws
+        if best > 1 and best_t <= 0.99 * t_whole:
+            need = max(need, best_ws)
+    return need
 
 
 SIZE_CASES = [("fp32", 4092, 4092, 4092, 1), ("3xtf32", 4092, 4092, 4092, 1),
