@@ -23,8 +23,8 @@ int launch_one(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
         return SGEMM_ERR_LAUNCH;
     long long grid = plan.p.num_units;
     if (grid > plan.num_sms) grid = plan.num_sms;
-    kern<<<static_cast<unsigned>(grid), tc::kThreads, C::SMEM_BYTES, plan.stream>>>(tmA, tmB,
-                                                                                  plan.p);
+    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, plan.stream>>>(tmA, tmB,
+                                                                                 plan.p);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
     return plan.p.splits > 1 ? launch_fixup(plan, tc::BM, kBN) : SGEMM_OK;
 }

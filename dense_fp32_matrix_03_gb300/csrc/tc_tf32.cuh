@@ -63,7 +63,7 @@ constexpr int kAConvWarp0 = 2;                   // warps 2-5: A -> TMEM
 constexpr int kBConvWarp0 = 6, kBConvWarps = 4;  // warps 6-9: B -> shared memory
 constexpr int kBConvThreads = kBConvWarps * 32;
 constexpr int kEpiWarp0 = kBConvWarp0 + kBConvWarps;  // warps 10-13: epilogue
-constexpr int kThreads = (kEpiWarp0 + 4) * 32;
+constexpr int kXProdWarp0 = kEpiWarp0 + 4;            // warps 14-: more cp.async producers
 constexpr int kConvWarps = 4 + kBConvWarps;      // arrivals that complete a stage
 constexpr uint32_t kTmemCols = 512;
 
@@ -71,6 +71,11 @@ template <int BN_, bool SPLIT3_, bool A_KIN_, bool B_KIN_, bool USE_TMA_>
 struct Cfg {
     static constexpr int BN = BN_;
     static constexpr bool SPLIT3 = SPLIT3_, A_KIN = A_KIN_, B_KIN = B_KIN_, USE_TMA = USE_TMA_;
+    // Producer warps: one lane issues the TMA copies; without TMA, the
+    // element-by-element cp.async copies of a stage are spread over warp 0
+    // and two extra warps (one warp alone could not keep the tensor core fed).
+    static constexpr int PROD_WARPS = USE_TMA ? 1 : 3;
+    static constexpr int THREADS = (kXProdWarp0 + PROD_WARPS - 1) * 32;
     static constexpr int A_BYTES = BM * BK * 4;          // one 128 x 32 fp32 tile
     static constexpr int B_BYTES = BN * BK * 4;
     static constexpr int RAW_BYTES = A_BYTES + B_BYTES;
@@ -419,7 +424,7 @@ struct Smem {
 };
 
 template <class C>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(C::THREADS, 1)
     tc_sgemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const GemmParams p)
 {
@@ -443,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::RAW_STAGES; ++s) {
-            mbar_init(&sm.raw_full[s], C::USE_TMA ? 1u : 32u);
+            mbar_init(&sm.raw_full[s], C::USE_TMA ? 1u : 32u * C::PROD_WARPS);
             mbar_init(&sm.raw_empty[s], kConvWarps);
         }
         for (int s = 0; s < C::SPLIT_STAGES; ++s) {
@@ -467,8 +472,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *sm.tmem_base;
     const Abort ab{sm.abort_flag, p.status, p.wait_limit};
 
-    if (warp == 0) {
-        // ------------------------------------------------ producer
+    if (warp == 0 || warp >= kXProdWarp0) {
+        // ------------------------------------------------ producer(s)
+        const int ptid = (warp == 0 ? 0 : warp - kXProdWarp0 + 1) * 32 + lane;
         Ring<C::RAW_STAGES> rr;
         long long issued = 0;
         bool ok = true;
@@ -502,9 +508,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = warp_wait(&sm.raw_empty[rr.s], rr.ph ^ 1u, ab, kStatusWaitEmpty, lane);
                     if (ok) {
                         cp_async_tile<BM, C::A_KIN, false>(sa, p.A + tc.q * p.sA, p.lda, m0, p.M,
-                                                           k0, p.K, p.a_vec4 != 0, lane, 32);
+                                                           k0, p.K, p.a_vec4 != 0, ptid,
+                                                           32 * C::PROD_WARPS);
                         cp_async_tile<C::BN, C::B_KIN, false>(sb, p.B + tc.q * p.sB, p.ldb, n0,
-                                                              p.N, k0, p.K, p.b_vec4 != 0, lane, 32);
+                                                              p.N, k0, p.K, p.b_vec4 != 0, ptid,
+                                                              32 * C::PROD_WARPS);
                         cp_async_arrive_noinc(&sm.raw_full[rr.s]);
                     }
                 }
