@@ -46,11 +46,13 @@ constexpr int kSubK = 32;
 // A stage holds SUBS sub-blocks of K (BK = 32 * SUBS): all of A's
 // sub-blocks (each BM x 32), then all of B's.  More sub-blocks per stage
 // means fewer barrier round trips per FFMA.
-template <int BM_, int BN_, int WM_, int WN_, int STAGES_, int SUBS_ = 1, int LAG_ = 1>
+template <int BM_, int BN_, int WM_, int WN_, int STAGES_, int SUBS_ = 1, int LAG_ = 1,
+          int KSTEP_ = 4>
 struct SimtCfg {
     static constexpr int BM = BM_, BN = BN_, WM = WM_, WN = WN_, STAGES = STAGES_;
     static constexpr int SUBS = SUBS_, BK = kSubK * SUBS_;
-    static constexpr int LAG = LAG_;  // see "Who fills the stages" below
+    static constexpr int LAG = LAG_;      // see "Who fills the stages" below
+    static constexpr int KSTEP = KSTEP_;  // k per fragment load (see Frag)
     static constexpr int WARPS_M = BM / WM, WARPS_N = BN / WN;
     static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
     // The consumer warps issue the copies themselves (no producer warp), so
@@ -67,6 +69,7 @@ struct SimtCfg {
     static_assert(BM <= 256 && BN <= 256, "a TMA box spans at most 256 rows");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     static_assert(LAG >= 0 && LAG < STAGES, "copies must run ahead of the consumers");
+    static_assert(KSTEP == 2 || KSTEP == 4, "fragment step");
 };
 
 // Who fills the stages.  The CTA's k-blocks are numbered j = 0, 1, ... over
@@ -265,22 +268,13 @@ __device__ __forceinline__ float4 lds128(uint32_t addr)
     return v;
 }
 
-// k values per fragment step: 4 (128-bit loads of K-inner rows) or 2 (64-bit
-// loads; an 8 x 8 lane tile then fits 128 registers, so two CTAs -- four
-// warps per scheduler -- fit on an SM).  Measured on GB300 at 4092^3 the two
-// are within 2%; 4 is the default.
-#ifndef SG_SIMT_KSTEP
-#define SG_SIMT_KSTEP 4
-#endif
-constexpr int kKStep = SG_SIMT_KSTEP;
-static_assert(kKStep == 2 || kKStep == 4, "fragment step");
-
-// Operand fragments of one k-step for one lane:
-// a[kk][i] = op(A)[row i of the lane, k = kKStep*g + kk], b[kk][j] likewise.
+// Operand fragments of one k-step (Cfg::KSTEP k values: 4 with 128-bit
+// loads of K-inner rows, 2 with 64-bit loads) for one lane:
+// a[kk][i] = op(A)[row i of the lane, k = KSTEP*g + kk], b[kk][j] likewise.
 template <class Cfg>
 struct Frag {
-    float a[kKStep][Cfg::TM];
-    float b[kKStep][Cfg::TN];
+    float a[Cfg::KSTEP][Cfg::TM];
+    float b[Cfg::KSTEP][Cfg::TN];
 };
 
 __device__ __forceinline__ float2 lds64(uint32_t addr)
@@ -293,9 +287,10 @@ __device__ __forceinline__ float2 lds64(uint32_t addr)
 // Byte offset, inside a lane's swizzled 128-byte row, of k-step g: the
 // 16-byte chunk (k / 4) moves by the XOR key, the 8-byte half (2-k steps)
 // stays in place.
+template <int KSTEP>
 __device__ __forceinline__ uint32_t kstep_offset(int g, uint32_t key)
 {
-    if (kKStep == 4) return (static_cast<uint32_t>(g) << 4) ^ key;
+    if (KSTEP == 4) return (static_cast<uint32_t>(g) << 4) ^ key;
     return ((static_cast<uint32_t>(g >> 1) << 4) ^ key) + (static_cast<uint32_t>(g & 1) << 3);
 }
 
@@ -305,9 +300,10 @@ template <class Cfg, bool A_KIN, bool B_KIN>
 __device__ __forceinline__ void load_frag(Frag<Cfg> &f, uint32_t a_base, uint32_t b_base,
                                           uint32_t a_key, uint32_t b_key, int g)
 {
+    constexpr int kKStep = Cfg::KSTEP;
     constexpr int WMITER = Cfg::WMITER, WNITER = Cfg::WNITER;
     if (A_KIN) {
-        const uint32_t ag = a_base + kstep_offset(g, a_key);
+        const uint32_t ag = a_base + kstep_offset<kKStep>(g, a_key);
 #pragma unroll
         for (int wm = 0; wm < WMITER; ++wm)
 #pragma unroll
@@ -339,8 +335,8 @@ __device__ __forceinline__ void load_frag(Frag<Cfg> &f, uint32_t a_base, uint32_
     }
     if (B_KIN) {
         // rows j = 1, 3 of a 4-row group have the swizzle key lc + 4
-        const uint32_t bg0 = b_base + kstep_offset(g, b_key);
-        const uint32_t bg1 = b_base + kstep_offset(g, b_key ^ (4u << 4));
+        const uint32_t bg0 = b_base + kstep_offset<kKStep>(g, b_key);
+        const uint32_t bg1 = b_base + kstep_offset<kKStep>(g, b_key ^ (4u << 4));
 #pragma unroll
         for (int wn = 0; wn < WNITER; ++wn)
 #pragma unroll
@@ -417,7 +413,7 @@ __device__ __forceinline__ void ffma2(uint64_t &d, uint64_t a, uint64_t b)
 // TM x TN fp32 accumulators of one lane, stored as PD says.
 template <class Cfg, int PD>
 struct Acc {
-    static constexpr int TM = Cfg::TM, TN = Cfg::TN;
+    static constexpr int TM = Cfg::TM, TN = Cfg::TN, kKStep = Cfg::KSTEP;
     static constexpr int R = PD == kPairI ? TM / 2 : TM;
     static constexpr int C = PD == kPairJ ? TN / 2 : TN;
     using T = typename std::conditional<PD == kPairNone, float, uint64_t>::type;
@@ -503,7 +499,7 @@ __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem
 {
     constexpr int WMITER = Cfg::WMITER, WNITER = Cfg::WNITER, TM = Cfg::TM, TN = Cfg::TN;
     constexpr int BM = Cfg::BM, BN = Cfg::BN;
-    constexpr int GROUPS = kSubK / kKStep;  // k-steps per sub-block
+    constexpr int GROUPS = kSubK / Cfg::KSTEP;  // k-steps per sub-block
     const int wm0 = (cw / Cfg::WARPS_N) * Cfg::WM;
     const int wn0 = (cw % Cfg::WARPS_N) * Cfg::WN;
     const int lr = lane >> 2, lc = lane & 3;
