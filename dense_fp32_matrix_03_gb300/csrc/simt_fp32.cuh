@@ -63,7 +63,8 @@ struct SimtCfg {
     static constexpr int A_SUB = BM * kSubK * 4, B_SUB = BN * kSubK * 4;
     static constexpr int A_BYTES = SUBS * A_SUB, B_BYTES = SUBS * B_SUB;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int BAR_BYTES = 2 * STAGES * 8 + 16;
+    // full/empty barriers, abort flag, release counters, the issue cursor
+    static constexpr int BAR_BYTES = 2 * STAGES * 8 + 16 + 4 * STAGES + 4 + 64;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
     static_assert(BM % WM == 0 && BN % WN == 0 && WM % 32 == 0 && WN % 16 == 0, "tile shape");
     static_assert(BM <= 256 && BN <= 256, "a TMA box spans at most 256 rows");
@@ -127,7 +128,23 @@ struct KPos {
     }
 };
 
-// TMA: lane 0 of warp 0 issues two tensor loads per stage.
+// Where the next k-block to load comes from: the cursor lives in shared
+// memory and is advanced by whichever warp issues the next copy.
+struct IssueCursor {
+    KPos pos;
+    long long issued;  // k-blocks issued so far
+};
+
+// TMA: the stages are refilled by the last warp to release them.  Every warp
+// counts its release of a stage on that stage's counter (an acq_rel atomic);
+// the warp that completes a round of the count knows that every warp is
+// done reading the stage, and at once issues the copies of the k-block that
+// goes there next (STAGES k-blocks later), so no warp ever waits for a
+// stage to become free.  The stages are released in k-block order (a warp
+// releases k-block j before j + 1), so the refills, and the cursor they
+// advance, follow k-block order too; each refill reads the cursor the
+// previous one wrote (ordered by the release-acquire chain of the counters).
+// Lane 0 of warp 0 issues the first STAGES k-blocks.
 template <class Cfg, bool A_KIN, bool B_KIN>
 struct TmaIssuer {
     static constexpr unsigned kFullCount = 1;
@@ -135,62 +152,74 @@ struct TmaIssuer {
     const GemmParams *p;
     uint8_t *smem;
     uint64_t *full, *empty;
-    long long total;   // k-blocks this CTA will consume
-    long long issued;  // k-blocks issued so far (lane 0 of warp 0)
-    KPos pos;          // next k-block to issue
+    unsigned int *released;  // per stage: warps that released it, ever (mod 2^32)
+    IssueCursor *cur;
+    long long total;         // k-blocks this CTA will consume
 
-    // Issues k-blocks until `target` (exclusive) have been issued.
-    __device__ __forceinline__ bool issue_to(long long target, const Abort &ab)
+    __device__ __forceinline__ void issue(KPos &pos)
     {
-        if (target > total) target = total;
-        while (issued < target) {
-            const int s = pos.stage;
-            // a fresh barrier passes parity 1 at once, so the first round
-            // needs no special case
-            if (!mbar_wait(&empty[s], pos.phase ^ 1u, ab, kStatusWaitEmpty)) return false;
-            uint8_t *sa = smem + s * Cfg::STAGE_BYTES;
-            uint8_t *sb = sa + Cfg::A_BYTES;
-            const int m0 = pos.tc.tm * Cfg::BM, n0 = pos.tc.tn * Cfg::BN;
-            const int qa = pos.tc.q * p->a_q_step, qb = pos.tc.q * p->b_q_step;
-            mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
+        const int s = pos.stage;
+        uint8_t *sa = smem + s * Cfg::STAGE_BYTES;
+        uint8_t *sb = sa + Cfg::A_BYTES;
+        const int m0 = pos.tc.tm * Cfg::BM, n0 = pos.tc.tn * Cfg::BN;
+        const int qa = pos.tc.q * p->a_q_step, qb = pos.tc.q * p->b_q_step;
+        mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
 #pragma unroll
-            for (int sub = 0; sub < Cfg::SUBS; ++sub) {
-                const int k0 = pos.kb * Cfg::BK + sub * kSubK;
-                if (A_KIN) tma_load_3d(sa + sub * Cfg::A_SUB, tmA, &full[s], k0, m0, qa);
-                else       tma_load_3d(sa + sub * Cfg::A_SUB, tmA, &full[s], m0, k0, qa);
-                if (B_KIN) tma_load_3d(sb + sub * Cfg::B_SUB, tmB, &full[s], k0, n0, qb);
-                else       tma_load_3d(sb + sub * Cfg::B_SUB, tmB, &full[s], n0, k0, qb);
-            }
-            ++issued;
-            pos.template next<Cfg::STAGES>(*p);
+        for (int sub = 0; sub < Cfg::SUBS; ++sub) {
+            const int k0 = pos.kb * Cfg::BK + sub * kSubK;
+            if (A_KIN) tma_load_3d(sa + sub * Cfg::A_SUB, tmA, &full[s], k0, m0, qa);
+            else       tma_load_3d(sa + sub * Cfg::A_SUB, tmA, &full[s], m0, k0, qa);
+            if (B_KIN) tma_load_3d(sb + sub * Cfg::B_SUB, tmB, &full[s], k0, n0, qb);
+            else       tma_load_3d(sb + sub * Cfg::B_SUB, tmB, &full[s], n0, k0, qb);
         }
-        return true;
+        pos.template next<Cfg::STAGES>(*p);
     }
 
-    __device__ __forceinline__ void prologue(int warp, int lane, const Abort &ab)
+    // Fills every stage once; the CTA synchronises before the first refill.
+    __device__ __forceinline__ void prologue(int warp, int lane, const Abort &)
     {
         if (warp != 0 || lane != 0) return;
         tma_prefetch_desc(tmA);
         tma_prefetch_desc(tmB);
-        issued = 0;
+        KPos pos;
         pos.start(*p);
-        issue_to(Cfg::STAGES, ab);
+        long long n = 0;
+        for (; n < Cfg::STAGES && n < total; ++n) issue(pos);
+        cur->pos = pos;
+        cur->issued = n;
+        for (int s = 0; s < Cfg::STAGES; ++s) released[s] = 0u;
     }
 
-    // Called by every lane of every consumer warp after k-block `it` was
-    // consumed and released.  Returns false (warp-uniformly) on abort.
-    __device__ __forceinline__ bool refill(long long it, const Abort &ab, int warp, int lane)
+    // Called by every lane of every consumer warp after it consumed the
+    // k-block in stage `s`.  Never waits.
+    __device__ __forceinline__ bool refill(long long, const Abort &, int, int lane, int s)
     {
-        if (warp != 0) return true;
-        int ok = 1;
-        if (lane == 0) ok = issue_to(it + 1 - Cfg::LAG + Cfg::STAGES, ab) ? 1 : 0;
-        return __shfl_sync(0xffffffffu, ok, 0) != 0;
+        __syncwarp();
+        if (lane == 0) {
+            unsigned int before;
+            asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                         : "=r"(before)
+                         : "r"(smem_u32(&released[s]))
+                         : "memory");
+            if (before % Cfg::CONSUMER_WARPS == Cfg::CONSUMER_WARPS - 1) {
+                const long long n = cur->issued;
+                if (n < total) {
+                    KPos pos = cur->pos;
+                    issue(pos);
+                    cur->pos = pos;
+                    cur->issued = n + 1;
+                }
+            }
+        }
+        return true;
     }
 
-    // After an abort: let every issued copy land before the CTA exits.
+    // After an abort (every warp has left its loop): let every issued copy
+    // land before the CTA exits.
     __device__ __forceinline__ void drain(long long limit, int warp, int lane)
     {
         if (warp != 0 || lane != 0) return;
+        const long long issued = cur->issued;
         for (long long j = issued - 1; j >= 0 && j >= issued - Cfg::STAGES; --j)
             mbar_drain(&full[j % Cfg::STAGES], static_cast<uint32_t>((j / Cfg::STAGES) & 1),
                        limit);
@@ -246,8 +275,15 @@ struct CpAsyncIssuer {
         issue_to(Cfg::STAGES, ab, warp, lane);
     }
 
-    __device__ __forceinline__ bool refill(long long it, const Abort &ab, int warp, int lane)
+    // Called by every lane of every consumer warp after it consumed the
+    // k-block `it` in stage `s`: releases the stage, then copies what this
+    // thread owes of the k-blocks up to it + 1 - LAG + STAGES (waiting, with
+    // a bound, until every warp has released the stages they go to).
+    __device__ __forceinline__ bool refill(long long it, const Abort &ab, int warp, int lane,
+                                           int s)
     {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
         return issue_to(it + 1 - Cfg::LAG + Cfg::STAGES, ab, warp, lane);
     }
 
@@ -546,9 +582,7 @@ __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem
                                              g % GROUPS);
                 accp.fma(f);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[cs]);
-            if (!iss.refill(it, ab, cw, lane)) return;
+            if (!iss.refill(it, ab, cw, lane, cs)) return;
             if (++cs == Cfg::STAGES) {
                 cs = 0;
                 cph ^= 1u;
@@ -629,6 +663,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, kMinBlocks)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
     uint64_t *empty = full + Cfg::STAGES;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + Cfg::STAGES);
+    unsigned int *released = reinterpret_cast<unsigned int *>(empty + Cfg::STAGES) + 1;
+    IssueCursor *cursor = reinterpret_cast<IssueCursor *>(
+        (reinterpret_cast<uintptr_t>(released + Cfg::STAGES) + 7) & ~static_cast<uintptr_t>(7));
+    static_assert(sizeof(IssueCursor) <= 48, "issue cursor fits the bookkeeping bytes");
     using Issuer = typename std::conditional<USE_TMA, TmaIssuer<Cfg, A_KIN, B_KIN>,
                                              CpAsyncIssuer<Cfg, A_KIN, B_KIN, EVEN_K>>::type;
 
@@ -660,6 +698,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, kMinBlocks)
     if constexpr (USE_TMA) {
         iss.tmA = &tmA;
         iss.tmB = &tmB;
+        iss.released = released;
+        iss.cur = cursor;
     }
     iss.p = &p;
     iss.smem = smem;
@@ -667,9 +707,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, kMinBlocks)
     iss.empty = empty;
     iss.total = my_kblocks;
     iss.prologue(warp, lane, ab);
-    __syncwarp();
+    __syncthreads();  // the cursor and release counters are set up
     simt_consumer<Cfg, A_KIN, B_KIN>(p, smem, full, empty, ab, warp, lane, iss);
-    __syncwarp();
+    __syncthreads();  // no copy is issued after this point
     if (*abort_flag) iss.drain(ab.limit, warp, lane);
     __syncthreads();
 }
