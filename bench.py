@@ -406,6 +406,9 @@ def main():
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": UNIT,
                 "frac": achieved / peak, "traffic": traffic,
                 "kernel": f"sgemm {mode} path ({kernel_key})",
+                "timed": ("each call: the GEMM kernel and the split-K fix-up kernel (events "
+                          "bracket the whole call; traffic is the GEMM kernel's)" if ws_bytes
+                          else "each call: the GEMM kernel"),
                 "peak_source": f"{peak_note}; {peak_src} MEASURED_PEAKS.json" if bound != "alu"
                 else peak_note,
                 "algorithmic_flops_per_launch": flops_step}
