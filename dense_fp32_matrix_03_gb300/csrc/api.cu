@@ -218,12 +218,13 @@ int min_slice_k(int mode) { return mode == SGEMM_MODE_FP32 ? 64 : 256; }
 
 // FLOP/s per multiprocessor each path sustains on GB300 (measured at 4092^3
 // with TMA-fed operands, and on the ragged 1000 x 1500 x 777 case, whose A
-// goes through the cp.async fallback).
+// TMA cannot describe: the FP32 kernel's cp.async fallback, the tensor-core
+// direct kernel).
 double path_rate_per_sm(int mode, bool tma)
 {
     if (mode == SGEMM_MODE_FP32) return tma ? 0.40e12 : 0.24e12;
-    if (mode == SGEMM_MODE_3XTF32) return tma ? 1.54e12 : 0.16e12;
-    return tma ? 2.16e12 : 0.16e12;
+    if (mode == SGEMM_MODE_3XTF32) return tma ? 1.54e12 : 0.47e12;
+    return tma ? 2.16e12 : 0.55e12;
 }
 
 size_t splitk_workspace_bytes(long long split_tiles, int splits, int bm, int bn)

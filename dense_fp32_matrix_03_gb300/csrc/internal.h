@@ -37,7 +37,7 @@ struct Plan {
 //                                                 i.e. <= 64 MB, else 3 TB/s))
 // with t_tile = 2 * BM * BN * K / (per-multiprocessor rate of the path, as
 // measured on GB300: 0.40 TFLOP/s FP32, 1.54 3xTF32, 2.16 TF32 with TMA-fed
-// operands; 0.24, 0.16, 0.16 through the cp.async fallback).  s runs over
+// operands; 0.24, 0.47, 0.55 for operands TMA cannot describe).  s runs over
 // 1 .. min(16, K / min_slice_k(mode)); the best s is used only when it
 // saves at least 1%.  Each slice is at least
 // min_slice_k(mode) deep: 64 for the FP32 path, 256 for the tensor-core

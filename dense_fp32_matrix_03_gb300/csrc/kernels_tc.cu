@@ -1,9 +1,18 @@
-// kernels_tc.cu -- host launcher of the tcgen05 tensor-core paths
-// (tc_tf32.cuh): 3xTF32 (FP32 accuracy) and plain TF32.
+// kernels_tc.cu -- host launcher of the tcgen05 tensor-core paths: 3xTF32
+// (FP32 accuracy) and plain TF32.  Operands TMA can describe run on the TMA
+// kernel (tc_tf32.cuh), whose copy engine stages them in shared memory;
+// others (a row pitch or batch stride that is not a multiple of 16 bytes, an
+// unaligned base) run on the direct kernel (tc_direct.cuh), whose converter
+// warps load them from global memory themselves.  Measured on GB300: the
+// direct kernel runs the ragged 1000 x 1500 x 777 case (lda = 777) at 43
+// TFLOP/s where staging it with cp.async gave 19-25, but it is slower than
+// TMA for aligned operands (232 vs 114 TFLOP/s at 4092^3: its loads wait on
+// L2 latency that the TMA ring hides).
 #include <cstring>
 
 #include "../../include/sgemm.h"
 #include "internal.h"
+#include "tc_direct.cuh"
 #include "tc_tf32.cuh"
 
 namespace sg {
@@ -13,30 +22,51 @@ namespace {
 constexpr int kBN = 128;
 constexpr int kGroupM = 8;
 
-template <bool SPLIT3, bool A_KIN, bool B_KIN, bool USE_TMA>
-int launch_one(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
+template <bool SPLIT3, bool A_KIN, bool B_KIN>
+int launch_tma(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
 {
-    using C = tc::Cfg<kBN, SPLIT3, A_KIN, B_KIN, USE_TMA>;
+    using C = tc::Cfg<kBN, SPLIT3, A_KIN, B_KIN>;
     auto kern = tc::tc_sgemm_kernel<C>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
     long long grid = plan.p.num_units;
     if (grid > plan.num_sms) grid = plan.num_sms;
-    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, plan.stream>>>(tmA, tmB,
-                                                                                 plan.p);
+    kern<<<static_cast<unsigned>(grid), tc::kThreads, C::SMEM_BYTES, plan.stream>>>(tmA, tmB,
+                                                                                  plan.p);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
     return plan.p.splits > 1 ? launch_fixup(plan, tc::BM, kBN) : SGEMM_OK;
 }
 
-template <bool SPLIT3, bool USE_TMA>
-int dispatch_layout(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
+template <bool SPLIT3, bool A_KIN, bool B_KIN>
+int launch_direct(Plan &plan)
+{
+    using C = tcd::Cfg<kBN, SPLIT3, A_KIN, B_KIN>;
+    auto kern = tcd::tcd_sgemm_kernel<C>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
+    long long grid = plan.p.num_units;
+    if (grid > plan.num_sms) grid = plan.num_sms;
+    kern<<<static_cast<unsigned>(grid), tcd::kThreads, C::SMEM_BYTES, plan.stream>>>(plan.p);
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    return plan.p.splits > 1 ? launch_fixup(plan, tc::BM, kBN) : SGEMM_OK;
+}
+
+template <bool SPLIT3>
+int dispatch(Plan &plan, bool use_tma, const CUtensorMap &tmA, const CUtensorMap &tmB)
 {
     const bool a_kin = !plan.transA, b_kin = plan.transB;
-    if (a_kin && !b_kin) return launch_one<SPLIT3, true, false, USE_TMA>(plan, tmA, tmB);
-    if (a_kin && b_kin) return launch_one<SPLIT3, true, true, USE_TMA>(plan, tmA, tmB);
-    if (!a_kin && !b_kin) return launch_one<SPLIT3, false, false, USE_TMA>(plan, tmA, tmB);
-    return launch_one<SPLIT3, false, true, USE_TMA>(plan, tmA, tmB);
+    if (use_tma) {
+        if (a_kin && !b_kin) return launch_tma<SPLIT3, true, false>(plan, tmA, tmB);
+        if (a_kin && b_kin) return launch_tma<SPLIT3, true, true>(plan, tmA, tmB);
+        if (!a_kin && !b_kin) return launch_tma<SPLIT3, false, false>(plan, tmA, tmB);
+        return launch_tma<SPLIT3, false, true>(plan, tmA, tmB);
+    }
+    if (a_kin && !b_kin) return launch_direct<SPLIT3, true, false>(plan);
+    if (a_kin && b_kin) return launch_direct<SPLIT3, true, true>(plan);
+    if (!a_kin && !b_kin) return launch_direct<SPLIT3, false, false>(plan);
+    return launch_direct<SPLIT3, false, true>(plan);
 }
 
 }  // namespace
@@ -68,13 +98,8 @@ int launch_tc(Plan &plan)
     }
     const int rc = plan_splits(plan, tc::BM, kBN, use_tma);
     if (rc != SGEMM_OK) return rc;
-    const bool split3 = plan.mode == SGEMM_MODE_3XTF32;
-    if (split3) {
-        return use_tma ? dispatch_layout<true, true>(plan, tmA, tmB)
-                       : dispatch_layout<true, false>(plan, tmA, tmB);
-    }
-    return use_tma ? dispatch_layout<false, true>(plan, tmA, tmB)
-                   : dispatch_layout<false, false>(plan, tmA, tmB);
+    return plan.mode == SGEMM_MODE_3XTF32 ? dispatch<true>(plan, use_tma, tmA, tmB)
+                                          : dispatch<false>(plan, use_tma, tmA, tmB);
 }
 
 }  // namespace sg

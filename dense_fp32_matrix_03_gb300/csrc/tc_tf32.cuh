@@ -18,7 +18,8 @@
 // margin.
 //
 // Data flow per 128 x BN output tile and 32-wide k-block:
-//   TMA (or cp.async)  raw fp32 A and B tiles -> shared-memory raw ring
+//   TMA                raw fp32 A and B tiles -> shared-memory raw ring
+//                      (operands TMA cannot describe go to tc_direct.cuh)
 //   A converters       raw A rows -> hi/lo planes in TMEM (tcgen05.st); the
 //                      MMA reads A from TMEM, so A's split planes never
 //                      touch shared memory
@@ -63,19 +64,14 @@ constexpr int kAConvWarp0 = 2;                   // warps 2-5: A -> TMEM
 constexpr int kBConvWarp0 = 6, kBConvWarps = 4;  // warps 6-9: B -> shared memory
 constexpr int kBConvThreads = kBConvWarps * 32;
 constexpr int kEpiWarp0 = kBConvWarp0 + kBConvWarps;  // warps 10-13: epilogue
-constexpr int kXProdWarp0 = kEpiWarp0 + 4;            // warps 14-: more cp.async producers
+constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 constexpr int kConvWarps = 4 + kBConvWarps;      // arrivals that complete a stage
 constexpr uint32_t kTmemCols = 512;
 
-template <int BN_, bool SPLIT3_, bool A_KIN_, bool B_KIN_, bool USE_TMA_>
+template <int BN_, bool SPLIT3_, bool A_KIN_, bool B_KIN_>
 struct Cfg {
     static constexpr int BN = BN_;
-    static constexpr bool SPLIT3 = SPLIT3_, A_KIN = A_KIN_, B_KIN = B_KIN_, USE_TMA = USE_TMA_;
-    // Producer warps: one lane issues the TMA copies; without TMA, the
-    // element-by-element cp.async copies of a stage are spread over warp 0
-    // and two extra warps (one warp alone could not keep the tensor core fed).
-    static constexpr int PROD_WARPS = USE_TMA ? 1 : 3;
-    static constexpr int THREADS = (kXProdWarp0 + PROD_WARPS - 1) * 32;
+    static constexpr bool SPLIT3 = SPLIT3_, A_KIN = A_KIN_, B_KIN = B_KIN_;
     static constexpr int A_BYTES = BM * BK * 4;          // one 128 x 32 fp32 tile
     static constexpr int B_BYTES = BN * BK * 4;
     static constexpr int RAW_BYTES = A_BYTES + B_BYTES;
@@ -424,7 +420,7 @@ struct Smem {
 };
 
 template <class C>
-__global__ void __launch_bounds__(C::THREADS, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     tc_sgemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const GemmParams p)
 {
@@ -448,7 +444,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::RAW_STAGES; ++s) {
-            mbar_init(&sm.raw_full[s], C::USE_TMA ? 1u : 32u * C::PROD_WARPS);
+            mbar_init(&sm.raw_full[s], 1u);
             mbar_init(&sm.raw_empty[s], kConvWarps);
         }
         for (int s = 0; s < C::SPLIT_STAGES; ++s) {
@@ -472,13 +468,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const uint32_t tmem = *sm.tmem_base;
     const Abort ab{sm.abort_flag, p.status, p.wait_limit};
 
-    if (warp == 0 || warp >= kXProdWarp0) {
-        // ------------------------------------------------ producer(s)
-        const int ptid = (warp == 0 ? 0 : warp - kXProdWarp0 + 1) * 32 + lane;
+    if (warp == 0) {
+        // ------------------------------------------------ producer
         Ring<C::RAW_STAGES> rr;
         long long issued = 0;
         bool ok = true;
-        if (C::USE_TMA && lane == 0) {
+        if (lane == 0) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
         }
@@ -490,50 +485,30 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 uint8_t *sa = sm.raw + rr.s * C::RAW_BYTES;
                 uint8_t *sb = sa + C::A_BYTES;
                 const int k0 = kb * BK;
-                if (C::USE_TMA) {
-                    if (lane == 0) {
-                        if (!mbar_wait(&sm.raw_empty[rr.s], rr.ph ^ 1u, ab, kStatusWaitEmpty)) {
-                            ok = false;
-                        } else {
-                            const int qa = tc.q * p.a_q_step, qb = tc.q * p.b_q_step;
-                            mbar_arrive_expect_tx(&sm.raw_full[rr.s], C::RAW_BYTES);
-                            if (C::A_KIN) tma_load_3d(sa, &tmA, &sm.raw_full[rr.s], k0, m0, qa);
-                            else          tma_load_3d(sa, &tmA, &sm.raw_full[rr.s], m0, k0, qa);
-                            if (C::B_KIN) tma_load_3d(sb, &tmB, &sm.raw_full[rr.s], k0, n0, qb);
-                            else          tma_load_3d(sb, &tmB, &sm.raw_full[rr.s], n0, k0, qb);
-                        }
-                    }
-                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                } else {
-                    ok = warp_wait(&sm.raw_empty[rr.s], rr.ph ^ 1u, ab, kStatusWaitEmpty, lane);
-                    if (ok) {
-                        cp_async_tile<BM, C::A_KIN, false>(sa, p.A + tc.q * p.sA, p.lda, m0, p.M,
-                                                           k0, p.K, p.a_vec4 != 0, ptid,
-                                                           32 * C::PROD_WARPS);
-                        cp_async_tile<C::BN, C::B_KIN, false>(sb, p.B + tc.q * p.sB, p.ldb, n0,
-                                                              p.N, k0, p.K, p.b_vec4 != 0, ptid,
-                                                              32 * C::PROD_WARPS);
-                        cp_async_arrive_noinc(&sm.raw_full[rr.s]);
+                if (lane == 0) {
+                    if (!mbar_wait(&sm.raw_empty[rr.s], rr.ph ^ 1u, ab, kStatusWaitEmpty)) {
+                        ok = false;
+                    } else {
+                        const int qa = tc.q * p.a_q_step, qb = tc.q * p.b_q_step;
+                        mbar_arrive_expect_tx(&sm.raw_full[rr.s], C::RAW_BYTES);
+                        if (C::A_KIN) tma_load_3d(sa, &tmA, &sm.raw_full[rr.s], k0, m0, qa);
+                        else          tma_load_3d(sa, &tmA, &sm.raw_full[rr.s], m0, k0, qa);
+                        if (C::B_KIN) tma_load_3d(sb, &tmB, &sm.raw_full[rr.s], k0, n0, qb);
+                        else          tma_load_3d(sb, &tmB, &sm.raw_full[rr.s], n0, k0, qb);
                     }
                 }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
                 ++issued;
                 rr.next();
             }
         }
-        if (!ok) {
-            if (C::USE_TMA) {
-                if (lane == 0) {
-                    // the stages issued last may still be landing
-                    Ring<C::RAW_STAGES> d;
-                    for (long long j = 0; j < issued; ++j) {
-                        if (j + C::RAW_STAGES >= issued)
-                            mbar_drain(&sm.raw_full[d.s], d.ph, ab.limit);
-                        d.next();
-                    }
-                }
-            } else {
-                asm volatile("cp.async.wait_all;" ::: "memory");
+        if (!ok && lane == 0) {
+            // the stages issued last may still be landing
+            Ring<C::RAW_STAGES> d;
+            for (long long j = 0; j < issued; ++j) {
+                if (j + C::RAW_STAGES >= issued) mbar_drain(&sm.raw_full[d.s], d.ph, ab.limit);
+                d.next();
             }
         }
     } else if (warp == 1) {

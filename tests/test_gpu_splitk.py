@@ -97,8 +97,8 @@ def planned_workspace(mode, M, N, K, Q, sms):
     need = 0
     for (bm, bn), tma in [(sh, t) for sh in shapes for t in (False, True)]:
         rate = {("fp32", True): 0.40e12, ("3xtf32", True): 1.54e12, ("tf32", True): 2.16e12,
-                ("fp32", False): 0.24e12, ("3xtf32", False): 0.16e12,
-                ("tf32", False): 0.16e12}[(mode, tma)]
+                ("fp32", False): 0.24e12, ("3xtf32", False): 0.47e12,
+                ("tf32", False): 0.55e12}[(mode, tma)]
         T = Q * math.ceil(M / bm) * math.ceil(N / bn)
         full, rem = divmod(T, sms)
         if rem == 0:
