@@ -45,11 +45,16 @@
 
 #include "common.cuh"
 
-// Ring depths (raw fp32 tiles / split stages) per mode; overridable at build
-// time for tuning sweeps.
+// Ring depths (raw fp32 tiles / split stages) per mode and B layout;
+// overridable at build time for tuning sweeps.  Measured on GB300 at 4092^3
+// (3xTF32): B N-inner 3/4 (238.7 TFLOP/s; 3/3 237.9), B K-inner 4/3 (235.6;
+// 3/3 219.9): the K-inner B tiles arrive as 128 short swizzled rows and want
+// one more TMA stage in flight.
 #ifndef SG_TC_RAW3
 #define SG_TC_RAW3 3
-#define SG_TC_SPLIT3 3
+#define SG_TC_SPLIT3 4
+#define SG_TC_RAW3_BK 4
+#define SG_TC_SPLIT3_BK 3
 #define SG_TC_RAW1 4
 #define SG_TC_SPLIT1 4
 #endif
@@ -77,8 +82,10 @@ struct Cfg {
     static constexpr int RAW_BYTES = A_BYTES + B_BYTES;
     static constexpr int PLANES = SPLIT3 ? 2 : 1;        // hi (+ lo)
     static constexpr int SPLIT_BYTES = PLANES * B_BYTES; // B planes in shared memory
-    static constexpr int RAW_STAGES = SPLIT3 ? SG_TC_RAW3 : SG_TC_RAW1;
-    static constexpr int SPLIT_STAGES = SPLIT3 ? SG_TC_SPLIT3 : SG_TC_SPLIT1;
+    static constexpr int RAW_STAGES =
+        SPLIT3 ? (B_KIN ? SG_TC_RAW3_BK : SG_TC_RAW3) : SG_TC_RAW1;
+    static constexpr int SPLIT_STAGES =
+        SPLIT3 ? (B_KIN ? SG_TC_SPLIT3_BK : SG_TC_SPLIT3) : SG_TC_SPLIT1;
     // TMEM columns: two accumulator buffers of BN fp32 columns, then the A
     // planes of every split stage (BK columns per plane, one row per lane).
     static constexpr int ACC_COLS = 2 * BN;
