@@ -145,6 +145,18 @@ def test_integer_batched_transposed_bit_exact(oracle_mod, mode):
                        exact=True)
 
 
+@pytest.mark.parametrize("mode", MODES)
+def test_integer_unaligned_operands_bit_exact(oracle_mod, mode):
+    """Operands TMA cannot describe (odd leading dimensions, unaligned bases)
+    take the element-wise producers: still exact on integer data."""
+    supported(mode)
+    A, B, C0 = workloads.integer_inputs(130, 150, 97, Q=2, seed=13)
+    for tA in (0, 1):
+        for tB in (0, 1):
+            check_full(Problem(A, B, C0, 2.0, -1.0, transA=tA, transB=tB, pads=(3, 5, 7),
+                               offsets=(1, 2, 3)), mode, oracle_mod, exact=True)
+
+
 # ---------------------------------------------------------- ragged sweeps
 
 RAGGED = [1, 7, 31, 127, 128, 129, 777]
