@@ -378,6 +378,77 @@ bool tma_eligible(const float *p, long long ld, int Q, long long stride)
     return true;
 }
 
+size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+// Workspace a transposed copy of an operand takes: `outer` rows of
+// round_up(inner, 4) floats per batch entry (one entry when broadcast).
+size_t repack_bytes(long long inner, long long outer, int Q, bool broadcast)
+{
+    const long long ld = (inner + 3) / 4 * 4;
+    return round256(static_cast<size_t>(broadcast ? 1 : Q) * static_cast<size_t>(outer) *
+                    static_cast<size_t>(ld) * sizeof(float));
+}
+
+// FP32 path with a workspace: copies a K-inner A (when N >= kRepackMinN) and
+// a K-inner B (when M >= kRepackMinM) into the front of the workspace,
+// transposed, so that the product runs with A M-inner and B N-inner, the
+// layout the FP32 kernel runs fastest (measured on GB300 at 4092^3: 69.2
+// TFLOP/s against 64.2 with K-inner A, 55.9 with both K-inner).  The copy
+// reads and writes the operand once; below the thresholds it costs more
+// than it saves.  What remains of the workspace goes to the split plan.
+int repack_for_simt(Plan &plan)
+{
+    GemmParams &p = plan.p;
+    if (plan.ws == nullptr || plan.ws_bytes == 0) return SGEMM_OK;
+    const bool want_a = !plan.transA && p.N >= kRepackMinN;
+    const bool want_b = plan.transB && p.M >= kRepackMinM;
+    const size_t a_bytes = want_a ? repack_bytes(p.M, p.K, p.Q, p.Q > 1 && p.sA == 0) : 0;
+    const size_t b_bytes = want_b ? repack_bytes(p.N, p.K, p.Q, p.Q > 1 && p.sB == 0) : 0;
+    bool do_a = want_a, do_b = want_b;
+    if (a_bytes + b_bytes > plan.ws_bytes) {
+        do_b = false;
+        if (a_bytes > plan.ws_bytes) do_a = false;
+    }
+    if (!do_a && !do_b) return SGEMM_OK;
+    char *w = static_cast<char *>(plan.ws);
+    size_t used = 0;
+    if (do_a) {
+        // A (M x K, lda) -> A' stored K x M: op(A)[i][k] = A'[k * lda' + i]
+        const long long ld = (p.M + 3) / 4 * 4;
+        const int qa = (p.Q > 1 && p.sA == 0) ? 1 : p.Q;
+        float *dst = reinterpret_cast<float *>(w + used);
+        const int rc = launch_transpose(p.A, p.lda, p.sA, p.M, p.K, qa, dst, ld,
+                                        static_cast<long long>(p.K) * ld, plan.num_sms, plan.stream);
+        if (rc != SGEMM_OK) return rc;
+        p.A = dst;
+        p.lda = ld;
+        p.sA = qa == 1 ? 0 : static_cast<long long>(p.K) * ld;
+        p.a_vec4 = 1;
+        plan.a_tma = true;
+        plan.transA = true;
+        used += a_bytes;
+    }
+    if (do_b) {
+        // B stored N x K (ldb) -> B' stored K x N: op(B)[k][j] = B'[k * ldb' + j]
+        const long long ld = (p.N + 3) / 4 * 4;
+        const int qb = (p.Q > 1 && p.sB == 0) ? 1 : p.Q;
+        float *dst = reinterpret_cast<float *>(w + used);
+        const int rc = launch_transpose(p.B, p.ldb, p.sB, p.N, p.K, qb, dst, ld,
+                                        static_cast<long long>(p.K) * ld, plan.num_sms, plan.stream);
+        if (rc != SGEMM_OK) return rc;
+        p.B = dst;
+        p.ldb = ld;
+        p.sB = qb == 1 ? 0 : static_cast<long long>(p.K) * ld;
+        p.b_vec4 = 1;
+        plan.b_tma = true;
+        plan.transB = false;
+        used += b_bytes;
+    }
+    plan.ws = used < plan.ws_bytes ? static_cast<void *>(w + used) : nullptr;
+    plan.ws_bytes = used < plan.ws_bytes ? plan.ws_bytes - used : 0;
+    return SGEMM_OK;
+}
+
 int run(int mode, int M, int N, int K, float alpha, const float *A, int lda, const float *B,
         int ldb, float beta, float *C, int ldc, int transA, int transB, long long sA,
         long long sB, long long sC, int Q, void *stream, void *ws = nullptr,
@@ -437,7 +508,11 @@ int run(int mode, int M, int N, int K, float alpha, const float *A, int lda, con
     plan.ws = ws;
     plan.ws_bytes = ws_bytes;
 
-    if (mode == SGEMM_MODE_FP32) return launch_simt(plan);
+    if (mode == SGEMM_MODE_FP32) {
+        rc = repack_for_simt(plan);
+        if (rc != SGEMM_OK) return rc;
+        return launch_simt(plan);
+    }
     return launch_tc(plan);
 }
 
@@ -484,7 +559,15 @@ int sgemm_batched_ex_ws(int mode, int M, int N, int K, float alpha, const float 
 
 size_t sgemm_workspace_size(int mode, int M, int N, int K, int Q)
 {
-    return preferred_plan(mode, M, N, K, Q).ws_bytes;
+    const size_t split = preferred_plan(mode, M, N, K, Q).ws_bytes;
+    if (mode == SGEMM_MODE_DEFAULT) mode = g_default_mode.load();
+    if (mode != SGEMM_MODE_FP32 || M <= 0 || N <= 0 || K <= 0 || Q <= 0) return split;
+    // room for the transposed operands the FP32 path may make (the layout
+    // is not known here; a broadcast operand would need less)
+    size_t repack = 0;
+    if (N >= kRepackMinN) repack += repack_bytes(M, K, Q, false);
+    if (M >= kRepackMinM) repack += repack_bytes(N, K, Q, false);
+    return split + repack;
 }
 
 int sgemm_set_default_mode(int mode)

@@ -83,6 +83,14 @@ SplitPlan one_wave_plan(int mode, int M, int N, int K, int Q);
 bool encode_operand(CUtensorMap *map, const float *base, bool kin, long long rows, long long K,
                     long long ld, int Q, long long stride, int box_rows);
 
+// Transposes Q matrices of rows x cols (row pitch lds, batch stride sstride)
+// into dst (row pitch ldd, batch stride dstride): dst[c][r] = src[r][c].
+int launch_transpose(const float *src, long long lds, long long sstride, int rows, int cols, int Q,
+                     float *dst, long long ldd, long long dstride, int num_sms, cudaStream_t stream);
+// Smallest N (for A) and M (for B) at which the FP32 path transposes a
+// K-inner operand into the workspace first (see repack_for_simt in api.cu).
+constexpr int kRepackMinN = 1024, kRepackMinM = 1024;
+
 int launch_simt(Plan &plan);   // returns an sgemm status code
 int launch_tc(Plan &plan);     // tcgen05 paths (3xTF32 and TF32)
 

@@ -109,8 +109,12 @@ int sgemm_batched_ex(int mode, int M, int N, int K, float alpha, const float *A,
  * rounding.  Every slice stores its partial tile in fp32; a second kernel,
  * enqueued on `stream` right after the first, sums each tile's slices in a
  * fixed order and applies alpha and beta, so repeated calls give identical
- * bits.  The workspace needs no initialisation; it must not be used by
- * another call running at the same time. */
+ * bits.  On the FP32 path the workspace also serves a transposed copy of a
+ * K-inner A (when N >= 1024) and of a K-inner B (when M >= 1024), made on
+ * `stream` before the product: that path runs fastest with A M-inner and B
+ * N-inner.  sgemm_workspace_size counts that room for both operands.  The
+ * workspace needs no initialisation; it must not be used by another call
+ * running at the same time. */
 size_t sgemm_workspace_size(int mode, int M, int N, int K, int Q);
 int sgemm_batched_ex_ws(int mode, int M, int N, int K, float alpha, const float *A, int lda,
                         const float *B, int ldb, float beta, float *C, int ldc, int transA,
@@ -121,7 +125,8 @@ int sgemm_batched_ex_ws(int mode, int M, int N, int K, float alpha, const float 
  * the pages: an addition of this library.)
  *
  * Same arguments and results as sgemm_batched_ex_ws, without the workspace:
- * the partial tiles live in a fixed 24 MB scratch array inside the library
+ * the partial tiles (and, on the FP32 path, a transposed operand when it
+ * fits beside them) live in a fixed 24 MB scratch array inside the library
  * image.  For code that may not call cudaMalloc or may not grow a memory pool
  * at the point where it multiplies (a host callback, another library's
  * critical section, a plugin that is handed only its input and output

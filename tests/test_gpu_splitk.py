@@ -56,6 +56,27 @@ def test_split_k_parity(oracle_mod, mode, shape):
     assert err <= TOL[mode], f"{mode} {shape}: max rel err {err:.3e}"
 
 
+@pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_fp32_operand_transposition_in_the_workspace(oracle_mod, tA, tB):
+    """The FP32 path copies a K-inner A (N >= 1024) or B (M >= 1024) into the
+    workspace transposed; with odd leading dimensions, unaligned bases, a
+    broadcast A and every layout the result matches the oracle, and on
+    integer data bit for bit."""
+    M, N, K, Q = 1030, 1100, 64, 2
+    A, B, C0 = workloads.random_inputs(M, N, K, Q=Q, seed=31 + 2 * tA + tB)
+    for strideA in (None, 0):
+        prob = Problem(A, B, C0, 0.75, -0.5, transA=tA, transB=tB, pads=(3, 5, 7),
+                       offsets=(1, 2, 3), strideA=strideA)
+        C = prob.run_gpu("fp32", api="ws")
+        Cref, D = prob.oracle(oracle_mod)
+        assert oracle_mod.max_rel_err(C, Cref, D) <= TOL["fp32"]
+    Ai, Bi, Ci = workloads.integer_inputs(M, N, K, Q=Q, seed=7)
+    prob = Problem(Ai, Bi, Ci, 2.0, 1.0, transA=tA, transB=tB, pads=(1, 3, 0))
+    C = prob.run_gpu("fp32", api="ws")
+    Cref, _ = prob.oracle(oracle_mod)
+    assert np.array_equal(C.astype(np.float64), Cref)
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_split_k_integer_bit_exact(oracle_mod, mode):
     A, B, C0 = workloads.integer_inputs(700, 900, 1500, seed=5)
@@ -92,7 +113,8 @@ def planned_workspace(mode, M, N, K, Q, sms):
     (bw 8 TB/s up to 64 MB of workspace, else 3 TB/s; t_tile from the path's
     per-multiprocessor rate with TMA-fed or cp.async-fed operands), used only
     if it saves 1%; returns the largest workspace over the shapes and feeds
-    (one BM x BN fp32 slot per split unit), 0 when none splits."""
+    (one BM x BN fp32 slot per split unit), 0 when none splits; on the FP32
+    path plus room for transposed copies of A and B (256-byte rounded)."""
     shapes = [(256, 128), (128, 128)] if mode == "fp32" else [(128, 128)]
     need = 0
     for (bm, bn), tma in [(sh, t) for sh in shapes for t in (False, True)]:
@@ -116,6 +138,11 @@ def planned_workspace(mode, M, N, K, Q, sms):
                 best_t, best, best_ws = t, s, ws
         if best > 1 and best_t <= 0.99 * t_whole:
             need = max(need, best_ws)
+    if mode == "fp32":
+        # room for transposed copies of A (N >= 1024) and B (M >= 1024)
+        def repack(inner, outer):
+            return (Q * outer * ((inner + 3) // 4 * 4) * 4 + 255) // 256 * 256
+        need += (repack(M, K) if N >= 1024 else 0) + (repack(N, K) if M >= 1024 else 0)
     return need
 
 
@@ -137,7 +164,8 @@ def test_workspace_size_follows_the_plan(case):
 
 def test_workspace_size_query():
     import dense_fp32_matrix_03_gb300 as lib
-    assert lib.sgemm_workspace_size("fp32", 1024, 1024, 32, 1) == 0      # one k-block: no split
+    assert lib.sgemm_workspace_size("fp32", 1000, 1000, 32, 1) == 0      # one k-block: no split
+    assert lib.sgemm_workspace_size("fp32", 1024, 1024, 32, 1) > 0       # room to transpose A, B
     assert lib.sgemm_workspace_size("3xtf32", 1024, 1024, 128, 1) == 0  # tensor path: >= 256 per slice
     assert lib.sgemm_workspace_size("fp32", 1024, 1024, 128, 1) > 0     # 2 slices of 64
     assert lib.sgemm_workspace_size("fp32", 0, 10, 10, 1) == 0
