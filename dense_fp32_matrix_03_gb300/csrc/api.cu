@@ -95,54 +95,51 @@ __global__ void scale_c_kernel(float *C, int M, int N, long long ldc, long long 
 // Split-K fix-up: for every split tile, sums its slices' partial tiles in
 // slice order 0, 1, ..., splits-1 and writes C = alpha * sum + beta * C
 // (C not read when beta == 0), masked at the M/N edges: the same result for
-// the same inputs whatever order the slices ran in.  One thread per four
-// consecutive columns of a tile row, grid-stride.  It runs after the GEMM
-// kernel on the same stream; when launched as a programmatic dependent it
-// first waits for that kernel's completion and memory.
+// the same inputs whatever order the slices ran in.  Block (x, y): split
+// tile y, 256 consecutive float4 of it (one per thread).  It runs after the
+// GEMM kernel on the same stream; when launched as a programmatic dependent
+// it first waits for that kernel's completion and memory.
 __global__ void __launch_bounds__(256) splitk_fixup_kernel(const GemmParams p, int bm, int bn)
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int row_v4 = bn / 4;                        // float4 per tile row
-    const long long tile_v4 = static_cast<long long>(bm) * row_v4;
-    const long long total = (p.num_tiles - p.dp_tiles) * tile_v4;
+    const int row_v4 = bn / 4;  // float4 per tile row
+    const int tile_v4 = bm * row_v4;
+    const int within = blockIdx.x * blockDim.x + threadIdx.x;
+    if (within >= tile_v4) return;
+    const long long sidx = blockIdx.y;
+    const TileCoord tc = tile_coord(p.dp_tiles + sidx, p);
+    const int r = within / row_v4, c = (within - r * row_v4) * 4;
+    const int m = tc.tm * bm + r, n0 = tc.tn * bn + c;
+    if (m >= p.M || n0 >= p.N) return;
+    const float4 *slot = reinterpret_cast<const float4 *>(p.ws_part) +
+                         sidx * p.splits * static_cast<long long>(tile_v4) + within;
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sl = 0; sl < p.splits; ++sl) {
+        const float4 x = slot[static_cast<long long>(sl) * tile_v4];
+        sum.x += x.x;
+        sum.y += x.y;
+        sum.z += x.z;
+        sum.w += x.w;
+    }
     const bool use_beta = p.beta != 0.f;
-    for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
-         e += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const long long sidx = e / tile_v4;
-        const int within = static_cast<int>(e - sidx * tile_v4);
-        const int r = within / row_v4, c = (within - r * row_v4) * 4;
-        const TileCoord tc = tile_coord(p.dp_tiles + sidx, p);
-        const int m = tc.tm * bm + r, n0 = tc.tn * bn + c;
-        if (m >= p.M || n0 >= p.N) continue;
-        const float4 *slot =
-            reinterpret_cast<const float4 *>(p.ws_part) + sidx * p.splits * tile_v4 + within;
-        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int sl = 0; sl < p.splits; ++sl) {
-            const float4 x = slot[sl * tile_v4];
-            sum.x += x.x;
-            sum.y += x.y;
-            sum.z += x.z;
-            sum.w += x.w;
+    float *crow = p.C + tc.q * p.sC + static_cast<long long>(m) * p.ldc;
+    const float v[4] = {sum.x, sum.y, sum.z, sum.w};
+    if (p.c_vec4 && n0 + 3 < p.N) {
+        float4 o = make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2], p.alpha * v[3]);
+        float4 *dst = reinterpret_cast<float4 *>(crow + n0);
+        if (use_beta) {
+            const float4 old = *dst;
+            o.x = fmaf(p.beta, old.x, o.x);
+            o.y = fmaf(p.beta, old.y, o.y);
+            o.z = fmaf(p.beta, old.z, o.z);
+            o.w = fmaf(p.beta, old.w, o.w);
         }
-        float *crow = p.C + tc.q * p.sC + static_cast<long long>(m) * p.ldc;
-        const float v[4] = {sum.x, sum.y, sum.z, sum.w};
-        if (p.c_vec4 && n0 + 3 < p.N) {
-            float4 o = make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2], p.alpha * v[3]);
-            float4 *dst = reinterpret_cast<float4 *>(crow + n0);
-            if (use_beta) {
-                const float4 old = *dst;
-                o.x = fmaf(p.beta, old.x, o.x);
-                o.y = fmaf(p.beta, old.y, o.y);
-                o.z = fmaf(p.beta, old.z, o.z);
-                o.w = fmaf(p.beta, old.w, o.w);
-            }
-            *dst = o;
-        } else {
-            for (int j = 0; j < 4 && n0 + j < p.N; ++j) {
-                float o = p.alpha * v[j];
-                if (use_beta) o = fmaf(p.beta, crow[n0 + j], o);
-                crow[n0 + j] = o;
-            }
+        *dst = o;
+    } else {
+        for (int j = 0; j < 4 && n0 + j < p.N; ++j) {
+            float o = p.alpha * v[j];
+            if (use_beta) o = fmaf(p.beta, crow[n0 + j], o);
+            crow[n0 + j] = o;
         }
     }
 }
@@ -283,12 +280,12 @@ int plan_splits(Plan &plan, int bm, int bn, bool tma)
 int launch_fixup(Plan &plan, int bm, int bn)
 {
     const GemmParams &p = plan.p;
-    const long long total = (p.num_tiles - p.dp_tiles) * (static_cast<long long>(bm) * bn / 4);
-    long long blocks = (total + 255) / 256;
-    if (blocks > 8LL * plan.num_sms) blocks = 8LL * plan.num_sms;
-    if (blocks < 1) return SGEMM_OK;
+    const long long split_tiles = p.num_tiles - p.dp_tiles;
+    if (split_tiles <= 0) return SGEMM_OK;
+    if (split_tiles > 65535) return SGEMM_ERR_UNSUPPORTED;  // a split wave is < one per SM
+    const int per_tile = (bm * bn / 4 + 255) / 256;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.gridDim = dim3(static_cast<unsigned>(per_tile), static_cast<unsigned>(split_tiles));
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = plan.stream;

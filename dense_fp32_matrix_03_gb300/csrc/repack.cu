@@ -20,50 +20,52 @@ constexpr int kT = 32;       // tile edge
 constexpr int kRowsPer = 8;  // thread rows per block (kT x kRowsPer threads)
 
 // dst[q][c * ldd + r] = src[q][r * lds + c] for r < rows, c < cols.
-// One kT x kT tile per block and step; blocks walk the tiles grid-stride.
+// Block (x, y, z) moves tile (column block x, row block y, batch z); y and z
+// step by the grid size when there are more tiles than the grid holds.
 __global__ void __launch_bounds__(kT * kRowsPer)
     transpose_kernel(const float *__restrict__ src, long long lds, long long sstride, int rows,
                      int cols, int Q, float *__restrict__ dst, long long ldd, long long dstride)
 {
     __shared__ float tile[kT][kT + 1];
-    const long long tiles_r = (rows + kT - 1) / kT, tiles_c = (cols + kT - 1) / kT;
-    const long long total = tiles_r * tiles_c * Q;
-    for (long long t = blockIdx.x; t < total; t += gridDim.x) {
-        const long long q = t / (tiles_r * tiles_c);
-        const long long rem = t - q * tiles_r * tiles_c;
-        const int r0 = static_cast<int>(rem / tiles_c) * kT;
-        const int c0 = static_cast<int>(rem % tiles_c) * kT;
+    const int c0 = blockIdx.x * kT;
+    for (int q = blockIdx.z; q < Q; q += gridDim.z) {
         const float *s = src + q * sstride;
         float *d = dst + q * dstride;
-        // read rows of src (coalesced along c)
+        for (long long r0l = static_cast<long long>(blockIdx.y) * kT; r0l < rows;
+             r0l += static_cast<long long>(gridDim.y) * kT) {
+            const int r0 = static_cast<int>(r0l);
+            // read rows of src (coalesced along c)
 #pragma unroll
-        for (int i = threadIdx.y; i < kT; i += kRowsPer) {
-            const int r = r0 + i, c = c0 + threadIdx.x;
-            if (r < rows && c < cols) tile[i][threadIdx.x] = s[static_cast<long long>(r) * lds + c];
-        }
-        __syncthreads();
-        // write rows of dst (coalesced along r)
+            for (int i = threadIdx.y; i < kT; i += kRowsPer) {
+                const int r = r0 + i, c = c0 + threadIdx.x;
+                if (r < rows && c < cols)
+                    tile[i][threadIdx.x] = s[static_cast<long long>(r) * lds + c];
+            }
+            __syncthreads();
+            // write rows of dst (coalesced along r)
 #pragma unroll
-        for (int i = threadIdx.y; i < kT; i += kRowsPer) {
-            const int c = c0 + i, r = r0 + threadIdx.x;
-            if (r < rows && c < cols) d[static_cast<long long>(c) * ldd + r] = tile[threadIdx.x][i];
+            for (int i = threadIdx.y; i < kT; i += kRowsPer) {
+                const int c = c0 + i, r = r0 + threadIdx.x;
+                if (r < rows && c < cols)
+                    d[static_cast<long long>(c) * ldd + r] = tile[threadIdx.x][i];
+            }
+            __syncthreads();
         }
-        __syncthreads();
     }
 }
 
 }  // namespace
 
 int launch_transpose(const float *src, long long lds, long long sstride, int rows, int cols, int Q,
-                     float *dst, long long ldd, long long dstride, int num_sms, cudaStream_t stream)
+                     float *dst, long long ldd, long long dstride, int, cudaStream_t stream)
 {
-    const long long tiles =
-        static_cast<long long>((rows + kT - 1) / kT) * ((cols + kT - 1) / kT) * Q;
-    if (tiles <= 0) return SGEMM_OK;
-    long long blocks = tiles;
-    if (blocks > 16LL * num_sms) blocks = 16LL * num_sms;
-    transpose_kernel<<<static_cast<unsigned>(blocks), dim3(kT, kRowsPer), 0, stream>>>(
-        src, lds, sstride, rows, cols, Q, dst, ldd, dstride);
+    if (rows <= 0 || cols <= 0 || Q <= 0) return SGEMM_OK;
+    const long long tc = (cols + kT - 1) / kT, tr = (rows + kT - 1) / kT;
+    if (tc > 0x7FFFFFFFLL) return SGEMM_ERR_UNSUPPORTED;
+    const dim3 grid(static_cast<unsigned>(tc), static_cast<unsigned>(tr < 65535 ? tr : 65535),
+                    static_cast<unsigned>(Q < 65535 ? Q : 65535));
+    transpose_kernel<<<grid, dim3(kT, kRowsPer), 0, stream>>>(src, lds, sstride, rows, cols, Q,
+                                                               dst, ldd, dstride);
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
 
