@@ -86,11 +86,17 @@ def roofline_peak(mode, num_sms, peaks, source):
     return "tensor", tf32, f"tf32 tensor peak ({source} bf16 burst x 1.1/2.25)"
 
 
+# Sources of the kernels a benchmark call runs and of the host code that
+# plans them; the probes, the host-buffer entry point and the allocation-free
+# entry point are left out (they do not change what the timed kernels do).
+TIMED_SOURCES = ("api.cu", "common.cuh", "internal.h", "kernels_simt.cu", "kernels_tc.cu",
+                 "params.h", "repack.cu", "simt_fp32.cuh", "tc_direct.cuh", "tc_tf32.cuh")
+
+
 def kernel_source_hash():
-    import glob
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "dense_fp32_matrix_03_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
+    for name in TIMED_SOURCES:
+        with open(os.path.join(ROOT, "dense_fp32_matrix_03_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -290,14 +296,16 @@ def reference_arm(args, rank, world):
 
 # --------------------------------------------------------------- GPU arm
 
-def time_calls(call, steps, warmup, stream, flush):
-    """Per-step CUDA-event times (ms) on `stream`, L2 flushed before each."""
+def time_calls(call, steps, warmup, stream, flush, lib=None):
+    """Per-step CUDA-event times (ms) on `stream`, L2 flushed before each;
+    with `lib`, also the library's kernel launches during the timed steps."""
     import torch
     for _ in range(warmup):
         flush.zero_()
         call()
     torch.cuda.synchronize()
     evs = []
+    n0 = lib.sgemm_kernel_launches() if lib is not None else 0
     for _ in range(steps):
         flush.zero_()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -307,7 +315,55 @@ def time_calls(call, steps, warmup, stream, flush):
         e1.record(stream)
         evs.append((e0, e1))
     torch.cuda.synchronize()
-    return [a.elapsed_time(b) for a, b in evs]
+    times = [a.elapsed_time(b) for a, b in evs]
+    if lib is None:
+        return times
+    return times, lib.sgemm_kernel_launches() - n0
+
+
+# Probe iterations: about a millisecond each on a GB300.
+PROBE_ITERS = {"ffma": 2048, "ffma2": 2048, "tf32_ss": 16384, "tf32_ts": 16384,
+               "bf16_ss": 16384}
+PROBE_FOR = {"fp32": "max(ffma, ffma2)", "3xtf32": "tf32_ts / 3 (three MMAs per k step)",
+             "tf32": "tf32_ts"}
+
+
+def peak_probes(lib, stream, reps=5):
+    """Median TFLOP/s of each throughput probe (a path's arithmetic with no
+    operand traffic), after one warm-up launch, with CUDA events on `stream`."""
+    import torch
+    out = {}
+    for kind, iters in PROBE_ITERS.items():
+        st, flops = lib.sgemm_peak_probe(kind, iters, stream)
+        if st != lib.SGEMM_OK:
+            out[kind] = None
+            continue
+        evs = []
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            lib.check(lib.sgemm_peak_probe(kind, iters, stream)[0])
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+        out[kind] = flops / (ms / 1e3) / 1e12
+    lib.check(lib.sgemm_poll_error(stream))
+    return out
+
+
+def probe_peak_for(mode, probes):
+    """The probe figure a path's roofline fraction is also set against."""
+    if not probes:
+        return None
+    if mode == "fp32":
+        vals = [v for v in (probes.get("ffma"), probes.get("ffma2")) if v]
+        return max(vals) if vals else None
+    ts = probes.get("tf32_ts")
+    if not ts:
+        return None
+    return ts / 3.0 if mode == "3xtf32" else ts
 
 
 def resolve_mode(lib, requested):
@@ -371,7 +427,6 @@ def main():
     # split-K workspace (the last, partial wave of tiles is cut along K),
     # allocated once, outside the timed region, like a library handle's
     ws_bytes, ws = workspace(lib, mode, M, N, K, 1, dev)
-    launches_per_call = 2 if ws_bytes else 1   # the GEMM kernel (+ the split-K fix-up)
 
     def call():
         lib.check(lib.sgemm_batched_ex_ws(mode, M, N, K, alpha, A, K, B, N, beta, C, N, 0, 0, 0,
@@ -386,7 +441,7 @@ def main():
     torch.cuda.synchronize()
     with ClockSampler(gpu_id) as clk:
         t_wall0 = time.perf_counter()
-        times = time_calls(call, args.steps, args.warmup, stream, flush)
+        times, launches = time_calls(call, args.steps, args.warmup, stream, flush, lib)
         t_wall = time.perf_counter() - t_wall0
     torch.cuda.synchronize()
     barrier(world)
@@ -416,28 +471,38 @@ def main():
         roofline["frac_at_sampled_clock"] = achieved / (
             num_sms * FP32_LANES_PER_SM * 2 * clocks["sm_mhz"] * 1e6 / 1e12)
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the host-buffer entry point (sgemm_host): the
+    # operands start in pinned host memory, C ends there; copies inside
     e2e = None
     if rank == 0 or world > 1:
         hA = torch.from_numpy(w["A"]).pin_memory()
         hB = torch.from_numpy(w["B"]).pin_memory()
-        hC = torch.empty(M, N, dtype=torch.float32).pin_memory()
-        dA = torch.empty_like(A)
-        dB = torch.empty_like(B)
-        dC = torch.empty_like(C)
+        hC = torch.from_numpy(w["C0"]).pin_memory()
+        dev_bytes = lib.sgemm_host_buffer_size(mode, M, N, K, 0, 0, 0)
+        dbuf = torch.empty(dev_bytes, dtype=torch.uint8, device=dev)
 
         def e2e_call():
-            dA.copy_(hA, non_blocking=True)
-            dB.copy_(hB, non_blocking=True)
-            lib.check(lib.sgemm_batched_ex_ws(mode, M, N, K, alpha, dA, K, dB, N, beta, dC, N, 0,
-                                              0, 0, 0, 0, 1, ws, ws_bytes, stream))
-            hC.copy_(dC, non_blocking=True)
+            lib.check(lib.sgemm_host(mode, M, N, K, alpha, hA, K, hB, N, beta, hC, N, 0, 0, 0,
+                                     dbuf, dev_bytes, stream))
         e_steps = max(3, min(args.steps, 10))
-        et = time_calls(e2e_call, e_steps, 3, stream, flush)
+        et, e_launches = time_calls(e2e_call, e_steps, 3, stream, flush, lib)
         e_ms = statistics.mean(et)
         e2e = {"value": flops_step / (e_ms / 1e3) / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": 4 * (M * K + K * N), "d2h_bytes_per_step": 4 * M * N,
-               "ms_per_step": e_ms}
+               "h2d_bytes_per_step": 4 * (M * K + K * N + (M * N if beta != 0 else 0)),
+               "d2h_bytes_per_step": 4 * M * N, "ms_per_step": e_ms,
+               "entry": "sgemm_host (pinned host buffers, panels of C overlap copies "
+                        "and products)", "gpu_launches": e_launches}
+        del dbuf
+
+    probes = None
+    if rank == 0:
+        probes = peak_probes(lib, stream)
+        probe_peak = probe_peak_for(mode, probes)
+        if probe_peak:
+            roofline["probe_peak"] = probe_peak
+            roofline["frac_of_probe"] = achieved / probe_peak
+            roofline["probe_note"] = ("the same instructions with no operand traffic, timed "
+                                      "here (sgemm_peak_probe): " + PROBE_FOR[mode])
 
     extra = {}
     if not args.no_extra and rank == 0:
@@ -461,8 +526,9 @@ def main():
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": launches_per_call * args.steps,
+            "gpu_launches": launches,
             "clocks": clocks,
+            "peak_probes_tflops": probes,
             "wall_s_timed_loop": t_wall,
         }
         line.update(extra)

@@ -26,6 +26,14 @@ SGEMM_ERR_LAUNCH = 3
 SGEMM_ERR_TIMEOUT = 4
 SGEMM_ERR_SCRATCH_LIMIT = 5
 
+SGEMM_PROBE_FFMA = 0
+SGEMM_PROBE_FFMA2 = 1
+SGEMM_PROBE_TF32_SS = 2
+SGEMM_PROBE_TF32_TS = 3
+SGEMM_PROBE_BF16_SS = 4
+PROBES = {"ffma": SGEMM_PROBE_FFMA, "ffma2": SGEMM_PROBE_FFMA2, "tf32_ss": SGEMM_PROBE_TF32_SS,
+          "tf32_ts": SGEMM_PROBE_TF32_TS, "bf16_ss": SGEMM_PROBE_BF16_SS}
+
 SGEMM_MODE_DEFAULT = -1
 SGEMM_MODE_FP32 = 0
 SGEMM_MODE_3XTF32 = 1
@@ -45,11 +53,16 @@ SIGNATURES = {
                                  _ll, _i, _p, ctypes.c_size_t, _p]),
     "sgemm_batched_ex_noalloc": (_i, [_i, _i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _i, _i, _ll,
                                       _ll, _ll, _i, _p]),
+    "sgemm_host_buffer_size": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i, _i]),
+    "sgemm_host": (_i, [_i, _i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _i, _i, _i, _p,
+                        ctypes.c_size_t, _p]),
+    "sgemm_peak_probe": (_i, [_i, _ll, ctypes.POINTER(ctypes.c_double), _p]),
     "sgemm_set_default_mode": (_i, [_i]),
     "sgemm_get_default_mode": (_i, []),
     "sgemm_status_string": (ctypes.c_char_p, [_i]),
     "sgemm_poll_error": (_i, [_p]),
     "sgemm_selftest_wait_timeout": (_i, [_ll, _p]),
+    "sgemm_kernel_launches": (ctypes.c_ulonglong, []),
     "sgemm_version": (_i, []),
 }
 
@@ -167,6 +180,32 @@ def sgemm_batched_ex_noalloc(mode, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
                                          strideC, Q, _stream(stream))
 
 
+def sgemm_host_buffer_size(mode, M, N, K, transA=0, transB=0, panel_rows=0) -> int:
+    if isinstance(mode, str):
+        mode = MODES[mode]
+    return int(_lib.sgemm_host_buffer_size(mode, M, N, K, int(transA), int(transB), panel_rows))
+
+
+def sgemm_host(mode, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, transA, transB, panel_rows,
+               dev, dev_bytes, stream=None) -> int:
+    """A, B, C: host buffers (CPU tensors, ideally pinned, or raw addresses);
+    dev: the device buffer (see include/sgemm.h)."""
+    if isinstance(mode, str):
+        mode = MODES[mode]
+    return _lib.sgemm_host(mode, M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C), ldc,
+                           int(transA), int(transB), panel_rows, _ptr(dev), int(dev_bytes),
+                           _stream(stream))
+
+
+def sgemm_peak_probe(kind, iters, stream=None):
+    """(status, flops) of one probe launch on `stream`."""
+    if isinstance(kind, str):
+        kind = PROBES[kind]
+    flops = ctypes.c_double(0.0)
+    st = _lib.sgemm_peak_probe(kind, iters, ctypes.byref(flops), _stream(stream))
+    return st, flops.value
+
+
 def sgemm_set_default_mode(mode) -> int:
     if isinstance(mode, str):
         mode = MODES[mode]
@@ -187,6 +226,10 @@ def sgemm_poll_error(stream=None) -> int:
 
 def sgemm_selftest_wait_timeout(wait_cycles: int, stream=None) -> int:
     return _lib.sgemm_selftest_wait_timeout(wait_cycles, _stream(stream))
+
+
+def sgemm_kernel_launches() -> int:
+    return int(_lib.sgemm_kernel_launches())
 
 
 def sgemm_version() -> int:

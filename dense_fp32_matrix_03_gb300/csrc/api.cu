@@ -181,6 +181,22 @@ int check_args(int mode, int M, int N, int K, float alpha, const float *A, int l
 
 }  // namespace
 
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+bool current_sm103(int *num_sms, unsigned int **status)
+{
+    int dev = 0;
+    const DeviceInfo *di = device_info(&dev);
+    if (di == nullptr || di->cc_major != 10 || di->cc_minor != 3) return false;
+    *num_sms = di->num_sms;
+    *status = di->status;
+    return true;
+}
+
 bool encode_operand(CUtensorMap *map, const float *base, bool kin, long long rows, long long K,
                     long long ld, int Q, long long stride, int box_rows)
 {
@@ -294,9 +310,10 @@ int launch_fixup(Plan &plan, int bm, int bn)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, splitk_fixup_kernel, p, bm, bn) == cudaSuccess
-               ? SGEMM_OK
-               : SGEMM_ERR_LAUNCH;
+    if (cudaLaunchKernelEx(&cfg, splitk_fixup_kernel, p, bm, bn) != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
+    note_launch();
+    return SGEMM_OK;
 }
 
 namespace {
@@ -467,7 +484,9 @@ int run(int mode, int M, int N, int K, float alpha, const float *A, int lda, con
         long long blocks = (total + 255) / 256;
         if (blocks > 8LL * di->num_sms) blocks = 8LL * di->num_sms;
         scale_c_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(C, M, N, ldc, sC, Q, beta);
-        return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+        if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        note_launch();
+        return SGEMM_OK;
     }
 
     Plan plan{};
@@ -618,8 +637,22 @@ int sgemm_selftest_wait_timeout(long long wait_cycles, void *stream)
     if (di == nullptr) return SGEMM_ERR_UNSUPPORTED;
     wait_timeout_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(di->status,
                                                                           wait_cycles);
-    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    note_launch();
+    return SGEMM_OK;
 }
+
+int sgemm_peak_probe(int kind, long long iters, double *flops, void *stream)
+{
+    if (flops == nullptr || !sg::probe_args_ok(kind, iters)) return SGEMM_ERR_INVALID_ARG;
+    int num_sms = 0;
+    unsigned int *status = nullptr;
+    if (!sg::current_sm103(&num_sms, &status)) return SGEMM_ERR_UNSUPPORTED;
+    return sg::launch_peak_probe(kind, iters, num_sms, status, static_cast<cudaStream_t>(stream),
+                                 flops);
+}
+
+unsigned long long sgemm_kernel_launches(void) { return sg::g_launches.load(); }
 
 int sgemm_version(void) { return 100; }
 

@@ -91,6 +91,19 @@ int launch_transpose(const float *src, long long lds, long long sstride, int row
 // K-inner operand into the workspace first (see repack_for_simt in api.cu).
 constexpr int kRepackMinN = 1024, kRepackMinM = 1024;
 
+// Multiprocessor count and device status word of the current device; false
+// when it cannot be queried or is not a compute capability 10.3 GPU.
+bool current_sm103(int *num_sms, unsigned int **status);
+// Counts one kernel the library enqueued (reported by sgemm_kernel_launches).
+void note_launch();
+
+// A known probe kind with an iteration count inside its documented range.
+bool probe_args_ok(int kind, long long iters);
+// Enqueues one throughput probe (SGEMM_PROBE_*); *flops receives the
+// operations it performs.  Returns an sgemm status.
+int launch_peak_probe(int kind, long long iters, int num_sms, unsigned int *status,
+                      cudaStream_t st, double *flops);
+
 int launch_simt(Plan &plan);   // returns an sgemm status code
 int launch_tc(Plan &plan);     // tcgen05 paths (3xTF32 and TF32)
 

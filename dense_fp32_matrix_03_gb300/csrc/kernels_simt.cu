@@ -39,6 +39,7 @@ int launch_one(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
     kern<<<static_cast<unsigned>(grid), Cfg::THREADS, Cfg::SMEM_BYTES, plan.stream>>>(
         tmA, tmB, plan.p);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    note_launch();
     return plan.p.splits > 1 ? launch_fixup(plan, Cfg::BM, Cfg::BN) : SGEMM_OK;
 }
 

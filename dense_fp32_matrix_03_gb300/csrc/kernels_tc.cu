@@ -35,6 +35,7 @@ int launch_tma(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
     kern<<<static_cast<unsigned>(grid), tc::kThreads, C::SMEM_BYTES, plan.stream>>>(tmA, tmB,
                                                                                   plan.p);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    note_launch();
     return plan.p.splits > 1 ? launch_fixup(plan, tc::BM, kBN) : SGEMM_OK;
 }
 
@@ -50,6 +51,7 @@ int launch_direct(Plan &plan)
     if (grid > plan.num_sms) grid = plan.num_sms;
     kern<<<static_cast<unsigned>(grid), tcd::kThreads, C::SMEM_BYTES, plan.stream>>>(plan.p);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    note_launch();
     return plan.p.splits > 1 ? launch_fixup(plan, tc::BM, kBN) : SGEMM_OK;
 }
 

@@ -106,7 +106,9 @@ int launch_transpose(const float *src, long long lds, long long sstride, int row
     else
         transpose_kernel<false><<<grid, kThreads, 0, stream>>>(src, lds, sstride, rows, cols, Q,
                                                                dst, ldd, dstride, dvec);
-    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    note_launch();
+    return SGEMM_OK;
 }
 
 }  // namespace sg

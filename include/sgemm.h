@@ -150,6 +150,65 @@ int sgemm_batched_ex_noalloc(int mode, int M, int N, int K, float alpha, const f
                              int transB, long long strideA, long long strideB, long long strideC,
                              int Q, void *stream);
 
+/* The product on HOST buffers.  (No counterpart on the pages, whose
+ * benchmarks start with the operands on the GPU: an addition of this library
+ * for callers whose data lives in host memory.)
+ *
+ * A, B and C are host pointers with the layout and leading dimensions of
+ * sgemm_batched (one product, no batch).  The call copies op(A), op(B) and,
+ * when beta != 0, C into `dev`, a DEVICE buffer the caller owns (256-byte
+ * aligned, at least sgemm_host_buffer_size(...) bytes), computes there, and
+ * copies C back.  C is cut into panels of `panel_rows` rows (0: the library
+ * picks about two waves of output tiles per panel; at most 64 panels, else
+ * SGEMM_ERR_INVALID_ARG): the copy-in of one panel, the product of the
+ * previous one and the copy-out of the one before run at the same time, on
+ * two copy streams the library keeps per device and on `stream` for the
+ * products.  The call is asynchronous like the others: C on the host holds
+ * the result once `stream` has reached the end of the call (synchronise it,
+ * or record an event after the call).  Host memory that is page-locked
+ * (cudaHostAlloc / cudaHostRegister) is copied at full speed and overlaps;
+ * pageable memory works but its copies are staged by the driver and do not
+ * overlap.  Arguments are checked as in sgemm_batched_ex_ws; a CUDA error
+ * part-way returns SGEMM_ERR_LAUNCH (C on the host is then unspecified).
+ * The buffer must not be used by another call running at the same time.
+ *
+ * sgemm_host_buffer_size returns the bytes of `dev` such a call needs (0 for
+ * invalid arguments or without a usable device): the three operands with
+ * rows padded to a multiple of four floats, plus the split-K / transposition
+ * workspace of the panel product. */
+size_t sgemm_host_buffer_size(int mode, int M, int N, int K, int transA, int transB,
+                              int panel_rows);
+int sgemm_host(int mode, int M, int N, int K, float alpha, const float *A, int lda,
+               const float *B, int ldb, float beta, float *C, int ldc, int transA, int transB,
+               int panel_rows, void *dev, size_t dev_bytes, void *stream);
+
+/* Throughput probes (measurement only; no product is computed).  Launches
+ * one kernel on `stream` that runs only the arithmetic instructions of a
+ * path, with no operand traffic, and stores in *flops the floating-point
+ * operations it performs (2 per multiply-add).  Timed with events on
+ * `stream`, it gives the peak those instructions reach on this GPU at that
+ * moment -- the denominator a kernel's own speed is best set against:
+ *   SGEMM_PROBE_FFMA     scalar fma.rn.f32 chains      iters: loop trips, 1 .. 65536
+ *   SGEMM_PROBE_FFMA2    packed fma.rn.f32x2 chains    (each trip: 128 multiply-
+ *                                                       adds per thread, 1024
+ *                                                       threads per multiprocessor)
+ *   SGEMM_PROBE_TF32_SS  tcgen05.mma kind::tf32 M=128 N=256 K=8, both operands
+ *                        in shared memory              iters: MMAs per
+ *   SGEMM_PROBE_TF32_TS  kind::tf32 M=128 N=128 K=8, A in tensor memory (the
+ *                        instruction of the 3xTF32 and TF32 kernels)
+ *   SGEMM_PROBE_BF16_SS  kind::f16, bf16 operands, M=128 N=256 K=16
+ *                                                      multiprocessor, 1 .. 2^22
+ * Returns SGEMM_ERR_INVALID_ARG for an unknown kind, iters out of range or a
+ * NULL flops, SGEMM_ERR_UNSUPPORTED without a compute capability 10.3 GPU,
+ * SGEMM_ERR_LAUNCH if the launch fails.  The tensor-core probes end with a
+ * bounded wait, reported by sgemm_poll_error like the GEMM kernels'. */
+#define SGEMM_PROBE_FFMA 0
+#define SGEMM_PROBE_FFMA2 1
+#define SGEMM_PROBE_TF32_SS 2
+#define SGEMM_PROBE_TF32_TS 3
+#define SGEMM_PROBE_BF16_SS 4
+int sgemm_peak_probe(int kind, long long iters, double *flops, void *stream);
+
 /* Process-wide default path used by sgemm() and sgemm_batched().  Returns
  * SGEMM_ERR_INVALID_ARG for an unknown mode (DEFAULT is not a valid value
  * here). */
@@ -171,6 +230,13 @@ int sgemm_poll_error(void *stream);
  * word and exits normally.  A following sgemm_poll_error() returns
  * SGEMM_ERR_TIMEOUT.  Nothing faults and the context stays usable. */
 int sgemm_selftest_wait_timeout(long long wait_cycles, void *stream);
+
+/* Number of kernels the library has enqueued in this process so far (every
+ * device and stream; a failed launch is not counted).  The difference across
+ * a stretch of calls is the number of kernels they launched: a GEMM call
+ * launches one product kernel, plus the split-K fix-up kernel when its plan
+ * splits, plus one transposition per operand the FP32 path copies. */
+unsigned long long sgemm_kernel_launches(void);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int sgemm_version(void);

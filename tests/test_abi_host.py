@@ -22,7 +22,7 @@ def lib():
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "sgemm.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(sgemm\w*)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:\w+\s+)+\**\s*(sgemm\w*)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_the_boundary():
@@ -106,3 +106,35 @@ def test_plain_sgemm_validates_too(lib):
     assert lib.sgemm_batched(4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4, 0, 0, 0, 0, 10, 2) \
         == lib.SGEMM_ERR_INVALID_ARG
     assert lib.sgemm_selftest_wait_timeout(0) == lib.SGEMM_ERR_INVALID_ARG
+
+
+def host(lib, **kw):
+    a = dict(mode=0, M=8, N=8, K=8, alpha=1.0, A=FAKE, lda=8, B=FAKE, ldb=8, beta=0.0, C=FAKE,
+             ldc=8, transA=0, transB=0, panel_rows=0, dev=FAKE, dev_bytes=1 << 20)
+    a.update(kw)
+    return lib.sgemm_host(a["mode"], a["M"], a["N"], a["K"], a["alpha"], a["A"], a["lda"], a["B"],
+                          a["ldb"], a["beta"], a["C"], a["ldc"], a["transA"], a["transB"],
+                          a["panel_rows"], a["dev"], a["dev_bytes"])
+
+
+@pytest.mark.parametrize("bad", [
+    dict(M=-1), dict(K=-1), dict(lda=7), dict(ldb=7), dict(ldc=7),
+    dict(transA=1, M=9, lda=8), dict(transB=2), dict(panel_rows=-1),
+    dict(C=0), dict(A=0), dict(B=0), dict(dev=0), dict(dev=FAKE + 16), dict(mode=5),
+])
+def test_host_entry_rejects_invalid_arguments(lib, bad):
+    assert host(lib, **bad) == lib.SGEMM_ERR_INVALID_ARG
+
+
+def test_host_entry_empty_is_a_no_op(lib):
+    assert host(lib, M=0, A=0, B=0, C=0, dev=0) == lib.SGEMM_OK
+    assert host(lib, N=0, A=0, B=0, C=0, dev=0) == lib.SGEMM_OK
+
+
+def test_peak_probe_rejects_invalid_arguments(lib):
+    assert lib.sgemm_peak_probe(7, 16)[0] == lib.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_peak_probe(-1, 16)[0] == lib.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_peak_probe("ffma", 0)[0] == lib.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_peak_probe("ffma", (1 << 16) + 1)[0] == lib.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_peak_probe("tf32_ss", (1 << 22) + 1)[0] == lib.SGEMM_ERR_INVALID_ARG
+    assert lib._lib.sgemm_peak_probe(0, 16, None, None) == lib.SGEMM_ERR_INVALID_ARG
