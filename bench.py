@@ -90,7 +90,8 @@ def roofline_peak(mode, num_sms, peaks, source):
 # plans them; the probes, the host-buffer entry point and the allocation-free
 # entry point are left out (they do not change what the timed kernels do).
 TIMED_SOURCES = ("api.cu", "common.cuh", "internal.h", "kernels_simt.cu", "kernels_tc.cu",
-                 "params.h", "repack.cu", "simt_fp32.cuh", "tc_direct.cuh", "tc_tf32.cuh")
+                 "kernels_tcp.cu", "params.h", "repack.cu", "simt_fp32.cuh", "tc_direct.cuh",
+                 "tc_pair.cuh", "tc_tf32.cuh")
 
 
 def kernel_source_hash():

@@ -229,15 +229,16 @@ bool encode_operand(CUtensorMap *map, const float *base, bool kin, long long row
 
 int min_slice_k(int mode) { return mode == SGEMM_MODE_FP32 ? 64 : 256; }
 
-// FLOP/s per multiprocessor each path sustains on GB300 (measured at 4092^3
-// with TMA-fed operands, and on the ragged 1000 x 1500 x 777 case, whose A
-// TMA cannot describe: the FP32 kernel's cp.async fallback, the tensor-core
-// direct kernel).
-double path_rate_per_sm(int mode, bool tma)
+// FLOP/s per multiprocessor each kernel sustains on GB300 (measured at
+// 4092^3 with TMA-fed operands -- the FP32 kernel, the tensor-core pair
+// kernel -- and on the ragged 1000 x 1500 x 777 case, whose A TMA cannot
+// describe: the FP32 kernel's cp.async fallback, the tensor-core direct
+// kernel).
+double path_rate_per_sm(int mode, int feed)
 {
-    if (mode == SGEMM_MODE_FP32) return tma ? 0.40e12 : 0.24e12;
-    if (mode == SGEMM_MODE_3XTF32) return tma ? 1.54e12 : 0.47e12;
-    return tma ? 2.16e12 : 0.55e12;
+    if (mode == SGEMM_MODE_FP32) return feed == kFeedDirect ? 0.24e12 : 0.40e12;
+    if (mode == SGEMM_MODE_3XTF32) return feed == kFeedDirect ? 0.47e12 : 1.6e12;
+    return feed == kFeedDirect ? 0.55e12 : 2.5e12;
 }
 
 size_t splitk_workspace_bytes(long long split_tiles, int splits, int bm, int bn)
@@ -246,16 +247,18 @@ size_t splitk_workspace_bytes(long long split_tiles, int splits, int bm, int bn)
     return static_cast<size_t>(split_tiles) * splits * static_cast<size_t>(bm) * bn * sizeof(float);
 }
 
-SplitPlan choose_plan(long long num_tiles, int K, int num_sms, int mode, int bm, int bn, bool tma,
+SplitPlan choose_plan(long long num_tiles, int K, int slots, int mode, int bm, int bn, int feed,
                       size_t budget)
 {
     SplitPlan best{1, num_tiles, 0};
-    if (num_tiles <= 0 || num_sms <= 0) return best;
+    if (num_tiles <= 0 || slots <= 0) return best;
+    const int num_sms = slots;  // units running at once
     const long long full = num_tiles / num_sms, rem = num_tiles % num_sms;
     if (rem == 0) return best;
     long long smax = K / min_slice_k(mode);
     if (smax > kMaxSplits) smax = kMaxSplits;
-    const double t_tile = 2.0 * bm * bn * static_cast<double>(K) / path_rate_per_sm(mode, tma);
+    const double unit_rate = path_rate_per_sm(mode, feed) * (feed == kFeedPair ? 2 : 1);
+    const double t_tile = 2.0 * bm * bn * static_cast<double>(K) / unit_rate;
     const double t_whole = t_tile * static_cast<double>(full + 1);
     double best_t = t_whole;
     for (int s = 2; s <= smax; ++s) {
@@ -274,7 +277,7 @@ SplitPlan choose_plan(long long num_tiles, int K, int num_sms, int mode, int bm,
     return best;
 }
 
-int plan_splits(Plan &plan, int bm, int bn, bool tma)
+int plan_splits(Plan &plan, int bm, int bn, int feed, int slots)
 {
     GemmParams &p = plan.p;
     p.splits = 1;
@@ -282,7 +285,7 @@ int plan_splits(Plan &plan, int bm, int bn, bool tma)
     p.ws_part = nullptr;
     if (plan.ws != nullptr) {
         const SplitPlan sp =
-            choose_plan(p.num_tiles, p.K, plan.num_sms, plan.mode, bm, bn, tma, plan.ws_bytes);
+            choose_plan(p.num_tiles, p.K, slots, plan.mode, bm, bn, feed, plan.ws_bytes);
         if (sp.splits > 1) {
             p.splits = sp.splits;
             p.dp_tiles = sp.dp_tiles;
@@ -334,25 +337,35 @@ SplitPlan plan_query(int mode, int M, int N, int K, int Q, bool one_wave)
     if (di == nullptr) return none;
     const int sms = di->num_sms;
     SplitPlan out = none;
-    for (int shape = 0; shape < (mode == SGEMM_MODE_FP32 ? 2 : 1); ++shape) {
-        int bm = 0, bn = 0;
-        if (mode == SGEMM_MODE_FP32)
+    // Whether the operands go through TMA depends on pointers and leading
+    // dimensions the query does not take: plan for every kernel the mode
+    // may run (FP32: the two tile shapes, each TMA-fed or not; tensor
+    // cores: the direct kernel's 128 x 128 tiles, the pair kernel's 256 x 128).
+    for (int shape = 0; shape < 2; ++shape) {
+        int bm = 0, bn = 0, slots = sms;
+        int feeds[2] = {kFeedDirect, kFeedTma};
+        if (mode == SGEMM_MODE_FP32) {
             simt_tile_dims(shape == 1, bm, bn);
-        else
-            tc_tile_dims(bm, bn);
+        } else {
+            tc_tile_dims(shape == 1, bm, bn);
+            if (shape == 1) {
+                slots = tc_pair_slots(sms);
+                feeds[0] = feeds[1] = kFeedPair;
+            } else {
+                feeds[1] = kFeedDirect;
+            }
+        }
         const long long tiles =
             static_cast<long long>(Q) * ((M + bm - 1) / bm) * ((N + bn - 1) / bn);
         SplitPlan sp{1, tiles, 0};
         if (!one_wave) {
-            // whether the operands go through TMA depends on pointers and
-            // leading dimensions the query does not take: plan for both
-            for (int tma = 0; tma < 2; ++tma) {
+            for (int f = 0; f < 2; ++f) {
                 const SplitPlan t =
-                    choose_plan(tiles, K, sms, mode, bm, bn, tma != 0, ~static_cast<size_t>(0));
+                    choose_plan(tiles, K, slots, mode, bm, bn, feeds[f], ~static_cast<size_t>(0));
                 if (t.ws_bytes > sp.ws_bytes) sp = t;
             }
-        } else if (2 * tiles <= sms) {
-            long long s = sms / tiles;
+        } else if (2 * tiles <= slots) {
+            long long s = slots / tiles;
             const long long by_k = K / min_slice_k(mode);
             if (s > by_k) s = by_k;
             if (s > kMaxSplits) s = kMaxSplits;

@@ -60,17 +60,21 @@ struct Layout {
 };
 
 // Rows per panel when the caller leaves it to the library: enough output
-// tiles for about two waves of the GPU per panel (fewer, smaller panels
-// would leave multiprocessors idle in every product), at most kMaxPanels.
+// tiles for about one wave of the GPU per panel (measured on GB300 at
+// 4092^3: one to two waves per panel beat both fewer, larger panels, whose
+// first copy-in and last copy-out overlap nothing, and smaller ones, which
+// leave multiprocessors idle in every product), at most kMaxPanels.
 int auto_panel_rows(int mode, int M, int N, int num_sms)
 {
-    int bm = 0, bn = 0;
-    if (mode == SGEMM_MODE_FP32)
+    int bm = 0, bn = 0, slots = num_sms;
+    if (mode == SGEMM_MODE_FP32) {
         simt_tile_dims(false, bm, bn);
-    else
-        tc_tile_dims(bm, bn);
+    } else {
+        tc_tile_dims(true, bm, bn);
+        slots = tc_pair_slots(num_sms);
+    }
     const long long tiles_n = (N + bn - 1) / bn;
-    long long rows_tiles = (2LL * num_sms + tiles_n - 1) / tiles_n;
+    long long rows_tiles = (static_cast<long long>(slots) + tiles_n - 1) / tiles_n;
     if (rows_tiles < 1) rows_tiles = 1;
     long long rows = rows_tiles * bm;
     const long long min_rows = (M + kMaxPanels - 1) / kMaxPanels;

@@ -23,10 +23,11 @@ struct Plan {
     size_t ws_bytes;
 };
 
-// Split-K plan shared by both kernels (BM x BN output tiles, one persistent
-// CTA per multiprocessor).  With T tiles on G multiprocessors the grid runs
-// floor(T/G) whole waves and a last wave of r = T mod G tiles that leaves
-// the rest of the GPU idle.  The planner may cut the tiles of that last wave
+// Split-K plan shared by the kernels (BM x BN output tiles, persistent: one
+// CTA per multiprocessor, or one CTA pair per two for the tensor-core pair
+// kernel).  With T tiles on G units at once (multiprocessors, or pairs) the
+// grid runs floor(T/G) whole waves and a last wave of r = T mod G tiles that
+// leaves the rest of the GPU idle.  The planner may cut the tiles of that last wave
 // (all tiles when T < G) along K into `splits` slices, so that the slices
 // spread over the whole GPU.  Each slice writes its partial tile, unscaled,
 // to its own BM x BN fp32 slot of the workspace, and a fix-up kernel
@@ -35,9 +36,10 @@ struct Plan {
 //     t_tile * (floor(T/G) + ceil(r * s / G) / s)
 //       + (s > 1: 3 us + 2 * workspace bytes / (8 TB/s if they stay in L2,
 //                                                 i.e. <= 64 MB, else 3 TB/s))
-// with t_tile = 2 * BM * BN * K / (per-multiprocessor rate of the path, as
-// measured on GB300: 0.40 TFLOP/s FP32, 1.54 3xTF32, 2.16 TF32 with TMA-fed
-// operands; 0.24, 0.47, 0.55 for operands TMA cannot describe).  s runs over
+// with t_tile = 2 * BM * BN * K / (multiprocessors per unit x the kernel's
+// per-multiprocessor rate, as measured on GB300: 0.40 TFLOP/s FP32, 1.6
+// 3xTF32, 2.5 TF32 with TMA-fed operands; 0.24, 0.47, 0.55 for operands TMA
+// cannot describe).  s runs over
 // 1 .. min(16, K / min_slice_k(mode)); the best s is used only when it
 // saves at least 1%.  Each slice is at least
 // min_slice_k(mode) deep: 64 for the FP32 path, 256 for the tensor-core
@@ -47,6 +49,10 @@ struct Plan {
 // kernel's k-block is at most the minimum slice, so no slice is empty).  A
 // plan whose workspace exceeds the caller's budget is not considered.
 constexpr int kMaxSplits = 16;
+// How a kernel is fed: operands loaded by the threads themselves (the FP32
+// kernel's cp.async producer, the tensor-core direct kernel), by TMA on one
+// CTA per unit, or by TMA on a CTA pair per unit (two multiprocessors).
+enum Feed { kFeedDirect = 0, kFeedTma = 1, kFeedPair = 2 };
 struct SplitPlan {
     int splits;          // 1 = no split
     long long dp_tiles;  // tiles computed whole (they come first in unit order)
@@ -54,16 +60,23 @@ struct SplitPlan {
 };
 int min_slice_k(int mode);
 size_t splitk_workspace_bytes(long long split_tiles, int splits, int bm, int bn);
-SplitPlan choose_plan(long long num_tiles, int K, int num_sms, int mode, int bm, int bn, bool tma,
+// slots: units that run at once (multiprocessors, or CTA pairs for kFeedPair).
+SplitPlan choose_plan(long long num_tiles, int K, int slots, int mode, int bm, int bn, int feed,
                       size_t budget);
 // Fills p.splits / dp_tiles / num_units / ws_part for the launch (bm x bn
 // tiles, operands through TMA or not) from the best plan that fits the
 // caller's workspace.  Returns an sgemm status.
-int plan_splits(Plan &plan, int bm, int bn, bool tma);
+int plan_splits(Plan &plan, int bm, int bn, int feed, int slots);
 // Output tile of each kernel (defined beside its launcher); the FP32 path's
 // depends on whether both operands are K-inner.
 void simt_tile_dims(bool both_k_inner, int &bm, int &bn);
-void tc_tile_dims(int &bm, int &bn);
+// pair: the CTA-pair kernel's tile (the single-CTA kernels' otherwise).
+void tc_tile_dims(bool pair, int &bm, int &bn);
+// CTA pairs of the pair kernel that fit on the device at once (cached).
+int tc_pair_slots(int num_sms);
+// Launches the CTA-pair tensor-core kernel (tile counts filled in by the
+// caller) with the tensor maps of its A (128-row boxes) and B (64-row boxes).
+int launch_tc_pair(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB, int slots);
 // Enqueues the split-K fix-up for a launch whose plan split (bm x bn tiles).
 int launch_fixup(Plan &plan, int bm, int bn);
 // The plan sgemm_workspace_size reports for a call (no budget), or splits = 1.

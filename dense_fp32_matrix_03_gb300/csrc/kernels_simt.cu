@@ -64,7 +64,8 @@ int launch_cfg(Plan &plan)
         use_tma = encode_operand(&tmA, p.A, A_KIN, p.M, p.K, p.lda, p.Q, p.sA, Cfg::BM) &&
                   encode_operand(&tmB, p.B, B_KIN, p.N, p.K, p.ldb, p.Q, p.sB, Cfg::BN);
     }
-    const int rc = plan_splits(plan, Cfg::BM, Cfg::BN, use_tma);
+    const int rc = plan_splits(plan, Cfg::BM, Cfg::BN, use_tma ? kFeedTma : kFeedDirect,
+                               plan.num_sms);
     if (rc != SGEMM_OK) return rc;
     if (use_tma) return launch_one<Cfg, A_KIN, B_KIN, true, false>(plan, tmA, tmB);
     if (plan.even_k) return launch_one<Cfg, A_KIN, B_KIN, false, true>(plan, tmA, tmB);

@@ -1,19 +1,20 @@
 // kernels_tc.cu -- host launcher of the tcgen05 tensor-core paths: 3xTF32
-// (FP32 accuracy) and plain TF32.  Operands TMA can describe run on the TMA
-// kernel (tc_tf32.cuh), whose copy engine stages them in shared memory;
-// others (a row pitch or batch stride that is not a multiple of 16 bytes, an
+// (FP32 accuracy) and plain TF32.  Operands TMA can describe run on the
+// CTA-pair kernel (tc_pair.cuh, launched from kernels_tcp.cu): 256 x 128
+// tiles, TMA-staged operands, each CTA of a pair converting half of B.
+// Others (a row pitch or batch stride that is not a multiple of 16 bytes, an
 // unaligned base) run on the direct kernel (tc_direct.cuh), whose converter
 // warps load them from global memory themselves.  Measured on GB300: the
 // direct kernel runs the ragged 1000 x 1500 x 777 case (lda = 777) at 43
 // TFLOP/s where staging it with cp.async gave 19-25, but it is slower than
-// TMA for aligned operands (232 vs 114 TFLOP/s at 4092^3: its loads wait on
-// L2 latency that the TMA ring hides).
+// TMA for aligned operands (114 TFLOP/s at 4092^3: its loads wait on L2
+// latency that the TMA ring hides).
 #include <cstring>
 
 #include "../../include/sgemm.h"
 #include "internal.h"
 #include "tc_direct.cuh"
-#include "tc_tf32.cuh"
+#include "tc_pair.cuh"
 
 namespace sg {
 
@@ -21,23 +22,6 @@ namespace {
 
 constexpr int kBN = 128;
 constexpr int kGroupM = 8;
-
-template <bool SPLIT3, bool A_KIN, bool B_KIN>
-int launch_tma(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
-{
-    using C = tc::Cfg<kBN, SPLIT3, A_KIN, B_KIN>;
-    auto kern = tc::tc_sgemm_kernel<C>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES) != cudaSuccess)
-        return SGEMM_ERR_LAUNCH;
-    long long grid = plan.p.num_units;
-    if (grid > plan.num_sms) grid = plan.num_sms;
-    kern<<<static_cast<unsigned>(grid), tc::kThreads, C::SMEM_BYTES, plan.stream>>>(tmA, tmB,
-                                                                                  plan.p);
-    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
-    note_launch();
-    return plan.p.splits > 1 ? launch_fixup(plan, tc::BM, kBN) : SGEMM_OK;
-}
 
 template <bool SPLIT3, bool A_KIN, bool B_KIN>
 int launch_direct(Plan &plan)
@@ -56,15 +40,9 @@ int launch_direct(Plan &plan)
 }
 
 template <bool SPLIT3>
-int dispatch(Plan &plan, bool use_tma, const CUtensorMap &tmA, const CUtensorMap &tmB)
+int dispatch_direct(Plan &plan)
 {
     const bool a_kin = !plan.transA, b_kin = plan.transB;
-    if (use_tma) {
-        if (a_kin && !b_kin) return launch_tma<SPLIT3, true, false>(plan, tmA, tmB);
-        if (a_kin && b_kin) return launch_tma<SPLIT3, true, true>(plan, tmA, tmB);
-        if (!a_kin && !b_kin) return launch_tma<SPLIT3, false, false>(plan, tmA, tmB);
-        return launch_tma<SPLIT3, false, true>(plan, tmA, tmB);
-    }
     if (a_kin && !b_kin) return launch_direct<SPLIT3, true, false>(plan);
     if (a_kin && b_kin) return launch_direct<SPLIT3, true, true>(plan);
     if (!a_kin && !b_kin) return launch_direct<SPLIT3, false, false>(plan);
@@ -73,35 +51,41 @@ int dispatch(Plan &plan, bool use_tma, const CUtensorMap &tmA, const CUtensorMap
 
 }  // namespace
 
-void tc_tile_dims(int &bm, int &bn)
+void tc_tile_dims(bool pair, int &bm, int &bn)
 {
-    bm = tc::BM;
-    bn = kBN;
+    bm = pair ? tcp::PM : tc::BM;
+    bn = pair ? tcp::BN : kBN;
 }
 
 int launch_tc(Plan &plan)
 {
     GemmParams &p = plan.p;
-    p.tiles_m = (p.M + tc::BM - 1) / tc::BM;
-    p.tiles_n = (p.N + kBN - 1) / kBN;
     p.k_blocks = (p.K + tc::BK - 1) / tc::BK;
     p.group_m = kGroupM;
-    p.num_tiles = static_cast<long long>(p.Q) * p.tiles_m * p.tiles_n;
     plan.even_k = (p.K % tc::BK) == 0;
 
     alignas(64) CUtensorMap tmA;
     alignas(64) CUtensorMap tmB;
     std::memset(&tmA, 0, sizeof(tmA));
     std::memset(&tmB, 0, sizeof(tmB));
-    bool use_tma = plan.a_tma && plan.b_tma;
-    if (use_tma) {
-        use_tma = encode_operand(&tmA, p.A, !plan.transA, p.M, p.K, p.lda, p.Q, p.sA, tc::BM) &&
-                  encode_operand(&tmB, p.B, plan.transB, p.N, p.K, p.ldb, p.Q, p.sB, kBN);
+    if (plan.a_tma && plan.b_tma &&
+        encode_operand(&tmA, p.A, !plan.transA, p.M, p.K, p.lda, p.Q, p.sA, tcp::BM) &&
+        encode_operand(&tmB, p.B, plan.transB, p.N, p.K, p.ldb, p.Q, p.sB, tcp::HN)) {
+        p.tiles_m = (p.M + tcp::PM - 1) / tcp::PM;
+        p.tiles_n = (p.N + tcp::BN - 1) / tcp::BN;
+        p.num_tiles = static_cast<long long>(p.Q) * p.tiles_m * p.tiles_n;
+        const int slots = tc_pair_slots(plan.num_sms);
+        const int rc = plan_splits(plan, tcp::PM, tcp::BN, kFeedPair, slots);
+        if (rc != SGEMM_OK) return rc;
+        return launch_tc_pair(plan, tmA, tmB, slots);
     }
-    const int rc = plan_splits(plan, tc::BM, kBN, use_tma);
+    p.tiles_m = (p.M + tc::BM - 1) / tc::BM;
+    p.tiles_n = (p.N + kBN - 1) / kBN;
+    p.num_tiles = static_cast<long long>(p.Q) * p.tiles_m * p.tiles_n;
+    const int rc = plan_splits(plan, tc::BM, kBN, kFeedDirect, plan.num_sms);
     if (rc != SGEMM_OK) return rc;
-    return plan.mode == SGEMM_MODE_3XTF32 ? dispatch<true>(plan, use_tma, tmA, tmB)
-                                          : dispatch<false>(plan, use_tma, tmA, tmB);
+    return plan.mode == SGEMM_MODE_3XTF32 ? dispatch_direct<true>(plan)
+                                          : dispatch_direct<false>(plan);
 }
 
 }  // namespace sg

@@ -1,0 +1,508 @@
+// tc_pair.cuh -- the tcgen05 SGEMM kernel on CTA pairs (3xTF32 and TF32).
+//
+// Same arithmetic as tc_tf32.cuh (hi/lo split, three kind::tf32 MMAs per
+// k step for 3xTF32, one for TF32), on 256 x 128 output tiles computed by a
+// cluster of two CTAs on two multiprocessors with cta_group::2 MMAs
+// (M = 256, N = 128, K = 8):
+//   - each CTA loads, splits and keeps in its own TMEM the A rows of its
+//     half of the tile (128 rows), as the single-CTA kernel does;
+//   - each CTA loads and splits only HALF of the B tile (64 of its 128
+//     rows of B^T) into its own shared memory; one MMA reads both halves;
+//   - one thread of the even CTA issues every MMA; its commits arrive on the
+//     barriers of both CTAs (multicast), and both CTAs' converters and
+//     epilogue warps arrive on the even CTA's barriers (remote arrives).
+// Per CTA and 32-wide k-block that halves the B work: 24 KB of TMA writes
+// (A 16 + B 8), 24 KB of converter reads, 16 KB of B-plane writes and 24 KB
+// of MMA B reads = 88 KB of shared-memory traffic, against 144 KB in the
+// single-CTA kernel, whose MMAs wait on shared-memory bandwidth (measured:
+// the 128 x 128 kernel's tensor pipe completes an MMA every ~105 cycles,
+// against ~69 cycles with its operands already resident).
+//
+// Warps and barriers as in tc_tf32.cuh.  Barriers that both CTAs arrive on
+// live in the even CTA (split_full: 16 converter warps; acc_empty: 8
+// epilogue warps); the others are per CTA.  Waits on barriers another CTA
+// signals use cluster-scope acquire.  Every wait is bounded; the CTAs meet
+// at a cluster barrier before they free their TMEM (jointly) and exit, so
+// that neither leaves while the other may still touch its shared memory.
+#pragma once
+
+#include "tc_tf32.cuh"
+
+// Ring depths (raw fp32 tiles / split stages); TMEM holds at most 4 split
+// stages of 3xTF32 A planes and 8 of TF32 beside the two accumulators.
+#ifndef SG_TCP_RAW3
+#define SG_TCP_RAW3 6
+#define SG_TCP_SPLIT3 4
+#define SG_TCP_RAW1 6
+#define SG_TCP_SPLIT1 8
+#endif
+
+namespace sg {
+namespace tcp {
+
+using tc::BK;
+using tc::kAConvWarp0;
+using tc::kBConvThreads;
+using tc::kBConvWarp0;
+using tc::kConvWarps;
+using tc::kEpiWarp0;
+using tc::kThreads;
+using tc::kTmemCols;
+using tc::Ring;
+using tc::UK;
+
+constexpr int BM = 128;      // rows of C per CTA
+constexpr int PM = 2 * BM;   // rows per pair tile (the MMA's M)
+constexpr int BN = 128;      // columns per pair tile (the MMA's N)
+constexpr int HN = BN / 2;   // rows of B^T each CTA holds
+
+template <bool SPLIT3_, bool A_KIN_, bool B_KIN_>
+struct Cfg {
+    static constexpr bool SPLIT3 = SPLIT3_, A_KIN = A_KIN_, B_KIN = B_KIN_;
+    static constexpr int A_BYTES = BM * BK * 4;
+    static constexpr int B_BYTES = HN * BK * 4;
+    static constexpr int RAW_BYTES = A_BYTES + B_BYTES;
+    static constexpr int PLANES = SPLIT3 ? 2 : 1;
+    static constexpr int SPLIT_BYTES = PLANES * B_BYTES;
+    static constexpr int RAW_STAGES = SPLIT3 ? SG_TCP_RAW3 : SG_TCP_RAW1;
+    static constexpr int SPLIT_STAGES = SPLIT3 ? SG_TCP_SPLIT3 : SG_TCP_SPLIT1;
+    static constexpr int ACC_COLS = 2 * BN;
+    static constexpr int A_COLS = PLANES * BK;
+    static constexpr int NBAR = 2 * RAW_STAGES + 2 * SPLIT_STAGES + 4 + 1;
+    static constexpr int SMEM_BYTES =
+        RAW_STAGES * RAW_BYTES + SPLIT_STAGES * SPLIT_BYTES + NBAR * 8 + 16 + 1024;
+    static_assert(ACC_COLS + SPLIT_STAGES * A_COLS <= static_cast<int>(kTmemCols), "TMEM columns");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+    static constexpr int OFF_BHI = 0, OFF_BLO = B_BYTES;
+};
+
+// Instruction descriptor: kind::tf32, fp32 accumulate, both operands
+// K-major, M = 256 (two CTAs), N = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) |
+                            (static_cast<uint32_t>(BN >> 3) << 17) |
+                            (static_cast<uint32_t>(PM >> 4) << 24);
+
+// ------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t cta_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of both CTAs: arrive (release) and wait (acquire).
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// One warp of EACH CTA of the pair takes part: both receive the same address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// The MMAs (issue_stage) compute D[tmem] (+)= A[tmem] * B[smem]^T over both
+// CTAs: rows 0..127 of A and D in the even CTA's TMEM, 128..255 in the odd
+// CTA's, at the same addresses; B's first 64 rows in the even CTA's shared
+// memory, the rest in the odd CTA's, at the descriptor's offset in each.
+// Issues one split stage's MMAs (four k steps of 8) into accumulator d: for
+// 3xTF32 lo_a*hi_b, hi_a*lo_b, hi_a*hi_b per step, else hi_a*hi_b; the
+// stage's first MMA overwrites d unless acc0.  The A planes are TMEM
+// columns a_hi / a_lo (+8 per step), the B planes descriptors b_hi / b_lo
+// (+2 per step: 32 bytes in 16-byte units).  In the same instruction block
+// it tests, without blocking, whether the barrier at shared address nbar has
+// completed the phase of parity npar (the next stage's), and returns that:
+// the test's latency then overlaps the MMA issue instead of leaving the
+// tensor pipe idle between stages (its queue holds little more than the MMA
+// in flight).  A true result carries the test's cluster-scope acquire.
+template <bool SPLIT3>
+__device__ __forceinline__ uint32_t issue_stage(uint32_t d, uint32_t a_hi, uint32_t a_lo,
+                                                uint64_t b_hi, uint64_t b_lo, uint32_t acc0,
+                                                uint32_t nbar, uint32_t npar)
+{
+    uint32_t ready;
+    if (SPLIT3) {
+        asm volatile(
+            "{\n\t.reg .pred q, p0, p1;\n\t.reg .b64 bh, bl;\n\t.reg .b32 ah, al;\n\t"
+            "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 q, [%7], %8;\n\t"
+            "setp.ne.b32 p0, %6, 0;\n\t"
+            "setp.eq.b32 p1, %6, %6;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%1], [%3], %4, %9, p0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%1], [%2], %5, %9, p1;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%1], [%2], %4, %9, p1;\n\t"
+            "add.u32 ah, %2, 8;\n\tadd.u32 al, %3, 8;\n\tadd.s64 bh, %4, 2;\n\tadd.s64 bl, %5, 2;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%1], [al], bh, %9, p1;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%1], [ah], bl, %9, p1;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%1], [ah], bh, %9, p1;\n\t"
+            "add.u32 ah, %2, 16;\n\tadd.u32 al, %3, 16;\n\tadd.s64 bh, %4, 4;\n\tadd.s64 bl, %5, 4;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%1], [al], bh, %9, p1;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%1], [ah], bl, %9, p1;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%1], [ah], bh, %9, p1;\n\t"
+            "add.u32 ah, %2, 24;\n\tadd.u32 al, %3, 24;\n\tadd.s64 bh, %4, 6;\n\tadd.s64 bl, %5, 6;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%1], [al], bh, %9, p1;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%1], [ah], bl, %9, p1;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%1], [ah], bh, %9, p1;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(ready)
+            : "r"(d), "r"(a_hi), "r"(a_lo), "l"(b_hi), "l"(b_lo), "r"(acc0), "r"(nbar),
+              "r"(npar), "r"(kIdesc)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred q, p0, p1;\n\t.reg .b64 bh;\n\t.reg .b32 ah;\n\t"
+            "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 q, [%4], %5;\n\t"
+            "setp.ne.b32 p0, %3, 0;\n\t"
+            "setp.eq.b32 p1, %3, %3;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%1], [%2], %6, %7, p0;\n\t"
+            "add.u32 ah, %2, 8;\n\tadd.s64 bh, %6, 2;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%1], [ah], bh, %7, p1;\n\t"
+            "add.u32 ah, %2, 16;\n\tadd.s64 bh, %6, 4;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%1], [ah], bh, %7, p1;\n\t"
+            "add.u32 ah, %2, 24;\n\tadd.s64 bh, %6, 6;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%1], [ah], bh, %7, p1;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(ready)
+            : "r"(d), "r"(a_hi), "r"(acc0), "r"(nbar), "r"(npar), "l"(b_hi), "r"(kIdesc)
+            : "memory");
+        (void)a_lo;
+        (void)b_lo;
+    }
+    return ready;
+}
+
+// Both CTAs' barriers at this offset receive one arrival once every MMA the
+// thread issued before has completed.
+__device__ __forceinline__ void umma_commit_both(uint64_t *bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
+}
+
+// Arrives on the barrier at this offset in CTA `rank` of the pair, with the
+// arrive's default (CTA-scope release) semantics.  The data it announces --
+// split planes in this CTA's shared memory, A planes in this CTA's TMEM --
+// has been made visible to the tensor core before the arrive, by
+// fence.proxy.async (shared-memory stores) or tcgen05.wait::st (TMEM
+// stores); the MMA that reads it is issued only after the even CTA's
+// cluster-scope acquire of the barrier.  (A cluster-scope release here
+// costs each converter warp ~1200 cycles per stage on GB300, more than the
+// whole stage's work.)
+__device__ __forceinline__ void arrive_on(uint64_t *bar, uint32_t rank)
+{
+    asm volatile(
+        "{\n\t.reg .b32 ra;\n\t"
+        "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
+        "mbarrier.arrive.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_u32(bar)),
+        "r"(rank)
+        : "memory");
+}
+
+__device__ __forceinline__ bool try_wait_cl(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool try_wait_cl_sleep(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kWaitSleepNs)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait with cluster-scope acquire (the barrier is signalled from the
+// other CTA or by a multicast commit).
+__device__ __forceinline__ bool wait_cl(uint64_t *bar, uint32_t parity, const Abort &ab,
+                                        unsigned int code, bool sleep = false)
+{
+    if (try_wait_cl(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (sleep ? try_wait_cl_sleep(bar, parity) : try_wait_cl(bar, parity)) return true;
+        if (*ab.flag) return false;
+        if (clock64() - t0 > ab.limit) {
+            atomicOr(ab.status, code);
+            *ab.flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void drain_cl(uint64_t *bar, uint32_t parity, long long limit)
+{
+    const long long t0 = clock64();
+    while (!try_wait_cl(bar, parity)) {
+        if (clock64() - t0 > limit) return;
+    }
+}
+
+__device__ __forceinline__ bool warp_wait_cl(uint64_t *bar, uint32_t parity, const Abort &ab,
+                                             unsigned int code)
+{
+    const bool ok = wait_cl(bar, parity, ab, code);
+    return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// ------------------------------------------------------------ the kernel
+
+template <class C>
+struct Smem {
+    uint8_t *raw;
+    uint8_t *split;
+    uint64_t *raw_full, *raw_empty, *split_full, *split_empty, *acc_full, *acc_empty, *mma_done;
+    uint32_t *tmem_base;
+    volatile int *abort_flag;
+};
+
+template <class C>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tcp_sgemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const GemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Smem<C> sm;
+    sm.raw = base;
+    sm.split = base + C::RAW_STAGES * C::RAW_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm.split + C::SPLIT_STAGES * C::SPLIT_BYTES);
+    sm.raw_full = bars;
+    sm.raw_empty = sm.raw_full + C::RAW_STAGES;
+    sm.split_full = sm.raw_empty + C::RAW_STAGES;
+    sm.split_empty = sm.split_full + C::SPLIT_STAGES;
+    sm.acc_full = sm.split_empty + C::SPLIT_STAGES;
+    sm.acc_empty = sm.acc_full + 2;
+    sm.mma_done = sm.acc_empty + 2;
+    sm.tmem_base = reinterpret_cast<uint32_t *>(sm.mma_done + 1);
+    sm.abort_flag = reinterpret_cast<volatile int *>(sm.tmem_base + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cta_rank();
+    const long long cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::RAW_STAGES; ++s) {
+            mbar_init(&sm.raw_full[s], 1u);
+            mbar_init(&sm.raw_empty[s], kConvWarps);
+        }
+        for (int s = 0; s < C::SPLIT_STAGES; ++s) {
+            mbar_init(&sm.split_full[s], 2 * kConvWarps);  // both CTAs' converters
+            mbar_init(&sm.split_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.acc_full[b], 1);
+            mbar_init(&sm.acc_empty[b], 2 * 4);  // both CTAs' epilogue warps
+        }
+        mbar_init(sm.mma_done, 1);
+        *sm.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc_pair(sm.tmem_base, kTmemCols);
+    tc::tc_fence_before();
+    cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
+    tc::tc_fence_after();
+    const uint32_t tmem = *sm.tmem_base;
+    const Abort ab{sm.abort_flag, p.status, p.wait_limit};
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer (own CTA's rows)
+        Ring<C::RAW_STAGES> rr;
+        long long issued = 0;
+        bool ok = true;
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+        }
+        for (long long u = cid; ok && u < p.num_units; u += ncl) {
+            const WorkUnit wu = work_unit(u, p);
+            const TileCoord &tc = wu.tc;
+            const int m0 = tc.tm * PM + static_cast<int>(rank) * BM;
+            const int n0 = tc.tn * BN + static_cast<int>(rank) * HN;
+            for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
+                uint8_t *sa = sm.raw + rr.s * C::RAW_BYTES;
+                uint8_t *sb = sa + C::A_BYTES;
+                const int k0 = kb * BK;
+                if (lane == 0) {
+                    if (!mbar_wait(&sm.raw_empty[rr.s], rr.ph ^ 1u, ab, kStatusWaitEmpty)) {
+                        ok = false;
+                    } else {
+                        const int qa = tc.q * p.a_q_step, qb = tc.q * p.b_q_step;
+                        mbar_arrive_expect_tx(&sm.raw_full[rr.s], C::RAW_BYTES);
+                        if (C::A_KIN) tma_load_3d(sa, &tmA, &sm.raw_full[rr.s], k0, m0, qa);
+                        else          tma_load_3d(sa, &tmA, &sm.raw_full[rr.s], m0, k0, qa);
+                        if (C::B_KIN) tma_load_3d(sb, &tmB, &sm.raw_full[rr.s], k0, n0, qb);
+                        else          tma_load_3d(sb, &tmB, &sm.raw_full[rr.s], n0, k0, qb);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                ++issued;
+                rr.next();
+            }
+        }
+        if (!ok && lane == 0) {
+            Ring<C::RAW_STAGES> d;
+            for (long long j = 0; j < issued; ++j) {
+                if (j + C::RAW_STAGES >= issued) mbar_drain(&sm.raw_full[d.s], d.ph, ab.limit);
+                d.next();
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (even CTA only)
+        if (rank == 0 && lane == 0) {
+            Ring<C::SPLIT_STAGES> sr;
+            Ring<2> acc;
+            bool ok = true;
+            bool any = false;
+            // B descriptors of split stage 0; stage s and k step kk are at
+            // + s * SPLIT_BYTES + 32 * kk bytes (the start address field
+            // counts 16-byte units), so the issue loop only adds constants.
+            const uint64_t bdesc0 = tc::kmajor_sw128_desc(smem_u32(sm.split) + C::OFF_BHI);
+            for (long long u = cid; ok && u < p.num_units; u += ncl) {
+                const WorkUnit wu = work_unit(u, p);
+                if (!wait_cl(&sm.acc_empty[acc.s], acc.ph ^ 1u, ab, kStatusWaitAcc)) {
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+                const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc.s * BN);
+                uint32_t ready = 0;  // split_full[sr] already seen complete
+                for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
+                    if (!ready && !wait_cl(&sm.split_full[sr.s], sr.ph, ab, kStatusWaitConv)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    const uint64_t b_hi =
+                        bdesc0 + static_cast<uint64_t>(sr.s * (C::SPLIT_BYTES >> 4));
+                    const uint64_t b_lo = b_hi + (C::OFF_BLO >> 4);
+                    const uint32_t a_hi = tmem + C::ACC_COLS + sr.s * C::A_COLS;
+                    Ring<C::SPLIT_STAGES> nx = sr;
+                    nx.next();
+                    ready = issue_stage<C::SPLIT3>(d_tmem, a_hi, a_hi + BK, b_hi, b_lo,
+                                                   kb > wu.kb_lo ? 1u : 0u,
+                                                   smem_u32(&sm.split_full[nx.s]), nx.ph);
+                    if (kb + 1 == wu.kb_hi) ready = 0;  // the next unit waits afresh
+                    any = true;
+                    umma_commit_both(&sm.split_empty[sr.s]);
+                    sr.next();
+                }
+                if (!ok) break;
+                umma_commit_both(&sm.acc_full[acc.s]);
+                acc.next();
+            }
+            if (any) {
+                umma_commit_both(sm.mma_done);
+                drain_cl(sm.mma_done, 0, ab.limit);
+            }
+        }
+        __syncwarp();
+    } else if (warp < kEpiWarp0) {
+        // ------------------------------------------------ converters (own CTA's halves)
+        const bool is_a = warp < kBConvWarp0;
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const int ct = threadIdx.x - kBConvWarp0 * 32;
+        Ring<C::RAW_STAGES> rr;
+        Ring<C::SPLIT_STAGES> sr;
+        bool ok = true;
+        for (long long u = cid; ok && u < p.num_units; u += ncl) {
+            const WorkUnit wu = work_unit(u, p);
+            for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
+                if (!warp_wait(&sm.raw_full[rr.s], rr.ph, ab, kStatusWaitFull, lane) ||
+                    !warp_wait_cl(&sm.split_empty[sr.s], sr.ph ^ 1u, ab, kStatusWaitMma)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *sa = sm.raw + rr.s * C::RAW_BYTES;
+                const uint8_t *sb = sa + C::A_BYTES;
+                if (is_a) {
+                    tc::tc_fence_after();
+                    const uint32_t t_hi = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                          C::ACC_COLS + sr.s * C::A_COLS;
+                    tc::convert_a_row<C::A_KIN, C::SPLIT3>(sa, row, t_hi, t_hi + BK);
+                    tc::tmem_wait_st();
+                    tc::tc_fence_before();
+                } else {
+                    uint8_t *st = sm.split + sr.s * C::SPLIT_BYTES;
+                    tc::convert_b_tile<HN, C::B_KIN, C::SPLIT3>(sb, st + C::OFF_BHI,
+                                                                st + C::OFF_BLO, ct);
+                    tc::fence_proxy_async_smem();
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&sm.raw_empty[rr.s]);
+                    arrive_on(&sm.split_full[sr.s], 0);
+                }
+                rr.next();
+                sr.next();
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue (own CTA's rows)
+        const int q = warp & 3;
+        const int row_in_tile = static_cast<int>(rank) * BM + q * 32 + lane;
+        Ring<2> acc;
+        for (long long u = cid; u < p.num_units; u += ncl) {
+            int w = 1;
+            if (lane == 0) w = wait_cl(&sm.acc_full[acc.s], acc.ph, ab, kStatusWaitAcc, true);
+            if (!__shfl_sync(0xffffffffu, w, 0)) break;
+            drain_cl(&sm.acc_full[acc.s], acc.ph, ab.limit);
+            tc::tc_fence_after();
+            const WorkUnit wu = work_unit(u, p);
+            const OutTile o = out_tile<PM, BN>(p, wu);
+            const uint32_t tbase =
+                tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc.s * BN);
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                float v[32];
+                tc::tmem_ld32(tbase + c0, v);
+                tc::store_chunk(o, row_in_tile, c0, v);
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) arrive_on(&sm.acc_empty[acc.s], 0);
+            acc.next();
+        }
+    }
+
+    // ---- teardown: both CTAs done with each other's memory; free TMEM jointly
+    tc::tc_fence_before();
+    __syncwarp();
+    cluster_sync();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tmem_dealloc_pair(tmem, kTmemCols);
+    }
+}
+
+}  // namespace tcp
+}  // namespace sg

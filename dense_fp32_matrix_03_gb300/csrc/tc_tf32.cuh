@@ -1,4 +1,8 @@
-// tc_tf32.cuh -- the tcgen05 tensor-core SGEMM kernel (3xTF32 and TF32).
+// tc_tf32.cuh -- building blocks of the tcgen05 tensor-core SGEMM kernels
+// (3xTF32 and TF32): PTX wrappers (TMEM allocation, MMA, commit, TMEM loads
+// and stores), the TF32 split, the A and B converters and the epilogue
+// store.  The kernels are tc_pair.cuh (TMA-fed, CTA pairs) and
+// tc_direct.cuh (operands TMA cannot describe).
 //
 // C = alpha * op(A) @ op(B) + beta * C with fp32 inputs and output, the
 // contraction on the 5th-generation tensor cores ("Tensor cores" in the
@@ -17,47 +21,26 @@
 // hi_a*hi_b only, with hi rounded to nearest (ties away) for accuracy
 // margin.
 //
-// Data flow per 128 x BN output tile and 32-wide k-block:
-//   TMA                raw fp32 A and B tiles -> shared-memory raw ring
-//                      (operands TMA cannot describe go to tc_direct.cuh)
+// Data flow per output tile and 32-wide k-block (both kernels):
+//   raw fp32 A and B tiles -> shared memory (TMA, or the direct kernel's
+//                      own loads)
 //   A converters       raw A rows -> hi/lo planes in TMEM (tcgen05.st); the
 //                      MMA reads A from TMEM, so A's split planes never
 //                      touch shared memory
 //   B converters       raw B tile -> hi/lo planes in shared memory, K-major
 //                      with the 128-byte swizzle (N-inner tiles transposed)
-//   MMA (one thread)   tcgen05.mma kind::tf32, M=128, N=BN, K=8, A from
-//                      TMEM, B by shared-memory descriptor, into one of two
-//                      TMEM accumulator buffers
+//   MMA (one thread)   tcgen05.mma kind::tf32, K=8, A from TMEM, B by
+//                      shared-memory descriptor, into one of two TMEM
+//                      accumulator buffers
 //   epilogue           tcgen05.ld of the other buffer; C = alpha*acc + beta*C
-// Shared-memory traffic per k-block (3xTF32, BN=128) is thus 32 KB of TMA
-// writes, 32 KB of converter reads, 32 KB of B-plane writes and 48 KB of MMA
-// B reads, instead of 224 KB with both operands' planes in shared memory.
-//
-// Warps: 0 producer, 1 TMEM allocator + MMA issuer, 2-5 A converters (warp
-// w owns TMEM lanes 32*(w%4) .. +31, i.e. those rows of A), 6-9 B
-// converters, 10-13 epilogue (lane quarter w%4).  One CTA per SM, persistent
-// over tiles in grouped order.  Every mbarrier wait is bounded; on a timeout
-// the CTA stops, lets copies and MMAs already issued finish, frees TMEM and
-// exits.
+// Warp roles: 0 producer, 1 TMEM allocator + MMA issuer, 2-5 A converters
+// (warp w owns TMEM lanes 32*(w%4) .. +31, i.e. those rows of A), 6-9 B
+// converters, 10-13 epilogue (lane quarter w%4).
 #pragma once
 
 #include <type_traits>
 
 #include "common.cuh"
-
-// Ring depths (raw fp32 tiles / split stages) per mode and B layout;
-// overridable at build time for tuning sweeps.  Measured on GB300 at 4092^3
-// (3xTF32): B N-inner 3/4 (238.7 TFLOP/s; 3/3 237.9), B K-inner 4/3 (235.6;
-// 3/3 219.9): the K-inner B tiles arrive as 128 short swizzled rows and want
-// one more TMA stage in flight.
-#ifndef SG_TC_RAW3
-#define SG_TC_RAW3 3
-#define SG_TC_SPLIT3 4
-#define SG_TC_RAW3_BK 4
-#define SG_TC_SPLIT3_BK 3
-#define SG_TC_RAW1 4
-#define SG_TC_SPLIT1 4
-#endif
 
 namespace sg {
 namespace tc {
@@ -72,33 +55,6 @@ constexpr int kEpiWarp0 = kBConvWarp0 + kBConvWarps;  // warps 10-13: epilogue
 constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 constexpr int kConvWarps = 4 + kBConvWarps;      // arrivals that complete a stage
 constexpr uint32_t kTmemCols = 512;
-
-template <int BN_, bool SPLIT3_, bool A_KIN_, bool B_KIN_>
-struct Cfg {
-    static constexpr int BN = BN_;
-    static constexpr bool SPLIT3 = SPLIT3_, A_KIN = A_KIN_, B_KIN = B_KIN_;
-    static constexpr int A_BYTES = BM * BK * 4;          // one 128 x 32 fp32 tile
-    static constexpr int B_BYTES = BN * BK * 4;
-    static constexpr int RAW_BYTES = A_BYTES + B_BYTES;
-    static constexpr int PLANES = SPLIT3 ? 2 : 1;        // hi (+ lo)
-    static constexpr int SPLIT_BYTES = PLANES * B_BYTES; // B planes in shared memory
-    static constexpr int RAW_STAGES =
-        SPLIT3 ? (B_KIN ? SG_TC_RAW3_BK : SG_TC_RAW3) : SG_TC_RAW1;
-    static constexpr int SPLIT_STAGES =
-        SPLIT3 ? (B_KIN ? SG_TC_SPLIT3_BK : SG_TC_SPLIT3) : SG_TC_SPLIT1;
-    // TMEM columns: two accumulator buffers of BN fp32 columns, then the A
-    // planes of every split stage (BK columns per plane, one row per lane).
-    static constexpr int ACC_COLS = 2 * BN;
-    static constexpr int A_COLS = PLANES * BK;
-    static constexpr int NBAR = 2 * RAW_STAGES + 2 * SPLIT_STAGES + 4 + 1;
-    static constexpr int SMEM_BYTES =
-        RAW_STAGES * RAW_BYTES + SPLIT_STAGES * SPLIT_BYTES + NBAR * 8 + 16 + 1024;
-    static_assert(BN == 128, "one UMMA N per tile (BN = 128 keeps two accumulators in TMEM)");
-    static_assert(ACC_COLS + SPLIT_STAGES * A_COLS <= static_cast<int>(kTmemCols), "TMEM columns");
-    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
-    // split stage layout (shared memory): B_hi | B_lo
-    static constexpr int OFF_BHI = 0, OFF_BLO = B_BYTES;
-};
 
 // ------------------------------------------------------------ PTX wrappers
 
@@ -316,7 +272,7 @@ __device__ __forceinline__ void convert_b_tile(const uint8_t *raw, uint8_t *hi, 
                                                int ct)
 {
     const uint32_t raw_a = smem_u32(raw), hi_a = smem_u32(hi), lo_a = smem_u32(lo);
-    if (KIN) {
+    if constexpr (KIN) {
         constexpr int CHUNKS = R * BK / 4;  // 16-byte chunks
 #pragma unroll 4
         for (int c = ct; c < CHUNKS; c += kBConvThreads) {
@@ -337,6 +293,38 @@ __device__ __forceinline__ void convert_b_tile(const uint8_t *raw, uint8_t *hi, 
                              "f"(l.x), "f"(l.y), "f"(l.z), "f"(l.w)
                              : "memory");
             }
+        }
+    } else if constexpr (R == 64) {
+        // Half a B tile (the CTA-pair kernel): 16 row blocks x 8 k-blocks of
+        // 4, one per thread.  Within each 8-lane phase the row blocks are 8
+        // consecutive 16-byte pieces (distinct banks) for the loads, and the
+        // k-block rotation by lane/2 puts the stores on 8 distinct chunks.
+        static_assert(kBConvThreads == 128, "one 4 x 4 block per converter thread");
+        const int warp = ct >> 5, lane = ct & 31;
+        const int rb4 = lane & 15;
+        const int kb4 = (2 * warp + (lane >> 4) + (lane >> 1)) & 7;
+        float v[4][4];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t a = raw_a + ((4 * kb4 + kk) * R + 4 * rb4) * 4;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(v[kk][0]), "=f"(v[kk][1]), "=f"(v[kk][2]), "=f"(v[kk][3])
+                         : "r"(a));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = 4 * rb4 + i;
+            const uint32_t off = sw128_offset(r, 4 * kb4);
+            float h[4], l[4];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) split_value<SPLIT3>(v[kk][i], h[kk], l[kk]);
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(hi_a + off), "f"(h[0]),
+                         "f"(h[1]), "f"(h[2]), "f"(h[3])
+                         : "memory");
+            if (SPLIT3)
+                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(lo_a + off),
+                             "f"(l[0]), "f"(l[1]), "f"(l[2]), "f"(l[3])
+                             : "memory");
         }
     } else {
         // raw: element (k, r) at (k*R + r)*4.  out: element (r, k) at sw128_offset(r, k).
@@ -412,243 +400,6 @@ __device__ __forceinline__ void store_chunk(const OutTile &o, int r, int c0, con
                 orow[c] = x;
             }
         }
-    }
-}
-
-// ------------------------------------------------------------ the kernel
-
-template <class C>
-struct Smem {
-    uint8_t *raw;      // RAW_STAGES x (A tile | B tile)
-    uint8_t *split;    // SPLIT_STAGES x (B_hi | B_lo)
-    uint64_t *raw_full, *raw_empty, *split_full, *split_empty, *acc_full, *acc_empty, *mma_done;
-    uint32_t *tmem_base;
-    volatile int *abort_flag;
-};
-
-template <class C>
-__global__ void __launch_bounds__(kThreads, 1)
-    tc_sgemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                    const __grid_constant__ CUtensorMap tmB, const GemmParams p)
-{
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *base = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    Smem<C> sm;
-    sm.raw = base;
-    sm.split = base + C::RAW_STAGES * C::RAW_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm.split + C::SPLIT_STAGES * C::SPLIT_BYTES);
-    sm.raw_full = bars;
-    sm.raw_empty = sm.raw_full + C::RAW_STAGES;
-    sm.split_full = sm.raw_empty + C::RAW_STAGES;
-    sm.split_empty = sm.split_full + C::SPLIT_STAGES;
-    sm.acc_full = sm.split_empty + C::SPLIT_STAGES;
-    sm.acc_empty = sm.acc_full + 2;
-    sm.mma_done = sm.acc_empty + 2;
-    sm.tmem_base = reinterpret_cast<uint32_t *>(sm.mma_done + 1);
-    sm.abort_flag = reinterpret_cast<volatile int *>(sm.tmem_base + 1);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < C::RAW_STAGES; ++s) {
-            mbar_init(&sm.raw_full[s], 1u);
-            mbar_init(&sm.raw_empty[s], kConvWarps);
-        }
-        for (int s = 0; s < C::SPLIT_STAGES; ++s) {
-            mbar_init(&sm.split_full[s], kConvWarps);
-            mbar_init(&sm.split_empty[s], 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&sm.acc_full[b], 1);
-            mbar_init(&sm.acc_empty[b], 4);
-        }
-        mbar_init(sm.mma_done, 1);
-        *sm.abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (warp == 1) {
-        tmem_alloc(sm.tmem_base, kTmemCols);
-        tc_fence_before();
-    }
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *sm.tmem_base;
-    const Abort ab{sm.abort_flag, p.status, p.wait_limit};
-
-    if (warp == 0) {
-        // ------------------------------------------------ producer
-        Ring<C::RAW_STAGES> rr;
-        long long issued = 0;
-        bool ok = true;
-        if (lane == 0) {
-            tma_prefetch_desc(&tmA);
-            tma_prefetch_desc(&tmB);
-        }
-        for (long long u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-            const WorkUnit wu = work_unit(u, p);
-            const TileCoord &tc = wu.tc;
-            const int m0 = tc.tm * BM, n0 = tc.tn * C::BN;
-            for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
-                uint8_t *sa = sm.raw + rr.s * C::RAW_BYTES;
-                uint8_t *sb = sa + C::A_BYTES;
-                const int k0 = kb * BK;
-                if (lane == 0) {
-                    if (!mbar_wait(&sm.raw_empty[rr.s], rr.ph ^ 1u, ab, kStatusWaitEmpty)) {
-                        ok = false;
-                    } else {
-                        const int qa = tc.q * p.a_q_step, qb = tc.q * p.b_q_step;
-                        mbar_arrive_expect_tx(&sm.raw_full[rr.s], C::RAW_BYTES);
-                        if (C::A_KIN) tma_load_3d(sa, &tmA, &sm.raw_full[rr.s], k0, m0, qa);
-                        else          tma_load_3d(sa, &tmA, &sm.raw_full[rr.s], m0, k0, qa);
-                        if (C::B_KIN) tma_load_3d(sb, &tmB, &sm.raw_full[rr.s], k0, n0, qb);
-                        else          tma_load_3d(sb, &tmB, &sm.raw_full[rr.s], n0, k0, qb);
-                    }
-                }
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                if (!ok) break;
-                ++issued;
-                rr.next();
-            }
-        }
-        if (!ok && lane == 0) {
-            // the stages issued last may still be landing
-            Ring<C::RAW_STAGES> d;
-            for (long long j = 0; j < issued; ++j) {
-                if (j + C::RAW_STAGES >= issued) mbar_drain(&sm.raw_full[d.s], d.ph, ab.limit);
-                d.next();
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            Ring<C::SPLIT_STAGES> sr;
-            Ring<2> acc;
-            constexpr uint32_t idesc = idesc_tf32<C::BN>();
-            bool ok = true;
-            bool any = false;
-            for (long long u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-                const WorkUnit wu = work_unit(u, p);
-                if (!mbar_wait(&sm.acc_empty[acc.s], acc.ph ^ 1u, ab, kStatusWaitAcc)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc.s * C::BN);
-                for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
-                    if (!mbar_wait(&sm.split_full[sr.s], sr.ph, ab, kStatusWaitConv)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t st = smem_u32(sm.split + sr.s * C::SPLIT_BYTES);
-                    const uint32_t a_hi = tmem + C::ACC_COLS + sr.s * C::A_COLS;
-                    const uint32_t a_lo = a_hi + BK;
-#pragma unroll
-                    for (int kk = 0; kk < BK / UK; ++kk) {
-                        const uint32_t koff = kk * UK * 4;  // bytes along the 128-byte row
-                        const uint64_t b_hi = kmajor_sw128_desc(st + C::OFF_BHI + koff);
-                        const uint32_t acc_in = (kb > wu.kb_lo || kk > 0) ? 1u : 0u;
-                        if (C::SPLIT3) {
-                            const uint64_t b_lo = kmajor_sw128_desc(st + C::OFF_BLO + koff);
-                            umma_tf32_ts(d_tmem, a_lo + kk * UK, b_hi, idesc, acc_in);
-                            umma_tf32_ts(d_tmem, a_hi + kk * UK, b_lo, idesc, 1u);
-                            umma_tf32_ts(d_tmem, a_hi + kk * UK, b_hi, idesc, 1u);
-                        } else {
-                            umma_tf32_ts(d_tmem, a_hi + kk * UK, b_hi, idesc, acc_in);
-                        }
-                    }
-                    any = true;
-                    umma_commit(&sm.split_empty[sr.s]);  // frees the split stage
-                    sr.next();
-                }
-                if (!ok) break;
-                umma_commit(&sm.acc_full[acc.s]);  // accumulator ready for the epilogue
-                acc.next();
-            }
-            // wait until every MMA issued has completed (TMEM is freed next)
-            if (any) {
-                umma_commit(sm.mma_done);
-                mbar_drain(sm.mma_done, 0, ab.limit);
-            }
-        }
-        __syncwarp();
-    } else if (warp < kEpiWarp0) {
-        // ------------------------------------------------ converters
-        const bool is_a = warp < kBConvWarp0;
-        const int quarter = warp & 3;  // TMEM lanes this warp may access (A converters)
-        const int row = quarter * 32 + lane;
-        const int ct = threadIdx.x - kBConvWarp0 * 32;
-        Ring<C::RAW_STAGES> rr;
-        Ring<C::SPLIT_STAGES> sr;
-        bool ok = true;
-        for (long long u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-            const WorkUnit wu = work_unit(u, p);
-            for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
-                if (!warp_wait(&sm.raw_full[rr.s], rr.ph, ab, kStatusWaitFull, lane) ||
-                    !warp_wait(&sm.split_empty[sr.s], sr.ph ^ 1u, ab, kStatusWaitMma, lane)) {
-                    ok = false;
-                    break;
-                }
-                const uint8_t *sa = sm.raw + rr.s * C::RAW_BYTES;
-                const uint8_t *sb = sa + C::A_BYTES;
-                if (is_a) {
-                    tc_fence_after();  // the MMA that read this TMEM stage has completed
-                    const uint32_t t_hi = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                          C::ACC_COLS + sr.s * C::A_COLS;
-                    convert_a_row<C::A_KIN, C::SPLIT3>(sa, row, t_hi, t_hi + BK);
-                    tmem_wait_st();
-                    tc_fence_before();  // our TMEM stores -> visible to the MMA
-                } else {
-                    uint8_t *st = sm.split + sr.s * C::SPLIT_BYTES;
-                    convert_b_tile<C::BN, C::B_KIN, C::SPLIT3>(sb, st + C::OFF_BHI,
-                                                               st + C::OFF_BLO, ct);
-                    fence_proxy_async_smem();  // our stores -> visible to the tensor core
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&sm.raw_empty[rr.s]);
-                    mbar_arrive(&sm.split_full[sr.s]);
-                }
-                rr.next();
-                sr.next();
-            }
-        }
-    } else {
-        // ------------------------------------------------ epilogue
-        const int q = warp & 3;            // TMEM lane quarter this warp may access
-        const int row_in_tile = q * 32 + lane;
-        Ring<2> acc;
-        for (long long u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-            int w = 1;
-            if (lane == 0) w = mbar_wait(&sm.acc_full[acc.s], acc.ph, ab, kStatusWaitAcc, true);
-            if (!__shfl_sync(0xffffffffu, w, 0)) break;
-            mbar_drain(&sm.acc_full[acc.s], acc.ph, ab.limit);
-            tc_fence_after();
-            const WorkUnit wu = work_unit(u, p);
-            // C, or this slice's workspace slot (unscaled) when the tile is split
-            const OutTile o = out_tile<BM, C::BN>(p, wu);
-            const uint32_t tbase =
-                tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc.s * C::BN);
-#pragma unroll 1
-            for (int c0 = 0; c0 < C::BN; c0 += 32) {
-                float v[32];
-                tmem_ld32(tbase + c0, v);  // all lanes take part, rows in range or not
-                store_chunk(o, row_in_tile, c0, v);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.acc_empty[acc.s]);
-            acc.next();
-        }
-    }
-
-    // ---- teardown: every role is done; free TMEM
-    tc_fence_before();
-    __syncwarp();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
     }
 }
 

@@ -88,9 +88,11 @@ int sgemm_batched_ex(int mode, int M, int N, int K, float alpha, const float *A,
                      int transB, long long strideA, long long strideB, long long strideC, int Q,
                      void *stream);
 
-/* Split-K workspace.  The output is cut into 128 x 128 tiles, one persistent
- * CTA per multiprocessor.  When the tiles do not fill a whole number of waves
- * (4092^3: 1024 tiles = 6.7 waves on 152 multiprocessors), or fill less than
+/* Split-K workspace.  The output is cut into tiles (256 x 128 on the FP32
+ * path and on the tensor-core paths with TMA-describable operands, 128 x 128
+ * otherwise), each computed by one persistent CTA per multiprocessor or, on
+ * the tensor cores, one CTA pair per two.  When the tiles do not fill a
+ * whole number of waves (4092^3: 512 tiles = 6.7 waves on 76 pairs), or fill less than
  * one (small or skinny products such as the ragged 1000 x 1500 x 777 case),
  * the library can cut the tiles of the last, partial wave along K into
  * slices computed in parallel -- the split-K scheme the SGEMM worklog sees

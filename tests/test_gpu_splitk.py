@@ -103,35 +103,44 @@ def test_small_or_missing_workspace_runs_unsplit(oracle_mod, mode):
         assert oracle_mod.max_rel_err(C, Cref, D) <= TOL[mode]
 
 
-def planned_workspace(mode, M, N, K, Q, sms):
+def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
     """The split plan as the library's header and planner describe it, for
-    every output tile shape the mode may use (FP32: 256 x 128 where the FMAs
-    pair, 128 x 128 with both operands K-inner; tensor cores: 128 x 128):
-    whole waves of tiles, then the last wave's r tiles cut into s slices
-    (s <= 16, each >= 64 deep for FP32 and >= 256 for the tensor paths), s
-    minimising t_tile * (floor(T/G) + ceil(r*s/G)/s) + 3 us + 2 * ws / bw
-    (bw 8 TB/s up to 64 MB of workspace, else 3 TB/s; t_tile from the path's
-    per-multiprocessor rate with TMA-fed or cp.async-fed operands), used only
-    if it saves 1%; returns the largest workspace over the shapes and feeds
-    (one BM x BN fp32 slot per split unit), 0 when none splits; on the FP32
-    path plus room for transposed copies of A and B (256-byte rounded)."""
-    shapes = [(256, 128), (128, 128)] if mode == "fp32" else [(128, 128)]
+    every kernel the mode may run (FP32: 256 x 128 tiles where the FMAs pair,
+    128 x 128 with both operands K-inner, each TMA- or cp.async-fed, one unit
+    per multiprocessor; tensor cores: the direct kernel's 128 x 128 tiles on
+    every multiprocessor and the pair kernel's 256 x 128 tiles, one unit per
+    CTA pair): whole waves of units, then the last wave's r tiles cut into s
+    slices (s <= 16, each >= 64 deep for FP32 and >= 256 for the tensor
+    paths), s minimising t_tile * (floor(T/G) + ceil(r*s/G)/s) + 3 us +
+    2 * ws / bw (G units at once; bw 8 TB/s up to 64 MB of workspace, else
+    3 TB/s; t_tile from the kernel's per-multiprocessor rate times its
+    multiprocessors per unit), used only if it saves 1%; returns the largest
+    workspace over the kernels (one BM x BN fp32 slot per split unit), 0 when
+    none splits; on the FP32 path plus room for transposed copies of A and B
+    (256-byte rounded)."""
+    rates = {("fp32", "direct"): 0.24e12, ("fp32", "tma"): 0.40e12,
+             ("3xtf32", "direct"): 0.47e12, ("3xtf32", "pair"): 1.6e12,
+             ("tf32", "direct"): 0.55e12, ("tf32", "pair"): 2.5e12}
+    if pair_slots is None:
+        pair_slots = sms // 2
+    if mode == "fp32":
+        kernels = [(bm, bn, feed, sms, 1) for (bm, bn) in ((256, 128), (128, 128))
+                   for feed in ("direct", "tma")]
+    else:
+        kernels = [(128, 128, "direct", sms, 1), (256, 128, "pair", pair_slots, 2)]
     need = 0
-    for (bm, bn), tma in [(sh, t) for sh in shapes for t in (False, True)]:
-        rate = {("fp32", True): 0.40e12, ("3xtf32", True): 1.54e12, ("tf32", True): 2.16e12,
-                ("fp32", False): 0.24e12, ("3xtf32", False): 0.47e12,
-                ("tf32", False): 0.55e12}[(mode, tma)]
+    for bm, bn, feed, G, per_unit in kernels:
         T = Q * math.ceil(M / bm) * math.ceil(N / bn)
-        full, rem = divmod(T, sms)
+        full, rem = divmod(T, G)
         if rem == 0:
             continue
         smax = min(16, K // (64 if mode == "fp32" else 256))
-        t_tile = 2.0 * bm * bn * float(K) / rate
+        t_tile = 2.0 * bm * bn * float(K) / (rates[(mode, feed)] * per_unit)
         t_whole = t_tile * float(full + 1)
         best_t, best, best_ws = t_whole, 1, 0
         for s in range(2, smax + 1):
             ws = rem * s * bm * bn * 4
-            waves = (rem * s + sms - 1) // sms
+            waves = (rem * s + G - 1) // G
             bw = 8e12 if ws <= (64 << 20) else 3e12
             t = t_tile * (float(full) + float(waves) / s) + 3e-6 + 2.0 * float(ws) / bw
             if t < best_t:
