@@ -237,8 +237,8 @@ int min_slice_k(int mode) { return mode == SGEMM_MODE_FP32 ? 64 : 256; }
 double path_rate_per_sm(int mode, int feed)
 {
     if (mode == SGEMM_MODE_FP32) return feed == kFeedDirect ? 0.24e12 : 0.40e12;
-    if (mode == SGEMM_MODE_3XTF32) return feed == kFeedDirect ? 0.47e12 : 1.6e12;
-    return feed == kFeedDirect ? 0.55e12 : 2.5e12;
+    if (mode == SGEMM_MODE_3XTF32) return feed == kFeedDirect ? 0.47e12 : 1.8e12;
+    return feed == kFeedDirect ? 0.55e12 : 3.0e12;
 }
 
 size_t splitk_workspace_bytes(long long split_tiles, int splits, int bm, int bn)

@@ -37,8 +37,8 @@ struct Plan {
 //       + (s > 1: 3 us + 2 * workspace bytes / (8 TB/s if they stay in L2,
 //                                                 i.e. <= 64 MB, else 3 TB/s))
 // with t_tile = 2 * BM * BN * K / (multiprocessors per unit x the kernel's
-// per-multiprocessor rate, as measured on GB300: 0.40 TFLOP/s FP32, 1.6
-// 3xTF32, 2.5 TF32 with TMA-fed operands; 0.24, 0.47, 0.55 for operands TMA
+// per-multiprocessor rate, as measured on GB300: 0.40 TFLOP/s FP32, 1.8
+// 3xTF32, 3.0 TF32 with TMA-fed operands; 0.24, 0.47, 0.55 for operands TMA
 // cannot describe).  s runs over
 // 1 .. min(16, K / min_slice_k(mode)); the best s is used only when it
 // saves at least 1%.  Each slice is at least

@@ -71,6 +71,7 @@ int launch_tc(Plan &plan)
     if (plan.a_tma && plan.b_tma &&
         encode_operand(&tmA, p.A, !plan.transA, p.M, p.K, p.lda, p.Q, p.sA, tcp::BM) &&
         encode_operand(&tmB, p.B, plan.transB, p.N, p.K, p.ldb, p.Q, p.sB, tcp::HN)) {
+        p.k_blocks = (p.K + tcp::STAGE_K - 1) / tcp::STAGE_K;  // the pair kernel's stages
         p.tiles_m = (p.M + tcp::PM - 1) / tcp::PM;
         p.tiles_n = (p.N + tcp::BN - 1) / tcp::BN;
         p.num_tiles = static_cast<long long>(p.Q) * p.tiles_m * p.tiles_n;

@@ -12,11 +12,12 @@
 //     barriers of both CTAs (multicast), and both CTAs' converters and
 //     epilogue warps arrive on the even CTA's barriers (remote arrives).
 // Per CTA and 32-wide k-block that halves the B work: 24 KB of TMA writes
-// (A 16 + B 8), 24 KB of converter reads, 16 KB of B-plane writes and 24 KB
-// of MMA B reads = 88 KB of shared-memory traffic, against 144 KB in the
-// single-CTA kernel, whose MMAs wait on shared-memory bandwidth (measured:
-// the 128 x 128 kernel's tensor pipe completes an MMA every ~105 cycles,
-// against ~69 cycles with its operands already resident).
+// (A 16 + B 8), 24 KB of converter reads and 16 KB of B-plane writes,
+// against 32 + 32 + 32 KB for a 128 x 128 tile on one CTA (each CTA's
+// tensor core still reads the whole B tile, half of it from the other CTA),
+// and 25% less L2 -> shared-memory traffic per flop.  Measured on GB300 at
+// 4092^3 against the single-CTA 128 x 128 kernel it replaces: 3xTF32
+// 238.7 -> 276 TFLOP/s, TF32 316.6 -> 464.
 //
 // Warps and barriers as in tc_tf32.cuh.  Barriers that both CTAs arrive on
 // live in the even CTA (split_full: 16 converter warps; acc_empty: 8
@@ -28,13 +29,28 @@
 
 #include "tc_tf32.cuh"
 
-// Ring depths (raw fp32 tiles / split stages); TMEM holds at most 4 split
-// stages of 3xTF32 A planes and 8 of TF32 beside the two accumulators.
+// A pipeline stage covers SG_TCP_KSUB k-blocks of 32 (one 128-byte swizzle
+// row of fp32 each): the MMA thread's per-stage work (wait, fence, commit)
+// leaves the tensor pipe idle for a few hundred cycles whatever the stage's
+// size, since its queue holds little more than the MMA in flight, so longer
+// stages waste less.  Ring depths (raw fp32 tiles / split stages): TMEM
+// holds (512 - 256) / (32 * KSUB * planes) split stages of A planes beside
+// the two accumulators.
+#ifndef SG_TCP_KSUB
+#define SG_TCP_KSUB 2
+#endif
 #ifndef SG_TCP_RAW3
+#if SG_TCP_KSUB == 2
+#define SG_TCP_RAW3 3
+#define SG_TCP_SPLIT3 2
+#define SG_TCP_RAW1 3
+#define SG_TCP_SPLIT1 4
+#else
 #define SG_TCP_RAW3 6
 #define SG_TCP_SPLIT3 4
 #define SG_TCP_RAW1 6
 #define SG_TCP_SPLIT1 8
+#endif
 #endif
 
 namespace sg {
@@ -55,25 +71,32 @@ constexpr int BM = 128;      // rows of C per CTA
 constexpr int PM = 2 * BM;   // rows per pair tile (the MMA's M)
 constexpr int BN = 128;      // columns per pair tile (the MMA's N)
 constexpr int HN = BN / 2;   // rows of B^T each CTA holds
+constexpr int KSUB = SG_TCP_KSUB;  // 32-wide k sub-blocks per stage
+constexpr int STAGE_K = KSUB * BK;
 
 template <bool SPLIT3_, bool A_KIN_, bool B_KIN_>
 struct Cfg {
     static constexpr bool SPLIT3 = SPLIT3_, A_KIN = A_KIN_, B_KIN = B_KIN_;
-    static constexpr int A_BYTES = BM * BK * 4;
-    static constexpr int B_BYTES = HN * BK * 4;
+    static constexpr int SUB_A = BM * BK * 4;   // raw A of one 32-wide sub-block
+    static constexpr int SUB_B = HN * BK * 4;   // raw B of one sub-block
+    static constexpr int A_BYTES = KSUB * SUB_A;
+    static constexpr int B_BYTES = KSUB * SUB_B;
     static constexpr int RAW_BYTES = A_BYTES + B_BYTES;
     static constexpr int PLANES = SPLIT3 ? 2 : 1;
-    static constexpr int SPLIT_BYTES = PLANES * B_BYTES;
+    static constexpr int SUB_SPLIT = PLANES * SUB_B;  // B planes of one sub-block
+    static constexpr int SPLIT_BYTES = KSUB * SUB_SPLIT;
     static constexpr int RAW_STAGES = SPLIT3 ? SG_TCP_RAW3 : SG_TCP_RAW1;
     static constexpr int SPLIT_STAGES = SPLIT3 ? SG_TCP_SPLIT3 : SG_TCP_SPLIT1;
     static constexpr int ACC_COLS = 2 * BN;
-    static constexpr int A_COLS = PLANES * BK;
+    static constexpr int SUB_COLS = PLANES * BK;      // TMEM A columns of one sub-block
+    static constexpr int A_COLS = KSUB * SUB_COLS;
     static constexpr int NBAR = 2 * RAW_STAGES + 2 * SPLIT_STAGES + 4 + 1;
     static constexpr int SMEM_BYTES =
         RAW_STAGES * RAW_BYTES + SPLIT_STAGES * SPLIT_BYTES + NBAR * 8 + 16 + 1024;
     static_assert(ACC_COLS + SPLIT_STAGES * A_COLS <= static_cast<int>(kTmemCols), "TMEM columns");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
-    static constexpr int OFF_BHI = 0, OFF_BLO = B_BYTES;
+    // a sub-block's split planes: B_hi | B_lo
+    static constexpr int OFF_BHI = 0, OFF_BLO = SUB_B;
 };
 
 // Instruction descriptor: kind::tf32, fp32 accumulate, both operands
@@ -349,17 +372,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
                 uint8_t *sa = sm.raw + rr.s * C::RAW_BYTES;
                 uint8_t *sb = sa + C::A_BYTES;
-                const int k0 = kb * BK;
                 if (lane == 0) {
                     if (!mbar_wait(&sm.raw_empty[rr.s], rr.ph ^ 1u, ab, kStatusWaitEmpty)) {
                         ok = false;
                     } else {
                         const int qa = tc.q * p.a_q_step, qb = tc.q * p.b_q_step;
                         mbar_arrive_expect_tx(&sm.raw_full[rr.s], C::RAW_BYTES);
-                        if (C::A_KIN) tma_load_3d(sa, &tmA, &sm.raw_full[rr.s], k0, m0, qa);
-                        else          tma_load_3d(sa, &tmA, &sm.raw_full[rr.s], m0, k0, qa);
-                        if (C::B_KIN) tma_load_3d(sb, &tmB, &sm.raw_full[rr.s], k0, n0, qb);
-                        else          tma_load_3d(sb, &tmB, &sm.raw_full[rr.s], n0, k0, qb);
+#pragma unroll
+                        for (int j = 0; j < KSUB; ++j) {
+                            const int k0 = kb * STAGE_K + j * BK;
+                            uint8_t *ja = sa + j * C::SUB_A;
+                            uint8_t *jb = sb + j * C::SUB_B;
+                            if (C::A_KIN) tma_load_3d(ja, &tmA, &sm.raw_full[rr.s], k0, m0, qa);
+                            else          tma_load_3d(ja, &tmA, &sm.raw_full[rr.s], m0, k0, qa);
+                            if (C::B_KIN) tma_load_3d(jb, &tmB, &sm.raw_full[rr.s], k0, n0, qb);
+                            else          tma_load_3d(jb, &tmB, &sm.raw_full[rr.s], n0, k0, qb);
+                        }
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -401,15 +429,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc::tc_fence_after();
-                    const uint64_t b_hi =
+                    const uint64_t b_st =
                         bdesc0 + static_cast<uint64_t>(sr.s * (C::SPLIT_BYTES >> 4));
-                    const uint64_t b_lo = b_hi + (C::OFF_BLO >> 4);
-                    const uint32_t a_hi = tmem + C::ACC_COLS + sr.s * C::A_COLS;
+                    const uint32_t a_st = tmem + C::ACC_COLS + sr.s * C::A_COLS;
                     Ring<C::SPLIT_STAGES> nx = sr;
                     nx.next();
-                    ready = issue_stage<C::SPLIT3>(d_tmem, a_hi, a_hi + BK, b_hi, b_lo,
-                                                   kb > wu.kb_lo ? 1u : 0u,
-                                                   smem_u32(&sm.split_full[nx.s]), nx.ph);
+#pragma unroll
+                    for (int j = 0; j < KSUB; ++j) {
+                        const uint64_t b_hi = b_st + static_cast<uint64_t>(j * (C::SUB_SPLIT >> 4));
+                        const uint32_t a_hi = a_st + j * C::SUB_COLS;
+                        ready = issue_stage<C::SPLIT3>(
+                            d_tmem, a_hi, a_hi + BK, b_hi, b_hi + (C::OFF_BLO >> 4),
+                            (kb > wu.kb_lo || j > 0) ? 1u : 0u, smem_u32(&sm.split_full[nx.s]),
+                            nx.ph);
+                    }
                     if (kb + 1 == wu.kb_hi) ready = 0;  // the next unit waits afresh
                     any = true;
                     umma_commit_both(&sm.split_empty[sr.s]);
@@ -446,15 +479,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint8_t *sb = sa + C::A_BYTES;
                 if (is_a) {
                     tc::tc_fence_after();
-                    const uint32_t t_hi = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                    const uint32_t t_st = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                                           C::ACC_COLS + sr.s * C::A_COLS;
-                    tc::convert_a_row<C::A_KIN, C::SPLIT3>(sa, row, t_hi, t_hi + BK);
+#pragma unroll 1
+                    for (int j = 0; j < KSUB; ++j) {
+                        const uint32_t t_hi = t_st + j * C::SUB_COLS;
+                        tc::convert_a_row<C::A_KIN, C::SPLIT3>(sa + j * C::SUB_A, row, t_hi,
+                                                               t_hi + BK);
+                    }
                     tc::tmem_wait_st();
                     tc::tc_fence_before();
                 } else {
                     uint8_t *st = sm.split + sr.s * C::SPLIT_BYTES;
-                    tc::convert_b_tile<HN, C::B_KIN, C::SPLIT3>(sb, st + C::OFF_BHI,
-                                                                st + C::OFF_BLO, ct);
+#pragma unroll 1
+                    for (int j = 0; j < KSUB; ++j) {
+                        uint8_t *jt = st + j * C::SUB_SPLIT;
+                        tc::convert_b_tile<HN, C::B_KIN, C::SPLIT3>(sb + j * C::SUB_B,
+                                                                    jt + C::OFF_BHI,
+                                                                    jt + C::OFF_BLO, ct);
+                    }
                     tc::fence_proxy_async_smem();
                 }
                 __syncwarp();

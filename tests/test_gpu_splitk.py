@@ -119,8 +119,8 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
     none splits; on the FP32 path plus room for transposed copies of A and B
     (256-byte rounded)."""
     rates = {("fp32", "direct"): 0.24e12, ("fp32", "tma"): 0.40e12,
-             ("3xtf32", "direct"): 0.47e12, ("3xtf32", "pair"): 1.6e12,
-             ("tf32", "direct"): 0.55e12, ("tf32", "pair"): 2.5e12}
+             ("3xtf32", "direct"): 0.47e12, ("3xtf32", "pair"): 1.8e12,
+             ("tf32", "direct"): 0.55e12, ("tf32", "pair"): 3.0e12}
     if pair_slots is None:
         pair_slots = sms // 2
     if mode == "fp32":
