@@ -547,6 +547,41 @@ def workspace(lib, mode, M, N, K, Q, dev):
     return ws_bytes, torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
 
 
+def half_figures(lib, dev, stream, flush, peaks, peak_src):
+    """The 16-bit-input path (bf16 / fp16 A and B, fp32 C) at 4092^3 and
+    8192^3, A times B-transpose (read directly) and A times B (B copied
+    transposed into the workspace first), against the measured bf16 peak."""
+    import torch
+    out = {}
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    for n in (4092, 8192):
+        g = torch.Generator(device=dev).manual_seed(5)
+        A = torch.randn(n, n, device=dev, generator=g).to(torch.bfloat16)
+        Bt = torch.randn(n, n, device=dev, generator=g).to(torch.bfloat16)
+        C = torch.zeros(n, n, device=dev)
+        for type_ in ("bf16", "fp16"):
+            if type_ == "fp16":
+                A, Bt = A.to(torch.float16), Bt.to(torch.float16)
+            for tB in (1, 0):
+                if n == 8192 and (type_ == "fp16" or tB == 0):
+                    continue
+                Bd = Bt if tB else Bt.t().contiguous()
+                wsb = lib.sgemm_half_workspace_size(type_, n, n, n, 0, tB, n, n, 1)
+                ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+
+                def call(type_=type_, tB=tB, Bd=Bd, ws=ws, wsb=wsb):
+                    lib.check(lib.sgemm_half_batched(type_, n, n, n, 1.0, A, n, Bd, n, 0.0, C, n, 0,
+                                                     tB, 0, 0, 0, 1, ws, wsb, stream))
+                t = statistics.median(time_calls(call, 10, 3, stream, flush))
+                tf = gemm_flops(n, n, n) / (t / 1e3) / 1e12
+                out[f"{type_}_{'a_bt' if tB else 'a_b'}_{n}"] = {
+                    "tflops": tf, "ms": t, "peak": peak, "frac": tf / peak,
+                    "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)"}
+        del A, Bt, C
+    lib.check(lib.sgemm_poll_error(stream))
+    return out
+
+
 def extra_figures(lib, default_mode, dev, stream, flush, num_sms, peaks, peak_src):
     """Per-path figures at 4092^3 and batched-GEMM figures (fewer steps)."""
     import torch
@@ -575,6 +610,7 @@ def extra_figures(lib, default_mode, dev, stream, flush, num_sms, peaks, peak_sr
         out["paths"][mode] = {"tflops": tf, "ms": t, "bound": bound, "peak": peak,
                               "frac": tf / peak}
     del A, B, C
+    out["half"] = half_figures(lib, dev, stream, flush, peaks, peak_src)
     wb = workloads.make("bmm_q32_1024x1024x512")
     Q, M, N, K = wb["Q"], wb["M"], wb["N"], wb["K"]
     A = torch.from_numpy(wb["A"]).to(dev)

@@ -34,6 +34,10 @@ SGEMM_PROBE_BF16_SS = 4
 PROBES = {"ffma": SGEMM_PROBE_FFMA, "ffma2": SGEMM_PROBE_FFMA2, "tf32_ss": SGEMM_PROBE_TF32_SS,
           "tf32_ts": SGEMM_PROBE_TF32_TS, "bf16_ss": SGEMM_PROBE_BF16_SS}
 
+SGEMM_HALF_BF16 = 0
+SGEMM_HALF_FP16 = 1
+HALF_TYPES = {"bf16": SGEMM_HALF_BF16, "fp16": SGEMM_HALF_FP16}
+
 SGEMM_MODE_DEFAULT = -1
 SGEMM_MODE_FP32 = 0
 SGEMM_MODE_3XTF32 = 1
@@ -53,6 +57,9 @@ SIGNATURES = {
                                  _ll, _i, _p, ctypes.c_size_t, _p]),
     "sgemm_batched_ex_noalloc": (_i, [_i, _i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _i, _i, _ll,
                                       _ll, _ll, _i, _p]),
+    "sgemm_half_workspace_size": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i, _i, _i, _i]),
+    "sgemm_half_batched": (_i, [_i, _i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _i, _i, _ll, _ll,
+                                _ll, _i, _p, ctypes.c_size_t, _p]),
     "sgemm_host_buffer_size": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i, _i]),
     "sgemm_host": (_i, [_i, _i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _i, _i, _i, _p,
                         ctypes.c_size_t, _p]),
@@ -178,6 +185,26 @@ def sgemm_batched_ex_noalloc(mode, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
     return _lib.sgemm_batched_ex_noalloc(mode, M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta,
                                          _ptr(C), ldc, int(transA), int(transB), strideA, strideB,
                                          strideC, Q, _stream(stream))
+
+
+def sgemm_half_workspace_size(type_, M, N, K, transA, transB, lda, ldb, Q=1) -> int:
+    if isinstance(type_, str):
+        type_ = HALF_TYPES[type_]
+    return int(_lib.sgemm_half_workspace_size(type_, M, N, K, int(transA), int(transB), lda, ldb,
+                                              Q))
+
+
+def sgemm_half_batched(type_, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, transA, transB,
+                       strideA, strideB, strideC, Q, workspace, workspace_bytes,
+                       stream=None) -> int:
+    """A, B: device buffers of 16-bit values (torch bfloat16 / float16 tensors
+    or raw addresses); C fp32 (see include/sgemm.h)."""
+    if isinstance(type_, str):
+        type_ = HALF_TYPES[type_]
+    return _lib.sgemm_half_batched(type_, M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta,
+                                   _ptr(C), ldc, int(transA), int(transB), strideA, strideB,
+                                   strideC, Q, _ptr(workspace), int(workspace_bytes),
+                                   _stream(stream))
 
 
 def sgemm_host_buffer_size(mode, M, N, K, transA=0, transB=0, panel_rows=0) -> int:

@@ -23,9 +23,6 @@ __device__ unsigned int g_status_word;
 namespace {
 
 constexpr int kMaxDevices = 64;
-// A wait may spin for this many SM clock cycles (about a second at the
-// GB300's clocks) before the kernel gives up and reports SGEMM_ERR_TIMEOUT.
-constexpr long long kWaitLimitCycles = 1LL << 31;
 
 struct DeviceInfo {
     bool ready = false;
@@ -74,7 +71,6 @@ bool get_encoder()
     return true;
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Scales C by beta (or zeroes it when beta == 0): the whole result when
 // alpha == 0 or K == 0.  One thread per element, grid-stride.
@@ -159,13 +155,14 @@ __global__ void wait_timeout_kernel(unsigned int *status, long long limit)
     mbar_arrive(&bar);
 }
 
-int check_args(int mode, int M, int N, int K, float alpha, const float *A, int lda,
-               const float *B, int ldb, float beta, float *C, int ldc, int transA, int transB,
-               long long sA, long long sB, long long sC, int Q)
+}  // namespace
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int M, int N, int K, float alpha, const void *A, int lda, const void *B, int ldb,
+                const float *C, int ldc, int transA, int transB, long long sA, long long sB,
+                long long sC, int Q)
 {
-    (void)beta;
-    if (mode != SGEMM_MODE_FP32 && mode != SGEMM_MODE_3XTF32 && mode != SGEMM_MODE_TF32)
-        return SGEMM_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0 || Q < 0) return SGEMM_ERR_INVALID_ARG;
     if (sA < 0 || sB < 0 || sC < 0) return SGEMM_ERR_INVALID_ARG;
     const long long a_row = transA ? M : K, b_row = transB ? K : N;
@@ -177,6 +174,18 @@ int check_args(int mode, int M, int N, int K, float alpha, const float *A, int l
     const bool reads_ab = (K > 0 && alpha != 0.f);
     if (reads_ab && (A == nullptr || B == nullptr)) return SGEMM_ERR_INVALID_ARG;
     return SGEMM_OK;
+}
+
+namespace {
+
+int check_args(int mode, int M, int N, int K, float alpha, const float *A, int lda,
+               const float *B, int ldb, float beta, float *C, int ldc, int transA, int transB,
+               long long sA, long long sB, long long sC, int Q)
+{
+    (void)beta;
+    if (mode != SGEMM_MODE_FP32 && mode != SGEMM_MODE_3XTF32 && mode != SGEMM_MODE_TF32)
+        return SGEMM_ERR_INVALID_ARG;
+    return check_shape(M, N, K, alpha, A, lda, B, ldb, C, ldc, transA, transB, sA, sB, sC, Q);
 }
 
 }  // namespace
@@ -227,6 +236,25 @@ bool encode_operand(CUtensorMap *map, const float *base, bool kin, long long row
     return r == CUDA_SUCCESS;
 }
 
+bool encode_operand16(CUtensorMap *map, const void *base, bool bf16, long long rows, long long K,
+                      long long ld, int Q, long long stride, int box_rows)
+{
+    if (!get_encoder()) return false;
+    const bool batched = Q > 1 && stride != 0;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows),
+                          batched ? static_cast<cuuint64_t>(Q) : 1};
+    cuuint64_t strides[2];
+    strides[0] = static_cast<cuuint64_t>(ld) * 2;
+    strides[1] = batched ? static_cast<cuuint64_t>(stride) * 2 : strides[0] * dims[1];
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1}, estr[3] = {1, 1, 1};
+    const CUresult r =
+        g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                 const_cast<void *>(base), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int min_slice_k(int mode) { return mode == SGEMM_MODE_FP32 ? 64 : 256; }
 
 // FLOP/s per multiprocessor each kernel sustains on GB300 (measured at
@@ -238,6 +266,7 @@ double path_rate_per_sm(int mode, int feed)
 {
     if (mode == SGEMM_MODE_FP32) return feed == kFeedDirect ? 0.24e12 : 0.40e12;
     if (mode == SGEMM_MODE_3XTF32) return feed == kFeedDirect ? 0.47e12 : 1.8e12;
+    if (mode == kModeHalf) return 11.0e12;
     return feed == kFeedDirect ? 0.55e12 : 3.0e12;
 }
 

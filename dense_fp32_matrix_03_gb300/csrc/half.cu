@@ -1,0 +1,205 @@
+// half.cu -- host side of the 16-bit-input path (bf16 / fp16 operands, fp32
+// accumulation and output): argument checks, copies of operands the kernel
+// cannot read directly, the split plan and the launch of tc_half.cuh.
+#include <atomic>
+#include <cstring>
+
+#include "../../include/sgemm.h"
+#include "internal.h"
+#include "tc_half.cuh"
+
+namespace sg {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kGroupM = 8;
+std::atomic<int> g_half_slots[kMaxDevices];
+
+long long round8(long long x) { return (x + 7) / 8 * 8; }
+size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+// The kernel reads an operand directly when it is K-inner, 16-byte aligned,
+// and its row pitch and batch stride are multiples of 8 values (16 bytes).
+bool direct(const void *p, bool k_inner, long long ld, int Q, long long stride)
+{
+    return k_inner && aligned16(p) && ld % 8 == 0 && (Q <= 1 || stride == 0 || stride % 8 == 0);
+}
+
+// Bytes of a K-inner copy of an operand with `rows` rows: round_up(K, 8)
+// values per row, per batch entry (one entry when broadcast).
+size_t copy_bytes(long long rows, long long K, int Q, bool broadcast)
+{
+    return round256(static_cast<size_t>(broadcast ? 1 : Q) * static_cast<size_t>(rows) *
+                    static_cast<size_t>(round8(K)) * 2);
+}
+
+int half_slots(int num_sms)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return num_sms / 2;
+    const int cached = g_half_slots[dev].load();
+    if (cached > 0) return cached;
+    auto kern = tch::tch_gemm_kernel<true>;
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tch::SMEM_BYTES) == cudaSuccess) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(2 * (num_sms / 2)));
+        cfg.blockDim = dim3(tch::kThreads);
+        cfg.dynamicSmemBytes = tch::SMEM_BYTES;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    if (n <= 0 || n > num_sms / 2) n = num_sms / 2;
+    if (n < 1) n = 1;
+    g_half_slots[dev].store(n);
+    return n;
+}
+
+template <bool BF16>
+int launch_half(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB, int slots)
+{
+    auto kern = tch::tch_gemm_kernel<BF16>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tch::SMEM_BYTES) != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
+    long long pairs = plan.p.num_units;
+    if (pairs > slots) pairs = slots;
+    kern<<<static_cast<unsigned>(2 * pairs), tch::kThreads, tch::SMEM_BYTES, plan.stream>>>(
+        tmA, tmB, plan.p);
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    note_launch();
+    return plan.p.splits > 1 ? launch_fixup(plan, tch::PM, tch::BN) : SGEMM_OK;
+}
+
+bool valid_type(int type) { return type == SGEMM_HALF_BF16 || type == SGEMM_HALF_FP16; }
+
+}  // namespace
+
+}  // namespace sg
+
+using namespace sg;
+
+extern "C" {
+
+size_t sgemm_half_workspace_size(int type, int M, int N, int K, int transA, int transB, int lda,
+                                 int ldb, int Q)
+{
+    if (!valid_type(type) || M <= 0 || N <= 0 || K <= 0 || Q <= 0) return 0;
+    int num_sms = 0;
+    unsigned int *status = nullptr;
+    if (!current_sm103(&num_sms, &status)) return 0;
+    size_t bytes = 0;
+    if (transA || lda % 8 != 0) bytes += copy_bytes(M, K, Q, false);
+    if (!transB || ldb % 8 != 0) bytes += copy_bytes(N, K, Q, false);
+    const long long tiles = static_cast<long long>(Q) * ((M + tch::PM - 1) / tch::PM) *
+                            ((N + tch::BN - 1) / tch::BN);
+    const SplitPlan sp = choose_plan(tiles, K, half_slots(num_sms), kModeHalf, tch::PM, tch::BN,
+                                     kFeedPair, ~static_cast<size_t>(0));
+    return bytes + sp.ws_bytes;
+}
+
+int sgemm_half_batched(int type, int M, int N, int K, float alpha, const void *A, int lda,
+                       const void *B, int ldb, float beta, float *C, int ldc, int transA,
+                       int transB, long long strideA, long long strideB, long long strideC, int Q,
+                       void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!valid_type(type)) return SGEMM_ERR_INVALID_ARG;
+    if (workspace_bytes > 0 &&
+        (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return SGEMM_ERR_INVALID_ARG;
+    int rc = check_shape(M, N, K, alpha, A, lda, B, ldb, C, ldc, transA, transB, strideA,
+                         strideB, strideC, Q);
+    if (rc != SGEMM_OK || M == 0 || N == 0 || Q == 0) return rc;
+    if (K == 0 || alpha == 0.f)  // C = beta * C; A and B are not read
+        return sgemm_batched_ex(SGEMM_MODE_3XTF32, M, N, 0, 0.f, nullptr, 1, nullptr, N, beta, C,
+                                ldc, 0, 0, 0, 0, strideC, Q, stream);
+    int num_sms = 0;
+    unsigned int *status = nullptr;
+    if (!current_sm103(&num_sms, &status)) return SGEMM_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    const long long sA = Q > 1 ? strideA : 0, sB = Q > 1 ? strideB : 0;
+    const uint16_t *pa = static_cast<const uint16_t *>(A);
+    const uint16_t *pb = static_cast<const uint16_t *>(B);
+    long long la = lda, lb = ldb, xa = sA, xb = sB;
+    char *w = static_cast<char *>(workspace);
+    size_t used = 0;
+    // operands the kernel cannot read as they are: a K-inner copy in the
+    // workspace (transposed when M- or N-inner), rows padded to 8 values
+    if (!direct(A, !transA, lda, Q, sA)) {
+        const bool bc = Q > 1 && sA == 0;
+        const size_t need = copy_bytes(M, K, Q, bc);
+        if (used + need > workspace_bytes) return SGEMM_ERR_INVALID_ARG;
+        uint16_t *dst = reinterpret_cast<uint16_t *>(w + used);
+        const long long ld = round8(K);
+        rc = launch_repack16(pa, lda, sA, M, K, bc ? 1 : Q, transA != 0, dst, ld,
+                             static_cast<long long>(M) * ld, st);
+        if (rc != SGEMM_OK) return rc;
+        pa = dst;
+        la = ld;
+        xa = bc ? 0 : static_cast<long long>(M) * ld;
+        used += need;
+    }
+    if (!direct(B, transB != 0, ldb, Q, sB)) {
+        const bool bc = Q > 1 && sB == 0;
+        const size_t need = copy_bytes(N, K, Q, bc);
+        if (used + need > workspace_bytes) return SGEMM_ERR_INVALID_ARG;
+        uint16_t *dst = reinterpret_cast<uint16_t *>(w + used);
+        const long long ld = round8(K);
+        rc = launch_repack16(pb, ldb, sB, N, K, bc ? 1 : Q, transB == 0, dst, ld,
+                             static_cast<long long>(N) * ld, st);
+        if (rc != SGEMM_OK) return rc;
+        pb = dst;
+        lb = ld;
+        xb = bc ? 0 : static_cast<long long>(N) * ld;
+        used += need;
+    }
+
+    Plan plan{};
+    GemmParams &p = plan.p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.Q = Q;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.C = C;
+    p.lda = la;
+    p.ldb = lb;
+    p.ldc = ldc;
+    p.sA = xa;
+    p.sB = xb;
+    p.sC = Q > 1 ? strideC : 0;
+    p.a_q_step = (Q > 1 && xa != 0) ? 1 : 0;
+    p.b_q_step = (Q > 1 && xb != 0) ? 1 : 0;
+    p.c_vec4 = aligned16(C) && ldc % 4 == 0 && (p.sC % 4) == 0;
+    p.status = status;
+    p.wait_limit = kWaitLimitCycles;
+    p.k_blocks = (K + tch::STAGE_K - 1) / tch::STAGE_K;
+    p.group_m = kGroupM;
+    p.tiles_m = (M + tch::PM - 1) / tch::PM;
+    p.tiles_n = (N + tch::BN - 1) / tch::BN;
+    p.num_tiles = static_cast<long long>(Q) * p.tiles_m * p.tiles_n;
+    plan.mode = kModeHalf;
+    plan.num_sms = num_sms;
+    plan.stream = st;
+    plan.ws = used < workspace_bytes ? static_cast<void *>(w + used) : nullptr;
+    plan.ws_bytes = used < workspace_bytes ? workspace_bytes - used : 0;
+
+    alignas(64) CUtensorMap tmA;
+    alignas(64) CUtensorMap tmB;
+    std::memset(&tmA, 0, sizeof(tmA));
+    std::memset(&tmB, 0, sizeof(tmB));
+    const bool bf16 = type == SGEMM_HALF_BF16;
+    if (!encode_operand16(&tmA, pa, bf16, M, K, la, Q, xa, tch::BM) ||
+        !encode_operand16(&tmB, pb, bf16, N, K, lb, Q, xb, tch::HN))
+        return SGEMM_ERR_UNSUPPORTED;
+    const int slots = half_slots(num_sms);
+    rc = plan_splits(plan, tch::PM, tch::BN, kFeedPair, slots);
+    if (rc != SGEMM_OK) return rc;
+    return bf16 ? launch_half<true>(plan, tmA, tmB, slots) : launch_half<false>(plan, tmA, tmB, slots);
+}
+
+}  // extern "C"

@@ -23,6 +23,21 @@ struct Plan {
     size_t ws_bytes;
 };
 
+// A wait may spin for this many SM clock cycles (about a second at the
+// GB300's clocks) before the kernel gives up and reports SGEMM_ERR_TIMEOUT.
+constexpr long long kWaitLimitCycles = 1LL << 31;
+
+// The planner's mode value for the 16-bit-input path (not a public mode).
+constexpr int kModeHalf = 16;
+
+bool aligned16(const void *p);
+// Argument checks shared by every entry point (dimensions, leading
+// dimensions, batch strides, pointers that will be read or written);
+// returns SGEMM_OK or SGEMM_ERR_INVALID_ARG.
+int check_shape(int M, int N, int K, float alpha, const void *A, int lda, const void *B, int ldb,
+                const float *C, int ldc, int transA, int transB, long long sA, long long sB,
+                long long sC, int Q);
+
 // Split-K plan shared by the kernels (BM x BN output tiles, persistent: one
 // CTA per multiprocessor, or one CTA pair per two for the tensor-core pair
 // kernel).  With T tiles on G units at once (multiprocessors, or pairs) the
@@ -95,6 +110,17 @@ SplitPlan one_wave_plan(int mode, int M, int N, int K, int Q);
 // the cp.async producer).
 bool encode_operand(CUtensorMap *map, const float *base, bool kin, long long rows, long long K,
                     long long ld, int Q, long long stride, int box_rows);
+
+// Tensor map of a K-inner 16-bit operand (bf16 or fp16): boxes of 64 k by
+// box_rows rows with the 128-byte swizzle.
+bool encode_operand16(CUtensorMap *map, const void *base, bool bf16, long long rows, long long K,
+                      long long ld, int Q, long long stride, int box_rows);
+// Copies Q matrices of 16-bit values into dst as rows x cols K-inner
+// matrices (row pitch ldd, batch stride dstride): dst[r][c] = src[c][r] when
+// trans (src stored cols x rows), else src[r][c] (src row pitch lds).
+int launch_repack16(const uint16_t *src, long long lds, long long sstride, int rows, int cols,
+                    int Q, bool trans, uint16_t *dst, long long ldd, long long dstride,
+                    cudaStream_t stream);
 
 // Transposes Q matrices of rows x cols (row pitch lds, batch stride sstride)
 // into dst (row pitch ldd, batch stride dstride): dst[c][r] = src[r][c].

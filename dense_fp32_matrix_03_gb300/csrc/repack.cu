@@ -86,7 +86,72 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// 16-bit values (bf16 / fp16 operands of the half path), moved as raw bits.
+// TRANS: dst[r][c] = src[c][r] for r < rows, c < cols (src stored cols x
+// rows, pitch lds), through a 64 x 65 shared tile; else dst[r][c] = src[r][c]
+// (pitch lds).  Block (x, y, z) = (column block, row block, batch), y and z
+// stepping by the grid when there are more blocks.
+template <bool TRANS>
+__global__ void __launch_bounds__(kThreads)
+    repack16_kernel(const uint16_t *__restrict__ src, long long lds, long long sstride, int rows,
+                    int cols, int Q, uint16_t *__restrict__ dst, long long ldd, long long dstride)
+{
+    __shared__ uint16_t tile[kT][kT + 1];
+    const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4
+    const int c0 = blockIdx.x * kT;
+    for (int q = blockIdx.z; q < Q; q += gridDim.z) {
+        const uint16_t *s = src + q * sstride;
+        uint16_t *d = dst + q * dstride;
+        for (long long r0l = static_cast<long long>(blockIdx.y) * kT; r0l < rows;
+             r0l += static_cast<long long>(gridDim.y) * kT) {
+            const int r0 = static_cast<int>(r0l);
+            if (TRANS) {
+                // source rows are destination columns c0 .. c0+63, read along r
+                for (int i = ty; i < kT; i += 4) {
+                    const int c = c0 + i, r = r0 + tx;
+                    tile[i][tx] = (c < cols && r < rows)
+                                      ? s[static_cast<long long>(c) * lds + r]
+                                      : static_cast<uint16_t>(0);
+                }
+                __syncthreads();
+                for (int i = ty; i < kT; i += 4) {
+                    const int r = r0 + i, c = c0 + tx;
+                    if (r < rows && c < cols) d[static_cast<long long>(r) * ldd + c] = tile[tx][i];
+                }
+                __syncthreads();
+            } else {
+                for (int i = ty; i < kT; i += 4) {
+                    const int r = r0 + i, c = c0 + tx;
+                    if (r < rows && c < cols)
+                        d[static_cast<long long>(r) * ldd + c] =
+                            s[static_cast<long long>(r) * lds + c];
+                }
+            }
+        }
+    }
+}
+
 }  // namespace
+
+int launch_repack16(const uint16_t *src, long long lds, long long sstride, int rows, int cols,
+                    int Q, bool trans, uint16_t *dst, long long ldd, long long dstride,
+                    cudaStream_t stream)
+{
+    if (rows <= 0 || cols <= 0 || Q <= 0) return SGEMM_OK;
+    const long long tc = (cols + kT - 1) / kT, tr = (rows + kT - 1) / kT;
+    if (tc > 0x7FFFFFFFLL) return SGEMM_ERR_UNSUPPORTED;
+    const dim3 grid(static_cast<unsigned>(tc), static_cast<unsigned>(tr < 65535 ? tr : 65535),
+                    static_cast<unsigned>(Q < 65535 ? Q : 65535));
+    if (trans)
+        repack16_kernel<true><<<grid, kThreads, 0, stream>>>(src, lds, sstride, rows, cols, Q, dst,
+                                                            ldd, dstride);
+    else
+        repack16_kernel<false><<<grid, kThreads, 0, stream>>>(src, lds, sstride, rows, cols, Q,
+                                                             dst, ldd, dstride);
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    note_launch();
+    return SGEMM_OK;
+}
 
 int launch_transpose(const float *src, long long lds, long long sstride, int rows, int cols, int Q,
                      float *dst, long long ldd, long long dstride, int, cudaStream_t stream)

@@ -1,0 +1,292 @@
+// tc_half.cuh -- GEMM with 16-bit inputs (bf16 or fp16) and fp32
+// accumulation and output on CTA pairs: C = alpha * op(A) @ op(B) + beta * C.
+//
+// The contraction the pages point to for tensor cores ("From 1% to 94% of
+// cuBLAS, one kernel at a time", future work: tensor cores with narrower
+// inputs) with operands that need no conversion: TMA stages both operands,
+// K-major with the 128-byte swizzle (64 values of 16 bits per row), straight
+// into the layout tcgen05.mma reads, and the MMA reads both from shared
+// memory.  Products of 16-bit values are exact in fp32; the sum is
+// accumulated in fp32 in TMEM.
+//
+// Tile 256 x 256 per CTA pair (cta_group::2, M = 256, N = 256, K = 16): each
+// CTA stages its 128 rows of A and its 128 of the tile's 256 rows of B^T, a
+// stage being 128 k (two 64-wide TMA boxes per operand, 64 KB per CTA),
+// three stages deep.  Both CTAs' TMA loads complete on the even CTA's
+// barrier (cta_group::2 form, which may name the peer's barrier); one thread
+// of the even CTA issues every MMA and multicasts its commits (stage free,
+// accumulator full) to both CTAs.  TMEM: two 256-column fp32 accumulators
+// per CTA (double buffered, so the epilogue overlaps the next tile).
+//
+// Warps: 0 TMA producer, 1 TMEM allocator + MMA issuer (even CTA), 2-5
+// epilogue (warp w reads TMEM lanes 32 * (w % 4) .. +31).  Every wait is
+// bounded; the CTAs meet at a cluster barrier before freeing TMEM.
+#pragma once
+
+#include "tc_pair.cuh"
+
+namespace sg {
+namespace tch {
+
+using tcp::arrive_on;
+using tcp::cluster_sync;
+using tcp::cta_rank;
+using tcp::drain_cl;
+using tcp::tmem_alloc_pair;
+using tcp::tmem_dealloc_pair;
+using tcp::umma_commit_both;
+using tcp::wait_cl;
+
+constexpr int BM = 128;      // rows of C per CTA
+constexpr int PM = 2 * BM;   // rows per pair tile (the MMA's M)
+constexpr int BN = 256;      // columns per pair tile (the MMA's N)
+constexpr int HN = BN / 2;   // rows of B^T each CTA holds
+constexpr int BKH = 64;      // 16-bit k per 128-byte swizzle row (one TMA box)
+constexpr int UKH = 16;      // k per kind::f16 MMA
+constexpr int KSUB = 2;      // boxes per stage
+constexpr int STAGE_K = KSUB * BKH;
+constexpr int SUB_A = BM * BKH * 2;  // 16 KB
+constexpr int SUB_B = HN * BKH * 2;  // 16 KB
+constexpr int STAGE_BYTES = KSUB * (SUB_A + SUB_B);  // per CTA
+constexpr int STAGES = 3;
+constexpr int kEpiWarp0 = 2;
+constexpr int kThreads = (kEpiWarp0 + 4) * 32;
+constexpr uint32_t kTmemCols = 512;
+constexpr int NBAR = 2 * STAGES + 4 + 1;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NBAR * 8 + 16 + 1024;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+static_assert(2 * BN <= static_cast<int>(kTmemCols), "TMEM columns");
+
+// Instruction descriptor: kind::f16 with bf16 (BF16) or fp16 inputs, fp32
+// accumulate, both operands K-major, M = 256 (two CTAs), N = 256.
+template <bool BF16>
+__host__ __device__ constexpr uint32_t idesc_half()
+{
+    return (1u << 4) | ((BF16 ? 1u : 0u) << 7) | ((BF16 ? 1u : 0u) << 10) |
+           (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(PM >> 4) << 24);
+}
+
+// TMA tile load into this CTA's shared memory whose completion is counted on
+// the barrier at shared::cluster address `bar` (the even CTA's).
+__device__ __forceinline__ void tma_load_pair(void *smem_dst, const CUtensorMap *m, uint32_t bar,
+                                              int c0, int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".cta_group::2 [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_addr(const void *p, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+// One stage's MMAs (two boxes x four k steps of 16) into accumulator d, A
+// and B by descriptors (a0/b0: box 0, k step 0; +2 per 32-byte k step,
+// + box bytes / 16 per box); the first overwrites d unless acc0.  Also tests,
+// without blocking, the barrier of the next stage (see tcp::issue_stage).
+template <bool BF16>
+__device__ __forceinline__ uint32_t issue_stage_half(uint32_t d, uint64_t a0, uint64_t b0,
+                                                     uint32_t acc0, uint32_t nbar, uint32_t npar)
+{
+    constexpr uint32_t idesc = idesc_half<BF16>();
+    constexpr uint64_t AB = SUB_A >> 4, BB = SUB_B >> 4;
+    uint32_t ready;
+    asm volatile(
+        "{\n\t.reg .pred q, p0, p1;\n\t.reg .b64 a, b;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 q, [%5], %6;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\t"
+        "setp.eq.b32 p1, %4, %4;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], %2, %3, %7, p0;\n\t"
+        "add.s64 a, %2, 2;\n\tadd.s64 b, %3, 2;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], a, b, %7, p1;\n\t"
+        "add.s64 a, %2, 4;\n\tadd.s64 b, %3, 4;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], a, b, %7, p1;\n\t"
+        "add.s64 a, %2, 6;\n\tadd.s64 b, %3, 6;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], a, b, %7, p1;\n\t"
+        "add.s64 a, %2, %8;\n\tadd.s64 b, %3, %9;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], a, b, %7, p1;\n\t"
+        "add.s64 a, a, 2;\n\tadd.s64 b, b, 2;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], a, b, %7, p1;\n\t"
+        "add.s64 a, a, 2;\n\tadd.s64 b, b, 2;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], a, b, %7, p1;\n\t"
+        "add.s64 a, a, 2;\n\tadd.s64 b, b, 2;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], a, b, %7, p1;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(ready)
+        : "r"(d), "l"(a0), "l"(b0), "r"(acc0), "r"(nbar), "r"(npar), "r"(idesc), "l"(AB),
+          "l"(BB)
+        : "memory");
+    return ready;
+}
+
+template <bool BF16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tch_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const GemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + STAGES * STAGE_BYTES);
+    uint64_t *full = bars;                  // even CTA's: both CTAs' bytes
+    uint64_t *empty = full + STAGES;        // per CTA: multicast commit
+    uint64_t *acc_full = empty + STAGES;    // per CTA: multicast commit
+    uint64_t *acc_empty = acc_full + 2;     // even CTA's: both CTAs' epilogues
+    uint64_t *mma_done = acc_empty + 2;
+    uint32_t *tmem_base = reinterpret_cast<uint32_t *>(mma_done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_base + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cta_rank();
+    const long long cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1u);
+            mbar_init(&empty[s], 1u);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1u);
+            mbar_init(&acc_empty[b], 2 * 4);
+        }
+        mbar_init(mma_done, 1u);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc_pair(tmem_base, kTmemCols);
+    tc::tc_fence_before();
+    cluster_sync();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_base;
+    const Abort ab{abort_flag, p.status, p.wait_limit};
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer (own CTA's rows)
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            tc::Ring<STAGES> rr;
+            long long issued = 0;
+            bool ok = true;
+            for (long long u = cid; ok && u < p.num_units; u += ncl) {
+                const WorkUnit wu = work_unit(u, p);
+                const int m0 = wu.tc.tm * PM + static_cast<int>(rank) * BM;
+                const int n0 = wu.tc.tn * BN + static_cast<int>(rank) * HN;
+                const int qa = wu.tc.q * p.a_q_step, qb = wu.tc.q * p.b_q_step;
+                for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
+                    if (!wait_cl(&empty[rr.s], rr.ph ^ 1u, ab, kStatusWaitEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    if (rank == 0) mbar_arrive_expect_tx(&full[rr.s], 2 * STAGE_BYTES);
+                    const uint32_t fb = cluster_addr(&full[rr.s], 0);
+                    uint8_t *sa = base + rr.s * STAGE_BYTES;
+                    uint8_t *sb = sa + KSUB * SUB_A;
+#pragma unroll
+                    for (int j = 0; j < KSUB; ++j) {
+                        const int k0 = kb * STAGE_K + j * BKH;
+                        tma_load_pair(sa + j * SUB_A, &tmA, fb, k0, m0, qa);
+                        tma_load_pair(sb + j * SUB_B, &tmB, fb, k0, n0, qb);
+                    }
+                    ++issued;
+                    rr.next();
+                }
+            }
+            (void)issued;
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (even CTA only)
+        if (rank == 0 && lane == 0) {
+            tc::Ring<STAGES> sr;
+            tc::Ring<2> acc;
+            bool ok = true;
+            bool any = false;
+            const uint64_t adesc0 = tc::kmajor_sw128_desc(smem_u32(base));
+            const uint64_t bdesc0 = tc::kmajor_sw128_desc(smem_u32(base + KSUB * SUB_A));
+            for (long long u = cid; ok && u < p.num_units; u += ncl) {
+                const WorkUnit wu = work_unit(u, p);
+                if (!wait_cl(&acc_empty[acc.s], acc.ph ^ 1u, ab, kStatusWaitAcc)) {
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+                const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc.s * BN);
+                uint32_t ready = 0;
+                for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
+                    if (!ready && !wait_cl(&full[sr.s], sr.ph, ab, kStatusWaitFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    const uint64_t soff = static_cast<uint64_t>(sr.s * (STAGE_BYTES >> 4));
+                    tc::Ring<STAGES> nx = sr;
+                    nx.next();
+                    ready = issue_stage_half<BF16>(d_tmem, adesc0 + soff, bdesc0 + soff,
+                                                   kb > wu.kb_lo ? 1u : 0u,
+                                                   smem_u32(&full[nx.s]), nx.ph);
+                    if (kb + 1 == wu.kb_hi) ready = 0;
+                    any = true;
+                    umma_commit_both(&empty[sr.s]);
+                    sr.next();
+                }
+                if (!ok) break;
+                umma_commit_both(&acc_full[acc.s]);
+                acc.next();
+            }
+            if (any) {
+                umma_commit_both(mma_done);
+                drain_cl(mma_done, 0, ab.limit);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (own CTA's rows)
+        const int q = warp & 3;
+        const int row_in_tile = static_cast<int>(rank) * BM + q * 32 + lane;
+        tc::Ring<2> acc;
+        for (long long u = cid; u < p.num_units; u += ncl) {
+            int w = 1;
+            if (lane == 0) w = wait_cl(&acc_full[acc.s], acc.ph, ab, kStatusWaitAcc, true);
+            if (!__shfl_sync(0xffffffffu, w, 0)) break;
+            drain_cl(&acc_full[acc.s], acc.ph, ab.limit);
+            tc::tc_fence_after();
+            const WorkUnit wu = work_unit(u, p);
+            const OutTile o = out_tile<PM, BN>(p, wu);
+            const uint32_t tbase =
+                tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc.s * BN);
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                float v[32];
+                tc::tmem_ld32(tbase + c0, v);
+                tc::store_chunk(o, row_in_tile, c0, v);
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) arrive_on(&acc_empty[acc.s], 0);
+            acc.next();
+        }
+    }
+
+    // ---- teardown: loads the producer issued land before anyone leaves
+    if (warp == 0 && lane == 0 && *abort_flag) {
+        // an aborted pair may leave TMA loads in flight: give them time
+        const long long t0 = clock64();
+        while (clock64() - t0 < (1LL << 20)) {
+        }
+    }
+    tc::tc_fence_before();
+    __syncwarp();
+    cluster_sync();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tmem_dealloc_pair(tmem, kTmemCols);
+    }
+}
+
+}  // namespace tch
+}  // namespace sg

@@ -152,6 +152,39 @@ int sgemm_batched_ex_noalloc(int mode, int M, int N, int K, float alpha, const f
                              int transB, long long strideA, long long strideB, long long strideC,
                              int Q, void *stream);
 
+/* GEMM with 16-bit inputs and fp32 accumulation and output:
+ *     C = alpha * op(A) @ op(B) + beta * C,  A and B bf16 or fp16, C fp32.
+ * (The next step the SGEMM worklog's future-work list points to -- tensor
+ * cores with narrower inputs -- on the same tcgen05 machinery: every
+ * product of two 16-bit values is exact in fp32, so results differ from
+ * the exact sum of products only by fp32 accumulation, within the FP32
+ * path's tolerance.)
+ *
+ * `type` is SGEMM_HALF_BF16 or SGEMM_HALF_FP16; A and B are DEVICE pointers
+ * to 16-bit values of that type, with the layout, leading dimensions
+ * (elements) and batch strides of sgemm_batched; C, alpha and beta as there.
+ * The kernel reads an operand directly when it is K-inner (A untransposed,
+ * B transposed: the "A times B-transpose" layout), 16-byte aligned, and its
+ * leading dimension and batch stride are multiples of 8; any other operand
+ * is first copied (transposed where needed) into the caller's DEVICE
+ * workspace (256-byte aligned when workspace_bytes > 0), which also serves
+ * the split-K partial tiles.  A call whose copies do not fit returns
+ * SGEMM_ERR_INVALID_ARG and launches nothing.
+ *
+ * sgemm_half_workspace_size returns the bytes of workspace the call wants
+ * for these layouts and leading dimensions (assuming 16-byte aligned
+ * operands), 0 when it needs none or for invalid arguments / no usable
+ * device.  K == 0 or alpha == 0 gives C = beta * C.  Errors as for
+ * sgemm_batched_ex_ws; SGEMM_ERR_INVALID_ARG also for an unknown type. */
+#define SGEMM_HALF_BF16 0
+#define SGEMM_HALF_FP16 1
+size_t sgemm_half_workspace_size(int type, int M, int N, int K, int transA, int transB, int lda,
+                                 int ldb, int Q);
+int sgemm_half_batched(int type, int M, int N, int K, float alpha, const void *A, int lda,
+                       const void *B, int ldb, float beta, float *C, int ldc, int transA,
+                       int transB, long long strideA, long long strideB, long long strideC, int Q,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
 /* The product on HOST buffers.  (No counterpart on the pages, whose
  * benchmarks start with the operands on the GPU: an addition of this library
  * for callers whose data lives in host memory.)

@@ -138,3 +138,26 @@ def test_peak_probe_rejects_invalid_arguments(lib):
     assert lib.sgemm_peak_probe("ffma", (1 << 16) + 1)[0] == lib.SGEMM_ERR_INVALID_ARG
     assert lib.sgemm_peak_probe("tf32_ss", (1 << 22) + 1)[0] == lib.SGEMM_ERR_INVALID_ARG
     assert lib._lib.sgemm_peak_probe(0, 16, None, None) == lib.SGEMM_ERR_INVALID_ARG
+
+
+def half(lib, **kw):
+    a = dict(type_=0, M=8, N=8, K=8, alpha=1.0, A=FAKE, lda=8, B=FAKE, ldb=8, beta=0.0, C=FAKE,
+             ldc=8, transA=0, transB=1, strideA=0, strideB=0, strideC=0, Q=1, ws=0, wsb=0)
+    a.update(kw)
+    return lib.sgemm_half_batched(a["type_"], a["M"], a["N"], a["K"], a["alpha"], a["A"],
+                                  a["lda"], a["B"], a["ldb"], a["beta"], a["C"], a["ldc"],
+                                  a["transA"], a["transB"], a["strideA"], a["strideB"],
+                                  a["strideC"], a["Q"], a["ws"], a["wsb"])
+
+
+@pytest.mark.parametrize("bad", [
+    dict(type_=2), dict(type_=-1), dict(M=-1), dict(lda=7), dict(ldb=7), dict(ldc=7),
+    dict(C=0), dict(A=0), dict(B=0), dict(ws=FAKE + 16, wsb=1024), dict(ws=0, wsb=1024),
+    dict(Q=2, strideC=7),
+])
+def test_half_entry_rejects_invalid_arguments(lib, bad):
+    assert half(lib, **bad) == lib.SGEMM_ERR_INVALID_ARG
+
+
+def test_half_entry_empty_is_a_no_op(lib):
+    assert half(lib, M=0, A=0, B=0, C=0) == lib.SGEMM_OK

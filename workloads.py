@@ -109,3 +109,29 @@ def random_inputs(M: int, N: int, K: int, Q: int = 1, seed: int = 0):
     B = rng.uniform(-1, 1, size=lead + (K, N)).astype(np.float32)
     C0 = rng.uniform(-1, 1, size=lead + (M, N)).astype(np.float32)
     return A, B, C0
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """float32 values rounded to the nearest bfloat16 (ties to even), returned
+    as float32 (exactly representable in bf16).  Input generation for the
+    16-bit-input path; NaN/Inf are not expected here."""
+    bits = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    bits = (bits + 0x7FFF + ((bits >> 16) & 1)) >> 16 << 16
+    return bits.astype(np.uint32).view(np.float32)
+
+
+def half_bits(x: np.ndarray, type_: str) -> np.ndarray:
+    """The 16-bit encodings (uint16) of float32 values already representable
+    in `type_` ("bf16": the high half of the fp32 bits; "fp16": IEEE half)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if type_ == "bf16":
+        return (x.view(np.uint32) >> 16).astype(np.uint16)
+    return x.astype(np.float16).view(np.uint16)
+
+
+def half_inputs(M: int, N: int, K: int, type_: str, Q: int = 1, seed: int = 0):
+    """Uniform[-1,1] matrices rounded to bf16 or fp16 (as float32), and C0."""
+    A, B, C0 = random_inputs(M, N, K, Q, seed)
+    if type_ == "bf16":
+        return round_to_bf16(A), round_to_bf16(B), C0
+    return A.astype(np.float16).astype(np.float32), B.astype(np.float16).astype(np.float32), C0
