@@ -87,17 +87,58 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // 16-bit values (bf16 / fp16 operands of the half path), moved as raw bits.
-// TRANS: dst[r][c] = src[c][r] for r < rows, c < cols (src stored cols x
-// rows, pitch lds), through a 64 x 65 shared tile; else dst[r][c] = src[r][c]
-// (pitch lds).  Block (x, y, z) = (column block, row block, batch), y and z
-// stepping by the grid when there are more blocks.
-template <bool TRANS>
+//
+// Re-pitched copy: dst[r][c] = src[r][c] (src pitch lds, dst pitch ldd a
+// multiple of 8).  A thread moves 8 values: one 16-byte store, loaded 16,
+// 4 or 2 bytes at a time as the source rows' alignment allows (LW values per
+// load).  Block (x, y, z) = (chunk of 2048 values, row, batch), y and z
+// stepping by the grid.
+template <int LW>
 __global__ void __launch_bounds__(kThreads)
-    repack16_kernel(const uint16_t *__restrict__ src, long long lds, long long sstride, int rows,
-                    int cols, int Q, uint16_t *__restrict__ dst, long long ldd, long long dstride)
+    copy16_kernel(const uint16_t *__restrict__ src, long long lds, long long sstride, int rows,
+                  int cols, int Q, uint16_t *__restrict__ dst, long long ldd, long long dstride)
 {
-    __shared__ uint16_t tile[kT][kT + 1];
-    const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4
+    const int c = (blockIdx.x * kThreads + threadIdx.x) * 8;
+    if (c >= cols) return;
+    for (int q = blockIdx.z; q < Q; q += gridDim.z) {
+        for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
+            const uint16_t *sp = src + q * sstride + r * lds + c;
+            uint16_t *dp = dst + q * dstride + r * ldd + c;
+            if (c + 8 <= cols) {
+                uint4 v;
+                if (LW == 8) {
+                    v = *reinterpret_cast<const uint4 *>(sp);
+                } else if (LW == 2) {
+                    const uint32_t *w = reinterpret_cast<const uint32_t *>(sp);
+                    v = make_uint4(w[0], w[1], w[2], w[3]);
+                } else {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        w[j] = static_cast<uint32_t>(sp[2 * j]) |
+                               (static_cast<uint32_t>(sp[2 * j + 1]) << 16);
+                    v = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                *reinterpret_cast<uint4 *>(dp) = v;
+            } else {
+                for (int j = 0; c + j < cols; ++j) dp[j] = sp[j];
+            }
+        }
+    }
+}
+
+// Transposed copy: dst[r][c] = src[c][r] (src stored cols x rows, pitch
+// lds), through a 64 x 64 shared tile; each thread reads two values of a
+// source row (one 4-byte load when the source allows) and writes two of a
+// destination row (one 4-byte store: ldd is even).
+template <bool SRC4>
+__global__ void __launch_bounds__(kThreads)
+    transpose16_kernel(const uint16_t *__restrict__ src, long long lds, long long sstride,
+                       int rows, int cols, int Q, uint16_t *__restrict__ dst, long long ldd,
+                       long long dstride)
+{
+    __shared__ uint16_t tile[kT][kT + 2];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
     const int c0 = blockIdx.x * kT;
     for (int q = blockIdx.z; q < Q; q += gridDim.z) {
         const uint16_t *s = src + q * sstride;
@@ -105,28 +146,42 @@ __global__ void __launch_bounds__(kThreads)
         for (long long r0l = static_cast<long long>(blockIdx.y) * kT; r0l < rows;
              r0l += static_cast<long long>(gridDim.y) * kT) {
             const int r0 = static_cast<int>(r0l);
-            if (TRANS) {
-                // source rows are destination columns c0 .. c0+63, read along r
-                for (int i = ty; i < kT; i += 4) {
-                    const int c = c0 + i, r = r0 + tx;
-                    tile[i][tx] = (c < cols && r < rows)
-                                      ? s[static_cast<long long>(c) * lds + r]
-                                      : static_cast<uint16_t>(0);
+            // source rows c0 + i, values r0 + 2tx, r0 + 2tx + 1
+#pragma unroll
+            for (int i = ty; i < kT; i += 8) {
+                const int c = c0 + i, r = r0 + 2 * tx;
+                uint16_t v0 = 0, v1 = 0;
+                if (c < cols) {
+                    const uint16_t *sp = s + static_cast<long long>(c) * lds + r;
+                    if (SRC4 && r + 1 < rows) {
+                        const uint32_t w = *reinterpret_cast<const uint32_t *>(sp);
+                        v0 = static_cast<uint16_t>(w & 0xFFFFu);
+                        v1 = static_cast<uint16_t>(w >> 16);
+                    } else {
+                        if (r < rows) v0 = sp[0];
+                        if (r + 1 < rows) v1 = sp[1];
+                    }
                 }
-                __syncthreads();
-                for (int i = ty; i < kT; i += 4) {
-                    const int r = r0 + i, c = c0 + tx;
-                    if (r < rows && c < cols) d[static_cast<long long>(r) * ldd + c] = tile[tx][i];
-                }
-                __syncthreads();
-            } else {
-                for (int i = ty; i < kT; i += 4) {
-                    const int r = r0 + i, c = c0 + tx;
-                    if (r < rows && c < cols)
-                        d[static_cast<long long>(r) * ldd + c] =
-                            s[static_cast<long long>(r) * lds + c];
+                tile[i][2 * tx] = v0;
+                tile[i][2 * tx + 1] = v1;
+            }
+            __syncthreads();
+            // destination rows r0 + i, values c0 + 2tx, c0 + 2tx + 1
+#pragma unroll
+            for (int i = ty; i < kT; i += 8) {
+                const int r = r0 + i, c = c0 + 2 * tx;
+                if (r < rows && c < cols) {
+                    uint16_t *dp = d + static_cast<long long>(r) * ldd + c;
+                    if (c + 1 < cols) {
+                        *reinterpret_cast<uint32_t *>(dp) =
+                            static_cast<uint32_t>(tile[2 * tx][i]) |
+                            (static_cast<uint32_t>(tile[2 * tx + 1][i]) << 16);
+                    } else {
+                        dp[0] = tile[2 * tx][i];
+                    }
                 }
             }
+            __syncthreads();
         }
     }
 }
@@ -138,16 +193,39 @@ int launch_repack16(const uint16_t *src, long long lds, long long sstride, int r
                     cudaStream_t stream)
 {
     if (rows <= 0 || cols <= 0 || Q <= 0) return SGEMM_OK;
-    const long long tc = (cols + kT - 1) / kT, tr = (rows + kT - 1) / kT;
-    if (tc > 0x7FFFFFFFLL) return SGEMM_ERR_UNSUPPORTED;
-    const dim3 grid(static_cast<unsigned>(tc), static_cast<unsigned>(tr < 65535 ? tr : 65535),
-                    static_cast<unsigned>(Q < 65535 ? Q : 65535));
-    if (trans)
-        repack16_kernel<true><<<grid, kThreads, 0, stream>>>(src, lds, sstride, rows, cols, Q, dst,
-                                                            ldd, dstride);
-    else
-        repack16_kernel<false><<<grid, kThreads, 0, stream>>>(src, lds, sstride, rows, cols, Q,
-                                                             dst, ldd, dstride);
+    if (ldd % 8 != 0 || (Q > 1 && dstride % 8 != 0) || (reinterpret_cast<uintptr_t>(dst) & 15))
+        return SGEMM_ERR_UNSUPPORTED;
+    const unsigned gz = static_cast<unsigned>(Q < 65535 ? Q : 65535);
+    const uintptr_t sa = reinterpret_cast<uintptr_t>(src);
+    const bool batch_even = Q <= 1 || sstride % 2 == 0;
+    if (trans) {
+        const long long tc = (cols + kT - 1) / kT, tr = (rows + kT - 1) / kT;
+        if (tc > 0x7FFFFFFFLL) return SGEMM_ERR_UNSUPPORTED;
+        const dim3 grid(static_cast<unsigned>(tc), static_cast<unsigned>(tr < 65535 ? tr : 65535),
+                        gz);
+        const bool src4 = (sa & 3) == 0 && lds % 2 == 0 && batch_even;
+        if (src4)
+            transpose16_kernel<true><<<grid, kThreads, 0, stream>>>(src, lds, sstride, rows, cols,
+                                                                   Q, dst, ldd, dstride);
+        else
+            transpose16_kernel<false><<<grid, kThreads, 0, stream>>>(src, lds, sstride, rows,
+                                                                    cols, Q, dst, ldd, dstride);
+    } else {
+        const long long cb = (cols + 8LL * kThreads - 1) / (8LL * kThreads);
+        const dim3 grid(static_cast<unsigned>(cb), static_cast<unsigned>(rows < 65535 ? rows : 65535),
+                        gz);
+        const bool w16 = (sa & 15) == 0 && lds % 8 == 0 && (Q <= 1 || sstride % 8 == 0);
+        const bool w4 = (sa & 3) == 0 && lds % 2 == 0 && batch_even;
+        if (w16)
+            copy16_kernel<8><<<grid, kThreads, 0, stream>>>(src, lds, sstride, rows, cols, Q, dst,
+                                                           ldd, dstride);
+        else if (w4)
+            copy16_kernel<2><<<grid, kThreads, 0, stream>>>(src, lds, sstride, rows, cols, Q, dst,
+                                                           ldd, dstride);
+        else
+            copy16_kernel<1><<<grid, kThreads, 0, stream>>>(src, lds, sstride, rows, cols, Q, dst,
+                                                           ldd, dstride);
+    }
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
     note_launch();
     return SGEMM_OK;

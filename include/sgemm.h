@@ -166,7 +166,8 @@ int sgemm_batched_ex_noalloc(int mode, int M, int N, int K, float alpha, const f
  * The kernel reads an operand directly when it is K-inner (A untransposed,
  * B transposed: the "A times B-transpose" layout), 16-byte aligned, and its
  * leading dimension and batch stride are multiples of 8; any other operand
- * is first copied (transposed where needed) into the caller's DEVICE
+ * is first copied (transposed where needed, rows padded to 64 values) into
+ * the caller's DEVICE
  * workspace (256-byte aligned when workspace_bytes > 0), which also serves
  * the split-K partial tiles.  A call whose copies do not fit returns
  * SGEMM_ERR_INVALID_ARG and launches nothing.
