@@ -388,6 +388,9 @@ def main():
     ap.add_argument("--mode", default="auto", choices=["auto", "fp32", "3xtf32", "tf32"])
     ap.add_argument("--no-extra", action="store_true", help="skip per-path and BMM figures")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
+    ap.add_argument("--half-only", action="store_true",
+                    help="instead of the benchmark line, print one JSON line with the "
+                         "16-bit-input path's figures (bf16 / fp16 at 4092^3 and 8192^3)")
     ap.add_argument("--all-configs", action="store_true",
                     help="instead of the benchmark line, print one JSON line per workload "
                          "configuration and path (256^3, ragged, size sweep, batched)")
@@ -400,6 +403,8 @@ def main():
         return reference_arm(args, rank, world)
     if args.all_configs:
         return all_configs(args)
+    if args.half_only:
+        return half_only()
 
     import torch
     import dense_fp32_matrix_03_gb300 as lib
@@ -627,6 +632,20 @@ def extra_figures(lib, default_mode, dev, stream, flush, num_sms, peaks, peak_sr
         out["bmm"][f"transB={tB}"] = {"tflops": gemm_flops(M, N, K, Q) / (t / 1e3) / 1e12,
                                       "ms": t, "mode": default_mode}
     return out
+
+
+def half_only():
+    import torch
+    import dense_fp32_matrix_03_gb300 as lib
+    dev = torch.device("cuda", 0)
+    lib.load()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    peaks, src = load_peaks()
+    out = half_figures(lib, dev, torch.cuda.current_stream(dev), flush, peaks, src)
+    print(json.dumps({"half": out, "l2": "flushed before every timed step"}), flush=True)
+    return 0
 
 
 def all_configs(args):
