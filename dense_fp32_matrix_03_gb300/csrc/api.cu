@@ -505,6 +505,62 @@ int repack_for_simt(Plan &plan)
     return SGEMM_OK;
 }
 
+// Tensor-core paths with a workspace: an operand TMA cannot describe (row
+// pitch or batch stride not a multiple of 16 bytes, unaligned base) is
+// copied, in its own layout, into the workspace with rows padded to whole
+// 128-byte lines, so that the product runs on the TMA-fed pair kernel
+// instead of the direct-load one (measured on GB300, the ragged
+// 1000 x 1500 x 777 case, lda = 777: see DESIGN).  What remains of the
+// workspace goes to the split plan; without room for the copy the operand
+// stays where it is and the direct kernel runs.
+int repack_for_tc(Plan &plan)
+{
+    GemmParams &p = plan.p;
+    if (plan.ws == nullptr || plan.ws_bytes == 0 || (plan.a_tma && plan.b_tma)) return SGEMM_OK;
+    char *w = static_cast<char *>(plan.ws);
+    size_t used = 0;
+    for (int which = 0; which < 2; ++which) {
+        const bool is_a = which == 0;
+        if (is_a ? plan.a_tma : plan.b_tma) continue;
+        // stored rows x row length of the operand as the caller holds it
+        const bool trans = is_a ? plan.transA : plan.transB;
+        const long long rows = is_a ? (trans ? p.K : p.M) : (trans ? p.N : p.K);
+        const long long len = is_a ? (trans ? p.M : p.K) : (trans ? p.K : p.N);
+        const long long ld = (len + 31) / 32 * 32;
+        const long long stride = is_a ? p.sA : p.sB;
+        const int q = (p.Q > 1 && stride == 0) ? 1 : p.Q;
+        const size_t bytes = round256(static_cast<size_t>(q) * rows * ld * sizeof(float));
+        if (used + bytes > plan.ws_bytes) continue;
+        float *dst = reinterpret_cast<float *>(w + used);
+        const float *src = is_a ? p.A : p.B;
+        const long long lds = is_a ? p.lda : p.ldb;
+        const int rc = launch_repack16(reinterpret_cast<const uint16_t *>(src), 2 * lds, 2 * stride,
+                                       static_cast<int>(rows), static_cast<int>(2 * len), q, false,
+                                       reinterpret_cast<uint16_t *>(dst), 2 * ld, 2 * rows * ld,
+                                       plan.stream);
+        if (rc != SGEMM_OK) return rc;
+        if (is_a) {
+            p.A = dst;
+            p.lda = ld;
+            p.sA = q == 1 ? 0 : rows * ld;
+            p.a_q_step = q == 1 ? 0 : 1;
+            p.a_vec4 = 1;
+            plan.a_tma = true;
+        } else {
+            p.B = dst;
+            p.ldb = ld;
+            p.sB = q == 1 ? 0 : rows * ld;
+            p.b_q_step = q == 1 ? 0 : 1;
+            p.b_vec4 = 1;
+            plan.b_tma = true;
+        }
+        used += bytes;
+    }
+    plan.ws = used < plan.ws_bytes ? static_cast<void *>(w + used) : nullptr;
+    plan.ws_bytes = used < plan.ws_bytes ? plan.ws_bytes - used : 0;
+    return SGEMM_OK;
+}
+
 int run(int mode, int M, int N, int K, float alpha, const float *A, int lda, const float *B,
         int ldb, float beta, float *C, int ldc, int transA, int transB, long long sA,
         long long sB, long long sC, int Q, void *stream, void *ws = nullptr,
@@ -571,6 +627,8 @@ int run(int mode, int M, int N, int K, float alpha, const float *A, int lda, con
         if (rc != SGEMM_OK) return rc;
         return launch_simt(plan);
     }
+    rc = repack_for_tc(plan);
+    if (rc != SGEMM_OK) return rc;
     return launch_tc(plan);
 }
 
@@ -619,7 +677,18 @@ size_t sgemm_workspace_size(int mode, int M, int N, int K, int Q)
 {
     const size_t split = preferred_plan(mode, M, N, K, Q).ws_bytes;
     if (mode == SGEMM_MODE_DEFAULT) mode = g_default_mode.load();
-    if (mode != SGEMM_MODE_FP32 || M <= 0 || N <= 0 || K <= 0 || Q <= 0) return split;
+    if (M <= 0 || N <= 0 || K <= 0 || Q <= 0) return split;
+    if (mode == SGEMM_MODE_3XTF32 || mode == SGEMM_MODE_TF32) {
+        // room for 128-byte-pitched copies of operands TMA cannot describe
+        // (pointers, leading dimensions and layouts are not known here)
+        auto copy = [Q, K](long long rows) {
+            const long long r32k = rows * ((K + 31) / 32 * 32);
+            const long long kr32 = static_cast<long long>(K) * ((rows + 31) / 32 * 32);
+            return round256(static_cast<size_t>(Q) * (r32k > kr32 ? r32k : kr32) * 4);
+        };
+        return split + copy(M) + copy(N);
+    }
+    if (mode != SGEMM_MODE_FP32) return split;
     // room for the transposed operands the FP32 path may make (the layout
     // is not known here; a broadcast operand would need less)
     size_t repack = 0;

@@ -114,7 +114,11 @@ int sgemm_batched_ex(int mode, int M, int N, int K, float alpha, const float *A,
  * bits.  On the FP32 path the workspace also serves a transposed copy of a
  * K-inner A (when N >= 1024) and of a K-inner B (when M >= 1024), made on
  * `stream` before the product: that path runs fastest with A M-inner and B
- * N-inner.  sgemm_workspace_size counts that room for both operands.  The
+ * N-inner.  On the tensor-core paths it serves a copy, rows padded to 128
+ * bytes, of an operand TMA cannot describe (row pitch or batch stride not a
+ * multiple of 4 floats, base not 16-byte aligned), which then runs on the
+ * TMA-fed kernel instead of the slower direct-load one.  sgemm_workspace_size
+ * counts that room for both operands.  The
  * workspace needs no initialisation; it must not be used by another call
  * running at the same time. */
 size_t sgemm_workspace_size(int mode, int M, int N, int K, int Q);

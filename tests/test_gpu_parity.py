@@ -157,6 +157,25 @@ def test_integer_unaligned_operands_bit_exact(oracle_mod, mode):
                                offsets=(1, 2, 3)), mode, oracle_mod, exact=True)
 
 
+@pytest.mark.parametrize("mode", MODES)
+def test_unaligned_operands_through_the_workspace(oracle_mod, mode):
+    """The same unaligned operands with a workspace: the tensor-core paths
+    copy them to 128-byte pitches and run the TMA-fed kernel, the FP32 path
+    transposes or keeps them; random data within tolerance, integer data
+    bit for bit, batched and broadcast."""
+    supported(mode)
+    A, B, C0 = workloads.random_inputs(300, 260, 197, Q=3, seed=14)
+    for tA in (0, 1):
+        for tB in (0, 1):
+            check_full(Problem(A, B, C0, 1.5, 0.5, transA=tA, transB=tB, pads=(1, 3, 0),
+                               offsets=(1, 0, 1)), mode, oracle_mod, api="ws")
+    A, B, C0 = workloads.integer_inputs(1000, 1500, 777, seed=15)
+    check_full(Problem(A, B, C0, 1.0, 0.0), mode, oracle_mod, exact=True, api="ws")
+    A, B, C0 = workloads.integer_inputs(129, 70, 33, Q=4, seed=16)
+    check_full(Problem(A, B, C0, 2.0, 1.0, strideA=0, offsets=(1, 0, 0)), mode, oracle_mod,
+               exact=True, api="ws")
+
+
 # ---------------------------------------------------------- ragged sweeps
 
 RAGGED = [1, 7, 31, 127, 128, 129, 777]

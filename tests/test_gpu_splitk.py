@@ -152,6 +152,12 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
         def repack(inner, outer):
             return (Q * outer * ((inner + 3) // 4 * 4) * 4 + 255) // 256 * 256
         need += (repack(M, K) if N >= 1024 else 0) + (repack(N, K) if M >= 1024 else 0)
+    else:
+        # room for 128-byte-pitched copies of A and B, either layout
+        def copy(rows):
+            r32 = lambda x: (x + 31) // 32 * 32
+            return (Q * max(rows * r32(K), K * r32(rows)) * 4 + 255) // 256 * 256
+        need += copy(M) + copy(N)
     return need
 
 
@@ -175,7 +181,8 @@ def test_workspace_size_query():
     import dense_fp32_matrix_03_gb300 as lib
     assert lib.sgemm_workspace_size("fp32", 1000, 1000, 32, 1) == 0      # one k-block: no split
     assert lib.sgemm_workspace_size("fp32", 1024, 1024, 32, 1) > 0       # room to transpose A, B
-    assert lib.sgemm_workspace_size("3xtf32", 1024, 1024, 128, 1) == 0  # tensor path: >= 256 per slice
+    # tensor path: no split (>= 256 per slice), room for aligned copies of A and B only
+    assert lib.sgemm_workspace_size("3xtf32", 1024, 1024, 128, 1) == 2 * 1024 * 128 * 4
     assert lib.sgemm_workspace_size("fp32", 1024, 1024, 128, 1) > 0     # 2 slices of 64
     assert lib.sgemm_workspace_size("fp32", 0, 10, 10, 1) == 0
     assert lib.sgemm_workspace_size(7, 100, 100, 100, 1) == 0
