@@ -196,7 +196,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     rr.next();
                 }
             }
-            (void)issued;
+            // Both CTAs' loads of a stage complete on the even CTA's barrier:
+            // when stopping early, the even CTA waits (bounded) for the last
+            // stages' phases, so that after the cluster barrier below no load
+            // is still in flight into either CTA's shared memory.  (On the
+            // normal path the MMAs consumed every stage.)  An abort in the
+            // odd CTA reaches the even one through the waits that then run
+            // out there.
+            if (rank == 0 && (!ok || *abort_flag)) {
+                tc::Ring<STAGES> d;
+                for (long long j = 0; j < issued; ++j) {
+                    if (j + STAGES >= issued) drain_cl(&full[d.s], d.ph, ab.limit);
+                    d.next();
+                }
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -272,13 +285,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
     }
 
-    // ---- teardown: loads the producer issued land before anyone leaves
-    if (warp == 0 && lane == 0 && *abort_flag) {
-        // an aborted pair may leave TMA loads in flight: give them time
-        const long long t0 = clock64();
-        while (clock64() - t0 < (1LL << 20)) {
-        }
-    }
+    // ---- teardown: free TMEM jointly once both CTAs are done
     tc::tc_fence_before();
     __syncwarp();
     cluster_sync();

@@ -396,7 +396,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 rr.next();
             }
         }
-        if (!ok && lane == 0) {
+        // when this CTA is stopping early (its own wait ran out, or another
+        // role's did), the stages issued last may still be landing: wait
+        // (bounded) for them before the teardown.  On the normal path every
+        // stage has been consumed, and the loop is not run (running it cost
+        // 2.4% at 4092^3 on GB300).
+        if (lane == 0 && (!ok || *sm.abort_flag)) {
             Ring<C::RAW_STAGES> d;
             for (long long j = 0; j < issued; ++j) {
                 if (j + C::RAW_STAGES >= issued) mbar_drain(&sm.raw_full[d.s], d.ph, ab.limit);

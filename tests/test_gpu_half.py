@@ -135,3 +135,12 @@ def test_half_rejects_a_workspace_too_small_for_its_copies():
     A, B, C0 = workloads.half_inputs(256, 256, 128, "bf16", seed=39)
     prob = Problem(A, B, C0, 1.0, 0.0, 1, 0)   # both operands need a copy
     run_half(prob, "bf16", ws_bytes=256, expect=lib.SGEMM_ERR_INVALID_ARG)
+
+
+@pytest.mark.parametrize("type_", TYPES)
+def test_half_broadcast_batch_strides(oracle_mod, type_):
+    """strideA = 0 (one A for every batch entry, read directly) and strideB =
+    0 with B N-inner (copied once, transposed)."""
+    A, B, C0 = workloads.half_inputs(96, 80, 64, type_, Q=4, seed=40)
+    check(Problem(A, B, C0, 1.0, 0.5, 0, 1, strideA=0), type_, oracle_mod)
+    check(Problem(A, B, C0, 1.0, 0.5, 0, 0, strideB=0), type_, oracle_mod)
