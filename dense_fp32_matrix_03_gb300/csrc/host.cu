@@ -1,9 +1,10 @@
 // host.cu -- the product on host buffers.  The operands are copied into a
 // device buffer the caller provides, the product is computed there, and C
-// is copied back.  C is cut into panels of rows: the copy-in of panel p+1,
-// the product of panel p and the copy-out of panel p-1 run at the same time
-// on three streams (the caller's, for the products, and two of the
-// library's own, one per copy direction), ordered by events.
+// is copied back.  C is cut into panels of rows and, for large K, K into two
+// slices: the copy-in of one (slice, panel), the product of the previous one
+// and the copy-out of a finished panel run at the same time on three streams
+// (the caller's, for the products, and two of the library's own, one per
+// copy direction), ordered by events.
 #include <cstdint>
 #include <mutex>
 
@@ -18,6 +19,9 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxPanels = 64;
+// K from which the call cuts the product in two K slices (below it, half of
+// op(B) arrives too soon for the overlap to pay for a second pass over C).
+constexpr int kKSplitMin = 1024;
 
 // Copy streams of a device, made on first use and kept for the process.
 struct CopyStreams {
@@ -167,7 +171,16 @@ int sgemm_host(int mode, int M, int N, int K, float alpha, const float *A, int l
     float *dC = reinterpret_cast<float *>(base + L.offC);
     void *ws = L.ws_bytes ? base + L.offW : nullptr;
 
-    cudaEvent_t fork = nullptr, join = nullptr, ready[kMaxPanels] = {}, done[kMaxPanels] = {};
+    // K is cut into kslices slices (two when K is large): the products of
+    // the first slice start once half of op(B) has arrived, while the rest
+    // of the copy-in is still under way; later slices accumulate (beta = 1).
+    // Slice boundaries are multiples of 32 so every slice of the device
+    // copies stays 16-byte aligned.
+    const int kslices = (reads_ab && K >= kKSplitMin) ? 2 : 1;
+    long long kb[3] = {0, K, K};
+    if (kslices == 2) kb[1] = (K / 2) / 32 * 32;
+
+    cudaEvent_t fork = nullptr, join = nullptr, ready[2][kMaxPanels] = {}, done[kMaxPanels] = {};
     int rc = SGEMM_OK;
     auto ok = [&rc](cudaError_t e) {
         if (e != cudaSuccess && rc == SGEMM_OK) rc = SGEMM_ERR_LAUNCH;
@@ -176,53 +189,63 @@ int sgemm_host(int mode, int M, int N, int K, float alpha, const float *A, int l
     const unsigned flags = cudaEventDisableTiming;
     bool made = ok(cudaEventCreateWithFlags(&fork, flags)) &&
                 ok(cudaEventCreateWithFlags(&join, flags));
-    for (int p = 0; made && p < L.panels; ++p)
-        made = ok(cudaEventCreateWithFlags(&ready[p], flags)) &&
-               ok(cudaEventCreateWithFlags(&done[p], flags));
+    for (int p = 0; made && p < L.panels; ++p) {
+        made = ok(cudaEventCreateWithFlags(&done[p], flags));
+        for (int h = 0; made && h < kslices; ++h)
+            made = ok(cudaEventCreateWithFlags(&ready[h][p], flags));
+    }
 
     // The copies wait for whatever the caller queued on `stream` before.
     if (made && ok(cudaEventRecord(fork, st)) && ok(cudaStreamWaitEvent(in, fork, 0)) &&
         ok(cudaStreamWaitEvent(out, fork, 0))) {
         const size_t f = sizeof(float);
-        if (reads_ab) {
-            if (transB)
-                ok(cudaMemcpy2DAsync(dB, L.ldB * f, B, ldb * f, K * f, N, cudaMemcpyHostToDevice,
-                                     in));
-            else
-                ok(cudaMemcpy2DAsync(dB, L.ldB * f, B, ldb * f, N * f, K, cudaMemcpyHostToDevice,
-                                     in));
-        }
-        for (int p = 0; rc == SGEMM_OK && p < L.panels; ++p) {
-            const long long m0 = static_cast<long long>(p) * L.panel;
-            const int rows = static_cast<int>(M - m0 < L.panel ? M - m0 : L.panel);
-            float *pA = transA ? dA + m0 : dA + m0 * L.ldA;
-            float *pC = dC + m0 * L.ldC;
+        for (int h = 0; rc == SGEMM_OK && h < kslices; ++h) {
+            const long long k0 = kb[h], kn = kb[h + 1] - kb[h];
+            // slice h of op(B): rows k0 .. k0+kn of K x N, or columns of N x K
+            float *sB = transB ? dB + k0 : dB + k0 * L.ldB;
             if (reads_ab) {
-                if (transA)
-                    ok(cudaMemcpy2DAsync(pA, L.ldA * f, A + m0, lda * f, rows * f, K,
+                if (transB)
+                    ok(cudaMemcpy2DAsync(sB, L.ldB * f, B + k0, ldb * f, kn * f, N,
                                          cudaMemcpyHostToDevice, in));
                 else
-                    ok(cudaMemcpy2DAsync(pA, L.ldA * f, A + m0 * lda, lda * f, K * f, rows,
+                    ok(cudaMemcpy2DAsync(sB, L.ldB * f, B + k0 * ldb, ldb * f, N * f, kn,
                                          cudaMemcpyHostToDevice, in));
             }
-            if (beta != 0.f)
-                ok(cudaMemcpy2DAsync(pC, L.ldC * f, C + m0 * ldc, ldc * f, N * f, rows,
-                                     cudaMemcpyHostToDevice, in));
-            if (!ok(cudaEventRecord(ready[p], in)) || !ok(cudaStreamWaitEvent(st, ready[p], 0)))
-                break;
-            const int g = sgemm_batched_ex_ws(mode, rows, N, K, alpha, reads_ab ? pA : nullptr,
-                                              static_cast<int>(L.ldA), reads_ab ? dB : nullptr,
-                                              static_cast<int>(L.ldB), beta, pC,
-                                              static_cast<int>(L.ldC), transA, transB, 0, 0, 0, 1,
-                                              ws, L.ws_bytes, st);
-            if (g != SGEMM_OK) {
-                rc = g;
-                break;
+            for (int p = 0; rc == SGEMM_OK && p < L.panels; ++p) {
+                const long long m0 = static_cast<long long>(p) * L.panel;
+                const int rows = static_cast<int>(M - m0 < L.panel ? M - m0 : L.panel);
+                // slice h of this panel's rows of op(A)
+                float *pA = transA ? dA + k0 * L.ldA + m0 : dA + m0 * L.ldA + k0;
+                float *pC = dC + m0 * L.ldC;
+                if (reads_ab) {
+                    if (transA)
+                        ok(cudaMemcpy2DAsync(pA, L.ldA * f, A + k0 * lda + m0, lda * f, rows * f,
+                                             kn, cudaMemcpyHostToDevice, in));
+                    else
+                        ok(cudaMemcpy2DAsync(pA, L.ldA * f, A + m0 * lda + k0, lda * f, kn * f,
+                                             rows, cudaMemcpyHostToDevice, in));
+                }
+                if (h == 0 && beta != 0.f)
+                    ok(cudaMemcpy2DAsync(pC, L.ldC * f, C + m0 * ldc, ldc * f, N * f, rows,
+                                         cudaMemcpyHostToDevice, in));
+                if (!ok(cudaEventRecord(ready[h][p], in)) ||
+                    !ok(cudaStreamWaitEvent(st, ready[h][p], 0)))
+                    break;
+                const int g = sgemm_batched_ex_ws(
+                    mode, rows, N, static_cast<int>(kn), alpha, reads_ab ? pA : nullptr,
+                    static_cast<int>(L.ldA), reads_ab ? sB : nullptr, static_cast<int>(L.ldB),
+                    h == 0 ? beta : 1.f, pC, static_cast<int>(L.ldC), transA, transB, 0, 0, 0, 1,
+                    ws, L.ws_bytes, st);
+                if (g != SGEMM_OK) {
+                    rc = g;
+                    break;
+                }
+                if (h + 1 < kslices) continue;
+                if (!ok(cudaEventRecord(done[p], st)) || !ok(cudaStreamWaitEvent(out, done[p], 0)))
+                    break;
+                ok(cudaMemcpy2DAsync(C + m0 * ldc, ldc * f, pC, L.ldC * f, N * f, rows,
+                                     cudaMemcpyDeviceToHost, out));
             }
-            if (!ok(cudaEventRecord(done[p], st)) || !ok(cudaStreamWaitEvent(out, done[p], 0)))
-                break;
-            ok(cudaMemcpy2DAsync(C + m0 * ldc, ldc * f, pC, L.ldC * f, N * f, rows,
-                                 cudaMemcpyDeviceToHost, out));
         }
     }
     // `stream` reaches its next work only once every copy-out is done (also
@@ -233,7 +256,8 @@ int sgemm_host(int mode, int M, int N, int K, float alpha, const float *A, int l
     if (fork) cudaEventDestroy(fork);
     if (join) cudaEventDestroy(join);
     for (int p = 0; p < L.panels; ++p) {
-        if (ready[p]) cudaEventDestroy(ready[p]);
+        for (int h = 0; h < 2; ++h)
+            if (ready[h][p]) cudaEventDestroy(ready[h][p]);
         if (done[p]) cudaEventDestroy(done[p]);
     }
     return rc;

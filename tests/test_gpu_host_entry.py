@@ -156,3 +156,21 @@ def test_peak_probe_runs_and_is_plausible(kind):
     tflops = flops / (e0.elapsed_time(e1) * 1e-3) / 1e12
     lo, hi = PROBE_RANGES[kind]
     assert lo <= tflops <= hi, f"{kind}: {tflops:.1f} TFLOP/s"
+
+
+@pytest.mark.parametrize("tA,tB", [(0, 0), (1, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("mode", MODES)
+def test_host_entry_k_slices(oracle_mod, mode, tA, tB):
+    """K >= 1024: the call cuts K in two slices (the second pass accumulates
+    with beta = 1); random data within tolerance, integer data bit for bit
+    (power-of-two alpha, integer beta: both passes are exact)."""
+    A, B, C0 = workloads.random_inputs(600, 500, 1500, seed=41)
+    prob = Problem(A, B, C0, 1.5, -0.5, tA, tB, pads=(2, 1, 3))
+    C = run_host(prob, mode, panel_rows=256)
+    Cref, D = prob.oracle(oracle_mod)
+    assert oracle_mod.max_rel_err(C, Cref, D) <= TOL[mode]
+    A, B, C0 = workloads.integer_inputs(300, 260, 1100, seed=42)
+    prob = Problem(A, B, C0, 2.0, -1.0, tA, tB)
+    C = run_host(prob, mode, panel_rows=128)
+    Cref, _ = prob.oracle(oracle_mod)
+    assert np.array_equal(C.astype(np.float64), Cref)
