@@ -298,17 +298,20 @@ def reference_arm(args, rank, world):
 # --------------------------------------------------------------- GPU arm
 
 def time_calls(call, steps, warmup, stream, flush, lib=None):
-    """Per-step CUDA-event times (ms) on `stream`, L2 flushed before each;
+    """Per-step CUDA-event times (ms) on `stream`, L2 flushed before each
+    (flush=None: not flushed, the warm-L2 variant);
     with `lib`, also the library's kernel launches during the timed steps."""
     import torch
     for _ in range(warmup):
-        flush.zero_()
+        if flush is not None:
+            flush.zero_()
         call()
     torch.cuda.synchronize()
     evs = []
     n0 = lib.sgemm_kernel_launches() if lib is not None else 0
     for _ in range(steps):
-        flush.zero_()
+        if flush is not None:
+            flush.zero_()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -648,9 +651,50 @@ def half_only():
     return 0
 
 
+def oracle_timing(w, beta, target_s=2.0):
+    """The oracle on a bounded row sample of workload w (rows spread over the
+    batch and M), sized for about target_s seconds on the threads it uses
+    (OMP_NUM_THREADS, else every core)."""
+    import numpy as np
+    import oracle
+    M, N, K, Q = w["M"], w["N"], w["K"], w["Q"]
+
+    def run(nrows):
+        idx = np.linspace(0, Q * M - 1, nrows).astype(np.int64)
+        rows = [(int(i // M), int(i % M)) for i in idx]
+        t0 = time.perf_counter()
+        oracle.sgemm_ref(M, N, K, w["alpha"], w["A"], K, w["B"], N, beta, w["C0"], N,
+                         strideA=M * K, strideB=K * N, strideC=M * N, Q=Q, rows=rows)
+        return time.perf_counter() - t0
+
+    t = run(4)
+    nrows = int(min(Q * M, max(4, 4 / max(t, 1e-6) * target_s)))
+    t = run(nrows)
+    flops = 2.0 * nrows * N * K
+    return {"gflops": round(flops / t / 1e9, 3), "threads": oracle.num_threads(),
+            "seconds": round(t, 3), "rows": f"{nrows} of {Q * M}"}
+
+
+def oracle_timing_single_thread(name, beta_idx):
+    """oracle_timing on one thread, in a child process (the oracle's thread
+    count is fixed when it loads)."""
+    import subprocess
+    code = ("import json, bench, workloads; w = workloads.make(%r); "
+            "print(json.dumps(bench.oracle_timing(w, w['betas'][%d])))" % (name, beta_idx))
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                         text=True, timeout=600)
+    if out.returncode != 0:
+        return {"error": out.stderr.strip().splitlines()[-1:]}
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
 def all_configs(args):
     """One JSON line per (workload, path): TFLOP/s and the roofline it is
-    bound by, min(peak, AI * HBM bandwidth) with AI over compulsory bytes."""
+    bound by, min(peak, AI * HBM bandwidth) with AI over compulsory bytes;
+    for working sets under 2 x L2 also the warm-L2 time.  Then one line per
+    workload with the oracle's rate on the host cores (and on one thread for
+    the two small configurations)."""
     import numpy as np
     import torch
     import dense_fp32_matrix_03_gb300 as lib
@@ -699,12 +743,25 @@ def all_configs(args):
                     tf = flops / (ms / 1e3) / 1e12
                     bound, peak, _ = roofline_peak(mode, props.multi_processor_count, peaks, src)
                     roof = min(peak, ai * bw)
-                    print(json.dumps({"workload": name, "beta": beta, "transB": tB, "mode": mode,
-                                      "entry": entry, "ms": round(ms, 4), "tflops": round(tf, 2),
-                                      "roof_tflops": round(roof, 1),
-                                      "roof_bound": bound if roof == peak else "hbm",
-                                      "frac": round(tf / roof, 3)}), flush=True)
+                    line = {"workload": name, "beta": beta, "transB": tB, "mode": mode,
+                            "entry": entry, "ms": round(ms, 4), "tflops": round(tf, 2),
+                            "roof_tflops": round(roof, 1),
+                            "roof_bound": bound if roof == peak else "hbm",
+                            "frac": round(tf / roof, 3)}
+                    if compulsory_bytes(M, N, K, Q, beta != 0) + ws_bytes < 2 * l2:
+                        msw = statistics.median(time_calls(call, args.steps, args.warmup,
+                                                           stream, None))
+                        line["ms_warm_l2"] = round(msw, 4)
+                        line["tflops_warm_l2"] = round(flops / (msw / 1e3) / 1e12, 2)
+                    print(json.dumps(line), flush=True)
     lib.check(lib.sgemm_poll_error(stream))
+    for name, beta_idx in cases:
+        w = workloads.make(name)
+        line = {"workload": name, "beta": w["betas"][beta_idx],
+                "oracle": oracle_timing(w, w["betas"][beta_idx])}
+        if name in ("sgemm_256", "sgemm_ragged_1000x1500x777"):
+            line["oracle_one_thread"] = oracle_timing_single_thread(name, beta_idx)
+        print(json.dumps(line), flush=True)
     return 0
 
 
