@@ -267,7 +267,7 @@ double path_rate_per_sm(int mode, int feed)
     if (mode == SGEMM_MODE_FP32) return feed == kFeedDirect ? 0.24e12 : 0.40e12;
     if (mode == SGEMM_MODE_3XTF32) return feed == kFeedDirect ? 0.47e12 : 1.8e12;
     if (mode == kModeHalf) return 11.0e12;
-    return feed == kFeedDirect ? 0.55e12 : 3.0e12;
+    return feed == kFeedDirect ? 0.55e12 : 3.6e12;
 }
 
 size_t splitk_workspace_bytes(long long split_tiles, int splits, int bm, int bn)
@@ -376,7 +376,7 @@ SplitPlan plan_query(int mode, int M, int N, int K, int Q, bool one_wave)
         if (mode == SGEMM_MODE_FP32) {
             simt_tile_dims(shape == 1, bm, bn);
         } else {
-            tc_tile_dims(shape == 1, bm, bn);
+            tc_tile_dims(mode, K, shape == 1, bm, bn);
             if (shape == 1) {
                 slots = tc_pair_slots(sms);
                 feeds[0] = feeds[1] = kFeedPair;

@@ -68,13 +68,13 @@ struct Layout {
 // 4092^3: one to two waves per panel beat both fewer, larger panels, whose
 // first copy-in and last copy-out overlap nothing, and smaller ones, which
 // leave multiprocessors idle in every product), at most kMaxPanels.
-int auto_panel_rows(int mode, int M, int N, int num_sms)
+int auto_panel_rows(int mode, int M, int N, int K, int num_sms)
 {
     int bm = 0, bn = 0, slots = num_sms;
     if (mode == SGEMM_MODE_FP32) {
         simt_tile_dims(false, bm, bn);
     } else {
-        tc_tile_dims(true, bm, bn);
+        tc_tile_dims(mode, K, true, bm, bn);
         slots = tc_pair_slots(num_sms);
     }
     const long long tiles_n = (N + bn - 1) / bn;
@@ -99,7 +99,7 @@ bool make_layout(int mode, int M, int N, int K, int transA, int transB, int pane
     L->ldC = round4(N);
     const long long rowsA = transA ? K : M, rowsB = transB ? N : K;
     L->panel = panel_rows > 0 ? (panel_rows < M ? panel_rows : M)
-                              : auto_panel_rows(mode, M, N, num_sms);
+                              : auto_panel_rows(mode, M, N, K, num_sms);
     if (L->panel < 1) L->panel = 1;
     L->panels = static_cast<int>((M + L->panel - 1) / L->panel);
     if (L->panels > kMaxPanels) return false;

@@ -53,7 +53,7 @@ int check_shape(int M, int N, int K, float alpha, const void *A, int lda, const 
 //                                                 i.e. <= 64 MB, else 3 TB/s))
 // with t_tile = 2 * BM * BN * K / (multiprocessors per unit x the kernel's
 // per-multiprocessor rate, as measured on GB300: 0.40 TFLOP/s FP32, 1.8
-// 3xTF32, 3.0 TF32 with TMA-fed operands; 0.24, 0.47, 0.55 for operands TMA
+// 3xTF32, 3.6 TF32 with TMA-fed operands; 0.24, 0.47, 0.55 for operands TMA
 // cannot describe).  s runs over
 // 1 .. min(16, K / min_slice_k(mode)); the best s is used only when it
 // saves at least 1%.  Each slice is at least
@@ -86,7 +86,7 @@ int plan_splits(Plan &plan, int bm, int bn, int feed, int slots);
 // depends on whether both operands are K-inner.
 void simt_tile_dims(bool both_k_inner, int &bm, int &bn);
 // pair: the CTA-pair kernel's tile (the single-CTA kernels' otherwise).
-void tc_tile_dims(bool pair, int &bm, int &bn);
+void tc_tile_dims(int mode, int K, bool pair, int &bm, int &bn);
 // CTA pairs of the pair kernel that fit on the device at once (cached).
 int tc_pair_slots(int num_sms);
 // Launches the CTA-pair tensor-core kernel (tile counts filled in by the

@@ -51,10 +51,10 @@ int dispatch_direct(Plan &plan)
 
 }  // namespace
 
-void tc_tile_dims(bool pair, int &bm, int &bn)
+void tc_tile_dims(int mode, int K, bool pair, int &bm, int &bn)
 {
     bm = pair ? tcp::PM : tc::BM;
-    bn = pair ? tcp::BN : kBN;
+    bn = pair ? tcp::pair_shape(tcp::pair_wide(mode == SGEMM_MODE_3XTF32, K)).bn : kBN;
 }
 
 int launch_tc(Plan &plan)
@@ -68,15 +68,17 @@ int launch_tc(Plan &plan)
     alignas(64) CUtensorMap tmB;
     std::memset(&tmA, 0, sizeof(tmA));
     std::memset(&tmB, 0, sizeof(tmB));
+    const tcp::PairShape sh =
+        tcp::pair_shape(tcp::pair_wide(plan.mode == SGEMM_MODE_3XTF32, p.K));
     if (plan.a_tma && plan.b_tma &&
         encode_operand(&tmA, p.A, !plan.transA, p.M, p.K, p.lda, p.Q, p.sA, tcp::BM) &&
-        encode_operand(&tmB, p.B, plan.transB, p.N, p.K, p.ldb, p.Q, p.sB, tcp::HN)) {
-        p.k_blocks = (p.K + tcp::STAGE_K - 1) / tcp::STAGE_K;  // the pair kernel's stages
+        encode_operand(&tmB, p.B, plan.transB, p.N, p.K, p.ldb, p.Q, p.sB, sh.hn)) {
+        p.k_blocks = (p.K + sh.stage_k - 1) / sh.stage_k;  // the pair kernel's stages
         p.tiles_m = (p.M + tcp::PM - 1) / tcp::PM;
-        p.tiles_n = (p.N + tcp::BN - 1) / tcp::BN;
+        p.tiles_n = (p.N + sh.bn - 1) / sh.bn;
         p.num_tiles = static_cast<long long>(p.Q) * p.tiles_m * p.tiles_n;
         const int slots = tc_pair_slots(plan.num_sms);
-        const int rc = plan_splits(plan, tcp::PM, tcp::BN, kFeedPair, slots);
+        const int rc = plan_splits(plan, tcp::PM, sh.bn, kFeedPair, slots);
         if (rc != SGEMM_OK) return rc;
         return launch_tc_pair(plan, tmA, tmB, slots);
     }

@@ -14,10 +14,10 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_slots[kMaxDevices];
 
-template <bool SPLIT3, bool A_KIN, bool B_KIN>
+template <bool SPLIT3, bool A_KIN, bool B_KIN, bool WIDE>
 int launch_one(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB, int slots)
 {
-    using C = tcp::Cfg<SPLIT3, A_KIN, B_KIN>;
+    using C = tcp::Cfg<SPLIT3, A_KIN, B_KIN, WIDE>;
     auto kern = tcp::tcp_sgemm_kernel<C>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
@@ -28,17 +28,17 @@ int launch_one(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB, int s
         tmA, tmB, plan.p);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
     note_launch();
-    return plan.p.splits > 1 ? launch_fixup(plan, tcp::PM, tcp::BN) : SGEMM_OK;
+    return plan.p.splits > 1 ? launch_fixup(plan, tcp::PM, C::BN) : SGEMM_OK;
 }
 
-template <bool SPLIT3>
+template <bool SPLIT3, bool WIDE>
 int dispatch(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB, int slots)
 {
     const bool a_kin = !plan.transA, b_kin = plan.transB;
-    if (a_kin && !b_kin) return launch_one<SPLIT3, true, false>(plan, tmA, tmB, slots);
-    if (a_kin && b_kin) return launch_one<SPLIT3, true, true>(plan, tmA, tmB, slots);
-    if (!a_kin && !b_kin) return launch_one<SPLIT3, false, false>(plan, tmA, tmB, slots);
-    return launch_one<SPLIT3, false, true>(plan, tmA, tmB, slots);
+    if (a_kin && !b_kin) return launch_one<SPLIT3, true, false, WIDE>(plan, tmA, tmB, slots);
+    if (a_kin && b_kin) return launch_one<SPLIT3, true, true, WIDE>(plan, tmA, tmB, slots);
+    if (!a_kin && !b_kin) return launch_one<SPLIT3, false, false, WIDE>(plan, tmA, tmB, slots);
+    return launch_one<SPLIT3, false, true, WIDE>(plan, tmA, tmB, slots);
 }
 
 }  // namespace
@@ -73,8 +73,9 @@ int tc_pair_slots(int num_sms)
 
 int launch_tc_pair(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB, int slots)
 {
-    return plan.mode == SGEMM_MODE_3XTF32 ? dispatch<true>(plan, tmA, tmB, slots)
-                                          : dispatch<false>(plan, tmA, tmB, slots);
+    if (plan.mode == SGEMM_MODE_3XTF32) return dispatch<true, false>(plan, tmA, tmB, slots);
+    if (tcp::pair_wide(false, plan.p.K)) return dispatch<false, true>(plan, tmA, tmB, slots);
+    return dispatch<false, false>(plan, tmA, tmB, slots);
 }
 
 }  // namespace sg

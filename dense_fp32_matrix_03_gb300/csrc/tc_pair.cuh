@@ -39,6 +39,14 @@
 #ifndef SG_TCP_KSUB
 #define SG_TCP_KSUB 2
 #endif
+// the wide (256 x 256) configuration's sub-blocks per stage and ring depths
+// (measured on GB300, TF32 4092^3 nn / nt, TFLOP/s: 1/4/4 556/428, 1/5/4
+// 543/424, 1/4/6 561/431, 2/2/2 520/441, 2/2/3 526/442)
+#ifndef SG_TCP_WIDE_KSUB
+#define SG_TCP_WIDE_KSUB 1
+#define SG_TCP_WIDE_RAW 4
+#define SG_TCP_WIDE_SPLIT 6
+#endif
 #ifndef SG_TCP_RAW3
 #if SG_TCP_KSUB == 2
 #define SG_TCP_RAW3 3
@@ -69,14 +77,22 @@ using tc::UK;
 
 constexpr int BM = 128;      // rows of C per CTA
 constexpr int PM = 2 * BM;   // rows per pair tile (the MMA's M)
-constexpr int BN = 128;      // columns per pair tile (the MMA's N)
-constexpr int HN = BN / 2;   // rows of B^T each CTA holds
-constexpr int KSUB = SG_TCP_KSUB;  // 32-wide k sub-blocks per stage
-constexpr int STAGE_K = KSUB * BK;
 
-template <bool SPLIT3_, bool A_KIN_, bool B_KIN_>
+// WIDE: 256 x 256 pair tiles (MMA N = 256) with one accumulator buffer and
+// 32-wide stages -- for plain TF32, whose 256 x 128 tiles are bound by L2 ->
+// shared-memory traffic (25% less per flop here; measured on GB300, TF32
+// 4092^3 nn 460 -> 561 TFLOP/s); the accumulator is then drained before the
+// next tile's MMAs start.  Otherwise (3xTF32, bound by the MMA issue, not
+// by L2) 256 x 128 tiles, two accumulator buffers, SG_TCP_KSUB sub-blocks
+// per stage.
+template <bool SPLIT3_, bool A_KIN_, bool B_KIN_, bool WIDE_ = false>
 struct Cfg {
-    static constexpr bool SPLIT3 = SPLIT3_, A_KIN = A_KIN_, B_KIN = B_KIN_;
+    static constexpr bool SPLIT3 = SPLIT3_, A_KIN = A_KIN_, B_KIN = B_KIN_, WIDE = WIDE_;
+    static constexpr int BN = WIDE ? 256 : 128;   // columns per pair tile (the MMA's N)
+    static constexpr int HN = BN / 2;             // rows of B^T each CTA holds
+    static constexpr int KSUB = WIDE ? SG_TCP_WIDE_KSUB : SG_TCP_KSUB;  // 32-wide sub-blocks
+    static constexpr int STAGE_K = KSUB * BK;
+    static constexpr int ACC_BUFS = WIDE ? 1 : 2;
     static constexpr int SUB_A = BM * BK * 4;   // raw A of one 32-wide sub-block
     static constexpr int SUB_B = HN * BK * 4;   // raw B of one sub-block
     static constexpr int A_BYTES = KSUB * SUB_A;
@@ -85,9 +101,11 @@ struct Cfg {
     static constexpr int PLANES = SPLIT3 ? 2 : 1;
     static constexpr int SUB_SPLIT = PLANES * SUB_B;  // B planes of one sub-block
     static constexpr int SPLIT_BYTES = KSUB * SUB_SPLIT;
-    static constexpr int RAW_STAGES = SPLIT3 ? SG_TCP_RAW3 : SG_TCP_RAW1;
-    static constexpr int SPLIT_STAGES = SPLIT3 ? SG_TCP_SPLIT3 : SG_TCP_SPLIT1;
-    static constexpr int ACC_COLS = 2 * BN;
+    static constexpr int RAW_STAGES =
+        WIDE ? SG_TCP_WIDE_RAW : (SPLIT3 ? SG_TCP_RAW3 : SG_TCP_RAW1);
+    static constexpr int SPLIT_STAGES =
+        WIDE ? SG_TCP_WIDE_SPLIT : (SPLIT3 ? SG_TCP_SPLIT3 : SG_TCP_SPLIT1);
+    static constexpr int ACC_COLS = ACC_BUFS * BN;
     static constexpr int SUB_COLS = PLANES * BK;      // TMEM A columns of one sub-block
     static constexpr int A_COLS = KSUB * SUB_COLS;
     static constexpr int NBAR = 2 * RAW_STAGES + 2 * SPLIT_STAGES + 4 + 1;
@@ -97,13 +115,34 @@ struct Cfg {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     // a sub-block's split planes: B_hi | B_lo
     static constexpr int OFF_BHI = 0, OFF_BLO = SUB_B;
+    // Instruction descriptor: kind::tf32, fp32 accumulate, both operands
+    // K-major, M = 256 (two CTAs), N = BN.
+    static constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) |
+                                      (static_cast<uint32_t>(BN >> 3) << 17) |
+                                      (static_cast<uint32_t>(PM >> 4) << 24);
 };
 
-// Instruction descriptor: kind::tf32, fp32 accumulate, both operands
-// K-major, M = 256 (two CTAs), N = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) |
-                            (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(PM >> 4) << 24);
+// Plain TF32 runs on the wide tiles when K is at least this long: with a
+// shorter K each tile is short, and the wide configuration's undrained
+// single accumulator and fewer tiles per wave cost more than its lighter
+// traffic saves (measured on GB300, TF32 wide / narrow, TFLOP/s: 4092^3
+// 574 / 490, 2048^3 396 / 336, 1024^3 95 / 105, batched 1024 x 1024 x 512
+// 224 / 240).
+constexpr int kWideMinK = 1536;
+
+inline bool pair_wide(bool split3, int K) { return !split3 && K >= kWideMinK; }
+
+// The tile shape the pair kernel uses: columns per pair tile, rows of B^T
+// per CTA (the B tensor map's box), k per pipeline stage.
+struct PairShape {
+    int bn, hn, stage_k;
+};
+constexpr PairShape pair_shape(bool wide)
+{
+    using W = Cfg<false, true, false, true>;
+    using N = Cfg<true, true, false, false>;
+    return wide ? PairShape{W::BN, W::HN, W::STAGE_K} : PairShape{N::BN, N::HN, N::STAGE_K};
+}
 
 // ------------------------------------------------------------ PTX wrappers
 
@@ -154,7 +193,7 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
 template <bool SPLIT3>
 __device__ __forceinline__ uint32_t issue_stage(uint32_t d, uint32_t a_hi, uint32_t a_lo,
                                                 uint64_t b_hi, uint64_t b_lo, uint32_t acc0,
-                                                uint32_t nbar, uint32_t npar)
+                                                uint32_t nbar, uint32_t npar, uint32_t idesc)
 {
     uint32_t ready;
     if (SPLIT3) {
@@ -181,7 +220,7 @@ __device__ __forceinline__ uint32_t issue_stage(uint32_t d, uint32_t a_hi, uint3
             "selp.u32 %0, 1, 0, q;\n\t}"
             : "=r"(ready)
             : "r"(d), "r"(a_hi), "r"(a_lo), "l"(b_hi), "l"(b_lo), "r"(acc0), "r"(nbar),
-              "r"(npar), "r"(kIdesc)
+              "r"(npar), "r"(idesc)
             : "memory");
     } else {
         asm volatile(
@@ -198,7 +237,7 @@ __device__ __forceinline__ uint32_t issue_stage(uint32_t d, uint32_t a_hi, uint3
             "tcgen05.mma.cta_group::2.kind::tf32 [%1], [ah], bh, %7, p1;\n\t"
             "selp.u32 %0, 1, 0, q;\n\t}"
             : "=r"(ready)
-            : "r"(d), "r"(a_hi), "r"(acc0), "r"(nbar), "r"(npar), "l"(b_hi), "r"(kIdesc)
+            : "r"(d), "r"(a_hi), "r"(acc0), "r"(nbar), "r"(npar), "l"(b_hi), "r"(idesc)
             : "memory");
         (void)a_lo;
         (void)b_lo;
@@ -368,7 +407,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const WorkUnit wu = work_unit(u, p);
             const TileCoord &tc = wu.tc;
             const int m0 = tc.tm * PM + static_cast<int>(rank) * BM;
-            const int n0 = tc.tn * BN + static_cast<int>(rank) * HN;
+            const int n0 = tc.tn * C::BN + static_cast<int>(rank) * C::HN;
             for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
                 uint8_t *sa = sm.raw + rr.s * C::RAW_BYTES;
                 uint8_t *sb = sa + C::A_BYTES;
@@ -379,8 +418,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const int qa = tc.q * p.a_q_step, qb = tc.q * p.b_q_step;
                         mbar_arrive_expect_tx(&sm.raw_full[rr.s], C::RAW_BYTES);
 #pragma unroll
-                        for (int j = 0; j < KSUB; ++j) {
-                            const int k0 = kb * STAGE_K + j * BK;
+                        for (int j = 0; j < C::KSUB; ++j) {
+                            const int k0 = kb * C::STAGE_K + j * BK;
                             uint8_t *ja = sa + j * C::SUB_A;
                             uint8_t *jb = sb + j * C::SUB_B;
                             if (C::A_KIN) tma_load_3d(ja, &tmA, &sm.raw_full[rr.s], k0, m0, qa);
@@ -412,7 +451,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ MMA issuer (even CTA only)
         if (rank == 0 && lane == 0) {
             Ring<C::SPLIT_STAGES> sr;
-            Ring<2> acc;
+            Ring<C::ACC_BUFS> acc;
             bool ok = true;
             bool any = false;
             // B descriptors of split stage 0; stage s and k step kk are at
@@ -426,7 +465,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc::tc_fence_after();
-                const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc.s * BN);
+                const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc.s * C::BN);
                 uint32_t ready = 0;  // split_full[sr] already seen complete
                 for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
                     if (!ready && !wait_cl(&sm.split_full[sr.s], sr.ph, ab, kStatusWaitConv)) {
@@ -440,13 +479,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     Ring<C::SPLIT_STAGES> nx = sr;
                     nx.next();
 #pragma unroll
-                    for (int j = 0; j < KSUB; ++j) {
+                    for (int j = 0; j < C::KSUB; ++j) {
                         const uint64_t b_hi = b_st + static_cast<uint64_t>(j * (C::SUB_SPLIT >> 4));
                         const uint32_t a_hi = a_st + j * C::SUB_COLS;
                         ready = issue_stage<C::SPLIT3>(
                             d_tmem, a_hi, a_hi + BK, b_hi, b_hi + (C::OFF_BLO >> 4),
                             (kb > wu.kb_lo || j > 0) ? 1u : 0u, smem_u32(&sm.split_full[nx.s]),
-                            nx.ph);
+                            nx.ph, C::IDESC);
                     }
                     if (kb + 1 == wu.kb_hi) ready = 0;  // the next unit waits afresh
                     any = true;
@@ -487,7 +526,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t t_st = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                                           C::ACC_COLS + sr.s * C::A_COLS;
 #pragma unroll 1
-                    for (int j = 0; j < KSUB; ++j) {
+                    for (int j = 0; j < C::KSUB; ++j) {
                         const uint32_t t_hi = t_st + j * C::SUB_COLS;
                         tc::convert_a_row<C::A_KIN, C::SPLIT3>(sa + j * C::SUB_A, row, t_hi,
                                                                t_hi + BK);
@@ -497,9 +536,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 } else {
                     uint8_t *st = sm.split + sr.s * C::SPLIT_BYTES;
 #pragma unroll 1
-                    for (int j = 0; j < KSUB; ++j) {
+                    for (int j = 0; j < C::KSUB; ++j) {
                         uint8_t *jt = st + j * C::SUB_SPLIT;
-                        tc::convert_b_tile<HN, C::B_KIN, C::SPLIT3>(sb + j * C::SUB_B,
+                        tc::convert_b_tile<C::HN, C::B_KIN, C::SPLIT3>(sb + j * C::SUB_B,
                                                                     jt + C::OFF_BHI,
                                                                     jt + C::OFF_BLO, ct);
                     }
@@ -518,7 +557,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ epilogue (own CTA's rows)
         const int q = warp & 3;
         const int row_in_tile = static_cast<int>(rank) * BM + q * 32 + lane;
-        Ring<2> acc;
+        Ring<C::ACC_BUFS> acc;
         for (long long u = cid; u < p.num_units; u += ncl) {
             int w = 1;
             if (lane == 0) w = wait_cl(&sm.acc_full[acc.s], acc.ph, ab, kStatusWaitAcc, true);
@@ -526,11 +565,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             drain_cl(&sm.acc_full[acc.s], acc.ph, ab.limit);
             tc::tc_fence_after();
             const WorkUnit wu = work_unit(u, p);
-            const OutTile o = out_tile<PM, BN>(p, wu);
-            const uint32_t tbase =
-                tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc.s * BN);
+            const OutTile o = out_tile<PM, C::BN>(p, wu);
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc.s * C::BN);
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
+            for (int c0 = 0; c0 < C::BN; c0 += 32) {
                 float v[32];
                 tc::tmem_ld32(tbase + c0, v);
                 tc::store_chunk(o, row_in_tile, c0, v);

@@ -89,8 +89,10 @@ int sgemm_batched_ex(int mode, int M, int N, int K, float alpha, const float *A,
                      void *stream);
 
 /* Split-K workspace.  The output is cut into tiles (256 x 128 on the FP32
- * path and on the tensor-core paths with TMA-describable operands, 128 x 128
- * otherwise), each computed by one persistent CTA per multiprocessor or, on
+ * and 3xTF32 paths, 256 x 256 on the TF32 path when the operands are
+ * TMA-describable and K >= 1536, 128 x 128 for operands TMA cannot
+ * describe), each computed by one persistent
+ * CTA per multiprocessor or, on
  * the tensor cores, one CTA pair per two.  When the tiles do not fill a
  * whole number of waves (4092^3: 512 tiles = 6.7 waves on 76 pairs), or fill less than
  * one (small or skinny products such as the ragged 1000 x 1500 x 777 case),

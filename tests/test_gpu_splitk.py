@@ -108,8 +108,8 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
     every kernel the mode may run (FP32: 256 x 128 tiles where the FMAs pair,
     128 x 128 with both operands K-inner, each TMA- or cp.async-fed, one unit
     per multiprocessor; tensor cores: the direct kernel's 128 x 128 tiles on
-    every multiprocessor and the pair kernel's 256 x 128 tiles, one unit per
-    CTA pair): whole waves of units, then the last wave's r tiles cut into s
+    every multiprocessor and the pair kernel's 256 x 128 tiles (256 x 256 for
+    TF32 with K >= 1536), one unit per CTA pair): whole waves of units, then the last wave's r tiles cut into s
     slices (s <= 16, each >= 64 deep for FP32 and >= 256 for the tensor
     paths), s minimising t_tile * (floor(T/G) + ceil(r*s/G)/s) + 3 us +
     2 * ws / bw (G units at once; bw 8 TB/s up to 64 MB of workspace, else
@@ -120,14 +120,16 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
     (256-byte rounded)."""
     rates = {("fp32", "direct"): 0.24e12, ("fp32", "tma"): 0.40e12,
              ("3xtf32", "direct"): 0.47e12, ("3xtf32", "pair"): 1.8e12,
-             ("tf32", "direct"): 0.55e12, ("tf32", "pair"): 3.0e12}
+             ("tf32", "direct"): 0.55e12, ("tf32", "pair"): 3.6e12}
     if pair_slots is None:
         pair_slots = sms // 2
     if mode == "fp32":
         kernels = [(bm, bn, feed, sms, 1) for (bm, bn) in ((256, 128), (128, 128))
                    for feed in ("direct", "tma")]
     else:
-        kernels = [(128, 128, "direct", sms, 1), (256, 128, "pair", pair_slots, 2)]
+        # the pair kernel: 256 x 128 tiles, 256 x 256 for TF32 with K >= 1536
+        wide = mode == "tf32" and K >= 1536
+        kernels = [(128, 128, "direct", sms, 1), (256, 256 if wide else 128, "pair", pair_slots, 2)]
     need = 0
     for bm, bn, feed, G, per_unit in kernels:
         T = Q * math.ceil(M / bm) * math.ceil(N / bn)
