@@ -51,7 +51,7 @@ extern "C" {
 /* Status codes returned by every entry point. */
 #define SGEMM_OK 0
 #define SGEMM_ERR_INVALID_ARG 1 /* a dimension, leading dimension, stride, pointer or mode */
-#define SGEMM_ERR_UNSUPPORTED 2 /* valid call this build cannot run (e.g. no sm_103 GPU)   */
+#define SGEMM_ERR_UNSUPPORTED 2 /* valid call the library cannot run here (no sm_103 GPU) */
 #define SGEMM_ERR_LAUNCH 3      /* the CUDA runtime refused a launch or attribute call    */
 #define SGEMM_ERR_TIMEOUT 4     /* a kernel's bounded internal wait ran out (device word) */
 #define SGEMM_ERR_SCRATCH_LIMIT 5 /* sgemm_batched_ex_noalloc: shape needs more than its scratch */

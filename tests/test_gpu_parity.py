@@ -35,7 +35,7 @@ def supported(mode):
     st = lib.sgemm_batched_ex(mode, 16, 16, 16, 1.0, a, 16, a, 16, 0.0, c, 16, 0, 0, 0, 0, 0, 1)
     torch.cuda.synchronize()
     if st == lib.SGEMM_ERR_UNSUPPORTED:
-        pytest.skip(f"mode {mode} not available in this build")
+        pytest.skip(f"mode {mode} not available on this device")
     assert st == lib.SGEMM_OK
 
 

@@ -22,7 +22,7 @@ from __future__ import annotations
 import numpy as np
 
 # name -> recipe.  dist_* is ("uniform",) or ("normal", sigma) or ("zeros",).
-CONFIGS = {
+RECIPES = {
     # small reference case
     "sgemm_256": dict(M=256, N=256, K=256, Q=1, seed=0, alpha=1.5, betas=(0.5,),
                       dist_ab=("uniform",), dist_c=("uniform",)),
@@ -53,7 +53,7 @@ def sweep_config(n: int) -> dict:
 def config(name: str) -> dict:
     if name.startswith("sweep_"):
         return sweep_config(int(name.split("_", 1)[1]))
-    return dict(CONFIGS[name])
+    return dict(RECIPES[name])
 
 
 def _draw(rng: np.random.Generator, dist: tuple, shape: tuple) -> np.ndarray:
