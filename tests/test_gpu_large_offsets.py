@@ -98,3 +98,34 @@ def test_a_operand_past_2_pow_31_elements(oracle_mod, mode, api):
     check_rows(oracle_mod, A[idx].cpu().numpy(), B.cpu().numpy(), C[idx].cpu().numpy(), 1.0)
     del A, B, C
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("tB", [1, 0])
+def test_half_path_past_2_pow_31_elements(oracle_mod, tB):
+    """The 16-bit-input path: C of 70000 x 32768 (> 2^31 elements) with K =
+    64, and A of 70000 x 32768 bf16 values (> 2^31) with N = 24; B read
+    directly (tB = 1) or copied transposed (tB = 0).  Integer data, sampled
+    rows bit-exact."""
+    import torch
+    import workloads
+    import dense_fp32_matrix_03_gb300 as lib
+    dev = torch.device("cuda", 0)
+    for M, N, K, seed in ((70000, 32768, 64, 7), (70000, 24, 32768, 9)):
+        A = int_tensor((M, K), seed, dev)
+        B = int_tensor((K, N), seed + 1, dev)
+        C = torch.empty((M, N), dtype=torch.float32, device=dev)
+        assert max(A.numel(), C.numel()) > 2 ** 31
+        Ah = A.to(torch.bfloat16)
+        Bh = (B.t().contiguous() if tB else B).to(torch.bfloat16)
+        ldb = K if tB else N
+        wsb = lib.sgemm_half_workspace_size("bf16", M, N, K, 0, tB, K, ldb, 1)
+        ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+        st = lib.sgemm_half_batched("bf16", M, N, K, 1.0, Ah, K, Bh, ldb, 0.0, C, N, 0, tB, 0, 0,
+                                    0, 1, ws, wsb)
+        assert st == lib.SGEMM_OK, lib.sgemm_status_string(st)
+        assert lib.sgemm_poll_error(None) == lib.SGEMM_OK
+        rows = sample(M, seed + 2)
+        idx = torch.tensor(rows, device=dev)
+        check_rows(oracle_mod, A[idx].cpu().numpy(), B.cpu().numpy(), C[idx].cpu().numpy(), 1.0)
+        del A, B, C, Ah, Bh, ws
+        torch.cuda.empty_cache()
