@@ -53,7 +53,8 @@ constexpr int kEpiWarp0 = 2;
 constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int NBAR = 2 * STAGES + 4 + 1;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NBAR * 8 + 16 + 1024;
+constexpr int EPI_BYTES = 4 * tc::kStageFloats * 4;  // epilogue staging (4 warps)
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + NBAR * 8 + 16 + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 static_assert(2 * BN <= static_cast<int>(kTmemCols), "TMEM columns");
 
@@ -132,7 +133,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(base + STAGES * STAGE_BYTES);
+    float4 *epi = reinterpret_cast<float4 *>(base + STAGES * STAGE_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + STAGES * STAGE_BYTES + EPI_BYTES);
     uint64_t *full = bars;                  // even CTA's: both CTAs' bytes
     uint64_t *empty = full + STAGES;        // per CTA: multicast commit
     uint64_t *acc_full = empty + STAGES;    // per CTA: multicast commit
@@ -260,23 +262,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------ epilogue (own CTA's rows)
         const int q = warp & 3;
-        const int row_in_tile = static_cast<int>(rank) * BM + q * 32 + lane;
+        const int r0 = static_cast<int>(rank) * BM + q * 32;  // this warp's first row
+        float4 *stage = epi + q * (tc::kStageFloats / 4);
         tc::Ring<2> acc;
         for (long long u = cid; u < p.num_units; u += ncl) {
+            const WorkUnit wu = work_unit(u, p);
+            const OutTile o = out_tile<PM, BN>(p, wu);
+            tc::prefetch_c_rows(o, r0, lane);
             int w = 1;
             if (lane == 0) w = wait_cl(&acc_full[acc.s], acc.ph, ab, kStatusWaitAcc, true);
             if (!__shfl_sync(0xffffffffu, w, 0)) break;
             drain_cl(&acc_full[acc.s], acc.ph, ab.limit);
             tc::tc_fence_after();
-            const WorkUnit wu = work_unit(u, p);
-            const OutTile o = out_tile<PM, BN>(p, wu);
             const uint32_t tbase =
                 tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc.s * BN);
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 float v[32];
                 tc::tmem_ld32(tbase + c0, v);
-                tc::store_chunk(o, row_in_tile, c0, v);
+                tc::store_chunk_staged(o, r0, c0, v, stage, lane);
             }
             tc::tc_fence_before();
             __syncwarp();

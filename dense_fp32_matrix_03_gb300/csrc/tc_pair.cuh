@@ -41,11 +41,12 @@
 #endif
 // the wide (256 x 256) configuration's sub-blocks per stage and ring depths
 // (measured on GB300, TF32 4092^3 nn / nt, TFLOP/s: 1/4/4 556/428, 1/5/4
-// 543/424, 1/4/6 561/431, 2/2/2 520/441, 2/2/3 526/442)
+// 543/424, 1/4/6 561/431, 2/2/2 520/441, 2/2/3 526/442; the epilogue's
+// staging buffer takes the room of the sixth split stage)
 #ifndef SG_TCP_WIDE_KSUB
 #define SG_TCP_WIDE_KSUB 1
 #define SG_TCP_WIDE_RAW 4
-#define SG_TCP_WIDE_SPLIT 6
+#define SG_TCP_WIDE_SPLIT 5
 #endif
 #ifndef SG_TCP_RAW3
 #if SG_TCP_KSUB == 2
@@ -109,8 +110,10 @@ struct Cfg {
     static constexpr int SUB_COLS = PLANES * BK;      // TMEM A columns of one sub-block
     static constexpr int A_COLS = KSUB * SUB_COLS;
     static constexpr int NBAR = 2 * RAW_STAGES + 2 * SPLIT_STAGES + 4 + 1;
-    static constexpr int SMEM_BYTES =
-        RAW_STAGES * RAW_BYTES + SPLIT_STAGES * SPLIT_BYTES + NBAR * 8 + 16 + 1024;
+    // the four epilogue warps' staging buffers (tc::store_chunk_staged)
+    static constexpr int EPI_BYTES = 4 * tc::kStageFloats * 4;
+    static constexpr int SMEM_BYTES = RAW_STAGES * RAW_BYTES + SPLIT_STAGES * SPLIT_BYTES +
+                                      EPI_BYTES + NBAR * 8 + 16 + 1024;
     static_assert(ACC_COLS + SPLIT_STAGES * A_COLS <= static_cast<int>(kTmemCols), "TMEM columns");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     // a sub-block's split planes: B_hi | B_lo
@@ -340,6 +343,7 @@ template <class C>
 struct Smem {
     uint8_t *raw;
     uint8_t *split;
+    float4 *epi;
     uint64_t *raw_full, *raw_empty, *split_full, *split_empty, *acc_full, *acc_empty, *mma_done;
     uint32_t *tmem_base;
     volatile int *abort_flag;
@@ -356,7 +360,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     Smem<C> sm;
     sm.raw = base;
     sm.split = base + C::RAW_STAGES * C::RAW_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm.split + C::SPLIT_STAGES * C::SPLIT_BYTES);
+    sm.epi = reinterpret_cast<float4 *>(sm.split + C::SPLIT_STAGES * C::SPLIT_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sm.epi) +
+                                                  C::EPI_BYTES);
     sm.raw_full = bars;
     sm.raw_empty = sm.raw_full + C::RAW_STAGES;
     sm.split_full = sm.raw_empty + C::RAW_STAGES;
@@ -556,23 +562,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------ epilogue (own CTA's rows)
         const int q = warp & 3;
-        const int row_in_tile = static_cast<int>(rank) * BM + q * 32 + lane;
+        const int r0 = static_cast<int>(rank) * BM + q * 32;  // this warp's first row
+        float4 *stage = sm.epi + q * (tc::kStageFloats / 4);
         Ring<C::ACC_BUFS> acc;
         for (long long u = cid; u < p.num_units; u += ncl) {
+            const WorkUnit wu = work_unit(u, p);
+            const OutTile o = out_tile<PM, C::BN>(p, wu);
+            tc::prefetch_c_rows(o, r0, lane);
             int w = 1;
             if (lane == 0) w = wait_cl(&sm.acc_full[acc.s], acc.ph, ab, kStatusWaitAcc, true);
             if (!__shfl_sync(0xffffffffu, w, 0)) break;
             drain_cl(&sm.acc_full[acc.s], acc.ph, ab.limit);
             tc::tc_fence_after();
-            const WorkUnit wu = work_unit(u, p);
-            const OutTile o = out_tile<PM, C::BN>(p, wu);
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc.s * C::BN);
 #pragma unroll 1
             for (int c0 = 0; c0 < C::BN; c0 += 32) {
                 float v[32];
                 tc::tmem_ld32(tbase + c0, v);
-                tc::store_chunk(o, row_in_tile, c0, v);
+                tc::store_chunk_staged(o, r0, c0, v, stage, lane);
             }
             tc::tc_fence_before();
             __syncwarp();

@@ -403,5 +403,97 @@ __device__ __forceinline__ void store_chunk(const OutTile &o, int r, int c0, con
     }
 }
 
+// ---- epilogue through a per-warp staging buffer --------------------------
+// A warp's accumulator chunk arrives one row per lane (TMEM lane = row), so a
+// direct store covers 32 rows x 16 B per warp instruction: 32 lines, half a
+// sector of each, and as many L1 wavefronts, which the converters' shared-
+// memory traffic then waits behind.  Transposed through 4 KB of shared
+// memory, each group of 8 lanes writes 128 contiguous bytes of one row (a
+// warp instruction covers 4 rows x 128 B, whole lines).  The 16-byte slots of
+// a staged row are XOR-swizzled by (row & 7), so both the row-per-lane
+// writes and the row-per-8-lanes reads are free of bank conflicts.
+constexpr int kStageFloats = 32 * 32;  // one warp's chunk
+
+// Asks L2 for the lines of C a warp's epilogue will read (rows [r0, r0 + 32)
+// of the tile, lane l row r0 + l), when beta != 0.  Issued as soon as the
+// tile is known, before its accumulator is ready, so that the epilogue's
+// loads find C in L2 instead of waiting on DRAM twice per chunk.  Only
+// addresses inside the tile's valid extent are touched.
+__device__ __forceinline__ void prefetch_c_rows(const OutTile &o, int r0, int lane)
+{
+    const int r = r0 + lane;
+    if (o.beta == 0.f || r >= o.rows || o.cols <= 0) return;
+    const float *row = o.base + static_cast<long long>(r) * o.ld;
+    for (int c = 0; c < o.cols; c += 32)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(row + c));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(row + o.cols - 1));
+}
+
+// out = alpha * v + beta * out for chunk [c0, c0 + 32) of rows [r0, r0 + 32)
+// (lane l holds row r0 + l in v; out is not read when beta == 0), masked at
+// the M/N edges; stage is this warp's kStageFloats-float buffer (16-byte
+// aligned).  After the transpose, lane l handles slot i = 0..7: row
+// r0 + 4 i + l / 8, columns c0 + 4 (l % 8) .. + 3, in two batches of four
+// slots whose loads of C are issued together, before their stores.
+__device__ __forceinline__ void store_chunk_staged(const OutTile &o, int r0, int c0,
+                                                   const float (&v)[32], float4 *stage, int lane)
+{
+    float4 *mine = stage + lane * 8;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        mine[j ^ (lane & 7)] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    __syncwarp();
+    const int g = lane & 7, col = c0 + 4 * g;
+    const bool full = o.vec4 && col + 4 <= o.cols;
+    const bool use_beta = o.beta != 0.f;
+    const long long step = 4 * o.ld;  // 4 rows
+    const int rl = r0 + (lane >> 3);
+    float *row = o.base + static_cast<long long>(rl) * o.ld + col;
+#pragma unroll
+    for (int h = 0; h < 8; h += 4) {  // two batches of four slots
+        float4 old[4];
+        if (use_beta) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float *src = row + i * step;
+                old[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (rl + 4 * (h + i) >= o.rows) continue;
+                if (full) {
+                    old[i] = *reinterpret_cast<const float4 *>(src);
+                } else {
+                    if (col < o.cols) old[i].x = src[0];
+                    if (col + 1 < o.cols) old[i].y = src[1];
+                    if (col + 2 < o.cols) old[i].z = src[2];
+                    if (col + 3 < o.cols) old[i].w = src[3];
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int rr = 4 * (h + i) + (lane >> 3);
+            const float4 a = stage[rr * 8 + (g ^ (rr & 7))];
+            if (rl + 4 * (h + i) >= o.rows) continue;
+            float4 x = make_float4(o.alpha * a.x, o.alpha * a.y, o.alpha * a.z, o.alpha * a.w);
+            if (use_beta) {
+                x.x = fmaf(o.beta, old[i].x, x.x);
+                x.y = fmaf(o.beta, old[i].y, x.y);
+                x.z = fmaf(o.beta, old[i].z, x.z);
+                x.w = fmaf(o.beta, old[i].w, x.w);
+            }
+            float *dst = row + i * step;
+            if (full) {
+                *reinterpret_cast<float4 *>(dst) = x;
+            } else {
+                if (col < o.cols) dst[0] = x.x;
+                if (col + 1 < o.cols) dst[1] = x.y;
+                if (col + 2 < o.cols) dst[2] = x.z;
+                if (col + 3 < o.cols) dst[3] = x.w;
+            }
+        }
+        row += 4 * step;
+    }
+    __syncwarp();  // the next chunk reuses the buffer
+}
+
 }  // namespace tc
 }  // namespace sg
