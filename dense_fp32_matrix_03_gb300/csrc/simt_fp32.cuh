@@ -567,6 +567,25 @@ __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem
     long long it = 0;  // k-blocks consumed so far by this CTA
     for (long long u = blockIdx.x; u < p.num_units; u += gridDim.x) {
         const WorkUnit wu = work_unit(u, p);
+        // out = C, or this slice's workspace slot with alpha 1, beta 0
+        const OutTile o = out_tile<BM, BN>(p, wu);
+        if (o.beta != 0.f) {
+            // ask L2 for this lane's lines of C now, so that the epilogue's
+            // loads do not wait on DRAM (valid addresses only)
+#pragma unroll
+            for (int wm = 0; wm < WMITER; ++wm)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = row_of(wm, i);
+                    if (r >= o.rows) continue;
+#pragma unroll
+                    for (int wn = 0; wn < WNITER; ++wn) {
+                        const int c = col_of(wn, 0);
+                        if (c < o.cols)
+                            asm volatile("prefetch.global.L2 [%0];" ::"l"(o.base + r * o.ld + c));
+                    }
+                }
+        }
         Acc<Cfg, pair_dim<A_KIN, B_KIN>()> accp;
         accp.zero();
 
@@ -593,8 +612,8 @@ __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem
         accp.to_float(acc);
 
         // ---- epilogue: out = alpha * acc + beta * out, masked at the M/N
-        // edges (out = C, or this slice's workspace slot with alpha 1, beta 0)
-        const OutTile o = out_tile<BM, BN>(p, wu);
+        // edges.  A row's loads of C are all issued before its stores (the
+        // compiler may not move a load of C past a store to C itself).
         const bool use_beta = o.beta != 0.f;
 #pragma unroll
         for (int wm = 0; wm < WMITER; ++wm)
@@ -603,6 +622,35 @@ __device__ __forceinline__ void simt_consumer(const GemmParams &p, uint8_t *smem
                 const int r = row_of(wm, i);
                 if (r >= o.rows) continue;
                 float *orow = o.base + r * o.ld;
+                if (!B_KIN && o.vec4 && use_beta) {
+                    float4 old[WNITER];
+#pragma unroll
+                    for (int wn = 0; wn < WNITER; ++wn) {
+                        const int c0 = col_of(wn, 0);
+                        old[wn] = c0 + 3 < o.cols ? *reinterpret_cast<const float4 *>(orow + c0)
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int wn = 0; wn < WNITER; ++wn) {
+                        const float *av = &acc[wm * 4 + i][wn * 4];
+                        const int c0 = col_of(wn, 0);
+                        if (c0 + 3 < o.cols) {
+                            float4 v;
+                            v.x = fmaf(o.beta, old[wn].x, o.alpha * av[0]);
+                            v.y = fmaf(o.beta, old[wn].y, o.alpha * av[1]);
+                            v.z = fmaf(o.beta, old[wn].z, o.alpha * av[2]);
+                            v.w = fmaf(o.beta, old[wn].w, o.alpha * av[3]);
+                            *reinterpret_cast<float4 *>(orow + c0) = v;
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const int c = c0 + j;
+                                if (c < o.cols) orow[c] = fmaf(o.beta, orow[c], o.alpha * av[j]);
+                            }
+                        }
+                    }
+                    continue;
+                }
 #pragma unroll
                 for (int wn = 0; wn < WNITER; ++wn) {
                     const float *av = &acc[wm * 4 + i][wn * 4];

@@ -53,7 +53,8 @@ struct Cfg {
     static constexpr int A_COLS = PLANES * BK;
     static constexpr int STAGES = (static_cast<int>(kTmemCols) - ACC_COLS) / A_COLS;
     static constexpr int NBAR = 2 * STAGES + 4 + 1;
-    static constexpr int SMEM_BYTES = STAGES * SPLIT_BYTES + NBAR * 8 + 16 + 1024;
+    static constexpr int EPI_BYTES = 4 * tc::kStageFloats * 4;  // epilogue staging (4 warps)
+    static constexpr int SMEM_BYTES = STAGES * SPLIT_BYTES + EPI_BYTES + NBAR * 8 + 16 + 1024;
     static constexpr int OFF_BHI = 0, OFF_BLO = B_BYTES;
     static_assert(BN == 128, "one UMMA N per tile (BN = 128 keeps two accumulators in TMEM)");
     static_assert(STAGES >= 2, "TMEM columns");
@@ -298,6 +299,7 @@ __device__ __forceinline__ void store_b(const float (&x)[32], uint32_t hi_a, uin
 template <class C>
 struct Smem {
     uint8_t *split;  // STAGES x (B_hi | B_lo)
+    float4 *epi;     // the epilogue warps' staging buffers
     uint64_t *split_full, *split_empty, *acc_full, *acc_empty, *mma_done;
     uint32_t *tmem_base;
     volatile int *abort_flag;
@@ -311,7 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1) tcd_sgemm_kernel(const GemmParams
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     Smem<C> sm;
     sm.split = base;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(base + C::STAGES * C::SPLIT_BYTES);
+    sm.epi = reinterpret_cast<float4 *>(base + C::STAGES * C::SPLIT_BYTES);
+    uint64_t *bars =
+        reinterpret_cast<uint64_t *>(base + C::STAGES * C::SPLIT_BYTES + C::EPI_BYTES);
     sm.split_full = bars;
     sm.split_empty = sm.split_full + C::STAGES;
     sm.acc_full = sm.split_empty + C::STAGES;
@@ -459,24 +463,26 @@ __global__ void __launch_bounds__(kThreads, 1) tcd_sgemm_kernel(const GemmParams
     } else {
         // ------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int row_in_tile = q * 32 + lane;
+        const int r0 = q * 32;  // this warp's first row
+        float4 *stage = sm.epi + q * (tc::kStageFloats / 4);
         tc::Ring<2> acc;
         for (long long u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+            const WorkUnit wu = work_unit(u, p);
+            // C, or this slice's workspace slot (unscaled) when the tile is split
+            const OutTile o = out_tile<BM, C::BN>(p, wu);
+            tc::prefetch_c_rows(o, r0, lane);
             int w = 1;
             if (lane == 0) w = mbar_wait(&sm.acc_full[acc.s], acc.ph, ab, kStatusWaitAcc, true);
             if (!__shfl_sync(0xffffffffu, w, 0)) break;
             mbar_drain(&sm.acc_full[acc.s], acc.ph, ab.limit);
             tc::tc_fence_after();
-            const WorkUnit wu = work_unit(u, p);
-            // C, or this slice's workspace slot (unscaled) when the tile is split
-            const OutTile o = out_tile<BM, C::BN>(p, wu);
             const uint32_t tbase =
                 tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc.s * C::BN);
 #pragma unroll 1
             for (int c0 = 0; c0 < C::BN; c0 += 32) {
                 float v[32];
                 tc::tmem_ld32(tbase + c0, v);  // all lanes take part, rows in range or not
-                tc::store_chunk(o, row_in_tile, c0, v);
+                tc::store_chunk_staged(o, r0, c0, v, stage, lane);
             }
             tc::tc_fence_before();
             __syncwarp();

@@ -368,41 +368,6 @@ __device__ __forceinline__ void convert_b_tile(const uint8_t *raw, uint8_t *hi, 
     }
 }
 
-// Stores 32 consecutive columns [c0, c0 + 32) of tile row r: out = alpha * v
-// + beta * out (out not read when beta == 0), masked at the M/N edges.
-__device__ __forceinline__ void store_chunk(const OutTile &o, int r, int c0, const float (&v)[32])
-{
-    if (r >= o.rows) return;
-    float *orow = o.base + static_cast<long long>(r) * o.ld;
-    const bool use_beta = o.beta != 0.f;
-    if (o.vec4 && c0 + 32 <= o.cols) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-            float4 x = make_float4(o.alpha * v[j], o.alpha * v[j + 1], o.alpha * v[j + 2],
-                                   o.alpha * v[j + 3]);
-            float4 *dst = reinterpret_cast<float4 *>(orow + c0 + j);
-            if (use_beta) {
-                const float4 old = *dst;
-                x.x = fmaf(o.beta, old.x, x.x);
-                x.y = fmaf(o.beta, old.y, x.y);
-                x.z = fmaf(o.beta, old.z, x.z);
-                x.w = fmaf(o.beta, old.w, x.w);
-            }
-            *dst = x;
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int c = c0 + j;
-            if (c < o.cols) {
-                float x = o.alpha * v[j];
-                if (use_beta) x = fmaf(o.beta, orow[c], x);
-                orow[c] = x;
-            }
-        }
-    }
-}
-
 // ---- epilogue through a per-warp staging buffer --------------------------
 // A warp's accumulator chunk arrives one row per lane (TMEM lane = row), so a
 // direct store covers 32 rows x 16 B per warp instruction: 32 lines, half a
