@@ -259,15 +259,16 @@ int min_slice_k(int mode) { return mode == SGEMM_MODE_FP32 ? 64 : 256; }
 
 // FLOP/s per multiprocessor each kernel sustains on GB300 (measured at
 // 4092^3 with TMA-fed operands -- the FP32 kernel, the tensor-core pair
-// kernel -- and on the ragged 1000 x 1500 x 777 case, whose A TMA cannot
-// describe: the FP32 kernel's cp.async fallback, the tensor-core direct
-// kernel).
+// kernel, the planes route's product alone -- and on the ragged
+// 1000 x 1500 x 777 case, whose A TMA cannot describe: the FP32 kernel's
+// cp.async fallback, the tensor-core direct kernel).
 double path_rate_per_sm(int mode, int feed)
 {
     if (mode == SGEMM_MODE_FP32) return feed == kFeedDirect ? 0.24e12 : 0.40e12;
-    if (mode == SGEMM_MODE_3XTF32) return feed == kFeedDirect ? 0.47e12 : 1.8e12;
+    if (mode == SGEMM_MODE_3XTF32)
+        return feed == kFeedDirect ? 0.47e12 : feed == kFeedPlanes ? 2.45e12 : 1.8e12;
     if (mode == kModeHalf) return 11.0e12;
-    return feed == kFeedDirect ? 0.55e12 : 3.6e12;
+    return feed == kFeedDirect ? 0.55e12 : feed == kFeedPlanes ? 6.4e12 : 3.6e12;
 }
 
 size_t splitk_workspace_bytes(long long split_tiles, int splits, int bm, int bn)
@@ -279,16 +280,18 @@ size_t splitk_workspace_bytes(long long split_tiles, int splits, int bm, int bn)
 SplitPlan choose_plan(long long num_tiles, int K, int slots, int mode, int bm, int bn, int feed,
                       size_t budget)
 {
-    SplitPlan best{1, num_tiles, 0};
+    SplitPlan best{1, num_tiles, 0, 0.0};
     if (num_tiles <= 0 || slots <= 0) return best;
     const int num_sms = slots;  // units running at once
     const long long full = num_tiles / num_sms, rem = num_tiles % num_sms;
+    const double unit_rate =
+        path_rate_per_sm(mode, feed) * ((feed == kFeedPair || feed == kFeedPlanes) ? 2 : 1);
+    const double t_tile = 2.0 * bm * bn * static_cast<double>(K) / unit_rate;
+    best.seconds = t_tile * static_cast<double>(full + (rem ? 1 : 0));
     if (rem == 0) return best;
     long long smax = K / min_slice_k(mode);
     if (smax > kMaxSplits) smax = kMaxSplits;
-    const double unit_rate = path_rate_per_sm(mode, feed) * (feed == kFeedPair ? 2 : 1);
-    const double t_tile = 2.0 * bm * bn * static_cast<double>(K) / unit_rate;
-    const double t_whole = t_tile * static_cast<double>(full + 1);
+    const double t_whole = best.seconds;
     double best_t = t_whole;
     for (int s = 2; s <= smax; ++s) {
         const size_t ws = splitk_workspace_bytes(rem, s, bm, bn);
@@ -299,10 +302,10 @@ SplitPlan choose_plan(long long num_tiles, int K, int slots, int mode, int bm, i
                          3e-6 + 2.0 * static_cast<double>(ws) / bw;
         if (t < best_t) {
             best_t = t;
-            best = SplitPlan{s, full * num_sms, ws};
+            best = SplitPlan{s, full * num_sms, ws, t};
         }
     }
-    if (best.splits > 1 && best_t > 0.99 * t_whole) best = SplitPlan{1, num_tiles, 0};
+    if (best.splits > 1 && best_t > 0.99 * t_whole) best = SplitPlan{1, num_tiles, 0, t_whole};
     return best;
 }
 
@@ -357,7 +360,7 @@ namespace {
 // entry point's rule (see one_wave_plan).
 SplitPlan plan_query(int mode, int M, int N, int K, int Q, bool one_wave)
 {
-    const SplitPlan none{1, 0, 0};
+    const SplitPlan none{1, 0, 0, 0.0};
     if (mode == SGEMM_MODE_DEFAULT) mode = g_default_mode.load();
     if (mode != SGEMM_MODE_FP32 && mode != SGEMM_MODE_3XTF32 && mode != SGEMM_MODE_TF32) return none;
     if (M <= 0 || N <= 0 || K <= 0 || Q <= 0) return none;
@@ -370,11 +373,15 @@ SplitPlan plan_query(int mode, int M, int N, int K, int Q, bool one_wave)
     // dimensions the query does not take: plan for every kernel the mode
     // may run (FP32: the two tile shapes, each TMA-fed or not; tensor
     // cores: the direct kernel's 128 x 128 tiles, the pair kernel's 256 x 128).
-    for (int shape = 0; shape < 2; ++shape) {
+    for (int shape = 0; shape < (mode == SGEMM_MODE_FP32 ? 2 : 3); ++shape) {
         int bm = 0, bn = 0, slots = sms;
         int feeds[2] = {kFeedDirect, kFeedTma};
         if (mode == SGEMM_MODE_FP32) {
             simt_tile_dims(shape == 1, bm, bn);
+        } else if (shape == 2) {  // the planes route's 256 x 256 pair tiles
+            bm = bn = 256;
+            slots = tc_pair_slots(sms);
+            feeds[0] = feeds[1] = kFeedPlanes;
         } else {
             tc_tile_dims(mode, K, shape == 1, bm, bn);
             if (shape == 1) {
@@ -386,7 +393,7 @@ SplitPlan plan_query(int mode, int M, int N, int K, int Q, bool one_wave)
         }
         const long long tiles =
             static_cast<long long>(Q) * ((M + bm - 1) / bm) * ((N + bn - 1) / bn);
-        SplitPlan sp{1, tiles, 0};
+        SplitPlan sp{1, tiles, 0, 0.0};
         if (!one_wave) {
             for (int f = 0; f < 2; ++f) {
                 const SplitPlan t =
@@ -400,7 +407,7 @@ SplitPlan plan_query(int mode, int M, int N, int K, int Q, bool one_wave)
             if (s > kMaxSplits) s = kMaxSplits;
             if (s >= 2)
                 sp = SplitPlan{static_cast<int>(s), 0,
-                               splitk_workspace_bytes(tiles, static_cast<int>(s), bm, bn)};
+                               splitk_workspace_bytes(tiles, static_cast<int>(s), bm, bn), 0.0};
         }
         if (sp.ws_bytes > out.ws_bytes) out = sp;
     }
@@ -627,12 +634,43 @@ int run(int mode, int M, int N, int K, float alpha, const float *A, int lda, con
         if (rc != SGEMM_OK) return rc;
         return launch_simt(plan);
     }
+    bool taken = false;
+    rc = run_planes(plan, taken);
+    if (taken || rc != SGEMM_OK) return rc;
     rc = repack_for_tc(plan);
     if (rc != SGEMM_OK) return rc;
     return launch_tc(plan);
 }
 
 }  // namespace
+
+namespace sg {
+
+size_t workspace_size_no_planes(int mode, int M, int N, int K, int Q)
+{
+    const size_t split = preferred_plan(mode, M, N, K, Q).ws_bytes;
+    if (mode == SGEMM_MODE_DEFAULT) mode = g_default_mode.load();
+    if (M <= 0 || N <= 0 || K <= 0 || Q <= 0) return split;
+    if (mode == SGEMM_MODE_3XTF32 || mode == SGEMM_MODE_TF32) {
+        // room for 128-byte-pitched copies of operands TMA cannot describe
+        // (pointers, leading dimensions and layouts are not known here)
+        auto copy = [Q, K](long long rows) {
+            const long long r32k = rows * ((K + 31) / 32 * 32);
+            const long long kr32 = static_cast<long long>(K) * ((rows + 31) / 32 * 32);
+            return round256(static_cast<size_t>(Q) * (r32k > kr32 ? r32k : kr32) * 4);
+        };
+        return split + copy(M) + copy(N);
+    }
+    if (mode != SGEMM_MODE_FP32) return split;
+    // room for the transposed operands the FP32 path may make (the layout
+    // is not known here; a broadcast operand would need less)
+    size_t repack = 0;
+    if (N >= kRepackMinN) repack += repack_bytes(M, K, Q, false);
+    if (M >= kRepackMinM) repack += repack_bytes(N, K, Q, false);
+    return split + repack;
+}
+
+}  // namespace sg
 
 extern "C" {
 
@@ -675,26 +713,17 @@ int sgemm_batched_ex_ws(int mode, int M, int N, int K, float alpha, const float 
 
 size_t sgemm_workspace_size(int mode, int M, int N, int K, int Q)
 {
-    const size_t split = preferred_plan(mode, M, N, K, Q).ws_bytes;
+    const size_t base = workspace_size_no_planes(mode, M, N, K, Q);
     if (mode == SGEMM_MODE_DEFAULT) mode = g_default_mode.load();
-    if (M <= 0 || N <= 0 || K <= 0 || Q <= 0) return split;
-    if (mode == SGEMM_MODE_3XTF32 || mode == SGEMM_MODE_TF32) {
-        // room for 128-byte-pitched copies of operands TMA cannot describe
-        // (pointers, leading dimensions and layouts are not known here)
-        auto copy = [Q, K](long long rows) {
-            const long long r32k = rows * ((K + 31) / 32 * 32);
-            const long long kr32 = static_cast<long long>(K) * ((rows + 31) / 32 * 32);
-            return round256(static_cast<size_t>(Q) * (r32k > kr32 ? r32k : kr32) * 4);
-        };
-        return split + copy(M) + copy(N);
-    }
-    if (mode != SGEMM_MODE_FP32) return split;
-    // room for the transposed operands the FP32 path may make (the layout
-    // is not known here; a broadcast operand would need less)
-    size_t repack = 0;
-    if (N >= kRepackMinN) repack += repack_bytes(M, K, Q, false);
-    if (M >= kRepackMinM) repack += repack_bytes(N, K, Q, false);
-    return split + repack;
+    if (M <= 0 || N <= 0 || K <= 0 || Q <= 0) return base;
+    if (mode != SGEMM_MODE_3XTF32 && mode != SGEMM_MODE_TF32) return base;
+    // where the planes route pays for this shape (planes_pay): both
+    // operands' planes (every batch entry stored) and the split plan of its
+    // tiles, or the copies and plans of the other routes, whichever is larger
+    if (!planes_pay(mode, M, N, K, Q, Q, Q, num_sms_or_zero())) return base;
+    const size_t planes =
+        planes_bytes(mode, M, N, K, Q, Q) + preferred_plan(mode, M, N, K, Q).ws_bytes;
+    return planes > base ? planes : base;
 }
 
 int sgemm_set_default_mode(int mode)

@@ -1,12 +1,12 @@
 // half.cu -- host side of the 16-bit-input path (bf16 / fp16 operands, fp32
 // accumulation and output): argument checks, copies of operands the kernel
-// cannot read directly, the split plan and the launch of tc_half.cuh.
+// cannot read directly, the split plan and the launch of the tc_ss.cuh kernel.
 #include <atomic>
 #include <cstring>
 
 #include "../../include/sgemm.h"
 #include "internal.h"
-#include "tc_half.cuh"
+#include "tc_ss.cuh"
 
 namespace sg {
 
@@ -53,14 +53,15 @@ int half_slots(int num_sms)
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return num_sms / 2;
     const int cached = g_half_slots[dev].load();
     if (cached > 0) return cached;
-    auto kern = tch::tch_gemm_kernel<true>;
+    using KD = tcs::KindHalf<true>;
+    auto kern = tcs::tcs_gemm_kernel<KD>;
     int n = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             tch::SMEM_BYTES) == cudaSuccess) {
+                             tcs::Shape<KD>::SMEM_BYTES) == cudaSuccess) {
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(static_cast<unsigned>(2 * (num_sms / 2)));
-        cfg.blockDim = dim3(tch::kThreads);
-        cfg.dynamicSmemBytes = tch::SMEM_BYTES;
+        cfg.blockDim = dim3(tcs::kThreads);
+        cfg.dynamicSmemBytes = tcs::Shape<KD>::SMEM_BYTES;
         if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();
@@ -73,17 +74,7 @@ int half_slots(int num_sms)
 template <bool BF16>
 int launch_half(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB, int slots)
 {
-    auto kern = tch::tch_gemm_kernel<BF16>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             tch::SMEM_BYTES) != cudaSuccess)
-        return SGEMM_ERR_LAUNCH;
-    long long pairs = plan.p.num_units;
-    if (pairs > slots) pairs = slots;
-    kern<<<static_cast<unsigned>(2 * pairs), tch::kThreads, tch::SMEM_BYTES, plan.stream>>>(
-        tmA, tmB, plan.p);
-    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
-    note_launch();
-    return plan.p.splits > 1 ? launch_fixup(plan, tch::PM, tch::BN) : SGEMM_OK;
+    return launch_ss<tcs::KindHalf<BF16>>(plan, tmA, tmB, slots);
 }
 
 bool valid_type(int type) { return type == SGEMM_HALF_BF16 || type == SGEMM_HALF_FP16; }
@@ -106,9 +97,9 @@ size_t sgemm_half_workspace_size(int type, int M, int N, int K, int transA, int 
     size_t bytes = 0;
     if (!direct_layout(!transA, lda, M, K)) bytes += copy_bytes(M, K, Q, false);
     if (!direct_layout(transB != 0, ldb, N, K)) bytes += copy_bytes(N, K, Q, false);
-    const long long tiles = static_cast<long long>(Q) * ((M + tch::PM - 1) / tch::PM) *
-                            ((N + tch::BN - 1) / tch::BN);
-    const SplitPlan sp = choose_plan(tiles, K, half_slots(num_sms), kModeHalf, tch::PM, tch::BN,
+    const long long tiles = static_cast<long long>(Q) * ((M + tcs::PM - 1) / tcs::PM) *
+                            ((N + tcs::BN - 1) / tcs::BN);
+    const SplitPlan sp = choose_plan(tiles, K, half_slots(num_sms), kModeHalf, tcs::PM, tcs::BN,
                                      kFeedPair, ~static_cast<size_t>(0));
     return bytes + sp.ws_bytes;
 }
@@ -190,10 +181,11 @@ int sgemm_half_batched(int type, int M, int N, int K, float alpha, const void *A
     p.c_vec4 = aligned16(C) && ldc % 4 == 0 && (p.sC % 4) == 0;
     p.status = status;
     p.wait_limit = kWaitLimitCycles;
-    p.k_blocks = (K + tch::STAGE_K - 1) / tch::STAGE_K;
+    constexpr int SK = tcs::Shape<tcs::KindHalf<true>>::STAGE_K;
+    p.k_blocks = (K + SK - 1) / SK;
     p.group_m = kGroupM;
-    p.tiles_m = (M + tch::PM - 1) / tch::PM;
-    p.tiles_n = (N + tch::BN - 1) / tch::BN;
+    p.tiles_m = (M + tcs::PM - 1) / tcs::PM;
+    p.tiles_n = (N + tcs::BN - 1) / tcs::BN;
     p.num_tiles = static_cast<long long>(Q) * p.tiles_m * p.tiles_n;
     plan.mode = kModeHalf;
     plan.num_sms = num_sms;
@@ -206,11 +198,11 @@ int sgemm_half_batched(int type, int M, int N, int K, float alpha, const void *A
     std::memset(&tmA, 0, sizeof(tmA));
     std::memset(&tmB, 0, sizeof(tmB));
     const bool bf16 = type == SGEMM_HALF_BF16;
-    if (!encode_operand16(&tmA, pa, bf16, M, K, la, Q, xa, tch::BM) ||
-        !encode_operand16(&tmB, pb, bf16, N, K, lb, Q, xb, tch::HN))
+    if (!encode_operand16(&tmA, pa, bf16, M, K, la, Q, xa, tcs::BM) ||
+        !encode_operand16(&tmB, pb, bf16, N, K, lb, Q, xb, tcs::HN))
         return SGEMM_ERR_UNSUPPORTED;
     const int slots = half_slots(num_sms);
-    rc = plan_splits(plan, tch::PM, tch::BN, kFeedPair, slots);
+    rc = plan_splits(plan, tcs::PM, tcs::BN, kFeedPair, slots);
     if (rc != SGEMM_OK) return rc;
     return bf16 ? launch_half<true>(plan, tmA, tmB, slots) : launch_half<false>(plan, tmA, tmB, slots);
 }

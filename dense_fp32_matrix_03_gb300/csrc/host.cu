@@ -104,8 +104,8 @@ bool make_layout(int mode, int M, int N, int K, int transA, int transB, int pane
     L->panels = static_cast<int>((M + L->panel - 1) / L->panel);
     if (L->panels > kMaxPanels) return false;
     const int last = M - (L->panels - 1) * L->panel;
-    size_t w1 = sgemm_workspace_size(mode, L->panel, N, K, 1);
-    size_t w2 = sgemm_workspace_size(mode, last, N, K, 1);
+    size_t w1 = workspace_size_no_planes(mode, L->panel, N, K, 1);
+    size_t w2 = workspace_size_no_planes(mode, last, N, K, 1);
     L->ws_bytes = w1 > w2 ? w1 : w2;
     L->offA = 0;
     L->offB = align256(L->offA + 4ull * rowsA * L->ldA);

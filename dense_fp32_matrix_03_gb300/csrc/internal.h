@@ -66,14 +66,18 @@ int check_shape(int M, int N, int K, float alpha, const void *A, int lda, const 
 constexpr int kMaxSplits = 16;
 // How a kernel is fed: operands loaded by the threads themselves (the FP32
 // kernel's cp.async producer, the tensor-core direct kernel), by TMA on one
-// CTA per unit, or by TMA on a CTA pair per unit (two multiprocessors).
-enum Feed { kFeedDirect = 0, kFeedTma = 1, kFeedPair = 2 };
+// CTA per unit, by TMA on a CTA pair per unit (two multiprocessors), or, on
+// a CTA pair, as TF32 planes made by a pass before the product (planes.cu).
+enum Feed { kFeedDirect = 0, kFeedTma = 1, kFeedPair = 2, kFeedPlanes = 3 };
 struct SplitPlan {
     int splits;          // 1 = no split
     long long dp_tiles;  // tiles computed whole (they come first in unit order)
     size_t ws_bytes;     // workspace the plan needs
+    double seconds;      // the model's time for the plan (0 when not modelled)
 };
 int min_slice_k(int mode);
+// FLOP/s per multiprocessor of the kernel a mode and feed run (GB300).
+double path_rate_per_sm(int mode, int feed);
 size_t splitk_workspace_bytes(long long split_tiles, int splits, int bm, int bn);
 // slots: units that run at once (multiprocessors, or CTA pairs for kFeedPair).
 SplitPlan choose_plan(long long num_tiles, int K, int slots, int mode, int bm, int bn, int feed,
@@ -94,6 +98,29 @@ int tc_pair_slots(int num_sms);
 int launch_tc_pair(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB, int slots);
 // Enqueues the split-K fix-up for a launch whose plan split (bm x bn tiles).
 int launch_fixup(Plan &plan, int bm, int bn);
+// Workspace the TF32 planes of a 3xTF32 / TF32 call take (QA, QB: stored
+// batch entries of A and B, 1 when broadcast).
+size_t planes_bytes(int mode, long long M, long long N, long long K, int QA, int QB);
+// The tensor-core paths' planes route (planes.cu): when the plan's workspace
+// holds the planes, enqueues the pass over both operands and the product
+// (taken = true) and returns its status; otherwise leaves the plan alone
+// (taken = false).
+int run_planes(Plan &plan, bool &taken);
+// Whether the planes route is expected to beat the pair kernel for this
+// shape (QA, QB: stored batch entries of A and B; num_sms 0: unknown, then
+// false).  Each route's product takes the split planner's modelled time for
+// its tiles (choose_plan: 256 x 256 pair tiles at the planes rate; the pair
+// kernel's tiles at its rate), and the planes route adds its pass, which
+// moves (QA * M + QB * N) * K * 4 * (1 + planes) bytes at 5.5 TB/s, and
+// 10 us for its two extra launches and the shorter grid's ramp (fitted on
+// GB300: 2048^3 runs faster on the pair kernel, 4096^3 on the planes).
+bool planes_pay(int mode, long long M, long long N, long long K, int QA, int QB, int Q,
+                int num_sms);
+// Multiprocessors of the current device, 0 when there is no usable one.
+int num_sms_or_zero();
+// sgemm_workspace_size without room for the planes (the host-buffer entry's
+// per-panel calls would rewrite all of B once per panel).
+size_t workspace_size_no_planes(int mode, int M, int N, int K, int Q);
 // The plan sgemm_workspace_size reports for a call (no budget), or splits = 1.
 SplitPlan preferred_plan(int mode, int M, int N, int K, int Q);
 // The plan of the allocation-free entry point: a grid of at most half as many

@@ -1,20 +1,26 @@
-// tc_half.cuh -- GEMM with 16-bit inputs (bf16 or fp16) and fp32
-// accumulation and output on CTA pairs: C = alpha * op(A) @ op(B) + beta * C.
+// tc_ss.cuh -- tensor-core GEMM on CTA pairs with both operands read by the
+// MMA from shared memory, fp32 accumulation and output:
+// C = alpha * op(A) @ op(B) + beta * C.
 //
-// The contraction the pages point to for tensor cores ("From 1% to 94% of
-// cuBLAS, one kernel at a time", future work: tensor cores with narrower
-// inputs) with operands that need no conversion: TMA stages both operands,
-// K-major with the 128-byte swizzle (64 values of 16 bits per row), straight
-// into the layout tcgen05.mma reads, and the MMA reads both from shared
-// memory.  Products of 16-bit values are exact in fp32; the sum is
-// accumulated in fp32 in TMEM.
+// Operands arrive ready for the MMA, K-major, and TMA stages them with the
+// 128-byte swizzle straight into the layout tcgen05.mma reads -- no
+// conversion inside the kernel:
+//   - 16-bit inputs (bf16 or fp16, kind::f16): the contraction the pages
+//     point to for tensor cores with narrower inputs ("From 1% to 94% of
+//     cuBLAS, one kernel at a time", future work); products of 16-bit values
+//     are exact in fp32;
+//   - fp32 operands already in TF32 form (kind::tf32), made by a pass over
+//     the operands into the caller's workspace: one plane rounded to the
+//     nearest TF32 value (TF32), or the hi and lo planes of the 3xTF32 split,
+//     multiplied as lo*hi + hi*lo + hi*hi (3xTF32).
 //
-// Tile 256 x 256 per CTA pair (cta_group::2, M = 256, N = 256, K = 16): each
-// CTA stages its 128 rows of A and its 128 of the tile's 256 rows of B^T, a
-// stage being 128 k (two 64-wide TMA boxes per operand, 64 KB per CTA),
-// three stages deep.  Both CTAs' TMA loads complete on the even CTA's
-// barrier (cta_group::2 form, which may name the peer's barrier); one thread
-// of the even CTA issues every MMA and multicasts its commits (stage free,
+// Tile 256 x 256 per CTA pair (cta_group::2, M = 256, N = 256): each CTA
+// stages its 128 rows of A and its 128 of the tile's 256 rows of B^T.  A
+// stage is 64 KB per CTA: two 128-byte boxes of one plane (128 k of 16-bit
+// values, 64 k of fp32), or one box of each of two planes (32 k); three
+// stages deep.  Both CTAs' TMA loads complete on the even CTA's barrier
+// (cta_group::2 form, which may name the peer's barrier); one thread of the
+// even CTA issues every MMA and multicasts its commits (stage free,
 // accumulator full) to both CTAs.  TMEM: two 256-column fp32 accumulators
 // per CTA (double buffered, so the epilogue overlaps the next tile).
 //
@@ -23,10 +29,12 @@
 // bounded; the CTAs meet at a cluster barrier before freeing TMEM.
 #pragma once
 
+#include "../../include/sgemm.h"
+#include "internal.h"
 #include "tc_pair.cuh"
 
 namespace sg {
-namespace tch {
+namespace tcs {
 
 using tcp::arrive_on;
 using tcp::cluster_sync;
@@ -41,31 +49,46 @@ constexpr int BM = 128;      // rows of C per CTA
 constexpr int PM = 2 * BM;   // rows per pair tile (the MMA's M)
 constexpr int BN = 256;      // columns per pair tile (the MMA's N)
 constexpr int HN = BN / 2;   // rows of B^T each CTA holds
-constexpr int BKH = 64;      // 16-bit k per 128-byte swizzle row (one TMA box)
-constexpr int UKH = 16;      // k per kind::f16 MMA
-constexpr int KSUB = 2;      // boxes per stage
-constexpr int STAGE_K = KSUB * BKH;
-constexpr int SUB_A = BM * BKH * 2;  // 16 KB
-constexpr int SUB_B = HN * BKH * 2;  // 16 KB
-constexpr int STAGE_BYTES = KSUB * (SUB_A + SUB_B);  // per CTA
+constexpr int SUB_A = BM * 128;  // one 128-byte box of A: 16 KB
+constexpr int SUB_B = HN * 128;  // one box of B: 16 KB
 constexpr int STAGES = 3;
 constexpr int kEpiWarp0 = 2;
 constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int NBAR = 2 * STAGES + 4 + 1;
 constexpr int EPI_BYTES = 4 * tc::kStageFloats * 4;  // epilogue staging (4 warps)
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + NBAR * 8 + 16 + 1024;
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 static_assert(2 * BN <= static_cast<int>(kTmemCols), "TMEM columns");
 
-// Instruction descriptor: kind::f16 with bf16 (BF16) or fp16 inputs, fp32
-// accumulate, both operands K-major, M = 256 (two CTAs), N = 256.
+// Operand kinds.  ELEM: bytes per value; BOX_K: k per 128-byte box; UK: k
+// per MMA (32 bytes); PLANES: 1, or 2 for the hi/lo planes of 3xTF32;
+// KSUB: boxes of each plane per stage.  Instruction descriptor: fp32
+// accumulate, both operands K-major, M = 256 (two CTAs), N = 256; operand
+// format bf16 = 1, fp16 = 0 (kind::f16), tf32 = 2 (kind::tf32).
 template <bool BF16>
-__host__ __device__ constexpr uint32_t idesc_half()
-{
-    return (1u << 4) | ((BF16 ? 1u : 0u) << 7) | ((BF16 ? 1u : 0u) << 10) |
-           (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(PM >> 4) << 24);
-}
+struct KindHalf {
+    static constexpr bool TF32 = false;
+    static constexpr int ELEM = 2, BOX_K = 64, UK = 16, PLANES = 1, KSUB = 2;
+    static constexpr uint32_t FMT = BF16 ? 1u : 0u;
+};
+template <int PLANES_>
+struct KindTF32 {
+    static constexpr bool TF32 = true;
+    static constexpr int ELEM = 4, BOX_K = 32, UK = 8, PLANES = PLANES_;
+    static constexpr int KSUB = PLANES_ == 1 ? 2 : 1;
+    static constexpr uint32_t FMT = 2u;
+};
+
+template <class KD>
+struct Shape {
+    static constexpr int STAGE_K = KD::KSUB * KD::BOX_K;
+    static constexpr int BOXES = KD::KSUB * KD::PLANES;  // per operand per stage
+    static constexpr int STAGE_BYTES = BOXES * (SUB_A + SUB_B);  // per CTA
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + NBAR * 8 + 16 + 1024;
+    static constexpr uint32_t IDESC = (1u << 4) | (KD::FMT << 7) | (KD::FMT << 10) |
+                                      (static_cast<uint32_t>(BN >> 3) << 17) |
+                                      (static_cast<uint32_t>(PM >> 4) << 24);
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+};
 
 // TMA tile load into this CTA's shared memory whose completion is counted on
 // the barrier at shared::cluster address `bar` (the even CTA's).
@@ -86,50 +109,71 @@ __device__ __forceinline__ uint32_t cluster_addr(const void *p, uint32_t rank)
     return r;
 }
 
-// One stage's MMAs (two boxes x four k steps of 16) into accumulator d, A
-// and B by descriptors (a0/b0: box 0, k step 0; +2 per 32-byte k step,
-// + box bytes / 16 per box); the first overwrites d unless acc0.  Also tests,
-// without blocking, the barrier of the next stage (see tcp::issue_stage).
-template <bool BF16>
-__device__ __forceinline__ uint32_t issue_stage_half(uint32_t d, uint64_t a0, uint64_t b0,
-                                                     uint32_t acc0, uint32_t nbar, uint32_t npar)
+// One pair MMA d (+)= a * b, operands by shared-memory descriptor; it
+// overwrites d unless acc.
+template <class KD>
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t acc)
 {
-    constexpr uint32_t idesc = idesc_half<BF16>();
+    if constexpr (KD::TF32)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+            "l"(a), "l"(b), "r"(Shape<KD>::IDESC), "r"(acc)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+            "l"(a), "l"(b), "r"(Shape<KD>::IDESC), "r"(acc)
+            : "memory");
+}
+
+// One stage's MMAs into accumulator d: per box, four k steps of 32 bytes
+// (+2 in a descriptor's 16-byte address units); with two planes, box
+// (j, lo) follows box (j, hi) and each k step is lo*hi + hi*lo + hi*hi.  The
+// first MMA overwrites d unless acc0.  Returns whether the next stage's
+// barrier (nbar, parity npar) has already completed, tested without
+// blocking (see tcp::issue_stage).
+template <class KD>
+__device__ __forceinline__ uint32_t issue_stage_ss(uint32_t d, uint64_t a0, uint64_t b0,
+                                                   uint32_t acc0, uint32_t nbar, uint32_t npar)
+{
     constexpr uint64_t AB = SUB_A >> 4, BB = SUB_B >> 4;
+#pragma unroll
+    for (int j = 0; j < KD::KSUB; ++j) {
+        const uint64_t a = a0 + static_cast<uint64_t>(j * KD::PLANES) * AB;
+        const uint64_t b = b0 + static_cast<uint64_t>(j * KD::PLANES) * BB;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ah = a + 2 * kk, bh = b + 2 * kk;
+            const uint32_t acc = (j == 0 && kk == 0) ? acc0 : 1u;
+            if (KD::PLANES == 2) {
+                mma_ss<KD>(d, ah + AB, bh, acc);  // lo * hi
+                mma_ss<KD>(d, ah, bh + BB, 1u);   // hi * lo
+                mma_ss<KD>(d, ah, bh, 1u);        // hi * hi
+            } else {
+                mma_ss<KD>(d, ah, bh, acc);
+            }
+        }
+    }
     uint32_t ready;
     asm volatile(
-        "{\n\t.reg .pred q, p0, p1;\n\t.reg .b64 a, b;\n\t"
-        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 q, [%5], %6;\n\t"
-        "setp.ne.b32 p0, %4, 0;\n\t"
-        "setp.eq.b32 p1, %4, %4;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], %2, %3, %7, p0;\n\t"
-        "add.s64 a, %2, 2;\n\tadd.s64 b, %3, 2;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], a, b, %7, p1;\n\t"
-        "add.s64 a, %2, 4;\n\tadd.s64 b, %3, 4;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], a, b, %7, p1;\n\t"
-        "add.s64 a, %2, 6;\n\tadd.s64 b, %3, 6;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], a, b, %7, p1;\n\t"
-        "add.s64 a, %2, %8;\n\tadd.s64 b, %3, %9;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], a, b, %7, p1;\n\t"
-        "add.s64 a, a, 2;\n\tadd.s64 b, b, 2;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], a, b, %7, p1;\n\t"
-        "add.s64 a, a, 2;\n\tadd.s64 b, b, 2;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], a, b, %7, p1;\n\t"
-        "add.s64 a, a, 2;\n\tadd.s64 b, b, 2;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], a, b, %7, p1;\n\t"
+        "{\n\t.reg .pred q;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 q, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(ready)
-        : "r"(d), "l"(a0), "l"(b0), "r"(acc0), "r"(nbar), "r"(npar), "r"(idesc), "l"(AB),
-          "l"(BB)
+        : "r"(nbar), "r"(npar)
         : "memory");
     return ready;
 }
 
-template <bool BF16>
+template <class KD>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    tch_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+    tcs_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const GemmParams p)
 {
+    using S = Shape<KD>;
+    constexpr int STAGE_BYTES = S::STAGE_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -179,6 +223,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int m0 = wu.tc.tm * PM + static_cast<int>(rank) * BM;
                 const int n0 = wu.tc.tn * BN + static_cast<int>(rank) * HN;
                 const int qa = wu.tc.q * p.a_q_step, qb = wu.tc.q * p.b_q_step;
+                // plane pl of an operand is batch entries pl * za .. (za per plane)
+                const int za = p.a_q_step ? p.Q : 1, zb = p.b_q_step ? p.Q : 1;
                 for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
                     if (!wait_cl(&empty[rr.s], rr.ph ^ 1u, ab, kStatusWaitEmpty)) {
                         ok = false;
@@ -187,12 +233,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (rank == 0) mbar_arrive_expect_tx(&full[rr.s], 2 * STAGE_BYTES);
                     const uint32_t fb = cluster_addr(&full[rr.s], 0);
                     uint8_t *sa = base + rr.s * STAGE_BYTES;
-                    uint8_t *sb = sa + KSUB * SUB_A;
+                    uint8_t *sb = sa + S::BOXES * SUB_A;
 #pragma unroll
-                    for (int j = 0; j < KSUB; ++j) {
-                        const int k0 = kb * STAGE_K + j * BKH;
-                        tma_load_pair(sa + j * SUB_A, &tmA, fb, k0, m0, qa);
-                        tma_load_pair(sb + j * SUB_B, &tmB, fb, k0, n0, qb);
+                    for (int j = 0; j < KD::KSUB; ++j) {
+                        const int k0 = kb * S::STAGE_K + j * KD::BOX_K;
+#pragma unroll
+                        for (int pl = 0; pl < KD::PLANES; ++pl) {
+                            const int x = j * KD::PLANES + pl;
+                            tma_load_pair(sa + x * SUB_A, &tmA, fb, k0, m0, qa + pl * za);
+                            tma_load_pair(sb + x * SUB_B, &tmB, fb, k0, n0, qb + pl * zb);
+                        }
                     }
                     ++issued;
                     rr.next();
@@ -222,7 +272,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bool ok = true;
             bool any = false;
             const uint64_t adesc0 = tc::kmajor_sw128_desc(smem_u32(base));
-            const uint64_t bdesc0 = tc::kmajor_sw128_desc(smem_u32(base + KSUB * SUB_A));
+            const uint64_t bdesc0 = tc::kmajor_sw128_desc(smem_u32(base + S::BOXES * SUB_A));
             for (long long u = cid; ok && u < p.num_units; u += ncl) {
                 const WorkUnit wu = work_unit(u, p);
                 if (!wait_cl(&acc_empty[acc.s], acc.ph ^ 1u, ab, kStatusWaitAcc)) {
@@ -241,9 +291,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint64_t soff = static_cast<uint64_t>(sr.s * (STAGE_BYTES >> 4));
                     tc::Ring<STAGES> nx = sr;
                     nx.next();
-                    ready = issue_stage_half<BF16>(d_tmem, adesc0 + soff, bdesc0 + soff,
-                                                   kb > wu.kb_lo ? 1u : 0u,
-                                                   smem_u32(&full[nx.s]), nx.ph);
+                    ready = issue_stage_ss<KD>(d_tmem, adesc0 + soff, bdesc0 + soff,
+                                               kb > wu.kb_lo ? 1u : 0u, smem_u32(&full[nx.s]),
+                                               nx.ph);
                     if (kb + 1 == wu.kb_hi) ready = 0;
                     any = true;
                     umma_commit_both(&empty[sr.s]);
@@ -299,5 +349,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 }
 
-}  // namespace tch
+}  // namespace tcs
+
+// Host side: launches the kernel for `plan` (at most `slots` CTA pairs, each
+// looping over work units) and, when the plan splits tiles along K, the
+// fix-up kernel after it.
+template <class KD>
+int launch_ss(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB, int slots)
+{
+    auto kern = tcs::tcs_gemm_kernel<KD>;
+    constexpr int smem = tcs::Shape<KD>::SMEM_BYTES;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
+    long long pairs = plan.p.num_units;
+    if (pairs > slots) pairs = slots;
+    kern<<<static_cast<unsigned>(2 * pairs), tcs::kThreads, smem, plan.stream>>>(tmA, tmB,
+                                                                                 plan.p);
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    note_launch();
+    return plan.p.splits > 1 ? launch_fixup(plan, tcs::PM, tcs::BN) : SGEMM_OK;
+}
+
 }  // namespace sg

@@ -1,0 +1,108 @@
+"""GPU parity of the tensor-core planes route: with a workspace, shapes large
+enough for it (the library's cost model: the operand pass must cost less than
+the product saves) first rewrite A and B into TF32 planes (3xTF32: hi and
+lo; TF32: rounded to nearest) and then multiply on the shared-memory-operand
+kernel.  Every layout, padded and unaligned operands, ragged M/N/K, batches
+with a broadcast operand, integer data bit for bit; sampled rows against the
+oracle.  The launch counter shows the route was taken (two pass kernels
+before the product)."""
+import numpy as np
+import pytest
+
+import workloads
+from _helpers import TOL, Problem, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+MODES = ["3xtf32", "tf32"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu_ready():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import dense_fp32_matrix_03_gb300 as lib
+    lib.load()
+
+
+def launches_of(fn):
+    import torch
+    import dense_fp32_matrix_03_gb300 as lib
+    torch.cuda.synchronize()
+    n0 = lib.sgemm_kernel_launches()
+    out = fn()
+    return out, lib.sgemm_kernel_launches() - n0
+
+
+def check(prob, mode, oracle_mod, rows, exact=False, route=True):
+    """route: the operands are TMA-aligned, so the pair kernel would run in
+    one or two launches; three or more show the planes route."""
+    C, n = launches_of(lambda: prob.run_gpu(mode, api="ws"))
+    if route:
+        assert n >= 3, f"planes route not taken ({n} launches)"
+    Cref, D = prob.oracle(oracle_mod, rows=rows)
+    got = np.stack([C[q, i] for q, i in rows])
+    if exact:
+        assert np.array_equal(got.astype(np.float64), Cref)
+    else:
+        err = oracle_mod.max_rel_err(got, Cref, D)
+        assert err <= TOL[mode], f"{mode}: max rel err {err:.3e}"
+    return C
+
+
+@pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("mode", MODES)
+def test_planes_route_every_layout(oracle_mod, mode, tA, tB):
+    """3100 x 3000 x 2333: ragged tiles in M and N, K not a multiple of the
+    32-wide box; padded leading dimensions, beta != 0."""
+    A, B, C0 = workloads.random_inputs(3100, 3000, 2333, seed=61 + 2 * tA + tB)
+    prob = Problem(A, B, C0, 1.25, -0.75, tA, tB, pads=(4, 8, 3))
+    check(prob, mode, oracle_mod, sample_rows(1, 3100, 24, seed=tA + 2 * tB, tile=256))
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_planes_route_unaligned_operands(oracle_mod, mode):
+    """Odd leading dimensions and bases off 16 bytes: the pass reads them
+    value by value; the planes are aligned whatever the source."""
+    A, B, C0 = workloads.random_inputs(3100, 3000, 2333, seed=67)
+    for tA, tB in ((0, 0), (1, 1)):
+        prob = Problem(A, B, C0, 1.0, 0.5, tA, tB, pads=(1, 3, 1), offsets=(1, 3, 2))
+        check(prob, mode, oracle_mod, sample_rows(1, 3100, 16, seed=5, tile=256), route=False)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_planes_route_batched_broadcast(oracle_mod, mode):
+    """Q = 3 with A broadcast (stride 0): A's planes hold one entry, B's
+    three; batch entries and planes share the tensor map's third dimension."""
+    Q = 3
+    A, B, C0 = workloads.random_inputs(3100, 3000, 800, Q=Q, seed=71)
+    prob = Problem(A[:1].repeat(Q, axis=0), B, C0, 0.5, 1.0, 0, 1, strideA=0)
+    check(prob, mode, oracle_mod, sample_rows(Q, 3100, 24, seed=6, tile=256))
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_planes_route_integer_bit_exact(oracle_mod, mode):
+    """Small integers: every plane, product and partial sum is exact, so the
+    result equals the oracle's bit for bit (the last wave's tiles are also
+    split along K)."""
+    A, B, C0 = workloads.integer_inputs(3072, 3072, 2000, seed=73)
+    for tA, tB in ((0, 0), (1, 1)):
+        prob = Problem(A, B, C0, 2.0, -1.0, tA, tB)
+        check(prob, mode, oracle_mod, sample_rows(1, 3072, 16, seed=7, tile=256), exact=True)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_planes_route_small_workspace_falls_back(oracle_mod, mode):
+    """A workspace too small for the planes: the pair kernel runs instead,
+    with the same results within tolerance."""
+    import dense_fp32_matrix_03_gb300 as lib
+    A, B, C0 = workloads.random_inputs(3100, 3000, 2333, seed=79)
+    prob = Problem(A, B, C0, 1.0, 0.0)
+    full = lib.sgemm_workspace_size(mode, 3100, 3000, 2333, 1)
+    C, n = launches_of(lambda: prob.run_gpu(mode, api="ws", ws_bytes=full // 4))
+    assert n <= 2
+    rows = sample_rows(1, 3100, 16, seed=8, tile=256)
+    Cref, D = prob.oracle(oracle_mod, rows=rows)
+    got = np.stack([C[q, i] for q, i in rows])
+    assert oracle_mod.max_rel_err(got, Cref, D) <= TOL[mode]

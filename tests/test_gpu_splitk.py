@@ -109,7 +109,8 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
     128 x 128 with both operands K-inner, each TMA- or cp.async-fed, one unit
     per multiprocessor; tensor cores: the direct kernel's 128 x 128 tiles on
     every multiprocessor and the pair kernel's 256 x 128 tiles (256 x 256 for
-    TF32 with K >= 1536), one unit per CTA pair): whole waves of units, then the last wave's r tiles cut into s
+    TF32 with K >= 1536), one unit per CTA pair, and the planes route's
+    256 x 256 pair tiles): whole waves of units, then the last wave's r tiles cut into s
     slices (s <= 16, each >= 64 deep for FP32 and >= 256 for the tensor
     paths), s minimising t_tile * (floor(T/G) + ceil(r*s/G)/s) + 3 us +
     2 * ws / bw (G units at once; bw 8 TB/s up to 64 MB of workspace, else
@@ -117,10 +118,14 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
     multiprocessors per unit), used only if it saves 1%; returns the largest
     workspace over the kernels (one BM x BN fp32 slot per split unit), 0 when
     none splits; on the FP32 path plus room for transposed copies of A and B
-    (256-byte rounded)."""
+    (256-byte rounded); on the tensor paths plus room for 128-byte-pitched
+    copies of A and B, or, where the planes route pays, for their TF32
+    planes if larger (two planes for 3xTF32, one for TF32; rows of
+    round_up(K, 32) values)."""
     rates = {("fp32", "direct"): 0.24e12, ("fp32", "tma"): 0.40e12,
              ("3xtf32", "direct"): 0.47e12, ("3xtf32", "pair"): 1.8e12,
-             ("tf32", "direct"): 0.55e12, ("tf32", "pair"): 3.6e12}
+             ("tf32", "direct"): 0.55e12, ("tf32", "pair"): 3.6e12,
+             ("3xtf32", "planes"): 2.45e12, ("tf32", "planes"): 6.4e12}
     if pair_slots is None:
         pair_slots = sms // 2
     if mode == "fp32":
@@ -129,15 +134,16 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
     else:
         # the pair kernel: 256 x 128 tiles, 256 x 256 for TF32 with K >= 1536
         wide = mode == "tf32" and K >= 1536
-        kernels = [(128, 128, "direct", sms, 1), (256, 256 if wide else 128, "pair", pair_slots, 2)]
-    need = 0
-    for bm, bn, feed, G, per_unit in kernels:
+        kernels = [(128, 128, "direct", sms, 1), (256, 256 if wide else 128, "pair", pair_slots, 2),
+                   (256, 256, "planes", pair_slots, 2)]
+    def plan(bm, bn, feed, G, per_unit):
+        """(workspace, modelled seconds) of the best split plan."""
         T = Q * math.ceil(M / bm) * math.ceil(N / bn)
         full, rem = divmod(T, G)
-        if rem == 0:
-            continue
-        smax = min(16, K // (64 if mode == "fp32" else 256))
         t_tile = 2.0 * bm * bn * float(K) / (rates[(mode, feed)] * per_unit)
+        if rem == 0:
+            return 0, t_tile * full
+        smax = min(16, K // (64 if mode == "fp32" else 256))
         t_whole = t_tile * float(full + 1)
         best_t, best, best_ws = t_whole, 1, 0
         for s in range(2, smax + 1):
@@ -148,7 +154,10 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
             if t < best_t:
                 best_t, best, best_ws = t, s, ws
         if best > 1 and best_t <= 0.99 * t_whole:
-            need = max(need, best_ws)
+            return best_ws, best_t
+        return 0, t_whole
+
+    need = max(plan(*k)[0] for k in kernels)
     if mode == "fp32":
         # room for transposed copies of A (N >= 1024) and B (M >= 1024)
         def repack(inner, outer):
@@ -156,10 +165,21 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
         need += (repack(M, K) if N >= 1024 else 0) + (repack(N, K) if M >= 1024 else 0)
     else:
         # room for 128-byte-pitched copies of A and B, either layout
+        r32 = lambda x: (x + 31) // 32 * 32
+        r256 = lambda b: (b + 255) // 256 * 256
+
         def copy(rows):
-            r32 = lambda x: (x + 31) // 32 * 32
-            return (Q * max(rows * r32(K), K * r32(rows)) * 4 + 255) // 256 * 256
-        need += copy(M) + copy(N)
+            return r256(Q * max(rows * r32(K), K * r32(rows)) * 4)
+        planes = 2 if mode == "3xtf32" else 1
+        # the planes route where it pays: the modelled time of its tiles' plan
+        # plus its pass ((M + N) * K * Q * 4 * (1 + planes) bytes at 5.5 TB/s)
+        # and 10 us, against the modelled time of the pair kernel's plan
+        t_pair = plan(*kernels[1])[1]
+        t_planes = plan(*kernels[2])[1] + (M + N) * K * Q * 4.0 * (1 + planes) / 5.5e12 + 10e-6
+        room = copy(M) + copy(N)
+        if t_planes < t_pair:
+            room = max(room, r256(planes * Q * M * r32(K) * 4) + r256(planes * Q * N * r32(K) * 4))
+        need += room
     return need
 
 
@@ -184,7 +204,10 @@ def test_workspace_size_query():
     assert lib.sgemm_workspace_size("fp32", 1000, 1000, 32, 1) == 0      # one k-block: no split
     assert lib.sgemm_workspace_size("fp32", 1024, 1024, 32, 1) > 0       # room to transpose A, B
     # tensor path: no split (>= 256 per slice), room for aligned copies of A and B only
+    # (the planes route does not pay at this size)
     assert lib.sgemm_workspace_size("3xtf32", 1024, 1024, 128, 1) == 2 * 1024 * 128 * 4
+    # the planes route at 4096^3: two planes each of A and B, 4 * 4096 * 4096 floats
+    assert lib.sgemm_workspace_size("3xtf32", 4096, 4096, 4096, 1) >= 4 * 4096 * 4096 * 4
     assert lib.sgemm_workspace_size("fp32", 1024, 1024, 128, 1) > 0     # 2 slices of 64
     assert lib.sgemm_workspace_size("fp32", 0, 10, 10, 1) == 0
     assert lib.sgemm_workspace_size(7, 100, 100, 100, 1) == 0
