@@ -90,8 +90,8 @@ def roofline_peak(mode, num_sms, peaks, source):
 # plans them; the probes, the host-buffer entry point and the allocation-free
 # entry point are left out (they do not change what the timed kernels do).
 TIMED_SOURCES = ("api.cu", "common.cuh", "internal.h", "kernels_simt.cu", "kernels_tc.cu",
-                 "kernels_tcp.cu", "params.h", "repack.cu", "simt_fp32.cuh", "tc_direct.cuh",
-                 "tc_pair.cuh", "tc_tf32.cuh")
+                 "kernels_tcp.cu", "params.h", "planes.cu", "repack.cu", "simt_fp32.cuh",
+                 "tc_direct.cuh", "tc_pair.cuh", "tc_ss.cuh", "tc_tf32.cuh")
 
 
 def kernel_source_hash():
@@ -470,9 +470,11 @@ def main():
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": UNIT,
                 "frac": achieved / peak, "traffic": traffic,
                 "kernel": f"sgemm {mode} path ({kernel_key})",
-                "timed": ("each call: the GEMM kernel and the split-K fix-up kernel (events "
-                          "bracket the whole call; traffic is the GEMM kernel's)" if ws_bytes
-                          else "each call: the GEMM kernel"),
+                "timed": ("each call: every kernel it launches -- on the tensor-core paths "
+                          "at this size the pass into TF32 planes, the GEMM kernel and the "
+                          "split-K fix-up; on the FP32 path the operand transposition, the GEMM "
+                          "kernel and the fix-up (events bracket the whole call; traffic is "
+                          "the GEMM kernel's)" if ws_bytes else "each call: the GEMM kernel"),
                 "peak_source": f"{peak_note}; {peak_src} MEASURED_PEAKS.json" if bound != "alu"
                 else peak_note,
                 "algorithmic_flops_per_launch": flops_step}

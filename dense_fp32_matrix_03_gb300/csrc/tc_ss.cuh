@@ -16,12 +16,13 @@
 //
 // Tile 256 x 256 per CTA pair (cta_group::2, M = 256, N = 256): each CTA
 // stages its 128 rows of A and its 128 of the tile's 256 rows of B^T.  A
-// stage is 64 KB per CTA: two 128-byte boxes of one plane (128 k of 16-bit
-// values, 64 k of fp32), or one box of each of two planes (32 k); three
-// stages deep.  Both CTAs' TMA loads complete on the even CTA's barrier
-// (cta_group::2 form, which may name the peer's barrier); one thread of the
-// even CTA issues every MMA and multicasts its commits (stage free,
-// accumulator full) to both CTAs.  TMEM: two 256-column fp32 accumulators
+// stage holds, per CTA, two 128-byte boxes of each operand (128 k of 16-bit
+// values; 64 KB, three stages), one box of each plane of 3xTF32 (32 k; 64
+// KB, three stages), or one box of TF32 (32 k; 32 KB, six stages).  Both
+// CTAs' TMA loads complete on the even CTA's barrier (cta_group::2 form,
+// which may name the peer's barrier); one thread of the even CTA issues
+// every MMA and multicasts its commits (stage free, accumulator full) to
+// both CTAs.  TMEM: two 256-column fp32 accumulators
 // per CTA (double buffered, so the epilogue overlaps the next tile).
 //
 // Warps: 0 TMA producer, 1 TMEM allocator + MMA issuer (even CTA), 2-5
@@ -51,11 +52,19 @@ constexpr int BN = 256;      // columns per pair tile (the MMA's N)
 constexpr int HN = BN / 2;   // rows of B^T each CTA holds
 constexpr int SUB_A = BM * 128;  // one 128-byte box of A: 16 KB
 constexpr int SUB_B = HN * 128;  // one box of B: 16 KB
-constexpr int STAGES = 3;
+// Single-plane TF32 stages: one 32-k box per stage, six deep (more bytes in
+// flight than three 64-k stages in the same room; measured on GB300, TF32
+// planes route, TFLOP/s: 4092^3 nn 635 -> 654, nt 648 -> 667, 8192^3 873 ->
+// 898; five stages 635 / 654).
+#ifndef SG_TCS_TF32_KSUB
+#define SG_TCS_TF32_KSUB 1
+#endif
+#ifndef SG_TCS_TF32_STAGES
+#define SG_TCS_TF32_STAGES 6
+#endif
 constexpr int kEpiWarp0 = 2;
 constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr int NBAR = 2 * STAGES + 4 + 1;
 constexpr int EPI_BYTES = 4 * tc::kStageFloats * 4;  // epilogue staging (4 warps)
 static_assert(2 * BN <= static_cast<int>(kTmemCols), "TMEM columns");
 
@@ -67,19 +76,22 @@ static_assert(2 * BN <= static_cast<int>(kTmemCols), "TMEM columns");
 template <bool BF16>
 struct KindHalf {
     static constexpr bool TF32 = false;
-    static constexpr int ELEM = 2, BOX_K = 64, UK = 16, PLANES = 1, KSUB = 2;
+    static constexpr int ELEM = 2, BOX_K = 64, UK = 16, PLANES = 1, KSUB = 2, STAGES = 3;
     static constexpr uint32_t FMT = BF16 ? 1u : 0u;
 };
 template <int PLANES_>
 struct KindTF32 {
     static constexpr bool TF32 = true;
     static constexpr int ELEM = 4, BOX_K = 32, UK = 8, PLANES = PLANES_;
-    static constexpr int KSUB = PLANES_ == 1 ? 2 : 1;
+    static constexpr int KSUB = PLANES_ == 1 ? SG_TCS_TF32_KSUB : 1;
+    static constexpr int STAGES = PLANES_ == 1 ? SG_TCS_TF32_STAGES : 3;
     static constexpr uint32_t FMT = 2u;
 };
 
 template <class KD>
 struct Shape {
+    static constexpr int STAGES = KD::STAGES;
+    static constexpr int NBAR = 2 * STAGES + 4 + 1;
     static constexpr int STAGE_K = KD::KSUB * KD::BOX_K;
     static constexpr int BOXES = KD::KSUB * KD::PLANES;  // per operand per stage
     static constexpr int STAGE_BYTES = BOXES * (SUB_A + SUB_B);  // per CTA
@@ -174,6 +186,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 {
     using S = Shape<KD>;
     constexpr int STAGE_BYTES = S::STAGE_BYTES;
+    constexpr int STAGES = S::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
