@@ -11,8 +11,9 @@
 //   - 3xTF32: two planes, hi = the value with its 13 low mantissa bits
 //     cleared and lo = (value - hi) likewise (tc::split_value),
 // and the product runs on tcs_gemm_kernel (tc_ss.cuh), which TMA feeds
-// with both operands straight into the MMA's layout.  The pass reads each
-// operand once and writes its planes once (HBM-bound).
+// with both operands straight into the MMA's layout.  The pass (one launch
+// for both operands) reads each operand once and writes its planes once
+// (HBM-bound).
 //
 // Plane layout of an operand with R rows (M for A, N for B) and E stored
 // batch entries (1 when broadcast): value (pl, q, r, k) at
@@ -50,66 +51,77 @@ __device__ __forceinline__ void put_planes(float *dst, long long pstride, const 
         *reinterpret_cast<float4 *>(dst + pstride) = make_float4(l[0], l[1], l[2], l[3]);
 }
 
-// K-inner source (src[q][r * lds + k]): each thread converts four
-// consecutive k of one row (a 16-byte load when VEC).  Block (x, y, z) =
-// (chunk of 4 * kThreads values of K, row, entry), y and z stepping by the
-// grid.  Values past K in the last group are written as zeros (the pitch
-// leaves room; TMA never reads them).
-template <int PLANES, bool VEC>
-__global__ void __launch_bounds__(kThreads)
-    planes_copy_kernel(const float *__restrict__ src, long long lds, long long sstride, int rows,
-                       int K, int E, float *__restrict__ dst, long long ldp, long long pstride)
-{
-    const int k = (blockIdx.x * kThreads + threadIdx.x) * 4;
-    if (k >= K) return;
-    for (int q = blockIdx.z; q < E; q += gridDim.z) {
-        for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
-            const float *sp = src + q * sstride + r * lds + k;
-            float v[4] = {0.f, 0.f, 0.f, 0.f};
-            if (VEC && k + 4 <= K) {
-                const float4 x = *reinterpret_cast<const float4 *>(sp);
-                v[0] = x.x;
-                v[1] = x.y;
-                v[2] = x.z;
-                v[3] = x.w;
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (k + j < K) v[j] = sp[j];
-            }
-            put_planes<PLANES>(dst + (static_cast<long long>(q) * rows + r) * ldp + k, pstride, v);
-        }
-    }
-}
+// One operand of the pass: R rows (M for A, N for B) of K values in E
+// stored batch entries; K-inner sources are read row by row, others
+// (stored K x R) through a shared-memory transpose.
+struct PassOperand {
+    const float *src;
+    long long lds, sstride;  // source pitch and batch stride (elements)
+    float *dst;
+    long long pstride;       // elements per plane (E * R * ldp)
+    int rows, E;
+    int k_inner, vec;        // vec: 16-byte loads allowed
+    long long tiles_r, tiles_k, tiles;  // 64 x 64 tiles per entry, and in all
+};
 
-// Source stored K x rows (src[q][k * lds + r]): through a 64 x 64 shared
-// tile, each thread reading four consecutive values of a source row (a
-// 16-byte load when VEC) and writing four consecutive k of a destination
-// row.  Block (x, y, z) = (64 destination rows, 64 k, entry), y and z
-// stepping by the grid.
-template <int PLANES, bool VEC>
+// The pass over both operands in one launch: block b converts 64 x 64 tile
+// b of A, then of B (tiles numbered entry-major, then row, then k).  256
+// threads; thread t reads and writes four consecutive values at slot
+// (it, t), it = 0..3: line (it / 2) * 32 + t / 8, values (it % 2) * 32 +
+// 4 (t % 8) .. + 3 -- a warp touches four rows of 128 bytes per access.
+// K-inner: line = row, values = k.  Transposed: lines are source rows (k)
+// on the read and destination rows (r) on the write, through tile[r][k]
+// with a 65-float pitch, which these slots access without bank conflicts.
+// Values past K in a row's last group of four are written as zeros (the
+// pitch leaves room; TMA never reads them).
+template <int PLANES>
 __global__ void __launch_bounds__(kThreads)
-    planes_transpose_kernel(const float *__restrict__ src, long long lds, long long sstride,
-                            int rows, int K, int E, float *__restrict__ dst, long long ldp,
-                            long long pstride)
+    planes_pass_kernel(PassOperand a, PassOperand b, int K, long long ldp)
 {
     __shared__ float tile[kT][kT + 1];
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;  // 16 x 16
-    const int r0 = blockIdx.x * kT;
-    for (int q = blockIdx.z; q < E; q += gridDim.z) {
-        const float *s = src + q * sstride;
-        float *d = dst + static_cast<long long>(q) * rows * ldp;
-        for (long long k0l = static_cast<long long>(blockIdx.y) * kT; k0l < K;
-             k0l += static_cast<long long>(gridDim.y) * kT) {
-            const int k0 = static_cast<int>(k0l);
-            // source rows k0 + ty + 16 i, columns r0 + 4 tx .. +3
+    const int t = threadIdx.x;
+    for (long long blk = blockIdx.x; blk < a.tiles + b.tiles; blk += gridDim.x) {
+        const bool is_a = blk < a.tiles;
+        const PassOperand &o = is_a ? a : b;
+        const long long id = is_a ? blk : blk - a.tiles;
+        const long long per_entry = o.tiles_r * o.tiles_k;
+        const int q = static_cast<int>(id / per_entry);
+        const long long rem = id - static_cast<long long>(q) * per_entry;
+        const int r0 = static_cast<int>(rem / o.tiles_k) * kT;
+        const int k0 = static_cast<int>(rem % o.tiles_k) * kT;
+        const float *s = o.src + q * o.sstride;
+        float *d = o.dst + static_cast<long long>(q) * o.rows * ldp;
+        if (o.k_inner) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int tk = ty + 16 * i, kk = k0 + tk, c = r0 + 4 * tx;
+            for (int it = 0; it < 4; ++it) {
+                const int r = r0 + (it >> 1) * 32 + (t >> 3);
+                const int k = k0 + (it & 1) * 32 + 4 * (t & 7);
+                if (r >= o.rows || k >= K) continue;
+                const float *sp = s + static_cast<long long>(r) * o.lds + k;
+                float v[4] = {0.f, 0.f, 0.f, 0.f};
+                if (o.vec && k + 4 <= K) {
+                    const float4 x = *reinterpret_cast<const float4 *>(sp);
+                    v[0] = x.x;
+                    v[1] = x.y;
+                    v[2] = x.z;
+                    v[3] = x.w;
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        if (k + jj < K) v[jj] = sp[jj];
+                }
+                put_planes<PLANES>(d + static_cast<long long>(r) * ldp + k, o.pstride, v);
+            }
+        } else {
+            // read: source rows k0 + line, values r0 + ... (stored K x rows)
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int kl = (it >> 1) * 32 + (t >> 3), rl = (it & 1) * 32 + 4 * (t & 7);
+                const int kk = k0 + kl, c = r0 + rl;
                 float v[4] = {0.f, 0.f, 0.f, 0.f};
                 if (kk < K) {
-                    const float *sp = s + static_cast<long long>(kk) * lds + c;
-                    if (VEC && c + 3 < rows) {
+                    const float *sp = s + static_cast<long long>(kk) * o.lds + c;
+                    if (o.vec && c + 3 < o.rows) {
                         const float4 x = *reinterpret_cast<const float4 *>(sp);
                         v[0] = x.x;
                         v[1] = x.y;
@@ -117,22 +129,23 @@ __global__ void __launch_bounds__(kThreads)
                         v[3] = x.w;
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            if (c + j < rows) v[j] = sp[j];
+                        for (int jj = 0; jj < 4; ++jj)
+                            if (c + jj < o.rows) v[jj] = sp[jj];
                     }
                 }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) tile[tk][4 * tx + j] = v[j];
+                for (int jj = 0; jj < 4; ++jj) tile[rl + jj][kl] = v[jj];
             }
             __syncthreads();
-            // destination rows r0 + ty + 16 i, k0 + 4 tx .. +3 (zeros past K)
+            // write: destination rows r0 + line, k0 + ...
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int tr = ty + 16 * i, r = r0 + tr, k = k0 + 4 * tx;
-                if (r < rows && k < K) {
-                    const float v[4] = {tile[4 * tx][tr], tile[4 * tx + 1][tr],
-                                        tile[4 * tx + 2][tr], tile[4 * tx + 3][tr]};
-                    put_planes<PLANES>(d + static_cast<long long>(r) * ldp + k, pstride, v);
+            for (int it = 0; it < 4; ++it) {
+                const int rl = (it >> 1) * 32 + (t >> 3), kl = (it & 1) * 32 + 4 * (t & 7);
+                const int r = r0 + rl, k = k0 + kl;
+                if (r < o.rows && k < K) {
+                    const float v[4] = {tile[rl][kl], tile[rl][kl + 1], tile[rl][kl + 2],
+                                        tile[rl][kl + 3]};
+                    put_planes<PLANES>(d + static_cast<long long>(r) * ldp + k, o.pstride, v);
                 }
             }
             __syncthreads();
@@ -140,36 +153,37 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-template <int PLANES>
-int launch_planes_pass(const float *src, long long lds, long long sstride, int rows, int K, int E,
-                       bool k_inner, float *dst, long long ldp, long long pstride,
-                       cudaStream_t stream)
+PassOperand pass_operand(const float *src, long long lds, long long sstride, int rows, int K,
+                         int E, bool k_inner, float *dst, long long ldp)
 {
-    const unsigned gz = static_cast<unsigned>(E < 65535 ? E : 65535);
-    const bool vec = (reinterpret_cast<uintptr_t>(src) & 15) == 0 && lds % 4 == 0 &&
-                     (E <= 1 || sstride % 4 == 0);
-    if (k_inner) {
-        const long long cb = (K + 4LL * kThreads - 1) / (4LL * kThreads);
-        const dim3 grid(static_cast<unsigned>(cb), static_cast<unsigned>(rows < 65535 ? rows : 65535),
-                        gz);
-        if (vec)
-            planes_copy_kernel<PLANES, true><<<grid, kThreads, 0, stream>>>(
-                src, lds, sstride, rows, K, E, dst, ldp, pstride);
-        else
-            planes_copy_kernel<PLANES, false><<<grid, kThreads, 0, stream>>>(
-                src, lds, sstride, rows, K, E, dst, ldp, pstride);
-    } else {
-        const long long tr = (rows + kT - 1) / kT, tk = (K + kT - 1) / kT;
-        if (tr > 0x7FFFFFFFLL) return SGEMM_ERR_UNSUPPORTED;
-        const dim3 grid(static_cast<unsigned>(tr), static_cast<unsigned>(tk < 65535 ? tk : 65535),
-                        gz);
-        if (vec)
-            planes_transpose_kernel<PLANES, true><<<grid, kThreads, 0, stream>>>(
-                src, lds, sstride, rows, K, E, dst, ldp, pstride);
-        else
-            planes_transpose_kernel<PLANES, false><<<grid, kThreads, 0, stream>>>(
-                src, lds, sstride, rows, K, E, dst, ldp, pstride);
-    }
+    PassOperand o;
+    o.src = src;
+    o.lds = lds;
+    o.sstride = sstride;
+    o.dst = dst;
+    o.pstride = static_cast<long long>(E) * rows * ldp;
+    o.rows = rows;
+    o.E = E;
+    o.k_inner = k_inner ? 1 : 0;
+    o.vec = (reinterpret_cast<uintptr_t>(src) & 15) == 0 && lds % 4 == 0 &&
+            (E <= 1 || sstride % 4 == 0);
+    o.tiles_r = (rows + kT - 1) / kT;
+    o.tiles_k = (K + kT - 1) / kT;
+    o.tiles = static_cast<long long>(E) * o.tiles_r * o.tiles_k;
+    return o;
+}
+
+template <int PLANES>
+int launch_planes_pass(const PassOperand &a, const PassOperand &b, int K, long long ldp,
+                       int num_sms, cudaStream_t stream)
+{
+    const long long total = a.tiles + b.tiles;
+    if (total <= 0) return SGEMM_OK;
+    // one tile per block; past 2^20 tiles the blocks step through the rest
+    (void)num_sms;
+    const long long cap = 1LL << 20;
+    const unsigned grid = static_cast<unsigned>(total < cap ? total : cap);
+    planes_pass_kernel<PLANES><<<grid, kThreads, 0, stream>>>(a, b, K, ldp);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
     note_launch();
     return SGEMM_OK;
@@ -257,23 +271,13 @@ int run_planes(Plan &plan, bool &taken)
     float *pa = reinterpret_cast<float *>(w);
     const size_t a_bytes = round256(static_cast<size_t>(planes) * QA * p.M * ldp * sizeof(float));
     float *pb = reinterpret_cast<float *>(w + a_bytes);
-    const long long a_pstride = static_cast<long long>(QA) * p.M * ldp;
-    const long long b_pstride = static_cast<long long>(QB) * p.N * ldp;
-    int rc;
     // A: K-inner unless stored K x M; B: K-inner when stored N x K
-    if (planes == 2) {
-        rc = launch_planes_pass<2>(p.A, p.lda, p.sA, p.M, p.K, QA, !plan.transA, pa, ldp,
-                                   a_pstride, plan.stream);
-        if (rc == SGEMM_OK)
-            rc = launch_planes_pass<2>(p.B, p.ldb, p.sB, p.N, p.K, QB, plan.transB != 0, pb, ldp,
-                                       b_pstride, plan.stream);
-    } else {
-        rc = launch_planes_pass<1>(p.A, p.lda, p.sA, p.M, p.K, QA, !plan.transA, pa, ldp,
-                                   a_pstride, plan.stream);
-        if (rc == SGEMM_OK)
-            rc = launch_planes_pass<1>(p.B, p.ldb, p.sB, p.N, p.K, QB, plan.transB != 0, pb, ldp,
-                                       b_pstride, plan.stream);
-    }
+    const PassOperand oa =
+        pass_operand(p.A, p.lda, p.sA, p.M, p.K, QA, !plan.transA, pa, ldp);
+    const PassOperand ob =
+        pass_operand(p.B, p.ldb, p.sB, p.N, p.K, QB, plan.transB != 0, pb, ldp);
+    int rc = planes == 2 ? launch_planes_pass<2>(oa, ob, p.K, ldp, plan.num_sms, plan.stream)
+                         : launch_planes_pass<1>(oa, ob, p.K, ldp, plan.num_sms, plan.stream);
     if (rc != SGEMM_OK) return rc;
 
     alignas(64) CUtensorMap tmA;

@@ -61,6 +61,7 @@ class Problem:
                 ws_bytes = lib.sgemm_workspace_size(mode, self.M, self.N, self.K, self.Q)
             ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
             self.last_ws_bytes = ws_bytes
+            self.last_ws = ws
             st = lib.sgemm_batched_ex_ws(mode, self.M, self.N, self.K, self.alpha, pa, self.lda,
                                          pb, self.ldb, self.beta, pc, self.ldc, self.transA,
                                          self.transB, self.sA, self.sB, self.sC, self.Q, ws,

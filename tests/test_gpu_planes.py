@@ -4,8 +4,9 @@ the product saves) first rewrite A and B into TF32 planes (3xTF32: hi and
 lo; TF32: rounded to nearest) and then multiply on the shared-memory-operand
 kernel.  Every layout, padded and unaligned operands, ragged M/N/K, batches
 with a broadcast operand, integer data bit for bit; sampled rows against the
-oracle.  The launch counter shows the route was taken (two pass kernels
-before the product)."""
+oracle.  The workspace shows the route was taken: it starts with op(A)'s
+first plane, row 0 of which the test recomputes from the definition (hi:
+the 13 low mantissa bits cleared; TF32: rounded to nearest, ties away)."""
 import numpy as np
 import pytest
 
@@ -26,6 +27,14 @@ def gpu_ready():
     lib.load()
 
 
+def first_plane_row(a_row, mode):
+    """Row 0 of op(A)'s first plane as the planes route writes it."""
+    bits = np.ascontiguousarray(a_row, dtype=np.float32).view(np.uint32)
+    if mode == "tf32":
+        bits = bits + np.uint32(0x1000)  # half of the dropped range: ties away
+    return (bits & np.uint32(0xFFFFE000)).view(np.float32)
+
+
 def launches_of(fn):
     import torch
     import dense_fp32_matrix_03_gb300 as lib
@@ -35,12 +44,15 @@ def launches_of(fn):
     return out, lib.sgemm_kernel_launches() - n0
 
 
-def check(prob, mode, oracle_mod, rows, exact=False, route=True):
-    """route: the operands are TMA-aligned, so the pair kernel would run in
-    one or two launches; three or more show the planes route."""
-    C, n = launches_of(lambda: prob.run_gpu(mode, api="ws"))
-    if route:
-        assert n >= 3, f"planes route not taken ({n} launches)"
+def check(prob, mode, oracle_mod, rows, exact=False, opA0=None):
+    """opA0: row 0 of op(A); the workspace must start with its first plane
+    (the planes route ran)."""
+    C = prob.run_gpu(mode, api="ws")
+    if opA0 is not None:
+        K = opA0.shape[0]
+        got = prob.last_ws[:4 * K].view(__import__("torch").float32).cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), first_plane_row(opA0, mode).view(np.uint32)), \
+            "planes route not taken"
     Cref, D = prob.oracle(oracle_mod, rows=rows)
     got = np.stack([C[q, i] for q, i in rows])
     if exact:
@@ -58,7 +70,7 @@ def test_planes_route_every_layout(oracle_mod, mode, tA, tB):
     32-wide box; padded leading dimensions, beta != 0."""
     A, B, C0 = workloads.random_inputs(3100, 3000, 2333, seed=61 + 2 * tA + tB)
     prob = Problem(A, B, C0, 1.25, -0.75, tA, tB, pads=(4, 8, 3))
-    check(prob, mode, oracle_mod, sample_rows(1, 3100, 24, seed=tA + 2 * tB, tile=256))
+    check(prob, mode, oracle_mod, sample_rows(1, 3100, 24, seed=tA + 2 * tB, tile=256), opA0=A[0])
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -68,7 +80,7 @@ def test_planes_route_unaligned_operands(oracle_mod, mode):
     A, B, C0 = workloads.random_inputs(3100, 3000, 2333, seed=67)
     for tA, tB in ((0, 0), (1, 1)):
         prob = Problem(A, B, C0, 1.0, 0.5, tA, tB, pads=(1, 3, 1), offsets=(1, 3, 2))
-        check(prob, mode, oracle_mod, sample_rows(1, 3100, 16, seed=5, tile=256), route=False)
+        check(prob, mode, oracle_mod, sample_rows(1, 3100, 16, seed=5, tile=256), opA0=A[0])
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -78,7 +90,7 @@ def test_planes_route_batched_broadcast(oracle_mod, mode):
     Q = 3
     A, B, C0 = workloads.random_inputs(3100, 3000, 800, Q=Q, seed=71)
     prob = Problem(A[:1].repeat(Q, axis=0), B, C0, 0.5, 1.0, 0, 1, strideA=0)
-    check(prob, mode, oracle_mod, sample_rows(Q, 3100, 24, seed=6, tile=256))
+    check(prob, mode, oracle_mod, sample_rows(Q, 3100, 24, seed=6, tile=256), opA0=A[0, 0])
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -89,7 +101,8 @@ def test_planes_route_integer_bit_exact(oracle_mod, mode):
     A, B, C0 = workloads.integer_inputs(3072, 3072, 2000, seed=73)
     for tA, tB in ((0, 0), (1, 1)):
         prob = Problem(A, B, C0, 2.0, -1.0, tA, tB)
-        check(prob, mode, oracle_mod, sample_rows(1, 3072, 16, seed=7, tile=256), exact=True)
+        check(prob, mode, oracle_mod, sample_rows(1, 3072, 16, seed=7, tile=256), exact=True,
+              opA0=A[0])
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -101,7 +114,7 @@ def test_planes_route_small_workspace_falls_back(oracle_mod, mode):
     prob = Problem(A, B, C0, 1.0, 0.0)
     full = lib.sgemm_workspace_size(mode, 3100, 3000, 2333, 1)
     C, n = launches_of(lambda: prob.run_gpu(mode, api="ws", ws_bytes=full // 4))
-    assert n <= 2
+    assert n <= 2  # the pair kernel and at most a fix-up: no pass
     rows = sample_rows(1, 3100, 16, seed=8, tile=256)
     Cref, D = prob.oracle(oracle_mod, rows=rows)
     got = np.stack([C[q, i] for q, i in rows])
