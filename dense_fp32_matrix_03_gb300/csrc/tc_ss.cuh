@@ -228,6 +228,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
+            // Launched as a programmatic dependent (launch_ss): the set-up
+            // above overlapped the previous kernel's tail; its writes (the
+            // operands' planes or copies) are visible after this wait.  Every
+            // other access to memory (MMAs, epilogue loads and stores of C
+            // and of split slots) follows the loads issued below.
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             tc::Ring<STAGES> rr;
             long long issued = 0;
             bool ok = true;
@@ -377,9 +383,19 @@ int launch_ss(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB, int sl
         return SGEMM_ERR_LAUNCH;
     long long pairs = plan.p.num_units;
     if (pairs > slots) pairs = slots;
-    kern<<<static_cast<unsigned>(2 * pairs), tcs::kThreads, smem, plan.stream>>>(tmA, tmB,
-                                                                                 plan.p);
-    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    // programmatic dependent launch: the CTAs' set-up (barriers, TMEM,
+    // descriptor prefetch) overlaps the end of the kernel before
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    cfg.blockDim = dim3(tcs::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = plan.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, plan.p) != cudaSuccess) return SGEMM_ERR_LAUNCH;
     note_launch();
     return plan.p.splits > 1 ? launch_fixup(plan, tcs::PM, tcs::BN) : SGEMM_OK;
 }
