@@ -261,6 +261,8 @@ int run_planes(Plan &plan, bool &taken)
     if (plan.ws == nullptr) return SGEMM_OK;
     const int planes = plan.mode == SGEMM_MODE_3XTF32 ? 2 : 1;
     const int QA = (p.Q > 1 && p.sA != 0) ? p.Q : 1, QB = (p.Q > 1 && p.sB != 0) ? p.Q : 1;
+    // plane * entries + entry indexes the tensor maps' third dimension (int)
+    if (2LL * p.Q > 0x7FFFFFFFLL) return SGEMM_OK;
     const size_t need = planes_bytes(plan.mode, p.M, p.N, p.K, QA, QB);
     if (need > plan.ws_bytes || !planes_pay(plan.mode, p.M, p.N, p.K, QA, QB, p.Q, plan.num_sms))
         return SGEMM_OK;
