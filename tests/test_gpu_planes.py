@@ -119,3 +119,13 @@ def test_planes_route_small_workspace_falls_back(oracle_mod, mode):
     Cref, D = prob.oracle(oracle_mod, rows=rows)
     got = np.stack([C[q, i] for q, i in rows])
     assert oracle_mod.max_rel_err(got, Cref, D) <= TOL[mode]
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_planes_route_long_k(oracle_mod, mode):
+    """2900 x 3000 x 12001: hundreds of k-blocks, K odd (the pass zero-fills
+    the last group of four, TMA the rest of the last box), the last wave's
+    tiles split along K into many slices; B stored transposed."""
+    A, B, C0 = workloads.random_inputs(2900, 3000, 12001, seed=83)
+    prob = Problem(A, B, C0, 1.0, 0.25, 0, 1)
+    check(prob, mode, oracle_mod, sample_rows(1, 2900, 12, seed=9, tile=256), opA0=A[0])
