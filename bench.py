@@ -394,6 +394,9 @@ def main():
     ap.add_argument("--half-only", action="store_true",
                     help="instead of the benchmark line, print one JSON line with the "
                          "16-bit-input path's figures (bf16 / fp16 at 4092^3 and 8192^3)")
+    ap.add_argument("--bmm-only", action="store_true",
+                    help="instead of the benchmark line, print one JSON line with the batched "
+                         "workload's figures on --mode (3xtf32 for auto), --steps timed calls")
     ap.add_argument("--all-configs", action="store_true",
                     help="instead of the benchmark line, print one JSON line per workload "
                          "configuration and path (256^3, ragged, size sweep, batched)")
@@ -408,6 +411,8 @@ def main():
         return all_configs(args)
     if args.half_only:
         return half_only()
+    if args.bmm_only:
+        return bmm_only(args.mode, args.steps)
 
     import torch
     import dense_fp32_matrix_03_gb300 as lib
@@ -621,22 +626,48 @@ def extra_figures(lib, default_mode, dev, stream, flush, num_sms, peaks, peak_sr
                               "frac": tf / peak}
     del A, B, C
     out["half"] = half_figures(lib, dev, stream, flush, peaks, peak_src)
+    out["bmm"] = bmm_figures(lib, default_mode, dev, stream, flush)
+    return out
+
+
+def bmm_figures(lib, mode, dev, stream, flush, steps=10):
+    """The batched workload (Q=32, 1024x1024x512, B stored N x K and K x N)
+    through the workspace entry on `mode`: TFLOP/s per layout."""
+    import torch
+    import workloads
+    out = {}
     wb = workloads.make("bmm_q32_1024x1024x512")
     Q, M, N, K = wb["Q"], wb["M"], wb["N"], wb["K"]
     A = torch.from_numpy(wb["A"]).to(dev)
     Bn = torch.from_numpy(wb["B"]).to(dev)                             # Q x K x N
     Bt = torch.from_numpy(wb["B"].transpose(0, 2, 1).copy()).to(dev)   # Q x N x K
     C = torch.from_numpy(wb["C0"]).to(dev)
-    ws_bytes, ws = workspace(lib, default_mode, M, N, K, Q, dev)
+    ws_bytes, ws = workspace(lib, mode, M, N, K, Q, dev)
     for tB, Bd, ldb in ((1, Bt, K), (0, Bn, N)):
         def call(tB=tB, Bd=Bd, ldb=ldb):
-            lib.check(lib.sgemm_batched_ex_ws(default_mode, M, N, K, wb["alpha"], A, K, Bd, ldb,
+            lib.check(lib.sgemm_batched_ex_ws(mode, M, N, K, wb["alpha"], A, K, Bd, ldb,
                                               wb["betas"][0], C, N, 0, tB, M * K, K * N, M * N, Q,
                                               ws, ws_bytes, stream))
-        t = statistics.median(time_calls(call, 10, 3, stream, flush))
-        out["bmm"][f"transB={tB}"] = {"tflops": gemm_flops(M, N, K, Q) / (t / 1e3) / 1e12,
-                                      "ms": t, "mode": default_mode}
+        t = statistics.median(time_calls(call, steps, 3, stream, flush))
+        out[f"transB={tB}"] = {"tflops": gemm_flops(M, N, K, Q) / (t / 1e3) / 1e12,
+                               "ms": t, "mode": mode}
     return out
+
+
+def bmm_only(mode, steps):
+    """--bmm-only: the batched workload alone (a short command to profile)."""
+    import torch
+    import dense_fp32_matrix_03_gb300 as lib
+    dev = torch.device("cuda", 0)
+    lib.load()
+    if mode == "auto":
+        mode = "3xtf32"
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    out = bmm_figures(lib, mode, dev, torch.cuda.current_stream(dev), flush, steps)
+    print(json.dumps({"bmm": out, "l2": "flushed before every timed step"}), flush=True)
+    return 0
 
 
 def half_only():
