@@ -101,9 +101,9 @@ int sgemm_batched_ex(int mode, int M, int N, int K, float alpha, const float *A,
  * cuBLAS use at 256^3 ("From 1% to 94% of cuBLAS", comparison across sizes).
  * Each slice's partial tile needs scratch memory, which the caller provides:
  *
- * sgemm_workspace_size returns the bytes of workspace the preferred split
- * plan wants for this shape on the current device (0: the shape is not
- * split, or the arguments are invalid, or there is no usable device).
+ * sgemm_workspace_size returns the bytes of workspace the preferred plan
+ * wants for this shape on the current device (0: the shape needs none, or
+ * the arguments are invalid, or there is no usable device).
  *
  * sgemm_batched_ex_ws is sgemm_batched_ex plus a DEVICE workspace owned by
  * the caller: `workspace` must be 256-byte aligned when workspace_bytes > 0
@@ -120,9 +120,19 @@ int sgemm_batched_ex(int mode, int M, int N, int K, float alpha, const float *A,
  * bytes, of an operand TMA cannot describe (row pitch or batch stride not a
  * multiple of 4 floats, base not 16-byte aligned), which then runs on the
  * TMA-fed kernel instead of the slower direct-load one.  sgemm_workspace_size
- * counts that room for both operands.  The
- * workspace needs no initialisation; it must not be used by another call
- * running at the same time. */
+ * counts that room for both operands.  For shapes where it pays (the
+ * library's time model: the pass over the operands must cost less than the
+ * product saves -- at 4092^3 yes, at 2048^3 or the batched 1024 x 1024 x 512
+ * case no), the tensor-core paths instead use the workspace for the
+ * operands' TF32 planes: a pass writes op(A) and op(B) K-major, rows of
+ * round_up(K, 32) floats, as hi and lo planes (3xTF32: the value with its 13
+ * low mantissa bits cleared, and the rest likewise) or one plane rounded to
+ * nearest (TF32), 2 * (M + N) * K * 4 bytes per batch entry for 3xTF32, and
+ * the product reads them through TMA with no conversion; the workspace then
+ * starts with op(A)'s planes.  sgemm_workspace_size counts that room where
+ * the route pays; with less, the call runs the other way.  The workspace
+ * needs no initialisation; it must not be used by another call running at
+ * the same time. */
 size_t sgemm_workspace_size(int mode, int M, int N, int K, int Q);
 int sgemm_batched_ex_ws(int mode, int M, int N, int K, float alpha, const float *A, int lda,
                         const float *B, int ldb, float beta, float *C, int ldc, int transA,
