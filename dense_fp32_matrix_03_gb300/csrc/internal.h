@@ -111,9 +111,11 @@ int run_planes(Plan &plan, bool &taken);
 // false).  Each route's product takes the split planner's modelled time for
 // its tiles (choose_plan: 256 x 256 pair tiles at the planes rate; the pair
 // kernel's tiles at its rate), and the planes route adds its pass, which
-// moves (QA * M + QB * N) * K * 4 * (1 + planes) bytes at 5.5 TB/s, and
-// 10 us for its two extra launches and the shorter grid's ramp (fitted on
-// GB300: 2048^3 runs faster on the pair kernel, 4096^3 on the planes).
+// moves (QA * M + QB * N) * K * 4 * (1 + planes) bytes at 6.0 TB/s, and
+// 7 us for its extra launch and the shorter grid's ramp (fitted on GB300,
+// TFLOP/s pair / planes: 2048^3 3xTF32 213 / 208, TF32 393 / 376; 2560^3
+// TF32 457 / 470; 4096 x 4096 x 1024 3xTF32 253 / 267; 2048 x 2048 x 8192
+// 3xTF32 264 / 244).
 bool planes_pay(int mode, long long M, long long N, long long K, int QA, int QB, int Q,
                 int num_sms);
 // Multiprocessors of the current device, 0 when there is no usable one.

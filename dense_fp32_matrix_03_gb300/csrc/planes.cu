@@ -232,7 +232,7 @@ bool planes_pay(int mode, long long M, long long N, long long K, int QA, int QB,
         static_cast<long long>(Q) * ((M + tcs::PM - 1) / tcs::PM) * ((N + tcs::BN - 1) / tcs::BN);
     const double bytes = static_cast<double>(QA * M + QB * N) * K * 4.0 * (1 + planes);
     const double t_planes =
-        bytes / 5.5e12 + 10e-6 +
+        bytes / 6.0e12 + 7e-6 +
         choose_plan(ss_tiles, static_cast<int>(K), slots, mode, tcs::PM, tcs::BN, kFeedPlanes, any)
             .seconds;
     return t_planes < t_pair;

@@ -172,10 +172,10 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
             return r256(Q * max(rows * r32(K), K * r32(rows)) * 4)
         planes = 2 if mode == "3xtf32" else 1
         # the planes route where it pays: the modelled time of its tiles' plan
-        # plus its pass ((M + N) * K * Q * 4 * (1 + planes) bytes at 5.5 TB/s)
-        # and 10 us, against the modelled time of the pair kernel's plan
+        # plus its pass ((M + N) * K * Q * 4 * (1 + planes) bytes at 6.0 TB/s)
+        # and 7 us, against the modelled time of the pair kernel's plan
         t_pair = plan(*kernels[1])[1]
-        t_planes = plan(*kernels[2])[1] + (M + N) * K * Q * 4.0 * (1 + planes) / 5.5e12 + 10e-6
+        t_planes = plan(*kernels[2])[1] + (M + N) * K * Q * 4.0 * (1 + planes) / 6.0e12 + 7e-6
         room = copy(M) + copy(N)
         if t_planes < t_pair:
             room = max(room, r256(planes * Q * M * r32(K) * 4) + r256(planes * Q * N * r32(K) * 4))
