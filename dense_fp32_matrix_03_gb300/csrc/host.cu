@@ -1,10 +1,12 @@
 // host.cu -- the product on host buffers.  The operands are copied into a
 // device buffer the caller provides, the product is computed there, and C
-// is copied back.  C is cut into panels of rows and, for large K, K into two
-// slices: the copy-in of one (slice, panel), the product of the previous one
-// and the copy-out of a finished panel run at the same time on three streams
-// (the caller's, for the products, and two of the library's own, one per
-// copy direction), ordered by events.
+// is copied back.  op(B) is copied first, then C is cut into panels of rows:
+// the copy-in of one panel's rows of op(A), the products of earlier panels
+// and the copy-out of a finished one run at the same time on four streams,
+// ordered by events -- the products of even panels on the caller's stream,
+// of odd panels on a library stream (each with its own split-K workspace),
+// so that one panel's product fills the multiprocessors the previous one's
+// last wave leaves idle, and one library stream per copy direction.
 #include <cstdint>
 #include <mutex>
 
@@ -19,19 +21,17 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxPanels = 64;
-// K from which the call cuts the product in two K slices (below it, half of
-// op(B) arrives too soon for the overlap to pay for a second pass over C).
-constexpr int kKSplitMin = 1024;
 
-// Copy streams of a device, made on first use and kept for the process.
+// Copy streams (and the second product stream) of a device, made on first
+// use and kept for the process.
 struct CopyStreams {
     bool ready = false;
-    cudaStream_t in = nullptr, out = nullptr;
+    cudaStream_t in = nullptr, out = nullptr, comp = nullptr;
 };
 std::mutex g_copy_mu;
 CopyStreams g_copy[kMaxDevices];
 
-bool copy_streams(cudaStream_t *in, cudaStream_t *out)
+bool copy_streams(cudaStream_t *in, cudaStream_t *out, cudaStream_t *comp)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
@@ -43,31 +43,52 @@ bool copy_streams(cudaStream_t *in, cudaStream_t *out)
             cudaStreamDestroy(c.in);
             return false;
         }
+        if (cudaStreamCreateWithFlags(&c.comp, cudaStreamNonBlocking) != cudaSuccess) {
+            cudaStreamDestroy(c.in);
+            cudaStreamDestroy(c.out);
+            return false;
+        }
         c.ready = true;
     }
     *in = c.in;
     *out = c.out;
+    *comp = c.comp;
     return true;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// A pitched copy; one contiguous copy when both pitches equal the row width
+// (measured on GB300, 3xTF32 at 4092^3: a call took 1.084 ms with every
+// copy in the 2-D form, 0.992 ms with the contiguous ones issued as 1-D
+// copies).
+cudaError_t copy_rows(void *dst, size_t dpitch, const void *src, size_t spitch, size_t width,
+                      size_t height, cudaMemcpyKind kind, cudaStream_t s)
+{
+    if (dpitch == width && spitch == width)
+        return cudaMemcpyAsync(dst, src, width * height, kind, s);
+    return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, height, kind, s);
+}
 long long round4(long long x) { return x < 4 ? 4 : (x + 3) & ~3LL; }
 
 // Where everything sits in the caller's device buffer.  Each operand is
 // stored with its rows padded to a multiple of four floats, so that the
-// kernels' TMA feeds can describe it whatever the host pitch.
+// kernels' TMA feeds can describe it whatever the host pitch; then one
+// split-K workspace per product stream.
 struct Layout {
     long long ldA, ldB, ldC;       // device row pitches (elements)
-    size_t offA, offB, offC, offW; // byte offsets into the buffer
+    size_t offA, offB, offC, offW; // byte offsets into the buffer (offW: two workspaces)
     size_t ws_bytes, total;
     int panel, panels;             // rows of C per panel, panel count
 };
 
-// Rows per panel when the caller leaves it to the library: enough output
-// tiles for about one wave of the GPU per panel (measured on GB300 at
-// 4092^3: one to two waves per panel beat both fewer, larger panels, whose
-// first copy-in and last copy-out overlap nothing, and smaller ones, which
-// leave multiprocessors idle in every product), at most kMaxPanels.
+// Rows per panel when the caller leaves it to the library: as many whole
+// rows of output tiles as fit in one wave of the GPU (at least one), so
+// that two panels' products, on the two product streams, together fill it
+// (measured on GB300, 3xTF32 at 4092^3 with 1-D copies, ms per call:
+// 512-row panels 1.004, 768 1.086, 1024 1.117; on one product stream
+// 1.133 / 1.079 / 1.108; the earlier schedule, K cut in two slices with
+// 768-row panels on one product stream, 1.076), at most kMaxPanels.
 int auto_panel_rows(int mode, int M, int N, int K, int num_sms)
 {
     int bm = 0, bn = 0, slots = num_sms;
@@ -78,7 +99,7 @@ int auto_panel_rows(int mode, int M, int N, int K, int num_sms)
         slots = tc_pair_slots(num_sms);
     }
     const long long tiles_n = (N + bn - 1) / bn;
-    long long rows_tiles = (static_cast<long long>(slots) + tiles_n - 1) / tiles_n;
+    long long rows_tiles = static_cast<long long>(slots) / tiles_n;
     if (rows_tiles < 1) rows_tiles = 1;
     long long rows = rows_tiles * bm;
     const long long min_rows = (M + kMaxPanels - 1) / kMaxPanels;
@@ -111,7 +132,7 @@ bool make_layout(int mode, int M, int N, int K, int transA, int transB, int pane
     L->offB = align256(L->offA + 4ull * rowsA * L->ldA);
     L->offC = align256(L->offB + 4ull * rowsB * L->ldB);
     L->offW = align256(L->offC + 4ull * M * L->ldC);
-    L->total = L->offW + L->ws_bytes;
+    L->total = L->offW + 2 * align256(L->ws_bytes);
     return true;
 }
 
@@ -163,24 +184,20 @@ int sgemm_host(int mode, int M, int N, int K, float alpha, const float *A, int l
         return SGEMM_ERR_INVALID_ARG;
     if (dev_bytes < L.total) return SGEMM_ERR_INVALID_ARG;
 
-    cudaStream_t st = static_cast<cudaStream_t>(stream), in = nullptr, out = nullptr;
-    if (!copy_streams(&in, &out)) return SGEMM_ERR_LAUNCH;
+    cudaStream_t st = static_cast<cudaStream_t>(stream), in = nullptr, out = nullptr,
+                 comp = nullptr;
+    if (!copy_streams(&in, &out, &comp)) return SGEMM_ERR_LAUNCH;
     uint8_t *base = static_cast<uint8_t *>(dev);
     float *dA = reinterpret_cast<float *>(base + L.offA);
     float *dB = reinterpret_cast<float *>(base + L.offB);
     float *dC = reinterpret_cast<float *>(base + L.offC);
-    void *ws = L.ws_bytes ? base + L.offW : nullptr;
+    // panel p's product: stream and split-K workspace of its parity
+    void *ws_of[2] = {L.ws_bytes ? base + L.offW : nullptr,
+                      L.ws_bytes ? base + L.offW + align256(L.ws_bytes) : nullptr};
+    cudaStream_t st_of[2] = {st, comp};
 
-    // K is cut into kslices slices (two when K is large): the products of
-    // the first slice start once half of op(B) has arrived, while the rest
-    // of the copy-in is still under way; later slices accumulate (beta = 1).
-    // Slice boundaries are multiples of 32 so every slice of the device
-    // copies stays 16-byte aligned.
-    const int kslices = (reads_ab && K >= kKSplitMin) ? 2 : 1;
-    long long kb[3] = {0, K, K};
-    if (kslices == 2) kb[1] = (K / 2) / 32 * 32;
-
-    cudaEvent_t fork = nullptr, join = nullptr, ready[2][kMaxPanels] = {}, done[kMaxPanels] = {};
+    cudaEvent_t fork = nullptr, join = nullptr, join2 = nullptr, ready[kMaxPanels] = {},
+                done[kMaxPanels] = {};
     int rc = SGEMM_OK;
     auto ok = [&rc](cudaError_t e) {
         if (e != cudaSuccess && rc == SGEMM_OK) rc = SGEMM_ERR_LAUNCH;
@@ -188,76 +205,67 @@ int sgemm_host(int mode, int M, int N, int K, float alpha, const float *A, int l
     };
     const unsigned flags = cudaEventDisableTiming;
     bool made = ok(cudaEventCreateWithFlags(&fork, flags)) &&
-                ok(cudaEventCreateWithFlags(&join, flags));
-    for (int p = 0; made && p < L.panels; ++p) {
-        made = ok(cudaEventCreateWithFlags(&done[p], flags));
-        for (int h = 0; made && h < kslices; ++h)
-            made = ok(cudaEventCreateWithFlags(&ready[h][p], flags));
-    }
+                ok(cudaEventCreateWithFlags(&join, flags)) &&
+                ok(cudaEventCreateWithFlags(&join2, flags));
+    for (int p = 0; made && p < L.panels; ++p)
+        made = ok(cudaEventCreateWithFlags(&done[p], flags)) &&
+               ok(cudaEventCreateWithFlags(&ready[p], flags));
 
-    // The copies wait for whatever the caller queued on `stream` before.
+    // Every stream waits for whatever the caller queued on `stream` before.
     if (made && ok(cudaEventRecord(fork, st)) && ok(cudaStreamWaitEvent(in, fork, 0)) &&
-        ok(cudaStreamWaitEvent(out, fork, 0))) {
+        ok(cudaStreamWaitEvent(out, fork, 0)) && ok(cudaStreamWaitEvent(comp, fork, 0))) {
         const size_t f = sizeof(float);
-        for (int h = 0; rc == SGEMM_OK && h < kslices; ++h) {
-            const long long k0 = kb[h], kn = kb[h + 1] - kb[h];
-            // slice h of op(B): rows k0 .. k0+kn of K x N, or columns of N x K
-            float *sB = transB ? dB + k0 : dB + k0 * L.ldB;
+        if (reads_ab)  // op(B) whole: K x N, or N x K when transposed
+            ok(transB ? copy_rows(dB, L.ldB * f, B, ldb * f, K * f, N,
+                                          cudaMemcpyHostToDevice, in)
+                      : copy_rows(dB, L.ldB * f, B, ldb * f, N * f, K,
+                                          cudaMemcpyHostToDevice, in));
+        for (int p = 0; rc == SGEMM_OK && p < L.panels; ++p) {
+            const long long m0 = static_cast<long long>(p) * L.panel;
+            const int rows = static_cast<int>(M - m0 < L.panel ? M - m0 : L.panel);
+            // this panel's rows of op(A) (columns m0.. of A when transposed)
+            float *pA = transA ? dA + m0 : dA + m0 * L.ldA;
+            float *pC = dC + m0 * L.ldC;
             if (reads_ab) {
-                if (transB)
-                    ok(cudaMemcpy2DAsync(sB, L.ldB * f, B + k0, ldb * f, kn * f, N,
+                if (transA)
+                    ok(copy_rows(pA, L.ldA * f, A + m0, lda * f, rows * f, K,
                                          cudaMemcpyHostToDevice, in));
                 else
-                    ok(cudaMemcpy2DAsync(sB, L.ldB * f, B + k0 * ldb, ldb * f, N * f, kn,
+                    ok(copy_rows(pA, L.ldA * f, A + m0 * lda, lda * f, K * f, rows,
                                          cudaMemcpyHostToDevice, in));
             }
-            for (int p = 0; rc == SGEMM_OK && p < L.panels; ++p) {
-                const long long m0 = static_cast<long long>(p) * L.panel;
-                const int rows = static_cast<int>(M - m0 < L.panel ? M - m0 : L.panel);
-                // slice h of this panel's rows of op(A)
-                float *pA = transA ? dA + k0 * L.ldA + m0 : dA + m0 * L.ldA + k0;
-                float *pC = dC + m0 * L.ldC;
-                if (reads_ab) {
-                    if (transA)
-                        ok(cudaMemcpy2DAsync(pA, L.ldA * f, A + k0 * lda + m0, lda * f, rows * f,
-                                             kn, cudaMemcpyHostToDevice, in));
-                    else
-                        ok(cudaMemcpy2DAsync(pA, L.ldA * f, A + m0 * lda + k0, lda * f, kn * f,
-                                             rows, cudaMemcpyHostToDevice, in));
-                }
-                if (h == 0 && beta != 0.f)
-                    ok(cudaMemcpy2DAsync(pC, L.ldC * f, C + m0 * ldc, ldc * f, N * f, rows,
-                                         cudaMemcpyHostToDevice, in));
-                if (!ok(cudaEventRecord(ready[h][p], in)) ||
-                    !ok(cudaStreamWaitEvent(st, ready[h][p], 0)))
-                    break;
-                const int g = sgemm_batched_ex_ws(
-                    mode, rows, N, static_cast<int>(kn), alpha, reads_ab ? pA : nullptr,
-                    static_cast<int>(L.ldA), reads_ab ? sB : nullptr, static_cast<int>(L.ldB),
-                    h == 0 ? beta : 1.f, pC, static_cast<int>(L.ldC), transA, transB, 0, 0, 0, 1,
-                    ws, L.ws_bytes, st);
-                if (g != SGEMM_OK) {
-                    rc = g;
-                    break;
-                }
-                if (h + 1 < kslices) continue;
-                if (!ok(cudaEventRecord(done[p], st)) || !ok(cudaStreamWaitEvent(out, done[p], 0)))
-                    break;
-                ok(cudaMemcpy2DAsync(C + m0 * ldc, ldc * f, pC, L.ldC * f, N * f, rows,
-                                     cudaMemcpyDeviceToHost, out));
+            if (beta != 0.f)
+                ok(copy_rows(pC, L.ldC * f, C + m0 * ldc, ldc * f, N * f, rows,
+                                     cudaMemcpyHostToDevice, in));
+            cudaStream_t ps = st_of[p & 1];
+            if (!ok(cudaEventRecord(ready[p], in)) || !ok(cudaStreamWaitEvent(ps, ready[p], 0)))
+                break;
+            const int g = sgemm_batched_ex_ws(
+                mode, rows, N, K, alpha, reads_ab ? pA : nullptr, static_cast<int>(L.ldA),
+                reads_ab ? dB : nullptr, static_cast<int>(L.ldB), beta, pC,
+                static_cast<int>(L.ldC), transA, transB, 0, 0, 0, 1, ws_of[p & 1], L.ws_bytes,
+                ps);
+            if (g != SGEMM_OK) {
+                rc = g;
+                break;
             }
+            if (!ok(cudaEventRecord(done[p], ps)) || !ok(cudaStreamWaitEvent(out, done[p], 0)))
+                break;
+            ok(copy_rows(C + m0 * ldc, ldc * f, pC, L.ldC * f, N * f, rows,
+                                 cudaMemcpyDeviceToHost, out));
         }
     }
-    // `stream` reaches its next work only once every copy-out is done (also
-    // after a failure part-way, so that nothing the call queued outlives it
-    // unordered).
+    // `stream` reaches its next work only once every copy-out and every
+    // product on the second stream is done (also after a failure part-way,
+    // so that nothing the call queued outlives it unordered).
     if (join && cudaEventRecord(join, out) == cudaSuccess) ok(cudaStreamWaitEvent(st, join, 0));
+    if (join2 && cudaEventRecord(join2, comp) == cudaSuccess) ok(cudaStreamWaitEvent(st, join2, 0));
     // Destroying a recorded event is safe: it is released once it completes.
     if (fork) cudaEventDestroy(fork);
     if (join) cudaEventDestroy(join);
+    if (join2) cudaEventDestroy(join2);
     for (int p = 0; p < L.panels; ++p) {
-        for (int h = 0; h < 2; ++h)
-            if (ready[h][p]) cudaEventDestroy(ready[h][p]);
+        if (ready[p]) cudaEventDestroy(ready[p]);
         if (done[p]) cudaEventDestroy(done[p]);
     }
     return rc;

@@ -210,12 +210,15 @@ int sgemm_half_batched(int type, int M, int N, int K, float alpha, const void *A
  * sgemm_batched (one product, no batch).  The call copies op(A), op(B) and,
  * when beta != 0, C into `dev`, a DEVICE buffer the caller owns (256-byte
  * aligned, at least sgemm_host_buffer_size(...) bytes), computes there, and
- * copies C back.  C is cut into panels of `panel_rows` rows (0: the library
- * picks about two waves of output tiles per panel; at most 64 panels, else
- * SGEMM_ERR_INVALID_ARG): the copy-in of one panel, the product of the
- * previous one and the copy-out of the one before run at the same time, on
- * two copy streams the library keeps per device and on `stream` for the
- * products.  The call is asynchronous like the others: C on the host holds
+ * copies C back.  op(B) is copied first; C is cut into panels of
+ * `panel_rows` rows (0: the library picks as many whole rows of output tiles
+ * as fit in one wave of the GPU; at most 64 panels, else
+ * SGEMM_ERR_INVALID_ARG): the copy-in of one panel's rows of op(A), the
+ * products of earlier panels and the copy-out of a finished one run at the
+ * same time, on two copy streams the library keeps per device, on `stream`
+ * for the products of even panels and on a third library stream for those of
+ * odd panels (so that two products together fill the GPU).  The call is
+ * asynchronous like the others: C on the host holds
  * the result once `stream` has reached the end of the call (synchronise it,
  * or record an event after the call).  Host memory that is page-locked
  * (cudaHostAlloc / cudaHostRegister) is copied at full speed and overlaps;
@@ -226,8 +229,8 @@ int sgemm_half_batched(int type, int M, int N, int K, float alpha, const void *A
  *
  * sgemm_host_buffer_size returns the bytes of `dev` such a call needs (0 for
  * invalid arguments or without a usable device): the three operands with
- * rows padded to a multiple of four floats, plus the split-K / transposition
- * workspace of the panel product. */
+ * rows padded to a multiple of four floats, plus two split-K / transposition
+ * workspaces of a panel product (one per product stream). */
 size_t sgemm_host_buffer_size(int mode, int M, int N, int K, int transA, int transB,
                               int panel_rows);
 int sgemm_host(int mode, int M, int N, int K, float alpha, const float *A, int lda,

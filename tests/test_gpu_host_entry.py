@@ -160,10 +160,10 @@ def test_peak_probe_runs_and_is_plausible(kind):
 
 @pytest.mark.parametrize("tA,tB", [(0, 0), (1, 0), (0, 1), (1, 1)])
 @pytest.mark.parametrize("mode", MODES)
-def test_host_entry_k_slices(oracle_mod, mode, tA, tB):
-    """K >= 1024: the call cuts K in two slices (the second pass accumulates
-    with beta = 1); random data within tolerance, integer data bit for bit
-    (power-of-two alpha, integer beta: both passes are exact)."""
+def test_host_entry_long_k(oracle_mod, mode, tA, tB):
+    """Long K (1500, 1100) with 256- and 128-row panels, products of even
+    and odd panels on two streams: random data within tolerance, integer
+    data bit for bit."""
     A, B, C0 = workloads.random_inputs(600, 500, 1500, seed=41)
     prob = Problem(A, B, C0, 1.5, -0.5, tA, tB, pads=(2, 1, 3))
     C = run_host(prob, mode, panel_rows=256)
