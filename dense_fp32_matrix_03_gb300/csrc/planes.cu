@@ -253,6 +253,38 @@ size_t planes_bytes(int mode, long long M, long long N, long long K, int QA, int
            round256(static_cast<size_t>(planes) * QB * N * ldp * sizeof(float));
 }
 
+// The product on planes already written (A's at pa, B's at pb; QA / QB
+// stored batch entries per plane): tensor maps, split plan (in plan.ws),
+// launch.
+static int product_on_planes(Plan &plan, const float *pa, const float *pb, int QA, int QB)
+{
+    GemmParams &p = plan.p;
+    const int planes = plan.mode == SGEMM_MODE_3XTF32 ? 2 : 1;
+    const long long ldp = plane_pitch(p.K);
+    alignas(64) CUtensorMap tmA;
+    alignas(64) CUtensorMap tmB;
+    std::memset(&tmA, 0, sizeof(tmA));
+    std::memset(&tmB, 0, sizeof(tmB));
+    if (!encode_operand(&tmA, pa, true, p.M, p.K, ldp, planes * QA, p.M * ldp, tcs::BM) ||
+        !encode_operand(&tmB, pb, true, p.N, p.K, ldp, planes * QB, p.N * ldp, tcs::HN))
+        return SGEMM_ERR_UNSUPPORTED;
+
+    p.a_q_step = QA > 1 ? 1 : 0;
+    p.b_q_step = QB > 1 ? 1 : 0;
+    const int stage_k = planes == 2 ? tcs::Shape<tcs::KindTF32<2>>::STAGE_K
+                                    : tcs::Shape<tcs::KindTF32<1>>::STAGE_K;
+    p.k_blocks = (p.K + stage_k - 1) / stage_k;
+    p.group_m = kGroupM;
+    p.tiles_m = (p.M + tcs::PM - 1) / tcs::PM;
+    p.tiles_n = (p.N + tcs::BN - 1) / tcs::BN;
+    p.num_tiles = static_cast<long long>(p.Q) * p.tiles_m * p.tiles_n;
+    const int slots = ss_slots(plan.num_sms);
+    const int rc = plan_splits(plan, tcs::PM, tcs::BN, kFeedPlanes, slots);
+    if (rc != SGEMM_OK) return rc;
+    return planes == 2 ? launch_ss<tcs::KindTF32<2>>(plan, tmA, tmB, slots)
+                       : launch_ss<tcs::KindTF32<1>>(plan, tmA, tmB, slots);
+}
+
 int run_planes(Plan &plan, bool &taken)
 {
     taken = false;
@@ -282,30 +314,55 @@ int run_planes(Plan &plan, bool &taken)
                          : launch_planes_pass<1>(oa, ob, p.K, ldp, plan.num_sms, plan.stream);
     if (rc != SGEMM_OK) return rc;
 
-    alignas(64) CUtensorMap tmA;
-    alignas(64) CUtensorMap tmB;
-    std::memset(&tmA, 0, sizeof(tmA));
-    std::memset(&tmB, 0, sizeof(tmB));
-    if (!encode_operand(&tmA, pa, true, p.M, p.K, ldp, planes * QA, p.M * ldp, tcs::BM) ||
-        !encode_operand(&tmB, pb, true, p.N, p.K, ldp, planes * QB, p.N * ldp, tcs::HN))
-        return SGEMM_ERR_UNSUPPORTED;
-
-    p.a_q_step = QA > 1 ? 1 : 0;
-    p.b_q_step = QB > 1 ? 1 : 0;
-    const int stage_k = planes == 2 ? tcs::Shape<tcs::KindTF32<2>>::STAGE_K
-                                    : tcs::Shape<tcs::KindTF32<1>>::STAGE_K;
-    p.k_blocks = (p.K + stage_k - 1) / stage_k;
-    p.group_m = kGroupM;
-    p.tiles_m = (p.M + tcs::PM - 1) / tcs::PM;
-    p.tiles_n = (p.N + tcs::BN - 1) / tcs::BN;
-    p.num_tiles = static_cast<long long>(p.Q) * p.tiles_m * p.tiles_n;
     plan.ws = need < plan.ws_bytes ? static_cast<void *>(w + need) : nullptr;
     plan.ws_bytes = need < plan.ws_bytes ? plan.ws_bytes - need : 0;
-    const int slots = ss_slots(plan.num_sms);
-    rc = plan_splits(plan, tcs::PM, tcs::BN, kFeedPlanes, slots);
-    if (rc != SGEMM_OK) return rc;
-    return planes == 2 ? launch_ss<tcs::KindTF32<2>>(plan, tmA, tmB, slots)
-                       : launch_ss<tcs::KindTF32<1>>(plan, tmA, tmB, slots);
+    return product_on_planes(plan, pa, pb, QA, QB);
+}
+
+size_t planes_operand_bytes(int mode, long long rows, long long K)
+{
+    const int planes = mode == SGEMM_MODE_3XTF32 ? 2 : 1;
+    return round256(static_cast<size_t>(planes) * rows * plane_pitch(K) * sizeof(float));
+}
+
+int planes_pass_operand(int mode, const float *src, long long lds, int rows, int K,
+                        bool k_inner, float *dst, int num_sms, cudaStream_t stream)
+{
+    const long long ldp = plane_pitch(K);
+    const PassOperand o = pass_operand(src, lds, 0, rows, K, 1, k_inner, dst, ldp);
+    PassOperand none = o;
+    none.tiles = 0;
+    return mode == SGEMM_MODE_3XTF32
+               ? launch_planes_pass<2>(o, none, K, ldp, num_sms, stream)
+               : launch_planes_pass<1>(o, none, K, ldp, num_sms, stream);
+}
+
+int planes_product(int mode, int M, int N, int K, float alpha, const float *pa,
+                   const float *pb, float beta, float *C, int ldc, void *ws, size_t ws_bytes,
+                   cudaStream_t stream)
+{
+    int num_sms = 0;
+    unsigned int *status = nullptr;
+    if (!current_sm103(&num_sms, &status)) return SGEMM_ERR_UNSUPPORTED;
+    Plan plan{};
+    GemmParams &p = plan.p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.Q = 1;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.C = C;
+    p.ldc = ldc;
+    p.c_vec4 = aligned16(C) && ldc % 4 == 0;
+    p.status = status;
+    p.wait_limit = kWaitLimitCycles;
+    plan.mode = mode;
+    plan.num_sms = num_sms;
+    plan.stream = stream;
+    plan.ws = ws_bytes ? ws : nullptr;
+    plan.ws_bytes = ws_bytes;
+    return product_on_planes(plan, pa, pb, 1, 1);
 }
 
 }  // namespace sg

@@ -174,3 +174,33 @@ def test_host_entry_long_k(oracle_mod, mode, tA, tB):
     C = run_host(prob, mode, panel_rows=128)
     Cref, _ = prob.oracle(oracle_mod)
     assert np.array_equal(C.astype(np.float64), Cref)
+
+
+@pytest.mark.parametrize("tA,tB", [(0, 0), (1, 1), (0, 1), (1, 0)])
+def test_host_entry_planes(oracle_mod, tA, tB):
+    """3xTF32 at 3072 x 3072 x 2000, a shape where the planes route pays: op(B)'s TF32
+    planes are written once, each 512-row panel's op(A) planes on its own
+    product stream, and the products run on the shared-memory-operand
+    kernel -- at least 1 + 2 x 6 launches (pass of B; pass and product per
+    panel), against at most 12 for six panel products and their fix-ups.
+    Random data on sampled rows within tolerance, integer data bit for bit."""
+    import torch
+    mode = "3xtf32"
+    import dense_fp32_matrix_03_gb300 as lib
+    from _helpers import sample_rows
+    M = N = 3072
+    K = 2000
+    rows = sample_rows(1, M, 16, seed=51, tile=256)
+    for data, exact in ((workloads.random_inputs, False), (workloads.integer_inputs, True)):
+        A, B, C0 = data(M, N, K, seed=52)
+        prob = Problem(A, B, C0, 2.0, -1.0, tA, tB)
+        torch.cuda.synchronize()
+        n0 = lib.sgemm_kernel_launches()
+        C = run_host(prob, mode, panel_rows=512)
+        assert lib.sgemm_kernel_launches() - n0 >= 13, "planes not used"
+        Cref, D = prob.oracle(oracle_mod, rows=rows)
+        got = np.stack([C[q, i] for q, i in rows])
+        if exact:
+            assert np.array_equal(got.astype(np.float64), Cref)
+        else:
+            assert oracle_mod.max_rel_err(got, Cref, D) <= TOL[mode]
