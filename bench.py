@@ -40,8 +40,9 @@ UNIT = "TFLOP/s"
 WORKLOAD = "sgemm_4092"
 # Fallbacks when the driver-written measured peaks are absent.
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0}
-# Dense tensor-core throughput ratio tf32 : bf16 (1.1 : 2.25 PFLOP/s nominal).
-TF32_PER_BF16 = 1.1 / 2.25
+# Dense tensor-core throughput ratio tf32 : bf16, nominal 1 : 2 (1.125 : 2.25
+# PFLOP/s per GPU; tables that print the tf32 figure as 1.1 round it).
+TF32_PER_BF16 = 1.0 / 2.0
 FP32_LANES_PER_SM = 128
 
 
@@ -81,9 +82,9 @@ def roofline_peak(mode, num_sms, peaks, source):
                              f"x {mhz:.0f} MHz max SM clock")
     tf32 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * TF32_PER_BF16
     if mode == "3xtf32":
-        return "tensor", tf32 / 3.0, (f"tf32 tensor peak ({source} bf16 burst x 1.1/2.25) "
-                                      f"/ 3 passes; credited 2MNK")
-    return "tensor", tf32, f"tf32 tensor peak ({source} bf16 burst x 1.1/2.25)"
+        return "tensor", tf32 / 3.0, (f"tf32 tensor peak ({source} bf16 burst x the nominal "
+                                      f"tf32:bf16 ratio 1/2) / 3 passes; credited 2MNK")
+    return "tensor", tf32, f"tf32 tensor peak ({source} bf16 burst x the nominal ratio 1/2)"
 
 
 # Sources of the kernels a benchmark call runs and of the host code that
@@ -523,6 +524,8 @@ def main():
     extra = {}
     if not args.no_extra and rank == 0:
         extra = extra_figures(lib, mode, dev, stream, flush, num_sms, peaks, peak_src)
+        extra["configs"] = config_figures(lib, dev, stream, flush, num_sms, peaks, peak_src,
+                                          probes)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -627,6 +630,64 @@ def extra_figures(lib, default_mode, dev, stream, flush, num_sms, peaks, peak_sr
     del A, B, C
     out["half"] = half_figures(lib, dev, stream, flush, peaks, peak_src)
     out["bmm"] = bmm_figures(lib, default_mode, dev, stream, flush)
+    return out
+
+
+def config_figures(lib, dev, stream, flush, num_sms, peaks, peak_src, probes, steps=5):
+    """Every workload configuration on every path, through the workspace
+    entry point (the library's preferred call, with the workspace it asks
+    for): TFLOP/s, the roofline that bounds it -- min(path peak, AI x HBM
+    bandwidth), AI over compulsory bytes -- and the fraction of it; beside
+    it the fraction of the path's probe-measured rate where the compute roof
+    binds.  L2 is flushed before every timed call."""
+    import numpy as np
+    import torch
+    import workloads
+    bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])) / 1e3  # TB/s
+    cases = [("sgemm_256", 0), ("sgemm_ragged_1000x1500x777", 0),
+             ("sgemm_ragged_1000x1500x777", 1)]
+    cases += [(f"sweep_{n}", 0) for n in workloads.SWEEP_SIZES]
+    cases += [("bmm_q32_1024x1024x512", 0)]
+    out = {}
+    for name, beta_idx in cases:
+        w = workloads.make(name)
+        M, N, K, Q = w["M"], w["N"], w["K"], w["Q"]
+        beta = w["betas"][beta_idx]
+        A = torch.from_numpy(w["A"]).to(dev)
+        Bn = torch.from_numpy(w["B"]).to(dev)
+        C = torch.from_numpy(w["C0"]).to(dev)
+        variants = [(0, Bn, N)]
+        if Q > 1:
+            Bt = torch.from_numpy(np.ascontiguousarray(np.swapaxes(w["B"], 1, 2))).to(dev)
+            variants = [(1, Bt, K), (0, Bn, N)]
+        flops = gemm_flops(M, N, K, Q)
+        ai = flops / compulsory_bytes(M, N, K, Q, beta != 0)
+        for tB, Bd, ldb in variants:
+            key = name + (f"_beta={beta:g}" if len(w["betas"]) > 1 else "") + \
+                (f"_transB={tB}" if Q > 1 else "")
+            row = {}
+            for mode in ("fp32", "3xtf32", "tf32"):
+                ws_bytes, ws = workspace(lib, mode, M, N, K, Q, dev)
+
+                def call(mode=mode, Bd=Bd, ldb=ldb, tB=tB, ws=ws, ws_bytes=ws_bytes):
+                    lib.check(lib.sgemm_batched_ex_ws(mode, M, N, K, w["alpha"], A, K, Bd, ldb,
+                                                      beta, C, N, 0, tB, M * K, K * N, M * N, Q,
+                                                      ws, ws_bytes, stream))
+                n_steps = steps if flops < 2e11 else 3
+                ms = statistics.median(time_calls(call, n_steps, 3, stream, flush))
+                tf = flops / (ms / 1e3) / 1e12
+                bound, peak, _ = roofline_peak(mode, num_sms, peaks, peak_src)
+                roof = min(peak, ai * bw)
+                cell = {"tflops": round(tf, 2), "ms": round(ms, 4), "roof": round(roof, 1),
+                        "bound": bound if roof == peak else "hbm", "frac": round(tf / roof, 3)}
+                pp = probe_peak_for(mode, probes) if probes else None
+                if pp:
+                    cell["frac_of_probe_roof"] = round(tf / min(pp, ai * bw), 3)
+                row[mode] = cell
+                del ws
+            out[key] = row
+        del A, Bn, C
+    lib.check(lib.sgemm_poll_error(stream))
     return out
 
 

@@ -48,6 +48,7 @@ MODES = {"fp32": SGEMM_MODE_FP32, "3xtf32": SGEMM_MODE_3XTF32, "tf32": SGEMM_MOD
 _i, _f, _p, _ll = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_longlong
 SIGNATURES = {
     "sgemm": (_i, [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]),
+    "sgemm_ex": (_i, [_i, _i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]),
     "sgemm_batched": (_i, [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _i, _i, _ll, _ll, _ll,
                            _i, _p]),
     "sgemm_batched_ex": (_i, [_i, _i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _i, _i, _ll, _ll,
@@ -141,6 +142,13 @@ def _stream(s):
 def sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
     return _lib.sgemm(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C), ldc,
                       _stream(stream))
+
+
+def sgemm_ex(mode, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
+    if isinstance(mode, str):
+        mode = MODES[mode]
+    return _lib.sgemm_ex(mode, M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C), ldc,
+                         _stream(stream))
 
 
 def sgemm_batched(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, transA, transB, strideA,

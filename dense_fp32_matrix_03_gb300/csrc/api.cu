@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -56,6 +57,14 @@ const DeviceInfo *device_info(int *dev_out)
     }
     return &d;
 }
+
+struct SmemAttr {
+    int dev;
+    const void *kernel;
+    int bytes;
+};
+std::mutex g_attr_mu;
+std::vector<SmemAttr> g_attr;
 
 bool get_encoder()
 {
@@ -253,6 +262,20 @@ bool encode_operand16(CUtensorMap *map, const void *base, bool bf16, long long r
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool smem_attr_once(const void *kernel, int bytes)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    for (const SmemAttr &a : g_attr)
+        if (a.dev == dev && a.kernel == kernel && a.bytes >= bytes) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess)
+        return false;
+    g_attr.push_back(SmemAttr{dev, kernel, bytes});
+    return true;
 }
 
 int min_slice_k(int mode) { return mode == SGEMM_MODE_FP32 ? 64 : 256; }
@@ -679,6 +702,12 @@ int sgemm(int M, int N, int K, float alpha, const float *A, int lda, const float
 {
     return run(SGEMM_MODE_DEFAULT, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, 0, 0, 0, 0, 0,
                1, stream);
+}
+
+int sgemm_ex(int mode, int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+             int ldb, float beta, float *C, int ldc, void *stream)
+{
+    return run(mode, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, 0, 0, 0, 0, 0, 1, stream);
 }
 
 int sgemm_batched(int M, int N, int K, float alpha, const float *A, int lda, const float *B,

@@ -118,6 +118,12 @@ int run_planes(Plan &plan, bool &taken);
 // 3xTF32 264 / 244).
 bool planes_pay(int mode, long long M, long long N, long long K, int QA, int QB, int Q,
                 int num_sms);
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once: the attribute belongs to the function on each device and
+// setting it is a driver call (about a microsecond), so the launchers ask
+// here, which remembers (device, kernel) pairs already set.  False when the
+// runtime refuses.
+bool smem_attr_once(const void *kernel, int bytes);
 // Multiprocessors of the current device, 0 when there is no usable one.
 int num_sms_or_zero();
 // The planes route in parts, for the host-buffer entry (host.cu), which

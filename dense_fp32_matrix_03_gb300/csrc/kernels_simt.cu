@@ -28,10 +28,7 @@ template <class Cfg, bool A_KIN, bool B_KIN, bool USE_TMA, bool EVEN_K>
 int launch_one(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB)
 {
     auto kern = simt_sgemm_kernel<Cfg, A_KIN, B_KIN, USE_TMA, EVEN_K>;
-    // The attribute is per device; setting it on every call costs about a
-    // microsecond and keeps the launcher free of per-device caches.
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg::SMEM_BYTES) != cudaSuccess)
+    if (!smem_attr_once(reinterpret_cast<const void *>(kern), Cfg::SMEM_BYTES))
         return SGEMM_ERR_LAUNCH;
     long long grid = plan.p.num_units;
     if (grid > static_cast<long long>(plan.num_sms) * kMinBlocks)

@@ -28,8 +28,7 @@ int launch_direct(Plan &plan)
 {
     using C = tcd::Cfg<kBN, SPLIT3, A_KIN, B_KIN>;
     auto kern = tcd::tcd_sgemm_kernel<C>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES) != cudaSuccess)
+    if (!smem_attr_once(reinterpret_cast<const void *>(kern), C::SMEM_BYTES))
         return SGEMM_ERR_LAUNCH;
     long long grid = plan.p.num_units;
     if (grid > plan.num_sms) grid = plan.num_sms;

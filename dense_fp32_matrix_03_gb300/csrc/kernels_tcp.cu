@@ -19,8 +19,7 @@ int launch_one(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB, int s
 {
     using C = tcp::Cfg<SPLIT3, A_KIN, B_KIN, WIDE>;
     auto kern = tcp::tcp_sgemm_kernel<C>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES) != cudaSuccess)
+    if (!smem_attr_once(reinterpret_cast<const void *>(kern), C::SMEM_BYTES))
         return SGEMM_ERR_LAUNCH;
     long long pairs = plan.p.num_units;
     if (pairs > slots) pairs = slots;

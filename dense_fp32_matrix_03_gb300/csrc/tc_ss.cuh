@@ -378,9 +378,7 @@ int launch_ss(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB, int sl
 {
     auto kern = tcs::tcs_gemm_kernel<KD>;
     constexpr int smem = tcs::Shape<KD>::SMEM_BYTES;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-        return SGEMM_ERR_LAUNCH;
+    if (!smem_attr_once(reinterpret_cast<const void *>(kern), smem)) return SGEMM_ERR_LAUNCH;
     long long pairs = plan.p.num_units;
     if (pairs > slots) pairs = slots;
     // programmatic dependent launch: the CTAs' set-up (barriers, TMEM,

@@ -74,6 +74,13 @@ extern "C" {
 int sgemm(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
           float beta, float *C, int ldc, void *stream);
 
+/* As sgemm, with the contraction path chosen explicitly (SGEMM_MODE_*;
+ * DEFAULT means the process default): the first kernel's host signature in
+ * "From 1% to 94% of cuBLAS, one kernel at a time" (M, N, K, alpha, A, B,
+ * beta, C) plus the leading dimensions, the mode and the stream. */
+int sgemm_ex(int mode, int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+             int ldb, float beta, float *C, int ldc, void *stream);
+
 /* Strided-batched, transposed-operand form (conventions above), default mode.
  * Requires strideC >= (M-1)*ldc + N when Q > 1 (batch outputs may not
  * overlap); strides must be >= 0. */
@@ -156,7 +163,15 @@ int sgemm_batched_ex_ws(int mode, int M, int N, int K, float alpha, const float 
  *  - Every GPU that loads the library holds the 24 MB until the process exits.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept for the life of the
+ *    process: after a cudaDeviceReset the library image may be loaded again
+ *    at another address, so do not call this function on a device that has
+ *    been reset since its first call.
+ *  - An operand copy the call makes first (the FP32 path's transposed
+ *    operand, the tensor-core paths' copy of an operand TMA cannot describe)
+ *    takes the front of the same scratch; what is left may be too small for
+ *    the split, and the call then runs with fewer slices or unsplit (the
+ *    same result up to rounding, only slower).
  *  - All calls on a device share the array; it needs no initialisation.
  *    Calls whose kernels overlap on the GPU (different streams, or another
  *    thread) race on the array: serialise them.

@@ -71,6 +71,10 @@ class Problem:
                                               self.lda, pb, self.ldb, self.beta, pc, self.ldc,
                                               self.transA, self.transB, self.sA, self.sB,
                                               self.sC, self.Q, stream)
+        elif api == "sgemm_ex":
+            assert self.Q == 1 and not self.transA and not self.transB
+            st = lib.sgemm_ex(mode, self.M, self.N, self.K, self.alpha, pa, self.lda, pb,
+                              self.ldb, self.beta, pc, self.ldc, stream)
         elif api == "sgemm":
             assert self.Q == 1 and not self.transA and not self.transB
             assert lib.sgemm_get_default_mode() == lib.MODES[mode]

@@ -103,6 +103,18 @@ def test_null_operands_allowed_when_not_read(lib):
 
 def test_plain_sgemm_validates_too(lib):
     assert lib.sgemm(4, 4, 4, 1.0, FAKE, 3, FAKE, 4, 0.0, FAKE, 4) == lib.SGEMM_ERR_INVALID_ARG
+    # the explicit-mode single GEMM: bad leading dimensions, a bad mode, NULL C
+    assert lib.sgemm_ex(0, 4, 4, 4, 1.0, FAKE, 3, FAKE, 4, 0.0, FAKE, 4) == \
+        lib.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_ex(1, 4, 4, 4, 1.0, FAKE, 4, FAKE, 3, 0.0, FAKE, 4) == \
+        lib.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_ex(2, 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 3) == \
+        lib.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_ex(5, 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4) == \
+        lib.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_ex(0, 4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, 0, 4) == \
+        lib.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_ex(0, 0, 4, 4, 1.0, 0, 4, 0, 4, 0.0, 0, 4) == lib.SGEMM_OK
     assert lib.sgemm_batched(4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4, 0, 0, 0, 0, 10, 2) \
         == lib.SGEMM_ERR_INVALID_ARG
     assert lib.sgemm_selftest_wait_timeout(0) == lib.SGEMM_ERR_INVALID_ARG

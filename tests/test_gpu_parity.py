@@ -77,14 +77,37 @@ def test_sgemm_ragged_beta_zero_then_minus_two(oracle_mod, mode):
         check_full(Problem(w["A"], w["B"], w["C0"], w["alpha"], beta), mode, oracle_mod)
 
 
-@pytest.mark.parametrize("api", ["ex", "ws"])
 @pytest.mark.parametrize("mode", MODES)
-def test_sgemm_4092_sampled_rows(oracle_mod, mode, api):
+def test_sgemm_4092_sampled_rows(oracle_mod, mode):
     supported(mode)
     w = workloads.make("sgemm_4092")
     prob = Problem(w["A"], w["B"], w["C0"], w["alpha"], w["betas"][0])
-    C = check_rows(prob, mode, oracle_mod, sample_rows(1, 4092, 40, seed=2), api=api)
+    C = check_rows(prob, mode, oracle_mod, sample_rows(1, 4092, 40, seed=2), api="ex")
     assert np.all(np.isfinite(C))
+
+
+@pytest.fixture(scope="module")
+def oracle_4092(oracle_mod):
+    """The oracle's whole 4092^3 result (every one of the 16.7 M outputs),
+    computed once for the three paths."""
+    w = workloads.make("sgemm_4092")
+    prob = Problem(w["A"], w["B"], w["C0"], w["alpha"], w["betas"][0])
+    Cref, D = prob.oracle(oracle_mod)
+    return prob, Cref, D
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_sgemm_4092_every_output_workspace_entry(oracle_4092, oracle_mod, mode):
+    """The benchmark's call (sgemm_batched_ex_ws with the workspace the
+    library asks for: operand pass, product, split-K fix-up of the last
+    wave) against the oracle on every output element, so that every split
+    tile of the last wave is checked, not only sampled rows."""
+    supported(mode)
+    prob, Cref, D = oracle_4092
+    C = prob.run_gpu(mode, api="ws")
+    assert np.all(np.isfinite(C))
+    err = oracle_mod.max_rel_err(C, Cref, D)
+    assert err <= TOL[mode], f"{mode}: max rel err {err:.3e} over all outputs"
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -281,6 +304,15 @@ def test_default_mode_entry_points(oracle_mod):
             assert oracle_mod.max_rel_err(C, Cref, D) <= TOL[mode]
     finally:
         lib.sgemm_set_default_mode(old)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_single_gemm_explicit_mode_entry(oracle_mod, mode):
+    """sgemm_ex: one GEMM, no transposes, the path named by the call."""
+    supported(mode)
+    A, B, C0 = workloads.random_inputs(333, 517, 258, seed=11)
+    prob = Problem(A, B, C0, -0.75, 1.5, pads=(4, 0, 8))
+    check_full(prob, mode, oracle_mod, api="sgemm_ex")
 
 
 def test_runs_on_a_side_stream(oracle_mod):

@@ -3,9 +3,10 @@
 It serves callers that may not allocate device memory where they multiply
 (a host callback, another library's critical section, a plugin handed only
 its buffers): its split-K scratch is a fixed array inside the library.  These
-tests call it through the C ABI and check, on two calls in a row (the second
-one reuses the scratch the first one left behind), that its output agrees
-with the ordinary entry point's within the accuracy bound of every path.
+tests call it through the C ABI, twice in a row (the second call reuses the
+scratch the first one left behind), and check each result against the fp64
+oracle within the accuracy bound of the path, and that the call really took
+the split route (the product kernel and the split-K fix-up both launched).
 The file is named to be collected last."""
 import numpy as np
 import pytest
@@ -15,7 +16,12 @@ from _helpers import TOL, Problem
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = [(1024, 1024, 1024, 1.0, 0.0), (600, 700, 777, 1.0, -2.0), (256, 256, 600, 1.5, 0.5)]
+# Shapes whose grids are small enough for this entry point's one-wave split
+# on every path and whose K is long enough for the split to pay (so the
+# library's planner takes it), with ragged edges in the second one; every
+# operand is TMA-describable, so no operand copy takes the scratch first.
+SHAPES = [(1000, 1000, 4096, 1.0, 0.0), (600, 700, 3000, 1.0, -2.0),
+          (256, 256, 2048, 1.5, 0.5)]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -29,18 +35,21 @@ def gpu_ready():
 
 @pytest.mark.parametrize("mode", ["fp32", "3xtf32", "tf32"])
 @pytest.mark.parametrize("shape", SHAPES)
-def test_noalloc_matches_the_existing_entry_point_twice(oracle_mod, mode, shape):
+def test_noalloc_matches_the_oracle_twice(oracle_mod, mode, shape):
     import dense_fp32_matrix_03_gb300 as lib
     M, N, K, alpha, beta = shape
-    assert lib.sgemm_workspace_size(mode, M, N, K, 1) > 0, "the shape should use split-K"
     A, B, C0 = workloads.random_inputs(M, N, K, seed=M + K)
     prob = Problem(A, B, C0, alpha, beta)
-    C_plain = prob.run_gpu(mode)                  # sgemm_batched_ex: no split, no scratch
-    _, D = prob.oracle(oracle_mod)                # magnitudes for the accuracy metric
+    Cref, D = prob.oracle(oracle_mod)
+    C_plain = prob.run_gpu(mode)  # sgemm_batched_ex: the ordinary entry point
+    assert oracle_mod.max_rel_err(C_plain, Cref, D) <= TOL[mode]
     for _ in range(2):
+        before = lib.sgemm_kernel_launches()
         C = prob.run_gpu(mode, api="noalloc")
-        err = float(np.max(np.abs(C.astype(np.float64) - C_plain) / (D + 1e-30)))
-        assert err <= TOL[mode], f"{mode} {shape}: {err:.3e}"
+        launched = lib.sgemm_kernel_launches() - before
+        err = oracle_mod.max_rel_err(C, Cref, D)
+        assert err <= TOL[mode], f"{mode} {shape[:3]}: {err:.3e}"
+        assert launched == 2, "expected the product kernel and the split-K fix-up"
 
 
 def test_noalloc_unsplit_shape_and_bad_arguments():
