@@ -398,6 +398,14 @@ def main():
     ap.add_argument("--bmm-only", action="store_true",
                     help="instead of the benchmark line, print one JSON line with the batched "
                          "workload's figures on --mode (3xtf32 for auto), --steps timed calls")
+    ap.add_argument("--tune", action="store_true",
+                    help="instead of the benchmark line, time every kernel route on one shape "
+                         "per (mode, size class), print one JSON line per shape, and write "
+                         "the table of the fastest routes to --tune-out")
+    ap.add_argument("--tune-out", default=os.path.join(ROOT, "dense_fp32_matrix_03_gb300", "csrc",
+                                                       "tune_table.h"),
+                    help="where --tune writes the table (a C++ header compiled into the "
+                         "library; rebuild to use it)")
     ap.add_argument("--all-configs", action="store_true",
                     help="instead of the benchmark line, print one JSON line per workload "
                          "configuration and path (256^3, ragged, size sweep, batched)")
@@ -410,6 +418,8 @@ def main():
         return reference_arm(args, rank, world)
     if args.all_configs:
         return all_configs(args)
+    if args.tune:
+        return tune(args)
     if args.half_only:
         return half_only()
     if args.bmm_only:
@@ -857,6 +867,124 @@ def all_configs(args):
             line["oracle_one_thread"] = oracle_timing_single_thread(name, beta_idx)
         print(json.dumps(line), flush=True)
     return 0
+
+
+# The sweep behind the committed route table (dense_fp32_matrix_03_gb300/
+# csrc/tune_table.h).  One representative shape per size class
+# (round(log2(M N K Q) / 3)): the square sizes 128 .. 8192 (4092 for class 12,
+# the benchmark shape), and the batched workload for the batched class 11.
+TUNE_SHAPES = [(128, 128, 128, 1), (256, 256, 256, 1), (512, 512, 512, 1),
+               (1024, 1024, 1024, 1), (2048, 2048, 2048, 1), (4092, 4092, 4092, 1),
+               (8192, 8192, 8192, 1), (1024, 1024, 512, 32)]
+TUNE_ROUTES = {"fp32": ("auto", "small"), "3xtf32": ("auto", "pair", "direct", "planes"),
+               "tf32": ("auto", "pair", "direct", "planes")}
+TUNE_KEEP_AUTO = 0.02  # a route must beat the cost models' choice by 2% to get an entry
+
+
+def size_class(M, N, K, Q):
+    import math
+    c = round(math.log2(max(M * N * K * Q, 1)) / 3.0)
+    return min(max(c, 7), 13)
+
+
+def tune(args):
+    """--tune: every route on every representative shape and mode, through
+    the workspace entry with the workspace the library asks for under that
+    route, L2 flushed before every timed call; the fastest route per (mode,
+    class) goes into the table unless the cost models' choice is within
+    TUNE_KEEP_AUTO of it."""
+    import torch
+    import dense_fp32_matrix_03_gb300 as lib
+    dev = torch.device("cuda", 0)
+    lib.load()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    entries = []
+    try:
+        for (M, N, K, Q) in TUNE_SHAPES:
+            g = torch.Generator(device=dev).manual_seed(3)
+            A = torch.rand(Q, M, K, device=dev, generator=g) * 2 - 1
+            B = torch.rand(Q, K, N, device=dev, generator=g) * 2 - 1
+            C = torch.zeros(Q, M, N, device=dev)
+            flops = gemm_flops(M, N, K, Q)
+            steps = 20 if flops < 2e10 else (8 if flops < 3e11 else 3)
+            for mode in ("fp32", "3xtf32", "tf32"):
+                times = {}
+                for route in TUNE_ROUTES[mode]:
+                    lib.check(lib.sgemm_tune_force(route))
+                    wsb, ws = workspace(lib, mode, M, N, K, Q, dev)
+
+                    def call(mode=mode, ws=ws, wsb=wsb):
+                        lib.check(lib.sgemm_batched_ex_ws(mode, M, N, K, 1.0, A, K, B, N, 0.0, C, N,
+                                                          0, 0, M * K, K * N, M * N, Q, ws, wsb,
+                                                          stream))
+                    times[route] = statistics.median(time_calls(call, steps, 3, stream, flush))
+                    del ws
+                lib.check(lib.sgemm_tune_force("auto"))
+                best = min(times, key=times.get)
+                cls, batched = size_class(M, N, K, Q), int(Q > 1)
+                chosen = best if times[best] < (1 - TUNE_KEEP_AUTO) * times["auto"] else "auto"
+                line = {"mode": mode, "M": M, "N": N, "K": K, "Q": Q, "size_class": cls,
+                        "batched": batched, "us": {r: round(t * 1e3, 1) for r, t in times.items()},
+                        "tflops": {r: round(flops / (t / 1e3) / 1e12, 2) for r, t in times.items()},
+                        "chosen": chosen}
+                print(json.dumps(line), flush=True)
+                entries.append(line)
+            del A, B, C
+        lib.check(lib.sgemm_poll_error(stream))
+    finally:
+        lib.sgemm_tune_force("auto")
+    write_tune_table(entries, args.tune_out, props.name)
+    return 0
+
+
+def write_tune_table(entries, path, gpu):
+    """The C++ header the library compiles in: one entry per (mode, class,
+    batched) whose fastest route is not the cost models' choice, each with
+    the times the sweep measured."""
+    import dense_fp32_matrix_03_gb300 as lib
+    modes = {"fp32": 0, "3xtf32": 1, "tf32": 2}
+    rows = []
+    for e in entries:
+        if e["chosen"] == "auto":
+            continue
+        times = ", ".join(f"{r} {t}" for r, t in e["us"].items())
+        rows.append(f"    {{{modes[e['mode']]}, {e['size_class']}, {e['batched']}, "
+                    f"{lib.ROUTES[e['chosen']]}}},  // {e['mode']} {e['M']}x{e['N']}x{e['K']}"
+                    f"{' Q=' + str(e['Q']) if e['Q'] > 1 else ''}: {e['chosen']}; us: {times}")
+    kept = [f"//   {e['mode']} {e['M']}x{e['N']}x{e['K']}{' Q=' + str(e['Q']) if e['Q'] > 1 else ''}"
+            f" (class {e['size_class']}): us " + ", ".join(f"{r} {t}" for r, t in e["us"].items())
+            for e in entries if e["chosen"] == "auto"]
+    text = "\n".join([
+        "// tune_table.h -- kernel route per (mode, size class, batched) call, as",
+        "// measured by the sweep `python bench.py --tune` (which rewrites this file)",
+        f"// on {gpu}, L2 flushed before every timed call, through the workspace entry.",
+        "// Size class and routes: internal.h (size_class, Route).  A (mode, class)",
+        "// without an entry takes the cost models' choice (kRouteAuto), which the",
+        f"// sweep keeps unless another route is more than {TUNE_KEEP_AUTO:.0%} faster; the",
+        "// shapes where it kept the cost models' choice:",
+        *kept,
+        "#pragma once",
+        "",
+        "namespace sg {",
+        "",
+        "struct TuneEntry {",
+        "    int mode, size_class, batched, route;",
+        "};",
+        "",
+        "// {mode (0 FP32, 1 3xTF32, 2 TF32), size class, batched, route}",
+        "constexpr TuneEntry kTuneTable[] = {",
+        *rows,
+        "    {-1, 0, 0, 0},  // end of table",
+        "};",
+        "",
+        "}  // namespace sg",
+        "",
+    ])
+    with open(path, "w") as f:
+        f.write(text)
 
 
 if __name__ == "__main__":

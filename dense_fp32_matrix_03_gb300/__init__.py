@@ -38,6 +38,14 @@ SGEMM_HALF_BF16 = 0
 SGEMM_HALF_FP16 = 1
 HALF_TYPES = {"bf16": SGEMM_HALF_BF16, "fp16": SGEMM_HALF_FP16}
 
+SGEMM_ROUTE_AUTO = 0
+SGEMM_ROUTE_SMALL = 1
+SGEMM_ROUTE_PAIR = 2
+SGEMM_ROUTE_DIRECT = 3
+SGEMM_ROUTE_PLANES = 4
+ROUTES = {"auto": SGEMM_ROUTE_AUTO, "small": SGEMM_ROUTE_SMALL, "pair": SGEMM_ROUTE_PAIR,
+          "direct": SGEMM_ROUTE_DIRECT, "planes": SGEMM_ROUTE_PLANES}
+
 SGEMM_MODE_DEFAULT = -1
 SGEMM_MODE_FP32 = 0
 SGEMM_MODE_3XTF32 = 1
@@ -65,6 +73,8 @@ SIGNATURES = {
     "sgemm_host": (_i, [_i, _i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _i, _i, _i, _p,
                         ctypes.c_size_t, _p]),
     "sgemm_peak_probe": (_i, [_i, _ll, ctypes.POINTER(ctypes.c_double), _p]),
+    "sgemm_tune_force": (_i, [_i]),
+    "sgemm_tune_route": (_i, [_i, _i, _i, _i, _i]),
     "sgemm_set_default_mode": (_i, [_i]),
     "sgemm_get_default_mode": (_i, []),
     "sgemm_status_string": (ctypes.c_char_p, [_i]),
@@ -239,6 +249,19 @@ def sgemm_peak_probe(kind, iters, stream=None):
     flops = ctypes.c_double(0.0)
     st = _lib.sgemm_peak_probe(kind, iters, ctypes.byref(flops), _stream(stream))
     return st, flops.value
+
+
+def sgemm_tune_force(route) -> int:
+    """Process-wide forced kernel route (measurement; see include/sgemm.h)."""
+    if isinstance(route, str):
+        route = ROUTES[route]
+    return _lib.sgemm_tune_force(route)
+
+
+def sgemm_tune_route(mode, M, N, K, Q=1) -> int:
+    if isinstance(mode, str):
+        mode = MODES[mode]
+    return _lib.sgemm_tune_route(mode, M, N, K, Q)
 
 
 def sgemm_set_default_mode(mode) -> int:

@@ -3,6 +3,7 @@
 // or tcgen05 launchers.  Nothing here allocates device memory.
 #include <atomic>
 #include <climits>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -15,6 +16,7 @@
 #include "../../include/sgemm.h"
 #include "common.cuh"
 #include "internal.h"
+#include "tune_table.h"
 
 namespace sg {
 
@@ -278,6 +280,40 @@ bool smem_attr_once(const void *kernel, int bytes)
     return true;
 }
 
+namespace {
+std::atomic<int> g_force_route{kRouteAuto};
+}  // namespace
+
+int size_class(long long M, long long N, long long K, int Q)
+{
+    const double work = static_cast<double>(M) * N * K * (Q > 1 ? Q : 1);
+    const int c = static_cast<int>(std::lround(std::log2(work > 1.0 ? work : 1.0) / 3.0));
+    return c < kClassMin ? kClassMin : (c > kClassMax ? kClassMax : c);
+}
+
+namespace {
+// A route the mode cannot take is the cost models' choice.
+int applicable(int mode, int route)
+{
+    const bool fp32 = mode == SGEMM_MODE_FP32;
+    if (route == kRouteSimtSmall) return fp32 ? route : kRouteAuto;
+    if (route == kRouteTcPair || route == kRouteTcDirect || route == kRouteTcPlanes)
+        return fp32 ? kRouteAuto : route;
+    return kRouteAuto;
+}
+}  // namespace
+
+int route_for(int mode, long long M, long long N, long long K, int Q)
+{
+    const int forced = g_force_route.load();
+    if (forced != kRouteAuto) return applicable(mode, forced);
+    const int cls = size_class(M, N, K, Q);
+    for (const TuneEntry &e : kTuneTable)
+        if (e.mode == mode && e.size_class == cls && e.batched == (Q > 1 ? 1 : 0))
+            return applicable(mode, e.route);
+    return kRouteAuto;
+}
+
 int min_slice_k(int mode) { return mode == SGEMM_MODE_FP32 ? 64 : 256; }
 
 // FLOP/s per multiprocessor each kernel sustains on GB300 (measured at
@@ -396,11 +432,13 @@ SplitPlan plan_query(int mode, int M, int N, int K, int Q, bool one_wave)
     // dimensions the query does not take: plan for every kernel the mode
     // may run (FP32: the two tile shapes, each TMA-fed or not; tensor
     // cores: the direct kernel's 128 x 128 tiles, the pair kernel's 256 x 128).
-    for (int shape = 0; shape < (mode == SGEMM_MODE_FP32 ? 2 : 3); ++shape) {
+    const bool small = mode == SGEMM_MODE_FP32 && route_for(mode, M, N, K, Q) == kRouteSimtSmall;
+    for (int shape = 0; shape < (mode == SGEMM_MODE_FP32 ? (small ? 3 : 2) : 3); ++shape) {
         int bm = 0, bn = 0, slots = sms;
         int feeds[2] = {kFeedDirect, kFeedTma};
         if (mode == SGEMM_MODE_FP32) {
-            simt_tile_dims(shape == 1, bm, bn);
+            if (shape == 2) simt_small_tile_dims(bm, bn);
+            else simt_tile_dims(shape == 1, bm, bn);
         } else if (shape == 2) {  // the planes route's 256 x 256 pair tiles
             bm = bn = 256;
             slots = tc_pair_slots(sms);
@@ -652,17 +690,23 @@ int run(int mode, int M, int N, int K, float alpha, const float *A, int lda, con
     plan.ws = ws;
     plan.ws_bytes = ws_bytes;
 
+    const int route = route_for(mode, M, N, K, Q);
     if (mode == SGEMM_MODE_FP32) {
+        if (route == kRouteSimtSmall) return launch_simt(plan, route);
         rc = repack_for_simt(plan);
         if (rc != SGEMM_OK) return rc;
-        return launch_simt(plan);
+        return launch_simt(plan, kRouteAuto);
     }
     bool taken = false;
-    rc = run_planes(plan, taken);
-    if (taken || rc != SGEMM_OK) return rc;
-    rc = repack_for_tc(plan);
-    if (rc != SGEMM_OK) return rc;
-    return launch_tc(plan);
+    if (route == kRouteAuto || route == kRouteTcPlanes) {
+        rc = run_planes(plan, taken, route == kRouteTcPlanes);
+        if (taken || rc != SGEMM_OK) return rc;
+    }
+    if (route != kRouteTcDirect) {  // the direct kernel reads any layout as it is
+        rc = repack_for_tc(plan);
+        if (rc != SGEMM_OK) return rc;
+    }
+    return launch_tc(plan, route);
 }
 
 }  // namespace
@@ -749,7 +793,10 @@ size_t sgemm_workspace_size(int mode, int M, int N, int K, int Q)
     // where the planes route pays for this shape (planes_pay): both
     // operands' planes (every batch entry stored) and the split plan of its
     // tiles, or the copies and plans of the other routes, whichever is larger
-    if (!planes_pay(mode, M, N, K, Q, Q, Q, num_sms_or_zero())) return base;
+    const int route = route_for(mode, M, N, K, Q);
+    if (route == kRouteTcPair || route == kRouteTcDirect) return base;
+    if (route != kRouteTcPlanes && !planes_pay(mode, M, N, K, Q, Q, Q, num_sms_or_zero()))
+        return base;
     const size_t planes =
         planes_bytes(mode, M, N, K, Q, Q) + preferred_plan(mode, M, N, K, Q).ws_bytes;
     return planes > base ? planes : base;
@@ -822,6 +869,22 @@ int sgemm_peak_probe(int kind, long long iters, double *flops, void *stream)
 }
 
 unsigned long long sgemm_kernel_launches(void) { return sg::g_launches.load(); }
+
+int sgemm_tune_force(int route)
+{
+    if (route < 0 || route >= sg::kRouteCount) return SGEMM_ERR_INVALID_ARG;
+    sg::g_force_route.store(route);
+    return SGEMM_OK;
+}
+
+int sgemm_tune_route(int mode, int M, int N, int K, int Q)
+{
+    if (mode == SGEMM_MODE_DEFAULT) mode = g_default_mode.load();
+    if (mode != SGEMM_MODE_FP32 && mode != SGEMM_MODE_3XTF32 && mode != SGEMM_MODE_TF32)
+        return -1;
+    if (M < 0 || N < 0 || K < 0 || Q < 0) return -1;
+    return sg::route_for(mode, M, N, K, Q);
+}
 
 int sgemm_version(void) { return 100; }
 

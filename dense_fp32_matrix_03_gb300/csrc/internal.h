@@ -89,6 +89,8 @@ int plan_splits(Plan &plan, int bm, int bn, int feed, int slots);
 // Output tile of each kernel (defined beside its launcher); the FP32 path's
 // depends on whether both operands are K-inner.
 void simt_tile_dims(bool both_k_inner, int &bm, int &bn);
+// The FP32 path's tile on kRouteSimtSmall.
+void simt_small_tile_dims(int &bm, int &bn);
 // pair: the CTA-pair kernel's tile (the single-CTA kernels' otherwise).
 void tc_tile_dims(int mode, int K, bool pair, int &bm, int &bn);
 // CTA pairs of the pair kernel that fit on the device at once (cached).
@@ -105,7 +107,9 @@ size_t planes_bytes(int mode, long long M, long long N, long long K, int QA, int
 // holds the planes, enqueues the pass over both operands and the product
 // (taken = true) and returns its status; otherwise leaves the plan alone
 // (taken = false).
-int run_planes(Plan &plan, bool &taken);
+// force: take the route whenever the planes fit (kRouteTcPlanes), without
+// asking planes_pay.
+int run_planes(Plan &plan, bool &taken, bool force = false);
 // Whether the planes route is expected to beat the pair kernel for this
 // shape (QA, QB: stored batch entries of A and B; num_sms 0: unknown, then
 // false).  Each route's product takes the split planner's modelled time for
@@ -190,7 +194,30 @@ bool probe_args_ok(int kind, long long iters);
 int launch_peak_probe(int kind, long long iters, int num_sms, unsigned int *status,
                       cudaStream_t st, double *flops);
 
-int launch_simt(Plan &plan);   // returns an sgemm status code
-int launch_tc(Plan &plan);     // tcgen05 paths (3xTF32 and TF32)
+// Kernel families a call can run, the vocabulary of the tuning table
+// (tune_table.h) and of sgemm_tune_force (include/sgemm.h):
+//   kRouteAuto       the cost models (FP32: the tile for the layout; tensor
+//                    cores: planes where planes_pay, else the pair kernel
+//                    for TMA-describable operands, else the direct kernel);
+//   kRouteSimtSmall  FP32 on 64 x 64 tiles (small grids);
+//   kRouteTcPair     tensor cores on the CTA-pair kernel (never the planes);
+//   kRouteTcDirect   tensor cores on the direct-load kernel (128 x 128);
+//   kRouteTcPlanes   tensor cores on the planes route whenever the
+//                    workspace holds the planes.
+// A route the call's mode or operands cannot take falls back to kRouteAuto.
+enum Route { kRouteAuto = 0, kRouteSimtSmall = 1, kRouteTcPair = 2, kRouteTcDirect = 3,
+             kRouteTcPlanes = 4, kRouteCount = 5 };
+// Size class of a call: round(log2(M * N * K * Q) / 3), clamped to
+// [kClassMin, kClassMax] -- the log2 of the edge of a cube of the same work
+// (4092^3: 12; the batched 32 x 1024 x 1024 x 512 workload: 11).
+constexpr int kClassMin = 7, kClassMax = 13;
+int size_class(long long M, long long N, long long K, int Q);
+// The route of a call: the forced route (sgemm_tune_force) when one is set,
+// else the tuning table's entry for (mode, size class, batched), else
+// kRouteAuto.
+int route_for(int mode, long long M, long long N, long long K, int Q);
+
+int launch_simt(Plan &plan, int route);  // returns an sgemm status code
+int launch_tc(Plan &plan, int route);    // tcgen05 paths (3xTF32 and TF32)
 
 }  // namespace sg

@@ -22,6 +22,12 @@ namespace {
 // fragment registers, 63.6 -> 64.0); the narrow one four at a time.
 using SimtWide = SimtCfg<256, 128, 64, 64, 2, 2, 0, 2>;
 using SimtNarrow = SimtCfg<128, 128, 64, 32, 3, 2, 1, 4>;
+// Small grids (kRouteSimtSmall, chosen by the tuning table): 64 x 64 tiles,
+// 32 x 32 per warp (4 x 8 outputs per lane), four warps, four stages of 32 k
+// -- four times the tiles of the narrow tile, sixteen times those of the
+// wide one, so that a 128^3 .. 512^3 product spreads over more
+// multiprocessors before any split along K.
+using SimtSmall = SimtCfg<64, 64, 32, 32, 4, 1, 1, 4>;
 constexpr int kGroupM = 8;
 
 template <class Cfg, bool A_KIN, bool B_KIN, bool USE_TMA, bool EVEN_K>
@@ -71,16 +77,28 @@ int launch_cfg(Plan &plan)
 
 }  // namespace
 
+void simt_small_tile_dims(int &bm, int &bn)
+{
+    bm = SimtSmall::BM;
+    bn = SimtSmall::BN;
+}
+
 void simt_tile_dims(bool both_k_inner, int &bm, int &bn)
 {
     bm = both_k_inner ? SimtNarrow::BM : SimtWide::BM;
     bn = both_k_inner ? SimtNarrow::BN : SimtWide::BN;
 }
 
-int launch_simt(Plan &plan)
+int launch_simt(Plan &plan, int route)
 {
     static_assert(kMinBlocks == 1, "the split planner assumes one CTA per multiprocessor");
     const bool a_kin = !plan.transA, b_kin = plan.transB;
+    if (route == kRouteSimtSmall) {
+        if (a_kin && b_kin) return launch_cfg<SimtSmall, true, true>(plan);
+        if (a_kin) return launch_cfg<SimtSmall, true, false>(plan);
+        if (b_kin) return launch_cfg<SimtSmall, false, true>(plan);
+        return launch_cfg<SimtSmall, false, false>(plan);
+    }
     if (a_kin && b_kin) return launch_cfg<SimtNarrow, true, true>(plan);
     if (a_kin) return launch_cfg<SimtWide, true, false>(plan);
     if (b_kin) return launch_cfg<SimtWide, false, true>(plan);

@@ -56,7 +56,7 @@ void tc_tile_dims(int mode, int K, bool pair, int &bm, int &bn)
     bn = pair ? tcp::pair_shape(tcp::pair_wide(mode == SGEMM_MODE_3XTF32, K)).bn : kBN;
 }
 
-int launch_tc(Plan &plan)
+int launch_tc(Plan &plan, int route)
 {
     GemmParams &p = plan.p;
     p.k_blocks = (p.K + tc::BK - 1) / tc::BK;
@@ -69,7 +69,7 @@ int launch_tc(Plan &plan)
     std::memset(&tmB, 0, sizeof(tmB));
     const tcp::PairShape sh =
         tcp::pair_shape(tcp::pair_wide(plan.mode == SGEMM_MODE_3XTF32, p.K));
-    if (plan.a_tma && plan.b_tma &&
+    if (route != kRouteTcDirect && plan.a_tma && plan.b_tma &&
         encode_operand(&tmA, p.A, !plan.transA, p.M, p.K, p.lda, p.Q, p.sA, tcp::BM) &&
         encode_operand(&tmB, p.B, plan.transB, p.N, p.K, p.ldb, p.Q, p.sB, sh.hn)) {
         p.k_blocks = (p.K + sh.stage_k - 1) / sh.stage_k;  // the pair kernel's stages

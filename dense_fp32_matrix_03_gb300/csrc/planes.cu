@@ -285,7 +285,7 @@ static int product_on_planes(Plan &plan, const float *pa, const float *pb, int Q
                        : launch_ss<tcs::KindTF32<1>>(plan, tmA, tmB, slots);
 }
 
-int run_planes(Plan &plan, bool &taken)
+int run_planes(Plan &plan, bool &taken, bool force)
 {
     taken = false;
     GemmParams &p = plan.p;
@@ -296,7 +296,8 @@ int run_planes(Plan &plan, bool &taken)
     // plane * entries + entry indexes the tensor maps' third dimension (int)
     if (2LL * p.Q > 0x7FFFFFFFLL) return SGEMM_OK;
     const size_t need = planes_bytes(plan.mode, p.M, p.N, p.K, QA, QB);
-    if (need > plan.ws_bytes || !planes_pay(plan.mode, p.M, p.N, p.K, QA, QB, p.Q, plan.num_sms))
+    if (need > plan.ws_bytes ||
+        (!force && !planes_pay(plan.mode, p.M, p.N, p.K, QA, QB, p.Q, plan.num_sms)))
         return SGEMM_OK;
     taken = true;
 

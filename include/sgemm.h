@@ -282,6 +282,35 @@ int sgemm_host(int mode, int M, int N, int K, float alpha, const float *A, int l
 #define SGEMM_PROBE_BF16_SS 4
 int sgemm_peak_probe(int kind, long long iters, double *flops, void *stream);
 
+/* Tuning hooks (measurement; the sweep `bench.py --tune` uses them).
+ * Which kernel family runs a call is chosen per (mode, size class, batched)
+ * by a table compiled into the library from that sweep, the size class
+ * being round(log2(M * N * K * Q) / 3) clamped to 7..13; a class without
+ * an entry follows the library's cost models.  The families ("routes"):
+ *   0  AUTO     the cost models (the FP32 tile that suits the layout; on the
+ *               tensor cores the TF32-planes route where its time model says
+ *               it pays and the workspace holds the planes, else the CTA-pair
+ *               kernel for TMA-describable operands, else the direct kernel)
+ *   1  SMALL    FP32 on 64 x 64 tiles
+ *   2  PAIR     tensor cores on the CTA-pair kernel, no planes
+ *   3  DIRECT   tensor cores on the direct-load kernel
+ *   4  PLANES   tensor cores on the planes route whenever the workspace holds
+ *               the planes (sgemm_workspace_size then counts them)
+ * A route the call's mode cannot take means AUTO; every route computes the
+ * same result within the mode's accuracy bound.
+ * sgemm_tune_force(route) makes every later call in the process take that
+ * route (AUTO: the table again); SGEMM_ERR_INVALID_ARG for an unknown route.
+ * It is a process-wide setting: do not change it while other threads call
+ * the library.  sgemm_tune_route returns the route a call of that shape
+ * would take now (-1 for an invalid mode or a negative dimension). */
+#define SGEMM_ROUTE_AUTO 0
+#define SGEMM_ROUTE_SMALL 1
+#define SGEMM_ROUTE_PAIR 2
+#define SGEMM_ROUTE_DIRECT 3
+#define SGEMM_ROUTE_PLANES 4
+int sgemm_tune_force(int route);
+int sgemm_tune_route(int mode, int M, int N, int K, int Q);
+
 /* Process-wide default path used by sgemm() and sgemm_batched().  Returns
  * SGEMM_ERR_INVALID_ARG for an unknown mode (DEFAULT is not a valid value
  * here). */

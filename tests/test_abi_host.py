@@ -173,3 +173,45 @@ def test_half_entry_rejects_invalid_arguments(lib, bad):
 
 def test_half_entry_empty_is_a_no_op(lib):
     assert half(lib, M=0, A=0, B=0, C=0) == lib.SGEMM_OK
+
+
+def tune_table_entries():
+    """(mode, class, batched) -> route, parsed from the committed header."""
+    text = open(os.path.join(ROOT, "dense_fp32_matrix_03_gb300", "csrc", "tune_table.h")).read()
+    out = {}
+    for m in re.finditer(r"^\s*\{(-?\d+), (\d+), (\d+), (\d+)\},", text, flags=re.M):
+        mode, cls, batched, route = map(int, m.groups())
+        if mode >= 0:
+            out[(mode, cls, batched)] = route
+    return out
+
+
+def test_tune_hooks_validate_arguments(lib):
+    assert lib.sgemm_tune_force(5) == lib.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_tune_force(-1) == lib.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_tune_route(7, 8, 8, 8, 1) == -1
+    assert lib.sgemm_tune_route(0, -1, 8, 8, 1) == -1
+    try:
+        assert lib.sgemm_tune_force("direct") == lib.SGEMM_OK
+        assert lib.sgemm_tune_route("tf32", 64, 64, 64, 1) == lib.SGEMM_ROUTE_DIRECT
+        assert lib.sgemm_tune_route("fp32", 64, 64, 64, 1) == lib.SGEMM_ROUTE_AUTO
+    finally:
+        assert lib.sgemm_tune_force("auto") == lib.SGEMM_OK
+
+
+def test_route_lookup_follows_the_committed_table(lib):
+    """For every mode and size class, single and batched, the route the
+    library picks is the header's entry, or AUTO where it has none.  Shapes:
+    M = N = K = 2^c (class c), and Q = 8 of M = N = K = 2^(c-1)."""
+    table = tune_table_entries()
+    for mode in (0, 1, 2):
+        for cls in range(7, 14):
+            for batched in (0, 1):
+                n = 2 ** (cls - batched)
+                Q = 8 if batched else 1
+                want = table.get((mode, cls, batched), 0)
+                if mode == 0 and want not in (0, 1):
+                    want = 0
+                if mode != 0 and want == 1:
+                    want = 0
+                assert lib.sgemm_tune_route(mode, n, n, n, Q) == want, (mode, cls, batched)

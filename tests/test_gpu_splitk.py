@@ -121,7 +121,10 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
     (256-byte rounded); on the tensor paths plus room for 128-byte-pitched
     copies of A and B, or, where the planes route pays, for their TF32
     planes if larger (two planes for 3xTF32, one for TF32; rows of
-    round_up(K, 32) values)."""
+    round_up(K, 32) values).  The route table (tune_table.h) adds the FP32
+    64 x 64 tile where it sends the shape to it, and decides the planes on
+    the tensor paths: always with route PLANES, never with PAIR or DIRECT,
+    by the time model with AUTO."""
     rates = {("fp32", "direct"): 0.24e12, ("fp32", "tma"): 0.40e12,
              ("3xtf32", "direct"): 0.47e12, ("3xtf32", "pair"): 1.8e12,
              ("tf32", "direct"): 0.55e12, ("tf32", "pair"): 3.6e12,
@@ -131,6 +134,10 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
     if mode == "fp32":
         kernels = [(bm, bn, feed, sms, 1) for (bm, bn) in ((256, 128), (128, 128))
                    for feed in ("direct", "tma")]
+        # the 64 x 64 tile where the route table sends this shape
+        import dense_fp32_matrix_03_gb300 as lib
+        if lib.sgemm_tune_route(mode, M, N, K, Q) == lib.SGEMM_ROUTE_SMALL:
+            kernels += [(64, 64, feed, sms, 1) for feed in ("direct", "tma")]
     else:
         # the pair kernel: 256 x 128 tiles, 256 x 256 for TF32 with K >= 1536
         wide = mode == "tf32" and K >= 1536
@@ -174,16 +181,20 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
         # the planes route where it pays: the modelled time of its tiles' plan
         # plus its pass ((M + N) * K * Q * 4 * (1 + planes) bytes at 6.0 TB/s)
         # and 7 us, against the modelled time of the pair kernel's plan
+        import dense_fp32_matrix_03_gb300 as lib
+        route = lib.sgemm_tune_route(mode, M, N, K, Q)
         t_pair = plan(*kernels[1])[1]
         t_planes = plan(*kernels[2])[1] + (M + N) * K * Q * 4.0 * (1 + planes) / 6.0e12 + 7e-6
         room = copy(M) + copy(N)
-        if t_planes < t_pair:
+        if (route == lib.SGEMM_ROUTE_PLANES or
+                (route == lib.SGEMM_ROUTE_AUTO and t_planes < t_pair)):
             room = max(room, r256(planes * Q * M * r32(K) * 4) + r256(planes * Q * N * r32(K) * 4))
         need += room
     return need
 
 
 SIZE_CASES = [("fp32", 4092, 4092, 4092, 1), ("3xtf32", 4092, 4092, 4092, 1),
+              ("fp32", 256, 256, 256, 1), ("tf32", 256, 256, 256, 1),
               ("fp32", 1024, 1024, 128, 1), ("3xtf32", 1024, 1024, 128, 1),
               ("fp32", 1000, 1500, 777, 1), ("tf32", 1000, 1500, 777, 1),
               ("fp32", 1024, 1024, 32, 1), ("3xtf32", 1024, 1024, 512, 32),
