@@ -135,3 +135,46 @@ def half_inputs(M: int, N: int, K: int, type_: str, Q: int = 1, seed: int = 0):
     if type_ == "bf16":
         return round_to_bf16(A), round_to_bf16(B), C0
     return A.astype(np.float16).astype(np.float32), B.astype(np.float16).astype(np.float32), C0
+
+
+# ------------------------------------------------- chunked linear attention
+#
+# Inputs of the linear-attention workload (the chunk kernels "From 1% to 94%
+# of cuBLAS, one kernel at a time" describes in "Why FLA sits somewhere else
+# on the roofline": chunks of BT = 64 tokens, head dimension 128).  Recipe,
+# numpy PCG64 with the given seed, each array drawn in C order as float64 and
+# rounded to float32, in this order:
+#   q, k (BH x T x DK) and v (BH x T x DV): rng.normal(0, 1);
+#   g (BH x T), the per-token log-decay: log(sigmoid(x)) / 16 with
+#     x = rng.normal(0, 1) -- a decay factor exp(g) between ~0.9 and 1, the
+#     range gated linear-attention layers run in (omitted when decay=False);
+#   h0 (BH x DK x DV), the initial state: rng.normal(0, 1) (only when
+#     with_h0 is set).
+# The attention scale is 1 / sqrt(DK).
+LA_WORKLOADS = {
+    # the benchmark's linear-attention case: batch 4 x 16 heads, 4096 tokens
+    "la_b4h16_t4096_d128": dict(BH=64, T=4096, DK=128, DV=128, seed=7),
+    # the small case the oracle finishes in seconds
+    "la_b2h2_t300_d64": dict(BH=4, T=300, DK=64, DV=64, seed=8),
+}
+
+
+def linattn_inputs(BH: int, T: int, DK: int, DV: int, seed: int = 0, decay: bool = True,
+                   with_h0: bool = False):
+    """(q, k, v, g, h0, scale) of one linear-attention call (see the recipe
+    above); g and h0 are None when not drawn."""
+    rng = np.random.default_rng(seed)
+    q = rng.normal(0.0, 1.0, size=(BH, T, DK)).astype(np.float32)
+    k = rng.normal(0.0, 1.0, size=(BH, T, DK)).astype(np.float32)
+    v = rng.normal(0.0, 1.0, size=(BH, T, DV)).astype(np.float32)
+    g = None
+    if decay:
+        x = rng.normal(0.0, 1.0, size=(BH, T))
+        g = (-np.logaddexp(0.0, -x) / 16.0).astype(np.float32)  # log(sigmoid(x)) / 16
+    h0 = rng.normal(0.0, 1.0, size=(BH, DK, DV)).astype(np.float32) if with_h0 else None
+    return q, k, v, g, h0, float(1.0 / np.sqrt(DK))
+
+
+def la_make(name: str, **kw):
+    cfg = dict(LA_WORKLOADS[name])
+    return linattn_inputs(cfg["BH"], cfg["T"], cfg["DK"], cfg["DV"], cfg["seed"], **kw)
