@@ -82,6 +82,11 @@ SIGNATURES = {
     "sgemm_selftest_wait_timeout": (_i, [_ll, _p]),
     "sgemm_kernel_launches": (ctypes.c_ulonglong, []),
     "sgemm_version": (_i, []),
+    # include/linear_attention.h
+    "la_state_bytes": (ctypes.c_size_t, [_i, _i, _i, _i]),
+    "la_chunk_state": (_i, [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p]),
+    "la_chunk_output": (_i, [_i, _i, _i, _i, _f, _p, _p, _p, _p, _p, _p, _p]),
+    "la_chunk_fused": (_i, [_i, _i, _i, _i, _f, _p, _p, _p, _p, _p, _p, _p, _p]),
 }
 
 
@@ -292,6 +297,27 @@ def sgemm_kernel_launches() -> int:
 
 def sgemm_version() -> int:
     return _lib.sgemm_version()
+
+
+# ---- chunked linear attention (include/linear_attention.h)
+
+def la_state_bytes(BH, T, DK, DV) -> int:
+    return int(_lib.la_state_bytes(BH, T, DK, DV))
+
+
+def la_chunk_state(BH, T, DK, DV, k, v, g, h0, h, state_out, stream=None) -> int:
+    return _lib.la_chunk_state(BH, T, DK, DV, _ptr(k), _ptr(v), _ptr(g), _ptr(h0), _ptr(h),
+                               _ptr(state_out), _stream(stream))
+
+
+def la_chunk_output(BH, T, DK, DV, scale, q, k, v, g, h, o, stream=None) -> int:
+    return _lib.la_chunk_output(BH, T, DK, DV, scale, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                _ptr(h), _ptr(o), _stream(stream))
+
+
+def la_chunk_fused(BH, T, DK, DV, scale, q, k, v, g, h0, o, state_out, stream=None) -> int:
+    return _lib.la_chunk_fused(BH, T, DK, DV, scale, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                               _ptr(h0), _ptr(o), _ptr(state_out), _stream(stream))
 
 
 def check(status: int) -> None:

@@ -20,15 +20,23 @@ def lib():
 
 
 def declared_functions():
-    text = open(os.path.join(ROOT, "include", "sgemm.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:\w+\s+)+\**\s*(sgemm\w*)\s*\(", text, flags=re.M)))
+    """Every function the headers under include/ declare."""
+    names = set()
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"^\s*(?:\w+\s+)+\**\s*(sgemm\w*|la_\w+)\s*\(", text,
+                                flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for want in ("sgemm", "sgemm_batched", "sgemm_batched_ex", "sgemm_poll_error",
-                 "sgemm_status_string", "sgemm_set_default_mode"):
+    for want in ("sgemm", "sgemm_ex", "sgemm_batched", "sgemm_batched_ex", "sgemm_poll_error",
+                 "sgemm_status_string", "sgemm_set_default_mode", "la_chunk_state",
+                 "la_chunk_output", "la_chunk_fused", "la_state_bytes"):
         assert want in names
 
 
@@ -215,3 +223,31 @@ def test_route_lookup_follows_the_committed_table(lib):
                 if mode != 0 and want == 1:
                     want = 0
                 assert lib.sgemm_tune_route(mode, n, n, n, Q) == want, (mode, cls, batched)
+
+
+def test_linear_attention_rejects_invalid_arguments(lib):
+    F = FAKE
+    # head dimensions other than 64 / 128, negative sizes, too many heads
+    for (BH, T, DK, DV) in [(1, 8, 32, 64), (1, 8, 64, 96), (-1, 8, 64, 64), (1, -1, 64, 64),
+                            (65536, 8, 64, 64)]:
+        assert lib.la_chunk_state(BH, T, DK, DV, F, F, None, None, F, None) == \
+            lib.SGEMM_ERR_INVALID_ARG
+        assert lib.la_chunk_output(BH, T, DK, DV, 1.0, F, F, F, None, F, F) == \
+            lib.SGEMM_ERR_INVALID_ARG
+        assert lib.la_chunk_fused(BH, T, DK, DV, 1.0, F, F, F, None, None, F, None) == \
+            lib.SGEMM_ERR_INVALID_ARG
+        assert lib.la_state_bytes(BH, T, DK, DV) == 0
+    # NULL operands that are read or written; misaligned pointers
+    assert lib.la_chunk_state(2, 8, 64, 64, 0, F, None, None, F, None) == lib.SGEMM_ERR_INVALID_ARG
+    assert lib.la_chunk_state(2, 8, 64, 64, F, F, None, None, 0, None) == lib.SGEMM_ERR_INVALID_ARG
+    assert lib.la_chunk_output(2, 8, 64, 64, 1.0, F, F, F, None, 0, F) == lib.SGEMM_ERR_INVALID_ARG
+    assert lib.la_chunk_fused(2, 8, 64, 64, 1.0, F, F, F, None, None, 0, None) == \
+        lib.SGEMM_ERR_INVALID_ARG
+    assert lib.la_chunk_fused(2, 8, 64, 64, 1.0, F + 4, F, F, None, None, F, None) == \
+        lib.SGEMM_ERR_INVALID_ARG
+    assert lib.la_chunk_state(2, 8, 64, 64, F, F, F + 2, None, F, None) == \
+        lib.SGEMM_ERR_INVALID_ARG
+    # empty problems
+    assert lib.la_chunk_fused(0, 8, 64, 64, 1.0, 0, 0, 0, None, None, 0, None) == lib.SGEMM_OK
+    assert lib.la_chunk_output(3, 0, 64, 64, 1.0, 0, 0, 0, None, 0, 0) == lib.SGEMM_OK
+    assert lib.la_state_bytes(2, 65, 128, 64) == 2 * 2 * 128 * 64 * 4
