@@ -536,6 +536,7 @@ def main():
         extra = extra_figures(lib, mode, dev, stream, flush, num_sms, peaks, peak_src)
         extra["configs"] = config_figures(lib, dev, stream, flush, num_sms, peaks, peak_src,
                                           probes)
+        extra["linear_attention"] = la_figures(lib, dev, stream, flush, num_sms, peaks)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -697,6 +698,69 @@ def config_figures(lib, dev, stream, flush, num_sms, peaks, peak_src, probes, st
                 del ws
             out[key] = row
         del A, Bn, C
+    lib.check(lib.sgemm_poll_error(stream))
+    return out
+
+
+LA_WORKLOAD = "la_b4h16_t4096_d128"
+
+
+def la_flops(BH, T, DK, DV, BT=64):
+    """Algorithmic FLOPs of the chunked form: per chunk of BT tokens and per
+    head, Q K^T (BT x BT x DK), A V (BT x DV x BT), Q h (BT x DV x DK) and the
+    state update K^T V (DK x DV x BT), two FLOPs per multiply-add."""
+    NT = -(-T // BT)
+    return 2.0 * BT * (BT * DK + BT * DV + 2 * DK * DV) * NT * BH
+
+
+def la_figures(lib, dev, stream, flush, num_sms, peaks, steps=10):
+    """The linear-attention building blocks on the benchmark's workload
+    (64 heads x 4096 tokens, head dimension 128): the chunked path (state
+    pass, then output pass) and the fused pass, L2 flushed before every
+    timed call; roofline: the FP32 FFMA peak (the kernels run on the CUDA
+    cores) and, beside it, the HBM time of their compulsory bytes."""
+    import torch
+    import workloads
+    q, k, v, g, _, scale = workloads.la_make(LA_WORKLOAD)
+    BH, T, DK = q.shape
+    DV = v.shape[2]
+    NT = -(-T // 64)
+    t = lambda x: torch.from_numpy(x).to(dev)
+    dq, dk, dv, dg = t(q), t(k), t(v), t(g)
+    h = torch.empty(BH, NT, DK, DV, device=dev)
+    o = torch.empty(BH, T, DV, device=dev)
+    so = torch.empty(BH, DK, DV, device=dev)
+
+    def state():
+        lib.check(lib.la_chunk_state(BH, T, DK, DV, dk, dv, dg, None, h, so, stream))
+
+    def output():
+        lib.check(lib.la_chunk_output(BH, T, DK, DV, scale, dq, dk, dv, dg, h, o, stream))
+
+    def chunked():
+        state()
+        output()
+
+    def fused():
+        lib.check(lib.la_chunk_fused(BH, T, DK, DV, scale, dq, dk, dv, dg, None, o, so, stream))
+    flops = la_flops(BH, T, DK, DV)
+    mhz = float(peaks.get("sm_max_mhz", FALLBACK_PEAKS["sm_max_mhz"]))
+    peak = num_sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+    bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])) / 1e3
+    io = 4.0 * BH * T * (2 * DK + 2 * DV)          # q, k, v read; o written
+    hb = 4.0 * BH * NT * DK * DV                    # h written and read back
+    out = {"workload": LA_WORKLOAD, "BH": BH, "T": T, "DK": DK, "DV": DV, "chunk": 64,
+           "algorithmic_gflop": flops / 1e9,
+           "roofline": {"bound": "alu", "peak": peak, "unit": "TFLOP/s",
+                        "peak_source": f"FP32 FFMA peak: {num_sms} SMs x 128 lanes x 2 x "
+                                       f"{mhz:.0f} MHz"}}
+    for name, fn, nbytes in (("chunked", chunked, io + 2 * hb), ("fused", fused, io)):
+        ms = statistics.median(time_calls(fn, steps, 3, stream, flush))
+        tf = flops / (ms / 1e3) / 1e12
+        out[name] = {"ms": ms, "tflops": tf, "frac": tf / peak,
+                     "hbm_bytes": nbytes, "hbm_floor_ms": nbytes / bw / 1e9}
+    out["chunked"]["state_ms"] = statistics.median(time_calls(state, steps, 3, stream, flush))
+    out["chunked"]["output_ms"] = statistics.median(time_calls(output, steps, 3, stream, flush))
     lib.check(lib.sgemm_poll_error(stream))
     return out
 

@@ -9,24 +9,27 @@
 //   o_t     = scale (exp(G_t) q_t h_c + sum_{s <= t} exp(G_t - G_s) (q_t . k_s) v_s)
 //   h_{c+1} = exp(G_last) h_c + sum_s exp(G_last - G_s) k_s^T v_s
 //
-// Three kernels, one CTA of 256 threads each:
-//   la_state_kernel   grid (DV / 64, BH): the scan over chunks.  A CTA keeps
-//                     its K x 64 slice of S in registers (thread (ti, tj):
-//                     rows 4 ti + 64 r, columns 4 tj), stores each chunk's
-//                     starting state to h, then adds the chunk's decayed
-//                     K^T V.  Parallelism: heads x state slices (the scan is
-//                     sequential in the chunks, as the pages note).
-//   la_output_kernel  grid (NT, BH): one chunk of one head: A = Q K^T in
-//                     registers (thread (ti, tj): rows ti + 16 r, columns
-//                     tj + 16 c), masked, scaled and decayed into shared
-//                     memory, then O = A V + scale exp(G_t) (Q h_c), thread
-//                     (ti, tj): rows ti + 16 r, columns 4 tj + 64 c.
-//   la_fused_kernel   grid (DV / 64, BH): both in one pass, chunk after
-//                     chunk, the state never leaving the CTA (registers for
-//                     the update, a shared copy for Q S).
-// Operands are staged in shared memory with rows padded by four floats so
-// that sixteen lanes reading sixteen consecutive rows' 16-byte words hit
-// distinct banks.  Every accumulation is fp32 FMA; exp is the CUDA expf.
+// Three kernels, one CTA of 256 threads each, operands staged in shared
+// memory by cp.async with rows padded by four floats (sixteen lanes reading
+// sixteen rows' 16-byte words at one column hit distinct banks):
+//   la_state_kernel   grid (DV / 64, DK / 64, BH), two CTAs per SM: the scan
+//                     over chunks.  A CTA keeps a 64 x 64 slice of S in
+//                     registers (thread (ti, tj): rows 4 ti + e, columns
+//                     4 tj + f), stores each chunk's starting state to h and
+//                     adds the chunk's K^T (w V), w the decay weights; the
+//                     next two chunks' slices are in flight meanwhile.
+//   la_output_kernel  grid (NT, BH), two CTAs per SM: one chunk of one head.
+//                     A = Q K^T (thread (ti, tj): rows ti + 16 r, columns
+//                     tj + 16 c), masked, scaled and decayed in shared
+//                     memory; then one accumulator takes A V and the
+//                     earlier chunks' (scale exp(G_t) q_t) h_c (thread
+//                     (ti, tj): rows ti + 16 r, columns 4 tj + 64 c).
+//   la_fused_kernel   grid (DV / 64, BH): both in one pass, the state slice
+//                     never leaving the CTA, the next chunk's operands in
+//                     flight while this one is computed.
+// Parallelism: the state and fused passes are sequential in the chunks (the
+// scan the pages describe); the output pass is parallel over chunks.  Every
+// product and sum is an fp32 FMA; exp is the CUDA expf.
 #include <cstddef>
 #include <cstdint>
 
@@ -34,6 +37,7 @@
 
 #include "../../include/linear_attention.h"
 #include "../../include/sgemm.h"
+#include "common.cuh"
 #include "internal.h"
 
 namespace sg {
@@ -49,21 +53,6 @@ struct Args {
     int T, NT;
     float scale;
 };
-
-// Copies rows [0, n) of `cols` floats (global row pitch gp, first column c0)
-// into shared memory rows of pitch sp, zero-filling rows n .. BT-1.
-template <int COLS>
-__device__ __forceinline__ void stage_rows(float *dst, int sp, const float *src, long long gp,
-                                           int n, int tid)
-{
-    constexpr int V4 = COLS / 4;
-    for (int i = tid; i < BT * V4; i += kThreads) {
-        const int r = i / V4, c = (i - r * V4) * 4;
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < n) x = *reinterpret_cast<const float4 *>(src + r * gp + c);
-        *reinterpret_cast<float4 *>(dst + r * sp + c) = x;
-    }
-}
 
 // G[t] = g[0] + ... + g[t] over the chunk's n tokens (constant past them;
 // zero without a decay), by warp 0: lane l sums tokens 2l, 2l+1, then an
@@ -82,6 +71,34 @@ __device__ __forceinline__ void chunk_decay(const float *g, int n, float *G, int
     }
     G[2 * l] = s - b;
     G[2 * l + 1] = s;
+}
+
+// 16-byte asynchronous copy global -> shared; zero-filled when !valid (src
+// is then not read, but must be a valid address).
+__device__ __forceinline__ void cp16(float *dst, const float *src, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Issues the copies of rows [0, n) of COLS floats (global pitch gp) into
+// shared rows of pitch sp, zero-filling rows n .. BT-1 (no commit).
+template <int COLS>
+__device__ __forceinline__ void stage_rows_async(float *dst, int sp, const float *src,
+                                                 long long gp, int n, int tid)
+{
+    constexpr int V4 = COLS / 4;
+    for (int i = tid; i < BT * V4; i += kThreads) {
+        const int r = i / V4, c = (i - r * V4) * 4;
+        cp16(dst + r * sp + c, r < n ? src + r * gp + c : src, r < n);
+    }
 }
 
 __device__ __forceinline__ void fma4(float (&acc)[4], float a, const float4 b)
@@ -162,56 +179,143 @@ __device__ __forceinline__ void state_load(StateRegs<DK> &S, const float *src, l
         }
 }
 
-// Stages the chunk's K (all DK columns) and V (columns v0 .. v0 + 63), the
-// running decay G and the state update's weights: V rows scaled by
-// exp(G_last - G_s) (zero past the chunk's n tokens).  Returns
-// exp(G_last).  Ends with a barrier.
-template <int DK, int DV>
-__device__ __forceinline__ float stage_update_operands(const Args &p, long long head, int t0,
-                                                       int n, int v0, float *Ks, float *Vw,
-                                                       float *G, int tid)
+// The chunk's decay for the state update, by warp 0 into W, from the
+// chunk's log-decays (lane l holds tokens 2l, 2l+1 in a, b; zero past the
+// chunk's n tokens): W[s] = exp(G_last - G_s) for s < n (0 past them),
+// W[BT] = exp(G_last), G the running sum over the chunk.
+__device__ __forceinline__ void update_weights(float a, float b, int n, float *W, int l)
 {
-    stage_rows<DK>(Ks, DK + 4, p.k + (head * p.T + t0) * DK, DK, n, tid);
-    stage_rows<BV>(Vw, BV + 4, p.v + (head * p.T + t0) * DV + v0, DV, n, tid);
-    chunk_decay(p.g != nullptr ? p.g + head * p.T + t0 : nullptr, n, G, tid);
-    __syncthreads();
-    const float glast = G[n - 1];
-    for (int i = tid; i < BT * (BV / 4); i += kThreads) {
-        const int s = i / (BV / 4), c = (i - s * (BV / 4)) * 4;
-        const float w = s < n ? expf(glast - G[s]) : 0.f;
-        float4 *x = reinterpret_cast<float4 *>(Vw + s * (BV + 4) + c);
-        float4 y = *x;
-        y.x *= w;
-        y.y *= w;
-        y.z *= w;
-        y.w *= w;
-        *x = y;
+    float s = a + b;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, s, off);
+        if (l >= off) s += y;
     }
-    __syncthreads();
-    return expf(glast);
+    // G[n-1]: the inclusive sum up to token n-1 (lane (n-1)/2 holds it)
+    const int src = (n - 1) >> 1;
+    const float hi = __shfl_sync(0xffffffffu, s, src);
+    const float bb = __shfl_sync(0xffffffffu, b, src);
+    const float glast = ((n - 1) & 1) ? hi : hi - bb;
+    W[2 * l] = 2 * l < n ? expf(glast - (s - b)) : 0.f;
+    W[2 * l + 1] = 2 * l + 1 < n ? expf(glast - s) : 0.f;
+    if (l == 0) W[BT] = expf(glast);
 }
 
-template <int DK, int DV>
-__global__ void __launch_bounds__(kThreads) la_state_kernel(const Args p)
+// Warp 0's pair of a chunk's log-decays (see update_weights).
+__device__ __forceinline__ void load_decay_pair(const Args &p, long long head, int c, int l,
+                                                float &a, float &b)
 {
+    a = b = 0.f;
+    if (p.g == nullptr || c >= p.NT) return;
+    const int t0 = c * BT, n = min(BT, p.T - t0);
+    const float *g = p.g + head * p.T + t0;
+    if (2 * l < n) a = g[2 * l];
+    if (2 * l + 1 < n) b = g[2 * l + 1];
+}
+
+// The state pass, grid (DV / 64, DK / 64, BH): a CTA owns a 64 x 64 slice of
+// one head's state, rows k0 = 64 blockIdx.y .., columns v0 = 64 blockIdx.x
+// .. -- thread (ti, tj) rows k0 + 4 ti + e, columns v0 + 4 tj + f -- and
+// walks the chunks in order.  The K and V slices of the next two chunks are
+// in flight (cp.async, three buffers) while this one's update runs, and
+// warp 0 holds the next chunk's log-decays in registers; the decay weights
+// multiply the K values as they are read.
+constexpr int kStateBufs = 3;
+template <int DK, int DV>
+__global__ void __launch_bounds__(kThreads, 2) la_state_kernel(const Args p)
+{
+    constexpr int P = 64 + 4;  // row pitch of the staged slices
     extern __shared__ float4 smem4[];
-    float *Ks = reinterpret_cast<float *>(smem4);  // BT x (DK + 4)
-    float *Vw = Ks + BT * (DK + 4);                // BT x (BV + 4)
-    float *G = Vw + BT * (BV + 4);                 // BT
+    float *Kb = reinterpret_cast<float *>(smem4);  // kStateBufs x BT x P
+    float *Vb = Kb + kStateBufs * BT * P;          // kStateBufs x BT x P
+    float *W = Vb + kStateBufs * BT * P;           // BT + 1
     const int tid = threadIdx.x, ti = tid >> 4, tj = tid & 15;
-    const int v0 = blockIdx.x * BV;
-    const long long head = blockIdx.y;
-    StateRegs<DK> S;
-    state_load<DK>(S, p.h0 != nullptr ? p.h0 + head * DK * DV : nullptr, DV, v0, ti, tj);
-    for (int c = 0; c < p.NT; ++c) {
-        const int t0 = c * BT, n = min(BT, p.T - t0);
-        state_store<DK>(S, p.h + (head * p.NT + c) * DK * DV, DV, v0, ti, tj);
-        const float a = stage_update_operands<DK, DV>(p, head, t0, n, v0, Ks, Vw, G, tid);
-        state_update<DK>(S, a, Ks, Vw, ti, tj);
-        __syncthreads();  // before the next chunk overwrites Ks, Vw, G
+    const int v0 = blockIdx.x * 64, k0 = blockIdx.y * 64;
+    const long long head = blockIdx.z;
+    float S[4][4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.h0 != nullptr)
+            x = *reinterpret_cast<const float4 *>(p.h0 + (head * DK + k0 + 4 * ti + e) * DV + v0 +
+                                                  4 * tj);
+        S[e][0] = x.x;
+        S[e][1] = x.y;
+        S[e][2] = x.z;
+        S[e][3] = x.w;
     }
-    if (p.state_out != nullptr)
-        state_store<DK>(S, p.state_out + head * DK * DV, DV, v0, ti, tj);
+    // one commit group per chunk (empty past the last chunk), so that
+    // "all but the newest kStateBufs - 1 groups done" means "this chunk landed"
+    auto issue = [&](int c) {
+        if (c < p.NT) {
+            const int t0 = c * BT, n = min(BT, p.T - t0), buf = c % kStateBufs;
+            stage_rows_async<64>(Kb + buf * BT * P, P, p.k + (head * p.T + t0) * DK + k0, DK, n,
+                                 tid);
+            stage_rows_async<64>(Vb + buf * BT * P, P, p.v + (head * p.T + t0) * DV + v0, DV, n,
+                                 tid);
+        }
+        cp_commit();
+    };
+    for (int c = 0; c < kStateBufs - 1; ++c) issue(c);
+    float ga = 0.f, gb = 0.f;
+    if (tid < 32) load_decay_pair(p, head, 0, tid, ga, gb);
+    for (int c = 0; c < p.NT; ++c) {
+        const int n = min(BT, p.T - c * BT), buf = c % kStateBufs;
+        float *hc = p.h + ((head * p.NT + c) * DK + k0 + 4 * ti) * DV + v0 + 4 * tj;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<float4 *>(hc + e * DV) = make_float4(S[e][0], S[e][1], S[e][2],
+                                                                   S[e][3]);
+        issue(c + kStateBufs - 1);
+        float na = 0.f, nb = 0.f;
+        if (tid < 32) {
+            load_decay_pair(p, head, c + 1, tid, na, nb);
+            update_weights(ga, gb, n, W, tid);
+        }
+        cp_wait<kStateBufs - 1>();
+        __syncthreads();
+        const float *Ks = Kb + buf * BT * P;
+        float *Vs = Vb + buf * BT * P;
+        // V rows times their weights (each thread four 16-byte words)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int u = tid + i * kThreads, s = u >> 4, cc = (u & 15) * 4;
+            float4 *x = reinterpret_cast<float4 *>(Vs + s * P + cc);
+            const float w = W[s];
+            float4 y = *x;
+            y.x *= w;
+            y.y *= w;
+            y.z *= w;
+            y.w *= w;
+            *x = y;
+        }
+        const float a = W[BT];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+            for (int f = 0; f < 4; ++f) S[e][f] *= a;
+        __syncthreads();
+#pragma unroll 8
+        for (int s = 0; s < BT; ++s) {
+            const float4 kk = *reinterpret_cast<const float4 *>(Ks + s * P + 4 * ti);
+            const float4 vv = *reinterpret_cast<const float4 *>(Vs + s * P + 4 * tj);
+            fma4(S[0], kk.x, vv);
+            fma4(S[1], kk.y, vv);
+            fma4(S[2], kk.z, vv);
+            fma4(S[3], kk.w, vv);
+        }
+        ga = na;
+        gb = nb;
+        __syncthreads();  // the next issue reuses a buffer read here, the next chunk W
+    }
+    cp_wait<0>();
+    if (p.state_out != nullptr) {
+        float *so = p.state_out + (head * DK + k0 + 4 * ti) * DV + v0 + 4 * tj;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<float4 *>(so + e * DV) = make_float4(S[e][0], S[e][1], S[e][2],
+                                                                   S[e][3]);
+    }
 }
 
 // --------------------------------------------------------------- output pass
@@ -220,7 +324,7 @@ __global__ void __launch_bounds__(kThreads) la_state_kernel(const Args p)
 // scaled and decayed: As[t][s] = scale exp(G_t - G_s) (q_t . k_s) (pitch
 // BT + 4).  Thread (ti, tj): rows ti + 16 r, columns tj + 16 c.  Ends with a
 // barrier.
-template <int DK>
+template <int DK, int AP = BT + 4>
 __device__ __forceinline__ void attention_tile(const float *Qs, const float *Ks, const float *G,
                                                int n, float scale, float *As, int ti, int tj)
 {
@@ -251,130 +355,205 @@ __device__ __forceinline__ void attention_tile(const float *Qs, const float *Ks,
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const int s = tj + 16 * c;
-            As[t * (BT + 4) + s] =
-                (s <= t && t < n) ? scale * expf(G[t] - G[s]) * acc[r][c] : 0.f;
+            As[t * AP + s] = (s <= t && t < n) ? scale * expf(G[t] - G[s]) * acc[r][c] : 0.f;
         }
     }
     __syncthreads();
 }
 
-// O rows ti + 16 r, columns cb + 4 tj + 64 c (c < NC): intra = A V (As
-// pitch BT + 4, Vs pitch vp), inter = Q X (Qs pitch DK + 4, X: DK rows of
-// pitch xp); o = intra + scale exp(G_t) inter, stored for rows t < n to
-// dst (row pitch dp).
-template <int DK, int NC>
-__device__ __forceinline__ void output_tile(const float *As, const float *Vs, int vp,
-                                            const float *Qs, const float *X, int xp,
-                                            const float *G, int n, float scale, float *dst,
-                                            long long dp, int ti, int tj)
+// acc[r][c] += sum_{x < X} L[(ti + 16 r) * lp + x] R[x * rp + 4 tj + 64 c ..]:
+// thread rows ti + 16 r of L (scalars), columns 4 tj + 64 c of R (16-byte).
+template <int X, int NC>
+__device__ __forceinline__ void rows_times(float (&acc)[4][NC][4], const float *L, int lp,
+                                           const float *R, int rp, int ti, int tj)
 {
-    constexpr int KP = DK + 4;
-    float intra[4][NC][4] = {}, inter[4][NC][4] = {};
 #pragma unroll 4
-    for (int s = 0; s < BT; ++s) {
-        float4 vv[NC];
+    for (int x = 0; x < X; ++x) {
+        float4 rr[NC];
 #pragma unroll
         for (int c = 0; c < NC; ++c)
-            vv[c] = *reinterpret_cast<const float4 *>(Vs + s * vp + 4 * tj + 64 * c);
+            rr[c] = *reinterpret_cast<const float4 *>(R + x * rp + 4 * tj + 64 * c);
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            const float a = As[(ti + 16 * r) * (BT + 4) + s];
+            const float l = L[(ti + 16 * r) * lp + x];
 #pragma unroll
-            for (int c = 0; c < NC; ++c) fma4(intra[r][c], a, vv[c]);
+            for (int c = 0; c < NC; ++c) fma4(acc[r][c], l, rr[c]);
         }
-    }
-#pragma unroll 4
-    for (int k = 0; k < DK; ++k) {
-        float4 xx[NC];
-#pragma unroll
-        for (int c = 0; c < NC; ++c)
-            xx[c] = *reinterpret_cast<const float4 *>(X + k * xp + 4 * tj + 64 * c);
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const float qv = Qs[(ti + 16 * r) * KP + k];
-#pragma unroll
-            for (int c = 0; c < NC; ++c) fma4(inter[r][c], qv, xx[c]);
-        }
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int t = ti + 16 * r;
-        if (t >= n) continue;
-        const float e = scale * expf(G[t]);
-#pragma unroll
-        for (int c = 0; c < NC; ++c)
-            *reinterpret_cast<float4 *>(dst + t * dp + 4 * tj + 64 * c) =
-                make_float4(fmaf(e, inter[r][c][0], intra[r][c][0]),
-                            fmaf(e, inter[r][c][1], intra[r][c][1]),
-                            fmaf(e, inter[r][c][2], intra[r][c][2]),
-                            fmaf(e, inter[r][c][3], intra[r][c][3]));
     }
 }
 
+// The output pass, grid (NT, BH), two CTAs per multiprocessor: one chunk of
+// one head.  Q and K are staged; A = Q K^T is masked, scaled and decayed
+// into As; then one buffer holds in turn V and the two 64-row halves of the
+// chunk's state h_c (DK = 128; one half for DK = 64), and one accumulator
+// takes A V and then (scale exp(G_t) q_t) h_c -- the Q rows rescaled in place
+// once A is formed.
 template <int DK, int DV>
-__global__ void __launch_bounds__(kThreads) la_output_kernel(const Args p)
+__global__ void __launch_bounds__(kThreads, 2) la_output_kernel(const Args p)
 {
+    constexpr int QP = DK + 4, BP = (DK > DV ? DK : DV) + 4, AP = BT + 1;
+    constexpr int NC = DV / 64;
     extern __shared__ float4 smem4[];
-    float *Qs = reinterpret_cast<float *>(smem4);  // BT x (DK + 4)
-    float *Ks = Qs + BT * (DK + 4);                // BT x (DK + 4)
-    float *Vs = Ks + BT * (DK + 4);                // BT x DV
-    float *Hs = Vs + BT * DV;                      // DK x DV
-    float *As = Hs + DK * DV;                      // BT x (BT + 4)
-    float *G = As + BT * (BT + 4);                 // BT
+    float *Qs = reinterpret_cast<float *>(smem4);  // BT x QP
+    float *Bs = Qs + BT * QP;                      // BT x BP: K, then V, then h_c halves
+    float *As = Bs + BT * BP;                      // BT x AP
+    float *G = As + BT * AP;                       // BT
     const int tid = threadIdx.x, ti = tid >> 4, tj = tid & 15;
     const int c = blockIdx.x;
     const long long head = blockIdx.y;
     const int t0 = c * BT, n = min(BT, p.T - t0);
-    stage_rows<DK>(Qs, DK + 4, p.q + (head * p.T + t0) * DK, DK, n, tid);
-    stage_rows<DK>(Ks, DK + 4, p.k + (head * p.T + t0) * DK, DK, n, tid);
-    stage_rows<DV>(Vs, DV, p.v + (head * p.T + t0) * DV, DV, n, tid);
-    {
-        const float4 *src = reinterpret_cast<const float4 *>(p.h + (head * p.NT + c) * DK * DV);
-        float4 *dst = reinterpret_cast<float4 *>(Hs);
-        for (int i = tid; i < DK * DV / 4; i += kThreads) dst[i] = src[i];
-    }
+    stage_rows_async<DK>(Qs, QP, p.q + (head * p.T + t0) * DK, DK, n, tid);
+    stage_rows_async<DK>(Bs, DK + 4, p.k + (head * p.T + t0) * DK, DK, n, tid);
+    cp_commit();
     chunk_decay(p.g != nullptr ? p.g + head * p.T + t0 : nullptr, n, G, tid);
+    cp_wait<0>();
     __syncthreads();
-    attention_tile<DK>(Qs, Ks, G, n, p.scale, As, ti, tj);
-    output_tile<DK, DV / 64>(As, Vs, DV, Qs, Hs, DV, G, n, p.scale,
-                             p.o + (head * p.T + t0) * DV, DV, ti, tj);
+    attention_tile<DK, AP>(Qs, Bs, G, n, p.scale, As, ti, tj);  // ends with a barrier
+    stage_rows_async<DV>(Bs, BP, p.v + (head * p.T + t0) * DV, DV, n, tid);
+    cp_commit();
+    // Q rows times scale exp(G_t), for the earlier chunks' term
+    for (int i = tid; i < BT * (DK / 4); i += kThreads) {
+        const int t = i / (DK / 4), k = (i - t * (DK / 4)) * 4;
+        const float e = p.scale * expf(G[t]);
+        float4 *x = reinterpret_cast<float4 *>(Qs + t * QP + k);
+        float4 y = *x;
+        y.x *= e;
+        y.y *= e;
+        y.z *= e;
+        y.w *= e;
+        *x = y;
+    }
+    cp_wait<0>();
+    __syncthreads();
+    float acc[4][NC][4] = {};
+    rows_times<BT, NC>(acc, As, AP, Bs, BP, ti, tj);
+    const float *hc = p.h + (head * p.NT + c) * DK * DV;
+#pragma unroll 1
+    for (int half = 0; half < DK / 64; ++half) {
+        __syncthreads();  // every thread is done with Bs
+        stage_rows_async<DV>(Bs, BP, hc + half * 64 * DV, DV, 64, tid);
+        cp_commit();
+        cp_wait<0>();
+        __syncthreads();
+        rows_times<64, NC>(acc, Qs + half * 64, QP, Bs, BP, ti, tj);
+    }
+    float *o = p.o + (head * p.T + t0) * DV;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int t = ti + 16 * r;
+        if (t >= n) continue;
+#pragma unroll
+        for (int cc = 0; cc < NC; ++cc)
+            *reinterpret_cast<float4 *>(o + t * DV + 4 * tj + 64 * cc) =
+                make_float4(acc[r][cc][0], acc[r][cc][1], acc[r][cc][2], acc[r][cc][3]);
+    }
 }
 
 // ---------------------------------------------------------------- fused pass
 
-template <int DK, int DV>
-__global__ void __launch_bounds__(kThreads) la_fused_kernel(const Args p)
+// Warp 0: the chunk's running decay G (the output's mask and the earlier
+// chunks' factor) and the state update's weights W (update_weights), from
+// the chunk's log-decays held in registers.
+__device__ __forceinline__ void chunk_decays(float a, float b, int n, float *G, float *W, int l)
 {
+    float s = a + b;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, s, off);
+        if (l >= off) s += y;
+    }
+    G[2 * l] = s - b;
+    G[2 * l + 1] = s;
+    const int src = (n - 1) >> 1;
+    const float hi = __shfl_sync(0xffffffffu, s, src);
+    const float bb = __shfl_sync(0xffffffffu, b, src);
+    const float glast = ((n - 1) & 1) ? hi : hi - bb;
+    W[2 * l] = 2 * l < n ? expf(glast - (s - b)) : 0.f;
+    W[2 * l + 1] = 2 * l + 1 < n ? expf(glast - s) : 0.f;
+    if (l == 0) W[BT] = expf(glast);
+}
+
+// The fused pass, grid (DV / 64, BH), one CTA per multiprocessor: a 64-column
+// slice of one head's state stays in the CTA (registers for the update, a
+// shared copy for Q S) while the CTA walks the chunks; the next chunk's Q, K
+// and V are in flight (cp.async, two buffers) while this one is computed,
+// and warp 0 holds the next chunk's log-decays.  Per chunk: A = Q K^T
+// masked, scaled and decayed; O = A V + (scale exp(G_t) q_t) S (one
+// accumulator, the Q rows rescaled in place once A is formed); then
+// S = exp(G_last) S + sum_s exp(G_last - G_s) k_s^T v_s.
+template <int DK, int DV>
+__global__ void __launch_bounds__(kThreads, 1) la_fused_kernel(const Args p)
+{
+    constexpr int QP = DK + 4, VP = BV + 4, AP = BT + 1;
     extern __shared__ float4 smem4[];
-    float *Qs = reinterpret_cast<float *>(smem4);  // BT x (DK + 4)
-    float *Ks = Qs + BT * (DK + 4);                // BT x (DK + 4)
-    float *Vs = Ks + BT * (DK + 4);                // BT x (BV + 4): V, then weighted V
-    float *Ss = Vs + BT * (BV + 4);                // DK x BV: the state before the chunk
-    float *As = Ss + DK * BV;                      // BT x (BT + 4)
-    float *G = As + BT * (BT + 4);                 // BT
+    float *Qb = reinterpret_cast<float *>(smem4);  // 2 x BT x QP
+    float *Kb = Qb + 2 * BT * QP;                  // 2 x BT x QP
+    float *Vb = Kb + 2 * BT * QP;                  // 2 x BT x VP
+    float *As = Vb + 2 * BT * VP;                  // BT x AP
+    float *Ss = As + BT * AP;                      // DK x VP: the state before the chunk
+    float *G = Ss + DK * VP;                       // BT
+    float *W = G + BT;                             // BT + 1
     const int tid = threadIdx.x, ti = tid >> 4, tj = tid & 15;
     const int v0 = blockIdx.x * BV;
     const long long head = blockIdx.y;
     StateRegs<DK> S;
     state_load<DK>(S, p.h0 != nullptr ? p.h0 + head * DK * DV : nullptr, DV, v0, ti, tj);
+    auto issue = [&](int c) {
+        if (c < p.NT) {
+            const int t0 = c * BT, n = min(BT, p.T - t0), buf = c & 1;
+            stage_rows_async<DK>(Qb + buf * BT * QP, QP, p.q + (head * p.T + t0) * DK, DK, n, tid);
+            stage_rows_async<DK>(Kb + buf * BT * QP, QP, p.k + (head * p.T + t0) * DK, DK, n, tid);
+            stage_rows_async<BV>(Vb + buf * BT * VP, VP, p.v + (head * p.T + t0) * DV + v0, DV, n,
+                                 tid);
+        }
+        cp_commit();
+    };
+    issue(0);
+    float ga = 0.f, gb = 0.f;
+    if (tid < 32) load_decay_pair(p, head, 0, tid, ga, gb);
     for (int c = 0; c < p.NT; ++c) {
-        const int t0 = c * BT, n = min(BT, p.T - t0);
-        state_store<DK>(S, Ss, BV, 0, ti, tj);
-        stage_rows<DK>(Qs, DK + 4, p.q + (head * p.T + t0) * DK, DK, n, tid);
-        stage_rows<DK>(Ks, DK + 4, p.k + (head * p.T + t0) * DK, DK, n, tid);
-        stage_rows<BV>(Vs, BV + 4, p.v + (head * p.T + t0) * DV + v0, DV, n, tid);
-        chunk_decay(p.g != nullptr ? p.g + head * p.T + t0 : nullptr, n, G, tid);
+        const int t0 = c * BT, n = min(BT, p.T - t0), buf = c & 1;
+        float *Qs = Qb + buf * BT * QP;
+        const float *Ks = Kb + buf * BT * QP;
+        float *Vs = Vb + buf * BT * VP;
+        issue(c + 1);
+        float na = 0.f, nb = 0.f;
+        if (tid < 32) {
+            load_decay_pair(p, head, c + 1, tid, na, nb);
+            chunk_decays(ga, gb, n, G, W, tid);
+        }
+        state_store<DK>(S, Ss, VP, 0, ti, tj);
+        cp_wait<1>();
         __syncthreads();
-        attention_tile<DK>(Qs, Ks, G, n, p.scale, As, ti, tj);
-        output_tile<DK, 1>(As, Vs, BV + 4, Qs, Ss, BV, G, n, p.scale,
-                           p.o + (head * p.T + t0) * DV + v0, DV, ti, tj);
-        // the state update: V rows weighted by exp(G_last - G_s)
-        const float glast = G[n - 1];
-        __syncthreads();  // every thread is done reading Vs as V
+        attention_tile<DK, AP>(Qs, Ks, G, n, p.scale, As, ti, tj);  // ends with a barrier
+        for (int i = tid; i < BT * (DK / 4); i += kThreads) {
+            const int t = i / (DK / 4), k = (i - t * (DK / 4)) * 4;
+            const float e = p.scale * expf(G[t]);
+            float4 *x = reinterpret_cast<float4 *>(Qs + t * QP + k);
+            float4 y = *x;
+            y.x *= e;
+            y.y *= e;
+            y.z *= e;
+            y.w *= e;
+            *x = y;
+        }
+        __syncthreads();
+        float acc[4][1][4] = {};
+        rows_times<BT, 1>(acc, As, AP, Vs, VP, ti, tj);
+        rows_times<DK, 1>(acc, Qs, QP, Ss, VP, ti, tj);
+        float *o = p.o + (head * p.T + t0) * DV + v0;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int t = ti + 16 * r;
+            if (t < n)
+                *reinterpret_cast<float4 *>(o + t * DV + 4 * tj) =
+                    make_float4(acc[r][0][0], acc[r][0][1], acc[r][0][2], acc[r][0][3]);
+        }
+        __syncthreads();  // V is read as V above; the update reads it weighted
         for (int i = tid; i < BT * (BV / 4); i += kThreads) {
-            const int s = i / (BV / 4), cc = (i - s * (BV / 4)) * 4;
-            const float w = s < n ? expf(glast - G[s]) : 0.f;
-            float4 *x = reinterpret_cast<float4 *>(Vs + s * (BV + 4) + cc);
+            const int s2 = i / (BV / 4), cc = (i - s2 * (BV / 4)) * 4;
+            const float w = W[s2];
+            float4 *x = reinterpret_cast<float4 *>(Vs + s2 * VP + cc);
             float4 y = *x;
             y.x *= w;
             y.y *= w;
@@ -383,9 +562,12 @@ __global__ void __launch_bounds__(kThreads) la_fused_kernel(const Args p)
             *x = y;
         }
         __syncthreads();
-        state_update<DK>(S, expf(glast), Ks, Vs, ti, tj);
-        __syncthreads();  // before the next chunk overwrites the staged operands
+        state_update<DK>(S, W[BT], Ks, Vs, ti, tj);
+        ga = na;
+        gb = nb;
+        __syncthreads();  // the next issue reuses this chunk's buffers; G, W, Ss
     }
+    cp_wait<0>();
     if (p.state_out != nullptr)
         state_store<DK>(S, p.state_out + head * DK * DV, DV, v0, ti, tj);
 }
@@ -393,17 +575,18 @@ __global__ void __launch_bounds__(kThreads) la_fused_kernel(const Args p)
 template <int DK, int DV>
 constexpr size_t state_smem()
 {
-    return sizeof(float) * (BT * (DK + 4) + BT * (BV + 4) + BT);
+    return sizeof(float) * (2 * kStateBufs * BT * 68 + BT + 4);
 }
 template <int DK, int DV>
 constexpr size_t output_smem()
 {
-    return sizeof(float) * (2 * BT * (DK + 4) + BT * DV + DK * DV + BT * (BT + 4) + BT);
+    return sizeof(float) * (BT * (DK + 4) + BT * ((DK > DV ? DK : DV) + 4) + BT * (BT + 1) + BT);
 }
 template <int DK, int DV>
 constexpr size_t fused_smem()
 {
-    return sizeof(float) * (2 * BT * (DK + 4) + BT * (BV + 4) + DK * BV + BT * (BT + 4) + BT);
+    return sizeof(float) *
+           (4 * BT * (DK + 4) + 2 * BT * (BV + 4) + BT * (BT + 1) + DK * (BV + 4) + 2 * BT + 4);
 }
 
 enum Which { kState, kOutput, kFused };
@@ -417,7 +600,7 @@ int launch(Which w, const Args &a, int BH, cudaStream_t st)
     if (w == kState) {
         kern = la_state_kernel<DK, DV>;
         smem = state_smem<DK, DV>();
-        grid = dim3(DV / BV, static_cast<unsigned>(BH));
+        grid = dim3(DV / 64, DK / 64, static_cast<unsigned>(BH));
     } else if (w == kOutput) {
         kern = la_output_kernel<DK, DV>;
         smem = output_smem<DK, DV>();
@@ -427,7 +610,7 @@ int launch(Which w, const Args &a, int BH, cudaStream_t st)
         smem = fused_smem<DK, DV>();
         grid = dim3(DV / BV, static_cast<unsigned>(BH));
     }
-    if (grid.x == 0 || grid.y == 0) return SGEMM_OK;
+    if (grid.x == 0 || grid.y == 0 || grid.z == 0) return SGEMM_OK;
     if (!smem_attr_once(reinterpret_cast<const void *>(kern), static_cast<int>(smem)))
         return SGEMM_ERR_LAUNCH;
     kern<<<grid, kThreads, smem, st>>>(a);
