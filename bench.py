@@ -92,7 +92,7 @@ def roofline_peak(mode, num_sms, peaks, source):
 # entry point are left out (they do not change what the timed kernels do).
 TIMED_SOURCES = ("api.cu", "common.cuh", "internal.h", "kernels_simt.cu", "kernels_tc.cu",
                  "kernels_tcp.cu", "params.h", "planes.cu", "repack.cu", "simt_fp32.cuh",
-                 "tc_direct.cuh", "tc_pair.cuh", "tc_ss.cuh", "tc_tf32.cuh")
+                 "tc_direct.cuh", "tc_pair.cuh", "tc_ss.cuh", "tc_tf32.cuh", "tune_table.h")
 
 
 def kernel_source_hash():
@@ -398,6 +398,9 @@ def main():
     ap.add_argument("--bmm-only", action="store_true",
                     help="instead of the benchmark line, print one JSON line with the batched "
                          "workload's figures on --mode (3xtf32 for auto), --steps timed calls")
+    ap.add_argument("--la-only", action="store_true",
+                    help="instead of the benchmark line, print one JSON line with the "
+                         "linear-attention kernels' figures (--steps timed calls each)")
     ap.add_argument("--tune", action="store_true",
                     help="instead of the benchmark line, time every kernel route on one shape "
                          "per (mode, size class), print one JSON line per shape, and write "
@@ -420,6 +423,8 @@ def main():
         return all_configs(args)
     if args.tune:
         return tune(args)
+    if args.la_only:
+        return la_only(args.steps)
     if args.half_only:
         return half_only()
     if args.bmm_only:
@@ -802,6 +807,24 @@ def bmm_only(mode, steps):
     flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
     out = bmm_figures(lib, mode, dev, torch.cuda.current_stream(dev), flush, steps)
     print(json.dumps({"bmm": out, "l2": "flushed before every timed step"}), flush=True)
+    return 0
+
+
+def la_only(steps):
+    """--la-only: the linear-attention building blocks alone (a short command
+    to profile)."""
+    import torch
+    import dense_fp32_matrix_03_gb300 as lib
+    dev = torch.device("cuda", 0)
+    lib.load()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    peaks, _ = load_peaks()
+    out = la_figures(lib, dev, torch.cuda.current_stream(dev), flush,
+                     props.multi_processor_count, peaks, steps)
+    print(json.dumps({"linear_attention": out, "l2": "flushed before every timed step"}),
+          flush=True)
     return 0
 
 
