@@ -101,6 +101,35 @@ __device__ __forceinline__ void stage_rows_async(float *dst, int sp, const float
     }
 }
 
+// Packed accumulation: two fp32 FMAs per instruction (fma.rn.f32x2 on a
+// 64-bit register pair; each half rounded exactly as a scalar fmaf, so the
+// results are those of scalar FMAs).  A 16-byte shared load gives two such
+// pairs; the scalar factor is broadcast into both halves.
+__device__ __forceinline__ unsigned long long dup2(float x)
+{
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void fma2(unsigned long long &d, unsigned long long a,
+                                     unsigned long long b)
+{
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ float2 unpack2(unsigned long long r)
+{
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+// acc (four values as two pairs) += a * (b.x, b.y, b.z, b.w)
+__device__ __forceinline__ void fma4p(unsigned long long (&acc)[2], float a, const ulonglong2 b)
+{
+    const unsigned long long aa = dup2(a);
+    fma2(acc[0], aa, b.x);
+    fma2(acc[1], aa, b.y);
+}
+
 __device__ __forceinline__ void fma4(float (&acc)[4], float a, const float4 b)
 {
     acc[0] = fmaf(a, b.x, acc[0]);
@@ -232,17 +261,15 @@ __global__ void __launch_bounds__(kThreads, 2) la_state_kernel(const Args p)
     const int tid = threadIdx.x, ti = tid >> 4, tj = tid & 15;
     const int v0 = blockIdx.x * 64, k0 = blockIdx.y * 64;
     const long long head = blockIdx.z;
-    float S[4][4];
+    unsigned long long S[4][2];  // row 4 ti + e, columns (4 tj, +1) and (+2, +3), packed
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        ulonglong2 x = make_ulonglong2(0ull, 0ull);
         if (p.h0 != nullptr)
-            x = *reinterpret_cast<const float4 *>(p.h0 + (head * DK + k0 + 4 * ti + e) * DV + v0 +
-                                                  4 * tj);
+            x = *reinterpret_cast<const ulonglong2 *>(p.h0 + (head * DK + k0 + 4 * ti + e) * DV +
+                                                      v0 + 4 * tj);
         S[e][0] = x.x;
         S[e][1] = x.y;
-        S[e][2] = x.z;
-        S[e][3] = x.w;
     }
     // one commit group per chunk (empty past the last chunk), so that
     // "all but the newest kStateBufs - 1 groups done" means "this chunk landed"
@@ -264,8 +291,7 @@ __global__ void __launch_bounds__(kThreads, 2) la_state_kernel(const Args p)
         float *hc = p.h + ((head * p.NT + c) * DK + k0 + 4 * ti) * DV + v0 + 4 * tj;
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-            *reinterpret_cast<float4 *>(hc + e * DV) = make_float4(S[e][0], S[e][1], S[e][2],
-                                                                   S[e][3]);
+            *reinterpret_cast<ulonglong2 *>(hc + e * DV) = make_ulonglong2(S[e][0], S[e][1]);
         issue(c + kStateBufs - 1);
         float na = 0.f, nb = 0.f;
         if (tid < 32) {
@@ -289,20 +315,24 @@ __global__ void __launch_bounds__(kThreads, 2) la_state_kernel(const Args p)
             y.w *= w;
             *x = y;
         }
-        const float a = W[BT];
+        {
+            // S *= exp(G_last): fma with a zero addend rounds like the product
+            const unsigned long long a = dup2(W[BT]);
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
+            for (int e = 0; e < 4; ++e)
 #pragma unroll
-            for (int f = 0; f < 4; ++f) S[e][f] *= a;
+                for (int f = 0; f < 2; ++f)
+                    asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(S[e][f]) : "l"(a), "l"(0ull));
+        }
         __syncthreads();
 #pragma unroll 8
         for (int s = 0; s < BT; ++s) {
             const float4 kk = *reinterpret_cast<const float4 *>(Ks + s * P + 4 * ti);
-            const float4 vv = *reinterpret_cast<const float4 *>(Vs + s * P + 4 * tj);
-            fma4(S[0], kk.x, vv);
-            fma4(S[1], kk.y, vv);
-            fma4(S[2], kk.z, vv);
-            fma4(S[3], kk.w, vv);
+            const ulonglong2 vv = *reinterpret_cast<const ulonglong2 *>(Vs + s * P + 4 * tj);
+            fma4p(S[0], kk.x, vv);
+            fma4p(S[1], kk.y, vv);
+            fma4p(S[2], kk.z, vv);
+            fma4p(S[3], kk.w, vv);
         }
         ga = na;
         gb = nb;
@@ -313,8 +343,7 @@ __global__ void __launch_bounds__(kThreads, 2) la_state_kernel(const Args p)
         float *so = p.state_out + (head * DK + k0 + 4 * ti) * DV + v0 + 4 * tj;
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-            *reinterpret_cast<float4 *>(so + e * DV) = make_float4(S[e][0], S[e][1], S[e][2],
-                                                                   S[e][3]);
+            *reinterpret_cast<ulonglong2 *>(so + e * DV) = make_ulonglong2(S[e][0], S[e][1]);
     }
 }
 
@@ -364,20 +393,38 @@ __device__ __forceinline__ void attention_tile(const float *Qs, const float *Ks,
 // acc[r][c] += sum_{x < X} L[(ti + 16 r) * lp + x] R[x * rp + 4 tj + 64 c ..]:
 // thread rows ti + 16 r of L (scalars), columns 4 tj + 64 c of R (16-byte).
 template <int X, int NC>
-__device__ __forceinline__ void rows_times(float (&acc)[4][NC][4], const float *L, int lp,
-                                           const float *R, int rp, int ti, int tj)
+__device__ __forceinline__ void rows_times(unsigned long long (&acc)[4][NC][2], const float *L,
+                                           int lp, const float *R, int rp, int ti, int tj)
 {
 #pragma unroll 4
     for (int x = 0; x < X; ++x) {
-        float4 rr[NC];
+        ulonglong2 rr[NC];
 #pragma unroll
         for (int c = 0; c < NC; ++c)
-            rr[c] = *reinterpret_cast<const float4 *>(R + x * rp + 4 * tj + 64 * c);
+            rr[c] = *reinterpret_cast<const ulonglong2 *>(R + x * rp + 4 * tj + 64 * c);
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const float l = L[(ti + 16 * r) * lp + x];
 #pragma unroll
-            for (int c = 0; c < NC; ++c) fma4(acc[r][c], l, rr[c]);
+            for (int c = 0; c < NC; ++c) fma4p(acc[r][c], l, rr[c]);
+        }
+    }
+}
+
+// Stores the packed accumulator rows t = ti + 16 r < n, columns 4 tj + 64 c.
+template <int NC>
+__device__ __forceinline__ void store_rows(const unsigned long long (&acc)[4][NC][2], float *o,
+                                           long long op, int n, int ti, int tj)
+{
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int t = ti + 16 * r;
+        if (t >= n) continue;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const float2 a = unpack2(acc[r][c][0]), b = unpack2(acc[r][c][1]);
+            *reinterpret_cast<float4 *>(o + t * op + 4 * tj + 64 * c) =
+                make_float4(a.x, a.y, b.x, b.y);
         }
     }
 }
@@ -425,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 2) la_output_kernel(const Args p)
     }
     cp_wait<0>();
     __syncthreads();
-    float acc[4][NC][4] = {};
+    unsigned long long acc[4][NC][2] = {};
     rows_times<BT, NC>(acc, As, AP, Bs, BP, ti, tj);
     const float *hc = p.h + (head * p.NT + c) * DK * DV;
 #pragma unroll 1
@@ -437,16 +484,7 @@ __global__ void __launch_bounds__(kThreads, 2) la_output_kernel(const Args p)
         __syncthreads();
         rows_times<64, NC>(acc, Qs + half * 64, QP, Bs, BP, ti, tj);
     }
-    float *o = p.o + (head * p.T + t0) * DV;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int t = ti + 16 * r;
-        if (t >= n) continue;
-#pragma unroll
-        for (int cc = 0; cc < NC; ++cc)
-            *reinterpret_cast<float4 *>(o + t * DV + 4 * tj + 64 * cc) =
-                make_float4(acc[r][cc][0], acc[r][cc][1], acc[r][cc][2], acc[r][cc][3]);
-    }
+    store_rows<NC>(acc, p.o + (head * p.T + t0) * DV, DV, n, ti, tj);
 }
 
 // ---------------------------------------------------------------- fused pass
@@ -538,17 +576,10 @@ __global__ void __launch_bounds__(kThreads, 1) la_fused_kernel(const Args p)
             *x = y;
         }
         __syncthreads();
-        float acc[4][1][4] = {};
+        unsigned long long acc[4][1][2] = {};
         rows_times<BT, 1>(acc, As, AP, Vs, VP, ti, tj);
         rows_times<DK, 1>(acc, Qs, QP, Ss, VP, ti, tj);
-        float *o = p.o + (head * p.T + t0) * DV + v0;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int t = ti + 16 * r;
-            if (t < n)
-                *reinterpret_cast<float4 *>(o + t * DV + 4 * tj) =
-                    make_float4(acc[r][0][0], acc[r][0][1], acc[r][0][2], acc[r][0][3]);
-        }
+        store_rows<1>(acc, p.o + (head * p.T + t0) * DV + v0, DV, n, ti, tj);
         __syncthreads();  // V is read as V above; the update reads it weighted
         for (int i = tid; i < BT * (BV / 4); i += kThreads) {
             const int s2 = i / (BV / 4), cc = (i - s2 * (BV / 4)) * 4;
