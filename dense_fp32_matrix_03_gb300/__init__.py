@@ -43,8 +43,9 @@ SGEMM_ROUTE_SMALL = 1
 SGEMM_ROUTE_PAIR = 2
 SGEMM_ROUTE_DIRECT = 3
 SGEMM_ROUTE_PLANES = 4
+SGEMM_ROUTE_RAW = 5
 ROUTES = {"auto": SGEMM_ROUTE_AUTO, "small": SGEMM_ROUTE_SMALL, "pair": SGEMM_ROUTE_PAIR,
-          "direct": SGEMM_ROUTE_DIRECT, "planes": SGEMM_ROUTE_PLANES}
+          "direct": SGEMM_ROUTE_DIRECT, "planes": SGEMM_ROUTE_PLANES, "raw": SGEMM_ROUTE_RAW}
 
 SGEMM_MODE_DEFAULT = -1
 SGEMM_MODE_FP32 = 0

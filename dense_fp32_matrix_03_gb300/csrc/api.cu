@@ -218,7 +218,7 @@ bool current_sm103(int *num_sms, unsigned int **status)
 }
 
 bool encode_operand(CUtensorMap *map, const float *base, bool kin, long long rows, long long K,
-                    long long ld, int Q, long long stride, int box_rows)
+                    long long ld, int Q, long long stride, int box_rows, bool promote256)
 {
     if (!get_encoder()) return false;
     const bool batched = Q > 1 && stride != 0;
@@ -242,7 +242,28 @@ bool encode_operand(CUtensorMap *map, const float *base, bool kin, long long row
     const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base),
                                 dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                 kin ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                promote256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                           : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool encode_operand_mn(CUtensorMap *map, const float *base, long long rows, long long K,
+                       long long ld, int Q, long long stride, bool promote256)
+{
+    if (!get_encoder()) return false;
+    const bool batched = Q > 1 && stride != 0;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(K),
+                          batched ? static_cast<cuuint64_t>(Q) : 1};
+    cuuint64_t strides[2];
+    strides[0] = static_cast<cuuint64_t>(ld) * 4;
+    strides[1] = batched ? static_cast<cuuint64_t>(stride) * 4 : strides[0] * dims[1];
+    cuuint32_t box[3] = {32, 32, 1}, estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B,
+                                promote256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                           : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -297,7 +318,8 @@ int applicable(int mode, int route)
 {
     const bool fp32 = mode == SGEMM_MODE_FP32;
     if (route == kRouteSimtSmall) return fp32 ? route : kRouteAuto;
-    if (route == kRouteTcPair || route == kRouteTcDirect || route == kRouteTcPlanes)
+    if (route == kRouteTcPair || route == kRouteTcDirect || route == kRouteTcPlanes ||
+        route == kRouteTcRaw)
         return fp32 ? kRouteAuto : route;
     return kRouteAuto;
 }
@@ -698,6 +720,10 @@ int run(int mode, int M, int N, int K, float alpha, const float *A, int lda, con
         return launch_simt(plan, kRouteAuto);
     }
     bool taken = false;
+    if (route == kRouteAuto || route == kRouteTcRaw) {
+        rc = run_raw(plan, taken, route == kRouteTcRaw);
+        if (taken || rc != SGEMM_OK) return rc;
+    }
     if (route == kRouteAuto || route == kRouteTcPlanes) {
         rc = run_planes(plan, taken, route == kRouteTcPlanes);
         if (taken || rc != SGEMM_OK) return rc;
@@ -790,16 +816,25 @@ size_t sgemm_workspace_size(int mode, int M, int N, int K, int Q)
     if (mode == SGEMM_MODE_DEFAULT) mode = g_default_mode.load();
     if (M <= 0 || N <= 0 || K <= 0 || Q <= 0) return base;
     if (mode != SGEMM_MODE_3XTF32 && mode != SGEMM_MODE_TF32) return base;
-    // where the planes route pays for this shape (planes_pay): both
-    // operands' planes (every batch entry stored) and the split plan of its
-    // tiles, or the copies and plans of the other routes, whichever is larger
+    // where the raw route (3xTF32: its lo planes) or the planes route pays
+    // for this shape (raw_pay, planes_pay): the planes (every batch entry
+    // stored) and the split plan of their tiles, or the copies and plans of
+    // the other routes, whichever is larger
     const int route = route_for(mode, M, N, K, Q);
     if (route == kRouteTcPair || route == kRouteTcDirect) return base;
-    if (route != kRouteTcPlanes && !planes_pay(mode, M, N, K, Q, Q, Q, num_sms_or_zero()))
-        return base;
-    const size_t planes =
-        planes_bytes(mode, M, N, K, Q, Q) + preferred_plan(mode, M, N, K, Q).ws_bytes;
-    return planes > base ? planes : base;
+    const int sms = num_sms_or_zero();
+    size_t need = base;
+    const size_t split = preferred_plan(mode, M, N, K, Q).ws_bytes;
+    if (route == kRouteTcRaw || (route == kRouteAuto && raw_pay(mode, M, N, K, Q, Q, Q, sms))) {
+        const size_t lo = raw_lo_bytes_max(mode, M, N, K, Q, Q) + split;
+        if (lo > need) need = lo;
+    }
+    // operands TMA cannot describe take the planes route instead
+    if (route == kRouteTcPlanes || (route != kRouteTcRaw && planes_pay(mode, M, N, K, Q, Q, Q, sms))) {
+        const size_t planes = planes_bytes(mode, M, N, K, Q, Q) + split;
+        if (planes > need) need = planes;
+    }
+    return need;
 }
 
 int sgemm_set_default_mode(int mode)

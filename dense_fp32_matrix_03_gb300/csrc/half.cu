@@ -74,7 +74,7 @@ int half_slots(int num_sms)
 template <bool BF16>
 int launch_half(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB, int slots)
 {
-    return launch_ss<tcs::KindHalf<BF16>>(plan, tmA, tmB, slots);
+    return launch_ss<tcs::KindHalf<BF16>>(plan, tmA, tmB, tmA, tmB, 0, 0, slots);
 }
 
 bool valid_type(int type) { return type == SGEMM_HALF_BF16 || type == SGEMM_HALF_FP16; }

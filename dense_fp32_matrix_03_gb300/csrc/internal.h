@@ -110,6 +110,28 @@ size_t planes_bytes(int mode, long long M, long long N, long long K, int QA, int
 // force: take the route whenever the planes fit (kRouteTcPlanes), without
 // asking planes_pay.
 int run_planes(Plan &plan, bool &taken, bool force = false);
+// The tensor-core paths' raw route (raw.cu): both operands straight from
+// the caller's matrices by TMA, K-major or M/N-major as stored; TF32 with no
+// pass, 3xTF32 with a pass that writes the operands' lo planes into the
+// workspace (the raw values are the hi planes).  Enqueues and sets taken
+// when the operands allow it (and the workspace holds the lo planes) and
+// either force is set or raw_pay says the route is expected to be fastest.
+int run_raw(Plan &plan, bool &taken, bool force = false);
+// Whether the raw route is expected to beat both the pair kernel and the
+// planes route: the split planner's time of each route's tiles, plus, for
+// 3xTF32, the raw route's lo pass ((QA * M + QB * N) * K * 8 bytes at 6.0
+// TB/s and 7 us) and the planes route's pass (12 bytes per operand value for
+// 3xTF32, 8 for TF32, at 6.0 TB/s, and 7 us); lines = false (some operand row
+// off a 128-byte boundary) makes the raw product 7% (3xTF32) or 27% (TF32)
+// slower, as measured on GB300 at a 4092-float pitch.
+bool raw_pay(int mode, long long M, long long N, long long K, int QA, int QB, int Q,
+             int num_sms, bool lines = true);
+// Workspace the raw route's lo planes take (3xTF32; 0 for TF32), for either
+// layout of each operand (the larger of rows x round_up(K, 32) and
+// K x round_up(rows, 32) values per stored entry).
+size_t raw_lo_bytes_max(int mode, long long M, long long N, long long K, int QA, int QB);
+// CTA pairs of the shared-memory-operand kernel that fit at once (cached).
+int ss_slots(int num_sms);
 // Whether the planes route is expected to beat the pair kernel for this
 // shape (QA, QB: stored batch entries of A and B; num_sms 0: unknown, then
 // false).  Each route's product takes the split planner's modelled time for
@@ -157,10 +179,21 @@ SplitPlan one_wave_plan(int mode, int M, int N, int K, int Q);
 //  kin  : contiguous dimension is K (rows are `rows` long runs of K values)
 //  rows : extent of the non-K dimension (M for A, N for B)
 //  box_rows : tile extent along that dimension
+// promote256: L2 fills of 256 bytes (else 128) -- measured on GB300, 256
+// suits rows on 128-byte boundaries, 128 rows that are not (TF32 from a
+// 4092-float pitch: 648 -> 725 TFLOP/s; a 4096-float pitch: equal).
 // Returns false if the driver rejects the description (the caller then uses
 // the cp.async producer).
 bool encode_operand(CUtensorMap *map, const float *base, bool kin, long long rows, long long K,
-                    long long ld, int Q, long long stride, int box_rows);
+                    long long ld, int Q, long long stride, int box_rows,
+                    bool promote256 = true);
+
+// Tensor map of an operand stored K x rows (rows-inner: A stored K x M, B
+// stored K x N) for M/N-major staging: boxes of 32 rows-inner values by 32 k
+// with the 128-byte swizzle of 32-byte atoms (dims rows, K, entries), the
+// layout kind::tf32 reads M/N-major.
+bool encode_operand_mn(CUtensorMap *map, const float *base, long long rows, long long K,
+                       long long ld, int Q, long long stride, bool promote256 = true);
 
 // Tensor map of a K-inner 16-bit operand (bf16 or fp16): boxes of 64 k by
 // box_rows rows with the 128-byte swizzle.
@@ -205,8 +238,11 @@ int launch_peak_probe(int kind, long long iters, int num_sms, unsigned int *stat
 //   kRouteTcPlanes   tensor cores on the planes route whenever the
 //                    workspace holds the planes.
 // A route the call's mode or operands cannot take falls back to kRouteAuto.
+//   kRouteTcRaw      tensor cores on the caller's matrices as stored (raw.cu)
+//                    whenever both operands are TMA-describable (and, for
+//                    3xTF32, the workspace holds the lo planes).
 enum Route { kRouteAuto = 0, kRouteSimtSmall = 1, kRouteTcPair = 2, kRouteTcDirect = 3,
-             kRouteTcPlanes = 4, kRouteCount = 5 };
+             kRouteTcPlanes = 4, kRouteTcRaw = 5, kRouteCount = 6 };
 // Size class of a call: round(log2(M * N * K * Q) / 3), clamped to
 // [kClassMin, kClassMax] -- the log2 of the edge of a cube of the same work
 // (4092^3: 12; the batched 32 x 1024 x 1024 x 512 workload: 11).

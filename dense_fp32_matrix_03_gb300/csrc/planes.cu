@@ -189,6 +189,8 @@ int launch_planes_pass(const PassOperand &a, const PassOperand &b, int K, long l
     return SGEMM_OK;
 }
 
+}  // namespace
+
 int ss_slots(int num_sms)
 {
     int dev = 0;
@@ -212,8 +214,6 @@ int ss_slots(int num_sms)
     g_ss_slots[dev].store(n);
     return n;
 }
-
-}  // namespace
 
 bool planes_pay(int mode, long long M, long long N, long long K, int QA, int QB, int Q,
                 int num_sms)
@@ -281,8 +281,9 @@ static int product_on_planes(Plan &plan, const float *pa, const float *pb, int Q
     const int slots = ss_slots(plan.num_sms);
     const int rc = plan_splits(plan, tcs::PM, tcs::BN, kFeedPlanes, slots);
     if (rc != SGEMM_OK) return rc;
-    return planes == 2 ? launch_ss<tcs::KindTF32<2>>(plan, tmA, tmB, slots)
-                       : launch_ss<tcs::KindTF32<1>>(plan, tmA, tmB, slots);
+    // lo planes: the same maps, entries QA / QB further on
+    return planes == 2 ? launch_ss<tcs::KindTF32<2>>(plan, tmA, tmB, tmA, tmB, QA, QB, slots)
+                       : launch_ss<tcs::KindTF32<1>>(plan, tmA, tmB, tmA, tmB, 0, 0, slots);
 }
 
 int run_planes(Plan &plan, bool &taken, bool force)

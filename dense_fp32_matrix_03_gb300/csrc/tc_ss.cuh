@@ -12,7 +12,14 @@
 //   - fp32 operands already in TF32 form (kind::tf32), made by a pass over
 //     the operands into the caller's workspace: one plane rounded to the
 //     nearest TF32 value (TF32), or the hi and lo planes of the 3xTF32 split,
-//     multiplied as lo*hi + hi*lo + hi*hi (3xTF32).
+//     multiplied as lo*hi + hi*lo + hi*hi (3xTF32);
+//   - the caller's fp32 matrices themselves (kind::tf32 reads the 19 high
+//     bits of each 32-bit value and ignores the 13 low mantissa bits): the
+//     single pass of TF32, or the hi planes of 3xTF32 beside lo planes that
+//     a pass wrote in the operands' own layout.  An operand whose rows run
+//     along M or N (A stored K x M, B stored K x N) is staged M/N-major: TMA
+//     boxes of 32 rows-inner values by 32 k in the 128-byte swizzle with
+//     32-byte atoms, read by the MMA through an M/N-major descriptor.
 //
 // Tile 256 x 256 per CTA pair (cta_group::2, M = 256, N = 256): each CTA
 // stages its 128 rows of A and its 128 of the tile's 256 rows of B^T.  A
@@ -73,19 +80,23 @@ static_assert(2 * BN <= static_cast<int>(kTmemCols), "TMEM columns");
 // KSUB: boxes of each plane per stage.  Instruction descriptor: fp32
 // accumulate, both operands K-major, M = 256 (two CTAs), N = 256; operand
 // format bf16 = 1, fp16 = 0 (kind::f16), tf32 = 2 (kind::tf32).
+// A_MN / B_MN: the operand is staged M/N-major (its stored rows run along
+// M or N), otherwise K-major.
 template <bool BF16>
 struct KindHalf {
     static constexpr bool TF32 = false;
     static constexpr int ELEM = 2, BOX_K = 64, UK = 16, PLANES = 1, KSUB = 2, STAGES = 3;
     static constexpr uint32_t FMT = BF16 ? 1u : 0u;
+    static constexpr bool A_MN = false, B_MN = false;
 };
-template <int PLANES_>
+template <int PLANES_, bool A_MN_ = false, bool B_MN_ = false>
 struct KindTF32 {
     static constexpr bool TF32 = true;
     static constexpr int ELEM = 4, BOX_K = 32, UK = 8, PLANES = PLANES_;
     static constexpr int KSUB = PLANES_ == 1 ? SG_TCS_TF32_KSUB : 1;
     static constexpr int STAGES = PLANES_ == 1 ? SG_TCS_TF32_STAGES : 3;
     static constexpr uint32_t FMT = 2u;
+    static constexpr bool A_MN = A_MN_, B_MN = B_MN_;
 };
 
 template <class KD>
@@ -96,9 +107,15 @@ struct Shape {
     static constexpr int BOXES = KD::KSUB * KD::PLANES;  // per operand per stage
     static constexpr int STAGE_BYTES = BOXES * (SUB_A + SUB_B);  // per CTA
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + NBAR * 8 + 16 + 1024;
+    // bits 15 / 16: A / B M/N-major ("transposed") instead of K-major
     static constexpr uint32_t IDESC = (1u << 4) | (KD::FMT << 7) | (KD::FMT << 10) |
+                                      (KD::A_MN ? 1u << 15 : 0u) | (KD::B_MN ? 1u << 16 : 0u) |
                                       (static_cast<uint32_t>(BN >> 3) << 17) |
                                       (static_cast<uint32_t>(PM >> 4) << 24);
+    // descriptor address step (16-byte units) per MMA's k: K-major rows
+    // advance by the MMA's 32 bytes of k; M/N-major boxes by eight 128-byte
+    // k rows (one swizzle atom)
+    static constexpr uint64_t A_KSTEP = KD::A_MN ? 64 : 2, B_KSTEP = KD::B_MN ? 64 : 2;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -112,6 +129,39 @@ __device__ __forceinline__ void tma_load_pair(void *smem_dst, const CUtensorMap 
         ".cta_group::2 [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
+}
+
+// Shared-memory descriptor of an M/N-major TF32 operand staged as TMA boxes
+// of 32 M/N values (one 128-byte row per k) by 32 k rows, in the 128-byte
+// swizzle with 32-byte atoms (TMA's SWIZZLE_128B_ATOM_32B; descriptor
+// swizzle mode 1), the M/N-major layout kind::tf32 reads: groups of four k
+// rows (512 bytes) are the stride byte offset apart, and consecutive 32-value
+// runs of M/N one 4096-byte box apart (leading byte offset).
+__device__ __forceinline__ uint64_t mnmajor_sw128a32_desc(uint32_t smem_addr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);  // start address
+    d |= static_cast<uint64_t>(4096 >> 4) << 16;                // leading byte offset
+    d |= static_cast<uint64_t>(512 >> 4) << 32;                 // stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;                        // descriptor version
+    d |= static_cast<uint64_t>(1) << 61;                        // 128-byte swizzle, 32-byte atoms
+    return d;
+}
+
+// One operand's box of a stage (ROWS rows of M or N by one box of k) into
+// this CTA's shared memory: K-major, one TMA load (coordinates k, row,
+// entry); M/N-major, ROWS / 32 loads of 32 rows-inner values by 32 k
+// (coordinates row, k, entry), 4096 bytes apart.
+template <bool MN, int ROWS>
+__device__ __forceinline__ void load_box(uint8_t *dst, const CUtensorMap *m, uint32_t bar, int k0,
+                                         int r0, int z)
+{
+    if constexpr (MN) {
+#pragma unroll
+        for (int c = 0; c < ROWS / 32; ++c) tma_load_pair(dst + c * 4096, m, bar, r0 + 32 * c, k0, z);
+    } else {
+        tma_load_pair(dst, m, bar, k0, r0, z);
+    }
 }
 
 __device__ __forceinline__ uint32_t cluster_addr(const void *p, uint32_t rank)
@@ -157,7 +207,7 @@ __device__ __forceinline__ uint32_t issue_stage_ss(uint32_t d, uint64_t a0, uint
         const uint64_t b = b0 + static_cast<uint64_t>(j * KD::PLANES) * BB;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ah = a + 2 * kk, bh = b + 2 * kk;
+            const uint64_t ah = a + Shape<KD>::A_KSTEP * kk, bh = b + Shape<KD>::B_KSTEP * kk;
             const uint32_t acc = (j == 0 && kk == 0) ? acc0 : 1u;
             if (KD::PLANES == 2) {
                 mma_ss<KD>(d, ah + AB, bh, acc);  // lo * hi
@@ -179,10 +229,16 @@ __device__ __forceinline__ uint32_t issue_stage_ss(uint32_t d, uint64_t a0, uint
     return ready;
 }
 
+// tmA / tmB: the operands (their hi planes for 3xTF32); tmA_lo / tmB_lo:
+// the lo planes, at batch coordinate entry + a_lo_z / b_lo_z (the same map
+// with the plane's offset when one map holds both planes).
 template <class KD>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tcs_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                    const __grid_constant__ CUtensorMap tmB, const GemmParams p)
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmA_lo,
+                    const __grid_constant__ CUtensorMap tmB_lo, const GemmParams p, int a_lo_z,
+                    int b_lo_z)
 {
     using S = Shape<KD>;
     constexpr int STAGE_BYTES = S::STAGE_BYTES;
@@ -228,6 +284,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
+            if (KD::PLANES == 2) {
+                tma_prefetch_desc(&tmA_lo);
+                tma_prefetch_desc(&tmB_lo);
+            }
             // Launched as a programmatic dependent (launch_ss): the set-up
             // above overlapped the previous kernel's tail; its writes (the
             // operands' planes or copies) are visible after this wait.  Every
@@ -242,8 +302,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int m0 = wu.tc.tm * PM + static_cast<int>(rank) * BM;
                 const int n0 = wu.tc.tn * BN + static_cast<int>(rank) * HN;
                 const int qa = wu.tc.q * p.a_q_step, qb = wu.tc.q * p.b_q_step;
-                // plane pl of an operand is batch entries pl * za .. (za per plane)
-                const int za = p.a_q_step ? p.Q : 1, zb = p.b_q_step ? p.Q : 1;
                 for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
                     if (!wait_cl(&empty[rr.s], rr.ph ^ 1u, ab, kStatusWaitEmpty)) {
                         ok = false;
@@ -259,8 +317,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int pl = 0; pl < KD::PLANES; ++pl) {
                             const int x = j * KD::PLANES + pl;
-                            tma_load_pair(sa + x * SUB_A, &tmA, fb, k0, m0, qa + pl * za);
-                            tma_load_pair(sb + x * SUB_B, &tmB, fb, k0, n0, qb + pl * zb);
+                            load_box<KD::A_MN, BM>(sa + x * SUB_A, pl ? &tmA_lo : &tmA, fb, k0, m0,
+                                                   qa + (pl ? a_lo_z : 0));
+                            load_box<KD::B_MN, HN>(sb + x * SUB_B, pl ? &tmB_lo : &tmB, fb, k0, n0,
+                                                   qb + (pl ? b_lo_z : 0));
                         }
                     }
                     ++issued;
@@ -290,8 +350,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc::Ring<2> acc;
             bool ok = true;
             bool any = false;
-            const uint64_t adesc0 = tc::kmajor_sw128_desc(smem_u32(base));
-            const uint64_t bdesc0 = tc::kmajor_sw128_desc(smem_u32(base + S::BOXES * SUB_A));
+            const uint32_t sa0 = smem_u32(base), sb0 = smem_u32(base + S::BOXES * SUB_A);
+            const uint64_t adesc0 =
+                KD::A_MN ? mnmajor_sw128a32_desc(sa0) : tc::kmajor_sw128_desc(sa0);
+            const uint64_t bdesc0 =
+                KD::B_MN ? mnmajor_sw128a32_desc(sb0) : tc::kmajor_sw128_desc(sb0);
             for (long long u = cid; ok && u < p.num_units; u += ncl) {
                 const WorkUnit wu = work_unit(u, p);
                 if (!wait_cl(&acc_empty[acc.s], acc.ph ^ 1u, ab, kStatusWaitAcc)) {
@@ -338,6 +401,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const WorkUnit wu = work_unit(u, p);
             const OutTile o = out_tile<PM, BN>(p, wu);
             tc::prefetch_c_rows(o, r0, lane);
+            // C of the first chunk is loaded while the accumulator is made;
+            // then each chunk's C is loaded before the previous chunk is
+            // stored (two chunks of loads per lane in flight)
+            float4 ca[8], cb[8];
+            tc::load_c_chunk(o, r0, 0, ca, lane);
             int w = 1;
             if (lane == 0) w = wait_cl(&acc_full[acc.s], acc.ph, ab, kStatusWaitAcc, true);
             if (!__shfl_sync(0xffffffffu, w, 0)) break;
@@ -346,10 +414,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t tbase =
                 tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc.s * BN);
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
+            for (int c0 = 0; c0 < BN; c0 += 64) {
                 float v[32];
+                tc::load_c_chunk(o, r0, c0 + 32, cb, lane);
                 tc::tmem_ld32(tbase + c0, v);
-                tc::store_chunk_staged(o, r0, c0, v, stage, lane);
+                tc::store_chunk_pre(o, r0, c0, v, ca, stage, lane);
+                if (c0 + 64 < BN) tc::load_c_chunk(o, r0, c0 + 64, ca, lane);
+                tc::tmem_ld32(tbase + c0 + 32, v);
+                tc::store_chunk_pre(o, r0, c0 + 32, v, cb, stage, lane);
             }
             tc::tc_fence_before();
             __syncwarp();
@@ -373,8 +445,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // Host side: launches the kernel for `plan` (at most `slots` CTA pairs, each
 // looping over work units) and, when the plan splits tiles along K, the
 // fix-up kernel after it.
+// tmA_lo / tmB_lo and a_lo_z / b_lo_z: the lo planes' maps and batch
+// offsets (3xTF32; ignored otherwise).
 template <class KD>
-int launch_ss(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB, int slots)
+int launch_ss(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB,
+              const CUtensorMap &tmA_lo, const CUtensorMap &tmB_lo, int a_lo_z, int b_lo_z,
+              int slots)
 {
     auto kern = tcs::tcs_gemm_kernel<KD>;
     constexpr int smem = tcs::Shape<KD>::SMEM_BYTES;
@@ -393,7 +469,9 @@ int launch_ss(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB, int sl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, plan.p) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmA_lo, tmB_lo, plan.p, a_lo_z, b_lo_z) !=
+        cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
     note_launch();
     return plan.p.splits > 1 ? launch_fixup(plan, tcs::PM, tcs::BN) : SGEMM_OK;
 }

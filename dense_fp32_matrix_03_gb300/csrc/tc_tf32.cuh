@@ -460,5 +460,76 @@ __device__ __forceinline__ void store_chunk_staged(const OutTile &o, int r0, int
     __syncwarp();  // the next chunk reuses the buffer
 }
 
+// The staged epilogue in two halves, so that the loads of C can run ahead:
+// load_c_chunk issues the loads of the C values a lane combines for chunk
+// [c0, c0 + 32) of rows [r0, r0 + 32) (slot i = 0..7: row r0 + 4 i + l / 8,
+// columns c0 + 4 (l % 8) .. + 3, as in store_chunk_staged; zeros outside the
+// tile's valid extent, nothing when beta == 0), and store_chunk_pre writes
+// out = alpha * v + beta * old for that chunk.  A caller loads chunk j + 1's
+// C before it stores chunk j: eight 16-byte loads per lane stay in flight
+// behind the transpose and the stores (store_chunk_staged has four).
+__device__ __forceinline__ void load_c_chunk(const OutTile &o, int r0, int c0, float4 (&old)[8],
+                                             int lane)
+{
+    const int col = c0 + 4 * (lane & 7);
+    const bool full = o.vec4 && col + 4 <= o.cols;
+    const int rl = r0 + (lane >> 3);
+    const float *row = o.base + static_cast<long long>(rl) * o.ld + col;
+    const long long step = 4 * o.ld;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        old[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (o.beta == 0.f || rl + 4 * i >= o.rows || col >= o.cols) continue;
+        const float *src = row + i * step;
+        if (full) {
+            old[i] = *reinterpret_cast<const float4 *>(src);
+        } else {
+            old[i].x = src[0];
+            if (col + 1 < o.cols) old[i].y = src[1];
+            if (col + 2 < o.cols) old[i].z = src[2];
+            if (col + 3 < o.cols) old[i].w = src[3];
+        }
+    }
+}
+
+__device__ __forceinline__ void store_chunk_pre(const OutTile &o, int r0, int c0,
+                                                const float (&v)[32], const float4 (&old)[8],
+                                                float4 *stage, int lane)
+{
+    float4 *mine = stage + lane * 8;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        mine[j ^ (lane & 7)] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    __syncwarp();
+    const int g = lane & 7, col = c0 + 4 * g;
+    const bool full = o.vec4 && col + 4 <= o.cols;
+    const int rl = r0 + (lane >> 3);
+    float *row = o.base + static_cast<long long>(rl) * o.ld + col;
+    const long long step = 4 * o.ld;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int rr = 4 * i + (lane >> 3);
+        const float4 a = stage[rr * 8 + (g ^ (rr & 7))];
+        if (rl + 4 * i >= o.rows || col >= o.cols) continue;
+        float4 x = make_float4(o.alpha * a.x, o.alpha * a.y, o.alpha * a.z, o.alpha * a.w);
+        if (o.beta != 0.f) {
+            x.x = fmaf(o.beta, old[i].x, x.x);
+            x.y = fmaf(o.beta, old[i].y, x.y);
+            x.z = fmaf(o.beta, old[i].z, x.z);
+            x.w = fmaf(o.beta, old[i].w, x.w);
+        }
+        float *dst = row + i * step;
+        if (full) {
+            *reinterpret_cast<float4 *>(dst) = x;
+        } else {
+            dst[0] = x.x;
+            if (col + 1 < o.cols) dst[1] = x.y;
+            if (col + 2 < o.cols) dst[2] = x.z;
+            if (col + 3 < o.cols) dst[3] = x.w;
+        }
+    }
+    __syncwarp();  // the next chunk reuses the buffer
+}
+
 }  // namespace tc
 }  // namespace sg

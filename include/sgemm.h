@@ -288,14 +288,22 @@ int sgemm_peak_probe(int kind, long long iters, double *flops, void *stream);
  * being round(log2(M * N * K * Q) / 3) clamped to 7..13; a class without
  * an entry follows the library's cost models.  The families ("routes"):
  *   0  AUTO     the cost models (the FP32 tile that suits the layout; on the
- *               tensor cores the TF32-planes route where its time model says
- *               it pays and the workspace holds the planes, else the CTA-pair
- *               kernel for TMA-describable operands, else the direct kernel)
+ *               tensor cores the raw route where its time model says it pays
+ *               and both operands are TMA-describable (3xTF32: and the
+ *               workspace holds their lo planes), else the TF32-planes route
+ *               where it pays and the workspace holds the planes, else the
+ *               CTA-pair kernel for TMA-describable operands, else the direct
+ *               kernel)
  *   1  SMALL    FP32 on 64 x 64 tiles
  *   2  PAIR     tensor cores on the CTA-pair kernel, no planes
  *   3  DIRECT   tensor cores on the direct-load kernel
  *   4  PLANES   tensor cores on the planes route whenever the workspace holds
  *               the planes (sgemm_workspace_size then counts them)
+ *   5  RAW      tensor cores on the caller's matrices as stored, whenever
+ *               both operands are TMA-describable (16-byte aligned base,
+ *               leading dimension and batch stride multiples of 4 values);
+ *               3xTF32 also needs the workspace to hold the operands' lo
+ *               planes (sgemm_workspace_size then counts them)
  * A route the call's mode cannot take means AUTO; every route computes the
  * same result within the mode's accuracy bound.
  * sgemm_tune_force(route) makes every later call in the process take that
@@ -308,6 +316,7 @@ int sgemm_peak_probe(int kind, long long iters, double *flops, void *stream);
 #define SGEMM_ROUTE_PAIR 2
 #define SGEMM_ROUTE_DIRECT 3
 #define SGEMM_ROUTE_PLANES 4
+#define SGEMM_ROUTE_RAW 5
 int sgemm_tune_force(int route);
 int sgemm_tune_route(int mode, int M, int N, int K, int Q);
 

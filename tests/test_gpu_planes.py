@@ -6,7 +6,11 @@ kernel.  Every layout, padded and unaligned operands, ragged M/N/K, batches
 with a broadcast operand, integer data bit for bit; sampled rows against the
 oracle.  The workspace shows the route was taken: it starts with op(A)'s
 first plane, row 0 of which the test recomputes from the definition (hi:
-the 13 low mantissa bits cleared; TF32: rounded to nearest, ties away)."""
+the 13 low mantissa bits cleared; TF32: rounded to nearest, ties away).
+
+Operands TMA can describe take the raw route under the cost models
+(test_gpu_raw.py), so these tests force the planes route; unaligned
+operands, which the raw route cannot take, reach it under the cost models."""
 import numpy as np
 import pytest
 
@@ -25,6 +29,16 @@ def gpu_ready():
         pytest.skip("no CUDA device")
     import dense_fp32_matrix_03_gb300 as lib
     lib.load()
+    yield
+    lib.sgemm_tune_force("auto")
+
+
+@pytest.fixture
+def planes_forced():
+    import dense_fp32_matrix_03_gb300 as lib
+    assert lib.sgemm_tune_force("planes") == lib.SGEMM_OK
+    yield
+    lib.sgemm_tune_force("auto")
 
 
 def first_plane_row(a_row, mode):
@@ -65,7 +79,7 @@ def check(prob, mode, oracle_mod, rows, exact=False, opA0=None):
 
 @pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("mode", MODES)
-def test_planes_route_every_layout(oracle_mod, mode, tA, tB):
+def test_planes_route_every_layout(oracle_mod, planes_forced, mode, tA, tB):
     """3100 x 3000 x 2333: ragged tiles in M and N, K not a multiple of the
     32-wide box; padded leading dimensions, beta != 0."""
     A, B, C0 = workloads.random_inputs(3100, 3000, 2333, seed=61 + 2 * tA + tB)
@@ -76,7 +90,9 @@ def test_planes_route_every_layout(oracle_mod, mode, tA, tB):
 @pytest.mark.parametrize("mode", MODES)
 def test_planes_route_unaligned_operands(oracle_mod, mode):
     """Odd leading dimensions and bases off 16 bytes: the pass reads them
-    value by value; the planes are aligned whatever the source."""
+    value by value; the planes are aligned whatever the source.  Under the
+    cost models: TMA cannot describe these operands, so the raw route does
+    not apply."""
     A, B, C0 = workloads.random_inputs(3100, 3000, 2333, seed=67)
     for tA, tB in ((0, 0), (1, 1)):
         prob = Problem(A, B, C0, 1.0, 0.5, tA, tB, pads=(1, 3, 1), offsets=(1, 3, 2))
@@ -84,7 +100,7 @@ def test_planes_route_unaligned_operands(oracle_mod, mode):
 
 
 @pytest.mark.parametrize("mode", MODES)
-def test_planes_route_batched_broadcast(oracle_mod, mode):
+def test_planes_route_batched_broadcast(oracle_mod, planes_forced, mode):
     """Q = 3 with A broadcast (stride 0): A's planes hold one entry, B's
     three; batch entries and planes share the tensor map's third dimension."""
     Q = 3
@@ -94,7 +110,7 @@ def test_planes_route_batched_broadcast(oracle_mod, mode):
 
 
 @pytest.mark.parametrize("mode", MODES)
-def test_planes_route_integer_bit_exact(oracle_mod, mode):
+def test_planes_route_integer_bit_exact(oracle_mod, planes_forced, mode):
     """Small integers: every plane, product and partial sum is exact, so the
     result equals the oracle's bit for bit (the last wave's tiles are also
     split along K)."""
@@ -106,7 +122,7 @@ def test_planes_route_integer_bit_exact(oracle_mod, mode):
 
 
 @pytest.mark.parametrize("mode", MODES)
-def test_planes_route_small_workspace_falls_back(oracle_mod, mode):
+def test_planes_route_small_workspace_falls_back(oracle_mod, planes_forced, mode):
     """A workspace too small for the planes: the pair kernel runs instead,
     with the same results within tolerance."""
     import dense_fp32_matrix_03_gb300 as lib
@@ -122,7 +138,7 @@ def test_planes_route_small_workspace_falls_back(oracle_mod, mode):
 
 
 @pytest.mark.parametrize("mode", MODES)
-def test_planes_route_long_k(oracle_mod, mode):
+def test_planes_route_long_k(oracle_mod, planes_forced, mode):
     """2900 x 3000 x 12001: hundreds of k-blocks, K odd (the pass zero-fills
     the last group of four, TMA the rest of the last box), the last wave's
     tiles split along K into many slices; B stored transposed."""

@@ -124,7 +124,9 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
     round_up(K, 32) values).  The route table (tune_table.h) adds the FP32
     64 x 64 tile where it sends the shape to it, and decides the planes on
     the tensor paths: always with route PLANES, never with PAIR or DIRECT,
-    by the time model with AUTO."""
+    by the time model with AUTO.  The raw route's lo planes (3xTF32) are
+    counted where it pays (always with route RAW, by its time model with
+    AUTO): rows of round_up(inner, 32) values, for either layout."""
     rates = {("fp32", "direct"): 0.24e12, ("fp32", "tma"): 0.40e12,
              ("3xtf32", "direct"): 0.47e12, ("3xtf32", "pair"): 1.8e12,
              ("tf32", "direct"): 0.55e12, ("tf32", "pair"): 3.6e12,
@@ -186,6 +188,18 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
         t_pair = plan(*kernels[1])[1]
         t_planes = plan(*kernels[2])[1] + (M + N) * K * Q * 4.0 * (1 + planes) / 6.0e12 + 7e-6
         room = copy(M) + copy(N)
+        # the raw route where it pays: the modelled time of its tiles' plan
+        # (the planes route's tiles) plus, for 3xTF32, its lo pass ((M + N) *
+        # K * Q * 8 bytes at 6.0 TB/s) and 7 us; room for the lo planes of
+        # either layout (rows of round_up(inner, 32) values)
+        t_raw = plan(*kernels[2])[1]
+        if mode == "3xtf32":
+            t_raw += (M + N) * K * Q * 8.0 / 6.0e12 + 7e-6
+        if route == lib.SGEMM_ROUTE_RAW or (route == lib.SGEMM_ROUTE_AUTO and t_raw < t_pair):
+            if mode == "3xtf32":
+                lo = (r256(Q * max(M * r32(K), K * r32(M)) * 4) +
+                      r256(Q * max(N * r32(K), K * r32(N)) * 4))
+                room = max(room, lo)
         if (route == lib.SGEMM_ROUTE_PLANES or
                 (route == lib.SGEMM_ROUTE_AUTO and t_planes < t_pair)):
             room = max(room, r256(planes * Q * M * r32(K) * 4) + r256(planes * Q * N * r32(K) * 4))
