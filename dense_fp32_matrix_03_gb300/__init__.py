@@ -44,8 +44,10 @@ SGEMM_ROUTE_PAIR = 2
 SGEMM_ROUTE_DIRECT = 3
 SGEMM_ROUTE_PLANES = 4
 SGEMM_ROUTE_RAW = 5
+SGEMM_ROUTE_INLINE = 6
 ROUTES = {"auto": SGEMM_ROUTE_AUTO, "small": SGEMM_ROUTE_SMALL, "pair": SGEMM_ROUTE_PAIR,
-          "direct": SGEMM_ROUTE_DIRECT, "planes": SGEMM_ROUTE_PLANES, "raw": SGEMM_ROUTE_RAW}
+          "direct": SGEMM_ROUTE_DIRECT, "planes": SGEMM_ROUTE_PLANES, "raw": SGEMM_ROUTE_RAW,
+          "inline": SGEMM_ROUTE_INLINE}
 
 SGEMM_MODE_DEFAULT = -1
 SGEMM_MODE_FP32 = 0

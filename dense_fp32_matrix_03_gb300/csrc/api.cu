@@ -319,7 +319,7 @@ int applicable(int mode, int route)
     const bool fp32 = mode == SGEMM_MODE_FP32;
     if (route == kRouteSimtSmall) return fp32 ? route : kRouteAuto;
     if (route == kRouteTcPair || route == kRouteTcDirect || route == kRouteTcPlanes ||
-        route == kRouteTcRaw)
+        route == kRouteTcRaw || route == kRouteTcInline)
         return fp32 ? kRouteAuto : route;
     return kRouteAuto;
 }
@@ -347,7 +347,10 @@ double path_rate_per_sm(int mode, int feed)
 {
     if (mode == SGEMM_MODE_FP32) return feed == kFeedDirect ? 0.24e12 : 0.40e12;
     if (mode == SGEMM_MODE_3XTF32)
-        return feed == kFeedDirect ? 0.47e12 : feed == kFeedPlanes ? 2.45e12 : 1.8e12;
+        return feed == kFeedDirect ? 0.47e12
+               : feed == kFeedPlanes ? 2.45e12
+               : feed == kFeedInline ? 2.35e12
+                                     : 1.8e12;
     if (mode == kModeHalf) return 11.0e12;
     return feed == kFeedDirect ? 0.55e12 : feed == kFeedPlanes ? 6.4e12 : 3.6e12;
 }
@@ -366,7 +369,8 @@ SplitPlan choose_plan(long long num_tiles, int K, int slots, int mode, int bm, i
     const int num_sms = slots;  // units running at once
     const long long full = num_tiles / num_sms, rem = num_tiles % num_sms;
     const double unit_rate =
-        path_rate_per_sm(mode, feed) * ((feed == kFeedPair || feed == kFeedPlanes) ? 2 : 1);
+        path_rate_per_sm(mode, feed) *
+        ((feed == kFeedPair || feed == kFeedPlanes || feed == kFeedInline) ? 2 : 1);
     const double t_tile = 2.0 * bm * bn * static_cast<double>(K) / unit_rate;
     best.seconds = t_tile * static_cast<double>(full + (rem ? 1 : 0));
     if (rem == 0) return best;
@@ -461,10 +465,11 @@ SplitPlan plan_query(int mode, int M, int N, int K, int Q, bool one_wave)
         if (mode == SGEMM_MODE_FP32) {
             if (shape == 2) simt_small_tile_dims(bm, bn);
             else simt_tile_dims(shape == 1, bm, bn);
-        } else if (shape == 2) {  // the planes route's 256 x 256 pair tiles
+        } else if (shape == 2) {  // the planes and raw routes' 256 x 256 pair tiles
             bm = bn = 256;
             slots = tc_pair_slots(sms);
-            feeds[0] = feeds[1] = kFeedPlanes;
+            feeds[0] = kFeedPlanes;
+            feeds[1] = mode == SGEMM_MODE_3XTF32 ? kFeedInline : kFeedPlanes;
         } else {
             tc_tile_dims(mode, K, shape == 1, bm, bn);
             if (shape == 1) {
@@ -720,8 +725,8 @@ int run(int mode, int M, int N, int K, float alpha, const float *A, int lda, con
         return launch_simt(plan, kRouteAuto);
     }
     bool taken = false;
-    if (route == kRouteAuto || route == kRouteTcRaw) {
-        rc = run_raw(plan, taken, route == kRouteTcRaw);
+    if (route == kRouteAuto || route == kRouteTcRaw || route == kRouteTcInline) {
+        rc = run_raw(plan, taken, route != kRouteAuto, route);
         if (taken || rc != SGEMM_OK) return rc;
     }
     if (route == kRouteAuto || route == kRouteTcPlanes) {
@@ -816,16 +821,16 @@ size_t sgemm_workspace_size(int mode, int M, int N, int K, int Q)
     if (mode == SGEMM_MODE_DEFAULT) mode = g_default_mode.load();
     if (M <= 0 || N <= 0 || K <= 0 || Q <= 0) return base;
     if (mode != SGEMM_MODE_3XTF32 && mode != SGEMM_MODE_TF32) return base;
-    // where the raw route (3xTF32: its lo planes) or the planes route pays
-    // for this shape (raw_pay, planes_pay): the planes (every batch entry
-    // stored) and the split plan of their tiles, or the copies and plans of
-    // the other routes, whichever is larger
+    // with route RAW (3xTF32: its lo planes) or where the planes route pays
+    // for this shape (planes_pay; operands TMA cannot describe take it): the
+    // planes (every batch entry stored) and the split plan of their tiles,
+    // or the copies and plans of the other routes, whichever is larger
     const int route = route_for(mode, M, N, K, Q);
-    if (route == kRouteTcPair || route == kRouteTcDirect) return base;
+    if (route == kRouteTcPair || route == kRouteTcDirect || route == kRouteTcInline) return base;
     const int sms = num_sms_or_zero();
     size_t need = base;
     const size_t split = preferred_plan(mode, M, N, K, Q).ws_bytes;
-    if (route == kRouteTcRaw || (route == kRouteAuto && raw_pay(mode, M, N, K, Q, Q, Q, sms))) {
+    if (route == kRouteTcRaw) {  // 3xTF32: the lo pass's planes
         const size_t lo = raw_lo_bytes_max(mode, M, N, K, Q, Q) + split;
         if (lo > need) need = lo;
     }

@@ -68,7 +68,9 @@ constexpr int kMaxSplits = 16;
 // kernel's cp.async producer, the tensor-core direct kernel), by TMA on one
 // CTA per unit, by TMA on a CTA pair per unit (two multiprocessors), or, on
 // a CTA pair, as TF32 planes made by a pass before the product (planes.cu).
-enum Feed { kFeedDirect = 0, kFeedTma = 1, kFeedPair = 2, kFeedPlanes = 3 };
+// kFeedInline: 3xTF32 on a CTA pair from the caller's matrices, the lo
+// planes made in the kernel (raw.cu).
+enum Feed { kFeedDirect = 0, kFeedTma = 1, kFeedPair = 2, kFeedPlanes = 3, kFeedInline = 4 };
 struct SplitPlan {
     int splits;          // 1 = no split
     long long dp_tiles;  // tiles computed whole (they come first in unit order)
@@ -116,16 +118,28 @@ int run_planes(Plan &plan, bool &taken, bool force = false);
 // workspace (the raw values are the hi planes).  Enqueues and sets taken
 // when the operands allow it (and the workspace holds the lo planes) and
 // either force is set or raw_pay says the route is expected to be fastest.
-int run_raw(Plan &plan, bool &taken, bool force = false);
-// Whether the raw route is expected to beat both the pair kernel and the
-// planes route: the split planner's time of each route's tiles, plus, for
-// 3xTF32, the raw route's lo pass ((QA * M + QB * N) * K * 8 bytes at 6.0
-// TB/s and 7 us) and the planes route's pass (12 bytes per operand value for
-// 3xTF32, 8 for TF32, at 6.0 TB/s, and 7 us); lines = false (some operand row
-// off a 128-byte boundary) makes the raw product 7% (3xTF32) or 27% (TF32)
-// slower, as measured on GB300 at a 4092-float pitch.
-bool raw_pay(int mode, long long M, long long N, long long K, int QA, int QB, int Q,
-             int num_sms, bool lines = true);
+// With force, route is the one forced (kRouteTcRaw: 3xTF32 with a lo pass
+// into the workspace; kRouteTcInline: 3xTF32 with the lo planes made in the
+// kernel); without, the cost models' form (raw_choice).
+int run_raw(Plan &plan, bool &taken, bool force = false, int route = 0);
+// The form of the raw route the cost models pick for a call, if any:
+// kRawNone, kRawPlain (TF32 on the raw operands) or kRawInline (3xTF32 with
+// the lo planes made in the kernel) -- when its modelled time beats both the
+// pair kernel's and the planes route's.  Each route's product takes the split
+// planner's time for its tiles; the planes route adds its pass (12 bytes per
+// operand value for 3xTF32, 8 for TF32, at 6.0 TB/s) and 7 us.  lines =
+// false (some operand row off a 128-byte boundary) makes the raw product
+// slower: 6% (3xTF32 inline) or 27% (TF32), as measured on GB300 at a
+// 4092-float pitch against 4096.  (The raw route with a lo pass is taken
+// only when forced: the inline form was faster on every shape measured.)
+enum RawForm { kRawNone = 0, kRawPlain = 1, kRawInline = 2 };
+int raw_choice(int mode, long long M, long long N, long long K, int QA, int QB, int Q,
+               int num_sms, bool lines = true);
+inline bool raw_pay(int mode, long long M, long long N, long long K, int QA, int QB, int Q,
+                    int num_sms, bool lines = true)
+{
+    return raw_choice(mode, M, N, K, QA, QB, Q, num_sms, lines) != kRawNone;
+}
 // Workspace the raw route's lo planes take (3xTF32; 0 for TF32), for either
 // layout of each operand (the larger of rows x round_up(K, 32) and
 // K x round_up(rows, 32) values per stored entry).
@@ -241,8 +255,10 @@ int launch_peak_probe(int kind, long long iters, int num_sms, unsigned int *stat
 //   kRouteTcRaw      tensor cores on the caller's matrices as stored (raw.cu)
 //                    whenever both operands are TMA-describable (and, for
 //                    3xTF32, the workspace holds the lo planes).
+//   kRouteTcInline   the raw route with 3xTF32's lo planes made inside the
+//                    product kernel (TF32: the raw route).
 enum Route { kRouteAuto = 0, kRouteSimtSmall = 1, kRouteTcPair = 2, kRouteTcDirect = 3,
-             kRouteTcPlanes = 4, kRouteTcRaw = 5, kRouteCount = 6 };
+             kRouteTcPlanes = 4, kRouteTcRaw = 5, kRouteTcInline = 6, kRouteCount = 7 };
 // Size class of a call: round(log2(M * N * K * Q) / 3), clamped to
 // [kClassMin, kClassMax] -- the log2 of the edge of a cube of the same work
 // (4092^3: 12; the batched 32 x 1024 x 1024 x 512 workload: 11).

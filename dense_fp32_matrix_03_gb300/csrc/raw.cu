@@ -184,18 +184,20 @@ bool encode_raw(CUtensorMap *map, const float *base, bool mn, long long rows, lo
               : encode_operand(map, base, true, rows, K, ld, E, stride, rows_box, lines);
 }
 
-template <int PLANES>
+// CONV: 3xTF32 with the lo planes made in the kernel (tmAl / tmBl unused).
+template <int PLANES, bool CONV = false>
 int launch_raw_product(Plan &plan, bool a_mn, bool b_mn, const CUtensorMap &tmA,
                        const CUtensorMap &tmB, const CUtensorMap &tmAl, const CUtensorMap &tmBl,
                        int slots)
 {
+    using namespace tcs;
     if (!a_mn && !b_mn)
-        return launch_ss<tcs::KindTF32<PLANES, false, false>>(plan, tmA, tmB, tmAl, tmBl, 0, 0, slots);
+        return launch_ss<KindTF32<PLANES, false, false, CONV>>(plan, tmA, tmB, tmAl, tmBl, 0, 0, slots);
     if (!a_mn && b_mn)
-        return launch_ss<tcs::KindTF32<PLANES, false, true>>(plan, tmA, tmB, tmAl, tmBl, 0, 0, slots);
+        return launch_ss<KindTF32<PLANES, false, true, CONV>>(plan, tmA, tmB, tmAl, tmBl, 0, 0, slots);
     if (a_mn && !b_mn)
-        return launch_ss<tcs::KindTF32<PLANES, true, false>>(plan, tmA, tmB, tmAl, tmBl, 0, 0, slots);
-    return launch_ss<tcs::KindTF32<PLANES, true, true>>(plan, tmA, tmB, tmAl, tmBl, 0, 0, slots);
+        return launch_ss<KindTF32<PLANES, true, false, CONV>>(plan, tmA, tmB, tmAl, tmBl, 0, 0, slots);
+    return launch_ss<KindTF32<PLANES, true, true, CONV>>(plan, tmA, tmB, tmAl, tmBl, 0, 0, slots);
 }
 
 }  // namespace
@@ -208,11 +210,11 @@ size_t raw_lo_bytes_max(int mode, long long M, long long N, long long K, int QA,
     return (a1 > a2 ? a1 : a2) + (b1 > b2 ? b1 : b2);
 }
 
-bool raw_pay(int mode, long long M, long long N, long long K, int QA, int QB, int Q, int num_sms,
-             bool lines)
+int raw_choice(int mode, long long M, long long N, long long K, int QA, int QB, int Q,
+               int num_sms, bool lines)
 {
-    if ((mode != SGEMM_MODE_3XTF32 && mode != SGEMM_MODE_TF32) || num_sms <= 0) return false;
-    if (K > 0x7FFFFFFFLL) return false;
+    if ((mode != SGEMM_MODE_3XTF32 && mode != SGEMM_MODE_TF32) || num_sms <= 0) return kRawNone;
+    if (K > 0x7FFFFFFFLL) return kRawNone;
     const int slots = tc_pair_slots(num_sms);
     const size_t any = ~static_cast<size_t>(0);
     int bm = 0, bn = 0;
@@ -223,39 +225,45 @@ bool raw_pay(int mode, long long M, long long N, long long K, int QA, int QB, in
         choose_plan(pair_tiles, static_cast<int>(K), slots, mode, bm, bn, kFeedPair, any).seconds;
     const long long ss_tiles =
         static_cast<long long>(Q) * ((M + tcs::PM - 1) / tcs::PM) * ((N + tcs::BN - 1) / tcs::BN);
-    const double product =
-        choose_plan(ss_tiles, static_cast<int>(K), slots, mode, tcs::PM, tcs::BN, kFeedPlanes, any)
+    auto product = [&](int feed) {
+        return choose_plan(ss_tiles, static_cast<int>(K), slots, mode, tcs::PM, tcs::BN, feed, any)
             .seconds;
+    };
     const double elems = static_cast<double>(QA * M + QB * N) * K;
     const bool split3 = mode == SGEMM_MODE_3XTF32;
-    // rows off 128-byte boundaries cost the raw product its L2 line
-    // efficiency (GB300, 4092^3 against 4096^3: 3xTF32 ~6%, TF32 ~27% more
-    // product time)
-    const double t_raw = product * (lines ? 1.0 : (split3 ? 1.07 : 1.27)) +
-                         (split3 ? elems * 8.0 / 6.0e12 + 7e-6 : 0.0);
-    const double t_planes = product + elems * 4.0 * (split3 ? 3.0 : 2.0) / 6.0e12 + 7e-6;
-    return t_raw < t_pair && t_raw < t_planes;
+    const double t_planes =
+        product(kFeedPlanes) + elems * 4.0 * (split3 ? 3.0 : 2.0) / 6.0e12 + 7e-6;
+    const double t_raw = split3 ? product(kFeedInline) * (lines ? 1.0 : 1.06)
+                                : product(kFeedPlanes) * (lines ? 1.0 : 1.27);
+    if (t_raw < t_pair && t_raw < t_planes) return split3 ? kRawInline : kRawPlain;
+    return kRawNone;
 }
 
-int run_raw(Plan &plan, bool &taken, bool force)
+int run_raw(Plan &plan, bool &taken, bool force, int route)
 {
     taken = false;
     GemmParams &p = plan.p;
     if (plan.mode != SGEMM_MODE_3XTF32 && plan.mode != SGEMM_MODE_TF32) return SGEMM_OK;
     if (!plan.a_tma || !plan.b_tma) return SGEMM_OK;
     const int planes = plan.mode == SGEMM_MODE_3XTF32 ? 2 : 1;
-    if (planes == 2 && plan.ws == nullptr) return SGEMM_OK;
     const int QA = (p.Q > 1 && p.sA != 0) ? p.Q : 1, QB = (p.Q > 1 && p.sB != 0) ? p.Q : 1;
+    if (!force) {
+        const bool lines =
+            rows_on_lines(p.A, p.lda, QA, p.sA) && rows_on_lines(p.B, p.ldb, QB, p.sB);
+        if (raw_choice(plan.mode, p.M, p.N, p.K, QA, QB, p.Q, plan.num_sms, lines) == kRawNone)
+            return SGEMM_OK;
+    }
+    // 3xTF32: lo planes from a pass into the workspace (forced RAW) or made
+    // in the product kernel (INLINE, and the cost models' choice)
+    const bool inline_lo = planes == 2 && (!force || route == kRouteTcInline);
+    const bool lo_pass = planes == 2 && !inline_lo;
+    if (lo_pass && plan.ws == nullptr) return SGEMM_OK;
     const bool a_mn = plan.transA != 0, b_mn = plan.transB == 0;
     const Stored sa = stored_a(plan), sb = stored_b(plan);
-    const size_t a_lo = planes == 2 ? lo_bytes(sa, QA) : 0;
-    const size_t need = planes == 2 ? a_lo + lo_bytes(sb, QB) : 0;
+    const size_t a_lo = lo_pass ? lo_bytes(sa, QA) : 0;
+    const size_t need = lo_pass ? a_lo + lo_bytes(sb, QB) : 0;
     if (need > plan.ws_bytes) return SGEMM_OK;
     if (sa.outer > 0x7FFFFFFFLL || sb.outer > 0x7FFFFFFFLL) return SGEMM_OK;
-    if (!force && !raw_pay(plan.mode, p.M, p.N, p.K, QA, QB, p.Q, plan.num_sms,
-                           rows_on_lines(p.A, p.lda, QA, p.sA) &&
-                               rows_on_lines(p.B, p.ldb, QB, p.sB)))
-        return SGEMM_OK;
 
     alignas(64) CUtensorMap tmA, tmB, tmAl, tmBl;
     std::memset(&tmA, 0, sizeof(tmA));
@@ -267,7 +275,7 @@ int run_raw(Plan &plan, bool &taken, bool force)
         return SGEMM_OK;
     char *w = static_cast<char *>(plan.ws);
     float *la = nullptr, *lb = nullptr;
-    if (planes == 2) {
+    if (lo_pass) {
         la = reinterpret_cast<float *>(w);
         lb = reinterpret_cast<float *>(w + a_lo);
         const long long lda_l = round32(sa.inner), ldb_l = round32(sb.inner);
@@ -280,7 +288,7 @@ int run_raw(Plan &plan, bool &taken, bool force)
     }
     taken = true;
 
-    if (planes == 2) {
+    if (lo_pass) {
         const LoOperand oa = lo_operand(p.A, p.lda, p.sA, sa, QA, la);
         const LoOperand ob = lo_operand(p.B, p.ldb, p.sB, sb, QB, lb);
         const int rc = launch_lo_pass(oa, ob, plan.num_sms, plan.stream);
@@ -300,10 +308,11 @@ int run_raw(Plan &plan, bool &taken, bool force)
     p.tiles_n = (p.N + tcs::BN - 1) / tcs::BN;
     p.num_tiles = static_cast<long long>(p.Q) * p.tiles_m * p.tiles_n;
     const int slots = ss_slots(plan.num_sms);
-    const int rc = plan_splits(plan, tcs::PM, tcs::BN, kFeedPlanes, slots);
+    const int rc = plan_splits(plan, tcs::PM, tcs::BN, inline_lo ? kFeedInline : kFeedPlanes, slots);
     if (rc != SGEMM_OK) return rc;
-    return planes == 2 ? launch_raw_product<2>(plan, a_mn, b_mn, tmA, tmB, tmAl, tmBl, slots)
-                       : launch_raw_product<1>(plan, a_mn, b_mn, tmA, tmB, tmAl, tmBl, slots);
+    if (planes == 1) return launch_raw_product<1>(plan, a_mn, b_mn, tmA, tmB, tmAl, tmBl, slots);
+    return inline_lo ? launch_raw_product<2, true>(plan, a_mn, b_mn, tmA, tmB, tmAl, tmBl, slots)
+                     : launch_raw_product<2>(plan, a_mn, b_mn, tmA, tmB, tmAl, tmBl, slots);
 }
 
 }  // namespace sg

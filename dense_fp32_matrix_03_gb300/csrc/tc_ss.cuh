@@ -35,6 +35,16 @@
 // Warps: 0 TMA producer, 1 TMEM allocator + MMA issuer (even CTA), 2-5
 // epilogue (warp w reads TMEM lanes 32 * (w % 4) .. +31).  Every wait is
 // bounded; the CTAs meet at a cluster barrier before freeing TMEM.
+//
+// In-kernel lo planes (3xTF32 on the caller's matrices, KindTF32 with CONV):
+// TMA stages only the raw boxes (the hi planes), each CTA's loads completing
+// on its own barrier; SG_TCS_CONV_WARPS converter warps per CTA (from 6) then write each
+// stage's lo boxes from its raw boxes, value by value at the same offsets
+// (the swizzle is a function of the offset, so the lo box has the raw box's
+// layout), make them visible to the tensor core (fence.proxy.async) and
+// arrive on the even CTA's conv barrier, which the MMA issuer waits on in
+// place of the load barrier.  No pass over the operands and no workspace
+// for planes.
 #pragma once
 
 #include "../../include/sgemm.h"
@@ -71,6 +81,11 @@ constexpr int SUB_B = HN * 128;  // one box of B: 16 KB
 #endif
 constexpr int kEpiWarp0 = 2;
 constexpr int kThreads = (kEpiWarp0 + 4) * 32;
+constexpr int kConvWarp0 = kEpiWarp0 + 4;  // in-kernel lo planes: converter warps
+#ifndef SG_TCS_CONV_WARPS
+#define SG_TCS_CONV_WARPS 2
+#endif
+constexpr int kConvWarps = SG_TCS_CONV_WARPS;
 constexpr uint32_t kTmemCols = 512;
 constexpr int EPI_BYTES = 4 * tc::kStageFloats * 4;  // epilogue staging (4 warps)
 static_assert(2 * BN <= static_cast<int>(kTmemCols), "TMEM columns");
@@ -87,22 +102,26 @@ struct KindHalf {
     static constexpr bool TF32 = false;
     static constexpr int ELEM = 2, BOX_K = 64, UK = 16, PLANES = 1, KSUB = 2, STAGES = 3;
     static constexpr uint32_t FMT = BF16 ? 1u : 0u;
-    static constexpr bool A_MN = false, B_MN = false;
+    static constexpr bool A_MN = false, B_MN = false, CONV = false;
 };
-template <int PLANES_, bool A_MN_ = false, bool B_MN_ = false>
+// CONV (3xTF32 only): the lo planes are made in the kernel from the raw
+// operands (which TMA stages as the hi planes); otherwise TMA loads both.
+template <int PLANES_, bool A_MN_ = false, bool B_MN_ = false, bool CONV_ = false>
 struct KindTF32 {
     static constexpr bool TF32 = true;
     static constexpr int ELEM = 4, BOX_K = 32, UK = 8, PLANES = PLANES_;
     static constexpr int KSUB = PLANES_ == 1 ? SG_TCS_TF32_KSUB : 1;
     static constexpr int STAGES = PLANES_ == 1 ? SG_TCS_TF32_STAGES : 3;
     static constexpr uint32_t FMT = 2u;
-    static constexpr bool A_MN = A_MN_, B_MN = B_MN_;
+    static constexpr bool A_MN = A_MN_, B_MN = B_MN_, CONV = CONV_;
+    static_assert(!CONV_ || PLANES_ == 2, "in-kernel lo planes are a 3xTF32 form");
 };
 
 template <class KD>
 struct Shape {
     static constexpr int STAGES = KD::STAGES;
-    static constexpr int NBAR = 2 * STAGES + 4 + 1;
+    static constexpr int THREADS = kThreads + (KD::CONV ? kConvWarps * 32 : 0);
+    static constexpr int NBAR = 2 * STAGES + 4 + 1 + (KD::CONV ? STAGES : 0);
     static constexpr int STAGE_K = KD::KSUB * KD::BOX_K;
     static constexpr int BOXES = KD::KSUB * KD::PLANES;  // per operand per stage
     static constexpr int STAGE_BYTES = BOXES * (SUB_A + SUB_B);  // per CTA
@@ -161,6 +180,52 @@ __device__ __forceinline__ void load_box(uint8_t *dst, const CUtensorMap *m, uin
         for (int c = 0; c < ROWS / 32; ++c) tma_load_pair(dst + c * 4096, m, bar, r0 + 32 * c, k0, z);
     } else {
         tma_load_pair(dst, m, bar, k0, r0, z);
+    }
+}
+
+// load_box with the completion counted on this CTA's own barrier.
+template <bool MN, int ROWS>
+__device__ __forceinline__ void load_box_own(uint8_t *dst, const CUtensorMap *m, uint64_t *bar,
+                                             int k0, int r0, int z)
+{
+    if constexpr (MN) {
+#pragma unroll
+        for (int c = 0; c < ROWS / 32; ++c) tma_load_3d(dst + c * 4096, m, bar, r0 + 32 * c, k0, z);
+    } else {
+        tma_load_3d(dst, m, bar, k0, r0, z);
+    }
+}
+
+// One stage box (16 KB: 1024 16-byte groups) of lo values from the raw box
+// at the same offsets: lo = (x - hi) with its 13 low mantissa bits cleared,
+// hi = x with its 13 low mantissa bits cleared (the value the tensor core
+// reads from the raw box).  Thread ct of the NT converter threads takes
+// groups ct, ct + NT, ..., eight loads in flight before their stores.
+template <int NT>
+__device__ __forceinline__ void lo_box(uint32_t raw, uint32_t lo, int ct)
+{
+    constexpr int G = 1024 / NT;  // groups per thread
+    static_assert(G % 8 == 0, "converter threads");
+#pragma unroll
+    for (int h = 0; h < G / 8; ++h) {
+        float4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t a = raw + 16u * static_cast<uint32_t>(ct + NT * (8 * h + i));
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(v[i].x), "=f"(v[i].y), "=f"(v[i].z), "=f"(v[i].w)
+                         : "r"(a));
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t a = lo + 16u * static_cast<uint32_t>(ct + NT * (8 * h + i));
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                         "f"(tc::trunc_tf32(v[i].x - tc::trunc_tf32(v[i].x))),
+                         "f"(tc::trunc_tf32(v[i].y - tc::trunc_tf32(v[i].y))),
+                         "f"(tc::trunc_tf32(v[i].z - tc::trunc_tf32(v[i].z))),
+                         "f"(tc::trunc_tf32(v[i].w - tc::trunc_tf32(v[i].w)))
+                         : "memory");
+        }
     }
 }
 
@@ -233,7 +298,7 @@ __device__ __forceinline__ uint32_t issue_stage_ss(uint32_t d, uint64_t a0, uint
 // the lo planes, at batch coordinate entry + a_lo_z / b_lo_z (the same map
 // with the plane's offset when one map holds both planes).
 template <class KD>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 1)
     tcs_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmA_lo,
@@ -253,7 +318,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint64_t *acc_full = empty + STAGES;    // per CTA: multicast commit
     uint64_t *acc_empty = acc_full + 2;     // even CTA's: both CTAs' epilogues
     uint64_t *mma_done = acc_empty + 2;
-    uint32_t *tmem_base = reinterpret_cast<uint32_t *>(mma_done + 1);
+    uint64_t *conv_full = mma_done + 1;     // CONV, even CTA's: both CTAs' converters
+    uint32_t *tmem_base = reinterpret_cast<uint32_t *>(conv_full + (KD::CONV ? STAGES : 0));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_base + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -263,6 +329,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1u);
             mbar_init(&empty[s], 1u);
+            if (KD::CONV) mbar_init(&conv_full[s], 2 * kConvWarps);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1u);
@@ -307,10 +374,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (rank == 0) mbar_arrive_expect_tx(&full[rr.s], 2 * STAGE_BYTES);
-                    const uint32_t fb = cluster_addr(&full[rr.s], 0);
                     uint8_t *sa = base + rr.s * STAGE_BYTES;
                     uint8_t *sb = sa + S::BOXES * SUB_A;
+                    if (KD::CONV) {
+                        // raw boxes only (the hi planes), on this CTA's barrier
+                        const int k0 = kb * S::STAGE_K;
+                        mbar_arrive_expect_tx(&full[rr.s], SUB_A + SUB_B);
+                        load_box_own<KD::A_MN, BM>(sa, &tmA, &full[rr.s], k0, m0, qa);
+                        load_box_own<KD::B_MN, HN>(sb, &tmB, &full[rr.s], k0, n0, qb);
+                        ++issued;
+                        rr.next();
+                        continue;
+                    }
+                    if (rank == 0) mbar_arrive_expect_tx(&full[rr.s], 2 * STAGE_BYTES);
+                    const uint32_t fb = cluster_addr(&full[rr.s], 0);
 #pragma unroll
                     for (int j = 0; j < KD::KSUB; ++j) {
                         const int k0 = kb * S::STAGE_K + j * KD::BOX_K;
@@ -334,7 +411,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // normal path the MMAs consumed every stage.)  An abort in the
             // odd CTA reaches the even one through the waits that then run
             // out there.
-            if (rank == 0 && (!ok || *abort_flag)) {
+            // (With CONV each CTA's loads complete on its own barrier.)
+            if ((KD::CONV || rank == 0) && (!ok || *abort_flag)) {
                 tc::Ring<STAGES> d;
                 for (long long j = 0; j < issued; ++j) {
                     if (j + STAGES >= issued) drain_cl(&full[d.s], d.ph, ab.limit);
@@ -364,8 +442,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc::tc_fence_after();
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc.s * BN);
                 uint32_t ready = 0;
+                // a stage is ready when loaded (CONV: and converted, in both CTAs)
+                uint64_t *ready_bar = KD::CONV ? conv_full : full;
                 for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
-                    if (!ready && !wait_cl(&full[sr.s], sr.ph, ab, kStatusWaitFull)) {
+                    if (!ready && !wait_cl(&ready_bar[sr.s], sr.ph, ab,
+                                           KD::CONV ? kStatusWaitConv : kStatusWaitFull)) {
                         ok = false;
                         break;
                     }
@@ -374,8 +455,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tc::Ring<STAGES> nx = sr;
                     nx.next();
                     ready = issue_stage_ss<KD>(d_tmem, adesc0 + soff, bdesc0 + soff,
-                                               kb > wu.kb_lo ? 1u : 0u, smem_u32(&full[nx.s]),
-                                               nx.ph);
+                                               kb > wu.kb_lo ? 1u : 0u,
+                                               smem_u32(&ready_bar[nx.s]), nx.ph);
                     if (kb + 1 == wu.kb_hi) ready = 0;
                     any = true;
                     umma_commit_both(&empty[sr.s]);
@@ -391,6 +472,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+    } else if (KD::CONV && warp >= kConvWarp0) {
+        // ------------------------------------------------ converters (own CTA's boxes)
+        const int ct = static_cast<int>(threadIdx.x) - kConvWarp0 * 32;
+        tc::Ring<STAGES> rr;
+        bool ok = true;
+        for (long long u = cid; ok && u < p.num_units; u += ncl) {
+            const WorkUnit wu = work_unit(u, p);
+            for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
+                if (!warp_wait(&full[rr.s], rr.ph, ab, kStatusWaitFull, lane)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sa = smem_u32(base + rr.s * STAGE_BYTES);
+                const uint32_t sb = sa + S::BOXES * SUB_A;
+                lo_box<kConvWarps * 32>(sa, sa + SUB_A, ct);
+                lo_box<kConvWarps * 32>(sb, sb + SUB_B, ct);
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) arrive_on(&conv_full[rr.s], 0);
+                rr.next();
+            }
+        }
     } else {
         // ------------------------------------------------ epilogue (own CTA's rows)
         const int q = warp & 3;
@@ -461,7 +564,7 @@ int launch_ss(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB,
     // descriptor prefetch) overlaps the end of the kernel before
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-    cfg.blockDim = dim3(tcs::kThreads);
+    cfg.blockDim = dim3(tcs::Shape<KD>::THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = plan.stream;
     cudaLaunchAttribute attr[1];

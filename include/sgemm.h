@@ -304,6 +304,9 @@ int sgemm_peak_probe(int kind, long long iters, double *flops, void *stream);
  *               leading dimension and batch stride multiples of 4 values);
  *               3xTF32 also needs the workspace to hold the operands' lo
  *               planes (sgemm_workspace_size then counts them)
+ *   6  INLINE   the RAW route with 3xTF32's lo planes made inside the product
+ *               kernel from the staged operands (no pass, no workspace for
+ *               planes); TF32 as RAW
  * A route the call's mode cannot take means AUTO; every route computes the
  * same result within the mode's accuracy bound.
  * sgemm_tune_force(route) makes every later call in the process take that
@@ -317,6 +320,7 @@ int sgemm_peak_probe(int kind, long long iters, double *flops, void *stream);
 #define SGEMM_ROUTE_DIRECT 3
 #define SGEMM_ROUTE_PLANES 4
 #define SGEMM_ROUTE_RAW 5
+#define SGEMM_ROUTE_INLINE 6
 int sgemm_tune_force(int route);
 int sgemm_tune_route(int mode, int M, int N, int K, int Q);
 

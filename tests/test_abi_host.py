@@ -195,7 +195,7 @@ def tune_table_entries():
 
 
 def test_tune_hooks_validate_arguments(lib):
-    assert lib.sgemm_tune_force(6) == lib.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_tune_force(7) == lib.SGEMM_ERR_INVALID_ARG
     assert lib.sgemm_tune_force(-1) == lib.SGEMM_ERR_INVALID_ARG
     assert lib.sgemm_tune_route(7, 8, 8, 8, 1) == -1
     assert lib.sgemm_tune_route(0, -1, 8, 8, 1) == -1

@@ -2,6 +2,10 @@
 caller's fp32 matrices (K-major or M/N-major as stored), kind::tf32 reading
 the 19 high bits of each value.
 
+For 3xTF32 the lo planes come from a pass into the workspace (route RAW) or
+are made inside the product kernel from the staged raw operands (route
+INLINE).
+
 Pins of what the tensor core does with an fp32 operand:
   - TF32 on the raw route multiplies each value with its 13 low mantissa bits
     cleared: on integer-valued data whose low bits are filled with noise it
@@ -76,13 +80,16 @@ def test_tf32_raw_drops_the_low_mantissa_bits(oracle_mod, forced, tA, tB):
     assert np.array_equal(C.astype(np.float64), Cref)
 
 
+@pytest.mark.parametrize("route", ["raw", "inline"])
 @pytest.mark.parametrize("tA,tB", LAYOUTS)
-def test_3xtf32_raw_matches_planes_bit_for_bit(forced, tA, tB):
+def test_3xtf32_raw_matches_planes_bit_for_bit(forced, tA, tB, route):
+    """The lo planes from the pass (RAW) or made in the product kernel
+    (INLINE): the same values in the same order as the planes route."""
     M, N, K = 520, 390, 700
     A, B, C0 = workloads.random_inputs(M, N, K, seed=41 + 2 * tA + tB)
     pa, pb, _ = tma_pads(M, N, K, tA, tB)
     prob = Problem(A, B, C0, 0.75, 0.25, transA=tA, transB=tB, pads=(pa + 4, pb + 8, 0))
-    forced("raw")
+    forced(route)
     C_raw = prob.run_gpu("3xtf32", api="ws")
     forced("planes")
     C_planes = prob.run_gpu("3xtf32", api="ws")
@@ -101,11 +108,11 @@ RAW_CASES = [
 ]
 
 
-@pytest.mark.parametrize("mode", ["3xtf32", "tf32"])
+@pytest.mark.parametrize("mode,route", [("3xtf32", "raw"), ("3xtf32", "inline"), ("tf32", "raw")])
 @pytest.mark.parametrize("case", RAW_CASES)
-def test_raw_route_matches_the_oracle(oracle_mod, forced, mode, case):
+def test_raw_route_matches_the_oracle(oracle_mod, forced, mode, route, case):
     M, N, K, Q, tA, tB, bcA, bcB = case
-    forced("raw")
+    forced(route)
     A, B, C0 = workloads.random_inputs(M, N, K, seed=M + 3 * N + K, Q=Q)
     if bcA:
         A = np.broadcast_to(A[:1], A.shape).copy()

@@ -2,7 +2,7 @@
 the oracle: the table changes which kernel runs, never what it computes.
 
 The FP32 path's 64 x 64 tile (route SMALL) and the tensor-core routes (PAIR,
-DIRECT, PLANES, RAW) each run ragged, transposed, padded, offset and batched
+DIRECT, PLANES, RAW, INLINE) each run ragged, transposed, padded, offset and batched
 shapes through the workspace entry and the plain one; integer-valued inputs
 must match bit for bit."""
 import numpy as np
@@ -13,8 +13,8 @@ from _helpers import TOL, Problem
 
 pytestmark = pytest.mark.gpu
 
-ROUTES = {"fp32": ["small"], "3xtf32": ["pair", "direct", "planes", "raw"],
-          "tf32": ["pair", "direct", "planes", "raw"]}
+ROUTES = {"fp32": ["small"], "3xtf32": ["pair", "direct", "planes", "raw", "inline"],
+          "tf32": ["pair", "direct", "planes", "raw", "inline"]}
 CASES = [(128, 128, 128, 1, 0, 0), (257, 130, 300, 1, 1, 0), (64, 320, 1000, 1, 0, 1),
          (500, 600, 777, 1, 1, 1), (96, 200, 64, 3, 0, 1), (1024, 1024, 512, 2, 0, 0)]
 

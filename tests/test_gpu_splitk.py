@@ -125,12 +125,14 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
     64 x 64 tile where it sends the shape to it, and decides the planes on
     the tensor paths: always with route PLANES, never with PAIR or DIRECT,
     by the time model with AUTO.  The raw route's lo planes (3xTF32) are
-    counted where it pays (always with route RAW, by its time model with
-    AUTO): rows of round_up(inner, 32) values, for either layout."""
+    counted with route RAW only: rows of round_up(inner, 32) values, for
+    either layout.  The 256 x 256 tiles' plan is also taken at the in-kernel
+    3xTF32 form's rate."""
     rates = {("fp32", "direct"): 0.24e12, ("fp32", "tma"): 0.40e12,
              ("3xtf32", "direct"): 0.47e12, ("3xtf32", "pair"): 1.8e12,
              ("tf32", "direct"): 0.55e12, ("tf32", "pair"): 3.6e12,
-             ("3xtf32", "planes"): 2.45e12, ("tf32", "planes"): 6.4e12}
+             ("3xtf32", "planes"): 2.45e12, ("tf32", "planes"): 6.4e12,
+             ("3xtf32", "inline"): 2.35e12}
     if pair_slots is None:
         pair_slots = sms // 2
     if mode == "fp32":
@@ -145,6 +147,8 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
         wide = mode == "tf32" and K >= 1536
         kernels = [(128, 128, "direct", sms, 1), (256, 256 if wide else 128, "pair", pair_slots, 2),
                    (256, 256, "planes", pair_slots, 2)]
+        if mode == "3xtf32":  # the raw route's in-kernel form, same tiles
+            kernels.append((256, 256, "inline", pair_slots, 2))
     def plan(bm, bn, feed, G, per_unit):
         """(workspace, modelled seconds) of the best split plan."""
         T = Q * math.ceil(M / bm) * math.ceil(N / bn)
@@ -188,18 +192,14 @@ def planned_workspace(mode, M, N, K, Q, sms, pair_slots=None):
         t_pair = plan(*kernels[1])[1]
         t_planes = plan(*kernels[2])[1] + (M + N) * K * Q * 4.0 * (1 + planes) / 6.0e12 + 7e-6
         room = copy(M) + copy(N)
-        # the raw route where it pays: the modelled time of its tiles' plan
-        # (the planes route's tiles) plus, for 3xTF32, its lo pass ((M + N) *
-        # K * Q * 8 bytes at 6.0 TB/s) and 7 us; room for the lo planes of
-        # either layout (rows of round_up(inner, 32) values)
-        t_raw = plan(*kernels[2])[1]
-        if mode == "3xtf32":
-            t_raw += (M + N) * K * Q * 8.0 / 6.0e12 + 7e-6
-        if route == lib.SGEMM_ROUTE_RAW or (route == lib.SGEMM_ROUTE_AUTO and t_raw < t_pair):
-            if mode == "3xtf32":
-                lo = (r256(Q * max(M * r32(K), K * r32(M)) * 4) +
-                      r256(Q * max(N * r32(K), K * r32(N)) * 4))
-                room = max(room, lo)
+        # route RAW on 3xTF32 (a lo pass into the workspace): room for the lo
+        # planes of either layout (rows of round_up(inner, 32) values); the
+        # cost models' raw form needs none (TF32 has no pass, 3xTF32 makes its
+        # lo planes in the kernel)
+        if route == lib.SGEMM_ROUTE_RAW and mode == "3xtf32":
+            lo = (r256(Q * max(M * r32(K), K * r32(M)) * 4) +
+                  r256(Q * max(N * r32(K), K * r32(N)) * 4))
+            room = max(room, lo)
         if (route == lib.SGEMM_ROUTE_PLANES or
                 (route == lib.SGEMM_ROUTE_AUTO and t_planes < t_pair)):
             room = max(room, r256(planes * Q * M * r32(K) * 4) + r256(planes * Q * N * r32(K) * 4))
