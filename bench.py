@@ -91,8 +91,9 @@ def roofline_peak(mode, num_sms, peaks, source):
 # plans them; the probes, the host-buffer entry point and the allocation-free
 # entry point are left out (they do not change what the timed kernels do).
 TIMED_SOURCES = ("api.cu", "common.cuh", "internal.h", "kernels_simt.cu", "kernels_tc.cu",
-                 "kernels_tcp.cu", "params.h", "planes.cu", "repack.cu", "simt_fp32.cuh",
-                 "tc_direct.cuh", "tc_pair.cuh", "tc_ss.cuh", "tc_tf32.cuh", "tune_table.h")
+                 "kernels_tcp.cu", "params.h", "planes.cu", "raw.cu", "repack.cu",
+                 "simt_fp32.cuh", "tc_direct.cuh", "tc_pair.cuh", "tc_ss.cuh", "tc_tf32.cuh",
+                 "tune_table.h")
 
 
 def kernel_source_hash():
@@ -492,10 +493,11 @@ def main():
                 "frac": achieved / peak, "traffic": traffic,
                 "kernel": f"sgemm {mode} path ({kernel_key})",
                 "timed": ("each call: every kernel it launches -- on the tensor-core paths "
-                          "at this size the pass into TF32 planes, the GEMM kernel and the "
-                          "split-K fix-up; on the FP32 path the operand transposition, the GEMM "
-                          "kernel and the fix-up (events bracket the whole call; traffic is "
-                          "the GEMM kernel's)" if ws_bytes else "each call: the GEMM kernel"),
+                          "at this size the GEMM kernel (the caller's A and B straight through "
+                          "TMA; 3xTF32's lo planes made inside it) and the split-K fix-up; on "
+                          "the FP32 path the operand transposition, the GEMM kernel and the "
+                          "fix-up (events bracket the whole call; traffic is the GEMM kernel's)"
+                          if ws_bytes else "each call: the GEMM kernel"),
                 "peak_source": f"{peak_note}; {peak_src} MEASURED_PEAKS.json" if bound != "alu"
                 else peak_note,
                 "algorithmic_flops_per_launch": flops_step}
@@ -963,8 +965,11 @@ def all_configs(args):
 TUNE_SHAPES = [(128, 128, 128, 1), (256, 256, 256, 1), (512, 512, 512, 1),
                (1024, 1024, 1024, 1), (2048, 2048, 2048, 1), (4092, 4092, 4092, 1),
                (8192, 8192, 8192, 1), (1024, 1024, 512, 32)]
-TUNE_ROUTES = {"fp32": ("auto", "small"), "3xtf32": ("auto", "pair", "direct", "planes"),
-               "tf32": ("auto", "pair", "direct", "planes")}
+# "models": the cost models' choice with the committed table ignored (the
+# baseline; "auto" would replay the table being rewritten)
+TUNE_ROUTES = {"fp32": ("models", "small"),
+               "3xtf32": ("models", "pair", "direct", "planes", "raw", "inline"),
+               "tf32": ("models", "pair", "direct", "planes", "raw")}
 TUNE_KEEP_AUTO = 0.02  # a route must beat the cost models' choice by 2% to get an entry
 
 
@@ -1012,7 +1017,7 @@ def tune(args):
                 lib.check(lib.sgemm_tune_force("auto"))
                 best = min(times, key=times.get)
                 cls, batched = size_class(M, N, K, Q), int(Q > 1)
-                chosen = best if times[best] < (1 - TUNE_KEEP_AUTO) * times["auto"] else "auto"
+                chosen = best if times[best] < (1 - TUNE_KEEP_AUTO) * times["models"] else "auto"
                 line = {"mode": mode, "M": M, "N": N, "K": K, "Q": Q, "size_class": cls,
                         "batched": batched, "us": {r: round(t * 1e3, 1) for r, t in times.items()},
                         "tflops": {r: round(flops / (t / 1e3) / 1e12, 2) for r, t in times.items()},

@@ -45,9 +45,10 @@ SGEMM_ROUTE_DIRECT = 3
 SGEMM_ROUTE_PLANES = 4
 SGEMM_ROUTE_RAW = 5
 SGEMM_ROUTE_INLINE = 6
+SGEMM_ROUTE_MODELS = 7
 ROUTES = {"auto": SGEMM_ROUTE_AUTO, "small": SGEMM_ROUTE_SMALL, "pair": SGEMM_ROUTE_PAIR,
           "direct": SGEMM_ROUTE_DIRECT, "planes": SGEMM_ROUTE_PLANES, "raw": SGEMM_ROUTE_RAW,
-          "inline": SGEMM_ROUTE_INLINE}
+          "inline": SGEMM_ROUTE_INLINE, "models": SGEMM_ROUTE_MODELS}
 
 SGEMM_MODE_DEFAULT = -1
 SGEMM_MODE_FP32 = 0

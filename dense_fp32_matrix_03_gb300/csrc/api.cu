@@ -328,6 +328,7 @@ int applicable(int mode, int route)
 int route_for(int mode, long long M, long long N, long long K, int Q)
 {
     const int forced = g_force_route.load();
+    if (forced == kRouteModels) return kRouteAuto;
     if (forced != kRouteAuto) return applicable(mode, forced);
     const int cls = size_class(M, N, K, Q);
     for (const TuneEntry &e : kTuneTable)

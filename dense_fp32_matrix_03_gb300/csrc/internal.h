@@ -257,8 +257,11 @@ int launch_peak_probe(int kind, long long iters, int num_sms, unsigned int *stat
 //                    3xTF32, the workspace holds the lo planes).
 //   kRouteTcInline   the raw route with 3xTF32's lo planes made inside the
 //                    product kernel (TF32: the raw route).
+//   kRouteModels     (forced only) the cost models' choice, the table
+//                    ignored: the baseline the tuning sweep measures against.
 enum Route { kRouteAuto = 0, kRouteSimtSmall = 1, kRouteTcPair = 2, kRouteTcDirect = 3,
-             kRouteTcPlanes = 4, kRouteTcRaw = 5, kRouteTcInline = 6, kRouteCount = 7 };
+             kRouteTcPlanes = 4, kRouteTcRaw = 5, kRouteTcInline = 6, kRouteModels = 7,
+             kRouteCount = 8 };
 // Size class of a call: round(log2(M * N * K * Q) / 3), clamped to
 // [kClassMin, kClassMax] -- the log2 of the edge of a cube of the same work
 // (4092^3: 12; the batched 32 x 1024 x 1024 x 512 workload: 11).

@@ -307,6 +307,8 @@ int sgemm_peak_probe(int kind, long long iters, double *flops, void *stream);
  *   6  INLINE   the RAW route with 3xTF32's lo planes made inside the product
  *               kernel from the staged operands (no pass, no workspace for
  *               planes); TF32 as RAW
+ *   7  MODELS   (to force only) the cost models' choice with the table
+ *               ignored: the baseline the sweep measures the others against
  * A route the call's mode cannot take means AUTO; every route computes the
  * same result within the mode's accuracy bound.
  * sgemm_tune_force(route) makes every later call in the process take that
@@ -321,6 +323,7 @@ int sgemm_peak_probe(int kind, long long iters, double *flops, void *stream);
 #define SGEMM_ROUTE_PLANES 4
 #define SGEMM_ROUTE_RAW 5
 #define SGEMM_ROUTE_INLINE 6
+#define SGEMM_ROUTE_MODELS 7
 int sgemm_tune_force(int route);
 int sgemm_tune_route(int mode, int M, int N, int K, int Q);
 

@@ -195,7 +195,7 @@ def tune_table_entries():
 
 
 def test_tune_hooks_validate_arguments(lib):
-    assert lib.sgemm_tune_force(7) == lib.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_tune_force(8) == lib.SGEMM_ERR_INVALID_ARG
     assert lib.sgemm_tune_force(-1) == lib.SGEMM_ERR_INVALID_ARG
     assert lib.sgemm_tune_route(7, 8, 8, 8, 1) == -1
     assert lib.sgemm_tune_route(0, -1, 8, 8, 1) == -1
@@ -203,6 +203,8 @@ def test_tune_hooks_validate_arguments(lib):
         assert lib.sgemm_tune_force("direct") == lib.SGEMM_OK
         assert lib.sgemm_tune_route("tf32", 64, 64, 64, 1) == lib.SGEMM_ROUTE_DIRECT
         assert lib.sgemm_tune_route("fp32", 64, 64, 64, 1) == lib.SGEMM_ROUTE_AUTO
+        assert lib.sgemm_tune_force("models") == lib.SGEMM_OK
+        assert lib.sgemm_tune_route("fp32", 128, 128, 128, 1) == lib.SGEMM_ROUTE_AUTO
         assert lib.sgemm_tune_force("raw") == lib.SGEMM_OK
         assert lib.sgemm_tune_route("3xtf32", 64, 64, 64, 1) == lib.SGEMM_ROUTE_RAW
         assert lib.sgemm_tune_route("fp32", 64, 64, 64, 1) == lib.SGEMM_ROUTE_AUTO
