@@ -268,6 +268,25 @@ bool encode_operand_mn(CUtensorMap *map, const float *base, long long rows, long
     return r == CUDA_SUCCESS;
 }
 
+bool encode_c_tiles(CUtensorMap *map, const float *C, long long M, long long N, long long ldc,
+                    int Q, long long sC)
+{
+    if (!get_encoder()) return false;
+    const bool batched = Q > 1 && sC != 0;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M),
+                          batched ? static_cast<cuuint64_t>(Q) : 1};
+    cuuint64_t strides[2];
+    strides[0] = static_cast<cuuint64_t>(ldc) * 4;
+    strides[1] = batched ? static_cast<cuuint64_t>(sC) * 4 : strides[0] * dims[1];
+    cuuint32_t box[3] = {16, 32, 1}, estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(C),
+                                dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool encode_operand16(CUtensorMap *map, const void *base, bool bf16, long long rows, long long K,
                       long long ld, int Q, long long stride, int box_rows)
 {

@@ -32,6 +32,7 @@ struct GemmParams {
     int a_q_step, b_q_step;    // TMA batch coordinate multiplier (0 = broadcast)
     int a_vec4, b_vec4;        // fallback producer may copy 16 bytes at a time
     int c_vec4;                // epilogue may use 16-byte C accesses
+    int c_tma;                 // the shared-memory-operand kernel's epilogue moves C by TMA
     unsigned int *status;      // device status word
     long long wait_limit;      // clock64 cycles a bounded wait may spin
     // split-K: tiles [0, dp_tiles) are whole work units (u = tile); every

@@ -47,6 +47,8 @@
 // for planes.
 #pragma once
 
+#include <cstring>
+
 #include "../../include/sgemm.h"
 #include "internal.h"
 #include "tc_pair.cuh"
@@ -87,7 +89,20 @@ constexpr int kConvWarp0 = kEpiWarp0 + 4;  // in-kernel lo planes: converter war
 #endif
 constexpr int kConvWarps = SG_TCS_CONV_WARPS;
 constexpr uint32_t kTmemCols = 512;
-constexpr int EPI_BYTES = 4 * tc::kStageFloats * 4;  // epilogue staging (4 warps)
+// Epilogue through TMA: per epilogue warp four 2 KB buffers, each one chunk
+// of 32 rows x 16 columns of C in TMA's 64-byte swizzle (16-byte slot j of
+// row r at slot j ^ ((r >> 1) & 3)), so that lane r's reads and writes of
+// its row are free of bank conflicts; C's loads run EPI_LA chunks ahead.
+// The other epilogue (split-K partial tiles, or a C TMA cannot describe)
+// stages 32 x 32 chunks in the first 4 KB.
+constexpr int EPI_CH = 16;                           // columns per chunk
+constexpr int EPI_NB = 4;                            // buffers per warp
+constexpr int EPI_LA = 2;                            // chunks of C loaded ahead
+constexpr int EPI_BUF = 32 * EPI_CH * 4;             // 2 KB
+constexpr int EPI_WARP_BYTES = EPI_NB * EPI_BUF;     // 8 KB
+static_assert(EPI_LA >= 1 && EPI_LA < EPI_NB, "lookahead");
+constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;        // 4 epilogue warps
+static_assert(EPI_WARP_BYTES >= tc::kStageFloats * 4, "register-path staging");
 static_assert(2 * BN <= static_cast<int>(kTmemCols), "TMEM columns");
 
 // Operand kinds.  ELEM: bytes per value; BOX_K: k per 128-byte box; UK: k
@@ -121,7 +136,7 @@ template <class KD>
 struct Shape {
     static constexpr int STAGES = KD::STAGES;
     static constexpr int THREADS = kThreads + (KD::CONV ? kConvWarps * 32 : 0);
-    static constexpr int NBAR = 2 * STAGES + 4 + 1 + (KD::CONV ? STAGES : 0);
+    static constexpr int NBAR = 2 * STAGES + 4 + 1 + (KD::CONV ? STAGES : 0) + 4 * EPI_NB;
     static constexpr int STAGE_K = KD::KSUB * KD::BOX_K;
     static constexpr int BOXES = KD::KSUB * KD::PLANES;  // per operand per stage
     static constexpr int STAGE_BYTES = BOXES * (SUB_A + SUB_B);  // per CTA
@@ -181,6 +196,34 @@ __device__ __forceinline__ void load_box(uint8_t *dst, const CUtensorMap *m, uin
     } else {
         tma_load_pair(dst, m, bar, k0, r0, z);
     }
+}
+
+// TMA store of a box from this CTA's shared memory (bulk group; the caller
+// commits and waits).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, const void *smem_src, int c0,
+                                             int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::
+            "l"(reinterpret_cast<uint64_t>(m)),
+        "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until at most N of this thread's committed bulk groups still read
+// shared memory (_read) or are still in progress at all.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait()
+{
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // load_box with the completion counted on this CTA's own barrier.
@@ -296,13 +339,15 @@ __device__ __forceinline__ uint32_t issue_stage_ss(uint32_t d, uint64_t a0, uint
 
 // tmA / tmB: the operands (their hi planes for 3xTF32); tmA_lo / tmB_lo:
 // the lo planes, at batch coordinate entry + a_lo_z / b_lo_z (the same map
-// with the plane's offset when one map holds both planes).
+// with the plane's offset when one map holds both planes); tmC: C in boxes
+// of 32 rows x 16 columns (used when p.c_tma).
 template <class KD>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 1)
     tcs_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmA_lo,
-                    const __grid_constant__ CUtensorMap tmB_lo, const GemmParams p, int a_lo_z,
+                    const __grid_constant__ CUtensorMap tmB_lo,
+                    const __grid_constant__ CUtensorMap tmC, const GemmParams p, int a_lo_z,
                     int b_lo_z)
 {
     using S = Shape<KD>;
@@ -311,7 +356,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    float4 *epi = reinterpret_cast<float4 *>(base + STAGES * STAGE_BYTES);
+    uint8_t *epi = base + STAGES * STAGE_BYTES;
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + STAGES * STAGE_BYTES + EPI_BYTES);
     uint64_t *full = bars;                  // even CTA's: both CTAs' bytes
     uint64_t *empty = full + STAGES;        // per CTA: multicast commit
@@ -319,7 +364,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
     uint64_t *acc_empty = acc_full + 2;     // even CTA's: both CTAs' epilogues
     uint64_t *mma_done = acc_empty + 2;
     uint64_t *conv_full = mma_done + 1;     // CONV, even CTA's: both CTAs' converters
-    uint32_t *tmem_base = reinterpret_cast<uint32_t *>(conv_full + (KD::CONV ? STAGES : 0));
+    uint64_t *cbar = conv_full + (KD::CONV ? STAGES : 0);  // epilogue C loads, per warp x buffer
+    uint32_t *tmem_base = reinterpret_cast<uint32_t *>(cbar + 4 * EPI_NB);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_base + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -336,6 +382,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
             mbar_init(&acc_empty[b], 2 * 4);
         }
         mbar_init(mma_done, 1u);
+        for (int b = 0; b < 4 * EPI_NB; ++b) mbar_init(&cbar[b], 1u);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -498,17 +545,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
         // ------------------------------------------------ epilogue (own CTA's rows)
         const int q = warp & 3;
         const int r0 = static_cast<int>(rank) * BM + q * 32;  // this warp's first row
-        float4 *stage = epi + q * (tc::kStageFloats / 4);
+        uint8_t *wbuf = epi + q * EPI_WARP_BYTES;
+        float4 *stage = reinterpret_cast<float4 *>(wbuf);   // register path: 32 x 32 staging
+        uint64_t *wbar = cbar + q * EPI_NB;
+        // Launched as a programmatic dependent: C may come from the kernel
+        // before, whose writes are visible after this wait.
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         tc::Ring<2> acc;
-        for (long long u = cid; u < p.num_units; u += ncl) {
+        long long gch = 0;  // TMA chunks this warp has handled: buffer gch % EPI_NB
+        bool ok = true;
+        for (long long u = cid; ok && u < p.num_units; u += ncl) {
             const WorkUnit wu = work_unit(u, p);
             const OutTile o = out_tile<PM, BN>(p, wu);
+            const bool tma = p.c_tma && !wu.split;
+            const bool use_beta = o.beta != 0.f;
+            const int gm = wu.tc.tm * PM + r0, gn = wu.tc.tn * BN, gz = p.Q > 1 ? wu.tc.q : 0;
             tc::prefetch_c_rows(o, r0, lane);
-            // C of the first chunk is loaded while the accumulator is made;
-            // then each chunk's C is loaded before the previous chunk is
-            // stored (two chunks of loads per lane in flight)
+            // C's first chunk is loaded while the accumulator is made
             float4 ca[8], cb[8];
-            tc::load_c_chunk(o, r0, 0, ca, lane);
+            constexpr int NCH = BN / EPI_CH;
+            if (tma) {
+                if (use_beta && lane == 0) {
+                    // chunks gch .. gch + EPI_LA - 1: their buffers' last stores
+                    // (chunks gch - EPI_NB ..) have read them
+                    bulk_wait_read<EPI_NB - EPI_LA>();
+#pragma unroll
+                    for (int i = 0; i < EPI_LA; ++i) {
+                        const int b = static_cast<int>((gch + i) % EPI_NB);
+                        mbar_arrive_expect_tx(&wbar[b], EPI_BUF);
+                        tma_load_3d(wbuf + b * EPI_BUF, &tmC, &wbar[b], gn + i * EPI_CH, gm, gz);
+                    }
+                }
+            } else {
+                if (lane == 0) bulk_wait_read<0>();  // TMA stores have read the staging
+                __syncwarp();
+                tc::load_c_chunk(o, r0, 0, ca, lane);
+            }
             int w = 1;
             if (lane == 0) w = wait_cl(&acc_full[acc.s], acc.ph, ab, kStatusWaitAcc, true);
             if (!__shfl_sync(0xffffffffu, w, 0)) break;
@@ -516,21 +588,89 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
             tc::tc_fence_after();
             const uint32_t tbase =
                 tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc.s * BN);
+            if (tma) {
+                // per chunk: the next chunk's C on its way (beta != 0), this
+                // chunk's accumulator from TMEM, alpha * acc + beta * C written
+                // in place (lane = row, as TMEM holds it), a TMA store
+                const int sw = (lane >> 1) & 3;
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 64) {
-                float v[32];
-                tc::load_c_chunk(o, r0, c0 + 32, cb, lane);
-                tc::tmem_ld32(tbase + c0, v);
-                tc::store_chunk_pre(o, r0, c0, v, ca, stage, lane);
-                if (c0 + 64 < BN) tc::load_c_chunk(o, r0, c0 + 64, ca, lane);
-                tc::tmem_ld32(tbase + c0 + 32, v);
-                tc::store_chunk_pre(o, r0, c0 + 32, v, cb, stage, lane);
+                for (int c = 0; c < NCH; ++c, ++gch) {
+                    const int b = static_cast<int>(gch % EPI_NB);
+                    if (use_beta && c + EPI_LA < NCH && lane == 0) {
+                        const int nb = static_cast<int>((gch + EPI_LA) % EPI_NB);
+                        // chunk gch + EPI_LA - EPI_NB's store has read buffer nb
+                        bulk_wait_read<EPI_NB - EPI_LA - 1>();
+                        mbar_arrive_expect_tx(&wbar[nb], EPI_BUF);
+                        tma_load_3d(wbuf + nb * EPI_BUF, &tmC, &wbar[nb], gn + (c + EPI_LA) * EPI_CH,
+                                    gm, gz);
+                    }
+                    float v[16];
+                    tc::tmem_ld16(tbase + c * EPI_CH, v);
+                    if (use_beta) {
+                        if (!warp_wait(&wbar[b], static_cast<uint32_t>((gch / EPI_NB) & 1), ab,
+                                       kStatusWaitAcc, lane)) {
+                            // the loads of chunks c .. c + EPI_LA - 1 (those of the
+                            // tile) may still be owed: wait (bounded) for them
+                            // before the teardown
+                            for (int i = 0; i < EPI_LA && c + i < NCH; ++i)
+                                drain_cl(&wbar[(gch + i) % EPI_NB],
+                                         static_cast<uint32_t>(((gch + i) / EPI_NB) & 1),
+                                         ab.limit);
+                            ok = false;
+                            break;
+                        }
+                    } else {
+                        if (lane == 0) bulk_wait_read<EPI_NB - 1>();  // chunk gch - EPI_NB's store
+                        __syncwarp();
+                    }
+                    const uint32_t row = smem_u32(wbuf + b * EPI_BUF) + lane * (EPI_CH * 4);
+#pragma unroll
+                    for (int j = 0; j < EPI_CH / 4; ++j) {
+                        const uint32_t a = row + static_cast<uint32_t>((j ^ sw) << 4);
+                        float4 x = make_float4(o.alpha * v[4 * j], o.alpha * v[4 * j + 1],
+                                               o.alpha * v[4 * j + 2], o.alpha * v[4 * j + 3]);
+                        if (use_beta) {
+                            float4 cv;
+                            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                         : "=f"(cv.x), "=f"(cv.y), "=f"(cv.z), "=f"(cv.w)
+                                         : "r"(a));
+                            x.x = fmaf(o.beta, cv.x, x.x);
+                            x.y = fmaf(o.beta, cv.y, x.y);
+                            x.z = fmaf(o.beta, cv.z, x.z);
+                            x.w = fmaf(o.beta, cv.w, x.w);
+                        }
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                                     "f"(x.x), "f"(x.y), "f"(x.z), "f"(x.w)
+                                     : "memory");
+                    }
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&tmC, wbuf + b * EPI_BUF, gn + c * EPI_CH, gm, gz);
+                        bulk_commit();
+                    }
+                }
+                if (!ok) break;
+            } else {
+                // C's next chunk is loaded before the current one is stored
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 64) {
+                    float v[32];
+                    tc::load_c_chunk(o, r0, c0 + 32, cb, lane);
+                    tc::tmem_ld32(tbase + c0, v);
+                    tc::store_chunk_pre(o, r0, c0, v, ca, stage, lane);
+                    if (c0 + 64 < BN) tc::load_c_chunk(o, r0, c0 + 64, ca, lane);
+                    tc::tmem_ld32(tbase + c0 + 32, v);
+                    tc::store_chunk_pre(o, r0, c0 + 32, v, cb, stage, lane);
+                }
             }
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) arrive_on(&acc_empty[acc.s], 0);
             acc.next();
         }
+        if (lane == 0) bulk_wait<0>();  // this warp's stores are done before the CTA exits
+        __syncwarp();
     }
 
     // ---- teardown: free TMEM jointly once both CTAs are done
@@ -572,7 +712,12 @@ int launch_ss(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmA_lo, tmB_lo, plan.p, a_lo_z, b_lo_z) !=
+    // C by TMA in the epilogue when its rows and batches suit TMA
+    alignas(64) CUtensorMap tmC;
+    std::memset(&tmC, 0, sizeof(tmC));
+    const GemmParams &p = plan.p;
+    plan.p.c_tma = p.c_vec4 && encode_c_tiles(&tmC, p.C, p.M, p.N, p.ldc, p.Q, p.sC) ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmA_lo, tmB_lo, tmC, plan.p, a_lo_z, b_lo_z) !=
         cudaSuccess)
         return SGEMM_ERR_LAUNCH;
     note_launch();
