@@ -651,13 +651,50 @@ def extra_figures(lib, default_mode, dev, stream, flush, num_sms, peaks, peak_sr
     return out
 
 
+def graph_device_ms(call_on, steps, flush):
+    """Device time of one call: the call captured in a CUDA graph and the
+    graph replayed between events (L2 flushed before each replay), so that
+    no host work of the library or of this binding is inside the interval
+    (median ms)."""
+    import torch
+    cur = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    side.wait_stream(cur)
+    with torch.cuda.stream(side):
+        call_on(side)  # any first-use set-up outside the capture
+    cur.wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        call_on(side)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(cur)
+        g.replay()
+        e1.record(cur)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    del g
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
 def config_figures(lib, dev, stream, flush, num_sms, peaks, peak_src, probes, steps=5):
     """Every workload configuration on every path, through the workspace
     entry point (the library's preferred call, with the workspace it asks
     for): TFLOP/s, the roofline that bounds it -- min(path peak, AI x HBM
     bandwidth), AI over compulsory bytes -- and the fraction of it; beside
     it the fraction of the path's probe-measured rate where the compute roof
-    binds.  L2 is flushed before every timed call."""
+    binds.  L2 is flushed before every timed call.  The call is timed with
+    events around it, so host work (the library's plan and launches, the
+    Python binding) is inside `ms`; for calls under 1e10 FLOP the cell also
+    gives `device_ms`, the same call replayed from a CUDA graph (device time
+    alone)."""
     import numpy as np
     import torch
     import workloads
@@ -687,10 +724,13 @@ def config_figures(lib, dev, stream, flush, num_sms, peaks, peak_src, probes, st
             for mode in ("fp32", "3xtf32", "tf32"):
                 ws_bytes, ws = workspace(lib, mode, M, N, K, Q, dev)
 
-                def call(mode=mode, Bd=Bd, ldb=ldb, tB=tB, ws=ws, ws_bytes=ws_bytes):
+                def call_on(st, mode=mode, Bd=Bd, ldb=ldb, tB=tB, ws=ws, ws_bytes=ws_bytes):
                     lib.check(lib.sgemm_batched_ex_ws(mode, M, N, K, w["alpha"], A, K, Bd, ldb,
                                                       beta, C, N, 0, tB, M * K, K * N, M * N, Q,
-                                                      ws, ws_bytes, stream))
+                                                      ws, ws_bytes, st))
+
+                def call(call_on=call_on):
+                    call_on(stream)
                 n_steps = steps if flops < 2e11 else 3
                 ms = statistics.median(time_calls(call, n_steps, 3, stream, flush))
                 tf = flops / (ms / 1e3) / 1e12
@@ -698,6 +738,10 @@ def config_figures(lib, dev, stream, flush, num_sms, peaks, peak_src, probes, st
                 roof = min(peak, ai * bw)
                 cell = {"tflops": round(tf, 2), "ms": round(ms, 4), "roof": round(roof, 1),
                         "bound": bound if roof == peak else "hbm", "frac": round(tf / roof, 3)}
+                if flops < 1e10:
+                    dms = graph_device_ms(call_on, 10, flush)
+                    cell["device_ms"] = round(dms, 4)
+                    cell["device_tflops"] = round(flops / (dms / 1e3) / 1e12, 2)
                 pp = probe_peak_for(mode, probes) if probes else None
                 if pp:
                     cell["frac_of_probe_roof"] = round(tf / min(pp, ai * bw), 3)

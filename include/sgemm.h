@@ -232,12 +232,13 @@ int sgemm_half_batched(int type, int M, int N, int K, float alpha, const void *A
  * products of earlier panels and the copy-out of a finished one run at the
  * same time, on two copy streams the library keeps per device, on `stream`
  * for the products of even panels and on a third library stream for those of
- * odd panels (so that two products together fill the GPU); each panel's
- * product is an ordinary workspace-entry call on the device copies (whose
- * rows suit TMA, so the tensor-core paths take their raw route where it
- * pays).  The host link bounds the call: on GB300 about 200 GB/s to the
- * device and 184 from it, ~265 in all while both directions run.  The call is
- * asynchronous like the others: C on the host holds
+ * odd panels (so that two products together fill the GPU); on 3xTF32, for
+ * shapes where the workspace entry would take the TF32 planes route, op(B)'s
+ * planes are written once and each panel's op(A) planes before its product
+ * (sgemm_host_buffer_size then includes their room).  The host link bounds
+ * the call: on GB300 about 200 GB/s to the device and 184 from it, ~265 in
+ * all while both directions run.  The call is asynchronous like the others:
+ * C on the host holds
  * the result once `stream` has reached the end of the call (synchronise it,
  * or record an event after the call).  Host memory that is page-locked
  * (cudaHostAlloc / cudaHostRegister) is copied at full speed and overlaps;
