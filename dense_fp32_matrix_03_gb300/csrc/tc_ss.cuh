@@ -64,6 +64,7 @@ using tcp::tmem_alloc_pair;
 using tcp::tmem_dealloc_pair;
 using tcp::umma_commit_both;
 using tcp::wait_cl;
+using tcp::warp_wait_cl;
 
 constexpr int BM = 128;      // rows of C per CTA
 constexpr int PM = 2 * BM;   // rows per pair tile (the MMA's M)
@@ -80,6 +81,12 @@ constexpr int SUB_B = HN * 128;  // one box of B: 16 KB
 #endif
 #ifndef SG_TCS_TF32_STAGES
 #define SG_TCS_TF32_STAGES 6
+#endif
+// In-kernel lo planes: raw (TMA) and lo (converter) ring depths, 32 KB per
+// stage each.
+#ifndef SG_TCS_CONV_RAW
+#define SG_TCS_CONV_RAW 4
+#define SG_TCS_CONV_LO 2
 #endif
 constexpr int kEpiWarp0 = 2;
 constexpr int kThreads = (kEpiWarp0 + 4) * 32;
@@ -117,6 +124,7 @@ struct KindHalf {
     static constexpr bool TF32 = false;
     static constexpr int ELEM = 2, BOX_K = 64, UK = 16, PLANES = 1, KSUB = 2, STAGES = 3;
     static constexpr uint32_t FMT = BF16 ? 1u : 0u;
+    static constexpr int LO_STAGES = 0;
     static constexpr bool A_MN = false, B_MN = false, CONV = false;
 };
 // CONV (3xTF32 only): the lo planes are made in the kernel from the raw
@@ -126,7 +134,11 @@ struct KindTF32 {
     static constexpr bool TF32 = true;
     static constexpr int ELEM = 4, BOX_K = 32, UK = 8, PLANES = PLANES_;
     static constexpr int KSUB = PLANES_ == 1 ? SG_TCS_TF32_KSUB : 1;
-    static constexpr int STAGES = PLANES_ == 1 ? SG_TCS_TF32_STAGES : 3;
+    // CONV: STAGES raw stages (hi boxes, by TMA) and LO_STAGES lo stages
+    // (made by the converters) in the room of three two-plane stages
+    static constexpr int STAGES =
+        PLANES_ == 1 ? SG_TCS_TF32_STAGES : (CONV_ ? SG_TCS_CONV_RAW : 3);
+    static constexpr int LO_STAGES = CONV_ ? SG_TCS_CONV_LO : 0;
     static constexpr uint32_t FMT = 2u;
     static constexpr bool A_MN = A_MN_, B_MN = B_MN_, CONV = CONV_;
     static_assert(!CONV_ || PLANES_ == 2, "in-kernel lo planes are a 3xTF32 form");
@@ -136,11 +148,15 @@ template <class KD>
 struct Shape {
     static constexpr int STAGES = KD::STAGES;
     static constexpr int THREADS = kThreads + (KD::CONV ? kConvWarps * 32 : 0);
-    static constexpr int NBAR = 2 * STAGES + 4 + 1 + (KD::CONV ? STAGES : 0) + 4 * EPI_NB;
+    static constexpr int LO_STAGES = KD::LO_STAGES;
+    static constexpr int NBAR = 2 * STAGES + 4 + 1 + 2 * LO_STAGES + 4 * EPI_NB;
     static constexpr int STAGE_K = KD::KSUB * KD::BOX_K;
-    static constexpr int BOXES = KD::KSUB * KD::PLANES;  // per operand per stage
+    // boxes per operand per stage TMA fills (CONV: the raw ones only)
+    static constexpr int BOXES = KD::KSUB * (KD::CONV ? 1 : KD::PLANES);
     static constexpr int STAGE_BYTES = BOXES * (SUB_A + SUB_B);  // per CTA
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + NBAR * 8 + 16 + 1024;
+    static constexpr int LO_BYTES = SUB_A + SUB_B;               // per CTA, CONV
+    static constexpr int RINGS_BYTES = STAGES * STAGE_BYTES + LO_STAGES * LO_BYTES;
+    static constexpr int SMEM_BYTES = RINGS_BYTES + EPI_BYTES + NBAR * 8 + 16 + 1024;
     // bits 15 / 16: A / B M/N-major ("transposed") instead of K-major
     static constexpr uint32_t IDESC = (1u << 4) | (KD::FMT << 7) | (KD::FMT << 10) |
                                       (KD::A_MN ? 1u << 15 : 0u) | (KD::B_MN ? 1u << 16 : 0u) |
@@ -304,23 +320,29 @@ __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint3
 // first MMA overwrites d unless acc0.  Returns whether the next stage's
 // barrier (nbar, parity npar) has already completed, tested without
 // blocking (see tcp::issue_stage).
+// a0 / b0: descriptors of the stage's first hi box, al0 / bl0 of its first
+// lo box (3xTF32; the box after the hi one when both come by TMA, a box of
+// the lo ring when the kernel makes them).
 template <class KD>
-__device__ __forceinline__ uint32_t issue_stage_ss(uint32_t d, uint64_t a0, uint64_t b0,
-                                                   uint32_t acc0, uint32_t nbar, uint32_t npar)
+__device__ __forceinline__ uint32_t issue_stage_ss(uint32_t d, uint64_t a0, uint64_t al0,
+                                                   uint64_t b0, uint64_t bl0, uint32_t acc0,
+                                                   uint32_t nbar, uint32_t npar)
 {
     constexpr uint64_t AB = SUB_A >> 4, BB = SUB_B >> 4;
 #pragma unroll
     for (int j = 0; j < KD::KSUB; ++j) {
         const uint64_t a = a0 + static_cast<uint64_t>(j * KD::PLANES) * AB;
         const uint64_t b = b0 + static_cast<uint64_t>(j * KD::PLANES) * BB;
+        const uint64_t al = al0 + static_cast<uint64_t>(j * KD::PLANES) * AB;
+        const uint64_t bl = bl0 + static_cast<uint64_t>(j * KD::PLANES) * BB;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ah = a + Shape<KD>::A_KSTEP * kk, bh = b + Shape<KD>::B_KSTEP * kk;
             const uint32_t acc = (j == 0 && kk == 0) ? acc0 : 1u;
             if (KD::PLANES == 2) {
-                mma_ss<KD>(d, ah + AB, bh, acc);  // lo * hi
-                mma_ss<KD>(d, ah, bh + BB, 1u);   // hi * lo
-                mma_ss<KD>(d, ah, bh, 1u);        // hi * hi
+                mma_ss<KD>(d, al + Shape<KD>::A_KSTEP * kk, bh, acc);  // lo * hi
+                mma_ss<KD>(d, ah, bl + Shape<KD>::B_KSTEP * kk, 1u);   // hi * lo
+                mma_ss<KD>(d, ah, bh, 1u);                             // hi * hi
             } else {
                 mma_ss<KD>(d, ah, bh, acc);
             }
@@ -356,15 +378,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *epi = base + STAGES * STAGE_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(base + STAGES * STAGE_BYTES + EPI_BYTES);
+    uint8_t *lo_base = base + STAGES * STAGE_BYTES;  // CONV: the lo ring
+    uint8_t *epi = base + S::RINGS_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + S::RINGS_BYTES + EPI_BYTES);
     uint64_t *full = bars;                  // even CTA's: both CTAs' bytes
     uint64_t *empty = full + STAGES;        // per CTA: multicast commit
     uint64_t *acc_full = empty + STAGES;    // per CTA: multicast commit
     uint64_t *acc_empty = acc_full + 2;     // even CTA's: both CTAs' epilogues
     uint64_t *mma_done = acc_empty + 2;
     uint64_t *conv_full = mma_done + 1;     // CONV, even CTA's: both CTAs' converters
-    uint64_t *cbar = conv_full + (KD::CONV ? STAGES : 0);  // epilogue C loads, per warp x buffer
+    uint64_t *lo_empty = conv_full + S::LO_STAGES;  // CONV, per CTA: multicast commit
+    uint64_t *cbar = lo_empty + S::LO_STAGES;       // epilogue C loads, per warp x buffer
     uint32_t *tmem_base = reinterpret_cast<uint32_t *>(cbar + 4 * EPI_NB);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_base + 1);
 
@@ -375,7 +399,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1u);
             mbar_init(&empty[s], 1u);
-            if (KD::CONV) mbar_init(&conv_full[s], 2 * kConvWarps);
+        }
+        for (int s = 0; s < S::LO_STAGES; ++s) {
+            mbar_init(&conv_full[s], 2 * kConvWarps);
+            mbar_init(&lo_empty[s], 1u);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1u);
@@ -422,7 +449,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
                         break;
                     }
                     uint8_t *sa = base + rr.s * STAGE_BYTES;
-                    uint8_t *sb = sa + S::BOXES * SUB_A;
+                    uint8_t *sb = sa + S::BOXES * SUB_A;  // CONV: BOXES = 1
                     if (KD::CONV) {
                         // raw boxes only (the hi planes), on this CTA's barrier
                         const int k0 = kb * S::STAGE_K;
@@ -480,6 +507,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
                 KD::A_MN ? mnmajor_sw128a32_desc(sa0) : tc::kmajor_sw128_desc(sa0);
             const uint64_t bdesc0 =
                 KD::B_MN ? mnmajor_sw128a32_desc(sb0) : tc::kmajor_sw128_desc(sb0);
+            // lo boxes: beside the hi ones, or (CONV) in the lo ring
+            const uint32_t la0 = smem_u32(lo_base), lb0 = la0 + SUB_A;
+            const uint64_t aldesc0 =
+                KD::CONV ? (KD::A_MN ? mnmajor_sw128a32_desc(la0) : tc::kmajor_sw128_desc(la0))
+                         : adesc0 + (SUB_A >> 4);
+            const uint64_t bldesc0 =
+                KD::CONV ? (KD::B_MN ? mnmajor_sw128a32_desc(lb0) : tc::kmajor_sw128_desc(lb0))
+                         : bdesc0 + (SUB_B >> 4);
+            tc::Ring<(S::LO_STAGES > 0 ? S::LO_STAGES : 1)> lr;  // CONV: lo ring position
             for (long long u = cid; ok && u < p.num_units; u += ncl) {
                 const WorkUnit wu = work_unit(u, p);
                 if (!wait_cl(&acc_empty[acc.s], acc.ph ^ 1u, ab, kStatusWaitAcc)) {
@@ -489,25 +525,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
                 tc::tc_fence_after();
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc.s * BN);
                 uint32_t ready = 0;
-                // a stage is ready when loaded (CONV: and converted, in both CTAs)
-                uint64_t *ready_bar = KD::CONV ? conv_full : full;
+                // a stage is ready when loaded (CONV: and its lo boxes made,
+                // in both CTAs -- the lo ring's barrier)
                 for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
-                    if (!ready && !wait_cl(&ready_bar[sr.s], sr.ph, ab,
+                    uint64_t *rb = KD::CONV ? &conv_full[lr.s] : &full[sr.s];
+                    if (!ready && !wait_cl(rb, KD::CONV ? lr.ph : sr.ph, ab,
                                            KD::CONV ? kStatusWaitConv : kStatusWaitFull)) {
                         ok = false;
                         break;
                     }
                     tc::tc_fence_after();
                     const uint64_t soff = static_cast<uint64_t>(sr.s * (STAGE_BYTES >> 4));
+                    const uint64_t loff =
+                        KD::CONV ? static_cast<uint64_t>(lr.s * (S::LO_BYTES >> 4)) : soff;
                     tc::Ring<STAGES> nx = sr;
                     nx.next();
-                    ready = issue_stage_ss<KD>(d_tmem, adesc0 + soff, bdesc0 + soff,
-                                               kb > wu.kb_lo ? 1u : 0u,
-                                               smem_u32(&ready_bar[nx.s]), nx.ph);
+                    auto lx = lr;
+                    lx.next();
+                    ready = issue_stage_ss<KD>(
+                        d_tmem, adesc0 + soff, aldesc0 + loff, bdesc0 + soff, bldesc0 + loff,
+                        kb > wu.kb_lo ? 1u : 0u,
+                        smem_u32(KD::CONV ? &conv_full[lx.s] : &full[nx.s]),
+                        KD::CONV ? lx.ph : nx.ph);
                     if (kb + 1 == wu.kb_hi) ready = 0;
                     any = true;
                     umma_commit_both(&empty[sr.s]);
+                    if (KD::CONV) umma_commit_both(&lo_empty[lr.s]);
                     sr.next();
+                    lr.next();
                 }
                 if (!ok) break;
                 umma_commit_both(&acc_full[acc.s]);
@@ -523,22 +568,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
         // ------------------------------------------------ converters (own CTA's boxes)
         const int ct = static_cast<int>(threadIdx.x) - kConvWarp0 * 32;
         tc::Ring<STAGES> rr;
+        tc::Ring<(S::LO_STAGES > 0 ? S::LO_STAGES : 1)> lr;
         bool ok = true;
         for (long long u = cid; ok && u < p.num_units; u += ncl) {
             const WorkUnit wu = work_unit(u, p);
             for (int kb = wu.kb_lo; kb < wu.kb_hi; ++kb) {
-                if (!warp_wait(&full[rr.s], rr.ph, ab, kStatusWaitFull, lane)) {
+                // the raw stage landed; the lo stage's last reader (the MMAs of
+                // the stage LO_STAGES back) is done
+                if (!warp_wait(&full[rr.s], rr.ph, ab, kStatusWaitFull, lane) ||
+                    !warp_wait_cl(&lo_empty[lr.s], lr.ph ^ 1u, ab, kStatusWaitMma)) {
                     ok = false;
                     break;
                 }
                 const uint32_t sa = smem_u32(base + rr.s * STAGE_BYTES);
-                const uint32_t sb = sa + S::BOXES * SUB_A;
-                lo_box<kConvWarps * 32>(sa, sa + SUB_A, ct);
-                lo_box<kConvWarps * 32>(sb, sb + SUB_B, ct);
+                const uint32_t la = smem_u32(lo_base + lr.s * S::LO_BYTES);
+                lo_box<kConvWarps * 32>(sa, la, ct);
+                lo_box<kConvWarps * 32>(sa + SUB_A, la + SUB_A, ct);
                 tc::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) arrive_on(&conv_full[rr.s], 0);
+                if (lane == 0) arrive_on(&conv_full[lr.s], 0);
                 rr.next();
+                lr.next();
             }
         }
     } else {
