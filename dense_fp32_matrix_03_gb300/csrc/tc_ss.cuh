@@ -72,15 +72,18 @@ constexpr int BN = 256;      // columns per pair tile (the MMA's N)
 constexpr int HN = BN / 2;   // rows of B^T each CTA holds
 constexpr int SUB_A = BM * 128;  // one 128-byte box of A: 16 KB
 constexpr int SUB_B = HN * 128;  // one box of B: 16 KB
-// Single-plane TF32 stages: one 32-k box per stage, six deep (more bytes in
-// flight than three 64-k stages in the same room; measured on GB300, TF32
-// planes route, TFLOP/s: 4092^3 nn 635 -> 654, nt 648 -> 667, 8192^3 873 ->
-// 898; five stages 635 / 654).
+// Single-plane TF32 stages: one 32-k box per stage (more bytes in flight
+// than 64-k stages in the same room; measured on GB300, TF32 planes route,
+// TFLOP/s: three 64-k stages 4092^3 nn 635, nt 648, 8192^3 873; six 32-k
+// stages 654 / 667 / 898; five 635 / 654), five deep, the sixth stage's
+// room given to the epilogue's C lookahead (EPI_NB, EPI_LA below).
 #ifndef SG_TCS_TF32_KSUB
 #define SG_TCS_TF32_KSUB 1
 #endif
 #ifndef SG_TCS_TF32_STAGES
-#define SG_TCS_TF32_STAGES 6
+#define SG_TCS_TF32_STAGES 5
+#define SG_TCS_TF32_EPI_NB 8
+#define SG_TCS_TF32_EPI_LA 6
 #endif
 // In-kernel lo planes: raw (TMA) and lo (converter) ring depths, 32 KB per
 // stage each.
@@ -96,20 +99,14 @@ constexpr int kConvWarp0 = kEpiWarp0 + 4;  // in-kernel lo planes: converter war
 #endif
 constexpr int kConvWarps = SG_TCS_CONV_WARPS;
 constexpr uint32_t kTmemCols = 512;
-// Epilogue through TMA: per epilogue warp four 2 KB buffers, each one chunk
-// of 32 rows x 16 columns of C in TMA's 64-byte swizzle (16-byte slot j of
-// row r at slot j ^ ((r >> 1) & 3)), so that lane r's reads and writes of
-// its row are free of bank conflicts; C's loads run EPI_LA chunks ahead.
-// The other epilogue (split-K partial tiles, or a C TMA cannot describe)
-// stages 32 x 32 chunks in the first 4 KB.
+// Epilogue through TMA: per epilogue warp EPI_NB 2 KB buffers (a kind's
+// choice, below), each one chunk of 32 rows x 16 columns of C in TMA's
+// 64-byte swizzle (16-byte slot j of row r at slot j ^ ((r >> 1) & 3)), so
+// that lane r's reads and writes of its row are free of bank conflicts; C's
+// loads run EPI_LA chunks ahead.  The other epilogue (split-K partial tiles,
+// or a C TMA cannot describe) stages 32 x 32 chunks in the first 4 KB.
 constexpr int EPI_CH = 16;                           // columns per chunk
-constexpr int EPI_NB = 4;                            // buffers per warp
-constexpr int EPI_LA = 2;                            // chunks of C loaded ahead
 constexpr int EPI_BUF = 32 * EPI_CH * 4;             // 2 KB
-constexpr int EPI_WARP_BYTES = EPI_NB * EPI_BUF;     // 8 KB
-static_assert(EPI_LA >= 1 && EPI_LA < EPI_NB, "lookahead");
-constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;        // 4 epilogue warps
-static_assert(EPI_WARP_BYTES >= tc::kStageFloats * 4, "register-path staging");
 static_assert(2 * BN <= static_cast<int>(kTmemCols), "TMEM columns");
 
 // Operand kinds.  ELEM: bytes per value; BOX_K: k per 128-byte box; UK: k
@@ -125,6 +122,7 @@ struct KindHalf {
     static constexpr int ELEM = 2, BOX_K = 64, UK = 16, PLANES = 1, KSUB = 2, STAGES = 3;
     static constexpr uint32_t FMT = BF16 ? 1u : 0u;
     static constexpr int LO_STAGES = 0;
+    static constexpr int EPI_NB = 4, EPI_LA = 2;
     static constexpr bool A_MN = false, B_MN = false, CONV = false;
 };
 // CONV (3xTF32 only): the lo planes are made in the kernel from the raw
@@ -139,6 +137,11 @@ struct KindTF32 {
     static constexpr int STAGES =
         PLANES_ == 1 ? SG_TCS_TF32_STAGES : (CONV_ ? SG_TCS_CONV_RAW : 3);
     static constexpr int LO_STAGES = CONV_ ? SG_TCS_CONV_LO : 0;
+    // epilogue buffers per warp and C's lookahead: single-plane TF32 gives a
+    // stage's room to a deeper lookahead (its epilogue, a third of 3xTF32's
+    // MMA time per tile away, is what short tiles wait on when beta != 0)
+    static constexpr int EPI_NB = PLANES_ == 1 ? SG_TCS_TF32_EPI_NB : 4;
+    static constexpr int EPI_LA = PLANES_ == 1 ? SG_TCS_TF32_EPI_LA : 2;
     static constexpr uint32_t FMT = 2u;
     static constexpr bool A_MN = A_MN_, B_MN = B_MN_, CONV = CONV_;
     static_assert(!CONV_ || PLANES_ == 2, "in-kernel lo planes are a 3xTF32 form");
@@ -149,6 +152,11 @@ struct Shape {
     static constexpr int STAGES = KD::STAGES;
     static constexpr int THREADS = kThreads + (KD::CONV ? kConvWarps * 32 : 0);
     static constexpr int LO_STAGES = KD::LO_STAGES;
+    static constexpr int EPI_NB = KD::EPI_NB, EPI_LA = KD::EPI_LA;
+    static constexpr int EPI_WARP_BYTES = EPI_NB * EPI_BUF;
+    static constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;  // 4 epilogue warps
+    static_assert(EPI_LA >= 1 && EPI_LA < EPI_NB, "lookahead");
+    static_assert(EPI_WARP_BYTES >= tc::kStageFloats * 4, "register-path staging");
     static constexpr int NBAR = 2 * STAGES + 4 + 1 + 2 * LO_STAGES + 4 * EPI_NB;
     static constexpr int STAGE_K = KD::KSUB * KD::BOX_K;
     // boxes per operand per stage TMA fills (CONV: the raw ones only)
@@ -380,7 +388,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *lo_base = base + STAGES * STAGE_BYTES;  // CONV: the lo ring
     uint8_t *epi = base + S::RINGS_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(base + S::RINGS_BYTES + EPI_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + S::RINGS_BYTES + S::EPI_BYTES);
     uint64_t *full = bars;                  // even CTA's: both CTAs' bytes
     uint64_t *empty = full + STAGES;        // per CTA: multicast commit
     uint64_t *acc_full = empty + STAGES;    // per CTA: multicast commit
@@ -389,7 +397,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
     uint64_t *conv_full = mma_done + 1;     // CONV, even CTA's: both CTAs' converters
     uint64_t *lo_empty = conv_full + S::LO_STAGES;  // CONV, per CTA: multicast commit
     uint64_t *cbar = lo_empty + S::LO_STAGES;       // epilogue C loads, per warp x buffer
-    uint32_t *tmem_base = reinterpret_cast<uint32_t *>(cbar + 4 * EPI_NB);
+    uint32_t *tmem_base = reinterpret_cast<uint32_t *>(cbar + 4 * S::EPI_NB);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_base + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -409,7 +417,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
             mbar_init(&acc_empty[b], 2 * 4);
         }
         mbar_init(mma_done, 1u);
-        for (int b = 0; b < 4 * EPI_NB; ++b) mbar_init(&cbar[b], 1u);
+        for (int b = 0; b < 4 * S::EPI_NB; ++b) mbar_init(&cbar[b], 1u);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -595,9 +603,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
         // ------------------------------------------------ epilogue (own CTA's rows)
         const int q = warp & 3;
         const int r0 = static_cast<int>(rank) * BM + q * 32;  // this warp's first row
-        uint8_t *wbuf = epi + q * EPI_WARP_BYTES;
+        uint8_t *wbuf = epi + q * S::EPI_WARP_BYTES;
         float4 *stage = reinterpret_cast<float4 *>(wbuf);   // register path: 32 x 32 staging
-        uint64_t *wbar = cbar + q * EPI_NB;
+        uint64_t *wbar = cbar + q * S::EPI_NB;
         // Launched as a programmatic dependent: C may come from the kernel
         // before, whose writes are visible after this wait.
         asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -618,10 +626,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
                 if (use_beta && lane == 0) {
                     // chunks gch .. gch + EPI_LA - 1: their buffers' last stores
                     // (chunks gch - EPI_NB ..) have read them
-                    bulk_wait_read<EPI_NB - EPI_LA>();
+                    bulk_wait_read<S::EPI_NB - S::EPI_LA>();
 #pragma unroll
-                    for (int i = 0; i < EPI_LA; ++i) {
-                        const int b = static_cast<int>((gch + i) % EPI_NB);
+                    for (int i = 0; i < S::EPI_LA; ++i) {
+                        const int b = static_cast<int>((gch + i) % S::EPI_NB);
                         mbar_arrive_expect_tx(&wbar[b], EPI_BUF);
                         tma_load_3d(wbuf + b * EPI_BUF, &tmC, &wbar[b], gn + i * EPI_CH, gm, gz);
                     }
@@ -645,32 +653,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
                 const int sw = (lane >> 1) & 3;
 #pragma unroll 1
                 for (int c = 0; c < NCH; ++c, ++gch) {
-                    const int b = static_cast<int>(gch % EPI_NB);
-                    if (use_beta && c + EPI_LA < NCH && lane == 0) {
-                        const int nb = static_cast<int>((gch + EPI_LA) % EPI_NB);
+                    const int b = static_cast<int>(gch % S::EPI_NB);
+                    if (use_beta && c + S::EPI_LA < NCH && lane == 0) {
+                        const int nb = static_cast<int>((gch + S::EPI_LA) % S::EPI_NB);
                         // chunk gch + EPI_LA - EPI_NB's store has read buffer nb
-                        bulk_wait_read<EPI_NB - EPI_LA - 1>();
+                        bulk_wait_read<S::EPI_NB - S::EPI_LA - 1>();
                         mbar_arrive_expect_tx(&wbar[nb], EPI_BUF);
-                        tma_load_3d(wbuf + nb * EPI_BUF, &tmC, &wbar[nb], gn + (c + EPI_LA) * EPI_CH,
-                                    gm, gz);
+                        tma_load_3d(wbuf + nb * EPI_BUF, &tmC, &wbar[nb],
+                                    gn + (c + S::EPI_LA) * EPI_CH, gm, gz);
                     }
                     float v[16];
                     tc::tmem_ld16(tbase + c * EPI_CH, v);
                     if (use_beta) {
-                        if (!warp_wait(&wbar[b], static_cast<uint32_t>((gch / EPI_NB) & 1), ab,
+                        if (!warp_wait(&wbar[b], static_cast<uint32_t>((gch / S::EPI_NB) & 1), ab,
                                        kStatusWaitAcc, lane)) {
                             // the loads of chunks c .. c + EPI_LA - 1 (those of the
                             // tile) may still be owed: wait (bounded) for them
                             // before the teardown
-                            for (int i = 0; i < EPI_LA && c + i < NCH; ++i)
-                                drain_cl(&wbar[(gch + i) % EPI_NB],
-                                         static_cast<uint32_t>(((gch + i) / EPI_NB) & 1),
+                            for (int i = 0; i < S::EPI_LA && c + i < NCH; ++i)
+                                drain_cl(&wbar[(gch + i) % S::EPI_NB],
+                                         static_cast<uint32_t>(((gch + i) / S::EPI_NB) & 1),
                                          ab.limit);
                             ok = false;
                             break;
                         }
                     } else {
-                        if (lane == 0) bulk_wait_read<EPI_NB - 1>();  // chunk gch - EPI_NB's store
+                        // chunk gch - EPI_NB's store has read buffer b
+                        if (lane == 0) bulk_wait_read<S::EPI_NB - 1>();
                         __syncwarp();
                     }
                     const uint32_t row = smem_u32(wbuf + b * EPI_BUF) + lane * (EPI_CH * 4);
