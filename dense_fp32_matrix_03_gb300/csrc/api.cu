@@ -217,13 +217,90 @@ bool current_sm103(int *num_sms, unsigned int **status)
     return true;
 }
 
+namespace {
+
+// Tensor maps already encoded, by their full description: a call that
+// repeats pointers and shapes (the common case in a loop) takes the map from
+// here instead of the driver (a map depends on nothing else, so an entry is
+// never stale).  Direct-mapped, 128 entries.
+struct MapKey {
+    int dtype, swizzle, promo;
+    const void *base;
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3];
+    bool operator==(const MapKey &o) const
+    {
+        return dtype == o.dtype && swizzle == o.swizzle && promo == o.promo && base == o.base &&
+               std::memcmp(dims, o.dims, sizeof(dims)) == 0 &&
+               std::memcmp(strides, o.strides, sizeof(strides)) == 0 &&
+               std::memcmp(box, o.box, sizeof(box)) == 0;
+    }
+};
+struct MapEntry {
+    bool used = false;
+    MapKey key;
+    CUtensorMap map;
+};
+constexpr int kMapCache = 128;
+std::mutex g_map_mu;
+MapEntry g_maps[kMapCache];
+
+size_t map_slot(const MapKey &k)
+{
+    uint64_t h = 1469598103934665603ull;
+    auto mix = [&h](uint64_t v) { h = (h ^ v) * 1099511628211ull; };
+    mix(static_cast<uint64_t>(k.dtype) | (static_cast<uint64_t>(k.swizzle) << 8) |
+        (static_cast<uint64_t>(k.promo) << 16));
+    mix(reinterpret_cast<uintptr_t>(k.base));
+    for (int i = 0; i < 3; ++i) mix(k.dims[i] ^ (static_cast<uint64_t>(k.box[i]) << 40));
+    for (int i = 0; i < 2; ++i) mix(k.strides[i]);
+    return static_cast<size_t>(h % kMapCache);
+}
+
+// A rank-3 tiled map with unit element strides, no interleave and zero fill.
+bool encode3(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
+             const cuuint64_t (&dims)[3], const cuuint64_t (&strides)[2],
+             const cuuint32_t (&box)[3], CUtensorMapSwizzle swizzle,
+             CUtensorMapL2promotion promo)
+{
+    if (!get_encoder()) return false;
+    MapKey k;
+    std::memset(&k, 0, sizeof(k));
+    k.dtype = static_cast<int>(dtype);
+    k.swizzle = static_cast<int>(swizzle);
+    k.promo = static_cast<int>(promo);
+    k.base = base;
+    std::memcpy(k.dims, dims, sizeof(k.dims));
+    std::memcpy(k.strides, strides, sizeof(k.strides));
+    std::memcpy(k.box, box, sizeof(k.box));
+    const size_t slot = map_slot(k);
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        if (g_maps[slot].used && g_maps[slot].key == k) {
+            *map = g_maps[slot].map;
+            return true;
+        }
+    }
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    g_maps[slot].used = true;
+    g_maps[slot].key = k;
+    g_maps[slot].map = *map;
+    return true;
+}
+
+}  // namespace
+
 bool encode_operand(CUtensorMap *map, const float *base, bool kin, long long rows, long long K,
                     long long ld, int Q, long long stride, int box_rows, bool promote256)
 {
-    if (!get_encoder()) return false;
     const bool batched = Q > 1 && stride != 0;
     cuuint64_t dims[3], strides[2];
-    cuuint32_t box[3], estr[3] = {1, 1, 1};
+    cuuint32_t box[3];
     if (kin) {
         dims[0] = static_cast<cuuint64_t>(K);
         dims[1] = static_cast<cuuint64_t>(rows);
@@ -239,71 +316,55 @@ bool encode_operand(CUtensorMap *map, const float *base, bool kin, long long row
     box[2] = 1;
     strides[0] = static_cast<cuuint64_t>(ld) * 4;
     strides[1] = batched ? static_cast<cuuint64_t>(stride) * 4 : strides[0] * dims[1];
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base),
-                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                kin ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                                promote256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
-                                           : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return encode3(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, dims, strides, box,
+                   kin ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   promote256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                              : CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
 }
 
 bool encode_operand_mn(CUtensorMap *map, const float *base, long long rows, long long K,
                        long long ld, int Q, long long stride, bool promote256)
 {
-    if (!get_encoder()) return false;
     const bool batched = Q > 1 && stride != 0;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(K),
                           batched ? static_cast<cuuint64_t>(Q) : 1};
     cuuint64_t strides[2];
     strides[0] = static_cast<cuuint64_t>(ld) * 4;
     strides[1] = batched ? static_cast<cuuint64_t>(stride) * 4 : strides[0] * dims[1];
-    cuuint32_t box[3] = {32, 32, 1}, estr[3] = {1, 1, 1};
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base),
-                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B,
-                                promote256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
-                                           : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    cuuint32_t box[3] = {32, 32, 1};
+    return encode3(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B,
+                   promote256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                              : CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
 }
 
 bool encode_c_tiles(CUtensorMap *map, const float *C, long long M, long long N, long long ldc,
                     int Q, long long sC)
 {
-    if (!get_encoder()) return false;
     const bool batched = Q > 1 && sC != 0;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M),
                           batched ? static_cast<cuuint64_t>(Q) : 1};
     cuuint64_t strides[2];
     strides[0] = static_cast<cuuint64_t>(ldc) * 4;
     strides[1] = batched ? static_cast<cuuint64_t>(sC) * 4 : strides[0] * dims[1];
-    cuuint32_t box[3] = {16, 32, 1}, estr[3] = {1, 1, 1};
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(C),
-                                dims, strides, box,
-                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    cuuint32_t box[3] = {16, 32, 1};
+    return encode3(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
 }
 
 bool encode_operand16(CUtensorMap *map, const void *base, bool bf16, long long rows, long long K,
                       long long ld, int Q, long long stride, int box_rows)
 {
-    if (!get_encoder()) return false;
     const bool batched = Q > 1 && stride != 0;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows),
                           batched ? static_cast<cuuint64_t>(Q) : 1};
     cuuint64_t strides[2];
     strides[0] = static_cast<cuuint64_t>(ld) * 2;
     strides[1] = batched ? static_cast<cuuint64_t>(stride) * 2 : strides[0] * dims[1];
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1}, estr[3] = {1, 1, 1};
-    const CUresult r =
-        g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                 const_cast<void *>(base), dims, strides, box, estr,
-                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+    return encode3(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                   base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 bool smem_attr_once(const void *kernel, int bytes)
