@@ -2,9 +2,7 @@
 // MMA from shared memory, fp32 accumulation and output:
 // C = alpha * op(A) @ op(B) + beta * C.
 //
-// Operands arrive ready for the MMA, K-major, and TMA stages them with the
-// 128-byte swizzle straight into the layout tcgen05.mma reads -- no
-// conversion inside the kernel:
+// TMA stages the operands straight into the layout tcgen05.mma reads:
 //   - 16-bit inputs (bf16 or fp16, kind::f16): the contraction the pages
 //     point to for tensor cores with narrower inputs ("From 1% to 94% of
 //     cuBLAS, one kernel at a time", future work); products of 16-bit values
@@ -16,35 +14,39 @@
 //   - the caller's fp32 matrices themselves (kind::tf32 reads the 19 high
 //     bits of each 32-bit value and ignores the 13 low mantissa bits): the
 //     single pass of TF32, or the hi planes of 3xTF32 beside lo planes that
-//     a pass wrote in the operands' own layout.  An operand whose rows run
-//     along M or N (A stored K x M, B stored K x N) is staged M/N-major: TMA
-//     boxes of 32 rows-inner values by 32 k in the 128-byte swizzle with
-//     32-byte atoms, read by the MMA through an M/N-major descriptor.
+//     a pass wrote in the operands' own layout or that the kernel makes
+//     itself (below).  An operand whose rows run along M or N (A stored
+//     K x M, B stored K x N) is staged M/N-major: TMA boxes of 32 rows-inner
+//     values by 32 k in the 128-byte swizzle with 32-byte atoms, read by the
+//     MMA through an M/N-major descriptor; the others K-major, boxes of 32 k
+//     (128 bytes of fp32, 64 k of 16-bit) by 128 rows, 128-byte swizzle.
 //
 // Tile 256 x 256 per CTA pair (cta_group::2, M = 256, N = 256): each CTA
 // stages its 128 rows of A and its 128 of the tile's 256 rows of B^T.  A
-// stage holds, per CTA, two 128-byte boxes of each operand (128 k of 16-bit
-// values; 64 KB, three stages), one box of each plane of 3xTF32 (32 k; 64
-// KB, three stages), or one box of TF32 (32 k; 32 KB, six stages).  Both
-// CTAs' TMA loads complete on the even CTA's barrier (cta_group::2 form,
-// which may name the peer's barrier); one thread of the even CTA issues
-// every MMA and multicasts its commits (stage free, accumulator full) to
-// both CTAs.  TMEM: two 256-column fp32 accumulators
-// per CTA (double buffered, so the epilogue overlaps the next tile).
+// stage holds, per CTA, two boxes of each operand (128 k of 16-bit values;
+// 64 KB, three stages), one box of each plane of 3xTF32 (32 k; 64 KB, three
+// stages), or one box of TF32 (32 k; 32 KB, five stages).  Both CTAs' TMA
+// loads complete on the even CTA's barrier (cta_group::2 form, which may
+// name the peer's barrier); one thread of the even CTA issues every MMA and
+// multicasts its commits (stage free, accumulator full) to both CTAs.  TMEM:
+// two 256-column fp32 accumulators per CTA (double buffered, so the epilogue
+// overlaps the next tile).
 //
 // Warps: 0 TMA producer, 1 TMEM allocator + MMA issuer (even CTA), 2-5
-// epilogue (warp w reads TMEM lanes 32 * (w % 4) .. +31).  Every wait is
-// bounded; the CTAs meet at a cluster barrier before freeing TMEM.
+// epilogue (warp w reads TMEM lanes 32 * (w % 4) .. +31; C by TMA in chunks
+// of 32 rows x 16 columns when C's rows suit TMA), 6-7 converters (in-kernel
+// lo planes only).  Every wait is bounded; the CTAs meet at a cluster barrier
+// before freeing TMEM.
 //
 // In-kernel lo planes (3xTF32 on the caller's matrices, KindTF32 with CONV):
-// TMA stages only the raw boxes (the hi planes), each CTA's loads completing
-// on its own barrier; SG_TCS_CONV_WARPS converter warps per CTA (from 6) then write each
-// stage's lo boxes from its raw boxes, value by value at the same offsets
-// (the swizzle is a function of the offset, so the lo box has the raw box's
-// layout), make them visible to the tensor core (fence.proxy.async) and
-// arrive on the even CTA's conv barrier, which the MMA issuer waits on in
-// place of the load barrier.  No pass over the operands and no workspace
-// for planes.
+// TMA stages only the raw boxes (the hi planes), in a ring of its own, each
+// CTA's loads completing on its own barrier; SG_TCS_CONV_WARPS converter
+// warps per CTA then write each stage's lo boxes into a second, shorter ring
+// from the raw boxes, value by value at the same offsets (the swizzle is a
+// function of the offset, so a lo box has its raw box's layout), make them
+// visible to the tensor core (fence.proxy.async) and arrive on the even
+// CTA's conv barrier, which the MMA issuer waits on in place of the load
+// barrier.  No pass over the operands and no workspace for planes.
 #pragma once
 
 #include <cstring>
