@@ -140,3 +140,36 @@ def test_raw_route_needs_tma_describable_operands(oracle_mod, forced, mode):
     C = prob.run_gpu(mode, api="ws")
     Cref, D = prob.oracle(oracle_mod)
     assert oracle_mod.max_rel_err(C, Cref, D) <= TOL[mode]
+
+
+@pytest.mark.parametrize("mode", ["3xtf32", "tf32"])
+def test_one_buffer_many_shapes(oracle_mod, mode):
+    """The same device buffers used for calls of different shapes, leading
+    dimensions and batch counts in turn (tensor maps are cached by their full
+    description: each shape must get its own), each call against the oracle."""
+    import torch
+    import dense_fp32_matrix_03_gb300 as lib
+    dev = torch.device("cuda", 0)
+    cap = 1 << 22
+    dA = torch.empty(cap, device=dev)
+    dB = torch.empty(cap, device=dev)
+    dC = torch.empty(cap, device=dev)
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device=dev)
+    shapes = [(640, 512, 384, 1, 0), (512, 640, 384, 1, 1), (640, 512, 384, 1, 0),
+              (256, 384, 512, 3, 0), (384, 256, 640, 1, 1), (640, 512, 384, 1, 0)]
+    for i, (M, N, K, Q, tB) in enumerate(shapes):
+        A, B, C0 = workloads.random_inputs(M, N, K, seed=200 + i, Q=Q)
+        prob = Problem(A, B, C0, 1.0, 0.5, transB=tB)
+        assert prob.Abuf.size <= cap and prob.Bbuf.size <= cap and prob.Cbuf.size <= cap
+        dA[:prob.Abuf.size].copy_(torch.from_numpy(prob.Abuf))
+        dB[:prob.Bbuf.size].copy_(torch.from_numpy(prob.Bbuf))
+        dC[:prob.Cbuf.size].copy_(torch.from_numpy(prob.Cbuf))
+        wsb = lib.sgemm_workspace_size(mode, M, N, K, Q)
+        assert wsb <= ws.numel()
+        st = lib.sgemm_batched_ex_ws(mode, M, N, K, 1.0, dA, prob.lda, dB, prob.ldb, 0.5, dC,
+                                     prob.ldc, 0, tB, prob.sA, prob.sB, prob.sC, Q, ws, wsb)
+        assert st == lib.SGEMM_OK
+        assert lib.sgemm_poll_error() == lib.SGEMM_OK
+        C = prob.extract(dC[:prob.Cbuf.size].cpu().numpy())
+        Cref, D = prob.oracle(oracle_mod)
+        assert oracle_mod.max_rel_err(C, Cref, D) <= TOL[mode], (mode, M, N, K, Q, tB)

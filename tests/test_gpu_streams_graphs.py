@@ -128,37 +128,44 @@ def test_calls_captured_in_a_cuda_graph(oracle_mod, mode):
     assert np.array_equal(Cs.cpu().numpy().astype(np.float64), want)
 
 
-@pytest.mark.parametrize("mode", ["3xtf32", "tf32"])
-def test_planes_route_captured_in_a_cuda_graph(oracle_mod, mode):
-    """A call on the planes route (the operand pass, then the product
-    launched as a programmatic dependent of it, then the split-K fix-up)
-    captured into a graph and replayed twice on new integer inputs: sampled
-    rows bit for bit."""
+@pytest.mark.parametrize("mode,route", [("3xtf32", "planes"), ("3xtf32", "inline"),
+                                        ("3xtf32", "raw"), ("tf32", "planes"), ("tf32", "raw")])
+def test_large_shape_routes_captured_in_a_cuda_graph(oracle_mod, mode, route):
+    """A call on each large-shape tensor-core route, forced -- the planes
+    route (the operand pass, then the product launched as a programmatic
+    dependent of it), the raw route with a lo pass, the raw route with the lo
+    planes made in the kernel -- each with its split-K fix-up and, beta != 0,
+    C loaded and stored by TMA in the epilogue, captured into a graph and
+    replayed twice on new integer inputs: sampled rows bit for bit."""
     import torch
     import dense_fp32_matrix_03_gb300 as lib
     from _helpers import sample_rows
     M = N = 3072
     K = 2000
-    prob = Problem(*workloads.integer_inputs(M, N, K, seed=90), 2.0, 0.0)
-    A, B, C = device_problem(prob)
-    wsb = lib.sgemm_workspace_size(mode, M, N, K, 1)
-    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
-    s = torch.cuda.Stream()
-    with torch.cuda.stream(s):
-        assert call_ws(lib, mode, prob, A, B, C, ws, wsb, s) == lib.SGEMM_OK
-    s.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        assert call_ws(lib, mode, prob, A, B, C, ws, wsb, s) == lib.SGEMM_OK
-    rows = sample_rows(1, M, 12, seed=91, tile=256)
-    for rep in range(2):
-        fresh = Problem(*workloads.integer_inputs(M, N, K, seed=92 + rep), 2.0, 0.0)
-        for dst, src in zip((A, B, C), (fresh.Abuf, fresh.Bbuf, fresh.Cbuf)):
-            dst.copy_(torch.from_numpy(src))
-        torch.cuda.synchronize()
-        g.replay()
-        torch.cuda.synchronize()
-        assert lib.sgemm_poll_error() == lib.SGEMM_OK
-        got = fresh.extract(C.cpu().numpy())
-        Cref, _ = fresh.oracle(oracle_mod, rows=rows)
-        assert np.array_equal(np.stack([got[q, i] for q, i in rows]).astype(np.float64), Cref)
+    assert lib.sgemm_tune_force(route) == lib.SGEMM_OK
+    try:
+        prob = Problem(*workloads.integer_inputs(M, N, K, seed=90), 2.0, -1.0)
+        A, B, C = device_problem(prob)
+        wsb = lib.sgemm_workspace_size(mode, M, N, K, 1)
+        ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            assert call_ws(lib, mode, prob, A, B, C, ws, wsb, s) == lib.SGEMM_OK
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            assert call_ws(lib, mode, prob, A, B, C, ws, wsb, s) == lib.SGEMM_OK
+        rows = sample_rows(1, M, 12, seed=91, tile=256)
+        for rep in range(2):
+            fresh = Problem(*workloads.integer_inputs(M, N, K, seed=92 + rep), 2.0, -1.0)
+            for dst, src in zip((A, B, C), (fresh.Abuf, fresh.Bbuf, fresh.Cbuf)):
+                dst.copy_(torch.from_numpy(src))
+            torch.cuda.synchronize()
+            g.replay()
+            torch.cuda.synchronize()
+            assert lib.sgemm_poll_error() == lib.SGEMM_OK
+            got = fresh.extract(C.cpu().numpy())
+            Cref, _ = fresh.oracle(oracle_mod, rows=rows)
+            assert np.array_equal(np.stack([got[q, i] for q, i in rows]).astype(np.float64), Cref)
+    finally:
+        lib.sgemm_tune_force("auto")
