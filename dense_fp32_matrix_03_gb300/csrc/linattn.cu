@@ -452,6 +452,16 @@ __global__ void __launch_bounds__(kThreads, 2) la_output_kernel(const Args p)
     stage_rows_async<DK>(Qs, QP, p.q + (head * p.T + t0) * DK, DK, n, tid);
     stage_rows_async<DK>(Bs, DK + 4, p.k + (head * p.T + t0) * DK, DK, n, tid);
     cp_commit();
+    // V and the chunk's state are staged only after A is formed: ask L2 for
+    // their lines now, so that those copies wait on L2 rather than DRAM
+    {
+        const float *vv = p.v + (head * p.T + t0) * DV;
+        const float *hh = p.h + (head * p.NT + c) * DK * DV;
+        for (int i = tid; i < n * DV / 32; i += kThreads)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(vv + 32 * i));
+        for (int i = tid; i < DK * DV / 32; i += kThreads)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(hh + 32 * i));
+    }
     chunk_decay(p.g != nullptr ? p.g + head * p.T + t0 : nullptr, n, G, tid);
     cp_wait<0>();
     __syncthreads();
