@@ -681,18 +681,44 @@ int repack_for_simt(Plan &plan)
     return SGEMM_OK;
 }
 
+// Whether copying the operands TMA cannot describe pays for a call: the
+// direct kernel's modelled time on the operands as they are, against the
+// copies' (each operand read and written at HBM rate, ~4 us of launch and
+// drain per copy) plus the pair kernel's.  Tiny problems keep the direct
+// kernel: one launch instead of three.
+bool repack_pays(const Plan &plan)
+{
+    const GemmParams &p = plan.p;
+    const size_t any = ~static_cast<size_t>(0);
+    int bm = 0, bn = 0;
+    tc_tile_dims(plan.mode, p.K, false, bm, bn);
+    long long tiles = static_cast<long long>(p.Q) * ((p.M + bm - 1) / bm) * ((p.N + bn - 1) / bn);
+    const double t_direct =
+        choose_plan(tiles, p.K, plan.num_sms, plan.mode, bm, bn, kFeedDirect, any).seconds;
+    tc_tile_dims(plan.mode, p.K, true, bm, bn);
+    tiles = static_cast<long long>(p.Q) * ((p.M + bm - 1) / bm) * ((p.N + bn - 1) / bn);
+    double t = choose_plan(tiles, p.K, tc_pair_slots(plan.num_sms), plan.mode, bm, bn, kFeedPair,
+                           any)
+                   .seconds;
+    if (!plan.a_tma) t += 4e-6 + 2.0 * 4.0 * p.Q * static_cast<double>(p.M) * p.K / 6.0e12;
+    if (!plan.b_tma) t += 4e-6 + 2.0 * 4.0 * p.Q * static_cast<double>(p.N) * p.K / 6.0e12;
+    return t < t_direct;
+}
+
 // Tensor-core paths with a workspace: an operand TMA cannot describe (row
 // pitch or batch stride not a multiple of 16 bytes, unaligned base) is
 // copied, in its own layout, into the workspace with rows padded to whole
 // 128-byte lines, so that the product runs on the TMA-fed pair kernel
 // instead of the direct-load one (measured on GB300, the ragged
-// 1000 x 1500 x 777 case, lda = 777: see DESIGN).  What remains of the
-// workspace goes to the split plan; without room for the copy the operand
-// stays where it is and the direct kernel runs.
-int repack_for_tc(Plan &plan)
+// 1000 x 1500 x 777 case, lda = 777: 3xTF32 45.5 -> 74.3 TFLOP/s).  The
+// cost models decide unless the caller forced the pair route (`force`).  What
+// remains of the workspace goes to the split plan; without room for the
+// copy the operand stays where it is and the direct kernel runs.
+int repack_for_tc(Plan &plan, bool force)
 {
     GemmParams &p = plan.p;
     if (plan.ws == nullptr || plan.ws_bytes == 0 || (plan.a_tma && plan.b_tma)) return SGEMM_OK;
+    if (!force && !repack_pays(plan)) return SGEMM_OK;
     char *w = static_cast<char *>(plan.ws);
     size_t used = 0;
     for (int which = 0; which < 2; ++which) {
@@ -815,7 +841,9 @@ int run(int mode, int M, int N, int K, float alpha, const float *A, int lda, con
         if (taken || rc != SGEMM_OK) return rc;
     }
     if (route != kRouteTcDirect) {  // the direct kernel reads any layout as it is
-        rc = repack_for_tc(plan);
+        // the tuning table's pair route was measured on TMA-fed operands: only a
+        // caller's explicit choice of it forces the copies
+        rc = repack_for_tc(plan, g_force_route.load() == kRouteTcPair);
         if (rc != SGEMM_OK) return rc;
     }
     return launch_tc(plan, route);

@@ -12,7 +12,7 @@
 //     mantissa bits cleared, which is what the tensor core reads); a pass
 //     writes each operand's lo plane, lo = (x - hi) with its 13 low mantissa
 //     bits cleared, in the operand's own layout (element by element, no
-//     transposition), and the product multiplies lo*hi + hi*lo + hi*hi per k
+//     transposition), and the product multiplies hi*hi + hi*lo + lo*hi per k
 //     step -- the same values and the same order as the planes route
 //     (planes.cu), whose pass writes both planes.
 // Against the planes route the pass moves two bytes per operand byte

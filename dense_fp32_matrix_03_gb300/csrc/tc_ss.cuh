@@ -10,7 +10,8 @@
 //   - fp32 operands already in TF32 form (kind::tf32), made by a pass over
 //     the operands into the caller's workspace: one plane rounded to the
 //     nearest TF32 value (TF32), or the hi and lo planes of the 3xTF32 split,
-//     multiplied as lo*hi + hi*lo + hi*hi (3xTF32);
+//     multiplied as hi*hi + hi*lo + lo*hi per k step (3xTF32; the first
+//     two read A's hi box once, through the collector buffer);
 //   - the caller's fp32 matrices themselves (kind::tf32 reads the 19 high
 //     bits of each 32-bit value and ignores the 13 low mantissa bits): the
 //     single pass of TF32, or the hi planes of 3xTF32 beside lo planes that
@@ -92,6 +93,11 @@ constexpr int SUB_B = HN * 128;  // one box of B: 16 KB
 #ifndef SG_TCS_CONV_RAW
 #define SG_TCS_CONV_RAW 4
 #define SG_TCS_CONV_LO 2
+#endif
+// 3xTF32: the k step's two MMAs on A's hi box share one read of it through
+// the collector buffer (1), or read it twice (0).
+#ifndef SG_TCS_COLLECT_A
+#define SG_TCS_COLLECT_A 1
 #endif
 constexpr int kEpiWarp0 = 2;
 constexpr int kThreads = (kEpiWarp0 + 4) * 32;
@@ -324,9 +330,32 @@ __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint3
             : "memory");
 }
 
+// The same MMA (kind::tf32) with A kept in the tensor core's collector
+// buffer for the next MMA (fill), or taken from it and then released
+// (lastuse): the two MMAs of a k step that share A's hi box read it from
+// shared memory once.
+__device__ __forceinline__ void mma_tf32_fill(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32.collector::a::fill [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_tf32_lastuse(uint32_t d, uint64_t a, uint64_t b,
+                                                 uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32.collector::a::lastuse [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
 // One stage's MMAs into accumulator d: per box, four k steps of 32 bytes
 // (+2 in a descriptor's 16-byte address units); with two planes, box
-// (j, lo) follows box (j, hi) and each k step is lo*hi + hi*lo + hi*hi.  The
+// (j, lo) follows box (j, hi) and each k step is hi*hi + hi*lo + lo*hi.  The
 // first MMA overwrites d unless acc0.  Returns whether the next stage's
 // barrier (nbar, parity npar) has already completed, tested without
 // blocking (see tcp::issue_stage).
@@ -350,9 +379,16 @@ __device__ __forceinline__ uint32_t issue_stage_ss(uint32_t d, uint64_t a0, uint
             const uint64_t ah = a + Shape<KD>::A_KSTEP * kk, bh = b + Shape<KD>::B_KSTEP * kk;
             const uint32_t acc = (j == 0 && kk == 0) ? acc0 : 1u;
             if (KD::PLANES == 2) {
+#if SG_TCS_COLLECT_A
+                // hi * hi, hi * lo (A's hi box from the collector), lo * hi
+                mma_tf32_fill(d, ah, bh, Shape<KD>::IDESC, acc);
+                mma_tf32_lastuse(d, ah, bl + Shape<KD>::B_KSTEP * kk, Shape<KD>::IDESC, 1u);
+                mma_ss<KD>(d, al + Shape<KD>::A_KSTEP * kk, bh, 1u);
+#else
                 mma_ss<KD>(d, al + Shape<KD>::A_KSTEP * kk, bh, acc);  // lo * hi
                 mma_ss<KD>(d, ah, bl + Shape<KD>::B_KSTEP * kk, 1u);   // hi * lo
                 mma_ss<KD>(d, ah, bh, 1u);                             // hi * hi
+#endif
             } else {
                 mma_ss<KD>(d, ah, bh, acc);
             }

@@ -77,3 +77,43 @@ def test_route_of_a_mode_that_cannot_take_it_is_auto(forced):
     assert lib.sgemm_tune_route("3xtf32", 128, 128, 128, 1) == lib.SGEMM_ROUTE_AUTO
     forced("planes")
     assert lib.sgemm_tune_route("fp32", 128, 128, 128, 1) == lib.SGEMM_ROUTE_AUTO
+
+
+def _launches(fn):
+    import torch
+    import dense_fp32_matrix_03_gb300 as lib
+    torch.cuda.synchronize()
+    n0 = lib.sgemm_kernel_launches()
+    out = fn()
+    return out, lib.sgemm_kernel_launches() - n0
+
+
+@pytest.mark.parametrize("mode", ["3xtf32", "tf32"])
+@pytest.mark.parametrize("shape", [(1, 1, 1), (5, 7, 3), (37, 29, 61)])
+def test_tiny_call_on_odd_pitches_keeps_the_direct_kernel(oracle_mod, mode, shape):
+    """Operands TMA cannot describe (pitches of 4-byte multiples only) on a
+    tiny problem, through the workspace entry: the cost models keep the
+    direct kernel on the operands as they are -- one launch -- instead of
+    copying them for the pair kernel."""
+    M, N, K = shape
+    A, B, C0 = workloads.random_inputs(M, N, K, seed=M * N + K)
+    prob = Problem(A, B, C0, 1.5, 0.5)
+    C, n = _launches(lambda: prob.run_gpu(mode, api="ws"))
+    assert n == 1, f"{n} launches"
+    Cref, D = prob.oracle(oracle_mod)
+    assert oracle_mod.max_rel_err(C, Cref, D) <= TOL[mode]
+
+
+@pytest.mark.parametrize("mode", ["3xtf32", "tf32"])
+def test_ragged_call_on_odd_pitches_copies_its_operand(oracle_mod, mode):
+    """The ragged 1000 x 1500 x 777 shape (A's pitch 777 floats): moving A
+    into the workspace pays there, so the call launches more than the
+    product."""
+    A, B, C0 = workloads.random_inputs(1000, 1500, 777, seed=3)
+    prob = Problem(A, B, C0, 1.0, -2.0)
+    C, n = _launches(lambda: prob.run_gpu(mode, api="ws"))
+    assert n >= 2, f"{n} launches"
+    rows = [0, 1, 127, 128, 511, 998, 999]
+    Cref, D = prob.oracle(oracle_mod, rows=[(0, i) for i in rows])
+    got = np.stack([C[0, i] for i in rows])
+    assert oracle_mod.max_rel_err(got, Cref, D) <= TOL[mode]
