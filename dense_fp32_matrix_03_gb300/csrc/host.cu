@@ -80,9 +80,6 @@ struct Layout {
     size_t offA, offB, offC, offW; // byte offsets into the buffer (offW: two workspaces)
     size_t ws_bytes, total;
     int panel, panels;             // rows of C per panel, panel count
-    bool planes;                   // tensor-core planes: op(B)'s once, op(A)'s per panel
-    size_t offPB, offPA;           // op(B)'s planes; two panels' op(A) planes
-    size_t pa_bytes;               // one panel's op(A) planes
 };
 
 // Rows per panel when the caller leaves it to the library: as many whole
@@ -136,27 +133,14 @@ bool make_layout(int mode, int M, int N, int K, int transA, int transB, int pane
     L->offC = align256(L->offB + 4ull * rowsB * L->ldB);
     L->offW = align256(L->offC + 4ull * M * L->ldC);
     L->total = L->offW + 2 * align256(L->ws_bytes);
-    // 3xTF32, where the planes route pays for the whole product: op(B) is
-    // written as TF32 planes once and each panel's op(A) on its own stream's
-    // buffer, and every panel's product runs on the shared-memory-operand
-    // kernel (measured on GB300 at 4092^3, ms per call: 3xTF32 0.992 -> 0.941;
-    // TF32, bound by the host link, 0.874 -> 0.885, so it stays on the pair
-    // kernel).  The other panel products are workspace-entry calls, which
-    // take the raw route where it pays; for 3xTF32 that is slower here
-    // (4092^3: 0.94-0.96 ms): the device copies keep the host's row pitch,
-    // off 128-byte lines at 4092 floats (128-byte-pitched copies, pitched
-    // rather than contiguous, made the call 1.08-1.15 ms), and B's planes
-    // are written once per call while the raw product reads unaligned rows in
-    // every panel.
-    L->planes =
-        mode == SGEMM_MODE_3XTF32 && K > 0 && planes_pay(mode, M, N, K, 1, 1, 1, num_sms);
-    L->offPB = L->offPA = L->pa_bytes = 0;
-    if (L->planes) {
-        L->offPB = L->total;
-        L->offPA = L->offPB + planes_operand_bytes(mode, N, K);
-        L->pa_bytes = planes_operand_bytes(mode, L->panel, K);
-        L->total = L->offPA + 2 * L->pa_bytes;
-    }
+    // Every panel's product is a workspace-entry call on the device copies,
+    // which takes the routes the cost models pick (3xTF32 at 4092^3: the raw
+    // route with the lo planes made in the kernel, no pass).  Measured on
+    // GB300, 3xTF32 4092^3, ms per call, interleaved: 0.943 with op(B)
+    // written as TF32 planes once and each panel's op(A) before its product
+    // (the planes route), 0.921 without (the device copies keep the host's
+    // row pitch, off 128-byte lines at 4092 floats; 128-byte-pitched copies,
+    // pitched rather than contiguous, made the call 1.08-1.15 ms).
     return true;
 }
 
@@ -219,13 +203,9 @@ int sgemm_host(int mode, int M, int N, int K, float alpha, const float *A, int l
     void *ws_of[2] = {L.ws_bytes ? base + L.offW : nullptr,
                       L.ws_bytes ? base + L.offW + align256(L.ws_bytes) : nullptr};
     cudaStream_t st_of[2] = {st, comp};
-    const bool planes = L.planes && reads_ab;
-    float *pPB = reinterpret_cast<float *>(base + L.offPB);
-    float *pPA[2] = {reinterpret_cast<float *>(base + L.offPA),
-                     reinterpret_cast<float *>(base + L.offPA + L.pa_bytes)};
 
-    cudaEvent_t fork = nullptr, join = nullptr, join2 = nullptr, b_in = nullptr,
-                b_planes = nullptr, ready[kMaxPanels] = {}, done[kMaxPanels] = {};
+    cudaEvent_t fork = nullptr, join = nullptr, join2 = nullptr, ready[kMaxPanels] = {},
+                done[kMaxPanels] = {};
     int rc = SGEMM_OK;
     auto ok = [&rc](cudaError_t e) {
         if (e != cudaSuccess && rc == SGEMM_OK) rc = SGEMM_ERR_LAUNCH;
@@ -234,9 +214,7 @@ int sgemm_host(int mode, int M, int N, int K, float alpha, const float *A, int l
     const unsigned flags = cudaEventDisableTiming;
     bool made = ok(cudaEventCreateWithFlags(&fork, flags)) &&
                 ok(cudaEventCreateWithFlags(&join, flags)) &&
-                ok(cudaEventCreateWithFlags(&join2, flags)) &&
-                ok(cudaEventCreateWithFlags(&b_in, flags)) &&
-                ok(cudaEventCreateWithFlags(&b_planes, flags));
+                ok(cudaEventCreateWithFlags(&join2, flags));
     for (int p = 0; made && p < L.panels; ++p)
         made = ok(cudaEventCreateWithFlags(&done[p], flags)) &&
                ok(cudaEventCreateWithFlags(&ready[p], flags));
@@ -250,15 +228,6 @@ int sgemm_host(int mode, int M, int N, int K, float alpha, const float *A, int l
                                   cudaMemcpyHostToDevice, in)
                       : copy_rows(dB, L.ldB * f, B, ldb * f, N * f, K,
                                   cudaMemcpyHostToDevice, in));
-        if (planes && ok(cudaEventRecord(b_in, in)) && ok(cudaStreamWaitEvent(st, b_in, 0))) {
-            // op(B)'s planes, once, before any product; the second product
-            // stream waits for them
-            const int g = planes_pass_operand(mode, dB, L.ldB, N, K, transB != 0, pPB, num_sms,
-                                              st);
-            if (g != SGEMM_OK) rc = g;
-            if (rc == SGEMM_OK && ok(cudaEventRecord(b_planes, st)))
-                ok(cudaStreamWaitEvent(comp, b_planes, 0));
-        }
         for (int p = 0; rc == SGEMM_OK && p < L.panels; ++p) {
             const long long m0 = static_cast<long long>(p) * L.panel;
             const int rows = static_cast<int>(M - m0 < L.panel ? M - m0 : L.panel);
@@ -279,20 +248,11 @@ int sgemm_host(int mode, int M, int N, int K, float alpha, const float *A, int l
             cudaStream_t ps = st_of[p & 1];
             if (!ok(cudaEventRecord(ready[p], in)) || !ok(cudaStreamWaitEvent(ps, ready[p], 0)))
                 break;
-            int g;
-            if (planes) {  // this panel's op(A) planes, then the product on planes
-                g = planes_pass_operand(mode, pA, L.ldA, rows, K, transA == 0, pPA[p & 1],
-                                        num_sms, ps);
-                if (g == SGEMM_OK)
-                    g = planes_product(mode, rows, N, K, alpha, pPA[p & 1], pPB, beta, pC,
-                                       static_cast<int>(L.ldC), ws_of[p & 1], L.ws_bytes, ps);
-            } else {
-                g = sgemm_batched_ex_ws(
-                    mode, rows, N, K, alpha, reads_ab ? pA : nullptr, static_cast<int>(L.ldA),
-                    reads_ab ? dB : nullptr, static_cast<int>(L.ldB), beta, pC,
-                    static_cast<int>(L.ldC), transA, transB, 0, 0, 0, 1, ws_of[p & 1],
-                    L.ws_bytes, ps);
-            }
+            const int g = sgemm_batched_ex_ws(
+                mode, rows, N, K, alpha, reads_ab ? pA : nullptr, static_cast<int>(L.ldA),
+                reads_ab ? dB : nullptr, static_cast<int>(L.ldB), beta, pC,
+                static_cast<int>(L.ldC), transA, transB, 0, 0, 0, 1, ws_of[p & 1], L.ws_bytes,
+                ps);
             if (g != SGEMM_OK) {
                 rc = g;
                 break;
@@ -312,8 +272,6 @@ int sgemm_host(int mode, int M, int N, int K, float alpha, const float *A, int l
     if (fork) cudaEventDestroy(fork);
     if (join) cudaEventDestroy(join);
     if (join2) cudaEventDestroy(join2);
-    if (b_in) cudaEventDestroy(b_in);
-    if (b_planes) cudaEventDestroy(b_planes);
     for (int p = 0; p < L.panels; ++p) {
         if (ready[p]) cudaEventDestroy(ready[p]);
         if (done[p]) cudaEventDestroy(done[p]);

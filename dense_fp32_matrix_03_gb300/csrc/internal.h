@@ -166,18 +166,6 @@ bool planes_pay(int mode, long long M, long long N, long long K, int QA, int QB,
 bool smem_attr_once(const void *kernel, int bytes);
 // Multiprocessors of the current device, 0 when there is no usable one.
 int num_sms_or_zero();
-// The planes route in parts, for the host-buffer entry (host.cu), which
-// writes op(B)'s planes once and each panel's op(A) planes on its own:
-// bytes of one operand's planes (rows x K, one batch entry); the pass over
-// one operand (rows x K, K-inner or stored K x rows) into dst; the product
-// of M x K and N x K planes at pa / pb into C (ldc), with a split-K
-// workspace.  Each enqueues on `stream` and returns an sgemm status.
-size_t planes_operand_bytes(int mode, long long rows, long long K);
-int planes_pass_operand(int mode, const float *src, long long lds, int rows, int K,
-                        bool k_inner, float *dst, int num_sms, cudaStream_t stream);
-int planes_product(int mode, int M, int N, int K, float alpha, const float *pa,
-                   const float *pb, float beta, float *C, int ldc, void *ws, size_t ws_bytes,
-                   cudaStream_t stream);
 // sgemm_workspace_size without room for the planes (the host-buffer entry's
 // per-panel calls would rewrite all of B once per panel).
 size_t workspace_size_no_planes(int mode, int M, int N, int K, int Q);

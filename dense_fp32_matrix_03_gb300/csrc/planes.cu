@@ -321,50 +321,4 @@ int run_planes(Plan &plan, bool &taken, bool force)
     return product_on_planes(plan, pa, pb, QA, QB);
 }
 
-size_t planes_operand_bytes(int mode, long long rows, long long K)
-{
-    const int planes = mode == SGEMM_MODE_3XTF32 ? 2 : 1;
-    return round256(static_cast<size_t>(planes) * rows * plane_pitch(K) * sizeof(float));
-}
-
-int planes_pass_operand(int mode, const float *src, long long lds, int rows, int K,
-                        bool k_inner, float *dst, int num_sms, cudaStream_t stream)
-{
-    const long long ldp = plane_pitch(K);
-    const PassOperand o = pass_operand(src, lds, 0, rows, K, 1, k_inner, dst, ldp);
-    PassOperand none = o;
-    none.tiles = 0;
-    return mode == SGEMM_MODE_3XTF32
-               ? launch_planes_pass<2>(o, none, K, ldp, num_sms, stream)
-               : launch_planes_pass<1>(o, none, K, ldp, num_sms, stream);
-}
-
-int planes_product(int mode, int M, int N, int K, float alpha, const float *pa,
-                   const float *pb, float beta, float *C, int ldc, void *ws, size_t ws_bytes,
-                   cudaStream_t stream)
-{
-    int num_sms = 0;
-    unsigned int *status = nullptr;
-    if (!current_sm103(&num_sms, &status)) return SGEMM_ERR_UNSUPPORTED;
-    Plan plan{};
-    GemmParams &p = plan.p;
-    p.M = M;
-    p.N = N;
-    p.K = K;
-    p.Q = 1;
-    p.alpha = alpha;
-    p.beta = beta;
-    p.C = C;
-    p.ldc = ldc;
-    p.c_vec4 = aligned16(C) && ldc % 4 == 0;
-    p.status = status;
-    p.wait_limit = kWaitLimitCycles;
-    plan.mode = mode;
-    plan.num_sms = num_sms;
-    plan.stream = stream;
-    plan.ws = ws_bytes ? ws : nullptr;
-    plan.ws_bytes = ws_bytes;
-    return product_on_planes(plan, pa, pb, 1, 1);
-}
-
 }  // namespace sg

@@ -232,10 +232,9 @@ int sgemm_half_batched(int type, int M, int N, int K, float alpha, const void *A
  * products of earlier panels and the copy-out of a finished one run at the
  * same time, on two copy streams the library keeps per device, on `stream`
  * for the products of even panels and on a third library stream for those of
- * odd panels (so that two products together fill the GPU); on 3xTF32, for
- * shapes where the workspace entry would take the TF32 planes route, op(B)'s
- * planes are written once and each panel's op(A) planes before its product
- * (sgemm_host_buffer_size then includes their room).  The host link bounds
+ * odd panels (so that two products together fill the GPU); each panel's
+ * product is a workspace-entry call on the device copies, which takes the
+ * route the cost models pick for it.  The host link bounds
  * the call: on GB300 about 200 GB/s to the device and 184 from it, ~265 in
  * all while both directions run.  The call is asynchronous like the others:
  * C on the host holds

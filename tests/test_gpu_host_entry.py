@@ -177,13 +177,12 @@ def test_host_entry_long_k(oracle_mod, mode, tA, tB):
 
 
 @pytest.mark.parametrize("tA,tB", [(0, 0), (1, 1), (0, 1), (1, 0)])
-def test_host_entry_planes(oracle_mod, tA, tB):
-    """3xTF32 at 3072 x 3072 x 2000, a shape where the planes route pays: op(B)'s TF32
-    planes are written once, each 512-row panel's op(A) planes on its own
-    product stream, and the products run on the shared-memory-operand
-    kernel -- at least 1 + 2 x 6 launches (pass of B; pass and product per
-    panel), against at most 12 for six panel products and their fix-ups.
-    Random data on sampled rows within tolerance, integer data bit for bit."""
+def test_host_entry_large_panels(oracle_mod, tA, tB):
+    """3xTF32 at 3072 x 3072 x 2000 with 512-row panels: each of the six
+    panels' products is one workspace-entry call on the device copies (the
+    raw route, no pass over the operands), so the call launches one product
+    and at most one split-K fix-up per panel.  Random data on sampled rows
+    within tolerance, integer data bit for bit."""
     import torch
     mode = "3xtf32"
     import dense_fp32_matrix_03_gb300 as lib
@@ -197,7 +196,8 @@ def test_host_entry_planes(oracle_mod, tA, tB):
         torch.cuda.synchronize()
         n0 = lib.sgemm_kernel_launches()
         C = run_host(prob, mode, panel_rows=512)
-        assert lib.sgemm_kernel_launches() - n0 >= 13, "planes not used"
+        launched = lib.sgemm_kernel_launches() - n0
+        assert 6 <= launched <= 12, f"{launched} launches"
         Cref, D = prob.oracle(oracle_mod, rows=rows)
         got = np.stack([C[q, i] for q, i in rows])
         if exact:
