@@ -85,6 +85,7 @@ SIGNATURES = {
     "sgemm_poll_error": (_i, [_p]),
     "sgemm_selftest_wait_timeout": (_i, [_ll, _p]),
     "sgemm_kernel_launches": (ctypes.c_ulonglong, []),
+    "sgemm_last_split_count": (_i, []),
     "sgemm_version": (_i, []),
     # include/linear_attention.h
     "la_state_bytes": (ctypes.c_size_t, [_i, _i, _i, _i]),
@@ -297,6 +298,10 @@ def sgemm_selftest_wait_timeout(wait_cycles: int, stream=None) -> int:
 
 def sgemm_kernel_launches() -> int:
     return int(_lib.sgemm_kernel_launches())
+
+
+def sgemm_last_split_count() -> int:
+    return int(_lib.sgemm_last_split_count())
 
 
 def sgemm_version() -> int:

@@ -442,6 +442,11 @@ size_t splitk_workspace_bytes(long long split_tiles, int splits, int bm, int bn)
     return static_cast<size_t>(split_tiles) * splits * static_cast<size_t>(bm) * bn * sizeof(float);
 }
 
+namespace {
+// The last plan's slice count (sgemm_last_split_count).
+std::atomic<int> g_last_splits{1};
+}  // namespace
+
 SplitPlan choose_plan(long long num_tiles, int K, int slots, int mode, int bm, int bn, int feed,
                       size_t budget)
 {
@@ -491,6 +496,7 @@ int plan_splits(Plan &plan, int bm, int bn, int feed, int slots)
         }
     }
     p.num_units = p.dp_tiles + (p.num_tiles - p.dp_tiles) * p.splits;
+    g_last_splits.store(p.splits, std::memory_order_relaxed);
     return SGEMM_OK;
 }
 
@@ -1018,6 +1024,8 @@ int sgemm_peak_probe(int kind, long long iters, double *flops, void *stream)
 }
 
 unsigned long long sgemm_kernel_launches(void) { return sg::g_launches.load(); }
+
+int sgemm_last_split_count(void) { return sg::g_last_splits.load(); }
 
 int sgemm_tune_force(int route)
 {

@@ -354,8 +354,14 @@ int sgemm_selftest_wait_timeout(long long wait_cycles, void *stream);
  * device and stream; a failed launch is not counted).  The difference across
  * a stretch of calls is the number of kernels they launched: a GEMM call
  * launches one product kernel, plus the split-K fix-up kernel when its plan
- * splits, plus one transposition per operand the FP32 path copies. */
+ * splits, plus one transposition per operand the FP32 path copies, plus the
+ * passes of the planes route and of the raw route's lo planes. */
 unsigned long long sgemm_kernel_launches(void);
+
+/* Slices per split tile of the most recent product kernel the library
+ * planned in this process (1: not split); for tests and tuning, racy across
+ * threads that call at the same time. */
+int sgemm_last_split_count(void);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int sgemm_version(void);

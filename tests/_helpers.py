@@ -43,10 +43,10 @@ class Problem:
         self.sB = sB if strideB is None else strideB
         self.sC = sC
 
-    def run_gpu(self, mode: str, api: str = "ex", stream=None, ws_bytes=None):
+    def run_gpu(self, mode: str, api: str = "ex", stream=None, ws_bytes=None, ws_fill=None):
         """Runs the library on the device and returns C as (Q, M, N) float32.
         api="ws" passes a split-K workspace of ws_bytes (default: the size the
-        library asks for)."""
+        library asks for), every byte set to ws_fill first when given."""
         import torch
         import dense_fp32_matrix_03_gb300 as lib
         dev = torch.device("cuda", 0)
@@ -60,6 +60,8 @@ class Problem:
             if ws_bytes is None:
                 ws_bytes = lib.sgemm_workspace_size(mode, self.M, self.N, self.K, self.Q)
             ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+            if ws_fill is not None:
+                ws.fill_(ws_fill)
             self.last_ws_bytes = ws_bytes
             self.last_ws = ws
             st = lib.sgemm_batched_ex_ws(mode, self.M, self.N, self.K, self.alpha, pa, self.lda,

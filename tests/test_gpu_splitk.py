@@ -56,6 +56,39 @@ def test_split_k_parity(oracle_mod, mode, shape):
     assert err <= TOL[mode], f"{mode} {shape}: max rel err {err:.3e}"
 
 
+@pytest.mark.parametrize("mode,route", [("3xtf32", "inline"), ("3xtf32", "planes"),
+                                        ("tf32", "raw")])
+@pytest.mark.parametrize("shape", [(2560, 2560, 2000, 0), (2500, 2400, 2000, 1)])
+def test_split_k_on_a_dirty_workspace(oracle_mod, mode, route, shape):
+    """The shared-memory-operand kernel's split plan on a workspace filled
+    with garbage first (the workspace needs no initialisation: every slot the
+    fix-up reads was written by the same call), the call made twice; integer
+    data bit for bit over the whole output, against the oracle.  100 tiles of
+    256 x 256 on 76 CTA pairs: one whole wave and 24 split tiles; the product
+    kernel and the fix-up launch (and the planes route's pass).  The second
+    shape is ragged (partial tiles on both edges) with C's pitch odd, so the
+    fix-up writes C with scalar stores."""
+    import torch
+    import dense_fp32_matrix_03_gb300 as lib
+    M, N, K, odd = shape
+    assert lib.sgemm_tune_force(route) == lib.SGEMM_OK
+    try:
+        A, B, C0 = workloads.integer_inputs(M, N, K, seed=M + N)
+        prob = Problem(A, B, C0, 2.0, -1.0, pads=(0, 0, 1 if odd else 0))
+        wsb = lib.sgemm_workspace_size(mode, M, N, K, 1)
+        for fill in (0xFF, 0x5A):
+            torch.cuda.synchronize()
+            n0 = lib.sgemm_kernel_launches()
+            C = prob.run_gpu(mode, api="ws", ws_bytes=wsb, ws_fill=fill)
+            launched = lib.sgemm_kernel_launches() - n0
+            assert lib.sgemm_last_split_count() > 1, "expected a split plan"
+            assert launched == (3 if route == "planes" else 2), launched
+            Cref, _ = prob.oracle(oracle_mod)
+            assert np.array_equal(C.astype(np.float64), Cref)
+    finally:
+        lib.sgemm_tune_force("auto")
+
+
 @pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
 def test_fp32_operand_transposition_in_the_workspace(oracle_mod, tA, tB):
     """The FP32 path copies a K-inner A (N >= 1024) or B (M >= 1024) into the

@@ -6,7 +6,8 @@ its buffers): its split-K scratch is a fixed array inside the library.  These
 tests call it through the C ABI, twice in a row (the second call reuses the
 scratch the first one left behind), and check each result against the fp64
 oracle within the accuracy bound of the path, and that the call really took
-the split route (the product kernel and the split-K fix-up both launched).
+the split route (its plan split, and the product kernel and the split-K
+fix-up both launched).
 The file is named to be collected last."""
 import numpy as np
 import pytest
@@ -49,6 +50,7 @@ def test_noalloc_matches_the_oracle_twice(oracle_mod, mode, shape):
         launched = lib.sgemm_kernel_launches() - before
         err = oracle_mod.max_rel_err(C, Cref, D)
         assert err <= TOL[mode], f"{mode} {shape[:3]}: {err:.3e}"
+        assert lib.sgemm_last_split_count() > 1, "expected a split plan"
         assert launched == 2, "expected the product kernel and the split-K fix-up"
 
 
