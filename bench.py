@@ -481,6 +481,14 @@ def main():
 
     ms_local = statistics.mean(times)
     ms = reduce_max(ms_local, world, dev)
+    # the spread of the timed steps on this rank: the loop runs long enough
+    # for the power cap to act, so its later steps are slower than its first
+    srt = sorted(times)
+    q = max(1, len(times) // 10)
+    step_ms = {"min": srt[0], "median": statistics.median(times),
+               "p90": srt[min(len(srt) - 1, (9 * len(srt)) // 10)], "max": srt[-1],
+               "first_tenth_mean": statistics.mean(times[:q]),
+               "last_tenth_mean": statistics.mean(times[-q:])}
     flops_step = gemm_flops(M, N, K)
     total_flops = reduce_sum(flops_step, world, dev)
     value = total_flops / (ms / 1e3) / 1e12
@@ -553,6 +561,7 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "step_ms": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "alpha": alpha,
