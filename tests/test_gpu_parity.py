@@ -110,26 +110,60 @@ def test_sgemm_4092_every_output_workspace_entry(oracle_4092, oracle_mod, mode):
     assert err <= TOL[mode], f"{mode}: max rel err {err:.3e} over all outputs"
 
 
+_SWEEP_ORACLE = {}
+
+
+def sweep_oracle(oracle_mod, n):
+    """The oracle's whole result for sweep size n (computed once for the
+    three paths)."""
+    if n not in _SWEEP_ORACLE:
+        _SWEEP_ORACLE.clear()
+        w = workloads.make(f"sweep_{n}")
+        prob = Problem(w["A"], w["B"], w["C0"], w["alpha"], w["betas"][0])
+        _SWEEP_ORACLE[n] = (prob,) + tuple(prob.oracle(oracle_mod))
+    return _SWEEP_ORACLE[n]
+
+
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("n", workloads.SWEEP_SIZES)
 def test_size_sweep(oracle_mod, mode, n):
+    """Every output element up to 4096 (the 4096^3 oracle takes a few seconds
+    on the host cores and is shared by the three paths); sampled rows at
+    8192 (over a minute of oracle time per path otherwise)."""
     supported(mode)
-    w = workloads.make(f"sweep_{n}")
-    prob = Problem(w["A"], w["B"], w["C0"], w["alpha"], w["betas"][0])
-    if n <= 1024:
-        check_full(prob, mode, oracle_mod)
+    if n <= 4096:
+        prob, Cref, D = sweep_oracle(oracle_mod, n)
+        C = prob.run_gpu(mode)
+        err = oracle_mod.max_rel_err(C, Cref, D)
+        assert err <= TOL[mode], f"{mode} sweep_{n}: max rel err {err:.3e} over all outputs"
     else:
+        w = workloads.make(f"sweep_{n}")
+        prob = Problem(w["A"], w["B"], w["C0"], w["alpha"], w["betas"][0])
         check_rows(prob, mode, oracle_mod, sample_rows(1, n, 24, seed=n))
+
+
+@pytest.fixture(scope="module")
+def oracle_bmm(oracle_mod):
+    """The oracle's whole result for the batched workload (32 x 1024 x 1024,
+    K = 512; every one of the 33.5 M outputs), computed once: both storages
+    of B hold the same logical B."""
+    w = workloads.make("bmm_q32_1024x1024x512")
+    prob = Problem(w["A"], w["B"], w["C0"], w["alpha"], w["betas"][0])
+    return w, prob.oracle(oracle_mod)
 
 
 @pytest.mark.parametrize("api", ["ex", "ws"])
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("transB", [1, 0])
-def test_batched_q32(oracle_mod, mode, transB, api):
+def test_batched_q32(oracle_bmm, oracle_mod, mode, transB, api):
+    """The batched workload on both storages of B, through the plain and the
+    workspace entry, on every output element."""
     supported(mode)
-    w = workloads.make("bmm_q32_1024x1024x512")
+    w, (Cref, D) = oracle_bmm
     prob = Problem(w["A"], w["B"], w["C0"], w["alpha"], w["betas"][0], transB=transB)
-    check_rows(prob, mode, oracle_mod, sample_rows(32, 1024, 64, seed=4), api=api)
+    C = prob.run_gpu(mode, api=api)
+    err = oracle_mod.max_rel_err(C, Cref, D)
+    assert err <= TOL[mode], f"{mode} transB={transB} {api}: max rel err {err:.3e}"
 
 
 # -------------------------------------------------------- exactness (integers)
@@ -149,13 +183,25 @@ def test_integer_inputs_bit_exact(oracle_mod, mode, shape, alpha, beta, tA, tB):
     check_full(Problem(A, B, C0, alpha, beta, transA=tA, transB=tB), mode, oracle_mod, exact=True)
 
 
-@pytest.mark.parametrize("api", ["ex", "ws"])
-@pytest.mark.parametrize("mode", MODES)
-def test_integer_4092_bit_exact_sampled(oracle_mod, mode, api):
-    supported(mode)
+@pytest.fixture(scope="module")
+def oracle_4092_integer(oracle_mod):
+    """Integer inputs at 4092^3 and the oracle's whole result for them
+    (every partial sum an integer below 2^24: exact in fp32 in any order)."""
     A, B, C0 = workloads.integer_inputs(4092, 4092, 4092, seed=42)
     prob = Problem(A, B, C0, 1.0, 0.0)
-    check_rows(prob, mode, oracle_mod, sample_rows(1, 4092, 16, seed=3), exact=True, api=api)
+    Cref, _ = prob.oracle(oracle_mod)
+    return prob, Cref
+
+
+@pytest.mark.parametrize("api", ["ex", "ws"])
+@pytest.mark.parametrize("mode", MODES)
+def test_integer_4092_bit_exact(oracle_4092_integer, mode, api):
+    """Every one of the 16.7 M outputs bit for bit, through the plain entry
+    and the benchmark's workspace entry (whose last wave is split along K)."""
+    supported(mode)
+    prob, Cref = oracle_4092_integer
+    C = prob.run_gpu(mode, api=api)
+    assert np.array_equal(C.astype(np.float64), Cref), "integer case not bit-exact"
 
 
 @pytest.mark.parametrize("mode", MODES)
