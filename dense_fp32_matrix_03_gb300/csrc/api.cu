@@ -339,7 +339,7 @@ bool encode_operand_mn(CUtensorMap *map, const float *base, long long rows, long
 }
 
 bool encode_c_tiles(CUtensorMap *map, const float *C, long long M, long long N, long long ldc,
-                    int Q, long long sC)
+                    int Q, long long sC, int chunk_cols)
 {
     const bool batched = Q > 1 && sC != 0;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M),
@@ -347,9 +347,11 @@ bool encode_c_tiles(CUtensorMap *map, const float *C, long long M, long long N, 
     cuuint64_t strides[2];
     strides[0] = static_cast<cuuint64_t>(ldc) * 4;
     strides[1] = batched ? static_cast<cuuint64_t>(sC) * 4 : strides[0] * dims[1];
-    cuuint32_t box[3] = {16, 32, 1};
+    const bool wide = chunk_cols == 32;
+    cuuint32_t box[3] = {wide ? 32u : 16u, 32, 1};
     return encode3(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, dims, strides, box,
-                   CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+                   wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
 }
 
 bool encode_operand16(CUtensorMap *map, const void *base, bool bf16, long long rows, long long K,

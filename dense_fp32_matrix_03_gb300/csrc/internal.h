@@ -197,12 +197,13 @@ bool encode_operand(CUtensorMap *map, const float *base, bool kin, long long row
 bool encode_operand_mn(CUtensorMap *map, const float *base, long long rows, long long K,
                        long long ld, int Q, long long stride, bool promote256 = true);
 
-// Tensor map of C (Q entries sC apart when batched) in boxes of 16 columns by
-// 32 rows with the 64-byte swizzle: the shared-memory-operand kernel's
-// epilogue loads and stores C through it.  C must be 16-byte aligned with
-// ldc and sC multiples of four values.
+// Tensor map of C (Q entries sC apart when batched) in boxes of 32 rows by
+// chunk_cols columns: 16 with the 64-byte swizzle, or 32 with the 128-byte
+// one; the shared-memory-operand kernel's epilogue loads and stores C
+// through it.  C must be 16-byte aligned with ldc and sC multiples of four
+// values.
 bool encode_c_tiles(CUtensorMap *map, const float *C, long long M, long long N, long long ldc,
-                    int Q, long long sC);
+                    int Q, long long sC, int chunk_cols);
 
 // Tensor map of a K-inner 16-bit operand (bf16 or fp16): boxes of 64 k by
 // box_rows rows with the 128-byte swizzle.

@@ -85,8 +85,8 @@ constexpr int SUB_B = HN * 128;  // one box of B: 16 KB
 #endif
 #ifndef SG_TCS_TF32_STAGES
 #define SG_TCS_TF32_STAGES 5
-#define SG_TCS_TF32_EPI_NB 8
-#define SG_TCS_TF32_EPI_LA 6
+#define SG_TCS_TF32_EPI_NB 4
+#define SG_TCS_TF32_EPI_LA 3
 #endif
 // In-kernel lo planes: raw (TMA) and lo (converter) ring depths, 32 KB per
 // stage each.
@@ -107,14 +107,13 @@ constexpr int kConvWarp0 = kEpiWarp0 + 4;  // in-kernel lo planes: converter war
 #endif
 constexpr int kConvWarps = SG_TCS_CONV_WARPS;
 constexpr uint32_t kTmemCols = 512;
-// Epilogue through TMA: per epilogue warp EPI_NB 2 KB buffers (a kind's
-// choice, below), each one chunk of 32 rows x 16 columns of C in TMA's
-// 64-byte swizzle (16-byte slot j of row r at slot j ^ ((r >> 1) & 3)), so
+// Epilogue through TMA: per epilogue warp EPI_NB buffers (a kind's choice,
+// below), each one chunk of 32 rows x EPI_CH columns of C: 16 columns (2 KB)
+// in TMA's 64-byte swizzle (16-byte slot j of row r at slot j ^ ((r >> 1) &
+// 3)), or 32 columns (4 KB) in its 128-byte swizzle (slot j ^ (r & 7)), so
 // that lane r's reads and writes of its row are free of bank conflicts; C's
 // loads run EPI_LA chunks ahead.  The other epilogue (split-K partial tiles,
 // or a C TMA cannot describe) stages 32 x 32 chunks in the first 4 KB.
-constexpr int EPI_CH = 16;                           // columns per chunk
-constexpr int EPI_BUF = 32 * EPI_CH * 4;             // 2 KB
 static_assert(2 * BN <= static_cast<int>(kTmemCols), "TMEM columns");
 
 // Operand kinds.  ELEM: bytes per value; BOX_K: k per 128-byte box; UK: k
@@ -130,7 +129,7 @@ struct KindHalf {
     static constexpr int ELEM = 2, BOX_K = 64, UK = 16, PLANES = 1, KSUB = 2, STAGES = 3;
     static constexpr uint32_t FMT = BF16 ? 1u : 0u;
     static constexpr int LO_STAGES = 0;
-    static constexpr int EPI_NB = 4, EPI_LA = 2;
+    static constexpr int EPI_CH = 16, EPI_NB = 4, EPI_LA = 2;
     static constexpr bool A_MN = false, B_MN = false, CONV = false;
 };
 // CONV (3xTF32 only): the lo planes are made in the kernel from the raw
@@ -145,9 +144,14 @@ struct KindTF32 {
     static constexpr int STAGES =
         PLANES_ == 1 ? SG_TCS_TF32_STAGES : (CONV_ ? SG_TCS_CONV_RAW : 3);
     static constexpr int LO_STAGES = CONV_ ? SG_TCS_CONV_LO : 0;
-    // epilogue buffers per warp and C's lookahead: single-plane TF32 gives a
-    // stage's room to a deeper lookahead (its epilogue, a third of 3xTF32's
-    // MMA time per tile away, is what short tiles wait on when beta != 0)
+    // epilogue chunks, buffers per warp and C's lookahead: single-plane TF32
+    // gives a stage's room to the epilogue (its epilogue, a third of
+    // 3xTF32's MMA time per tile away, is what short tiles wait on when
+    // beta != 0) in 32-column chunks, half the TMA operations of 16-column
+    // ones (measured on GB300, interleaved, batched workload beta = 0.25:
+    // 406 -> 426 TFLOP/s; 3xTF32 with 32-column chunks, two buffers in its
+    // room: 282.7 -> 278.1, so it keeps four 16-column ones)
+    static constexpr int EPI_CH = PLANES_ == 1 ? 32 : 16;
     static constexpr int EPI_NB = PLANES_ == 1 ? SG_TCS_TF32_EPI_NB : 4;
     static constexpr int EPI_LA = PLANES_ == 1 ? SG_TCS_TF32_EPI_LA : 2;
     static constexpr uint32_t FMT = 2u;
@@ -161,6 +165,9 @@ struct Shape {
     static constexpr int THREADS = kThreads + (KD::CONV ? kConvWarps * 32 : 0);
     static constexpr int LO_STAGES = KD::LO_STAGES;
     static constexpr int EPI_NB = KD::EPI_NB, EPI_LA = KD::EPI_LA;
+    static constexpr int EPI_CH = KD::EPI_CH;              // columns per chunk
+    static constexpr int EPI_BUF = 32 * EPI_CH * 4;        // bytes per chunk
+    static_assert(EPI_CH == 16 || EPI_CH == 32, "epilogue chunk width");
     static constexpr int EPI_WARP_BYTES = EPI_NB * EPI_BUF;
     static constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;  // 4 epilogue warps
     static_assert(EPI_LA >= 1 && EPI_LA < EPI_NB, "lookahead");
@@ -662,7 +669,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
             tc::prefetch_c_rows(o, r0, lane);
             // C's first chunk is loaded while the accumulator is made
             float4 ca[8], cb[8];
-            constexpr int NCH = BN / EPI_CH;
+            constexpr int EPI_CH = S::EPI_CH, EPI_BUF = S::EPI_BUF, NCH = BN / EPI_CH;
             if (tma) {
                 if (use_beta && lane == 0) {
                     // chunks gch .. gch + EPI_LA - 1: their buffers' last stores
@@ -691,7 +698,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
                 // per chunk: the next chunk's C on its way (beta != 0), this
                 // chunk's accumulator from TMEM, alpha * acc + beta * C written
                 // in place (lane = row, as TMEM holds it), a TMA store
-                const int sw = (lane >> 1) & 3;
+                const int sw = EPI_CH == 32 ? (lane & 7) : ((lane >> 1) & 3);
 #pragma unroll 1
                 for (int c = 0; c < NCH; ++c, ++gch) {
                     const int b = static_cast<int>(gch % S::EPI_NB);
@@ -703,8 +710,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Shape<KD>::THREADS, 
                         tma_load_3d(wbuf + nb * EPI_BUF, &tmC, &wbar[nb],
                                     gn + (c + S::EPI_LA) * EPI_CH, gm, gz);
                     }
-                    float v[16];
-                    tc::tmem_ld16(tbase + c * EPI_CH, v);
+                    float v[EPI_CH];
+                    if constexpr (EPI_CH == 32)
+                        tc::tmem_ld32(tbase + c * EPI_CH, v);
+                    else
+                        tc::tmem_ld16(tbase + c * EPI_CH, v);
                     if (use_beta) {
                         if (!warp_wait(&wbar[b], static_cast<uint32_t>((gch / S::EPI_NB) & 1), ab,
                                        kStatusWaitAcc, lane)) {
@@ -816,7 +826,10 @@ int launch_ss(Plan &plan, const CUtensorMap &tmA, const CUtensorMap &tmB,
     alignas(64) CUtensorMap tmC;
     std::memset(&tmC, 0, sizeof(tmC));
     const GemmParams &p = plan.p;
-    plan.p.c_tma = p.c_vec4 && encode_c_tiles(&tmC, p.C, p.M, p.N, p.ldc, p.Q, p.sC) ? 1 : 0;
+    plan.p.c_tma = p.c_vec4 && encode_c_tiles(&tmC, p.C, p.M, p.N, p.ldc, p.Q, p.sC,
+                                              tcs::Shape<KD>::EPI_CH)
+                       ? 1
+                       : 0;
     if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmA_lo, tmB_lo, tmC, plan.p, a_lo_z, b_lo_z) !=
         cudaSuccess)
         return SGEMM_ERR_LAUNCH;
