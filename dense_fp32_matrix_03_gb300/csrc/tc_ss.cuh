@@ -26,7 +26,8 @@
 // stages its 128 rows of A and its 128 of the tile's 256 rows of B^T.  A
 // stage holds, per CTA, two boxes of each operand (128 k of 16-bit values;
 // 64 KB, three stages), one box of each plane of 3xTF32 (32 k; 64 KB, three
-// stages), or one box of TF32 (32 k; 32 KB, five stages).  Both CTAs' TMA
+// stages; with the lo planes made in the kernel, four raw stages of 32 KB
+// and two lo stages), or one box of TF32 (32 k; 32 KB, five stages).  Both CTAs' TMA
 // loads complete on the even CTA's barrier (cta_group::2 form, which may
 // name the peer's barrier); one thread of the even CTA issues every MMA and
 // multicasts its commits (stage free, accumulator full) to both CTAs.  TMEM:
@@ -35,8 +36,8 @@
 //
 // Warps: 0 TMA producer, 1 TMEM allocator + MMA issuer (even CTA), 2-5
 // epilogue (warp w reads TMEM lanes 32 * (w % 4) .. +31; C by TMA in chunks
-// of 32 rows x 16 columns when C's rows suit TMA), 6-7 converters (in-kernel
-// lo planes only).  Every wait is bounded; the CTAs meet at a cluster barrier
+// of 32 rows x 16 columns, 32 x 32 for single-plane TF32, when C's rows suit
+// TMA), 6-7 converters (in-kernel lo planes only).  Every wait is bounded; the CTAs meet at a cluster barrier
 // before freeing TMEM.
 //
 // In-kernel lo planes (3xTF32 on the caller's matrices, KindTF32 with CONV):
